@@ -1,0 +1,287 @@
+"""Seeded synthetic inputs for the FP4 indexer scorer.
+
+This module only draws random numbers and lays them out; it holds none of the
+scorer's arithmetic.  The CUDA tests, the bench and the oracle all take their
+inputs from here.
+
+Every problem is a set of host (numpy) arrays in the layouts of the M3-indexer
+README ("输入 shape 和类型"):
+
+- ``q``        [T, Hq, 64]  uint8, two E2M1 codes per byte (low nibble = even element)
+- ``q_scale``  [T, Hq, G]   uint8, E8M0 (MXFP4, G=4) or E4M3 (NVFP4, G=8)
+- ``k``        [P, Hkv, page, 64] uint8, paged K cache
+- ``k_scale``  [P, Hkv, page, G]  uint8
+- ``cu_seqlens_q`` / ``cu_seqlens_k`` [B+1] int32
+- ``block_table``  [B, stride] int32 (logical page -> physical page), or a flat
+  ``kv_indices``-style table plus ``page_offsets`` [B]
+- ``visible_len`` [T] int32 (SGLang PR 42861's per-row visible length) or
+  ``causal`` with optional ``qo_offset`` [B]
+- ``w`` [T, Hq] float32 head weights
+
+Named workloads follow the five configurations the scorer is measured on:
+a tiny MXFP4 decode, SGLang PR 42861's 16,384-key verify decode, a batched
+long-context decode, the M3-indexer NVFP4 GQA block-score prefill and a 32k
+causal weighted-ReLU prefill with top-k.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional, Sequence
+
+import numpy as np
+
+MXFP4 = 0
+NVFP4 = 1
+HEAD_DIM = 128
+
+
+def groups(fmt: int) -> int:
+    return 4 if fmt == MXFP4 else 8
+
+
+@dataclasses.dataclass
+class Problem:
+    name: str
+    format: int
+    num_heads: int
+    num_kv_heads: int
+    page_size: int
+    q: np.ndarray
+    q_scale: np.ndarray
+    k: np.ndarray
+    k_scale: np.ndarray
+    cu_seqlens_q: np.ndarray
+    cu_seqlens_k: np.ndarray
+    block_table: np.ndarray
+    page_offsets: Optional[np.ndarray]
+    visible_len: Optional[np.ndarray]
+    causal: bool
+    qo_offset: Optional[np.ndarray]
+    w: Optional[np.ndarray]
+    max_seqlen_q: int
+    max_seqlen_k: int
+    topk: int = 0
+    q_lens: Sequence[int] = ()
+    k_lens: Sequence[int] = ()
+
+    @property
+    def num_rows(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.cu_seqlens_q.shape[0] - 1)
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k.shape[0])
+
+    @property
+    def ktiles(self) -> int:
+        return (self.max_seqlen_k + 127) // 128
+
+    def summary(self) -> dict:
+        return {
+            "workload": self.name,
+            "format": "mxfp4" if self.format == MXFP4 else "nvfp4",
+            "requests": self.num_seqs,
+            "rows": self.num_rows,
+            "heads": self.num_heads,
+            "kv_heads": self.num_kv_heads,
+            "head_dim": HEAD_DIM,
+            "page_size": self.page_size,
+            "max_seqlen_k": self.max_seqlen_k,
+            "cache_pages": self.num_pages,
+            "topk": self.topk,
+        }
+
+
+def _scales(rng: np.random.Generator, fmt: int, shape, e8m0_range) -> np.ndarray:
+    if fmt == MXFP4:
+        lo, hi = e8m0_range
+        return rng.integers(lo, hi + 1, size=shape, dtype=np.uint8)
+    # NVFP4: |N(0,1)| rounded to E4M3 by torch's float8_e4m3fn conversion;
+    # a value that rounds to zero takes the smallest subnormal code.
+    import torch
+
+    mag = np.abs(rng.standard_normal(size=shape)).astype(np.float32)
+    codes = torch.from_numpy(mag).to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+    codes[codes == 0] = 1
+    return codes
+
+
+def _weights(rng: np.random.Generator, kind: str, shape) -> np.ndarray:
+    if kind == "sixteenths":  # j/16, j uniform in [-16, 16]
+        return (rng.integers(-16, 17, size=shape).astype(np.float32) / np.float32(16.0))
+    if kind == "normal":
+        return rng.standard_normal(size=shape).astype(np.float32)
+    if kind == "strict":  # {0, +-1/2, +-1}
+        return (rng.integers(-2, 3, size=shape).astype(np.float32) / np.float32(2.0))
+    raise ValueError(kind)
+
+
+def make_problem(
+    *,
+    name: str,
+    seed: int,
+    fmt: int,
+    q_lens: Sequence[int],
+    k_lens: Sequence[int],
+    num_heads: int,
+    num_kv_heads: int = 1,
+    page_size: int = 64,
+    e8m0_range=(124, 130),
+    weights: Optional[str] = "sixteenths",
+    visibility: str = "minus_row",
+    qo_offset: Optional[Sequence[int]] = None,
+    cache_pages: Optional[int] = None,
+    table_form: str = "strided",
+    topk: int = 0,
+    visible_len: Optional[Sequence[int]] = None,
+) -> Problem:
+    """Build one seeded problem.
+
+    visibility: "minus_row" (row r of a request with q_len rows sees
+    k_len-(q_len-1-r) keys), "full" (every row sees k_len), "causal"
+    (bottom-right aligned, optional explicit qo_offset) or "explicit"
+    (``visible_len`` given).
+    """
+    rng = np.random.default_rng(seed)
+    table_rng = np.random.default_rng(seed + 1_000_003)
+    G = groups(fmt)
+    B = len(q_lens)
+    assert len(k_lens) == B
+    T = int(sum(q_lens))
+    q = rng.integers(0, 256, size=(T, num_heads, 64), dtype=np.uint8)
+    q_scale = _scales(rng, fmt, (T, num_heads, G), e8m0_range)
+    pages_per_req = [(kl + page_size - 1) // page_size for kl in k_lens]
+    need = int(sum(pages_per_req))
+    P = max(need, 1) if cache_pages is None else int(cache_pages)
+    assert P >= need, "cache too small for the requests"
+    k = rng.integers(0, 256, size=(P, num_kv_heads, page_size, 64), dtype=np.uint8)
+    k_scale = _scales(rng, fmt, (P, num_kv_heads, page_size, G), e8m0_range)
+    perm = table_rng.permutation(P).astype(np.int32)
+    cu_q = np.zeros(B + 1, np.int32)
+    cu_q[1:] = np.cumsum(q_lens)
+    cu_k = np.zeros(B + 1, np.int32)
+    cu_k[1:] = np.cumsum(k_lens)
+    page_offsets = None
+    if table_form == "strided":
+        stride = max(max(pages_per_req), 1)
+        table = np.full((B, stride), -1, np.int32)
+        off = 0
+        for b, n in enumerate(pages_per_req):
+            table[b, :n] = perm[off : off + n]
+            off += n
+    elif table_form == "offsets":
+        table = np.ascontiguousarray(perm[: max(need, 1)].reshape(1, -1))
+        page_offsets = np.zeros(B, np.int32)
+        page_offsets[1:] = np.cumsum(pages_per_req)[:-1]
+    else:
+        raise ValueError(table_form)
+    vis = None
+    causal = False
+    qo = None
+    if visibility == "minus_row":
+        vis = np.concatenate(
+            [np.asarray([kl - (ql - 1 - r) for r in range(ql)], np.int64) for ql, kl in zip(q_lens, k_lens)]
+        ).clip(min=0).astype(np.int32)
+    elif visibility == "full":
+        vis = np.concatenate([np.full(ql, kl, np.int32) for ql, kl in zip(q_lens, k_lens)])
+    elif visibility == "causal":
+        causal = True
+        qo = None if qo_offset is None else np.asarray(qo_offset, np.int32)
+    elif visibility == "explicit":
+        vis = np.asarray(visible_len, np.int32)
+        assert vis.shape == (T,)
+    else:
+        raise ValueError(visibility)
+    w = None if weights is None else _weights(rng, weights, (T, num_heads))
+    return Problem(
+        name=name,
+        format=fmt,
+        num_heads=num_heads,
+        num_kv_heads=num_kv_heads,
+        page_size=page_size,
+        q=q,
+        q_scale=q_scale,
+        k=k,
+        k_scale=k_scale,
+        cu_seqlens_q=cu_q,
+        cu_seqlens_k=cu_k,
+        block_table=table,
+        page_offsets=page_offsets,
+        visible_len=vis,
+        causal=causal,
+        qo_offset=qo,
+        w=w,
+        max_seqlen_q=int(max(q_lens)),
+        max_seqlen_k=int(max(k_lens)),
+        topk=topk,
+        q_lens=tuple(int(x) for x in q_lens),
+        k_lens=tuple(int(x) for x in k_lens),
+    )
+
+
+# ---------------------------------------------------------------------------
+# The five measured workloads.
+# ---------------------------------------------------------------------------
+
+def tiny_mx_decode() -> Problem:
+    """1 request, 4 rows, 8 heads, 1,024 keys in 16 shuffled 64-key pages,
+    E8M0 124..130, w = j/16; row r sees 1024-(3-r) keys; top-64."""
+    return make_problem(name="tiny_mxfp4_decode_1k", seed=1000, fmt=MXFP4, q_lens=[4], k_lens=[1024],
+                        num_heads=8, e8m0_range=(124, 130), weights="sixteenths", topk=64)
+
+
+def verify_decode_16k(strict: bool = False) -> Problem:
+    """SGLang PR 42861's benchmark shape: 4 verify rows x 32 heads, 16,384
+    keys on shuffled 64-key pages, MXFP4, top-2048.  ``strict`` sets every
+    scale code to 127 and w in {0, +-1/2, +-1} so that every logit is exact in
+    fp32 under any summation order."""
+    p = make_problem(name="verify_mxfp4_decode_16k" + ("_strict" if strict else ""), seed=1001,
+                     fmt=MXFP4, q_lens=[4], k_lens=[16384], num_heads=32, e8m0_range=(124, 130),
+                     weights="strict" if strict else "sixteenths", topk=2048)
+    if strict:
+        p.q_scale[...] = 127
+        p.k_scale[...] = 127
+    return p
+
+
+def long_batched_decode(num_requests: int = 16, cache_keys: int = 14_000_000) -> Problem:
+    """16 requests x 4 rows, 32 heads, MXFP4, each context drawn from
+    {100,000, 400,000}; 64-key pages dealt from one random permutation of a
+    14M-key cache; E8M0 120..134; w ~ N(0,1); top-2048."""
+    rng = np.random.default_rng(2002)
+    ctx = [int(x) for x in rng.choice([100_000, 400_000], size=num_requests)]
+    return make_problem(name="long_mxfp4_decode_16x4_ctx100k-400k", seed=1002, fmt=MXFP4,
+                        q_lens=[4] * num_requests, k_lens=ctx, num_heads=32,
+                        e8m0_range=(120, 134), weights="normal", cache_pages=cache_keys // 64,
+                        topk=2048)
+
+
+def nvfp4_gqa_block_scores() -> Problem:
+    """M3-indexer shape: B=4, q_len 4,096, k_len 8,192, Hq=32, Hkv=4, NVFP4
+    (E4M3 |N(0,1)| per 16), 128-key pages through a kv_indices permutation,
+    causal with qo_offset = k_len - q_len; output [32, 64, 16384]."""
+    return make_problem(name="gqa_nvfp4_block_scores_4x4k_k8k", seed=1003, fmt=NVFP4,
+                        q_lens=[4096] * 4, k_lens=[8192] * 4, num_heads=32, num_kv_heads=4,
+                        page_size=128, weights=None, visibility="causal", qo_offset=[4096] * 4,
+                        table_form="offsets")
+
+
+def prefill_32k() -> Problem:
+    """1 request, 32,768 causal query rows over 32,768 keys, 64 heads, MXFP4
+    (E8M0 120..134), w ~ N(0,1), 64-key pages, top-2048 per row."""
+    return make_problem(name="prefill_mxfp4_32k_h64_top2048", seed=1004, fmt=MXFP4, q_lens=[32768],
+                        k_lens=[32768], num_heads=64, e8m0_range=(120, 134), weights="normal",
+                        visibility="causal", topk=2048)
+
+
+WORKLOADS = {
+    "tiny": tiny_mx_decode,
+    "verify16k": verify_decode_16k,
+    "long_decode": long_batched_decode,
+    "block_scores": nvfp4_gqa_block_scores,
+    "prefill": prefill_32k,
+}

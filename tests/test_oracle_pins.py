@@ -1,0 +1,338 @@
+"""Pins of the CPU oracle to facts fixed outside the oracle itself.
+
+Each test checks the oracle against one of: values the pages print
+(tests/golden/*), a library routine (torch's float8 decodes, float64 matmul
+on independently dequantised operands), a closed form, a brute-force
+computation on tiny inputs, or an invariant of the definition.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp4_sparse_attention_gb300 import workloads as wl
+from tests.conftest import read_golden
+
+
+# ---------------------------------------------------------------------------
+# independent dequantisation through library conversions
+# ---------------------------------------------------------------------------
+
+def _e2m1_table():
+    rows = read_golden("e2m1_levels.txt")
+    table = np.zeros(16, np.float64)
+    for code, value in rows:
+        table[int(code)] = float(value)
+    return table
+
+
+def _scale_values(codes: np.ndarray, fmt: int) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(codes))
+    dt = torch.float8_e8m0fnu if fmt == wl.MXFP4 else torch.float8_e4m3fn
+    return t.view(dt).to(torch.float64).numpy()
+
+
+def _dequant(codes: np.ndarray, scales: np.ndarray, fmt: int) -> np.ndarray:
+    """[..., 64] packed bytes + [..., G] scales -> [..., 128] float64."""
+    table = _e2m1_table()
+    lo = codes & 15
+    hi = codes >> 4
+    nib = np.stack([lo, hi], axis=-1).reshape(*codes.shape[:-1], 128)
+    vals = table[nib]
+    group = 32 if fmt == wl.MXFP4 else 16
+    return vals * np.repeat(_scale_values(scales, fmt), group, axis=-1)
+
+
+def _library_dots(p: wl.Problem):
+    """dots[t][h, s] for every row and logical key of its request (float64 matmul)."""
+    Q = _dequant(p.q, p.q_scale, p.format)  # [T, H, 128]
+    K = _dequant(p.k, p.k_scale, p.format)  # [P, Hkv, page, 128]
+    rep = p.num_heads // p.num_kv_heads
+    out = []
+    for b in range(p.num_seqs):
+        k_len = int(p.cu_seqlens_k[b + 1] - p.cu_seqlens_k[b])
+        s = np.arange(k_len)
+        if p.page_offsets is None:
+            pages = p.block_table[b][s // p.page_size]
+        else:
+            pages = p.block_table.reshape(-1)[p.page_offsets[b] + s // p.page_size]
+        keys = K[pages, :, s % p.page_size, :]  # [k_len, Hkv, 128]
+        for t in range(int(p.cu_seqlens_q[b]), int(p.cu_seqlens_q[b + 1])):
+            qt = torch.from_numpy(Q[t]).reshape(p.num_kv_heads, rep, 128)
+            kt = torch.from_numpy(np.ascontiguousarray(keys.transpose(1, 2, 0)))  # [Hkv,128,k_len]
+            out.append(torch.matmul(qt, kt).reshape(p.num_heads, k_len).numpy())
+    return out
+
+
+def _library_logits(p: wl.Problem, ncols: int):
+    dots = _library_dots(p)
+    vis = oracle.visible_all(p)
+    res = np.full((p.num_rows, ncols), -np.inf, np.float32)
+    for t in range(p.num_rows):
+        d = dots[t][:, : vis[t]]
+        lg = (p.w[t].astype(np.float64)[:, None] * np.maximum(d, 0.0)).sum(axis=0)
+        res[t, : vis[t]] = lg.astype(np.float32)
+    return res
+
+
+def _small(fmt=wl.MXFP4, **kw):
+    args = dict(name="pin", seed=7, fmt=fmt, q_lens=[3, 2], k_lens=[300, 129], num_heads=4,
+                page_size=64, weights="sixteenths")
+    args.update(kw)
+    return wl.make_problem(**args)
+
+
+# ---------------------------------------------------------------------------
+# decodes
+# ---------------------------------------------------------------------------
+
+def test_e2m1_every_code_matches_level_set():
+    table = _e2m1_table()
+    for code in range(16):
+        got = oracle.e2m1(code)
+        assert got == table[code]
+        assert math.copysign(1.0, got) == math.copysign(1.0, table[code])
+
+
+def test_e2m1_is_not_the_linear_magnitude_defect():
+    for idx, true, buggy in read_golden("e2m1_linear_magnitude_defect.txt"):
+        v = oracle.e2m1(int(idx))
+        assert v == float(true)
+        assert v != float(buggy)
+        assert oracle.e2m1(int(idx) | 8) == -float(true)
+
+
+def test_e8m0_stored_codes_are_exact_powers_of_two():
+    lib = _scale_values(np.arange(256, dtype=np.uint8), wl.MXFP4)
+    for code in range(1, 255):
+        v = oracle.e8m0(code)
+        assert v == math.ldexp(1.0, code - 127)
+        assert v == lib[code]
+
+
+def test_e8m0_scorer_codes_from_page(golden):
+    for code, value in golden("e8m0_scorer_codes.txt"):
+        expect = math.inf if value == "inf" else (
+            math.ldexp(1.0, int(value[2:])) if value.startswith("2^") else float(value))
+        assert oracle.e8m0(int(code)) == expect
+
+
+def test_e4m3_every_code_matches_torch():
+    lib = _scale_values(np.arange(256, dtype=np.uint8), wl.NVFP4)
+    for code in range(256):
+        v = oracle.e4m3(code)
+        if math.isnan(lib[code]):
+            assert math.isnan(v)
+        else:
+            assert v == lib[code]
+            assert math.copysign(1.0, v) == math.copysign(1.0, lib[code])
+    assert oracle.e4m3(0x7E) == 448.0
+    assert oracle.e4m3(0x01) == 2.0 ** -9
+
+
+# ---------------------------------------------------------------------------
+# visibility
+# ---------------------------------------------------------------------------
+
+def test_visibility_hand_worked_cases(golden):
+    for case in golden("visibility_cases.txt"):
+        name, q_len, k_len, qo = case[0], int(case[1]), int(case[2]), case[3]
+        expect = [int(x) for x in case[4:]]
+        p = wl.make_problem(name=name, seed=1, fmt=wl.MXFP4, q_lens=[q_len], k_lens=[k_len],
+                            num_heads=1, visibility="causal",
+                            qo_offset=None if qo == "d" else [int(qo)])
+        assert list(oracle.visible_all(p)) == expect, name
+
+
+def test_visible_len_is_clipped_to_request_length():
+    p = wl.make_problem(name="clip", seed=2, fmt=wl.MXFP4, q_lens=[3], k_lens=[100], num_heads=1,
+                        visibility="explicit", visible_len=[-5, 40, 1000])
+    assert list(oracle.visible_all(p)) == [0, 40, 100]
+
+
+def test_minus_row_visibility_of_verify_rows():
+    p = wl.make_problem(name="v", seed=3, fmt=wl.MXFP4, q_lens=[4], k_lens=[1024], num_heads=1)
+    assert list(oracle.visible_all(p)) == [1021, 1022, 1023, 1024]
+
+
+# ---------------------------------------------------------------------------
+# closed forms
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt,unit_scale", [(wl.MXFP4, 127), (wl.NVFP4, 0x38)])
+def test_constant_operands_closed_form(fmt, unit_scale):
+    p = _small(fmt=fmt)
+    p.q[...] = 0x11  # every element 0.5
+    p.k[...] = 0x22  # every element 1.0
+    p.q_scale[...] = unit_scale
+    p.k_scale[...] = unit_scale
+    out, bound, safe = oracle.logits_rows(p, 300)
+    vis = oracle.visible_all(p)
+    for t in range(p.num_rows):
+        expect = np.float32(64.0 * p.w[t].astype(np.float64).sum())
+        assert np.all(out[t, : vis[t]] == expect)
+        assert np.all(np.isneginf(out[t, vis[t]:]))
+        np.testing.assert_allclose(bound[t, : vis[t]], 1e-5 * 64.0 * np.abs(p.w[t]).sum())
+        assert safe[t].all()
+    d, asum, ok = oracle.dot(p, 0, 1, 5)
+    assert (d, asum, ok) == (64.0, 64.0, True)
+
+
+def test_negated_keys_give_zero_logits():
+    p = _small()
+    p.q[...] = 0x11
+    p.k[...] = 0xAA  # every element -1.0
+    p.q_scale[...] = 127
+    p.k_scale[...] = 127
+    out, _, _ = oracle.logits_rows(p, 300)
+    vis = oracle.visible_all(p)
+    for t in range(p.num_rows):
+        assert np.all(out[t, : vis[t]] == 0.0)
+
+
+def test_one_hot_weights_pick_relu_of_one_head():
+    p = _small()
+    p.w[...] = 0.0
+    p.w[:, 2] = 1.0
+    out, _, _ = oracle.logits_rows(p, 300)
+    for t, s in [(0, 0), (1, 17), (2, 299), (3, 5), (4, 128)]:
+        if s < oracle.visible(p, t):
+            d, _, _ = oracle.dot(p, t, 2, s)
+            assert out[t, s] == np.float32(max(d, 0.0))
+
+
+def test_bound_and_exact_flag_on_strict_config():
+    p = wl.verify_decode_16k(strict=True)
+    rows = np.array([0, 3], np.int32)
+    out, bound, safe = oracle.logits_at(p, rows, np.arange(0, 16384, 97))
+    assert safe.all()
+
+
+def test_exact_flag_detects_an_inexact_sum():
+    # two heads whose weighted terms differ by 2^25: their fp32 sum is inexact
+    p = wl.make_problem(name="inexact", seed=4, fmt=wl.MXFP4, q_lens=[1], k_lens=[64], num_heads=2,
+                        weights="sixteenths")
+    p.q[...] = 0x22
+    p.k[...] = 0x22
+    p.q_scale[...] = 127
+    p.k_scale[...] = 127  # every dot = 128
+    p.w[0, 0] = np.float32(2.0 ** 25)
+    p.w[0, 1] = np.float32(2.0 ** -7)
+    out, _, safe = oracle.logits_at(p, [0], [0])
+    exact = 128.0 * (2.0 ** 25 + 2.0 ** -7)
+    assert not safe[0, 0]
+    assert out[0, 0] == np.float32(exact)
+    assert float(np.float32(exact)) != exact
+
+
+# ---------------------------------------------------------------------------
+# library routine: float64 matmul over independently dequantised operands
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("maker", [
+    lambda: wl.tiny_mx_decode(),
+    lambda: _small(),
+    lambda: _small(fmt=wl.NVFP4, num_heads=8, num_kv_heads=2, page_size=128),
+    lambda: _small(fmt=wl.NVFP4, table_form="offsets", q_lens=[2, 5, 1], k_lens=[70, 1, 200]),
+])
+def test_oracle_logits_match_library_matmul(maker):
+    p = maker()
+    ncols = p.max_seqlen_k + 8
+    got, _, _ = oracle.logits_rows(p, ncols)
+    ref = _library_logits(p, ncols)
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("maker", [
+    lambda: _small(fmt=wl.NVFP4, num_heads=8, num_kv_heads=2, page_size=128, weights=None,
+                   visibility="causal"),
+    lambda: _small(fmt=wl.MXFP4, num_heads=4, num_kv_heads=4, weights=None, visibility="causal",
+                   qo_offset=[150, 3]),
+])
+def test_oracle_block_scores_match_library_matmul(maker):
+    p = maker()
+    kt = p.ktiles
+    got, _, _ = oracle.block_scores(p, kt)
+    dots = _library_dots(p)
+    vis = oracle.visible_all(p)
+    for t in range(p.num_rows):
+        for kb in range(kt):
+            lo, hi = 128 * kb, min(128 * (kb + 1), vis[t])
+            expect = (dots[t][:, lo:hi].max(axis=1).astype(np.float32) if hi > lo
+                      else np.full(p.num_heads, -np.inf, np.float32))
+            np.testing.assert_array_equal(got[:, kb, t], expect)
+
+
+# ---------------------------------------------------------------------------
+# invariants and brute force
+# ---------------------------------------------------------------------------
+
+def test_physical_page_permutation_is_invisible():
+    p = _small(q_lens=[2, 3], k_lens=[500, 250])
+    base, _, _ = oracle.logits_rows(p, 512)
+    rng = np.random.default_rng(11)
+    perm = rng.permutation(p.num_pages)  # new physical slot of each old page
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(len(perm))
+    p.k = np.ascontiguousarray(p.k[inv])
+    p.k_scale = np.ascontiguousarray(p.k_scale[inv])
+    p.block_table = np.where(p.block_table >= 0, perm[np.maximum(p.block_table, 0)], -1).astype(np.int32)
+    moved, _, _ = oracle.logits_rows(p, 512)
+    np.testing.assert_array_equal(base, moved)
+
+
+def test_topk_matches_bruteforce_sort():
+    p = _small(q_lens=[3, 4], k_lens=[300, 90], visibility="minus_row")
+    p.w[...] = np.round(p.w * 2) / 2  # coarse weights create exact ties
+    k = 64
+    idx, val, cnt = oracle.topk(p, k)
+    full, _, _ = oracle.logits_rows(p, 300)
+    vis = oracle.visible_all(p)
+    for t in range(p.num_rows):
+        order = sorted(range(vis[t]), key=lambda s: (-(float(full[t, s]) + 0.0), s))[:k]
+        n = min(k, vis[t])
+        assert cnt[t] == n
+        assert list(idx[t, :n]) == order
+        assert np.all(idx[t, n:] == -1)
+        assert np.all(np.isneginf(val[t, n:]))
+        np.testing.assert_array_equal(val[t, :n], full[t, order])
+
+
+def test_topk_of_short_rows_keeps_every_visible_position():
+    p = _small(q_lens=[2], k_lens=[40], visibility="explicit", visible_len=[0, 17])
+    idx, val, cnt = oracle.topk(p, 32)
+    assert list(cnt) == [0, 17]
+    assert np.all(idx[0] == -1)
+    assert sorted(idx[1, :17]) == list(range(17))
+
+
+def test_block_score_is_max_of_unweighted_logits_when_dots_nonnegative():
+    p = _small(q_lens=[2], k_lens=[300], num_heads=1, visibility="full")
+    p.q &= 0x77  # positive nibbles only: every dot >= 0
+    p.k &= 0x77
+    p.w[...] = 1.0
+    full, _, _ = oracle.logits_rows(p, 300)
+    bs, _, _ = oracle.block_scores(p, 3)
+    for t in range(2):
+        for kb in range(3):
+            assert bs[0, kb, t] == full[t, 128 * kb: 128 * (kb + 1)].max()
+
+
+def test_block_score_of_single_visible_key_is_its_dot():
+    p = _small(q_lens=[1], k_lens=[200], weights=None, visibility="explicit", visible_len=[129])
+    bs, _, _ = oracle.block_scores(p, 2)
+    for h in range(p.num_heads):
+        d, _, _ = oracle.dot(p, 0, h, 128)
+        assert bs[h, 1, 0] == np.float32(d)
+    assert bs.shape == (p.num_heads, 2, 1)
+
+
+def test_nan_query_scale_leaves_invisible_positions_neg_inf():
+    p = _small(fmt=wl.NVFP4, q_lens=[2], k_lens=[256], visibility="explicit", visible_len=[100, 0])
+    p.q_scale[...] = 0x7F  # E4M3 NaN
+    out, _, _ = oracle.logits_rows(p, 256)
+    assert np.isnan(out[0, :100]).all()
+    assert np.isneginf(out[0, 100:]).all()
+    assert np.isneginf(out[1]).all()
