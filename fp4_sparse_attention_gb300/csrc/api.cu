@@ -1,0 +1,346 @@
+// api.cu -- the C ABI of include/fp4idx.h: host-side argument checks, TMA
+// tensor-map construction, launch planning and kernel launches.  Nothing here
+// reads device memory or synchronises (except fp4idx_get_error).
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "fp4idx.h"
+#include "internal.h"
+
+namespace fp4idx {
+namespace {
+
+thread_local char g_msg[512] = "";
+
+fp4idx_status_t fail(fp4idx_status_t s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+fp4idx_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(FP4IDX_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Device error word: one per device that loads this library.
+__device__ uint32_t g_device_error;
+
+struct DeviceInfo {
+  bool ready = false;
+  int major = 0, minor = 0, sms = 0;
+  uint32_t* err = nullptr;
+};
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+fp4idx_status_t device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(FP4IDX_EDEVICE, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (d.major != 10 || d.minor != 3)
+      return fail(FP4IDX_EDEVICE, "device %d is sm_%d%d; this library is built for sm_103a", dev, d.major,
+                  d.minor);
+    void* ptr = nullptr;
+    if ((e = cudaGetSymbolAddress(&ptr, g_device_error)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+    d.err = static_cast<uint32_t*>(ptr);
+    d.ready = true;
+  }
+  *out = &d;
+  return FP4IDX_OK;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+fp4idx_status_t encode_fn(EncodeTiledFn* out) {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (!fn) return fail(FP4IDX_ECUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(err));
+  *out = fn;
+  return FP4IDX_OK;
+}
+
+fp4idx_status_t make_tmap(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                          const cuuint64_t* strides, const cuuint32_t* box) {
+  EncodeTiledFn fn;
+  fp4idx_status_t s = encode_fn(&fn);
+  if (s != FP4IDX_OK) return s;
+  cuuint32_t elem[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), dims, strides, box, elem,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FP4IDX_EINVAL, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return FP4IDX_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int groups_of(int format) { return format == FP4IDX_MXFP4 ? 4 : 8; }
+
+// Checks shared by every entry point.
+fp4idx_status_t check_problem(const fp4idx_problem_t* p) {
+  if (!p) return fail(FP4IDX_EINVAL, "problem is NULL");
+  if (p->format != FP4IDX_MXFP4 && p->format != FP4IDX_NVFP4)
+    return fail(FP4IDX_EINVAL, "format %d is neither MXFP4 (0) nor NVFP4 (1)", p->format);
+  if (p->num_seqs < 1) return fail(FP4IDX_EINVAL, "num_seqs must be >= 1 (got %d)", p->num_seqs);
+  if (p->num_rows < 0) return fail(FP4IDX_EINVAL, "num_rows must be >= 0");
+  if (p->num_heads < 1 || p->num_kv_heads < 1 || p->num_heads % p->num_kv_heads != 0)
+    return fail(FP4IDX_EINVAL, "num_heads (%d) must be a positive multiple of num_kv_heads (%d)", p->num_heads,
+                p->num_kv_heads);
+  if (p->page_size != 64 && p->page_size != 128)
+    return fail(FP4IDX_EUNSUPPORTED, "page_size %d: only 64 and 128 are supported", p->page_size);
+  if (p->num_pages < 1) return fail(FP4IDX_EINVAL, "num_pages must be >= 1");
+  if (p->num_pages * p->num_kv_heads * p->page_size > INT32_MAX)
+    return fail(FP4IDX_EUNSUPPORTED, "cache rows exceed 2^31");
+  if (p->max_seqlen_q < 1) return fail(FP4IDX_EINVAL, "max_seqlen_q must be >= 1");
+  if (p->max_seqlen_k < 0) return fail(FP4IDX_EINVAL, "max_seqlen_k must be >= 0");
+  if (!p->q || !p->q_scale || !p->k || !p->k_scale || !p->cu_seqlens_q || !p->cu_seqlens_k || !p->block_table)
+    return fail(FP4IDX_EINVAL, "q, q_scale, k, k_scale, cu_seqlens_q, cu_seqlens_k and block_table are required");
+  if (!aligned(p->q, 128) || !aligned(p->k, 128))
+    return fail(FP4IDX_EINVAL, "q and k must be 128-byte aligned");
+  if (!aligned(p->q_scale, 16) || !aligned(p->k_scale, 16))
+    return fail(FP4IDX_EINVAL, "q_scale and k_scale must be 16-byte aligned");
+  const int G = groups_of(p->format);
+  if (p->q_row_stride < static_cast<int64_t>(p->num_heads) * 64 || p->q_row_stride % 16 != 0)
+    return fail(FP4IDX_EINVAL, "q_row_stride %lld must be a multiple of 16 and >= num_heads*64",
+                static_cast<long long>(p->q_row_stride));
+  if (p->q_scale_row_stride < static_cast<int64_t>(p->num_heads) * G || p->q_scale_row_stride % 8 != 0)
+    return fail(FP4IDX_EINVAL, "q_scale_row_stride %lld must be a multiple of 8 and >= num_heads*%d",
+                static_cast<long long>(p->q_scale_row_stride), G);
+  if (!p->page_offsets) {
+    const int64_t need = (static_cast<int64_t>(p->max_seqlen_k) + p->page_size - 1) / p->page_size;
+    if (p->table_stride < need)
+      return fail(FP4IDX_EINVAL, "table_stride %lld < pages of max_seqlen_k (%lld)",
+                  static_cast<long long>(p->table_stride), static_cast<long long>(need));
+  }
+  if (p->qo_offset && !p->causal) return fail(FP4IDX_EINVAL, "qo_offset is only allowed with causal != 0");
+  return FP4IDX_OK;
+}
+
+// Checks of the weighted-ReLU paths (logits, top-k).
+fp4idx_status_t check_weighted(const fp4idx_problem_t* p, const float* w, int64_t w_row_stride) {
+  if (p->num_kv_heads != 1)
+    return fail(FP4IDX_EUNSUPPORTED, "weighted-ReLU scoring supports one K head (num_kv_heads = %d)",
+                p->num_kv_heads);
+  if (p->num_heads != 8 && p->num_heads != 16 && p->num_heads != 32 && p->num_heads != 64)
+    return fail(FP4IDX_EUNSUPPORTED, "num_heads %d: supported 8, 16, 32, 64", p->num_heads);
+  if (!w) return fail(FP4IDX_EINVAL, "w is NULL");
+  if (!aligned(w, 4)) return fail(FP4IDX_EINVAL, "w must be 4-byte aligned");
+  if (w_row_stride < p->num_heads) return fail(FP4IDX_EINVAL, "w_row_stride must be >= num_heads");
+  return FP4IDX_OK;
+}
+
+// Common part of the scorer parameters.
+fp4idx_status_t fill_score_params(const fp4idx_problem_t* pr, const float* w, int64_t w_row_stride,
+                                  ScoreParams* sp, int rows_per_cta, uint32_t* err) {
+  std::memset(sp, 0, sizeof(*sp));
+  const int G = groups_of(pr->format);
+  {
+    cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(pr->num_pages) * pr->num_kv_heads * pr->page_size};
+    cuuint64_t strides[1] = {64};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(pr->page_size)};
+    fp4idx_status_t s = make_tmap(&sp->tmap_k, pr->k, 2, dims, strides, box);
+    if (s != FP4IDX_OK) return s;
+  }
+  {
+    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(pr->num_heads), static_cast<cuuint64_t>(pr->num_rows)};
+    cuuint64_t strides[2] = {64, static_cast<cuuint64_t>(pr->q_row_stride)};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(pr->num_heads), static_cast<cuuint32_t>(rows_per_cta)};
+    fp4idx_status_t s = make_tmap(&sp->tmap_q, pr->q, 3, dims, strides, box);
+    if (s != FP4IDX_OK) return s;
+  }
+  (void)G;
+  sp->k_scale = pr->k_scale;
+  sp->q_scale = pr->q_scale;
+  sp->q_scale_row_stride = pr->q_scale_row_stride;
+  sp->cu_seqlens_q = pr->cu_seqlens_q;
+  sp->cu_seqlens_k = pr->cu_seqlens_k;
+  sp->block_table = pr->block_table;
+  sp->page_offsets = pr->page_offsets;
+  sp->table_stride = pr->table_stride;
+  sp->visible_len = pr->visible_len;
+  sp->qo_offset = pr->qo_offset;
+  sp->causal = pr->causal;
+  sp->page_size = pr->page_size;
+  sp->num_pages = pr->num_pages;
+  sp->num_rows = pr->num_rows;
+  sp->num_heads = pr->num_heads;
+  sp->num_seqs = pr->num_seqs;
+  sp->row_groups = (pr->max_seqlen_q + rows_per_cta - 1) / rows_per_cta;
+  sp->w = w;
+  sp->w_row_stride = w_row_stride;
+  sp->err = err;
+  return FP4IDX_OK;
+}
+
+// Scorer CTAs for top-k: one per SM, fewer when there are fewer tiles.
+int topk_ctas(const fp4idx_problem_t* p, int sms) {
+  const int R = score_rows_per_cta(p->num_heads);
+  const int64_t items = static_cast<int64_t>(p->num_seqs) * ((p->max_seqlen_q + R - 1) / R);
+  const int64_t tiles = items * ((static_cast<int64_t>(p->max_seqlen_k) + kTileKeys - 1) / kTileKeys);
+  int64_t c = tiles < sms ? tiles : sms;
+  return c < 1 ? 1 : static_cast<int>(c);
+}
+
+struct TopkWorkspace {
+  size_t keys_off, count_off, bytes;
+};
+
+TopkWorkspace topk_workspace(const fp4idx_problem_t* p, int32_t k, int sms) {
+  const int R = score_rows_per_cta(p->num_heads);
+  const int64_t items = static_cast<int64_t>(p->num_seqs) * ((p->max_seqlen_q + R - 1) / R);
+  const int64_t slots = (topk_ctas(p, sms) + items) * R;
+  TopkWorkspace ws;
+  ws.keys_off = 0;
+  ws.count_off = (static_cast<size_t>(slots) * k * 8 + 255) / 256 * 256;
+  ws.bytes = ws.count_off + (static_cast<size_t>(slots) * 4 + 255) / 256 * 256;
+  return ws;
+}
+
+}  // namespace
+}  // namespace fp4idx
+
+using namespace fp4idx;
+
+extern "C" {
+
+const char* fp4idx_status_string(fp4idx_status_t s) {
+  switch (s) {
+    case FP4IDX_OK: return "ok";
+    case FP4IDX_EINVAL: return "invalid argument";
+    case FP4IDX_EUNSUPPORTED: return "unsupported configuration";
+    case FP4IDX_EWORKSPACE: return "workspace too small";
+    case FP4IDX_ECUDA: return "CUDA error";
+    case FP4IDX_EDEVICE: return "unsupported device";
+  }
+  return "unknown status";
+}
+
+const char* fp4idx_last_error_message(void) { return g_msg; }
+
+fp4idx_status_t fp4idx_logits(const fp4idx_problem_t* problem, const float* w, int64_t w_row_stride,
+                              float* logits, int64_t ld, void* stream) {
+  g_msg[0] = 0;
+  fp4idx_status_t s = check_problem(problem);
+  if (s != FP4IDX_OK) return s;
+  if ((s = check_weighted(problem, w, w_row_stride)) != FP4IDX_OK) return s;
+  if (!logits) return fail(FP4IDX_EINVAL, "logits is NULL");
+  if (ld < 1 || ld % 4 != 0) return fail(FP4IDX_EINVAL, "ld must be a positive multiple of 4");
+  if (!aligned(logits, 16)) return fail(FP4IDX_EINVAL, "logits must be 16-byte aligned");
+  if (problem->num_rows == 0) return FP4IDX_OK;
+  DeviceInfo* dev;
+  if ((s = device_info(&dev)) != FP4IDX_OK) return s;
+  const int R = score_rows_per_cta(problem->num_heads);
+  ScoreParams sp;
+  if ((s = fill_score_params(problem, w, w_row_stride, &sp, R, dev->err)) != FP4IDX_OK) return s;
+  sp.total_tiles = static_cast<int32_t>((ld + kTileKeys - 1) / kTileKeys);
+  sp.logits = logits;
+  sp.ld = ld;
+  sp.k = 1;
+  const int64_t items = static_cast<int64_t>(problem->num_seqs) * sp.row_groups;
+  const int64_t tiles = items * sp.total_tiles;
+  const int ctas = static_cast<int>(tiles < dev->sms ? tiles : dev->sms);
+  sp.score_ctas = ctas;
+  cudaError_t e = launch_score(sp, problem->format, kModeLogits, problem->num_heads, dim3(ctas),
+                               static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "scorer launch");
+  return FP4IDX_OK;
+}
+
+size_t fp4idx_topk_workspace_bytes(const fp4idx_problem_t* problem, int32_t k) {
+  if (check_problem(problem) != FP4IDX_OK || k < 1) return 0;
+  DeviceInfo* dev;
+  if (device_info(&dev) != FP4IDX_OK) return 0;
+  return topk_workspace(problem, k, dev->sms).bytes;
+}
+
+fp4idx_status_t fp4idx_topk(const fp4idx_problem_t* problem, const float* w, int64_t w_row_stride, int32_t k,
+                            uint32_t flags, int32_t* indices, float* values, int32_t* valid_count,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  g_msg[0] = 0;
+  fp4idx_status_t s = check_problem(problem);
+  if (s != FP4IDX_OK) return s;
+  if ((s = check_weighted(problem, w, w_row_stride)) != FP4IDX_OK) return s;
+  if (k < 1 || k > 2048) return fail(FP4IDX_EUNSUPPORTED, "k = %d: supported 1..2048", k);
+  if (flags & ~static_cast<uint32_t>(FP4IDX_TOPK_SORTED)) return fail(FP4IDX_EINVAL, "unknown flags 0x%x", flags);
+  if (!indices) return fail(FP4IDX_EINVAL, "indices is NULL");
+  if (problem->num_rows == 0) return FP4IDX_OK;
+  DeviceInfo* dev;
+  if ((s = device_info(&dev)) != FP4IDX_OK) return s;
+  const TopkWorkspace ws = topk_workspace(problem, k, dev->sms);
+  if (!workspace || workspace_bytes < ws.bytes)
+    return fail(FP4IDX_EWORKSPACE, "workspace needs %zu bytes (got %zu)", ws.bytes, workspace_bytes);
+  if (!aligned(workspace, 256)) return fail(FP4IDX_EINVAL, "workspace must be 256-byte aligned");
+  const int R = score_rows_per_cta(problem->num_heads);
+  ScoreParams sp;
+  if ((s = fill_score_params(problem, w, w_row_stride, &sp, R, dev->err)) != FP4IDX_OK) return s;
+  sp.total_tiles = (problem->max_seqlen_k + kTileKeys - 1) / kTileKeys;
+  sp.k = k;
+  sp.part_keys = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(workspace) + ws.keys_off);
+  sp.part_count = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + ws.count_off);
+  const int ctas = topk_ctas(problem, dev->sms);
+  sp.score_ctas = ctas;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_score(sp, problem->format, kModeTopk, problem->num_heads, dim3(ctas), st);
+  if (e != cudaSuccess) return cuda_fail(e, "scorer launch");
+  MergeParams mp;
+  mp.sp = sp;
+  mp.rows_per_cta = R;
+  mp.flags = flags;
+  mp.indices = indices;
+  mp.values = values;
+  mp.valid_count = valid_count;
+  e = launch_topk_merge(mp, problem->num_rows, st);
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return FP4IDX_OK;
+}
+
+fp4idx_status_t fp4idx_block_scores(const fp4idx_problem_t* problem, float* scores, void* stream) {
+  g_msg[0] = 0;
+  fp4idx_status_t s = check_problem(problem);
+  if (s != FP4IDX_OK) return s;
+  (void)scores;
+  (void)stream;
+  return fail(FP4IDX_EUNSUPPORTED, "block scores are not built yet");
+}
+
+fp4idx_status_t fp4idx_get_error(uint32_t* bits, int32_t clear, void* stream) {
+  g_msg[0] = 0;
+  if (!bits) return fail(FP4IDX_EINVAL, "bits is NULL");
+  DeviceInfo* dev;
+  fp4idx_status_t s = device_info(&dev);
+  if (s != FP4IDX_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  if ((e = cudaMemcpy(bits, dev->err, sizeof(uint32_t), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "read error word");
+  if (clear && (e = cudaMemset(dev->err, 0, sizeof(uint32_t))) != cudaSuccess)
+    return cuda_fail(e, "clear error word");
+  return FP4IDX_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,79 @@
+// internal.h -- launch parameters shared by the host layer (api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fp4idx {
+
+constexpr int kHeadDim = 128;
+constexpr int kTileKeys = 128;       // keys per MMA tile (M of the scorer MMA)
+constexpr int kCodeBytes = 64;       // packed E2M1 bytes per 128-value row
+
+enum Mode : int { kModeLogits = 0, kModeTopk = 1 };
+
+// Keys-on-M scorer: one CTA owns up to R query rows of one request (the MMA
+// N dimension is R*H) and a contiguous chunk of 128-key tiles.
+struct ScoreParams {
+  CUtensorMap tmap_k;   // 2D {64 B, num_pages*Hkv*page}, box {64, page}, 64B swizzle
+  CUtensorMap tmap_q;   // 3D {64 B, Hq, T}, box {64, H, R}, 64B swizzle
+  const uint8_t* k_scale;
+  const uint8_t* q_scale;
+  int64_t q_scale_row_stride;
+  const int32_t* cu_seqlens_q;
+  const int32_t* cu_seqlens_k;
+  const int32_t* block_table;
+  const int32_t* page_offsets;
+  int64_t table_stride;
+  const int32_t* visible_len;
+  const int32_t* qo_offset;
+  int32_t causal;
+  int32_t page_size;
+  int64_t num_pages;
+  int32_t num_rows;
+  int32_t num_heads;
+  int32_t num_seqs;
+  int32_t row_groups;       // ceil(max_seqlen_q / R) row groups per request
+  const float* w;
+  int64_t w_row_stride;
+  int32_t total_tiles;      // logits: output tiles per row group, ceil(ld / 128)
+  int32_t score_ctas;       // grid size of the scorer launch
+  // logits output
+  float* logits;
+  int64_t ld;
+  // top-k partials: slot s (s < score_ctas: first segment of CTA s; else
+  // score_ctas + item: an item that starts inside a CTA's chunk) x R rows,
+  // up to k keys each.
+  int32_t k;
+  uint64_t* part_keys;      // [slots * R][k]
+  int32_t* part_count;      // [slots * R]
+  uint32_t* err;
+};
+
+// Merge of the per-CTA top-k partials of each row into the final output.
+struct MergeParams {
+  ScoreParams sp;
+  int32_t rows_per_cta;
+  uint32_t flags;
+  int32_t* indices;
+  float* values;
+  int32_t* valid_count;
+};
+
+// Launchers (defined in the kernel translation units).  Return cudaSuccess
+// or the launch error.
+cudaError_t launch_score_mx(const ScoreParams& p, int mode, int heads, dim3 grid, cudaStream_t stream);
+cudaError_t launch_score_nv(const ScoreParams& p, int mode, int heads, dim3 grid, cudaStream_t stream);
+inline cudaError_t launch_score(const ScoreParams& p, int format, int mode, int heads, dim3 grid,
+                                cudaStream_t stream) {
+  return format == 0 ? launch_score_mx(p, mode, heads, grid, stream)
+                     : launch_score_nv(p, mode, heads, grid, stream);
+}
+cudaError_t launch_topk_merge(const MergeParams& p, int rows, cudaStream_t stream);
+
+// Query rows per scorer CTA for a head count (the MMA N is rows * heads).
+inline int score_rows_per_cta(int heads) { return heads >= 64 ? 2 : 4; }
+
+}  // namespace fp4idx

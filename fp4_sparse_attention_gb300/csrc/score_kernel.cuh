@@ -1,0 +1,738 @@
+// score_kernel.cuh -- keys-on-M FP4 indexer scorer for sm_103a.
+//
+// logit(t, s) = sum_h w[t,h] * max(q[t,h] . k[s], 0)  (CURRENT_ISSUE...,
+// "TL;DR"), evaluated as one tcgen05 block-scaled FP4 MMA per 128-key tile:
+//
+//   D[key, r*H + h] = sum_d K_real[key, d] * Q_real[row r, head h, d]
+//
+// with the 128 keys of a tile on the MMA M dimension (TMEM lanes) and the
+// R rows x H heads of one request on N (TMEM columns).  The head sum then is
+// a serial loop inside one thread: thread = key, no shuffles.
+//
+// Warp roles (192 threads):
+//   warp 0    producer: resolves pages through the block table, issues the
+//             TMA gather of K codes (64-byte swizzle) and the bulk copy of K
+//             scales into a kStages-deep shared-memory ring; loads Q per item.
+//   warp 1    MMA: owns the TMEM allocation, rewrites K / Q scales into the
+//             32x4x4 scale-factor atom, copies them to TMEM (tcgen05.cp) and
+//             issues two K=64 MMAs per tile into a double-buffered accumulator.
+//   warps 2-5 epilogue: tcgen05.ld of the accumulator, ReLU * w summed over
+//             heads (packed fp32x2 FMAs), visibility mask, then either the
+//             fp32 logits store or the streaming top-k append.
+//
+// Work split: the tiles of all (request, row-group) items are concatenated
+// and cut into gridDim.x equal contiguous chunks, one per CTA, so long and
+// short requests balance across the GPU.  A CTA that crosses an item
+// boundary reloads Q and, for top-k, flushes its per-row candidates.
+#pragma once
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "topk_smem.cuh"
+
+namespace fp4idx {
+
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr uint32_t kTmemCols = 512;
+
+template <int FMT>
+struct FmtTraits;
+template <>
+struct FmtTraits<0> {  // MXFP4: E8M0 per 32 values
+  static constexpr int G = 4, kAtoms = 1, kScaleVec = 2;
+  static constexpr bool kUe8m0 = true;
+};
+template <>
+struct FmtTraits<1> {  // NVFP4: E4M3 per 16 values
+  static constexpr int G = 8, kAtoms = 2, kScaleVec = 4;
+  static constexpr bool kUe8m0 = false;
+};
+
+// Per-CTA bookkeeping in shared memory.
+struct CtaState {
+  uint32_t tmem_base;
+  int32_t abort;
+  int32_t item0;        // item holding the first tile of this CTA's chunk
+  int32_t item0_start;  // global tile index where item0 starts
+  int32_t total_tiles;  // over all items
+  int32_t chunk;        // tiles per CTA
+  int32_t pad[2];
+};
+
+template <int R>
+struct RowState {  // epilogue view of the current item's rows
+  int32_t vis[R];
+  int32_t valid[R];
+  int32_t cnt[R];
+  int32_t pad[R];
+  uint64_t thr[R];  // inclusive acceptance threshold of each candidate buffer
+};
+
+__host__ __device__ constexpr int topk_capacity(int k) {
+  return 2 * ((k + 127) / 128) * 128 < 1024 ? 1024 : 2 * ((k + 127) / 128) * 128;
+}
+
+template <int H, int R, int FMT, int MODE>
+struct ScoreLayout {
+  static constexpr int N = H * R;
+  static_assert(N % 16 == 0 && N >= 16 && N <= 128, "MMA N");
+  static constexpr int G = FmtTraits<FMT>::G;
+  static constexpr int kAtoms = FmtTraits<FMT>::kAtoms;
+  static constexpr uint32_t kCodes = 0;                                  // kStages x 8 KB
+  static constexpr uint32_t kQ = kCodes + kStages * 8192;                // N x 64 B
+  static constexpr uint32_t kQBytes = ((N * 64 + 1023) / 1024) * 1024;
+  static constexpr uint32_t kRawSf = kQ + kQBytes;                       // kStages x 128*G
+  static constexpr uint32_t kSfa = kRawSf + kStages * 128 * G;           // kStages x kAtoms x 512
+  static constexpr uint32_t kSfb = kSfa + kStages * kAtoms * 512;        // kAtoms x 512
+  static constexpr uint32_t kBars = kSfb + kAtoms * 512;                 // mbarriers
+  static constexpr int kNumBars = 2 * kStages + 6;
+  static constexpr uint32_t kState = kBars + kNumBars * 8;
+  static constexpr uint32_t kRows = (kState + sizeof(CtaState) + 15) / 16 * 16;
+  static constexpr uint32_t kW = (kRows + sizeof(RowState<R>) + 15) / 16 * 16;  // N floats
+  static constexpr uint32_t kScan = kW + N * 4;                                  // kThreads ints
+  static constexpr uint32_t kScratch = kScan + kThreads * 4;
+  static constexpr uint32_t kHist = (kScratch + sizeof(SelectScratch) + 15) / 16 * 16;
+  static constexpr uint32_t kCand = kHist + (MODE == kModeTopk ? R * kHistBins * 4 : 0);
+  static constexpr uint32_t bytes(int cap) {
+    return kCand + (MODE == kModeTopk ? static_cast<uint32_t>(R) * cap * 8 : 0) + 1024;
+  }
+  // TMEM columns
+  static constexpr uint32_t kAccCol = 0;    // two accumulators of 128 columns
+  static constexpr uint32_t kSfbCol = 256;  // two Q-scale slots of 8 columns
+  static constexpr uint32_t kSfaCol = 272;  // kStages K-scale slots of 8 columns
+};
+
+// ---------------------------------------------------------------------------
+// Items: item i = (request b, row group g), i = b * row_groups + g.
+// ---------------------------------------------------------------------------
+struct ItemInfo {
+  int32_t b, row0, nrows, k_len;
+  int64_t table_base;
+};
+
+__device__ __forceinline__ ItemInfo item_info(const ScoreParams& p, int32_t i, int rows_per_cta) {
+  ItemInfo it;
+  it.b = i / p.row_groups;
+  const int g = i - it.b * p.row_groups;
+  const int q0 = __ldg(p.cu_seqlens_q + it.b), q1 = __ldg(p.cu_seqlens_q + it.b + 1);
+  it.row0 = q0 + g * rows_per_cta;
+  const int n = q1 - it.row0;
+  it.nrows = n < 0 ? 0 : (n > rows_per_cta ? rows_per_cta : n);
+  it.k_len = __ldg(p.cu_seqlens_k + it.b + 1) - __ldg(p.cu_seqlens_k + it.b);
+  it.table_base = p.page_offsets ? static_cast<int64_t>(__ldg(p.page_offsets + it.b))
+                                 : static_cast<int64_t>(it.b) * p.table_stride;
+  return it;
+}
+
+// Tiles an item contributes to the concatenated work space.
+template <int MODE>
+__device__ __forceinline__ int32_t item_tiles(const ScoreParams& p, const ItemInfo& it) {
+  if (it.nrows <= 0) return 0;
+  if constexpr (MODE == kModeLogits) return p.total_tiles;  // every output column of the rows
+  return (it.k_len + kTileKeys - 1) / kTileKeys;
+}
+
+// Visible key count of row t (rule of the public header).
+__device__ __forceinline__ int32_t row_visible(const ScoreParams& p, const ItemInfo& it, int32_t t) {
+  int64_t vis;
+  if (p.visible_len) {
+    vis = __ldg(p.visible_len + t);
+  } else if (p.causal) {
+    const int q0 = __ldg(p.cu_seqlens_q + it.b), q1 = __ldg(p.cu_seqlens_q + it.b + 1);
+    const int64_t off = p.qo_offset ? static_cast<int64_t>(__ldg(p.qo_offset + it.b))
+                                    : static_cast<int64_t>(it.k_len) - (q1 - q0);
+    vis = static_cast<int64_t>(t - q0) + off + 1;
+  } else {
+    vis = it.k_len;
+  }
+  if (vis < 0) vis = 0;
+  if (vis > it.k_len) vis = it.k_len;
+  return static_cast<int32_t>(vis);
+}
+
+// Cooperative over kNT threads (tid in [0, kNT)): prefix of item tiles.
+// Writes the total and, for the global tile x (if < total), the item
+// holding it and that item's start.  `scan` holds kNT ints.
+template <int MODE, int kNT>
+__device__ void plan_items(const ScoreParams& p, int rows_per_cta, int tid, int64_t x, int32_t* scan,
+                           int32_t* total_out, int32_t* item_out, int32_t* start_out) {
+  const int items = p.num_seqs * p.row_groups;
+  const int per = (items + kNT - 1) / kNT;
+  const int i0 = tid * per;
+  const int i1 = min(items, i0 + per);
+  int32_t s = 0;
+  for (int i = i0; i < i1; ++i) s += item_tiles<MODE>(p, item_info(p, i, rows_per_cta));
+  scan[tid] = s;
+  __syncthreads();
+  if (tid == 0) {
+    int32_t acc = 0;
+    for (int j = 0; j < kNT; ++j) {
+      const int32_t v = scan[j];
+      scan[j] = acc;
+      acc += v;
+    }
+    *total_out = acc;
+    *item_out = -1;
+    *start_out = 0;
+  }
+  __syncthreads();
+  const int32_t pre = scan[tid];
+  if (x < *total_out && pre <= x && x < pre + s) {
+    int32_t acc = pre;
+    for (int i = i0; i < i1; ++i) {
+      const int32_t ti = item_tiles<MODE>(p, item_info(p, i, rows_per_cta));
+      if (x < acc + ti) {
+        *item_out = i;
+        *start_out = acc;
+        break;
+      }
+      acc += ti;
+    }
+  }
+  __syncthreads();
+}
+
+// Visit the (item, tile range) segments of this CTA's chunk in order:
+// f(item, info, lo, hi, seg) with tiles [lo, hi) of the item, seg = index of
+// the segment within the chunk.
+template <int MODE, int R, class F>
+__device__ __forceinline__ void for_each_segment(const ScoreParams& p, const CtaState* st, F&& f) {
+  const int items = p.num_seqs * p.row_groups;
+  int64_t x = static_cast<int64_t>(blockIdx.x) * st->chunk;
+  const int64_t end = min(static_cast<int64_t>(st->total_tiles), x + st->chunk);
+  if (x >= end || st->item0 < 0) return;
+  int32_t i = st->item0;
+  int64_t start = st->item0_start;
+  int seg = 0;
+  while (x < end && i < items) {
+    const ItemInfo it = item_info(p, i, R);
+    const int32_t ti = item_tiles<MODE>(p, it);
+    const int64_t lo = x - start;
+    const int64_t hi = min(end, start + ti) - start;
+    if (hi > lo) {
+      f(i, it, static_cast<int>(lo), static_cast<int>(hi), seg);
+      ++seg;
+      x = start + hi;
+    }
+    start += ti;
+    ++i;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Scale-factor atoms.  tcgen05 reads a block scale of MMA row m from TMEM
+// lane m%32, column m/32; tcgen05.cp 32x128b.warpx4 fills 4 columns from a
+// 512-byte atom whose 16-byte line l holds, for row groups j = 0..3, the
+// four scale bytes of row 32j + l.
+// ---------------------------------------------------------------------------
+template <int FMT>
+__device__ __forceinline__ void k_scale_atoms(const uint8_t* raw, uint8_t* atoms, int lane) {
+  if constexpr (FMT == 0) {  // raw: [128 keys][4]
+    const uint32_t* r32 = reinterpret_cast<const uint32_t*>(raw);
+    uint4 v = make_uint4(r32[lane], r32[32 + lane], r32[64 + lane], r32[96 + lane]);
+    *reinterpret_cast<uint4*>(atoms + lane * 16) = v;
+  } else {  // raw: [128 keys][8]; atom 0 = scales 0..3, atom 1 = scales 4..7
+    const uint2* r64 = reinterpret_cast<const uint2*>(raw);
+    const uint2 a = r64[lane], b = r64[32 + lane], c = r64[64 + lane], d = r64[96 + lane];
+    *reinterpret_cast<uint4*>(atoms + lane * 16) = make_uint4(a.x, b.x, c.x, d.x);
+    *reinterpret_cast<uint4*>(atoms + 512 + lane * 16) = make_uint4(a.y, b.y, c.y, d.y);
+  }
+}
+
+// Q scales of the item's rows (B row n = r*H + h) into the atom layout.
+template <int H, int R, int FMT>
+__device__ __forceinline__ void q_scale_atoms(const ScoreParams& p, const ItemInfo& it, uint8_t* atoms,
+                                              int lane) {
+  constexpr int N = H * R;
+  constexpr int G = FmtTraits<FMT>::G;
+  uint32_t lo[4], hi[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int n = 32 * j + lane;
+    const int r = n / H, h = n % H;
+    lo[j] = 0;
+    hi[j] = 0;
+    if (n < N && r < it.nrows) {
+      const uint8_t* src = p.q_scale + static_cast<int64_t>(it.row0 + r) * p.q_scale_row_stride + h * G;
+      if constexpr (FMT == 0) {
+        lo[j] = __ldg(reinterpret_cast<const uint32_t*>(src));
+      } else {
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(src));
+        lo[j] = v.x;
+        hi[j] = v.y;
+      }
+    }
+  }
+  *reinterpret_cast<uint4*>(atoms + lane * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  if constexpr (FMT == 1)
+    *reinterpret_cast<uint4*>(atoms + 512 + lane * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+}
+
+// sum_h w[h] * max(v[h], 0), NaN propagating, with packed fp32x2 FMAs.
+template <int H>
+__device__ __forceinline__ float weighted_relu(const uint32_t (&v)[H], const float* w) {
+  float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int h = 0; h < H; h += 4) {
+    const float4 ww = *reinterpret_cast<const float4*>(w + h);
+    const float2 x0 = make_float2(relu_nan(__uint_as_float(v[h])), relu_nan(__uint_as_float(v[h + 1])));
+    const float2 x1 =
+        make_float2(relu_nan(__uint_as_float(v[h + 2])), relu_nan(__uint_as_float(v[h + 3])));
+    acc = __ffma2_rn(make_float2(ww.x, ww.y), x0, acc);
+    acc = __ffma2_rn(make_float2(ww.z, ww.w), x1, acc);
+  }
+  return acc.x + acc.y;
+}
+
+// Keep the keys >= T of cand[0, n) in place (order not kept); returns the
+// number kept.  All threads of the group call it.
+template <class G>
+__device__ int compact_keep_ge(const G& g, uint64_t* cand, int n, uint64_t T, SelectScratch* sc) {
+  const int lane = g.tid & 31;
+  if (g.tid == 0) sc->bcast[3] = 0;
+  g.sync();
+  constexpr int kPer = 8;
+  constexpr int kChunk = kEpiThreads * kPer;
+  for (int base = 0; base < n; base += kChunk) {
+    uint64_t v[kPer];
+    bool keep[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int idx = base + j * kEpiThreads + g.tid;
+      keep[j] = false;
+      v[j] = 0;
+      if (idx < n) {
+        v[j] = cand[idx];
+        keep[j] = v[j] >= T;
+      }
+    }
+    g.sync();
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const uint32_t m = __ballot_sync(0xffffffffu, keep[j]);
+      if (m) {
+        const int leader = __ffs(m) - 1;
+        uint32_t dst = 0;
+        if (lane == leader) dst = atomicAdd(&sc->bcast[3], static_cast<uint32_t>(__popc(m)));
+        dst = __shfl_sync(0xffffffffu, dst, leader);
+        if (keep[j]) cand[dst + __popc(m & ((1u << lane) - 1u))] = v[j];
+      }
+    }
+    g.sync();
+  }
+  const int kept = static_cast<int>(sc->bcast[3]);
+  g.sync();
+  return kept;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel.
+// ---------------------------------------------------------------------------
+template <int H, int R, int FMT, int MODE>
+__global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constant__ ScoreParams p) {
+  using L = ScoreLayout<H, R, FMT, MODE>;
+  using F = FmtTraits<FMT>;
+  constexpr int N = L::N;
+  constexpr int G = F::G;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto accf_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
+  auto acce_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
+  const uint32_t qfull_bar = bar0 + 8u * (2 * kStages + 4);
+  const uint32_t qempty_bar = bar0 + 8u * (2 * kStages + 5);
+
+  CtaState* st = reinterpret_cast<CtaState*>(smem + L::kState);
+  RowState<R>* rs = reinterpret_cast<RowState<R>*>(smem + L::kRows);
+  float* w_s = reinterpret_cast<float*>(smem + L::kW);
+  int32_t* scan = reinterpret_cast<int32_t*>(smem + L::kScan);
+  SelectScratch* sc = reinterpret_cast<SelectScratch*>(smem + L::kScratch);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L::kHist);
+  uint64_t* cand = reinterpret_cast<uint64_t*>(smem + L::kCand);
+  const int cap = topk_capacity(p.k);
+  volatile int* abort_flag = &st->abort;
+
+  // ---- plan this CTA's chunk of the concatenated tile space
+  {
+    int32_t total = 0, item = -1, start = 0;
+    if (threadIdx.x == 0) st->abort = 0;
+    // first pass only for the total; the chunk start depends on it
+    plan_items<MODE, kThreads>(p, R, threadIdx.x, INT64_MAX, scan, &st->total_tiles, &st->item0,
+                               &st->item0_start);
+    total = st->total_tiles;
+    const int32_t chunk = (total + gridDim.x - 1) / gridDim.x;
+    const int64_t x = static_cast<int64_t>(blockIdx.x) * chunk;
+    if (chunk == 0 || x >= total) return;  // uniform: no work for this CTA
+    plan_items<MODE, kThreads>(p, R, threadIdx.x, x, scan, &st->total_tiles, &st->item0, &st->item0_start);
+    if (threadIdx.x == 0) st->chunk = chunk;
+    (void)item;
+    (void)start;
+  }
+
+  // ---- one-time setup
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf_bar(a), 1);
+      mbar_init(acce_bar(a), kEpiThreads);
+    }
+    mbar_init(qfull_bar, 1);
+    mbar_init(qempty_bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc<kTmemCols>(smem_u32(&st->tmem_base));
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = st->tmem_base;
+
+  const uint32_t codes_s = smem_u32(smem + L::kCodes);
+  const uint32_t q_s = smem_u32(smem + L::kQ);
+  uint8_t* rawsf = smem + L::kRawSf;
+  uint8_t* sfa_atoms = smem + L::kSfa;
+  uint8_t* sfb_atoms = smem + L::kSfb;
+
+  if (warp == 0) {
+    // ================================================================ producer
+    if (lane == 0) {
+      prefetch_tmap(&p.tmap_k);
+      prefetch_tmap(&p.tmap_q);
+      uint32_t tile_iter = 0, item_iter = 0;
+      bool ok = true;
+      const int page = p.page_size;
+      const int slots = kTileKeys / page;
+      for_each_segment<MODE, R>(p, st, [&](int, const ItemInfo& it, int lo, int hi, int) {
+        if (!ok) return;
+        ok = mbar_wait(qempty_bar, (item_iter & 1u) ^ 1u, abort_flag, p.err);
+        if (!ok) return;
+        mbar_arrive_expect_tx(qfull_bar, N * kCodeBytes);
+        tma_load_3d(q_s, &p.tmap_q, 0, 0, it.row0, qfull_bar);
+        ++item_iter;
+        for (int j = lo; j < hi; ++j) {
+          if (MODE == kModeLogits && static_cast<int64_t>(j) * kTileKeys >= it.k_len) continue;
+          const int s = tile_iter % kStages;
+          const uint32_t ph = (tile_iter / kStages) & 1u;
+          ok = mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.err);
+          if (!ok) return;
+          int32_t phys[2] = {-1, -1};
+          uint32_t bytes = 0;
+          for (int sl = 0; sl < slots; ++sl) {
+            const int64_t key0 = static_cast<int64_t>(j) * kTileKeys + sl * page;
+            if (key0 < it.k_len) {
+              const int32_t pg = __ldg(p.block_table + it.table_base + key0 / page);
+              if (pg >= 0 && pg < p.num_pages) {
+                phys[sl] = pg;
+                bytes += page * (kCodeBytes + G);
+              } else {
+                atomicOr(p.err, kErrPageRange);
+              }
+            }
+          }
+          mbar_arrive_expect_tx(full_bar(s), bytes);
+          for (int sl = 0; sl < slots; ++sl) {
+            if (phys[sl] < 0) continue;
+            tma_load_2d(codes_s + s * 8192 + sl * page * kCodeBytes, &p.tmap_k, 0, phys[sl] * page,
+                        full_bar(s));
+            bulk_load(smem_u32(rawsf + s * 128 * G + sl * page * G),
+                      p.k_scale + static_cast<int64_t>(phys[sl]) * page * G, page * G, full_bar(s));
+          }
+          ++tile_iter;
+        }
+      });
+      if (!ok) {
+        // Let copies already in flight land before the CTA can exit.
+        const uint32_t first = tile_iter > kStages ? tile_iter - kStages : 0;
+        for (uint32_t u = first; u < tile_iter; ++u) {
+          volatile int never = 0;
+          mbar_wait(full_bar(u % kStages), (u / kStages) & 1u, &never, p.err);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    uint32_t tile_iter = 0, item_iter = 0;
+    bool ok = true;
+    int last_acc = -1;
+    uint32_t last_acc_phase = 0;
+    for_each_segment<MODE, R>(p, st, [&](int, const ItemInfo& it, int lo, int hi, int) {
+      if (!ok) return;
+      ok = __shfl_sync(0xffffffffu,
+                       lane == 0 ? mbar_wait(qfull_bar, item_iter & 1u, abort_flag, p.err) : false, 0);
+      if (!ok) return;
+      q_scale_atoms<H, R, FMT>(p, it, sfb_atoms, lane);
+      fence_proxy_async_smem();
+      __syncwarp();
+      tc_fence_after();
+      const uint32_t sfb_t = tmem + L::kSfbCol + (item_iter & 1u) * 8u;
+      if (lane == 0) {
+#pragma unroll
+        for (int a = 0; a < F::kAtoms; ++a)
+          tc_cp_32x128b_warpx4(sfb_t + 4u * a, desc_sf_atom(smem_u32(sfb_atoms + 512 * a)));
+      }
+      __syncwarp();
+      for (int j = lo; j < hi; ++j) {
+        if (MODE == kModeLogits && static_cast<int64_t>(j) * kTileKeys >= it.k_len) continue;
+        const int s = tile_iter % kStages;
+        const uint32_t ph = (tile_iter / kStages) & 1u;
+        const int a = tile_iter & 1u;
+        const uint32_t aph = (tile_iter >> 1) & 1u;
+        ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(full_bar(s), ph, abort_flag, p.err) : false, 0);
+        if (!ok) return;
+        k_scale_atoms<FMT>(rawsf + s * 128 * G, sfa_atoms + s * F::kAtoms * 512, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        ok = __shfl_sync(0xffffffffu,
+                         lane == 0 ? mbar_wait(acce_bar(a), aph ^ 1u, abort_flag, p.err) : false, 0);
+        if (!ok) return;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sfa_t = tmem + L::kSfaCol + s * 8u;
+#pragma unroll
+          for (int at = 0; at < F::kAtoms; ++at)
+            tc_cp_32x128b_warpx4(sfa_t + 4u * at,
+                                 desc_sf_atom(smem_u32(sfa_atoms + (s * F::kAtoms + at) * 512)));
+          const uint32_t d = tmem + L::kAccCol + a * 128u;
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const uint64_t adesc = desc_kmajor_sw64(codes_s + s * 8192 + 32 * kk);
+            const uint64_t bdesc = desc_kmajor_sw64(q_s + 32 * kk);
+            const uint32_t sf_id = F::kScaleVec == 2 ? 2u * kk : 0u;
+            const uint32_t idesc = idesc_fp4(128, N, F::kUe8m0, sf_id, sf_id);
+            const uint32_t col = F::kScaleVec == 2 ? 0u : 4u * kk;
+            tc_mma_fp4<F::kScaleVec>(d, adesc, bdesc, idesc, sfa_t + col, sfb_t + col,
+                                     static_cast<uint32_t>(kk));
+          }
+          tc_commit(empty_bar(s));
+          tc_commit(accf_bar(a));
+        }
+        __syncwarp();
+        last_acc = a;
+        last_acc_phase = aph;
+        ++tile_iter;
+      }
+      if (lane == 0) tc_commit(qempty_bar);
+      __syncwarp();
+      ++item_iter;
+    });
+    if (!ok && last_acc >= 0 && lane == 0) {
+      // Outstanding MMAs must finish before TMEM is released.
+      volatile int never = 0;
+      mbar_wait(accf_bar(last_acc), last_acc_phase, &never, p.err);
+    }
+    __syncwarp();
+  } else {
+    // ================================================================ epilogue
+    Group<kEpiThreads, 1> g{static_cast<int>(threadIdx.x) - 64};
+    const int quad = warp & 3;
+    const int key_local = quad * 32 + lane;
+    uint32_t tile_iter = 0;
+    bool ok = true;
+    for_each_segment<MODE, R>(p, st, [&](int item, const ItemInfo& it, int lo, int hi, int seg) {
+      // -- rows of this item
+      g.sync();
+      if (g.tid < R) {
+        const int r = g.tid;
+        const bool valid = r < it.nrows;
+        rs->valid[r] = valid ? 1 : 0;
+        rs->vis[r] = valid ? row_visible(p, it, it.row0 + r) : 0;
+        rs->cnt[r] = 0;
+        rs->thr[r] = 0;
+      }
+      for (int e = g.tid; e < N; e += kEpiThreads) {
+        const int r = e / H, h = e % H;
+        w_s[e] = r < it.nrows ? __ldg(p.w + static_cast<int64_t>(it.row0 + r) * p.w_row_stride + h) : 0.0f;
+      }
+      if constexpr (MODE == kModeTopk) {
+        for (int e = g.tid; e < R * kHistBins; e += kEpiThreads) hist[e] = 0;
+      }
+      g.sync();
+      for (int j = lo; j < hi; ++j) {
+        const int64_t pos = static_cast<int64_t>(j) * kTileKeys + key_local;
+        const bool real = !(MODE == kModeLogits && static_cast<int64_t>(j) * kTileKeys >= it.k_len);
+        float vals[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) vals[r] = -INFINITY;
+        if (real) {
+          const int a = tile_iter & 1u;
+          const uint32_t aph = (tile_iter >> 1) & 1u;
+          if (ok) ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(accf_bar(a), aph, abort_flag, p.err) : false, 0);
+          if (ok) {
+            tc_fence_after();
+            const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16) + L::kAccCol + a * 128u;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              uint32_t v[H];
+              tmem_ld<H>(trow + r * H, v);
+              tmem_wait_ld();
+              vals[r] = weighted_relu<H>(v, w_s + r * H);
+            }
+            tc_fence_before();
+            mbar_arrive(acce_bar(a));
+          }
+          ++tile_iter;
+        }
+        bool key_ok = false;
+        if (pos < it.k_len) {
+          const int32_t pg = __ldg(p.block_table + it.table_base + pos / p.page_size);
+          key_ok = pg >= 0 && pg < p.num_pages;
+        }
+        if constexpr (MODE == kModeLogits) {
+          if (ok) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              if (rs->valid[r] && pos < p.ld) {
+                const bool vis = key_ok && pos < rs->vis[r];
+                p.logits[static_cast<int64_t>(it.row0 + r) * p.ld + pos] = vis ? vals[r] : -INFINITY;
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const bool vis = ok && rs->valid[r] && key_ok && pos < rs->vis[r];
+            const uint64_t key = topk_key(vals[r], static_cast<uint32_t>(pos));
+            const bool take = vis && key >= rs->thr[r];
+            const uint32_t m = __ballot_sync(0xffffffffu, take);
+            if (m) {
+              const int leader = __ffs(m) - 1;
+              int base = 0;
+              if (lane == leader) base = atomicAdd(&rs->cnt[r], __popc(m));
+              base = __shfl_sync(0xffffffffu, base, leader);
+              const int o = base + __popc(m & ((1u << lane) - 1u));
+              if (take && o < cap) {
+                cand[r * cap + o] = key;
+                atomicAdd(&hist[r * kHistBins + static_cast<int>(key >> kHistShift)], 1u);
+              }
+            }
+          }
+          g.sync();
+          // -- compaction of full candidate buffers
+#pragma unroll 1
+          for (int r = 0; r < R; ++r) {
+            const int n = rs->cnt[r];
+            if (n <= cap - kTileKeys) continue;  // uniform: read after the barrier
+            uint32_t* hr = hist + r * kHistBins;
+            uint64_t* cr = cand + r * cap;
+            uint32_t above = 0;
+            const uint32_t bkt = find_kth_bucket(g, hr, static_cast<uint32_t>(p.k), sc, &above);
+            const uint32_t kept = above + hr[bkt];
+            uint64_t T = static_cast<uint64_t>(bkt) << kHistShift;
+            const bool exact = kept > static_cast<uint32_t>(cap - 2 * kTileKeys);
+            if (exact) {
+              T = select_in_bucket(g, bkt, static_cast<uint32_t>(p.k) - above, sc, [&](auto&& fn) {
+                for (int e = g.tid; e < n; e += kEpiThreads) fn(cr[e]);
+              });
+            }
+            const int left = compact_keep_ge(g, cr, n, T, sc);
+            for (int b = g.tid; b < static_cast<int>(bkt); b += kEpiThreads) hr[b] = 0;
+            g.sync();
+            if (g.tid == 0) {
+              if (exact) hr[bkt] = static_cast<uint32_t>(p.k) - above;
+              rs->cnt[r] = left;
+              rs->thr[r] = T;
+            }
+            g.sync();
+          }
+        }
+      }
+      if constexpr (MODE == kModeTopk) {
+        // -- flush the exact top-k of each row of this segment
+        const int slot = seg == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + item;
+#pragma unroll 1
+        for (int r = 0; r < R; ++r) {
+          g.sync();
+          const int n = rs->cnt[r];
+          uint32_t* hr = hist + r * kHistBins;
+          uint64_t* cr = cand + r * cap;
+          uint64_t T = 0;
+          if (n > p.k) {
+            uint32_t above = 0;
+            const uint32_t bkt = find_kth_bucket(g, hr, static_cast<uint32_t>(p.k), sc, &above);
+            T = select_in_bucket(g, bkt, static_cast<uint32_t>(p.k) - above, sc, [&](auto&& fn) {
+              for (int e = g.tid; e < n; e += kEpiThreads) fn(cr[e]);
+            });
+          }
+          const int64_t part = static_cast<int64_t>(slot) * R + r;
+          uint64_t* out = p.part_keys + part * p.k;
+          if (g.tid == 0) sc->bcast[3] = 0;
+          g.sync();
+          for (int base = 0; base < n; base += kEpiThreads) {
+            const int e = base + g.tid;
+            const uint64_t key = e < n ? cr[e] : 0;
+            const bool keep = ok && e < n && key >= T;
+            const uint32_t m = __ballot_sync(0xffffffffu, keep);
+            if (m) {
+              const int leader = __ffs(m) - 1;
+              uint32_t dst = 0;
+              if (lane == leader) dst = atomicAdd(&sc->bcast[3], static_cast<uint32_t>(__popc(m)));
+              dst = __shfl_sync(0xffffffffu, dst, leader);
+              const uint32_t o = dst + __popc(m & ((1u << lane) - 1u));
+              if (keep && o < static_cast<uint32_t>(p.k)) out[o] = key;
+            }
+          }
+          g.sync();
+          if (g.tid == 0) {
+            const int32_t wrote = static_cast<int32_t>(min(sc->bcast[3], static_cast<uint32_t>(p.k)));
+            p.part_count[part] = rs->valid[r] ? wrote : 0;
+          }
+        }
+      }
+    });
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<kTmemCols>(tmem);
+  }
+}
+
+template <int H, int R, int FMT, int MODE>
+cudaError_t launch_score_t(const ScoreParams& p, dim3 grid, cudaStream_t stream) {
+  using L = ScoreLayout<H, R, FMT, MODE>;
+  const uint32_t want = L::bytes(topk_capacity(p.k));
+  // At least ~120 KB so that one CTA (and one 512-column TMEM allocation) runs per SM.
+  const uint32_t bytes = want < 120u * 1024u ? 120u * 1024u : want;
+  if (bytes > 232448u) return cudaErrorInvalidConfiguration;
+  auto kern = score_kernel<H, R, FMT, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, bytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int FMT>
+cudaError_t launch_score_fmt(const ScoreParams& p, int mode, int heads, dim3 grid, cudaStream_t stream) {
+  if (mode == kModeLogits) {
+    switch (heads) {
+      case 8: return launch_score_t<8, 4, FMT, kModeLogits>(p, grid, stream);
+      case 16: return launch_score_t<16, 4, FMT, kModeLogits>(p, grid, stream);
+      case 32: return launch_score_t<32, 4, FMT, kModeLogits>(p, grid, stream);
+      case 64: return launch_score_t<64, 2, FMT, kModeLogits>(p, grid, stream);
+    }
+  } else {
+    switch (heads) {
+      case 8: return launch_score_t<8, 4, FMT, kModeTopk>(p, grid, stream);
+      case 16: return launch_score_t<16, 4, FMT, kModeTopk>(p, grid, stream);
+      case 32: return launch_score_t<32, 4, FMT, kModeTopk>(p, grid, stream);
+      case 64: return launch_score_t<64, 2, FMT, kModeTopk>(p, grid, stream);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fp4idx

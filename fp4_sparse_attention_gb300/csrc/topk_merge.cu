@@ -1,0 +1,190 @@
+// topk_merge.cu -- exact top-k of each query row from the per-CTA partial
+// candidate lists written by the scorer in top-k mode.
+//
+// Every scorer CTA kept, for each row of each item it touched, the exact
+// top-k of the keys it scored.  The union of those lists therefore holds the
+// row's global top-k; this kernel selects it exactly (bucket histogram, then
+// radix passes inside the bucket of the k-th key) and writes logical
+// positions, values and the valid count.  One CTA per query row.
+#include "score_kernel.cuh"
+
+namespace fp4idx {
+namespace {
+
+constexpr int kMergeThreads = 512;
+constexpr int kMergeBuf = 8192;  // keys of the k-th key's bucket held in shared memory
+
+struct MergeSmem {
+  uint32_t hist[kHistBins];
+  int32_t scan[kMergeThreads];
+  SelectScratch sc;
+  int32_t info[8];
+  uint64_t out[2048];
+  uint64_t buf[kMergeBuf];
+};
+
+// Tiles of all items before `item` and of all items (cooperative).
+__device__ void item_prefix(const ScoreParams& p, int rows_per_cta, int tid, int item, int32_t* scan,
+                            int32_t* before_out, int32_t* total_out) {
+  const int items = p.num_seqs * p.row_groups;
+  const int per = (items + kMergeThreads - 1) / kMergeThreads;
+  const int i0 = tid * per, i1 = min(items, i0 + per);
+  int32_t s_all = 0, s_before = 0;
+  for (int i = i0; i < i1; ++i) {
+    const int32_t ti = item_tiles<kModeTopk>(p, item_info(p, i, rows_per_cta));
+    s_all += ti;
+    if (i < item) s_before += ti;
+  }
+  scan[tid] = s_all;
+  __syncthreads();
+  if (tid == 0) {
+    int32_t acc = 0;
+    for (int j = 0; j < kMergeThreads; ++j) acc += scan[j];
+    *total_out = acc;
+  }
+  __syncthreads();
+  scan[tid] = s_before;
+  __syncthreads();
+  if (tid == 0) {
+    int32_t acc = 0;
+    for (int j = 0; j < kMergeThreads; ++j) acc += scan[j];
+    *before_out = acc;
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const __grid_constant__ MergeParams mp) {
+  const ScoreParams& p = mp.sp;
+  extern __shared__ uint8_t smem_raw[];
+  MergeSmem* sm = reinterpret_cast<MergeSmem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int t = blockIdx.x;
+  const int k = p.k;
+  const int R = mp.rows_per_cta;
+  Group<kMergeThreads, 0> g{tid};
+
+  // request of row t: largest b with cu_seqlens_q[b] <= t
+  int lo = 0, hi = p.num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(p.cu_seqlens_q + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
+  const int q_local = t - __ldg(p.cu_seqlens_q + b);
+  const int item = b * p.row_groups + q_local / R;
+  const int r = q_local % R;
+
+  for (int i = tid; i < kHistBins; i += kMergeThreads) sm->hist[i] = 0;
+  item_prefix(p, R, tid, item, sm->scan, &sm->info[0], &sm->info[1]);
+  const int32_t P = sm->info[0], total = sm->info[1];
+  const ItemInfo it = item_info(p, item, R);
+  const int32_t tiles = item_tiles<kModeTopk>(p, it);
+  const int C = p.score_ctas;
+  const int32_t chunk = total > 0 ? (total + C - 1) / C : 1;
+  const int c_lo = tiles > 0 ? P / chunk : 0;
+  const int c_hi = tiles > 0 ? (P + tiles - 1) / chunk : -1;
+  auto slot_of = [&](int c) -> int64_t {
+    const int s = static_cast<int64_t>(c) * chunk >= P ? c : C + item;
+    return static_cast<int64_t>(s) * R + r;
+  };
+  auto for_each_key = [&](auto&& fn) {
+    for (int c = c_lo; c <= c_hi; ++c) {
+      const int64_t part = slot_of(c);
+      const int n = __ldg(p.part_count + part);
+      const uint64_t* keys = p.part_keys + part * k;
+      for (int e = tid; e < n; e += kMergeThreads) fn(__ldg(keys + e));
+    }
+  };
+
+  // pass 1: bucket histogram of every candidate
+  g.sync();
+  for_each_key([&](uint64_t key) { atomicAdd(&sm->hist[key >> kHistShift], 1u); });
+  g.sync();
+  int M = 0;
+  for (int c = c_lo; c <= c_hi; ++c) M += __ldg(p.part_count + slot_of(c));
+  const int n_out = M < k ? M : k;
+
+  uint64_t T = 0;
+  if (M > k) {
+    uint32_t above = 0;
+    const uint32_t bkt = find_kth_bucket(g, sm->hist, static_cast<uint32_t>(k), &sm->sc, &above);
+    const uint32_t nb = sm->hist[bkt];
+    const uint32_t rank = static_cast<uint32_t>(k) - above;
+    if (nb <= static_cast<uint32_t>(kMergeBuf)) {
+      if (tid == 0) sm->info[2] = 0;
+      g.sync();
+      for_each_key([&](uint64_t key) {
+        if ((key >> kHistShift) == bkt) {
+          const uint32_t o = atomicAdd(reinterpret_cast<uint32_t*>(&sm->info[2]), 1u);
+          if (o < static_cast<uint32_t>(kMergeBuf)) sm->buf[o] = key;
+        }
+      });
+      g.sync();
+      const int nbuf = min(sm->info[2], kMergeBuf);
+      T = select_in_bucket(g, bkt, rank, &sm->sc, [&](auto&& fn) {
+        for (int e = tid; e < nbuf; e += kMergeThreads) fn(sm->buf[e]);
+      });
+    } else {
+      T = select_in_bucket(g, bkt, rank, &sm->sc, for_each_key);
+    }
+  }
+
+  // gather the selected keys
+  if (tid == 0) sm->info[3] = 0;
+  g.sync();
+  for_each_key([&](uint64_t key) {
+    if (key >= T) {
+      const uint32_t o = atomicAdd(reinterpret_cast<uint32_t*>(&sm->info[3]), 1u);
+      if (o < 2048u) sm->out[o] = key;
+    }
+  });
+  g.sync();
+
+  if (mp.flags & 1u) {
+    int P2 = 1;
+    while (P2 < n_out) P2 <<= 1;
+    for (int i = n_out + tid; i < P2; i += kMergeThreads) sm->out[i] = 0;
+    g.sync();
+    for (int size = 2; size <= P2; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = tid; i < P2; i += kMergeThreads) {
+          const int j = i ^ stride;
+          if (j > i) {
+            const uint64_t a = sm->out[i], c = sm->out[j];
+            const bool desc = (i & size) == 0;
+            if (desc ? (a < c) : (a > c)) {
+              sm->out[i] = c;
+              sm->out[j] = a;
+            }
+          }
+        }
+        g.sync();
+      }
+    }
+  }
+
+  const int64_t row = static_cast<int64_t>(t) * k;
+  for (int j = tid; j < k; j += kMergeThreads) {
+    const bool have = j < n_out;
+    const uint64_t key = have ? sm->out[j] : 0;
+    mp.indices[row + j] = have ? key_pos(key) : -1;
+    if (mp.values) mp.values[row + j] = have ? key_value(key) : -INFINITY;
+  }
+  if (tid == 0 && mp.valid_count) mp.valid_count[t] = n_out;
+  (void)lane;
+}
+
+}  // namespace
+
+cudaError_t launch_topk_merge(const MergeParams& p, int rows, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  const int bytes = static_cast<int>(sizeof(MergeSmem) + 16);
+  cudaError_t e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  topk_merge_kernel<<<rows, kMergeThreads, bytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace fp4idx

@@ -1,0 +1,194 @@
+/*
+ * fp4idx.h -- C ABI of the GB300 (sm_103a) FP4 lightning-indexer scorer.
+ *
+ * The scorer reads FP4 queries and a paged FP4 key cache and computes, for
+ * every query row t and logical key position s of its request,
+ *
+ *     dot(t, h, s)  = sum_{d<128} Q_real[t,h,d] * K_real[s,hk(h),d]
+ *     logit(t, s)   = sum_h w[t,h] * max(dot(t,h,s), 0)        (s visible)
+ *                   = -inf                                      (s not visible)
+ *
+ * (CURRENT_ISSUE_FROM_OUTSIDE_CONSULTANT.md, "TL;DR": I[t,s] = sum_h w_h *
+ * ReLU(q.K); M3-indexer README, "数学语义": Q_real/K_real are E2M1 values times
+ * their block scale, hk = h / (Hq/Hkv)).  Three outputs are offered: the full
+ * logits, the per-128-key block max of dot (M3-indexer README, "输出 shape 和
+ * 类型"), and the top-k positions of each row.
+ *
+ * Formats (M3-indexer README, "FP4 和 scale layout"; SGLang PR 42861,
+ * "Modifications"):
+ *   FP4IDX_MXFP4: E2M1 codes, one E8M0 scale per 32 values (G = 4 per row of
+ *                 128); scale value 2^(code-127), codes 1..254.
+ *   FP4IDX_NVFP4: E2M1 codes, one E4M3 scale per 16 values (G = 8), no
+ *                 tensor-level global scale; codes 0x00..0x7E.
+ * Two E2M1 codes per byte, the low nibble holding the even element.  The
+ * head dimension is fixed at 128 (64 bytes of codes per row).
+ *
+ * Memory and ownership.  Every pointer in fp4idx_problem_t, the weights, the
+ * outputs and the workspace are DEVICE pointers owned by the caller; the
+ * library never allocates, frees or retains them.  The library reads no
+ * device memory on the host and performs no host<->device synchronisation
+ * in fp4idx_logits / fp4idx_block_scores / fp4idx_topk, so those calls can be
+ * captured in a CUDA graph; the device metadata (sequence bounds, block
+ * table, visible lengths) is read on the device at run time, so replays see
+ * updated contents.
+ *
+ * Errors.  Argument checks run on the host before any launch and return
+ * FP4IDX_EINVAL / FP4IDX_EUNSUPPORTED / FP4IDX_EWORKSPACE without touching
+ * the device.  A block-table entry outside [0, num_pages) is found on the
+ * device: the keys of that page are treated as invisible and bit
+ * FP4IDX_ERR_PAGE_RANGE is set in the device error word; a pipeline wait
+ * that exceeds its time limit sets FP4IDX_ERR_TIMEOUT and the kernel returns
+ * early.  fp4idx_get_error() reads that word.  No kernel traps.
+ * fp4idx_last_error_message() gives a human-readable reason for the last
+ * non-OK status returned on the calling thread.
+ */
+#ifndef FP4IDX_H
+#define FP4IDX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fp4idx_format {
+  FP4IDX_MXFP4 = 0,
+  FP4IDX_NVFP4 = 1
+} fp4idx_format_t;
+
+typedef enum fp4idx_status {
+  FP4IDX_OK = 0,
+  FP4IDX_EINVAL = 1,        /* malformed argument: null pointer, size, stride or alignment */
+  FP4IDX_EUNSUPPORTED = 2,  /* well-formed but outside what the kernels implement          */
+  FP4IDX_EWORKSPACE = 3,    /* workspace missing or smaller than the size query returned   */
+  FP4IDX_ECUDA = 4,         /* a CUDA runtime or driver call failed                        */
+  FP4IDX_EDEVICE = 5        /* current device is not an sm_103 GPU                         */
+} fp4idx_status_t;
+
+/* Bits of the device error word. */
+#define FP4IDX_ERR_PAGE_RANGE 0x1u  /* block-table entry outside [0, num_pages)   */
+#define FP4IDX_ERR_TIMEOUT    0x2u  /* a pipeline wait exceeded its time limit    */
+
+/* Flags of fp4idx_topk. */
+#define FP4IDX_TOPK_SORTED 0x1u     /* order each row by (value desc, index asc)  */
+
+/*
+ * The problem: queries, the paged key cache and the visibility rule.
+ *
+ *   num_seqs B, num_rows T = cu_seqlens_q[B] (host copy supplied by the
+ *   caller), num_heads Hq, num_kv_heads Hkv (Hq % Hkv == 0), page_size 64 or
+ *   128 tokens, num_pages = physical pages in the cache.
+ *
+ *   q        [T][Hq][64] bytes, row t at q + t*q_row_stride (q_row_stride a
+ *            multiple of 16, >= Hq*64); 128-byte aligned base.
+ *   q_scale  [T][Hq][G] bytes, row t at q_scale + t*q_scale_row_stride (>= Hq*G).
+ *   k        [num_pages][Hkv][page_size][64] bytes, 128-byte aligned.
+ *   k_scale  [num_pages][Hkv][page_size][G] bytes, 16-byte aligned.
+ *   cu_seqlens_q, cu_seqlens_k  [B+1] int32 exclusive prefix sums of the
+ *            per-request query rows and key counts (M3-indexer README,
+ *            "输入 shape 和类型"); k_len[b] bounds the visible keys only.
+ *   block_table  logical page j of request b is the physical page
+ *            block_table[base(b) + j], base(b) = page_offsets[b] when
+ *            page_offsets != NULL (the README's kv_indices + cu_page_offsets
+ *            form), else b * table_stride (a [B][table_stride] table).
+ *   max_seqlen_q, max_seqlen_k  host upper bounds of q_len[b], k_len[b];
+ *            they size grids and outputs and must hold for the device data.
+ *
+ * Visible keys of row t in request b (q_local = t - cu_seqlens_q[b]):
+ *   visible_len != NULL:  vis = clamp(visible_len[t], 0, k_len[b])
+ *                          (SGLang PR 42861: a per-row visible length)
+ *   causal:               vis = clamp(q_local + off + 1, 0, k_len[b]),
+ *                          off = qo_offset ? qo_offset[b] : k_len[b]-q_len[b]
+ *                          (M3-indexer README, "数学语义": bottom-right causal)
+ *   otherwise:            vis = k_len[b]
+ * Positions [0, vis) are visible.  qo_offset with causal == 0 is EINVAL.
+ */
+typedef struct fp4idx_problem {
+  int32_t format;           /* fp4idx_format_t */
+  int32_t num_seqs;
+  int32_t num_rows;
+  int32_t num_heads;
+  int32_t num_kv_heads;
+  int32_t page_size;
+  int64_t num_pages;
+  int64_t table_stride;
+  int32_t max_seqlen_q;
+  int32_t max_seqlen_k;
+  const uint8_t* q;
+  const uint8_t* q_scale;
+  int64_t q_row_stride;
+  int64_t q_scale_row_stride;
+  const uint8_t* k;
+  const uint8_t* k_scale;
+  const int32_t* cu_seqlens_q;
+  const int32_t* cu_seqlens_k;
+  const int32_t* block_table;
+  const int32_t* page_offsets;
+  const int32_t* visible_len;
+  int32_t causal;
+  const int32_t* qo_offset;
+} fp4idx_problem_t;
+
+/*
+ * Full weighted-ReLU logits (CURRENT_ISSUE..., "TL;DR"; SGLang PR 42861,
+ * fp4_index_logits_paged: [rows, cap] fp32 with -inf where invisible).
+ *   w       [T][Hq] fp32 head weights, row stride w_row_stride floats (>= Hq).
+ *   logits  [T][ld] fp32; every column s in [0, ld) of every row is written:
+ *           logit(t, s) for s < vis(t), -inf otherwise.  ld % 4 == 0, ld >= 1.
+ * Supported: num_kv_heads == 1; num_heads in {8, 16, 32, 64}.
+ */
+fp4idx_status_t fp4idx_logits(const fp4idx_problem_t* problem, const float* w,
+                              int64_t w_row_stride, float* logits, int64_t ld,
+                              void* stream);
+
+/*
+ * Per-128-key block max of the unweighted dot (M3-indexer README,
+ * "数学语义" / "输出 shape 和类型"):
+ *   scores[h][kb][t] = max over visible s in [128*kb, 128*kb+128) of dot(t,h,s),
+ *                      -inf when the block has no visible key,
+ *   for kb < ceil(max_seqlen_k / 128).  scores is [Hq][Ktiles][T] fp32.
+ * Supported: Hq/Hkv <= 128 with Hq % Hkv == 0, num_heads <= 128.
+ */
+fp4idx_status_t fp4idx_block_scores(const fp4idx_problem_t* problem, float* scores,
+                                    void* stream);
+
+/*
+ * Top-k positions of each row's logits (CURRENT_ISSUE..., "Fix (production
+ * target)": ReLU + per-head weight epilogue followed by a top-k; the output
+ * convention is that of a sparse-attention consumer: logical positions, -1
+ * padding, a valid count).
+ *   indices      [T][k] int32: the min(k, vis(t)) positions with the largest
+ *                logits, ties broken by the lower position; -1 after them.
+ *                Order: (value desc, index asc) when flags has
+ *                FP4IDX_TOPK_SORTED, otherwise unspecified.
+ *   values       [T][k] fp32 logits of those positions (-inf padding), or NULL.
+ *   valid_count  [T] int32 = min(k, vis(t)), or NULL.
+ *   workspace    device scratch of at least fp4idx_topk_workspace_bytes();
+ *                may be NULL when that size is 0.  Contents need no
+ *                initialisation and are meaningless after the call.
+ * Full logits are never written to memory.
+ * Supported: num_kv_heads == 1; num_heads in {8, 16, 32, 64}; 1 <= k <= 4096.
+ */
+size_t fp4idx_topk_workspace_bytes(const fp4idx_problem_t* problem, int32_t k);
+fp4idx_status_t fp4idx_topk(const fp4idx_problem_t* problem, const float* w,
+                            int64_t w_row_stride, int32_t k, uint32_t flags,
+                            int32_t* indices, float* values, int32_t* valid_count,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Device error word of the current device (FP4IDX_ERR_* bits).  Synchronises
+ * `stream` first; when clear != 0 the word is reset to 0 afterwards.
+ */
+fp4idx_status_t fp4idx_get_error(uint32_t* bits, int32_t clear, void* stream);
+
+/* Static description of a status code. */
+const char* fp4idx_status_string(fp4idx_status_t status);
+
+/* Detail of the last non-OK status returned on this thread ("" if none). */
+const char* fp4idx_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP4IDX_H */

@@ -1,0 +1,101 @@
+"""The C-ABI library loads, exports every entry point include/fp4idx.h declares,
+and rejects malformed arguments on the host before touching any device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from fp4_sparse_attention_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load_library()
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(fp4idx_[a-z_0-9]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_symbols()
+    for required in ("fp4idx_logits", "fp4idx_block_scores", "fp4idx_topk",
+                     "fp4idx_topk_workspace_bytes", "fp4idx_get_error"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+    for name in binding.EXPORTED:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.fp4idx_status_string(s)
+    assert lib.fp4idx_status_string(99) == b"unknown status"
+
+
+def _problem(**over):
+    fake = 1 << 20  # 128-byte aligned non-null placeholder addresses; never dereferenced
+    c = binding.CProblem(format=0, num_seqs=1, num_rows=4, num_heads=32, num_kv_heads=1, page_size=64,
+                         num_pages=16, table_stride=16, max_seqlen_q=4, max_seqlen_k=1024,
+                         q=fake, q_scale=fake, q_row_stride=32 * 64, q_scale_row_stride=32 * 4, k=fake,
+                         k_scale=fake, cu_seqlens_q=fake, cu_seqlens_k=fake, block_table=fake,
+                         page_offsets=None, visible_len=None, causal=0, qo_offset=None)
+    for k_, v in over.items():
+        setattr(c, k_, v)
+    return c
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(format=7), 1),
+    (dict(num_seqs=0), 1),
+    (dict(num_heads=30, num_kv_heads=4), 1),
+    (dict(num_heads=30), 2),
+    (dict(page_size=32), 2),
+    (dict(q=(1 << 20) + 16), 1),
+    (dict(k_scale=(1 << 20) + 4), 1),
+    (dict(q_row_stride=100), 1),
+    (dict(table_stride=3), 1),
+    (dict(causal=0, qo_offset=1 << 20), 1),
+    (dict(num_kv_heads=2), 2),
+    (dict(num_heads=48, q_row_stride=48 * 64, q_scale_row_stride=48 * 4), 2),
+])
+def test_logits_rejects_bad_problems_on_host(lib, over, status):
+    c = _problem(**over)
+    w = ctypes.c_void_p(1 << 20)
+    out = ctypes.c_void_p(1 << 20)
+    got = lib.fp4idx_logits(ctypes.byref(c), w, 32, out, 1024, None)
+    assert got == status, lib.fp4idx_last_error_message()
+    assert lib.fp4idx_last_error_message()
+
+
+def test_null_problem_and_bad_ld(lib):
+    assert lib.fp4idx_logits(None, None, 0, None, 0, None) == 1
+    c = _problem()
+    assert lib.fp4idx_logits(ctypes.byref(c), ctypes.c_void_p(1 << 20), 32, ctypes.c_void_p(1 << 20), 6, None) == 1
+
+
+@pytest.mark.parametrize("k,flags,status", [(0, 0, 2), (4097, 0, 2), (64, 0x8, 1)])
+def test_topk_rejects_bad_k_and_flags(lib, k, flags, status):
+    c = _problem()
+    p = ctypes.c_void_p(1 << 20)
+    got = lib.fp4idx_topk(ctypes.byref(c), p, 32, k, flags, p, None, None, p, 1 << 30, None)
+    assert got == status
+
+
+def test_block_scores_rejects_bad_problem(lib):
+    c = _problem(format=3)
+    assert lib.fp4idx_block_scores(ctypes.byref(c), ctypes.c_void_p(1 << 20), None) == 1

@@ -1,0 +1,76 @@
+"""GPU parity of fp4idx_topk (fused scorer + streaming top-k + merge) against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp4_sparse_attention_gb300 import binding as B
+from fp4_sparse_attention_gb300 import workloads as wl
+from tests.parity import compare_topk
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(p, k, sorted_=False, dp=None):
+    dp = dp or B.DeviceProblem.from_host(p)
+    idx, val, cnt = B.fp4idx_topk(dp, torch.as_tensor(p.w).cuda(), k, sorted=sorted_)
+    torch.cuda.synchronize()
+    assert B.fp4idx_get_error() == 0
+    return idx.cpu().numpy(), val.cpu().numpy(), cnt.cpu().numpy()
+
+
+def _check(p, k, rows=None, sorted_=False):
+    idx, val, cnt = _run(p, k, sorted_)
+    rows = np.arange(p.num_rows) if rows is None else np.asarray(rows)
+    return compare_topk(p, rows, k, idx[rows], val[rows], cnt[rows], sorted_order=sorted_)
+
+
+def test_tiny_decode_top64():
+    _check(wl.tiny_mx_decode(), 64, sorted_=True)
+
+
+def test_verify_decode_16k_top2048():
+    _check(wl.verify_decode_16k(), 2048)
+
+
+def test_verify_decode_16k_strict_top2048_is_exact():
+    p = wl.verify_decode_16k(strict=True)
+    idx, val, cnt = _run(p, 2048, sorted_=True)
+    o_idx, o_val, o_cnt = oracle.topk(p, 2048)
+    np.testing.assert_array_equal(cnt, o_cnt)
+    np.testing.assert_array_equal(idx, o_idx)
+    np.testing.assert_array_equal(val, o_val)
+
+
+@pytest.mark.parametrize("fmt", [wl.MXFP4, wl.NVFP4])
+@pytest.mark.parametrize("heads,page,k", [(8, 64, 7), (16, 128, 300), (32, 64, 2048), (64, 128, 1)])
+def test_ragged_requests(fmt, heads, page, k):
+    p = wl.make_problem(name=f"ragged_topk_f{fmt}_h{heads}", seed=200 + heads + fmt, fmt=fmt,
+                        q_lens=[4, 1, 3, 6], k_lens=[5000, 129, 1, 2500], num_heads=heads, page_size=page,
+                        e8m0_range=(120, 134), weights="normal", cache_pages=200)
+    _check(p, k, sorted_=(k % 2 == 0))
+
+
+def test_rows_with_few_visible_keys():
+    p = wl.make_problem(name="few", seed=12, fmt=wl.MXFP4, q_lens=[5], k_lens=[3000], num_heads=32,
+                        visibility="explicit", visible_len=[0, 1, 100, 2047, 2049])
+    _check(p, 2048, sorted_=True)
+
+
+def test_ties_break_on_lower_position():
+    p = wl.make_problem(name="ties", seed=13, fmt=wl.MXFP4, q_lens=[4], k_lens=[4096], num_heads=8,
+                        weights="strict")
+    p.q_scale[...] = 127
+    p.k_scale[...] = 127
+    p.k[:, :, :, 4:] = 0  # only the first 8 elements of every key vary: many equal logits
+    idx, val, cnt = _run(p, 500, sorted_=True)
+    o_idx, o_val, o_cnt = oracle.topk(p, 500)
+    np.testing.assert_array_equal(idx, o_idx)
+    np.testing.assert_array_equal(val, o_val)
+
+
+def test_long_batched_decode_sampled_rows():
+    p = wl.long_batched_decode()
+    idx, val, cnt = _run(p, 2048)
+    rows = [0, 21, 63]
+    compare_topk(p, rows, 2048, idx[rows], val[rows], cnt[rows])
