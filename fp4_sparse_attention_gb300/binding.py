@@ -34,6 +34,8 @@ EXPORTED = (
     "fp4idx_block_scores",
     "fp4idx_topk_workspace_bytes",
     "fp4idx_topk",
+    "fp4idx_topk_score",
+    "fp4idx_topk_merge",
     "fp4idx_get_error",
     "fp4idx_status_string",
     "fp4idx_last_error_message",
@@ -100,6 +102,10 @@ def load_library(path: str = LIB_PATH):
         lib.fp4idx_topk_workspace_bytes.restype = sz
         lib.fp4idx_topk.argtypes = [P, vp, i64, i32, u32, vp, vp, vp, vp, sz, vp]
         lib.fp4idx_topk.restype = i32
+        lib.fp4idx_topk_score.argtypes = [P, vp, i64, i32, vp, sz, vp]
+        lib.fp4idx_topk_score.restype = i32
+        lib.fp4idx_topk_merge.argtypes = [P, i32, u32, vp, vp, vp, vp, sz, vp]
+        lib.fp4idx_topk_merge.restype = i32
         lib.fp4idx_get_error.argtypes = [ctypes.POINTER(u32), i32, vp]
         lib.fp4idx_get_error.restype = i32
         lib.fp4idx_status_string.argtypes = [i32]
@@ -254,6 +260,24 @@ def fp4idx_topk(problem: DeviceProblem, w: torch.Tensor, k: int, sorted: bool = 
                            _ptr(values), _ptr(valid_count), _ptr(workspace), workspace.numel(), _stream(stream)),
            "fp4idx_topk")
     return indices, values, valid_count
+
+
+def fp4idx_topk_score(problem: DeviceProblem, w: torch.Tensor, k: int, workspace: torch.Tensor, stream=None):
+    """Phase 1 of fp4idx_topk: scorer + per-CTA exact top-k partials in `workspace`."""
+    lib = load_library()
+    _check(lib.fp4idx_topk_score(ctypes.byref(problem.c), _ptr(w), w.stride(0), int(k), _ptr(workspace),
+                                 workspace.numel(), _stream(stream)), "fp4idx_topk_score")
+
+
+def fp4idx_topk_merge(problem: DeviceProblem, k: int, indices: torch.Tensor, values: Optional[torch.Tensor],
+                      valid_count: Optional[torch.Tensor], workspace: torch.Tensor, sorted: bool = False,
+                      stream=None):
+    """Phase 2 of fp4idx_topk: exact per-row top-k from the partials in `workspace`."""
+    lib = load_library()
+    flags = FP4IDX_TOPK_SORTED if sorted else 0
+    _check(lib.fp4idx_topk_merge(ctypes.byref(problem.c), int(k), flags, _ptr(indices), _ptr(values),
+                                 _ptr(valid_count), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "fp4idx_topk_merge")
 
 
 def fp4idx_get_error(clear: bool = True, stream=None) -> int:

@@ -140,13 +140,20 @@ fp4idx_status_t check_problem(const fp4idx_problem_t* p) {
   return FP4IDX_OK;
 }
 
-// Checks of the weighted-ReLU paths (logits, top-k).
-fp4idx_status_t check_weighted(const fp4idx_problem_t* p, const float* w, int64_t w_row_stride) {
+// Shapes the weighted-ReLU kernels (logits, top-k) implement.
+fp4idx_status_t check_weighted_shape(const fp4idx_problem_t* p) {
   if (p->num_kv_heads != 1)
     return fail(FP4IDX_EUNSUPPORTED, "weighted-ReLU scoring supports one K head (num_kv_heads = %d)",
                 p->num_kv_heads);
   if (p->num_heads != 8 && p->num_heads != 16 && p->num_heads != 32 && p->num_heads != 64)
     return fail(FP4IDX_EUNSUPPORTED, "num_heads %d: supported 8, 16, 32, 64", p->num_heads);
+  return FP4IDX_OK;
+}
+
+// Checks of the weighted-ReLU paths (logits, top-k) including the weights.
+fp4idx_status_t check_weighted(const fp4idx_problem_t* p, const float* w, int64_t w_row_stride) {
+  fp4idx_status_t s = check_weighted_shape(p);
+  if (s != FP4IDX_OK) return s;
   if (!w) return fail(FP4IDX_EINVAL, "w is NULL");
   if (!aligned(w, 4)) return fail(FP4IDX_EINVAL, "w must be 4-byte aligned");
   if (w_row_stride < p->num_heads) return fail(FP4IDX_EINVAL, "w_row_stride must be >= num_heads");
@@ -277,17 +284,20 @@ size_t fp4idx_topk_workspace_bytes(const fp4idx_problem_t* problem, int32_t k) {
   return topk_workspace(problem, k, dev->sms).bytes;
 }
 
-fp4idx_status_t fp4idx_topk(const fp4idx_problem_t* problem, const float* w, int64_t w_row_stride, int32_t k,
-                            uint32_t flags, int32_t* indices, float* values, int32_t* valid_count,
-                            void* workspace, size_t workspace_bytes, void* stream) {
-  g_msg[0] = 0;
+}  // extern "C"
+
+namespace fp4idx {
+namespace {
+
+// Validation and parameters common to both top-k phases.
+fp4idx_status_t topk_prepare(const fp4idx_problem_t* problem, const float* w, int64_t w_row_stride, int32_t k,
+                             void* workspace, size_t workspace_bytes, bool need_w, ScoreParams* sp,
+                             int* ctas) {
   fp4idx_status_t s = check_problem(problem);
   if (s != FP4IDX_OK) return s;
-  if ((s = check_weighted(problem, w, w_row_stride)) != FP4IDX_OK) return s;
+  s = need_w ? check_weighted(problem, w, w_row_stride) : check_weighted_shape(problem);
+  if (s != FP4IDX_OK) return s;
   if (k < 1 || k > 2048) return fail(FP4IDX_EUNSUPPORTED, "k = %d: supported 1..2048", k);
-  if (flags & ~static_cast<uint32_t>(FP4IDX_TOPK_SORTED)) return fail(FP4IDX_EINVAL, "unknown flags 0x%x", flags);
-  if (!indices) return fail(FP4IDX_EINVAL, "indices is NULL");
-  if (problem->num_rows == 0) return FP4IDX_OK;
   DeviceInfo* dev;
   if ((s = device_info(&dev)) != FP4IDX_OK) return s;
   const TopkWorkspace ws = topk_workspace(problem, k, dev->sms);
@@ -295,27 +305,67 @@ fp4idx_status_t fp4idx_topk(const fp4idx_problem_t* problem, const float* w, int
     return fail(FP4IDX_EWORKSPACE, "workspace needs %zu bytes (got %zu)", ws.bytes, workspace_bytes);
   if (!aligned(workspace, 256)) return fail(FP4IDX_EINVAL, "workspace must be 256-byte aligned");
   const int R = score_rows_per_cta(problem->num_heads);
+  if ((s = fill_score_params(problem, w, w_row_stride, sp, R, dev->err)) != FP4IDX_OK) return s;
+  sp->total_tiles = (problem->max_seqlen_k + kTileKeys - 1) / kTileKeys;
+  sp->k = k;
+  sp->part_keys = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(workspace) + ws.keys_off);
+  sp->part_count = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + ws.count_off);
+  *ctas = topk_ctas(problem, dev->sms);
+  sp->score_ctas = *ctas;
+  return FP4IDX_OK;
+}
+
+}  // namespace
+}  // namespace fp4idx
+
+extern "C" {
+
+fp4idx_status_t fp4idx_topk_score(const fp4idx_problem_t* problem, const float* w, int64_t w_row_stride,
+                                  int32_t k, void* workspace, size_t workspace_bytes, void* stream) {
+  g_msg[0] = 0;
+  if (problem && problem->num_rows == 0 && check_problem(problem) == FP4IDX_OK) return FP4IDX_OK;
   ScoreParams sp;
-  if ((s = fill_score_params(problem, w, w_row_stride, &sp, R, dev->err)) != FP4IDX_OK) return s;
-  sp.total_tiles = (problem->max_seqlen_k + kTileKeys - 1) / kTileKeys;
-  sp.k = k;
-  sp.part_keys = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(workspace) + ws.keys_off);
-  sp.part_count = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + ws.count_off);
-  const int ctas = topk_ctas(problem, dev->sms);
-  sp.score_ctas = ctas;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_score(sp, problem->format, kModeTopk, problem->num_heads, dim3(ctas), st);
+  int ctas = 0;
+  fp4idx_status_t s = topk_prepare(problem, w, w_row_stride, k, workspace, workspace_bytes, true, &sp, &ctas);
+  if (s != FP4IDX_OK) return s;
+  cudaError_t e = launch_score(sp, problem->format, kModeTopk, problem->num_heads, dim3(ctas),
+                               static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "scorer launch");
+  return FP4IDX_OK;
+}
+
+fp4idx_status_t fp4idx_topk_merge(const fp4idx_problem_t* problem, int32_t k, uint32_t flags, int32_t* indices,
+                                  float* values, int32_t* valid_count, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  g_msg[0] = 0;
+  if (flags & ~static_cast<uint32_t>(FP4IDX_TOPK_SORTED)) return fail(FP4IDX_EINVAL, "unknown flags 0x%x", flags);
+  if (!indices) return fail(FP4IDX_EINVAL, "indices is NULL");
+  if (problem && problem->num_rows == 0 && check_problem(problem) == FP4IDX_OK) return FP4IDX_OK;
+  ScoreParams sp;
+  int ctas = 0;
+  fp4idx_status_t s = topk_prepare(problem, nullptr, 0, k, workspace, workspace_bytes, false, &sp, &ctas);
+  if (s != FP4IDX_OK) return s;
   MergeParams mp;
   mp.sp = sp;
-  mp.rows_per_cta = R;
+  mp.rows_per_cta = score_rows_per_cta(problem->num_heads);
   mp.flags = flags;
   mp.indices = indices;
   mp.values = values;
   mp.valid_count = valid_count;
-  e = launch_topk_merge(mp, problem->num_rows, st);
+  cudaError_t e = launch_topk_merge(mp, problem->num_rows, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return FP4IDX_OK;
+}
+
+fp4idx_status_t fp4idx_topk(const fp4idx_problem_t* problem, const float* w, int64_t w_row_stride, int32_t k,
+                            uint32_t flags, int32_t* indices, float* values, int32_t* valid_count,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  g_msg[0] = 0;
+  if (flags & ~static_cast<uint32_t>(FP4IDX_TOPK_SORTED)) return fail(FP4IDX_EINVAL, "unknown flags 0x%x", flags);
+  if (!indices) return fail(FP4IDX_EINVAL, "indices is NULL");
+  fp4idx_status_t s = fp4idx_topk_score(problem, w, w_row_stride, k, workspace, workspace_bytes, stream);
+  if (s != FP4IDX_OK) return s;
+  return fp4idx_topk_merge(problem, k, flags, indices, values, valid_count, workspace, workspace_bytes, stream);
 }
 
 fp4idx_status_t fp4idx_block_scores(const fp4idx_problem_t* problem, float* scores, void* stream) {

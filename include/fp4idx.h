@@ -168,13 +168,30 @@ fp4idx_status_t fp4idx_block_scores(const fp4idx_problem_t* problem, float* scor
  *                may be NULL when that size is 0.  Contents need no
  *                initialisation and are meaningless after the call.
  * Full logits are never written to memory.
- * Supported: num_kv_heads == 1; num_heads in {8, 16, 32, 64}; 1 <= k <= 4096.
+ * Supported: num_kv_heads == 1; num_heads in {8, 16, 32, 64}; 1 <= k <= 2048.
  */
 size_t fp4idx_topk_workspace_bytes(const fp4idx_problem_t* problem, int32_t k);
 fp4idx_status_t fp4idx_topk(const fp4idx_problem_t* problem, const float* w,
                             int64_t w_row_stride, int32_t k, uint32_t flags,
                             int32_t* indices, float* values, int32_t* valid_count,
                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The two phases of fp4idx_topk, for callers that schedule them separately
+ * (fp4idx_topk is exactly fp4idx_topk_score followed by fp4idx_topk_merge
+ * on the same stream, problem, k and workspace).
+ *   fp4idx_topk_score  runs the scorer and leaves, in the workspace, the exact
+ *                      top-k of every row within each CTA's share of the keys.
+ *   fp4idx_topk_merge  selects each row's exact top-k from those partials and
+ *                      writes indices / values / valid_count as fp4idx_topk.
+ * The workspace must not be modified between the two calls.
+ */
+fp4idx_status_t fp4idx_topk_score(const fp4idx_problem_t* problem, const float* w,
+                                  int64_t w_row_stride, int32_t k, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+fp4idx_status_t fp4idx_topk_merge(const fp4idx_problem_t* problem, int32_t k, uint32_t flags,
+                                  int32_t* indices, float* values, int32_t* valid_count,
+                                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Device error word of the current device (FP4IDX_ERR_* bits).  Synchronises
