@@ -228,6 +228,14 @@ TopkWorkspace topk_workspace(const fp4idx_problem_t* p, int32_t k, int sms) {
 }
 
 }  // namespace
+
+void set_last_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+}
+
 }  // namespace fp4idx
 
 using namespace fp4idx;

@@ -73,6 +73,9 @@ inline cudaError_t launch_score(const ScoreParams& p, int format, int mode, int 
 }
 cudaError_t launch_topk_merge(const MergeParams& p, int rows, cudaStream_t stream);
 
+// Sets the message fp4idx_last_error_message() returns on this thread.
+void set_last_error(const char* fmt, ...);
+
 // Query rows per scorer CTA for a head count (the MMA N is rows * heads).
 inline int score_rows_per_cta(int heads) { return heads >= 64 ? 2 : 4; }
 

@@ -194,6 +194,30 @@ fp4idx_status_t fp4idx_topk_merge(const fp4idx_problem_t* problem, int32_t k, ui
                                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fp4idx_topk without a caller-supplied workspace, for callers that cannot
+ * allocate device memory: an engine that reserved the GPU's memory up front
+ * for its own pool (another cudaMalloc fails or fragments it), or a
+ * latency-critical loop that cannot take the synchronisation cudaMalloc and
+ * cudaFree imply.  The pages describe no such entry point; it exists only
+ * for these callers.
+ *
+ * Results are those of fp4idx_topk (same arguments, minus the workspace).
+ * The scratch is a fixed 16 MiB array inside the library's device memory,
+ * held by every GPU that loads the library until the process exits.  A
+ * problem whose fp4idx_topk_workspace_bytes() exceeds 16 MiB is rejected
+ * with FP4IDX_EWORKSPACE before anything runs.  The first call on a device
+ * looks up the array's device address (with that device current); make that
+ * first call before capturing any stream.  All calls on a device share the
+ * one array, so calls that may overlap on the GPU (different streams without
+ * ordering between them) race and must be serialised by the caller.  Nothing
+ * in it needs clearing between calls.  No memory is allocated or freed.
+ */
+fp4idx_status_t fp4idx_topk_noalloc(const fp4idx_problem_t* problem, const float* w,
+                                    int64_t w_row_stride, int32_t k, uint32_t flags,
+                                    int32_t* indices, float* values, int32_t* valid_count,
+                                    void* stream);
+
+/*
  * Device error word of the current device (FP4IDX_ERR_* bits).  Synchronises
  * `stream` first; when clear != 0 the word is reset to 0 afterwards.
  */
