@@ -192,6 +192,7 @@ fp4idx_status_t fill_score_params(const fp4idx_problem_t* pr, const float* w, in
   sp->qo_offset = pr->qo_offset;
   sp->causal = pr->causal;
   sp->page_size = pr->page_size;
+  sp->page_shift = pr->page_size == 128 ? 7 : 6;
   sp->num_pages = pr->num_pages;
   sp->num_rows = pr->num_rows;
   sp->num_heads = pr->num_heads;

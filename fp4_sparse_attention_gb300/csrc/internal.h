@@ -31,6 +31,7 @@ struct ScoreParams {
   const int32_t* qo_offset;
   int32_t causal;
   int32_t page_size;
+  int32_t page_shift;       // log2(page_size)
   int64_t num_pages;
   int32_t num_rows;
   int32_t num_heads;

@@ -9,16 +9,20 @@
 // R rows x H heads of one request on N (TMEM columns).  The head sum then is
 // a serial loop inside one thread: thread = key, no shuffles.
 //
-// Warp roles (192 threads):
+// Warp roles (64 + 128*R threads):
 //   warp 0    producer: resolves pages through the block table, issues the
 //             TMA gather of K codes (64-byte swizzle) and the bulk copy of K
 //             scales into a kStages-deep shared-memory ring; loads Q per item.
 //   warp 1    MMA: owns the TMEM allocation, rewrites K / Q scales into the
 //             32x4x4 scale-factor atom, copies them to TMEM (tcgen05.cp) and
 //             issues two K=64 MMAs per tile into a double-buffered accumulator.
-//   warps 2-5 epilogue: tcgen05.ld of the accumulator, ReLU * w summed over
-//             heads (packed fp32x2 FMAs), visibility mask, then either the
-//             fp32 logits store or the streaming top-k append.
+//   warps 2.. epilogue, one group of four warps (one warp per TMEM lane
+//             quadrant) per query row of the item: tcgen05.ld of the row's
+//             H accumulator columns, ReLU * w summed over heads (packed fp32x2
+//             FMAs, four independent chains), visibility mask, then either the
+//             fp32 logits store or the streaming top-k append.  Each group
+//             synchronises on its own named barrier, only every few tiles, so
+//             one row's candidate compaction never stalls another row.
 //
 // Work split: the tiles of all (request, row-group) items are concatenated
 // and cut into gridDim.x equal contiguous chunks, one per CTA, so long and
@@ -32,9 +36,7 @@
 
 namespace fp4idx {
 
-constexpr int kStages = 4;
-constexpr int kThreads = 192;
-constexpr int kEpiThreads = 128;
+constexpr int kEpiThreads = 128;  // one epilogue group: four warps, one per TMEM lane quadrant
 constexpr uint32_t kTmemCols = 512;
 
 template <int FMT>
@@ -76,6 +78,10 @@ __host__ __device__ constexpr int topk_capacity(int k) {
 
 template <int H, int R, int FMT, int MODE>
 struct ScoreLayout {
+  // K-tile ring depth: deeper for logits, where shared memory holds no candidates.
+  static constexpr int kStages = MODE == kModeTopk ? 6 : 8;
+  static constexpr int kGroups = R;  // epilogue groups, one query row each
+  static constexpr int kThreads = 64 + kEpiThreads * kGroups;
   static constexpr int N = H * R;
   static_assert(N % 16 == 0 && N >= 16 && N <= 128, "MMA N");
   static constexpr int G = FmtTraits<FMT>::G;
@@ -92,16 +98,17 @@ struct ScoreLayout {
   static constexpr uint32_t kRows = (kState + sizeof(CtaState) + 15) / 16 * 16;
   static constexpr uint32_t kW = (kRows + sizeof(RowState<R>) + 15) / 16 * 16;  // N floats
   static constexpr uint32_t kScan = kW + N * 4;                                  // kThreads ints
-  static constexpr uint32_t kScratch = kScan + kThreads * 4;
-  static constexpr uint32_t kHist = (kScratch + sizeof(SelectScratch) + 15) / 16 * 16;
-  static constexpr uint32_t kCand = kHist + (MODE == kModeTopk ? R * kHistBins * 4 : 0);
+  static constexpr uint32_t kScratch = kScan + kThreads * 4;                      // per group
+  static constexpr uint32_t kHist = (kScratch + kGroups * sizeof(SelectScratch) + 15) / 16 * 16;
+  static constexpr uint32_t kCand = kHist + (MODE == kModeTopk ? R * kHistBins * 2 : 0);
   static constexpr uint32_t bytes(int cap) {
     return kCand + (MODE == kModeTopk ? static_cast<uint32_t>(R) * cap * 8 : 0) + 1024;
   }
   // TMEM columns
   static constexpr uint32_t kAccCol = 0;    // two accumulators of 128 columns
   static constexpr uint32_t kSfbCol = 256;  // two Q-scale slots of 8 columns
-  static constexpr uint32_t kSfaCol = 272;  // kStages K-scale slots of 8 columns
+  static constexpr uint32_t kSfaCol = 272;  // kStages K-scale slots of 8 columns (<= 64)
+  static_assert(kSfaCol + 8 * kStages <= kTmemCols, "TMEM columns");
 };
 
 // ---------------------------------------------------------------------------
@@ -270,20 +277,27 @@ __device__ __forceinline__ void q_scale_atoms(const ScoreParams& p, const ItemIn
     *reinterpret_cast<uint4*>(atoms + 512 + lane * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
 }
 
-// sum_h w[h] * max(v[h], 0), NaN propagating, with packed fp32x2 FMAs.
+// sum_h w[h] * max(v[h], 0), NaN propagating, with packed fp32x2 FMAs in
+// four independent chains.
 template <int H>
-__device__ __forceinline__ float weighted_relu(const uint32_t (&v)[H], const float* w) {
-  float2 acc = make_float2(0.0f, 0.0f);
+__device__ __forceinline__ float weighted_relu(const uint32_t* v, const float* w) {
+  constexpr int kChains = H >= 16 ? 4 : 2;
+  float2 acc[kChains];
+#pragma unroll
+  for (int c = 0; c < kChains; ++c) acc[c] = make_float2(0.0f, 0.0f);
 #pragma unroll
   for (int h = 0; h < H; h += 4) {
     const float4 ww = *reinterpret_cast<const float4*>(w + h);
     const float2 x0 = make_float2(relu_nan(__uint_as_float(v[h])), relu_nan(__uint_as_float(v[h + 1])));
     const float2 x1 =
         make_float2(relu_nan(__uint_as_float(v[h + 2])), relu_nan(__uint_as_float(v[h + 3])));
-    acc = __ffma2_rn(make_float2(ww.x, ww.y), x0, acc);
-    acc = __ffma2_rn(make_float2(ww.z, ww.w), x1, acc);
+    const int c = (h / 2) % kChains;
+    acc[c] = __ffma2_rn(make_float2(ww.x, ww.y), x0, acc[c]);
+    acc[c + 1] = __ffma2_rn(make_float2(ww.z, ww.w), x1, acc[c + 1]);
   }
-  return acc.x + acc.y;
+#pragma unroll
+  for (int c = 1; c < kChains; ++c) acc[0] = __fadd2_rn(acc[0], acc[c]);
+  return acc[0].x + acc[0].y;
 }
 
 // Keep the keys >= T of cand[0, n) in place (order not kept); returns the
@@ -331,11 +345,13 @@ __device__ int compact_keep_ge(const G& g, uint64_t* cand, int n, uint64_t T, Se
 // The kernel.
 // ---------------------------------------------------------------------------
 template <int H, int R, int FMT, int MODE>
-__global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constant__ ScoreParams p) {
+__global__ void __launch_bounds__(64 + kEpiThreads * R, 1) score_kernel(const __grid_constant__ ScoreParams p) {
   using L = ScoreLayout<H, R, FMT, MODE>;
+  constexpr int kThreads = L::kThreads;
   using F = FmtTraits<FMT>;
   constexpr int N = L::N;
   constexpr int G = F::G;
+  constexpr int kStages = L::kStages;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -356,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
   float* w_s = reinterpret_cast<float*>(smem + L::kW);
   int32_t* scan = reinterpret_cast<int32_t*>(smem + L::kScan);
   SelectScratch* sc = reinterpret_cast<SelectScratch*>(smem + L::kScratch);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L::kHist);
+  uint32_t* hist_words = reinterpret_cast<uint32_t*>(smem + L::kHist);
   uint64_t* cand = reinterpret_cast<uint64_t*>(smem + L::kCand);
   const int cap = topk_capacity(p.k);
   volatile int* abort_flag = &st->abort;
@@ -386,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf_bar(a), 1);
-      mbar_init(acce_bar(a), kEpiThreads);
+      mbar_init(acce_bar(a), L::kGroups * kEpiThreads);
     }
     mbar_init(qfull_bar, 1);
     mbar_init(qempty_bar, 1);
@@ -406,60 +422,76 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
 
   if (warp == 0) {
     // ================================================================ producer
+    // The whole warp walks the tiles.  Lane l caches the physical id of
+    // logical page base+l (and of the next 32, prefetched); for each tile the
+    // lanes sl < slots pick up the id of page sl and issue that page's code
+    // and scale copies together, one warp instruction per copy type.
+    uint32_t tile_iter = 0, item_iter = 0;
+    bool ok = true;
+    const int page = p.page_size;
+    const int pshift = p.page_shift;
+    const int slots = kTileKeys >> pshift;  // 2 for 64-key pages, 1 for 128
     if (lane == 0) {
       prefetch_tmap(&p.tmap_k);
       prefetch_tmap(&p.tmap_q);
-      uint32_t tile_iter = 0, item_iter = 0;
-      bool ok = true;
-      const int page = p.page_size;
-      const int slots = kTileKeys / page;
-      for_each_segment<MODE, R>(p, st, [&](int, const ItemInfo& it, int lo, int hi, int) {
-        if (!ok) return;
-        ok = mbar_wait(qempty_bar, (item_iter & 1u) ^ 1u, abort_flag, p.err);
-        if (!ok) return;
+    }
+    for_each_segment<MODE, R>(p, st, [&](int, const ItemInfo& it, int lo, int hi, int) {
+      if (!ok) return;
+      ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(qempty_bar, (item_iter & 1u) ^ 1u, abort_flag, p.err) : false, 0);
+      if (!ok) return;
+      if (lane == 0) {
         mbar_arrive_expect_tx(qfull_bar, N * kCodeBytes);
         tma_load_3d(q_s, &p.tmap_q, 0, 0, it.row0, qfull_bar);
-        ++item_iter;
-        for (int j = lo; j < hi; ++j) {
-          if (MODE == kModeLogits && static_cast<int64_t>(j) * kTileKeys >= it.k_len) continue;
-          const int s = tile_iter % kStages;
-          const uint32_t ph = (tile_iter / kStages) & 1u;
-          ok = mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.err);
-          if (!ok) return;
-          int32_t phys[2] = {-1, -1};
-          uint32_t bytes = 0;
-          for (int sl = 0; sl < slots; ++sl) {
-            const int64_t key0 = static_cast<int64_t>(j) * kTileKeys + sl * page;
-            if (key0 < it.k_len) {
-              const int32_t pg = __ldg(p.block_table + it.table_base + key0 / page);
-              if (pg >= 0 && pg < p.num_pages) {
-                phys[sl] = pg;
-                bytes += page * (kCodeBytes + G);
-              } else {
-                atomicOr(p.err, kErrPageRange);
-              }
-            }
-          }
-          mbar_arrive_expect_tx(full_bar(s), bytes);
-          for (int sl = 0; sl < slots; ++sl) {
-            if (phys[sl] < 0) continue;
-            tma_load_2d(codes_s + s * 8192 + sl * page * kCodeBytes, &p.tmap_k, 0, phys[sl] * page,
-                        full_bar(s));
-            bulk_load(smem_u32(rawsf + s * 128 * G + sl * page * G),
-                      p.k_scale + static_cast<int64_t>(phys[sl]) * page * G, page * G, full_bar(s));
-          }
-          ++tile_iter;
+      }
+      ++item_iter;
+      const int32_t npages = (it.k_len + page - 1) >> pshift;
+      const int32_t* table = p.block_table + it.table_base;
+      auto fetch = [&](int32_t b) -> int32_t {
+        const int32_t lp = b + lane;
+        return lp < npages ? __ldg(table + lp) : -1;
+      };
+      int32_t base = (lo * slots) & ~31;
+      int32_t cur_ids = fetch(base), next_ids = fetch(base + 32);
+      for (int j = lo; j < hi; ++j) {
+        if (MODE == kModeLogits && (j << 7) >= it.k_len) continue;
+        const int32_t lp0 = j * slots;
+        if (lp0 >= base + 32) {  // warp-uniform
+          base += 32;
+          cur_ids = next_ids;
+          next_ids = fetch(base + 32);
         }
-      });
-      if (!ok) {
-        // Let copies already in flight land before the CTA can exit.
-        const uint32_t first = tile_iter > kStages ? tile_iter - kStages : 0;
-        for (uint32_t u = first; u < tile_iter; ++u) {
-          volatile int never = 0;
-          mbar_wait(full_bar(u % kStages), (u / kStages) & 1u, &never, p.err);
+        const int32_t phys = __shfl_sync(0xffffffffu, cur_ids, (lp0 - base) + (lane & (slots - 1)));
+        const bool mine = lane < slots;
+        const bool in_req = mine && ((lp0 + lane) << pshift) < it.k_len;
+        const bool valid = in_req && phys >= 0 && phys < p.num_pages;
+        if (in_req && !valid) atomicOr(p.err, kErrPageRange);
+        const uint32_t bytes =
+            static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, valid))) * page * (kCodeBytes + G);
+        const int s = tile_iter % kStages;
+        const uint32_t ph = (tile_iter / kStages) & 1u;
+        ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.err) : false, 0);
+        if (!ok) return;
+        if (lane == 0) mbar_arrive_expect_tx(full_bar(s), bytes);
+        __syncwarp();
+        if (valid) {
+          tma_load_2d(codes_s + s * 8192 + ((lane * kCodeBytes) << pshift), &p.tmap_k, 0, phys << pshift,
+                      full_bar(s));
+          bulk_load(smem_u32(rawsf + s * 128 * G + ((lane * G) << pshift)),
+                    p.k_scale + (static_cast<int64_t>(phys) << pshift) * G, page * G, full_bar(s));
         }
+        __syncwarp();
+        ++tile_iter;
+      }
+    });
+    if (!ok && lane == 0) {
+      // Let copies already in flight land before the CTA can exit.
+      const uint32_t first = tile_iter > static_cast<uint32_t>(kStages) ? tile_iter - kStages : 0;
+      for (uint32_t u = first; u < tile_iter; ++u) {
+        volatile int never = 0;
+        mbar_wait(full_bar(u % kStages), (u / kStages) & 1u, &never, p.err);
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ================================================================ MMA issuer
     uint32_t tile_iter = 0, item_iter = 0;
@@ -534,75 +566,92 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     __syncwarp();
   } else {
     // ================================================================ epilogue
-    Group<kEpiThreads, 1> g{static_cast<int>(threadIdx.x) - 64};
+    constexpr int RG = R / L::kGroups;  // rows of one group
+    const int gi = (warp - 2) >> 2;
+    // Compaction is checked every `check_every` tiles; the buffer keeps that
+    // many tiles of room above the trigger so appends never overflow it.
+    const int check_every = max(1, min(4, (cap - p.k) / (2 * kTileKeys)));
+    const int margin = check_every * kTileKeys;
+    int since_check = 0;
+    Group<kEpiThreads, -1> g{static_cast<int>(threadIdx.x) - 64 - gi * kEpiThreads, 1 + gi};
+    SelectScratch* gsc = sc + gi;
     const int quad = warp & 3;
     const int key_local = quad * 32 + lane;
+    const int r0 = gi * RG;
     uint32_t tile_iter = 0;
     bool ok = true;
     for_each_segment<MODE, R>(p, st, [&](int item, const ItemInfo& it, int lo, int hi, int seg) {
-      // -- rows of this item
+      // -- this group's rows of the item
       g.sync();
-      if (g.tid < R) {
-        const int r = g.tid;
+      if (g.tid < RG) {
+        const int r = r0 + g.tid;
         const bool valid = r < it.nrows;
         rs->valid[r] = valid ? 1 : 0;
         rs->vis[r] = valid ? row_visible(p, it, it.row0 + r) : 0;
         rs->cnt[r] = 0;
         rs->thr[r] = 0;
       }
-      for (int e = g.tid; e < N; e += kEpiThreads) {
-        const int r = e / H, h = e % H;
-        w_s[e] = r < it.nrows ? __ldg(p.w + static_cast<int64_t>(it.row0 + r) * p.w_row_stride + h) : 0.0f;
+      for (int e = g.tid; e < RG * H; e += kEpiThreads) {
+        const int r = r0 + e / H, h = e % H;
+        w_s[r * H + h] =
+            r < it.nrows ? __ldg(p.w + static_cast<int64_t>(it.row0 + r) * p.w_row_stride + h) : 0.0f;
       }
       if constexpr (MODE == kModeTopk) {
-        for (int e = g.tid; e < R * kHistBins; e += kEpiThreads) hist[e] = 0;
+        for (int e = g.tid; e < RG * kHistBins / 2; e += kEpiThreads)
+          hist_words[r0 * (kHistBins / 2) + e] = 0;
       }
       g.sync();
+      // page id of this thread's key, one tile ahead (validity check off the critical path)
+      auto page_of = [&](int j) -> int32_t {
+        const int32_t pos = (j << 7) + key_local;
+        return pos < it.k_len ? __ldg(p.block_table + it.table_base + (pos >> p.page_shift)) : -1;
+      };
+      int32_t pg_cur = lo < hi ? page_of(lo) : -1;
       for (int j = lo; j < hi; ++j) {
+        const int32_t pg_next = j + 1 < hi ? page_of(j + 1) : -1;
         const int64_t pos = static_cast<int64_t>(j) * kTileKeys + key_local;
         const bool real = !(MODE == kModeLogits && static_cast<int64_t>(j) * kTileKeys >= it.k_len);
-        float vals[R];
+        float vals[RG];
 #pragma unroll
-        for (int r = 0; r < R; ++r) vals[r] = -INFINITY;
+        for (int rr = 0; rr < RG; ++rr) vals[rr] = -INFINITY;
         if (real) {
           const int a = tile_iter & 1u;
           const uint32_t aph = (tile_iter >> 1) & 1u;
           if (ok) ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(accf_bar(a), aph, abort_flag, p.err) : false, 0);
           if (ok) {
             tc_fence_after();
-            const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16) + L::kAccCol + a * 128u;
+            const uint32_t tcol =
+                tmem + (static_cast<uint32_t>(quad * 32) << 16) + L::kAccCol + a * 128u + r0 * H;
+            uint32_t v[RG * H];
+            tmem_ld<RG * H>(tcol, v);
+            tmem_wait_ld();
+            reg_fence(v);
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-              uint32_t v[H];
-              tmem_ld<H>(trow + r * H, v);
-              tmem_wait_ld();
-              vals[r] = weighted_relu<H>(v, w_s + r * H);
-            }
+            for (int rr = 0; rr < RG; ++rr) vals[rr] = weighted_relu<H>(v + rr * H, w_s + (r0 + rr) * H);
             tc_fence_before();
             mbar_arrive(acce_bar(a));
           }
           ++tile_iter;
         }
-        bool key_ok = false;
-        if (pos < it.k_len) {
-          const int32_t pg = __ldg(p.block_table + it.table_base + pos / p.page_size);
-          key_ok = pg >= 0 && pg < p.num_pages;
-        }
+        const bool key_ok = pg_cur >= 0 && pg_cur < p.num_pages;
+        pg_cur = pg_next;
         if constexpr (MODE == kModeLogits) {
           if (ok) {
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
+            for (int rr = 0; rr < RG; ++rr) {
+              const int r = r0 + rr;
               if (rs->valid[r] && pos < p.ld) {
                 const bool vis = key_ok && pos < rs->vis[r];
-                p.logits[static_cast<int64_t>(it.row0 + r) * p.ld + pos] = vis ? vals[r] : -INFINITY;
+                p.logits[static_cast<int64_t>(it.row0 + r) * p.ld + pos] = vis ? vals[rr] : -INFINITY;
               }
             }
           }
         } else {
 #pragma unroll
-          for (int r = 0; r < R; ++r) {
+          for (int rr = 0; rr < RG; ++rr) {
+            const int r = r0 + rr;
             const bool vis = ok && rs->valid[r] && key_ok && pos < rs->vis[r];
-            const uint64_t key = topk_key(vals[r], static_cast<uint32_t>(pos));
+            const uint64_t key = topk_key(vals[rr], static_cast<uint32_t>(pos));
             const bool take = vis && key >= rs->thr[r];
             const uint32_t m = __ballot_sync(0xffffffffu, take);
             if (m) {
@@ -613,33 +662,38 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
               const int o = base + __popc(m & ((1u << lane) - 1u));
               if (take && o < cap) {
                 cand[r * cap + o] = key;
-                atomicAdd(&hist[r * kHistBins + static_cast<int>(key >> kHistShift)], 1u);
+                Hist16{hist_words + r * (kHistBins / 2)}.add(static_cast<int>(key >> kHistShift));
               }
             }
           }
+          if (++since_check < check_every) continue;
+          since_check = 0;
           g.sync();
           // -- compaction of full candidate buffers
 #pragma unroll 1
-          for (int r = 0; r < R; ++r) {
+          for (int rr = 0; rr < RG; ++rr) {
+            const int r = r0 + rr;
             const int n = rs->cnt[r];
-            if (n <= cap - kTileKeys) continue;  // uniform: read after the barrier
-            uint32_t* hr = hist + r * kHistBins;
+            if (n <= cap - margin) continue;  // uniform: read after the barrier
+            const Hist16 hr{hist_words + r * (kHistBins / 2)};
             uint64_t* cr = cand + r * cap;
             uint32_t above = 0;
-            const uint32_t bkt = find_kth_bucket(g, hr, static_cast<uint32_t>(p.k), sc, &above);
-            const uint32_t kept = above + hr[bkt];
+            const uint32_t bkt = find_kth_bucket(g, hr, static_cast<uint32_t>(p.k), gsc, &above);
+            const uint32_t kept = above + hr(static_cast<int>(bkt));
             uint64_t T = static_cast<uint64_t>(bkt) << kHistShift;
-            const bool exact = kept > static_cast<uint32_t>(cap - 2 * kTileKeys);
+            const bool exact = kept > static_cast<uint32_t>(cap - 2 * margin);
             if (exact) {
-              T = select_in_bucket(g, bkt, static_cast<uint32_t>(p.k) - above, sc, [&](auto&& fn) {
+              T = select_in_bucket(g, bkt, static_cast<uint32_t>(p.k) - above, gsc, [&](auto&& fn) {
                 for (int e = g.tid; e < n; e += kEpiThreads) fn(cr[e]);
               });
             }
-            const int left = compact_keep_ge(g, cr, n, T, sc);
-            for (int b = g.tid; b < static_cast<int>(bkt); b += kEpiThreads) hr[b] = 0;
+            const int left = compact_keep_ge(g, cr, n, T, gsc);
+            // buckets below bkt are empty now
+            for (int wd = g.tid; wd < static_cast<int>(bkt >> 1); wd += kEpiThreads) hr.w[wd] = 0;
             g.sync();
             if (g.tid == 0) {
-              if (exact) hr[bkt] = static_cast<uint32_t>(p.k) - above;
+              if (bkt & 1u) hr.set(static_cast<int>(bkt) - 1, 0);
+              if (exact) hr.set(static_cast<int>(bkt), static_cast<uint32_t>(p.k) - above);
               rs->cnt[r] = left;
               rs->thr[r] = T;
             }
@@ -648,25 +702,26 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
         }
       }
       if constexpr (MODE == kModeTopk) {
-        // -- flush the exact top-k of each row of this segment
+        // -- flush the exact top-k of each of this group's rows
         const int slot = seg == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + item;
 #pragma unroll 1
-        for (int r = 0; r < R; ++r) {
+        for (int rr = 0; rr < RG; ++rr) {
+          const int r = r0 + rr;
           g.sync();
           const int n = rs->cnt[r];
-          uint32_t* hr = hist + r * kHistBins;
+          const Hist16 hr{hist_words + r * (kHistBins / 2)};
           uint64_t* cr = cand + r * cap;
           uint64_t T = 0;
           if (n > p.k) {
             uint32_t above = 0;
-            const uint32_t bkt = find_kth_bucket(g, hr, static_cast<uint32_t>(p.k), sc, &above);
-            T = select_in_bucket(g, bkt, static_cast<uint32_t>(p.k) - above, sc, [&](auto&& fn) {
+            const uint32_t bkt = find_kth_bucket(g, hr, static_cast<uint32_t>(p.k), gsc, &above);
+            T = select_in_bucket(g, bkt, static_cast<uint32_t>(p.k) - above, gsc, [&](auto&& fn) {
               for (int e = g.tid; e < n; e += kEpiThreads) fn(cr[e]);
             });
           }
           const int64_t part = static_cast<int64_t>(slot) * R + r;
           uint64_t* out = p.part_keys + part * p.k;
-          if (g.tid == 0) sc->bcast[3] = 0;
+          if (g.tid == 0) gsc->bcast[3] = 0;
           g.sync();
           for (int base = 0; base < n; base += kEpiThreads) {
             const int e = base + g.tid;
@@ -676,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
             if (m) {
               const int leader = __ffs(m) - 1;
               uint32_t dst = 0;
-              if (lane == leader) dst = atomicAdd(&sc->bcast[3], static_cast<uint32_t>(__popc(m)));
+              if (lane == leader) dst = atomicAdd(&gsc->bcast[3], static_cast<uint32_t>(__popc(m)));
               dst = __shfl_sync(0xffffffffu, dst, leader);
               const uint32_t o = dst + __popc(m & ((1u << lane) - 1u));
               if (keep && o < static_cast<uint32_t>(p.k)) out[o] = key;
@@ -684,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
           }
           g.sync();
           if (g.tid == 0) {
-            const int32_t wrote = static_cast<int32_t>(min(sc->bcast[3], static_cast<uint32_t>(p.k)));
+            const int32_t wrote = static_cast<int32_t>(min(gsc->bcast[3], static_cast<uint32_t>(p.k)));
             p.part_count[part] = rs->valid[r] ? wrote : 0;
           }
         }
@@ -711,7 +766,7 @@ cudaError_t launch_score_t(const ScoreParams& p, dim3 grid, cudaStream_t stream)
   auto kern = score_kernel<H, R, FMT, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, bytes, stream>>>(p);
+  kern<<<grid, L::kThreads, bytes, stream>>>(p);
   return cudaGetLastError();
 }
 

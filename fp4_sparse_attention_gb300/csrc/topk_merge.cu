@@ -5,22 +5,29 @@
 // top-k of the keys it scored.  The union of those lists therefore holds the
 // row's global top-k; this kernel selects it exactly (bucket histogram, then
 // radix passes inside the bucket of the k-th key) and writes logical
-// positions, values and the valid count.  One CTA per query row.
+// positions, values and the valid count.  One CTA per query row.  The row's
+// partial lists are read with one warp per list and, when the union fits,
+// copied into shared memory so that every later pass runs from there.
 #include "score_kernel.cuh"
 
 namespace fp4idx {
 namespace {
 
 constexpr int kMergeThreads = 512;
-constexpr int kMergeBuf = 8192;  // keys of the k-th key's bucket held in shared memory
+constexpr int kMergeWarps = kMergeThreads / 32;
+constexpr int kMergeLocal = 20480;  // candidate keys held in shared memory
+constexpr int kMaxSlots = 1024;     // partial lists of one row (<= score CTAs + 1)
 
 struct MergeSmem {
   uint32_t hist[kHistBins];
   int32_t scan[kMergeThreads];
+  int32_t slot_cnt[kMaxSlots];
+  int32_t slot_off[kMaxSlots + 1];
+  int64_t slot_part[kMaxSlots];
   SelectScratch sc;
   int32_t info[8];
   uint64_t out[2048];
-  uint64_t buf[kMergeBuf];
+  uint64_t buf[kMergeLocal];
 };
 
 // Tiles of all items before `item` and of all items (cooperative).
@@ -56,10 +63,10 @@ __device__ void item_prefix(const ScoreParams& p, int rows_per_cta, int tid, int
 __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const __grid_constant__ MergeParams mp) {
   const ScoreParams& p = mp.sp;
   extern __shared__ uint8_t smem_raw[];
-  MergeSmem* sm = reinterpret_cast<MergeSmem*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
+  MergeSmem* sm = reinterpret_cast<MergeSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
   const int tid = threadIdx.x;
   const int lane = tid & 31;
+  const int warp = tid >> 5;
   const int t = blockIdx.x;
   const int k = p.k;
   const int R = mp.rows_per_cta;
@@ -84,62 +91,90 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const __grid_
   const int C = p.score_ctas;
   const int32_t chunk = total > 0 ? (total + C - 1) / C : 1;
   const int c_lo = tiles > 0 ? P / chunk : 0;
-  const int c_hi = tiles > 0 ? (P + tiles - 1) / chunk : -1;
-  auto slot_of = [&](int c) -> int64_t {
-    const int s = static_cast<int64_t>(c) * chunk >= P ? c : C + item;
-    return static_cast<int64_t>(s) * R + r;
-  };
-  auto for_each_key = [&](auto&& fn) {
-    for (int c = c_lo; c <= c_hi; ++c) {
-      const int64_t part = slot_of(c);
-      const int n = __ldg(p.part_count + part);
-      const uint64_t* keys = p.part_keys + part * k;
-      for (int e = tid; e < n; e += kMergeThreads) fn(__ldg(keys + e));
-    }
-  };
+  const int nslots = tiles > 0 ? min((P + tiles - 1) / chunk - c_lo + 1, kMaxSlots) : 0;
 
-  // pass 1: bucket histogram of every candidate
+  // partial lists of this row: count and global offset of each
+  for (int i = tid; i < nslots; i += kMergeThreads) {
+    const int c = c_lo + i;
+    const int s = static_cast<int64_t>(c) * chunk >= P ? c : C + item;
+    const int64_t part = static_cast<int64_t>(s) * R + r;
+    sm->slot_part[i] = part;
+    sm->slot_cnt[i] = min(max(__ldg(p.part_count + part), 0), k);
+  }
   g.sync();
-  for_each_key([&](uint64_t key) { atomicAdd(&sm->hist[key >> kHistShift], 1u); });
+  if (tid == 0) {
+    int32_t acc = 0;
+    for (int i = 0; i < nslots; ++i) {
+      sm->slot_off[i] = acc;
+      acc += sm->slot_cnt[i];
+    }
+    sm->slot_off[nslots] = acc;
+  }
   g.sync();
-  int M = 0;
-  for (int c = c_lo; c <= c_hi; ++c) M += __ldg(p.part_count + slot_of(c));
+  const int M = sm->slot_off[nslots];
+  const bool local = M <= kMergeLocal;
   const int n_out = M < k ? M : k;
 
+  // visit every candidate in global memory: one warp per list
+  auto for_each_global = [&](auto&& fn) {
+    for (int i = warp; i < nslots; i += kMergeWarps) {
+      const uint64_t* keys = p.part_keys + sm->slot_part[i] * k;
+      const int n = sm->slot_cnt[i];
+      const int off = sm->slot_off[i];
+      for (int e = lane; e < n; e += 32) fn(__ldg(keys + e), off + e);
+    }
+  };
+  // pass 1: bucket histogram (and the copy into shared memory when it fits)
+  for_each_global([&](uint64_t key, int at) {
+    atomicAdd(&sm->hist[key >> kHistShift], 1u);
+    if (local) sm->buf[at] = key;
+  });
+  g.sync();
+
+  auto hist_get = [&](int bin) { return sm->hist[bin]; };
   uint64_t T = 0;
   if (M > k) {
     uint32_t above = 0;
-    const uint32_t bkt = find_kth_bucket(g, sm->hist, static_cast<uint32_t>(k), &sm->sc, &above);
-    const uint32_t nb = sm->hist[bkt];
+    const uint32_t bkt = find_kth_bucket(g, hist_get, static_cast<uint32_t>(k), &sm->sc, &above);
     const uint32_t rank = static_cast<uint32_t>(k) - above;
-    if (nb <= static_cast<uint32_t>(kMergeBuf)) {
+    if (local) {
+      T = select_in_bucket(g, bkt, rank, &sm->sc, [&](auto&& fn) {
+        for (int e = tid; e < M; e += kMergeThreads) fn(sm->buf[e]);
+      });
+    } else if (sm->hist[bkt] <= static_cast<uint32_t>(kMergeLocal)) {
       if (tid == 0) sm->info[2] = 0;
       g.sync();
-      for_each_key([&](uint64_t key) {
+      for_each_global([&](uint64_t key, int) {
         if ((key >> kHistShift) == bkt) {
           const uint32_t o = atomicAdd(reinterpret_cast<uint32_t*>(&sm->info[2]), 1u);
-          if (o < static_cast<uint32_t>(kMergeBuf)) sm->buf[o] = key;
+          if (o < static_cast<uint32_t>(kMergeLocal)) sm->buf[o] = key;
         }
       });
       g.sync();
-      const int nbuf = min(sm->info[2], kMergeBuf);
+      const int nbuf = min(sm->info[2], kMergeLocal);
       T = select_in_bucket(g, bkt, rank, &sm->sc, [&](auto&& fn) {
         for (int e = tid; e < nbuf; e += kMergeThreads) fn(sm->buf[e]);
       });
     } else {
-      T = select_in_bucket(g, bkt, rank, &sm->sc, for_each_key);
+      T = select_in_bucket(g, bkt, rank, &sm->sc,
+                           [&](auto&& fn) { for_each_global([&](uint64_t key, int) { fn(key); }); });
     }
   }
 
   // gather the selected keys
   if (tid == 0) sm->info[3] = 0;
   g.sync();
-  for_each_key([&](uint64_t key) {
+  auto keep = [&](uint64_t key) {
     if (key >= T) {
       const uint32_t o = atomicAdd(reinterpret_cast<uint32_t*>(&sm->info[3]), 1u);
       if (o < 2048u) sm->out[o] = key;
     }
-  });
+  };
+  if (local) {
+    for (int e = tid; e < M; e += kMergeThreads) keep(sm->buf[e]);
+  } else {
+    for_each_global([&](uint64_t key, int) { keep(key); });
+  }
   g.sync();
 
   if (mp.flags & 1u) {
@@ -173,7 +208,6 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const __grid_
     if (mp.values) mp.values[row + j] = have ? key_value(key) : -INFINITY;
   }
   if (tid == 0 && mp.valid_count) mp.valid_count[t] = n_out;
-  (void)lane;
 }
 
 }  // namespace

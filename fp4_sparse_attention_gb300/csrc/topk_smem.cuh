@@ -19,16 +19,20 @@ constexpr int kHistBins = 2048;
 constexpr int kHistShift = 53;  // bucket = key >> 53 (sign, exponent, 2 mantissa bits)
 
 // Group of kThreads threads (a multiple of 32, <= 1024) that synchronise
-// with a named barrier.
+// with a named barrier: barrier 0 is __syncthreads, kBarrierId < 0 takes the
+// barrier id from `bar` at run time.
 template <int kThreads, int kBarrierId>
 struct Group {
   static_assert(kThreads % 32 == 0, "whole warps");
   int tid;  // 0 .. kThreads-1
+  int bar = kBarrierId;
   __device__ __forceinline__ void sync() const {
     if constexpr (kBarrierId == 0)
       __syncthreads();
-    else
+    else if constexpr (kBarrierId > 0)
       asm volatile("bar.sync %0, %1;" ::"n"(kBarrierId), "n"(kThreads) : "memory");
+    else
+      asm volatile("bar.sync %0, %1;" ::"r"(bar), "n"(kThreads) : "memory");
   }
 };
 
@@ -66,18 +70,31 @@ __device__ __forceinline__ uint32_t group_excl_suffix(const Group<kThreads, kBar
   return after + incl - v;
 }
 
-// Bucket of the k-th largest key given a bucket histogram (k >= 1 and
-// total >= k).  Returns the bucket and writes the count of keys in higher
-// buckets to *above.  Every thread of the group gets the same answer.
-template <int kThreads, int kBarrierId>
-__device__ uint32_t find_kth_bucket(const Group<kThreads, kBarrierId>& g, const uint32_t* hist,
+// Bucket histogram with 16-bit counters, two per 32-bit word (a row's
+// candidate buffer never holds 65,536 keys).
+struct Hist16 {
+  uint32_t* w;  // kHistBins / 2 words
+  __device__ __forceinline__ uint32_t operator()(int b) const { return (w[b >> 1] >> ((b & 1) * 16)) & 0xFFFFu; }
+  __device__ __forceinline__ void add(int b) const { atomicAdd(&w[b >> 1], 1u << ((b & 1) * 16)); }
+  // Single thread: overwrite one counter.
+  __device__ __forceinline__ void set(int b, uint32_t v) const {
+    const int sh = (b & 1) * 16;
+    w[b >> 1] = (w[b >> 1] & ~(0xFFFFu << sh)) | (v << sh);
+  }
+};
+
+// Bucket of the k-th largest key given a bucket histogram hist(b) (k >= 1
+// and total >= k).  Returns the bucket and writes the count of keys in
+// higher buckets to *above.  Every thread of the group gets the same answer.
+template <int kThreads, int kBarrierId, class HistGet>
+__device__ uint32_t find_kth_bucket(const Group<kThreads, kBarrierId>& g, const HistGet& hist,
                                     uint32_t k, SelectScratch* sc, uint32_t* above) {
   constexpr int kPer = kHistBins / kThreads;
   static_assert(kHistBins % kThreads == 0, "bins per thread");
   const int b0 = g.tid * kPer;
   uint32_t s = 0;
 #pragma unroll 4
-  for (int i = 0; i < kPer; ++i) s += hist[b0 + i];
+  for (int i = 0; i < kPer; ++i) s += hist(b0 + i);
   if (g.tid == 0) {  // answer when fewer than k keys exist: keep everything
     sc->bcast[0] = 0;
     sc->bcast[1] = 0;
@@ -87,7 +104,7 @@ __device__ uint32_t find_kth_bucket(const Group<kThreads, kBarrierId>& g, const 
   if (after < k && after + s >= k) {
     uint32_t acc = after;
     for (int i = kPer - 1; i >= 0; --i) {
-      uint32_t h = hist[b0 + i];
+      uint32_t h = hist(b0 + i);
       if (acc + h >= k) {
         sc->bcast[0] = static_cast<uint32_t>(b0 + i);
         sc->bcast[1] = acc;
