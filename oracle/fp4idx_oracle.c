@@ -277,8 +277,12 @@ void orc_topk(const orc_problem* p, const float* w, int64_t w_row_stride, int32_
       all[s].value = logit_one(p, w, w_row_stride, t, s, vis, NULL, NULL);
       all[s].index = s;
     }
-    qsort(all, (size_t)vis, sizeof(scored_pos), cmp_scored);
-    int64_t n = vis < k ? vis : k;
+    /* A NaN logit has no place in the order: such positions are not selected. */
+    int64_t m = 0;
+    for (int64_t s = 0; s < vis; ++s)
+      if (!isnan(all[s].value)) all[m++] = all[s];
+    qsort(all, (size_t)m, sizeof(scored_pos), cmp_scored);
+    int64_t n = m < k ? m : k;
     for (int64_t j = 0; j < k; ++j) {
       idx[(int64_t)i * k + j] = j < n ? (int32_t)all[j].index : -1;
       if (val) val[(int64_t)i * k + j] = j < n ? all[j].value : -INFINITY;

@@ -23,7 +23,8 @@
  *   - block score = max over visible keys of a 128-key block of dot, -inf when
  *     the block has none (M3-indexer README, "数学语义" / "输出 shape 和类型").
  *   - top-k = full sort of the visible positions by (value desc, index asc),
- *     first k kept, -1 padded.
+ *     first k kept, -1 padded; a position whose logit is NaN has no rank and
+ *     is not selected.
  *
  * Parity pins: see tests/test_oracle_pins.py (exhaustive decodes, closed forms,
  * library-routine cross-checks, brute-force top-k, invariants).
@@ -93,7 +94,8 @@ void orc_block_scores(const orc_problem* p, int32_t ktiles, const int32_t* rows,
                       float* out, double* bound, uint8_t* safe);
 
 /* Top-k for the listed rows: idx[i*k+j] (-1 padded), val[i*k+j] (-inf padded,
- * nullable), count[i] = min(k, vis) (nullable). */
+ * nullable), count[i] = min(k, visible positions with a non-NaN logit)
+ * (nullable). */
 void orc_topk(const orc_problem* p, const float* w, int64_t w_row_stride, int32_t k,
               const int32_t* rows, int32_t nrows, int32_t* idx, float* val, int32_t* count);
 
