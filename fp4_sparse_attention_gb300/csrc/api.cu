@@ -214,17 +214,22 @@ int topk_ctas(const fp4idx_problem_t* p, int sms) {
 }
 
 struct TopkWorkspace {
-  size_t keys_off, count_off, bytes;
+  size_t keys_off, count_off, cand_off, bytes;
 };
 
+// Workspace of the top-k path: per-CTA partial lists, their counts, and each
+// scorer CTA's per-row streaming candidate buffers.
 TopkWorkspace topk_workspace(const fp4idx_problem_t* p, int32_t k, int sms) {
   const int R = score_rows_per_cta(p->num_heads);
+  const int ctas = topk_ctas(p, sms);
   const int64_t items = static_cast<int64_t>(p->num_seqs) * ((p->max_seqlen_q + R - 1) / R);
-  const int64_t slots = (topk_ctas(p, sms) + items) * R;
+  const int64_t slots = (ctas + items) * R;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   TopkWorkspace ws;
   ws.keys_off = 0;
-  ws.count_off = (static_cast<size_t>(slots) * k * 8 + 255) / 256 * 256;
-  ws.bytes = ws.count_off + (static_cast<size_t>(slots) * 4 + 255) / 256 * 256;
+  ws.count_off = up(static_cast<size_t>(slots) * k * 8);
+  ws.cand_off = ws.count_off + up(static_cast<size_t>(slots) * 4);
+  ws.bytes = ws.cand_off + up(static_cast<size_t>(ctas) * R * topk_capacity(k) * 8);
   return ws;
 }
 
@@ -319,6 +324,7 @@ fp4idx_status_t topk_prepare(const fp4idx_problem_t* problem, const float* w, in
   sp->k = k;
   sp->part_keys = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(workspace) + ws.keys_off);
   sp->part_count = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + ws.count_off);
+  sp->cand = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(workspace) + ws.cand_off);
   *ctas = topk_ctas(problem, dev->sms);
   sp->score_ctas = *ctas;
   return FP4IDX_OK;

@@ -50,6 +50,7 @@ struct ScoreParams {
   int32_t k;
   uint64_t* part_keys;      // [slots * R][k]
   int32_t* part_count;      // [slots * R]
+  uint64_t* cand;           // [score_ctas * R][candidate capacity] streaming candidate buffers
   uint32_t* err;
 };
 
@@ -76,6 +77,12 @@ cudaError_t launch_topk_merge(const MergeParams& p, int rows, cudaStream_t strea
 
 // Sets the message fp4idx_last_error_message() returns on this thread.
 void set_last_error(const char* fmt, ...);
+
+// Keys a streaming top-k candidate buffer holds per row: at least twice k
+// (rounded to whole tiles), at least 1,024.
+__host__ __device__ constexpr int topk_capacity(int k) {
+  return 2 * ((k + 127) / 128) * 128 < 1024 ? 1024 : 2 * ((k + 127) / 128) * 128;
+}
 
 // Query rows per scorer CTA for a head count (the MMA N is rows * heads).
 inline int score_rows_per_cta(int heads) { return heads >= 64 ? 2 : 4; }

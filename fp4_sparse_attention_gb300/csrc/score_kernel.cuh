@@ -9,10 +9,11 @@
 // R rows x H heads of one request on N (TMEM columns).  The head sum then is
 // a serial loop inside one thread: thread = key, no shuffles.
 //
-// Warp roles (64 + 128*R threads):
-//   warp 0    producer: resolves pages through the block table, issues the
-//             TMA gather of K codes (64-byte swizzle) and the bulk copy of K
-//             scales into a kStages-deep shared-memory ring; loads Q per item.
+// Warp roles (96 + 128*R threads):
+//   warp 0 and the last warp: producers, each owning alternate tiles:
+//             resolve pages through the block table, issue the TMA gather of
+//             K codes (64-byte swizzle) and the bulk copy of K scales into a
+//             kStages-deep shared-memory ring; warp 0 also loads Q per item.
 //   warp 1    MMA: owns the TMEM allocation, rewrites K / Q scales into the
 //             32x4x4 scale-factor atom, copies them to TMEM (tcgen05.cp) and
 //             issues two K=64 MMAs per tile into a double-buffered accumulator.
@@ -38,6 +39,7 @@ namespace fp4idx {
 
 constexpr int kEpiThreads = 128;  // one epilogue group: four warps, one per TMEM lane quadrant
 constexpr uint32_t kTmemCols = 512;
+constexpr int kAccBufs = 3;  // accumulator buffers: the MMA may run two tiles ahead of the epilogue
 
 template <int FMT>
 struct FmtTraits;
@@ -72,16 +74,17 @@ struct RowState {  // epilogue view of the current item's rows
   uint64_t thr[R];  // inclusive acceptance threshold of each candidate buffer
 };
 
-__host__ __device__ constexpr int topk_capacity(int k) {
-  return 2 * ((k + 127) / 128) * 128 < 1024 ? 1024 : 2 * ((k + 127) / 128) * 128;
-}
 
 template <int H, int R, int FMT, int MODE>
 struct ScoreLayout {
-  // K-tile ring depth: deeper for logits, where shared memory holds no candidates.
-  static constexpr int kStages = MODE == kModeTopk ? 6 : 8;
+  // K-tile ring depth.  A loaded HBM round trip for a random page is ~2 us,
+  // so ~100+ KB must be in flight per SM; the ring takes most of shared memory.
+  static constexpr int kStages = 20;
   static constexpr int kGroups = R;  // epilogue groups, one query row each
-  static constexpr int kThreads = 64 + kEpiThreads * kGroups;
+  // warp 0 and the last warp: producers (alternate tiles); warp 1: MMA
+  static constexpr int kProducer2Warp = 2 + 4 * kGroups;
+  static constexpr int kThreads = 96 + kEpiThreads * kGroups;
+  static_assert(kStages % 2 == 0, "the two producers own alternate stages");
   static constexpr int N = H * R;
   static_assert(N % 16 == 0 && N >= 16 && N <= 128, "MMA N");
   static constexpr int G = FmtTraits<FMT>::G;
@@ -89,26 +92,28 @@ struct ScoreLayout {
   static constexpr uint32_t kCodes = 0;                                  // kStages x 8 KB
   static constexpr uint32_t kQ = kCodes + kStages * 8192;                // N x 64 B
   static constexpr uint32_t kQBytes = ((N * 64 + 1023) / 1024) * 1024;
-  static constexpr uint32_t kRawSf = kQ + kQBytes;                       // kStages x 128*G
-  static constexpr uint32_t kSfa = kRawSf + kStages * 128 * G;           // kStages x kAtoms x 512
+  static constexpr uint32_t kSfa = kQ + kQBytes;                         // kStages x kAtoms x 512
   static constexpr uint32_t kSfb = kSfa + kStages * kAtoms * 512;        // kAtoms x 512
   static constexpr uint32_t kBars = kSfb + kAtoms * 512;                 // mbarriers
-  static constexpr int kNumBars = 2 * kStages + 6;
+  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 2;
   static constexpr uint32_t kState = kBars + kNumBars * 8;
   static constexpr uint32_t kRows = (kState + sizeof(CtaState) + 15) / 16 * 16;
   static constexpr uint32_t kW = (kRows + sizeof(RowState<R>) + 15) / 16 * 16;  // N floats
   static constexpr uint32_t kScan = kW + N * 4;                                  // kThreads ints
   static constexpr uint32_t kScratch = kScan + kThreads * 4;                      // per group
   static constexpr uint32_t kHist = (kScratch + kGroups * sizeof(SelectScratch) + 15) / 16 * 16;
-  static constexpr uint32_t kCand = kHist + (MODE == kModeTopk ? R * kHistBins * 2 : 0);
-  static constexpr uint32_t bytes(int cap) {
-    return kCand + (MODE == kModeTopk ? static_cast<uint32_t>(R) * cap * 8 : 0) + 1024;
-  }
+  static constexpr uint32_t kEnd = kHist + (MODE == kModeTopk ? R * kHistBins * 2 : 0);
+  static constexpr uint32_t bytes() { return kEnd + 1024; }
   // TMEM columns
-  static constexpr uint32_t kAccCol = 0;    // two accumulators of 128 columns
-  static constexpr uint32_t kSfbCol = 256;  // two Q-scale slots of 8 columns
-  static constexpr uint32_t kSfaCol = 272;  // kStages K-scale slots of 8 columns (<= 64)
-  static_assert(kSfaCol + 8 * kStages <= kTmemCols, "TMEM columns");
+  static constexpr uint32_t kAccCol = 0;                  // kAccBufs accumulators of 128 columns
+  static constexpr uint32_t kSfbCol = 128 * kAccBufs;     // two Q-scale slots of 8 columns
+  static constexpr uint32_t kSfaCol = kSfbCol + 16;       // kSfaSlots K-scale slots of 8 columns
+  // K-scale TMEM slot of tile i is i % kSfaSlots; its previous reader, the MMA
+  // of tile i - kSfaSlots, has completed once the accumulator of tile i-1 was
+  // free (kAccBufs < kSfaSlots), which precedes the copy into the slot.
+  static constexpr int kSfaSlots = 4;
+  static_assert(kAccBufs < kSfaSlots, "scale slot reuse");
+  static_assert(kSfaCol + 8 * kSfaSlots <= kTmemCols, "TMEM columns");
 };
 
 // ---------------------------------------------------------------------------
@@ -277,8 +282,35 @@ __device__ __forceinline__ void q_scale_atoms(const ScoreParams& p, const ItemIn
     *reinterpret_cast<uint4*>(atoms + 512 + lane * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
 }
 
-// sum_h w[h] * max(v[h], 0), NaN propagating, with packed fp32x2 FMAs in
-// four independent chains.
+// sum_h w[h] * max(v[h], 0) with packed fp32x2 FMAs in four independent
+// chains, given hw2[i] = (w[2i]/2, w[2i+1]/2).  The ReLU is taken as
+// x + |x| = 2*max(x, 0) (one add with an absolute-value operand, on the FMA
+// pipe): (w/2)*(x+|x|) is exactly w*max(x,0), so every FMA rounds the same
+// value as w*max(x,0) would; NaN stays NaN.
+template <int H>
+__device__ __forceinline__ float weighted_relu_reg(const uint32_t (&v)[H], const float2 (&hw2)[H / 2]) {
+  constexpr int kChains = H >= 16 ? 4 : 2;
+  float2 acc[kChains];
+#pragma unroll
+  for (int c = 0; c < kChains; ++c) acc[c] = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int i = 0; i < H / 2; ++i) {
+    const float a = __uint_as_float(v[2 * i]), b = __uint_as_float(v[2 * i + 1]);
+    const float2 x = __fadd2_rn(make_float2(a, b), make_float2(fabsf(a), fabsf(b)));
+    acc[i % kChains] = __ffma2_rn(hw2[i], x, acc[i % kChains]);
+  }
+#pragma unroll
+  for (int c = 1; c < kChains; ++c) acc[0] = __fadd2_rn(acc[0], acc[c]);
+  return acc[0].x + acc[0].y;
+}
+
+// Order-preserving 32-bit image of a logit (-0 folded into +0); the high
+// half of topk_key().
+__device__ __forceinline__ uint32_t ordered_bits(float v) {
+  const uint32_t u = __float_as_uint(v + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 template <int H>
 __device__ __forceinline__ float weighted_relu(const uint32_t* v, const float* w) {
   constexpr int kChains = H >= 16 ? 4 : 2;
@@ -345,7 +377,7 @@ __device__ int compact_keep_ge(const G& g, uint64_t* cand, int n, uint64_t T, Se
 // The kernel.
 // ---------------------------------------------------------------------------
 template <int H, int R, int FMT, int MODE>
-__global__ void __launch_bounds__(64 + kEpiThreads * R, 1) score_kernel(const __grid_constant__ ScoreParams p) {
+__global__ void __launch_bounds__(96 + kEpiThreads * R, 1) score_kernel(const __grid_constant__ ScoreParams p) {
   using L = ScoreLayout<H, R, FMT, MODE>;
   constexpr int kThreads = L::kThreads;
   using F = FmtTraits<FMT>;
@@ -363,9 +395,9 @@ __global__ void __launch_bounds__(64 + kEpiThreads * R, 1) score_kernel(const __
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
   auto accf_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
-  auto acce_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
-  const uint32_t qfull_bar = bar0 + 8u * (2 * kStages + 4);
-  const uint32_t qempty_bar = bar0 + 8u * (2 * kStages + 5);
+  auto acce_bar = [&](int a) { return bar0 + 8u * (2 * kStages + kAccBufs + a); };
+  const uint32_t qfull_bar = bar0 + 8u * (2 * kStages + 2 * kAccBufs);
+  const uint32_t qempty_bar = bar0 + 8u * (2 * kStages + 2 * kAccBufs + 1);
 
   CtaState* st = reinterpret_cast<CtaState*>(smem + L::kState);
   RowState<R>* rs = reinterpret_cast<RowState<R>*>(smem + L::kRows);
@@ -373,7 +405,6 @@ __global__ void __launch_bounds__(64 + kEpiThreads * R, 1) score_kernel(const __
   int32_t* scan = reinterpret_cast<int32_t*>(smem + L::kScan);
   SelectScratch* sc = reinterpret_cast<SelectScratch*>(smem + L::kScratch);
   uint32_t* hist_words = reinterpret_cast<uint32_t*>(smem + L::kHist);
-  uint64_t* cand = reinterpret_cast<uint64_t*>(smem + L::kCand);
   const int cap = topk_capacity(p.k);
   volatile int* abort_flag = &st->abort;
 
@@ -397,10 +428,10 @@ __global__ void __launch_bounds__(64 + kEpiThreads * R, 1) score_kernel(const __
   // ---- one-time setup
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), 1 + 32);  // producer's expect-tx arrive + one cp.async arrive per lane
       mbar_init(empty_bar(s), 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < kAccBufs; ++a) {
       mbar_init(accf_bar(a), 1);
       mbar_init(acce_bar(a), L::kGroups * kEpiThreads);
     }
@@ -416,16 +447,17 @@ __global__ void __launch_bounds__(64 + kEpiThreads * R, 1) score_kernel(const __
 
   const uint32_t codes_s = smem_u32(smem + L::kCodes);
   const uint32_t q_s = smem_u32(smem + L::kQ);
-  uint8_t* rawsf = smem + L::kRawSf;
   uint8_t* sfa_atoms = smem + L::kSfa;
   uint8_t* sfb_atoms = smem + L::kSfb;
 
-  if (warp == 0) {
-    // ================================================================ producer
-    // The whole warp walks the tiles.  Lane l caches the physical id of
-    // logical page base+l (and of the next 32, prefetched); for each tile the
-    // lanes sl < slots pick up the id of page sl and issue that page's code
-    // and scale copies together, one warp instruction per copy type.
+  if (warp == 0 || warp == L::kProducer2Warp) {
+    // ================================================================ producers
+    // Each producer warp walks every tile and issues the even (warp 0) or odd
+    // (last warp) ones.  Lane l caches the physical id of logical page base+l
+    // (and of the next 32, prefetched); for each tile the lanes sl < slots
+    // pick up the id of page sl and issue that page's code and scale copies
+    // together, one warp instruction per copy type.
+    const uint32_t pidx = warp == 0 ? 0u : 1u;
     uint32_t tile_iter = 0, item_iter = 0;
     bool ok = true;
     const int page = p.page_size;
@@ -433,15 +465,17 @@ __global__ void __launch_bounds__(64 + kEpiThreads * R, 1) score_kernel(const __
     const int slots = kTileKeys >> pshift;  // 2 for 64-key pages, 1 for 128
     if (lane == 0) {
       prefetch_tmap(&p.tmap_k);
-      prefetch_tmap(&p.tmap_q);
+      if (pidx == 0) prefetch_tmap(&p.tmap_q);
     }
     for_each_segment<MODE, R>(p, st, [&](int, const ItemInfo& it, int lo, int hi, int) {
       if (!ok) return;
-      ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(qempty_bar, (item_iter & 1u) ^ 1u, abort_flag, p.err) : false, 0);
-      if (!ok) return;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(qfull_bar, N * kCodeBytes);
-        tma_load_3d(q_s, &p.tmap_q, 0, 0, it.row0, qfull_bar);
+      if (pidx == 0) {
+        ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(qempty_bar, (item_iter & 1u) ^ 1u, abort_flag, p.err) : false, 0);
+        if (!ok) return;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(qfull_bar, N * kCodeBytes);
+          tma_load_3d(q_s, &p.tmap_q, 0, 0, it.row0, qfull_bar);
+        }
       }
       ++item_iter;
       const int32_t npages = (it.k_len + page - 1) >> pshift;
@@ -454,32 +488,50 @@ __global__ void __launch_bounds__(64 + kEpiThreads * R, 1) score_kernel(const __
       int32_t cur_ids = fetch(base), next_ids = fetch(base + 32);
       for (int j = lo; j < hi; ++j) {
         if (MODE == kModeLogits && (j << 7) >= it.k_len) continue;
+        if ((tile_iter & 1u) != pidx) {  // the other producer's tile
+          ++tile_iter;
+          continue;
+        }
         const int32_t lp0 = j * slots;
         if (lp0 >= base + 32) {  // warp-uniform
           base += 32;
           cur_ids = next_ids;
           next_ids = fetch(base + 32);
         }
-        const int32_t phys = __shfl_sync(0xffffffffu, cur_ids, (lp0 - base) + (lane & (slots - 1)));
-        const bool mine = lane < slots;
-        const bool in_req = mine && ((lp0 + lane) << pshift) < it.k_len;
-        const bool valid = in_req && phys >= 0 && phys < p.num_pages;
-        if (in_req && !valid) atomicOr(p.err, kErrPageRange);
-        const uint32_t bytes =
-            static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, valid))) * page * (kCodeBytes + G);
+        // physical page of slot 0 and 1 of this tile (slot 1 only for 64-key pages)
+        const int32_t phys0 = __shfl_sync(0xffffffffu, cur_ids, lp0 - base);
+        const int32_t phys1 = __shfl_sync(0xffffffffu, cur_ids, lp0 - base + (slots - 1));
+        auto page_ok = [&](int sl, int32_t ph_id) {
+          return ((lp0 + sl) << pshift) < it.k_len && ph_id >= 0 && ph_id < p.num_pages;
+        };
+        const bool ok0 = page_ok(0, phys0);
+        const bool ok1 = slots == 2 && page_ok(1, phys1);
+        if (lane < slots && ((lp0 + lane) << pshift) < it.k_len && !(lane == 0 ? ok0 : ok1))
+          atomicOr(p.err, kErrPageRange);
+        const uint32_t bytes = static_cast<uint32_t>((ok0 ? 1 : 0) + (ok1 ? 1 : 0)) * page * kCodeBytes;
         const int s = tile_iter % kStages;
         const uint32_t ph = (tile_iter / kStages) & 1u;
         ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.err) : false, 0);
         if (!ok) return;
         if (lane == 0) mbar_arrive_expect_tx(full_bar(s), bytes);
         __syncwarp();
-        if (valid) {
-          tma_load_2d(codes_s + s * 8192 + ((lane * kCodeBytes) << pshift), &p.tmap_k, 0, phys << pshift,
-                      full_bar(s));
-          bulk_load(smem_u32(rawsf + s * 128 * G + ((lane * G) << pshift)),
-                    p.k_scale + (static_cast<int64_t>(phys) << pshift) * G, page * G, full_bar(s));
+        if (lane < slots && (lane == 0 ? ok0 : ok1))
+          tma_load_2d(codes_s + s * 8192 + ((lane * kCodeBytes) << pshift), &p.tmap_k, 0,
+                      (lane == 0 ? phys0 : phys1) << pshift, full_bar(s));
+        // K scales straight into the scale-factor atom: key m = 32q + lane goes
+        // to atom line `lane`, word q (and the second atom for scales 4..7).
+        uint8_t* atom = sfa_atoms + s * F::kAtoms * 512 + lane * 16;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int m = 32 * q + lane;
+          const int sl = m >> pshift;
+          if (sl == 0 ? ok0 : ok1) {
+            const uint8_t* src = p.k_scale + ((static_cast<int64_t>(sl == 0 ? phys0 : phys1) << pshift) + (m & (page - 1))) * G;
+            cp_async_4(smem_u32(atom + 4 * q), src);
+            if constexpr (G == 8) cp_async_4(smem_u32(atom + 512 + 4 * q), src + 4);
+          }
         }
-        __syncwarp();
+        cp_async_arrive(full_bar(s));
         ++tile_iter;
       }
     });
@@ -487,6 +539,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads * R, 1) score_kernel(const __
       // Let copies already in flight land before the CTA can exit.
       const uint32_t first = tile_iter > static_cast<uint32_t>(kStages) ? tile_iter - kStages : 0;
       for (uint32_t u = first; u < tile_iter; ++u) {
+        if ((u & 1u) != pidx) continue;
         volatile int never = 0;
         mbar_wait(full_bar(u % kStages), (u / kStages) & 1u, &never, p.err);
       }
@@ -494,6 +547,11 @@ __global__ void __launch_bounds__(64 + kEpiThreads * R, 1) score_kernel(const __
     __syncwarp();
   } else if (warp == 1) {
     // ================================================================ MMA issuer
+    // Descriptors of stage 0 / K half 0; other stages and the second K half
+    // only move the 16-byte-unit start address (+32 B = +2).
+    const uint64_t a_desc0 = desc_kmajor_sw64(codes_s);
+    const uint64_t b_desc0 = desc_kmajor_sw64(q_s);
+    const uint64_t sfa_desc0 = desc_sf_atom(smem_u32(sfa_atoms));
     uint32_t tile_iter = 0, item_iter = 0;
     bool ok = true;
     int last_acc = -1;
@@ -514,46 +572,44 @@ __global__ void __launch_bounds__(64 + kEpiThreads * R, 1) score_kernel(const __
           tc_cp_32x128b_warpx4(sfb_t + 4u * a, desc_sf_atom(smem_u32(sfb_atoms + 512 * a)));
       }
       __syncwarp();
-      for (int j = lo; j < hi; ++j) {
-        if (MODE == kModeLogits && static_cast<int64_t>(j) * kTileKeys >= it.k_len) continue;
-        const int s = tile_iter % kStages;
-        const uint32_t ph = (tile_iter / kStages) & 1u;
-        const int a = tile_iter & 1u;
-        const uint32_t aph = (tile_iter >> 1) & 1u;
-        ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(full_bar(s), ph, abort_flag, p.err) : false, 0);
-        if (!ok) return;
-        k_scale_atoms<FMT>(rawsf + s * 128 * G, sfa_atoms + s * F::kAtoms * 512, lane);
-        fence_proxy_async_smem();
-        __syncwarp();
-        ok = __shfl_sync(0xffffffffu,
-                         lane == 0 ? mbar_wait(acce_bar(a), aph ^ 1u, abort_flag, p.err) : false, 0);
-        if (!ok) return;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t sfa_t = tmem + L::kSfaCol + s * 8u;
+      // The tiles: one thread issues everything (no per-tile warp traffic).
+      if (lane == 0) {
+        for (int j = lo; j < hi && ok; ++j) {
+          if (MODE == kModeLogits && static_cast<int64_t>(j) * kTileKeys >= it.k_len) continue;
+          const int s = tile_iter % kStages;
+          const uint32_t ph = (tile_iter / kStages) & 1u;
+          const int a = tile_iter % kAccBufs;
+          const uint32_t aph = (tile_iter / kAccBufs) & 1u;
+          if (!(ok = mbar_wait(full_bar(s), ph, abort_flag, p.err))) break;
+          // The scale atoms were written by cp.async (generic proxy): make
+          // them visible to the tensor core's copy, then move them to TMEM
+          // now (the copy needs no accumulator).
+          const uint32_t sfa_t = tmem + L::kSfaCol + (tile_iter % L::kSfaSlots) * 8u;
+          fence_proxy_async_smem();
 #pragma unroll
           for (int at = 0; at < F::kAtoms; ++at)
-            tc_cp_32x128b_warpx4(sfa_t + 4u * at,
-                                 desc_sf_atom(smem_u32(sfa_atoms + (s * F::kAtoms + at) * 512)));
+            tc_cp_32x128b_warpx4(sfa_t + 4u * at, sfa_desc0 + static_cast<uint64_t>(((s * F::kAtoms + at) * 512) >> 4));
+          if (!(ok = mbar_wait(acce_bar(a), aph ^ 1u, abort_flag, p.err))) break;
+          tc_fence_after();
           const uint32_t d = tmem + L::kAccCol + a * 128u;
+          const uint64_t adesc = a_desc0 + static_cast<uint64_t>((s * 8192) >> 4);
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {
-            const uint64_t adesc = desc_kmajor_sw64(codes_s + s * 8192 + 32 * kk);
-            const uint64_t bdesc = desc_kmajor_sw64(q_s + 32 * kk);
-            const uint32_t sf_id = F::kScaleVec == 2 ? 2u * kk : 0u;
-            const uint32_t idesc = idesc_fp4(128, N, F::kUe8m0, sf_id, sf_id);
+            constexpr uint32_t sf1 = F::kScaleVec == 2 ? 2u : 0u;
+            const uint32_t idesc = kk == 0 ? idesc_fp4(128, N, F::kUe8m0, 0, 0) : idesc_fp4(128, N, F::kUe8m0, sf1, sf1);
             const uint32_t col = F::kScaleVec == 2 ? 0u : 4u * kk;
-            tc_mma_fp4<F::kScaleVec>(d, adesc, bdesc, idesc, sfa_t + col, sfb_t + col,
+            tc_mma_fp4<F::kScaleVec>(d, adesc + 2u * kk, b_desc0 + 2u * kk, idesc, sfa_t + col, sfb_t + col,
                                      static_cast<uint32_t>(kk));
           }
           tc_commit(empty_bar(s));
           tc_commit(accf_bar(a));
+          last_acc = a;
+          last_acc_phase = aph;
+          ++tile_iter;
         }
-        __syncwarp();
-        last_acc = a;
-        last_acc_phase = aph;
-        ++tile_iter;
       }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) return;
       if (lane == 0) tc_commit(qempty_bar);
       __syncwarp();
       ++item_iter;
@@ -566,41 +622,47 @@ __global__ void __launch_bounds__(64 + kEpiThreads * R, 1) score_kernel(const __
     __syncwarp();
   } else {
     // ================================================================ epilogue
-    constexpr int RG = R / L::kGroups;  // rows of one group
-    const int gi = (warp - 2) >> 2;
+    static_assert(L::kGroups == R, "one epilogue group per query row");
+    const int r = (warp - 2) >> 2;  // this group's query row within the item
+    Group<kEpiThreads, -1> g{static_cast<int>(threadIdx.x) - 64 - r * kEpiThreads, 1 + r};
+    SelectScratch* gsc = sc + r;
+    const int quad = warp & 3;
+    const int key_local = quad * 32 + lane;
     // Compaction is checked every `check_every` tiles; the buffer keeps that
     // many tiles of room above the trigger so appends never overflow it.
     const int check_every = max(1, min(4, (cap - p.k) / (2 * kTileKeys)));
     const int margin = check_every * kTileKeys;
     int since_check = 0;
-    Group<kEpiThreads, -1> g{static_cast<int>(threadIdx.x) - 64 - gi * kEpiThreads, 1 + gi};
-    SelectScratch* gsc = sc + gi;
-    const int quad = warp & 3;
-    const int key_local = quad * 32 + lane;
-    const int r0 = gi * RG;
     uint32_t tile_iter = 0;
     bool ok = true;
+    const Hist16 hr{hist_words + r * (kHistBins / 2)};
+    // this row's candidate buffer: global workspace, L2-resident
+    uint64_t* cr = p.cand + (static_cast<int64_t>(blockIdx.x) * R + r) * cap;
+    // Acceptance threshold T of the candidate buffer (key >= T), kept as the
+    // logit value of T and the largest position accepted at that value.
     for_each_segment<MODE, R>(p, st, [&](int item, const ItemInfo& it, int lo, int hi, int seg) {
-      // -- this group's rows of the item
+      // -- this group's row of the item: weights in registers, visibility
+      const bool row_valid = r < it.nrows;
+      const int32_t t = it.row0 + r;
+      const int32_t vis = row_valid ? row_visible(p, it, t) : 0;
+      float2 w2[H / 2];  // half weights, see weighted_relu_reg
+#pragma unroll
+      for (int i = 0; i < H / 2; ++i) {
+        const float* wr = p.w + static_cast<int64_t>(t) * p.w_row_stride + 2 * i;
+        w2[i] = row_valid ? make_float2(0.5f * __ldg(wr), 0.5f * __ldg(wr + 1)) : make_float2(0.0f, 0.0f);
+      }
+      float thr_v = -INFINITY;
+      uint32_t thr_p = 0xFFFFFFFFu;
       g.sync();
-      if (g.tid < RG) {
-        const int r = r0 + g.tid;
-        const bool valid = r < it.nrows;
-        rs->valid[r] = valid ? 1 : 0;
-        rs->vis[r] = valid ? row_visible(p, it, it.row0 + r) : 0;
-        rs->cnt[r] = 0;
-        rs->thr[r] = 0;
-      }
-      for (int e = g.tid; e < RG * H; e += kEpiThreads) {
-        const int r = r0 + e / H, h = e % H;
-        w_s[r * H + h] =
-            r < it.nrows ? __ldg(p.w + static_cast<int64_t>(it.row0 + r) * p.w_row_stride + h) : 0.0f;
-      }
       if constexpr (MODE == kModeTopk) {
-        for (int e = g.tid; e < RG * kHistBins / 2; e += kEpiThreads)
-          hist_words[r0 * (kHistBins / 2) + e] = 0;
+        if (g.tid == 0) {
+          rs->cnt[r] = 0;
+          rs->thr[r] = 0;
+        }
+        for (int e = g.tid; e < kHistBins / 2; e += kEpiThreads) hr.w[e] = 0;
       }
       g.sync();
+      since_check = 0;
       // page id of this thread's key, one tile ahead (validity check off the critical path)
       auto page_of = [&](int j) -> int32_t {
         const int32_t pos = (j << 7) + key_local;
@@ -609,74 +671,57 @@ __global__ void __launch_bounds__(64 + kEpiThreads * R, 1) score_kernel(const __
       int32_t pg_cur = lo < hi ? page_of(lo) : -1;
       for (int j = lo; j < hi; ++j) {
         const int32_t pg_next = j + 1 < hi ? page_of(j + 1) : -1;
-        const int64_t pos = static_cast<int64_t>(j) * kTileKeys + key_local;
-        const bool real = !(MODE == kModeLogits && static_cast<int64_t>(j) * kTileKeys >= it.k_len);
-        float vals[RG];
-#pragma unroll
-        for (int rr = 0; rr < RG; ++rr) vals[rr] = -INFINITY;
+        const int32_t pos = (j << 7) + key_local;
+        const bool real = !(MODE == kModeLogits && (j << 7) >= it.k_len);
+        float val = -INFINITY;
         if (real) {
-          const int a = tile_iter & 1u;
-          const uint32_t aph = (tile_iter >> 1) & 1u;
-          if (ok) ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(accf_bar(a), aph, abort_flag, p.err) : false, 0);
+          const int a = tile_iter % kAccBufs;
+          const uint32_t aph = (tile_iter / kAccBufs) & 1u;
+          // One thread of the group polls the accumulator barrier; the rest
+          // block on the group's named barrier instead of spinning.
+          if (g.tid == 0 && ok && !mbar_wait(accf_bar(a), aph, abort_flag, p.err)) st->abort = 1;
+          g.sync();
+          ok = ok && !*abort_flag;
           if (ok) {
             tc_fence_after();
-            const uint32_t tcol =
-                tmem + (static_cast<uint32_t>(quad * 32) << 16) + L::kAccCol + a * 128u + r0 * H;
-            uint32_t v[RG * H];
-            tmem_ld<RG * H>(tcol, v);
+            uint32_t v[H];
+            tmem_ld<H>(tmem + (static_cast<uint32_t>(quad * 32) << 16) + L::kAccCol + a * 128u + r * H, v);
             tmem_wait_ld();
             reg_fence(v);
-#pragma unroll
-            for (int rr = 0; rr < RG; ++rr) vals[rr] = weighted_relu<H>(v + rr * H, w_s + (r0 + rr) * H);
             tc_fence_before();
             mbar_arrive(acce_bar(a));
+            val = weighted_relu_reg<H>(v, w2);
           }
           ++tile_iter;
         }
-        const bool key_ok = pg_cur >= 0 && pg_cur < p.num_pages;
+        const bool visible = pos < vis && pg_cur >= 0 && pg_cur < p.num_pages;
         pg_cur = pg_next;
         if constexpr (MODE == kModeLogits) {
-          if (ok) {
-#pragma unroll
-            for (int rr = 0; rr < RG; ++rr) {
-              const int r = r0 + rr;
-              if (rs->valid[r] && pos < p.ld) {
-                const bool vis = key_ok && pos < rs->vis[r];
-                p.logits[static_cast<int64_t>(it.row0 + r) * p.ld + pos] = vis ? vals[rr] : -INFINITY;
-              }
-            }
-          }
+          if (ok && row_valid && pos < p.ld)
+            p.logits[static_cast<int64_t>(t) * p.ld + pos] = visible ? val : -INFINITY;
         } else {
-#pragma unroll
-          for (int rr = 0; rr < RG; ++rr) {
-            const int r = r0 + rr;
-            const bool vis = ok && rs->valid[r] && key_ok && pos < rs->vis[r];
-            const uint64_t key = topk_key(vals[rr], static_cast<uint32_t>(pos));
-            const bool take = vis && key >= rs->thr[r];
-            const uint32_t m = __ballot_sync(0xffffffffu, take);
-            if (m) {
-              const int leader = __ffs(m) - 1;
-              int base = 0;
-              if (lane == leader) base = atomicAdd(&rs->cnt[r], __popc(m));
-              base = __shfl_sync(0xffffffffu, base, leader);
-              const int o = base + __popc(m & ((1u << lane) - 1u));
-              if (take && o < cap) {
-                cand[r * cap + o] = key;
-                Hist16{hist_words + r * (kHistBins / 2)}.add(static_cast<int>(key >> kHistShift));
-              }
+          // NaN logits are never selected (every comparison is false).
+          const bool take = ok && visible && (val > thr_v || (val == thr_v && static_cast<uint32_t>(pos) <= thr_p));
+          const uint32_t m = __ballot_sync(0xffffffffu, take);
+          if (m) {
+            const int leader = __ffs(m) - 1;
+            int base = 0;
+            if (lane == leader) base = atomicAdd(&rs->cnt[r], __popc(m));
+            base = __shfl_sync(0xffffffffu, base, leader);
+            const int slot_i = base + __popc(m & ((1u << lane) - 1u));
+            if (take && slot_i < cap) {
+              const uint64_t key = (static_cast<uint64_t>(ordered_bits(val)) << 32) |
+                                   static_cast<uint64_t>(~static_cast<uint32_t>(pos));
+              cr[slot_i] = key;
+              hr.add(static_cast<int>(key >> kHistShift));
             }
           }
           if (++since_check < check_every) continue;
           since_check = 0;
           g.sync();
-          // -- compaction of full candidate buffers
-#pragma unroll 1
-          for (int rr = 0; rr < RG; ++rr) {
-            const int r = r0 + rr;
-            const int n = rs->cnt[r];
-            if (n <= cap - margin) continue;  // uniform: read after the barrier
-            const Hist16 hr{hist_words + r * (kHistBins / 2)};
-            uint64_t* cr = cand + r * cap;
+          // -- compaction of a full candidate buffer
+          const int n = rs->cnt[r];
+          if (n > cap - margin) {  // uniform: read after the barrier
             uint32_t above = 0;
             const uint32_t bkt = find_kth_bucket(g, hr, static_cast<uint32_t>(p.k), gsc, &above);
             const uint32_t kept = above + hr(static_cast<int>(bkt));
@@ -695,53 +740,48 @@ __global__ void __launch_bounds__(64 + kEpiThreads * R, 1) score_kernel(const __
               if (bkt & 1u) hr.set(static_cast<int>(bkt) - 1, 0);
               if (exact) hr.set(static_cast<int>(bkt), static_cast<uint32_t>(p.k) - above);
               rs->cnt[r] = left;
-              rs->thr[r] = T;
             }
+            thr_v = key_value(T);
+            thr_p = ~static_cast<uint32_t>(T);
             g.sync();
           }
         }
       }
       if constexpr (MODE == kModeTopk) {
-        // -- flush the exact top-k of each of this group's rows
+        // -- flush the exact top-k of this group's row
         const int slot = seg == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + item;
-#pragma unroll 1
-        for (int rr = 0; rr < RG; ++rr) {
-          const int r = r0 + rr;
-          g.sync();
-          const int n = rs->cnt[r];
-          const Hist16 hr{hist_words + r * (kHistBins / 2)};
-          uint64_t* cr = cand + r * cap;
-          uint64_t T = 0;
-          if (n > p.k) {
-            uint32_t above = 0;
-            const uint32_t bkt = find_kth_bucket(g, hr, static_cast<uint32_t>(p.k), gsc, &above);
-            T = select_in_bucket(g, bkt, static_cast<uint32_t>(p.k) - above, gsc, [&](auto&& fn) {
-              for (int e = g.tid; e < n; e += kEpiThreads) fn(cr[e]);
-            });
+        g.sync();
+        const int n = rs->cnt[r];
+        uint64_t T = 0;
+        if (n > p.k) {
+          uint32_t above = 0;
+          const uint32_t bkt = find_kth_bucket(g, hr, static_cast<uint32_t>(p.k), gsc, &above);
+          T = select_in_bucket(g, bkt, static_cast<uint32_t>(p.k) - above, gsc, [&](auto&& fn) {
+            for (int e = g.tid; e < n; e += kEpiThreads) fn(cr[e]);
+          });
+        }
+        const int64_t part = static_cast<int64_t>(slot) * R + r;
+        uint64_t* out = p.part_keys + part * p.k;
+        if (g.tid == 0) gsc->bcast[3] = 0;
+        g.sync();
+        for (int base = 0; base < n; base += kEpiThreads) {
+          const int e = base + g.tid;
+          const uint64_t key = e < n ? cr[e] : 0;
+          const bool keep = ok && e < n && key >= T;
+          const uint32_t m = __ballot_sync(0xffffffffu, keep);
+          if (m) {
+            const int leader = __ffs(m) - 1;
+            uint32_t dst = 0;
+            if (lane == leader) dst = atomicAdd(&gsc->bcast[3], static_cast<uint32_t>(__popc(m)));
+            dst = __shfl_sync(0xffffffffu, dst, leader);
+            const uint32_t o = dst + __popc(m & ((1u << lane) - 1u));
+            if (keep && o < static_cast<uint32_t>(p.k)) out[o] = key;
           }
-          const int64_t part = static_cast<int64_t>(slot) * R + r;
-          uint64_t* out = p.part_keys + part * p.k;
-          if (g.tid == 0) gsc->bcast[3] = 0;
-          g.sync();
-          for (int base = 0; base < n; base += kEpiThreads) {
-            const int e = base + g.tid;
-            const uint64_t key = e < n ? cr[e] : 0;
-            const bool keep = ok && e < n && key >= T;
-            const uint32_t m = __ballot_sync(0xffffffffu, keep);
-            if (m) {
-              const int leader = __ffs(m) - 1;
-              uint32_t dst = 0;
-              if (lane == leader) dst = atomicAdd(&gsc->bcast[3], static_cast<uint32_t>(__popc(m)));
-              dst = __shfl_sync(0xffffffffu, dst, leader);
-              const uint32_t o = dst + __popc(m & ((1u << lane) - 1u));
-              if (keep && o < static_cast<uint32_t>(p.k)) out[o] = key;
-            }
-          }
-          g.sync();
-          if (g.tid == 0) {
-            const int32_t wrote = static_cast<int32_t>(min(gsc->bcast[3], static_cast<uint32_t>(p.k)));
-            p.part_count[part] = rs->valid[r] ? wrote : 0;
-          }
+        }
+        g.sync();
+        if (g.tid == 0) {
+          const int32_t wrote = static_cast<int32_t>(min(gsc->bcast[3], static_cast<uint32_t>(p.k)));
+          p.part_count[part] = row_valid ? wrote : 0;
         }
       }
     });
@@ -759,7 +799,7 @@ __global__ void __launch_bounds__(64 + kEpiThreads * R, 1) score_kernel(const __
 template <int H, int R, int FMT, int MODE>
 cudaError_t launch_score_t(const ScoreParams& p, dim3 grid, cudaStream_t stream) {
   using L = ScoreLayout<H, R, FMT, MODE>;
-  const uint32_t want = L::bytes(topk_capacity(p.k));
+  const uint32_t want = L::bytes();
   // At least ~120 KB so that one CTA (and one 512-column TMEM allocation) runs per SM.
   const uint32_t bytes = want < 120u * 1024u ? 120u * 1024u : want;
   if (bytes > 232448u) return cudaErrorInvalidConfiguration;

@@ -163,7 +163,10 @@ fp4idx_status_t fp4idx_block_scores(const fp4idx_problem_t* problem, float* scor
  *                Order: (value desc, index asc) when flags has
  *                FP4IDX_TOPK_SORTED, otherwise unspecified.
  *   values       [T][k] fp32 logits of those positions (-inf padding), or NULL.
- *   valid_count  [T] int32 = min(k, vis(t)), or NULL.
+ *   valid_count  [T] int32 = min(k, vis(t)), or NULL.  (A position whose
+ *                logit is NaN -- only possible with NaN/inf scale codes,
+ *                outside the formats' contract -- has no rank and is never
+ *                selected; it does not count towards vis(t) here.)
  *   workspace    device scratch of at least fp4idx_topk_workspace_bytes();
  *                may be NULL when that size is 0.  Contents need no
  *                initialisation and are meaningless after the call.
@@ -202,9 +205,9 @@ fp4idx_status_t fp4idx_topk_merge(const fp4idx_problem_t* problem, int32_t k, ui
  * for these callers.
  *
  * Results are those of fp4idx_topk (same arguments, minus the workspace).
- * The scratch is a fixed 16 MiB array inside the library's device memory,
+ * The scratch is a fixed 64 MiB array inside the library's device memory,
  * held by every GPU that loads the library until the process exits.  A
- * problem whose fp4idx_topk_workspace_bytes() exceeds 16 MiB is rejected
+ * problem whose fp4idx_topk_workspace_bytes() exceeds 64 MiB is rejected
  * with FP4IDX_EWORKSPACE before anything runs.  The first call on a device
  * looks up the array's device address (with that device current); make that
  * first call before capturing any stream.  All calls on a device share the
