@@ -387,9 +387,65 @@ fp4idx_status_t fp4idx_block_scores(const fp4idx_problem_t* problem, float* scor
   g_msg[0] = 0;
   fp4idx_status_t s = check_problem(problem);
   if (s != FP4IDX_OK) return s;
-  (void)scores;
-  (void)stream;
-  return fail(FP4IDX_EUNSUPPORTED, "block scores are not built yet");
+  if (!scores) return fail(FP4IDX_EINVAL, "scores is NULL");
+  if (!aligned(scores, 4)) return fail(FP4IDX_EINVAL, "scores must be 4-byte aligned");
+  const int g = problem->num_heads / problem->num_kv_heads;
+  if (g > 128 || (g & (g - 1)) != 0)
+    return fail(FP4IDX_EUNSUPPORTED, "num_heads / num_kv_heads = %d: supported powers of two up to 128", g);
+  const int64_t ktiles = (static_cast<int64_t>(problem->max_seqlen_k) + kTileKeys - 1) / kTileKeys;
+  if (problem->num_rows == 0 || ktiles == 0) return FP4IDX_OK;  // nothing to write
+  int group_shift = 0;
+  while ((1 << group_shift) < g) ++group_shift;
+  const int rt_shift = 7 - group_shift;
+  const int64_t row_tiles = (static_cast<int64_t>(problem->max_seqlen_q) + (1 << rt_shift) - 1) >> rt_shift;
+  const int64_t items = static_cast<int64_t>(problem->num_seqs) * problem->num_kv_heads * row_tiles;
+  if (items * ktiles > INT32_MAX) return fail(FP4IDX_EUNSUPPORTED, "more than 2^31 block tiles");
+  DeviceInfo* dev;
+  if ((s = device_info(&dev)) != FP4IDX_OK) return s;
+  BlockParams bp;
+  std::memset(&bp, 0, sizeof(bp));
+  {
+    cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(problem->num_pages) * problem->num_kv_heads * problem->page_size};
+    cuuint64_t strides[1] = {64};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(problem->page_size)};
+    if ((s = make_tmap(&bp.tmap_k, problem->k, 2, dims, strides, box)) != FP4IDX_OK) return s;
+  }
+  {
+    // rows (t) before heads (h) in the box: MMA row m = h_local * RT + t_local
+    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(problem->num_rows), static_cast<cuuint64_t>(problem->num_heads)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(problem->q_row_stride), 64};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(1 << rt_shift), static_cast<cuuint32_t>(g)};
+    if ((s = make_tmap(&bp.tmap_q, problem->q, 3, dims, strides, box)) != FP4IDX_OK) return s;
+  }
+  bp.k_scale = problem->k_scale;
+  bp.q_scale = problem->q_scale;
+  bp.q_scale_row_stride = problem->q_scale_row_stride;
+  bp.cu_seqlens_q = problem->cu_seqlens_q;
+  bp.cu_seqlens_k = problem->cu_seqlens_k;
+  bp.block_table = problem->block_table;
+  bp.page_offsets = problem->page_offsets;
+  bp.table_stride = problem->table_stride;
+  bp.visible_len = problem->visible_len;
+  bp.qo_offset = problem->qo_offset;
+  bp.causal = problem->causal;
+  bp.page_size = problem->page_size;
+  bp.page_shift = problem->page_size == 128 ? 7 : 6;
+  bp.num_pages = problem->num_pages;
+  bp.num_rows = problem->num_rows;
+  bp.num_heads = problem->num_heads;
+  bp.num_kv_heads = problem->num_kv_heads;
+  bp.num_seqs = problem->num_seqs;
+  bp.group_shift = group_shift;
+  bp.rt_shift = rt_shift;
+  bp.row_tiles = static_cast<int32_t>(row_tiles);
+  bp.ktiles = static_cast<int32_t>(ktiles);
+  bp.scores = scores;
+  bp.err = dev->err;
+  const int64_t tiles = items * ktiles;
+  const int ctas = static_cast<int>(tiles < dev->sms ? tiles : dev->sms);
+  cudaError_t e = launch_block_scores(bp, problem->format, dim3(ctas), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "block-score launch");
+  return FP4IDX_OK;
 }
 
 fp4idx_status_t fp4idx_get_error(uint32_t* bits, int32_t clear, void* stream) {

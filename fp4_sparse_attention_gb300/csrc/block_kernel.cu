@@ -1,0 +1,576 @@
+// block_kernel.cu -- per-128-key block max of the unweighted FP4 dot, sm_103a.
+//
+//   scores[h][kb][t] = max over visible s in [128 kb, 128 kb + 128) of q[t,h] . k[s, hk(h)]
+//                      (-inf when the block holds no visible key)
+// (M3-indexer README, "数学语义" and "输出 shape 和类型"; hk(h) = h / (Hq/Hkv)).
+//
+// Queries on the MMA M dimension.  One item = (request b, K head hk, RT query
+// rows).  Its 128 MMA rows are the g = Hq/Hkv query heads of group hk times
+// the RT rows (row m = h_local * RT + t_local), brought in by one 3-D TMA box.
+// A tile is one 128-key block of the item: D[m, n] = Q_real[m] . K_real[128 kb + n]
+// lands in TMEM lane m, column n, so an epilogue thread owns one (head, row)
+// and reduces the block along its 128 columns without shuffles.  Blocks after
+// the last visible key of every row of the item are not computed; their
+// scores are written as -inf.
+//
+// Warp roles (64 + 128 * kGroups threads):
+//   warp 0      producer: Q codes of each item by TMA and Q scales by cp.async
+//               (double buffered, one item ahead); per tile the K codes by TMA
+//               (64-byte swizzle) and the K scales by cp.async straight into the
+//               32x4x4 scale atom, into a kStages-deep ring.
+//   warp 1      MMA: TMEM owner.  Q scales -> TMEM once per item, K scales ->
+//               TMEM per tile, two K = 64 block-scaled MMAs per tile into a
+//               triple-buffered accumulator.
+//   warps 2..   epilogue, kGroups groups of four warps (one per TMEM lane
+//               quadrant) taking alternate tiles: tcgen05.ld of the 128
+//               columns, masked max (NaN-propagating), one fp32 store per
+//               (head, row).
+//
+// Work split: the tiles of all items are concatenated and cut into one equal
+// contiguous chunk per CTA; every output element is produced by exactly one
+// tile, so no cross-CTA combination is needed.
+#include "formats.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+#include "topk_smem.cuh"  // Group
+
+namespace fp4idx {
+namespace {
+
+constexpr int kStages = 12;
+constexpr int kAccBufs = 3;
+constexpr int kKsfSlots = 4;  // K-scale TMEM slots; > kAccBufs (see the MMA loop)
+constexpr int kGroups = 2;
+constexpr int kThreads = 64 + 128 * kGroups;
+constexpr uint32_t kTmemCols = 512;
+static_assert(kAccBufs < kKsfSlots, "K-scale slot reuse");
+
+struct BlockCta {
+  uint32_t tmem_base;
+  int32_t abort;
+  int32_t item0;        // item holding the first tile of this CTA's chunk
+  int32_t item0_start;  // global tile index where item0 starts
+  int32_t total_tiles;
+  int32_t chunk;
+  int32_t pad[2];
+};
+
+template <int FMT>
+struct BlockLayout {
+  using F = FmtTraits<FMT>;
+  static constexpr uint32_t kCodes = 0;                                // kStages x 8 KB K codes
+  static constexpr uint32_t kQ = kCodes + kStages * 8192;              // 2 x 8 KB Q codes
+  static constexpr uint32_t kKsf = kQ + 2 * 8192;                      // kStages x kAtoms x 512
+  static constexpr uint32_t kQsf = kKsf + kStages * F::kAtoms * 512;   // 2 x kAtoms x 512
+  static constexpr uint32_t kBars = kQsf + 2 * F::kAtoms * 512;
+  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 4;
+  static constexpr uint32_t kState = kBars + kNumBars * 8;
+  static constexpr uint32_t kScan = (kState + sizeof(BlockCta) + 15) / 16 * 16;
+  static constexpr uint32_t kEnd = kScan + kThreads * 4;
+  static constexpr uint32_t bytes() { return kEnd + 1024; }  // + alignment slack
+  // TMEM columns
+  static constexpr uint32_t kAccCol = 0;                      // kAccBufs x 128
+  static constexpr uint32_t kQsfCol = 128 * kAccBufs;         // 2 item slots x 8
+  static constexpr uint32_t kKsfCol = kQsfCol + 16;           // kKsfSlots x 8
+  static_assert(kKsfCol + 8 * kKsfSlots <= kTmemCols, "TMEM columns");
+};
+
+// ---------------------------------------------------------------------------
+// Items: i = (b * Hkv + hk) * row_tiles + rt.
+// ---------------------------------------------------------------------------
+struct BlockItem {
+  int32_t b, hk, q0, q_len, row0, nrows, k_len, maxvis, tiles;
+  int64_t table_base;
+};
+
+__device__ __forceinline__ int32_t clamp_vis(int64_t v, int32_t k_len) {
+  return static_cast<int32_t>(v < 0 ? 0 : (v > k_len ? k_len : v));
+}
+
+// Visible key count of row t of the item (rule of the public header).
+__device__ __forceinline__ int32_t row_vis(const BlockParams& p, const BlockItem& it, int32_t t) {
+  if (p.visible_len) return clamp_vis(__ldg(p.visible_len + t), it.k_len);
+  if (p.causal) {
+    const int64_t off = p.qo_offset ? static_cast<int64_t>(__ldg(p.qo_offset + it.b))
+                                    : static_cast<int64_t>(it.k_len) - it.q_len;
+    return clamp_vis(static_cast<int64_t>(t - it.q0) + off + 1, it.k_len);
+  }
+  return it.k_len;
+}
+
+__device__ BlockItem block_item(const BlockParams& p, int32_t i) {
+  BlockItem it;
+  const int per_seq = p.num_kv_heads * p.row_tiles;
+  it.b = i / per_seq;
+  const int rem = i - it.b * per_seq;
+  it.hk = rem / p.row_tiles;
+  const int rt = rem - it.hk * p.row_tiles;
+  it.q0 = __ldg(p.cu_seqlens_q + it.b);
+  it.q_len = __ldg(p.cu_seqlens_q + it.b + 1) - it.q0;
+  it.row0 = it.q0 + (rt << p.rt_shift);
+  const int n = it.q_len - (rt << p.rt_shift);
+  const int RT = 1 << p.rt_shift;
+  it.nrows = n < 0 ? 0 : (n > RT ? RT : n);
+  it.k_len = __ldg(p.cu_seqlens_k + it.b + 1) - __ldg(p.cu_seqlens_k + it.b);
+  if (it.k_len < 0) it.k_len = 0;
+  it.table_base = p.page_offsets ? static_cast<int64_t>(__ldg(p.page_offsets + it.b))
+                                 : static_cast<int64_t>(it.b) * p.table_stride;
+  // Largest visible count over the item's rows: the last row for the causal
+  // rule (visibility grows with the row), every row for explicit lengths.
+  it.maxvis = 0;
+  if (it.nrows > 0) {
+    if (p.visible_len) {
+      for (int r = 0; r < it.nrows; ++r) it.maxvis = max(it.maxvis, row_vis(p, it, it.row0 + r));
+    } else {
+      it.maxvis = row_vis(p, it, it.row0 + it.nrows - 1);
+    }
+  }
+  // At least one tile (computed or not) so that some CTA writes the item's -inf blocks.
+  it.tiles = it.nrows > 0 ? max(1, (it.maxvis + kTileKeys - 1) / kTileKeys) : 0;
+  return it;
+}
+
+__device__ __forceinline__ bool tile_computed(const BlockItem& it, int j) {
+  return j * kTileKeys < it.maxvis;
+}
+
+// Cooperative over kThreads threads: total tiles and, for the global tile x
+// (if < total), the item holding it and that item's start.
+__device__ void block_plan(const BlockParams& p, int tid, int64_t x, int32_t* scan, BlockCta* st) {
+  const int items = p.num_seqs * p.num_kv_heads * p.row_tiles;
+  const int per = (items + kThreads - 1) / kThreads;
+  const int i0 = tid * per, i1 = min(items, i0 + per);
+  int32_t s = 0;
+  for (int i = i0; i < i1; ++i) s += block_item(p, i).tiles;
+  scan[tid] = s;
+  __syncthreads();
+  if (tid == 0) {
+    int32_t acc = 0;
+    for (int j = 0; j < kThreads; ++j) {
+      const int32_t v = scan[j];
+      scan[j] = acc;
+      acc += v;
+    }
+    st->total_tiles = acc;
+    st->item0 = -1;
+    st->item0_start = 0;
+  }
+  __syncthreads();
+  const int32_t pre = scan[tid];
+  if (x < st->total_tiles && pre <= x && x < pre + s) {
+    int32_t acc = pre;
+    for (int i = i0; i < i1; ++i) {
+      const int32_t ti = block_item(p, i).tiles;
+      if (x < acc + ti) {
+        st->item0 = i;
+        st->item0_start = acc;
+        break;
+      }
+      acc += ti;
+    }
+  }
+  __syncthreads();
+}
+
+// Visit the (item, tile range) segments of this CTA's chunk in order.
+template <class Fn>
+__device__ __forceinline__ void block_segments(const BlockParams& p, const BlockCta* st, Fn&& f) {
+  const int items = p.num_seqs * p.num_kv_heads * p.row_tiles;
+  int64_t x = static_cast<int64_t>(blockIdx.x) * st->chunk;
+  const int64_t end = min(static_cast<int64_t>(st->total_tiles), x + st->chunk);
+  if (x >= end || st->item0 < 0) return;
+  int32_t i = st->item0;
+  int64_t start = st->item0_start;
+  while (x < end && i < items) {
+    const BlockItem it = block_item(p, i);
+    const int64_t lo = x - start;
+    const int64_t hi = min(end, start + it.tiles) - start;
+    if (hi > lo) {
+      f(i, it, static_cast<int>(lo), static_cast<int>(hi));
+      x = start + hi;
+    }
+    start += it.tiles;
+    ++i;
+  }
+}
+
+__device__ __forceinline__ float max2n(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+__device__ __forceinline__ float max3n(float a, float b, float c) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Max of the 128 columns (four independent chains of three-input max).
+__device__ __forceinline__ float block_max_all(const uint32_t (&v)[128]) {
+  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int i = 0; i < 128; i += 8) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) m[c] = max3n(m[c], __uint_as_float(v[i + 2 * c]), __uint_as_float(v[i + 2 * c + 1]));
+  }
+  return max2n(max2n(m[0], m[1]), max2n(m[2], m[3]));
+}
+
+// Max of the columns n in [lo, hi); -inf when empty.  Masked columns are
+// replaced by -inf by selection, so whatever they hold never reaches the max.
+__device__ __forceinline__ float block_max_range(const uint32_t (&v)[128], int lo, int hi) {
+  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  const uint32_t span = hi > lo ? static_cast<uint32_t>(hi - lo) : 0u;
+#pragma unroll
+  for (int i = 0; i < 128; i += 8) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int n0 = i + 2 * c, n1 = n0 + 1;
+      const float a = static_cast<uint32_t>(n0 - lo) < span ? __uint_as_float(v[n0]) : -INFINITY;
+      const float b = static_cast<uint32_t>(n1 - lo) < span ? __uint_as_float(v[n1]) : -INFINITY;
+      m[c] = max3n(m[c], a, b);
+    }
+  }
+  return max2n(max2n(m[0], m[1]), max2n(m[2], m[3]));
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_constant__ BlockParams p) {
+  using L = BlockLayout<FMT>;
+  using F = FmtTraits<FMT>;
+  constexpr int G = F::G;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const uint32_t bar0 = smem_u32(smem + L::kBars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto accf_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
+  auto acce_bar = [&](int a) { return bar0 + 8u * (2 * kStages + kAccBufs + a); };
+  auto qfull_bar = [&](uint32_t qb) { return bar0 + 8u * (2 * kStages + 2 * kAccBufs + qb); };
+  auto qempty_bar = [&](uint32_t qb) { return bar0 + 8u * (2 * kStages + 2 * kAccBufs + 2 + qb); };
+
+  BlockCta* st = reinterpret_cast<BlockCta*>(smem + L::kState);
+  int32_t* scan = reinterpret_cast<int32_t*>(smem + L::kScan);
+  volatile int* abort_flag = &st->abort;
+
+  // ---- this CTA's chunk of the concatenated tile space
+  if (threadIdx.x == 0) st->abort = 0;
+  block_plan(p, threadIdx.x, INT64_MAX, scan, st);
+  {
+    const int32_t total = st->total_tiles;
+    const int32_t chunk = (total + gridDim.x - 1) / gridDim.x;
+    const int64_t x = static_cast<int64_t>(blockIdx.x) * chunk;
+    if (chunk == 0 || x >= total) return;  // uniform: no work for this CTA
+    block_plan(p, threadIdx.x, x, scan, st);
+    if (threadIdx.x == 0) st->chunk = chunk;
+  }
+
+  // ---- one-time setup
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1 + 32);  // expect-tx arrive + one cp.async arrive per producer lane
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < kAccBufs; ++a) {
+      mbar_init(accf_bar(a), 1);
+      mbar_init(acce_bar(a), 128);  // the four warps of the group that owns the tile
+    }
+    for (uint32_t qb = 0; qb < 2; ++qb) {
+      mbar_init(qfull_bar(qb), 1 + 32);
+      mbar_init(qempty_bar(qb), 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc<kTmemCols>(smem_u32(&st->tmem_base));
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = st->tmem_base;
+
+  const uint32_t codes_s = smem_u32(smem + L::kCodes);
+  const uint32_t q_s = smem_u32(smem + L::kQ);
+  uint8_t* ksf_atoms = smem + L::kKsf;
+  uint8_t* qsf_atoms = smem + L::kQsf;
+  const int pshift = p.page_shift;
+  const int page = p.page_size;
+  const int slots = kTileKeys >> pshift;  // pages per tile: 2 (64-key pages) or 1 (128)
+  const int rt_shift = p.rt_shift;
+
+  if (warp == 0) {
+    // ================================================================ producer
+    uint32_t tile_iter = 0, item_iter = 0;
+    bool ok = true;
+    if (lane == 0) {
+      prefetch_tmap(&p.tmap_k);
+      prefetch_tmap(&p.tmap_q);
+    }
+    block_segments(p, st, [&](int, const BlockItem& it, int lo, int hi) {
+      if (!ok) return;
+      // -- Q of the item: codes by TMA, scales by cp.async into the atom
+      const uint32_t qb = item_iter & 1u, qph = (item_iter >> 1) & 1u;
+      ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(qempty_bar(qb), qph ^ 1u, abort_flag, p.err) : false, 0);
+      if (!ok) return;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(qfull_bar(qb), 128 * kCodeBytes);
+        tma_load_3d(q_s + qb * 8192u, &p.tmap_q, 0, it.row0, it.hk << p.group_shift, qfull_bar(qb));
+      }
+      {
+        uint8_t* atom = qsf_atoms + qb * F::kAtoms * 512 + lane * 16;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int m = 32 * q + lane;
+          const int t_local = m & ((1 << rt_shift) - 1);
+          const int h = (it.hk << p.group_shift) + (m >> rt_shift);
+          // rows past the item's last row read row0's scales (results discarded)
+          const int64_t t = it.row0 + (t_local < it.nrows ? t_local : 0);
+          const uint8_t* src = p.q_scale + t * p.q_scale_row_stride + h * G;
+          cp_async_4(smem_u32(atom + 4 * q), src);
+          if constexpr (G == 8) cp_async_4(smem_u32(atom + 512 + 4 * q), src + 4);
+        }
+        cp_async_arrive(qfull_bar(qb));
+      }
+      ++item_iter;
+      // -- K tiles: lane l caches the physical id of logical page base + l
+      const int32_t npages = (it.k_len + page - 1) >> pshift;
+      const int32_t* table = p.block_table + it.table_base;
+      auto fetch = [&](int32_t b) -> int32_t {
+        const int32_t lp = b + lane;
+        return lp < npages ? __ldg(table + lp) : -1;
+      };
+      int32_t base = (lo * slots) & ~31;
+      int32_t cur_ids = fetch(base), next_ids = fetch(base + 32);
+      for (int j = lo; j < hi; ++j) {
+        if (!tile_computed(it, j)) continue;
+        const int32_t lp0 = j * slots;
+        if (lp0 >= base + 32) {  // warp-uniform
+          base += 32;
+          cur_ids = next_ids;
+          next_ids = fetch(base + 32);
+        }
+        const int32_t phys0 = __shfl_sync(0xffffffffu, cur_ids, lp0 - base);
+        const int32_t phys1 = __shfl_sync(0xffffffffu, cur_ids, lp0 - base + (slots - 1));
+        auto page_ok = [&](int sl, int32_t ph_id) {
+          return ((lp0 + sl) << pshift) < it.k_len && ph_id >= 0 && ph_id < p.num_pages;
+        };
+        const bool ok0 = page_ok(0, phys0);
+        const bool ok1 = slots == 2 && page_ok(1, phys1);
+        if (lane < slots && ((lp0 + lane) << pshift) < it.k_len && !(lane == 0 ? ok0 : ok1))
+          atomicOr(p.err, kErrPageRange);
+        // cache rows of the two slots (< 2^31 for resolved pages: checked on the host)
+        const int32_t row0k = ok0 ? static_cast<int32_t>((static_cast<int64_t>(phys0) * p.num_kv_heads + it.hk) << pshift) : 0;
+        const int32_t row1k = ok1 ? static_cast<int32_t>((static_cast<int64_t>(phys1) * p.num_kv_heads + it.hk) << pshift) : 0;
+        const uint32_t bytes = static_cast<uint32_t>((ok0 ? 1 : 0) + (ok1 ? 1 : 0)) * page * kCodeBytes;
+        const int s = tile_iter % kStages;
+        const uint32_t ph = (tile_iter / kStages) & 1u;
+        ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.err) : false, 0);
+        if (!ok) return;
+        if (lane == 0) mbar_arrive_expect_tx(full_bar(s), bytes);
+        __syncwarp();
+        if (lane < slots && (lane == 0 ? ok0 : ok1))
+          tma_load_2d(codes_s + s * 8192 + ((lane * kCodeBytes) << pshift), &p.tmap_k, 0,
+                      lane == 0 ? row0k : row1k, full_bar(s));
+        // key n = 32q + lane -> atom line `lane`, word q (second atom: scales 4..7)
+        uint8_t* atom = ksf_atoms + s * F::kAtoms * 512 + lane * 16;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int n = 32 * q + lane;
+          const int sl = n >> pshift;
+          if (sl == 0 ? ok0 : ok1) {
+            const uint8_t* src = p.k_scale + static_cast<int64_t>((sl == 0 ? row0k : row1k) + (n & (page - 1))) * G;
+            cp_async_4(smem_u32(atom + 4 * q), src);
+            if constexpr (G == 8) cp_async_4(smem_u32(atom + 512 + 4 * q), src + 4);
+          }
+        }
+        cp_async_arrive(full_bar(s));
+        ++tile_iter;
+      }
+    });
+    if (!ok && lane == 0) {
+      // Let copies already in flight land before the CTA can exit.
+      volatile int never = 0;
+      const uint32_t first = tile_iter > static_cast<uint32_t>(kStages) ? tile_iter - kStages : 0;
+      for (uint32_t u = first; u < tile_iter; ++u) mbar_wait(full_bar(u % kStages), (u / kStages) & 1u, &never, p.err);
+      for (uint32_t u = item_iter > 2u ? item_iter - 2u : 0u; u < item_iter; ++u)
+        mbar_wait(qfull_bar(u & 1u), (u >> 1) & 1u, &never, p.err);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    const uint64_t q_desc0 = desc_kmajor_sw64(q_s);
+    const uint64_t k_desc0 = desc_kmajor_sw64(codes_s);
+    const uint64_t ksf_desc0 = desc_sf_atom(smem_u32(ksf_atoms));
+    const uint64_t qsf_desc0 = desc_sf_atom(smem_u32(qsf_atoms));
+    uint32_t tile_iter = 0, item_iter = 0;
+    bool ok = true;
+    int last_acc = -1;
+    uint32_t last_acc_phase = 0;
+    block_segments(p, st, [&](int, const BlockItem& it, int lo, int hi) {
+      if (!ok) return;
+      const uint32_t qb = item_iter & 1u, qph = (item_iter >> 1) & 1u;
+      if (lane == 0) {
+        ok = mbar_wait(qfull_bar(qb), qph, abort_flag, p.err);
+        if (ok) {
+          // Q scales were written by cp.async (generic proxy): make them
+          // visible to the tensor core's copy.
+          fence_proxy_async_smem();
+          tc_fence_after();
+          const uint32_t qsf_t = tmem + L::kQsfCol + qb * 8u;
+#pragma unroll
+          for (int at = 0; at < F::kAtoms; ++at)
+            tc_cp_32x128b_warpx4(qsf_t + 4u * at,
+                                 qsf_desc0 + static_cast<uint64_t>(((qb * F::kAtoms + at) * 512) >> 4));
+          const uint64_t adesc = q_desc0 + static_cast<uint64_t>((qb * 8192u) >> 4);
+          for (int j = lo; j < hi && ok; ++j) {
+            if (!tile_computed(it, j)) continue;
+            const int s = tile_iter % kStages;
+            const uint32_t ph = (tile_iter / kStages) & 1u;
+            const int a = tile_iter % kAccBufs;
+            const uint32_t aph = (tile_iter / kAccBufs) & 1u;
+            if (!(ok = mbar_wait(full_bar(s), ph, abort_flag, p.err))) break;
+            // K-scale slot of tile i is i % kKsfSlots: its previous reader, the
+            // MMA of tile i - kKsfSlots, completed before the accumulator of
+            // tile i - 1 could be free (kAccBufs < kKsfSlots).
+            const uint32_t ksf_t = tmem + L::kKsfCol + (tile_iter % kKsfSlots) * 8u;
+            fence_proxy_async_smem();
+#pragma unroll
+            for (int at = 0; at < F::kAtoms; ++at)
+              tc_cp_32x128b_warpx4(ksf_t + 4u * at, ksf_desc0 + static_cast<uint64_t>(((s * F::kAtoms + at) * 512) >> 4));
+            if (!(ok = mbar_wait(acce_bar(a), aph ^ 1u, abort_flag, p.err))) break;
+            tc_fence_after();
+            const uint32_t d = tmem + L::kAccCol + a * 128u;
+            const uint64_t bdesc = k_desc0 + static_cast<uint64_t>((s * 8192) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+              constexpr uint32_t sf1 = F::kScaleVec == 2 ? 2u : 0u;
+              const uint32_t idesc =
+                  kk == 0 ? idesc_fp4(128, 128, F::kUe8m0, 0, 0) : idesc_fp4(128, 128, F::kUe8m0, sf1, sf1);
+              const uint32_t col = F::kScaleVec == 2 ? 0u : 4u * kk;
+              tc_mma_fp4<F::kScaleVec>(d, adesc + 2u * kk, bdesc + 2u * kk, idesc, qsf_t + col, ksf_t + col,
+                                       static_cast<uint32_t>(kk));
+            }
+            tc_commit(empty_bar(s));
+            tc_commit(accf_bar(a));
+            last_acc = a;
+            last_acc_phase = aph;
+            ++tile_iter;
+          }
+          // Q buffer and Q-scale slot free once this item's MMAs complete.
+          tc_commit(qempty_bar(qb));
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      ++item_iter;
+    });
+    if (!ok && last_acc >= 0 && lane == 0) {
+      // Outstanding MMAs must finish before TMEM is released.
+      volatile int never = 0;
+      mbar_wait(accf_bar(last_acc), last_acc_phase, &never, p.err);
+    }
+    __syncwarp();
+  } else {
+    // ================================================================ epilogue
+    const int e = (warp - 2) >> 2;  // group: takes the tiles with tile_iter % kGroups == e
+    Group<128, -1> g{static_cast<int>(threadIdx.x) - 64 - e * 128, 1 + e};
+    const int quad = warp & 3;
+    const int m = quad * 32 + lane;  // TMEM lane = MMA row
+    const int h_local = m >> rt_shift;
+    const int t_local = m & ((1 << rt_shift) - 1);
+    uint32_t tile_iter = 0;
+    bool ok = true;
+    const int64_t T = p.num_rows;
+    block_segments(p, st, [&](int, const BlockItem& it, int lo, int hi) {
+      const int32_t t = it.row0 + t_local;
+      const bool row_valid = t_local < it.nrows && t < p.num_rows;
+      const int h = (it.hk << p.group_shift) + h_local;
+      const int32_t vis = row_valid ? row_vis(p, it, t) : 0;
+      float* out = p.scores + static_cast<int64_t>(h) * p.ktiles * T + t;  // + kb * T
+      const int nreal = (it.maxvis + kTileKeys - 1) / kTileKeys;
+      for (int j = lo; j < hi; ++j) {
+        bool owner;
+        if (tile_computed(it, j)) {
+          owner = static_cast<int>(tile_iter % kGroups) == e;
+          if (owner) {
+            const int a = tile_iter % kAccBufs;
+            const uint32_t aph = (tile_iter / kAccBufs) & 1u;
+            if (g.tid == 0 && ok && !mbar_wait(accf_bar(a), aph, abort_flag, p.err)) st->abort = 1;
+            g.sync();
+            // warp-uniform: tcgen05.ld below is a whole-warp instruction
+            ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+            if (ok) {
+              tc_fence_after();
+              uint32_t v[128];
+              const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + L::kAccCol + a * 128u;
+#pragma unroll
+              for (int c = 0; c < 128; c += 32) {
+                uint32_t part[32];
+                tmem_ld_x32(taddr + c, part);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[c + i] = part[i];
+              }
+              tmem_wait_ld();
+              reg_fence(v);
+              tc_fence_before();
+              mbar_arrive(acce_bar(a));
+              // columns [lo_c, hi_c) are visible keys of this row in pages that resolved
+              int lo_c = 0;
+              int hi_c = vis - j * kTileKeys;
+              hi_c = hi_c < 0 ? 0 : (hi_c > kTileKeys ? kTileKeys : hi_c);
+              const int32_t lp0 = j * slots;
+              for (int sl = 0; sl < slots; ++sl) {
+                if (((lp0 + sl) << pshift) >= it.k_len) break;
+                const int32_t ph_id = __ldg(p.block_table + it.table_base + lp0 + sl);
+                if (ph_id < 0 || ph_id >= p.num_pages) {
+                  if (sl == 0) lo_c = page;  // 64-key pages: the second half may still count
+                  else hi_c = min(hi_c, page);
+                  if (slots == 1) hi_c = 0;
+                }
+              }
+              const bool full = lo_c == 0 && hi_c == kTileKeys;
+              const float r = __all_sync(0xffffffffu, full) ? block_max_all(v) : block_max_range(v, lo_c, hi_c);
+              if (row_valid && j < p.ktiles) out[static_cast<int64_t>(j) * T] = r;
+            }
+          }
+          ++tile_iter;
+        } else {
+          owner = e == 0;  // a tile nothing is computed for: group 0 writes its -inf
+        }
+        if (j == it.tiles - 1 && owner && row_valid) {
+          for (int kb = nreal; kb < p.ktiles; ++kb) out[static_cast<int64_t>(kb) * T] = -INFINITY;
+        }
+      }
+    });
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<kTmemCols>(tmem);
+  }
+}
+
+template <int FMT>
+cudaError_t launch_fmt(const BlockParams& p, dim3 grid, cudaStream_t stream) {
+  using L = BlockLayout<FMT>;
+  // At least ~120 KB so that one CTA (and one 512-column TMEM allocation) runs per SM.
+  const uint32_t bytes = L::bytes() < 120u * 1024u ? 120u * 1024u : L::bytes();
+  if (bytes > 232448u) return cudaErrorInvalidConfiguration;
+  auto kern = block_score_kernel<FMT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, bytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_block_scores(const BlockParams& p, int format, dim3 grid, cudaStream_t stream) {
+  return format == 0 ? launch_fmt<0>(p, grid, stream) : launch_fmt<1>(p, grid, stream);
+}
+
+}  // namespace fp4idx

@@ -64,6 +64,39 @@ struct MergeParams {
   int32_t* valid_count;
 };
 
+// Queries-on-M block scorer: one item = (request b, K head hk, RT query
+// rows); its M = 128 MMA rows are the g = Hq/Hkv heads of group hk x RT rows
+// (row m = h_local * RT + t_local, RT = 128 / g).  Tiles are the item's
+// 128-key blocks; the tiles of all items are split evenly across CTAs.
+struct BlockParams {
+  CUtensorMap tmap_k;   // 2D {64 B, num_pages*Hkv*page}, box {64, page}, 64B swizzle
+  CUtensorMap tmap_q;   // 3D {64 B, T (q_row_stride), Hq (64 B)}, box {64, RT, g}, 64B swizzle
+  const uint8_t* k_scale;
+  const uint8_t* q_scale;
+  int64_t q_scale_row_stride;
+  const int32_t* cu_seqlens_q;
+  const int32_t* cu_seqlens_k;
+  const int32_t* block_table;
+  const int32_t* page_offsets;
+  int64_t table_stride;
+  const int32_t* visible_len;
+  const int32_t* qo_offset;
+  int32_t causal;
+  int32_t page_size;
+  int32_t page_shift;
+  int64_t num_pages;
+  int32_t num_rows;
+  int32_t num_heads;
+  int32_t num_kv_heads;
+  int32_t num_seqs;
+  int32_t group_shift;  // log2(Hq / Hkv)
+  int32_t rt_shift;     // log2(RT) = 7 - group_shift
+  int32_t row_tiles;    // ceil(max_seqlen_q / RT)
+  int32_t ktiles;       // output blocks per (head, row): ceil(max_seqlen_k / 128)
+  float* scores;        // [Hq][ktiles][T]
+  uint32_t* err;
+};
+
 // Launchers (defined in the kernel translation units).  Return cudaSuccess
 // or the launch error.
 cudaError_t launch_score_mx(const ScoreParams& p, int mode, int heads, dim3 grid, cudaStream_t stream);
@@ -74,6 +107,7 @@ inline cudaError_t launch_score(const ScoreParams& p, int format, int mode, int 
                      : launch_score_nv(p, mode, heads, grid, stream);
 }
 cudaError_t launch_topk_merge(const MergeParams& p, int rows, cudaStream_t stream);
+cudaError_t launch_block_scores(const BlockParams& p, int format, dim3 grid, cudaStream_t stream);
 
 // Sets the message fp4idx_last_error_message() returns on this thread.
 void set_last_error(const char* fmt, ...);

@@ -31,6 +31,7 @@
 // boundary reloads Q and, for top-k, flushes its per-row candidates.
 #pragma once
 
+#include "formats.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "topk_smem.cuh"
@@ -40,19 +41,6 @@ namespace fp4idx {
 constexpr int kEpiThreads = 128;  // one epilogue group: four warps, one per TMEM lane quadrant
 constexpr uint32_t kTmemCols = 512;
 constexpr int kAccBufs = 3;  // accumulator buffers: the MMA may run two tiles ahead of the epilogue
-
-template <int FMT>
-struct FmtTraits;
-template <>
-struct FmtTraits<0> {  // MXFP4: E8M0 per 32 values
-  static constexpr int G = 4, kAtoms = 1, kScaleVec = 2;
-  static constexpr bool kUe8m0 = true;
-};
-template <>
-struct FmtTraits<1> {  // NVFP4: E4M3 per 16 values
-  static constexpr int G = 8, kAtoms = 2, kScaleVec = 4;
-  static constexpr bool kUe8m0 = false;
-};
 
 // Per-CTA bookkeeping in shared memory.
 struct CtaState {
@@ -681,7 +669,8 @@ __global__ void __launch_bounds__(96 + kEpiThreads * R, 1) score_kernel(const __
           // block on the group's named barrier instead of spinning.
           if (g.tid == 0 && ok && !mbar_wait(accf_bar(a), aph, abort_flag, p.err)) st->abort = 1;
           g.sync();
-          ok = ok && !*abort_flag;
+          // warp-uniform: tcgen05.ld below is a whole-warp instruction
+          ok = __all_sync(0xffffffffu, ok && !*abort_flag);
           if (ok) {
             tc_fence_after();
             uint32_t v[H];

@@ -99,3 +99,19 @@ def test_topk_rejects_bad_k_and_flags(lib, k, flags, status):
 def test_block_scores_rejects_bad_problem(lib):
     c = _problem(format=3)
     assert lib.fp4idx_block_scores(ctypes.byref(c), ctypes.c_void_p(1 << 20), None) == 1
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(num_heads=24, num_kv_heads=8, q_row_stride=24 * 64, q_scale_row_stride=24 * 4), 2),  # group 3
+    (dict(num_heads=256, num_kv_heads=1, q_row_stride=256 * 64, q_scale_row_stride=256 * 4), 2),  # group 256
+    (dict(num_heads=12, num_kv_heads=8), 1),  # not a multiple
+])
+def test_block_scores_rejects_unsupported_groups_on_host(lib, over, status):
+    c = _problem(**over)
+    assert lib.fp4idx_block_scores(ctypes.byref(c), ctypes.c_void_p(1 << 20), None) == status
+    assert lib.fp4idx_last_error_message()
+
+
+def test_block_scores_null_output(lib):
+    c = _problem()
+    assert lib.fp4idx_block_scores(ctypes.byref(c), None, None) == 1
