@@ -8,15 +8,19 @@ the C ABI.  The default workload is the 4-row x 32-head verify decode over
 16,384 MXFP4 keys on shuffled 64-key pages (SGLang PR 42861's benchmark
 shape): per step the full logits [4, 16384] and the top-2048 of every row.
 Other workloads: ``long_decode`` (16 requests x 4 rows over 100k/400k keys,
-fused top-2048), ``tiny`` (4 rows x 8 heads over 1,024 keys).
+fused top-2048), ``block_scores`` (4 x 4,096 causal rows over 8,192 keys,
+Hq=32 / Hkv=4, NVFP4: the [Hq, 64, T] block maxima), ``prefill`` (32,768
+causal rows over 32,768 keys, 64 heads, fused top-2048), ``tiny`` (4 rows x
+8 heads over 1,024 keys).
 
 Prints one JSON line.  ``value`` is query x key scores per second over all
-ranks (a score is one (row, visible key) pair of the step), timed on the
-device with CUDA events over K graph-replayed steps with the inputs already
-in HBM; ``e2e`` repeats the measurement with the per-step inputs copied from
-pinned host memory and the results read back inside the timed region.
-``--impl reference`` times the CPU oracle on a bounded sample of the same
-workload instead.  Multi-GPU runs (torchrun) are independent replicas.
+ranks (a score is one (row, visible key) pair of the step, over all heads),
+timed on the device with CUDA events over K graph-replayed steps with the
+inputs already in HBM; ``e2e`` repeats the measurement with the per-step
+inputs copied from pinned host memory and the results read back inside the
+timed region.  ``--impl reference`` times the CPU oracle on a bounded sample
+of the same workload instead.  Multi-GPU runs (torchrun) are independent
+replicas.
 """
 from __future__ import annotations
 
@@ -58,13 +62,20 @@ def source_sha() -> str:
     return h.hexdigest()[:16]
 
 
+# Dense FP4 : bf16 tensor throughput of the part's nominal figures (13.5 : 2.25
+# PFLOP/s); the FP4 peak is the measured bf16 peak times this ratio.
+FP4_PER_BF16 = 6.0
+
+
 def measured_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
 # ---------------------------------------------------------------------------
@@ -126,10 +137,14 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # workloads
 # ---------------------------------------------------------------------------
+# kind "topk": [logits +] top-k score + merge; kind "block": block maxima.
+# bound: the roofline of the workload's scorer kernel.
 WORKLOADS = {
-    "verify16k": dict(maker="verify_decode_16k", k=2048, logits=True),
-    "long_decode": dict(maker="long_batched_decode", k=2048, logits=False),
-    "tiny": dict(maker="tiny_mx_decode", k=64, logits=True),
+    "verify16k": dict(maker="verify_decode_16k", kind="topk", k=2048, logits=True, bound="hbm"),
+    "long_decode": dict(maker="long_batched_decode", kind="topk", k=2048, logits=False, bound="hbm"),
+    "block_scores": dict(maker="nvfp4_gqa_block_scores", kind="block", k=0, logits=False, bound="tensor"),
+    "prefill": dict(maker="prefill_32k", kind="topk", k=2048, logits=False, bound="tensor"),
+    "tiny": dict(maker="tiny_mx_decode", kind="topk", k=64, logits=True, bound="hbm"),
 }
 
 
@@ -186,7 +201,8 @@ def record_external(event, stream) -> bool:
 
 
 class OursBench:
-    """Device-resident decode step: [logits] + top-k score + top-k merge, graph captured."""
+    """Device-resident step, graph captured: [logits +] top-k score + merge, or
+    the block maxima."""
 
     def __init__(self, host, spec, device):
         import torch
@@ -196,47 +212,59 @@ class OursBench:
         self.B, self.torch = B, torch
         self.host, self.spec, self.device = host, spec, device
         self.k = spec["k"]
+        self.block = spec["kind"] == "block"
         base = B.DeviceProblem.from_host(host, device=device)
-        key_bytes = host.k.nbytes + host.k_scale.nbytes
-        # Enough K-cache copies that a step never finds its keys in L2.
-        self.copies = 1 if key_bytes >= 2 * L2_BYTES else int(min(512, -(-2 * L2_BYTES // key_bytes)))
-        self.problems = [base]
+        T = base.num_rows
+        self.w = None if host.w is None else torch.as_tensor(host.w).to(device)
+        in_bytes = sum(t.numel() * t.element_size() for t in (base.q, base.q_scale, base.k, base.k_scale))
+        if self.w is not None:
+            in_bytes += self.w.numel() * 4
+        self.input_bytes = in_bytes
+        # Enough input copies (queries, keys, weights) that a step never finds them in L2.
+        self.copies = 1 if in_bytes >= 2 * L2_BYTES else int(min(512, -(-2 * L2_BYTES // in_bytes)))
+        self.problems, self.ws_list = [base], [self.w]
         for _ in range(self.copies - 1):
             self.problems.append(B.DeviceProblem(
                 format=base.format, num_heads=base.num_heads, num_kv_heads=base.num_kv_heads,
-                page_size=base.page_size, q=base.q, q_scale=base.q_scale, k=base.k.clone(),
+                page_size=base.page_size, q=base.q.clone(), q_scale=base.q_scale.clone(), k=base.k.clone(),
                 k_scale=base.k_scale.clone(), cu_seqlens_q=base.cu_seqlens_q, cu_seqlens_k=base.cu_seqlens_k,
                 block_table=base.block_table, page_offsets=base.page_offsets, visible_len=base.visible_len,
                 causal=base.causal, qo_offset=base.qo_offset, max_seqlen_q=base.max_seqlen_q,
                 max_seqlen_k=base.max_seqlen_k))
-        T = base.num_rows
-        self.w = torch.as_tensor(host.w).to(device)
-        self.ld = (host.max_seqlen_k + 3) // 4 * 4
-        self.logits = torch.empty((T, self.ld), dtype=torch.float32, device=device) if spec["logits"] else None
-        self.idx = torch.empty((T, self.k), dtype=torch.int32, device=device)
-        self.val = torch.empty((T, self.k), dtype=torch.float32, device=device)
-        self.cnt = torch.empty((T,), dtype=torch.int32, device=device)
-        self.ws = torch.empty((B.fp4idx_topk_workspace_bytes(base, self.k),), dtype=torch.uint8, device=device)
-        self.kernels = (["scorer_logits"] if spec["logits"] else []) + ["scorer_topk", "topk_merge"]
+            self.ws_list.append(None if self.w is None else self.w.clone())
+        if self.block:
+            self.scores = torch.empty((base.num_heads, base.ktiles, T), dtype=torch.float32, device=device)
+            self.kernels = ["block_scores"]
+        else:
+            self.ld = (host.max_seqlen_k + 3) // 4 * 4
+            self.logits = torch.empty((T, self.ld), dtype=torch.float32, device=device) if spec["logits"] else None
+            self.idx = torch.empty((T, self.k), dtype=torch.int32, device=device)
+            self.val = torch.empty((T, self.k), dtype=torch.float32, device=device)
+            self.cnt = torch.empty((T,), dtype=torch.int32, device=device)
+            self.ws = torch.empty((B.fp4idx_topk_workspace_bytes(base, self.k),), dtype=torch.uint8, device=device)
+            self.kernels = (["scorer_logits"] if spec["logits"] else []) + ["scorer_topk", "topk_merge"]
         self.launches_per_step = len(self.kernels)
         self.graphs = []
         self.events = []
 
-    def _calls(self, prob):
+    def _calls(self, n):
         B = self.B
+        prob, w = self.problems[n], self.ws_list[n]
+        if self.block:
+            return [lambda: B.fp4idx_block_scores(prob, out=self.scores)]
         calls = []
         if self.logits is not None:
-            calls.append(lambda: B.fp4idx_logits(prob, self.w, out=self.logits))
-        calls.append(lambda: B.fp4idx_topk_score(prob, self.w, self.k, self.ws))
+            calls.append(lambda: B.fp4idx_logits(prob, w, out=self.logits))
+        calls.append(lambda: B.fp4idx_topk_score(prob, w, self.k, self.ws))
         calls.append(lambda: B.fp4idx_topk_merge(prob, self.k, self.idx, self.val, self.cnt, self.ws))
         return calls
 
-    def _step(self, prob, evs=None):
+    def _step(self, n, evs=None):
         stream = self.torch.cuda.current_stream(self.device)
         ok = True
         if evs is not None:
             ok &= record_external(evs[0], stream)
-        for i, call in enumerate(self._calls(prob)):
+        for i, call in enumerate(self._calls(n)):
             call()
             if evs is not None:
                 ok &= record_external(evs[i + 1], stream)
@@ -247,19 +275,19 @@ class OursBench:
         s = torch.cuda.Stream(device=self.device)
         s.wait_stream(torch.cuda.current_stream(self.device))
         with torch.cuda.stream(s):
-            for prob in self.problems[:2]:
-                self._step(prob)
+            for n in range(min(2, len(self.problems))):
+                self._step(n)
         torch.cuda.current_stream(self.device).wait_stream(s)
         torch.cuda.synchronize(self.device)
         self.timed_nodes = True
-        for prob in self.problems:
+        for n in range(len(self.problems)):
             evs = [torch.cuda.Event(enable_timing=True) for _ in range(self.launches_per_step + 1)]
             for e in evs:  # torch creates the CUDA event lazily, on its first record
                 e.record(s)
             torch.cuda.synchronize(self.device)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                self.timed_nodes &= self._step(prob, evs)
+                self.timed_nodes &= self._step(n, evs)
             self.graphs.append(g)
             self.events.append(evs)
 
@@ -282,10 +310,10 @@ class OursBench:
         res = {}
         for n, name in enumerate(self.kernels):
             graphs = []
-            for prob in self.problems[:reps]:
+            for c in range(min(reps, len(self.problems))):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g):
-                    self._calls(prob)[n]()
+                    self._calls(c)[n]()
                 graphs.append(g)
             for g in graphs[:3]:
                 g.replay()
@@ -304,13 +332,13 @@ class OursBench:
         torch = self.torch
         B = self.B
         prob = self.problems[0]
-        pin = lambda t: t.cpu().pin_memory()
-        h_in = [pin(prob.q), pin(prob.q_scale), pin(self.w), pin(prob.block_table)]
-        if prob.visible_len is not None:
-            h_in.append(pin(prob.visible_len))
-        d_in = [prob.q, prob.q_scale, self.w, prob.block_table] + (
+        d_in = [prob.q, prob.q_scale, prob.block_table] + ([self.w] if self.w is not None else []) + (
             [prob.visible_len] if prob.visible_len is not None else [])
-        d_out = [self.idx, self.val, self.cnt] + ([self.logits] if self.logits is not None else [])
+        h_in = [t.cpu().pin_memory() for t in d_in]
+        if self.block:
+            d_out = [self.scores]
+        else:
+            d_out = [self.idx, self.val, self.cnt] + ([self.logits] if self.logits is not None else [])
         h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in d_out]
         bi = sum(t.numel() * t.element_size() for t in h_in)
         bo = sum(t.numel() * t.element_size() for t in h_out)
@@ -321,10 +349,13 @@ class OursBench:
         for _ in range(steps):
             for h, d in zip(h_in, d_in):
                 d.copy_(h, non_blocking=True)
-            if self.logits is not None:
-                B.fp4idx_logits(prob, self.w, out=self.logits)
-            B.fp4idx_topk(prob, self.w, self.k, indices=self.idx, values=self.val, valid_count=self.cnt,
-                          workspace=self.ws)
+            if self.block:
+                B.fp4idx_block_scores(prob, out=self.scores)
+            else:
+                if self.logits is not None:
+                    B.fp4idx_logits(prob, self.w, out=self.logits)
+                B.fp4idx_topk(prob, self.w, self.k, indices=self.idx, values=self.val, valid_count=self.cnt,
+                              workspace=self.ws)
             for h, d in zip(h_out, d_out):
                 h.copy_(d, non_blocking=True)
         end.record()
@@ -343,38 +374,88 @@ def kernel_algorithmic_bytes(host, name: str, k: int) -> int:
     for b in range(host.num_seqs):
         r0, r1 = int(host.cu_seqlens_q[b]), int(host.cu_seqlens_q[b + 1])
         keys += int(vis[r0:r1].max()) if r1 > r0 else 0
-    kv = keys * kv_bytes_per_key(host.format)
+    kv = keys * kv_bytes_per_key(host.format) * host.num_kv_heads
     T, H = host.q.shape[0], host.num_heads
-    qb = host.q.nbytes + host.q_scale.nbytes + T * H * 4
+    qb = host.q.nbytes + host.q_scale.nbytes + (T * H * 4 if host.w is not None else 0)
     if name == "scorer_logits":
         return kv + qb + T * ((host.max_seqlen_k + 3) // 4 * 4) * 4
     if name == "scorer_topk":
         return kv + qb
     if name == "topk_merge":
         return T * k * 8 + T * 4
+    if name == "block_scores":
+        return kv + qb + H * ((host.max_seqlen_k + 127) // 128) * T * 4
     raise KeyError(name)
 
 
-def cpu_baseline(host, spec, budget_s: float = 10.0) -> dict:
-    """The oracle on the host cores over a bounded sample: the last row of
-    the first request, its full logits and its top-k, repeated for ~budget_s."""
+def kernel_algorithmic_flops(host) -> int:
+    """FP4 tensor FLOPs of the visible part of the QK contraction:
+    2 * 128 per (row, head, visible key)."""
+    import oracle
+
+    return int(oracle.visible_all(host).astype(np.int64).sum()) * host.num_heads * 2 * 128
+
+
+def roofline(host, spec, name: str, launch_ms: float, step_ms: float, peaks: dict) -> dict:
+    """Roofline of one kernel: the scorer kernels against the workload's bound
+    (HBM bytes for decode, FP4 tensor FLOPs for prefill / block scores), the
+    merge against HBM."""
+    tensor = spec["bound"] == "tensor" and name in ("scorer_topk", "scorer_logits", "block_scores")
+    if tensor:
+        flops = kernel_algorithmic_flops(host)
+        sustained = step_ms > 1.0  # a long step runs the tensor pipe at its power-capped rate
+        bf16 = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+        peak = bf16 * FP4_PER_BF16
+        achieved = flops / (launch_ms * 1e-3) / 1e12
+        return {"bound": "tensor", "kernel": name, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None, "algorithmic_flops": flops,
+                "launch_us": launch_ms * 1e3,
+                "peak_source": f"{peaks['source']} bf16 {'sustained' if sustained else 'burst'} "
+                               f"{bf16:.1f} TFLOP/s x {FP4_PER_BF16:g} (nominal FP4/bf16 ratio)"}
+    alg = kernel_algorithmic_bytes(host, name, spec["k"])
+    achieved = alg / (launch_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes": alg,
+            "launch_us": launch_ms * 1e3, "peak_source": peaks["source"]}
+
+
+def oracle_sample(host, spec):
+    """One bounded unit of oracle work on the workload: the last row of the
+    first request -- its full logits and top-k, or all its block maxima."""
     import oracle
 
     row = int(host.cu_seqlens_q[1]) - 1
     vis = oracle.visible(host, row)
     op = oracle.OracleProblem(host)
+    if spec["kind"] == "block":
+        def step():
+            oracle.block_scores(op, host.ktiles, rows=[row])
+        what = f"row {row} ({vis} visible keys): its block maxima for all {host.num_heads} heads"
+    else:
+        def step():
+            if spec["logits"]:
+                oracle.logits_rows(op, vis, rows=[row])
+            oracle.topk(op, spec["k"], rows=[row])
+        what = f"row {row} ({vis} visible keys): " + ("full logits and " if spec["logits"] else "") + \
+            f"top-{spec['k']}"
+    return step, vis, what
+
+
+def cpu_baseline(host, spec, budget_s: float = 10.0) -> dict:
+    """The oracle on the host cores over a bounded sample (oracle_sample),
+    repeated for ~budget_s."""
+    import oracle
+
+    step, vis, what = oracle_sample(host, spec)
     reps, t0 = 0, time.perf_counter()
     while True:
-        if spec["logits"]:
-            oracle.logits_rows(op, vis, rows=[row])
-        oracle.topk(op, spec["k"], rows=[row])
+        step()
         reps += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     el = time.perf_counter() - t0
     return {"value": reps * vis / el, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"row {row} ({vis} visible keys): full logits and top-{spec['k']}" if spec["logits"]
-            else f"row {row} ({vis} visible keys): top-{spec['k']}", "seconds": round(el, 2), "reps": reps}
+            "sample": what, "seconds": round(el, 2), "reps": reps}
 
 
 # ---------------------------------------------------------------------------
@@ -419,15 +500,7 @@ def run_reference(args, world, rank):
     import oracle
 
     oracle.build()
-    row = int(host.cu_seqlens_q[1]) - 1
-    vis = oracle.visible(host, row)
-    op = oracle.OracleProblem(host)
-
-    def step():
-        if spec["logits"]:
-            oracle.logits_rows(op, vis, rows=[row])
-        oracle.topk(op, spec["k"], rows=[row])
-
+    step, vis, what = oracle_sample(host, spec)
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
@@ -435,8 +508,7 @@ def run_reference(args, world, rank):
         step()
     el = time.perf_counter() - t0
     value = args.steps * vis / el
-    sample = f"row {row} ({vis} visible keys) per step: " + ("full logits and " if spec["logits"] else "") + \
-        f"top-{spec['k']}"
+    sample = what + " per step"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
@@ -503,12 +575,16 @@ def run_ours(args, world, rank, local):
     e2e_ms = reduce_max(e2e["ms"], world)
 
     peaks = measured_peaks()
+    step_ms = ms_max / args.steps
     dominant = max(kt, key=lambda n: kt[n])
-    alg = kernel_algorithmic_bytes(host, dominant, spec["k"])
-    achieved = alg / (kt[dominant] * 1e-3) / 1e9
+    roof = roofline(host, spec, dominant, kt[dominant], step_ms, peaks)
     sha = source_sha()
     rec = RECORDED_TRAFFIC.get((args.workload, dominant))
-    traffic = rec["bytes"] if rec and rec["sha"] == sha else None
+    roof["traffic"] = rec["bytes"] if rec and rec["sha"] == sha else None
+    if spec["kind"] == "block":
+        step_desc = f"block maxima [{host.num_heads}, {host.ktiles}, {host.q.shape[0]}]"
+    else:
+        step_desc = ("logits + " if spec["logits"] else "") + f"top-{spec['k']} (score + merge)"
     line = {
         "metric": METRIC,
         "value": value,
@@ -516,24 +592,25 @@ def run_ours(args, world, rank, local):
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": ms_max / args.steps,
-        "us_per_call": 1e3 * ms_max / args.steps,
+        "ms_per_step": step_ms,
+        "us_per_call": 1e3 * step_ms,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "fp4-e2m1 x fp4-e2m1 -> fp32",
         "data": "synthetic",
         "config": {**host.summary(),
-                   "step": ("logits + " if spec["logits"] else "") + f"top-{spec['k']} (score + merge)",
+                   "step": step_desc,
                    "scores_per_step": pairs,
-                   "l2": (f"inputs rotated over {bench.copies} K-cache copies "
-                          f"({bench.copies * (host.k.nbytes + host.k_scale.nbytes) / 2**20:.0f} MiB > 2x L2)"
-                          if bench.copies > 1 else "K cache larger than 2x L2"),
+                   "l2": (f"inputs (q, k, scales, w) rotated over {bench.copies} copies "
+                          f"({bench.copies * bench.input_bytes / 2**20:.0f} MiB > 2x L2)"
+                          if bench.copies > 1 else
+                          f"inputs ({bench.input_bytes / 2**20:.0f} MiB) larger than 2x L2"),
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "algorithmic_bytes": alg, "launch_us": kt[dominant] * 1e3,
-                     "peak_source": peaks["source"]},
+        "roofline": roof,
+        "kernels_roofline": {n: {"bound": r["bound"], "frac": round(r["frac"], 4), "achieved": round(r["achieved"], 1),
+                                 "unit": r["unit"]}
+                             for n in kt for r in [roofline(host, spec, n, kt[n], step_ms, peaks)]},
         "kernels_us": {n: round(v * 1e3, 3) for n, v in kt.items()},
         "kernels_timing": kt_method,
         "e2e": {"value": world * e2e_steps * pairs / (e2e_ms * 1e-3), "unit": UNIT,

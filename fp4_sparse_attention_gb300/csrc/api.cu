@@ -214,7 +214,7 @@ int topk_ctas(const fp4idx_problem_t* p, int sms) {
 }
 
 struct TopkWorkspace {
-  size_t keys_off, count_off, cand_off, bytes;
+  size_t keys_off, count_off, cand_off, start_off, bytes;
 };
 
 // Workspace of the top-k path: per-CTA partial lists, their counts, and each
@@ -229,7 +229,8 @@ TopkWorkspace topk_workspace(const fp4idx_problem_t* p, int32_t k, int sms) {
   ws.keys_off = 0;
   ws.count_off = up(static_cast<size_t>(slots) * k * 8);
   ws.cand_off = ws.count_off + up(static_cast<size_t>(slots) * 4);
-  ws.bytes = ws.cand_off + up(static_cast<size_t>(ctas) * R * topk_capacity(k) * 8);
+  ws.start_off = ws.cand_off + up(static_cast<size_t>(ctas) * R * topk_capacity(k) * 8);
+  ws.bytes = ws.start_off + up(static_cast<size_t>(items + 1) * 4);
   return ws;
 }
 
@@ -325,7 +326,9 @@ fp4idx_status_t topk_prepare(const fp4idx_problem_t* problem, const float* w, in
   sp->part_keys = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(workspace) + ws.keys_off);
   sp->part_count = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + ws.count_off);
   sp->cand = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(workspace) + ws.cand_off);
+  sp->item_start = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + ws.start_off);
   *ctas = topk_ctas(problem, dev->sms);
+  if (*ctas >= kMaxMergeSlots) return fail(FP4IDX_EUNSUPPORTED, "more than %d SMs", kMaxMergeSlots - 1);
   sp->score_ctas = *ctas;
   return FP4IDX_OK;
 }
@@ -367,7 +370,10 @@ fp4idx_status_t fp4idx_topk_merge(const fp4idx_problem_t* problem, int32_t k, ui
   mp.indices = indices;
   mp.values = values;
   mp.valid_count = valid_count;
-  cudaError_t e = launch_topk_merge(mp, problem->num_rows, static_cast<cudaStream_t>(stream));
+  DeviceInfo* dev;
+  if ((s = device_info(&dev)) != FP4IDX_OK) return s;
+  cudaError_t e = launch_topk_merge(mp, problem->num_rows, problem->num_rows > 4 * dev->sms,
+                                    static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
   return FP4IDX_OK;
 }

@@ -51,6 +51,7 @@ struct ScoreParams {
   uint64_t* part_keys;      // [slots * R][k]
   int32_t* part_count;      // [slots * R]
   uint64_t* cand;           // [score_ctas * R][candidate capacity] streaming candidate buffers
+  int32_t* item_start;      // [items + 1] first global tile of each item, total last (top-k only)
   uint32_t* err;
 };
 
@@ -106,7 +107,10 @@ inline cudaError_t launch_score(const ScoreParams& p, int format, int mode, int 
   return format == 0 ? launch_score_mx(p, mode, heads, grid, stream)
                      : launch_score_nv(p, mode, heads, grid, stream);
 }
-cudaError_t launch_topk_merge(const MergeParams& p, int rows, cudaStream_t stream);
+// Partial lists one row can have: at most one per scorer CTA.
+constexpr int kMaxMergeSlots = 256;
+// many_rows: the small-shared-memory variant (several CTAs per SM).
+cudaError_t launch_topk_merge(const MergeParams& p, int rows, bool many_rows, cudaStream_t stream);
 cudaError_t launch_block_scores(const BlockParams& p, int format, dim3 grid, cudaStream_t stream);
 
 // Sets the message fp4idx_last_error_message() returns on this thread.

@@ -109,30 +109,9 @@ struct ScoreLayout {
 // ---------------------------------------------------------------------------
 struct ItemInfo {
   int32_t b, row0, nrows, k_len;
+  int32_t maxvis;  // largest visible key count over the item's rows
   int64_t table_base;
 };
-
-__device__ __forceinline__ ItemInfo item_info(const ScoreParams& p, int32_t i, int rows_per_cta) {
-  ItemInfo it;
-  it.b = i / p.row_groups;
-  const int g = i - it.b * p.row_groups;
-  const int q0 = __ldg(p.cu_seqlens_q + it.b), q1 = __ldg(p.cu_seqlens_q + it.b + 1);
-  it.row0 = q0 + g * rows_per_cta;
-  const int n = q1 - it.row0;
-  it.nrows = n < 0 ? 0 : (n > rows_per_cta ? rows_per_cta : n);
-  it.k_len = __ldg(p.cu_seqlens_k + it.b + 1) - __ldg(p.cu_seqlens_k + it.b);
-  it.table_base = p.page_offsets ? static_cast<int64_t>(__ldg(p.page_offsets + it.b))
-                                 : static_cast<int64_t>(it.b) * p.table_stride;
-  return it;
-}
-
-// Tiles an item contributes to the concatenated work space.
-template <int MODE>
-__device__ __forceinline__ int32_t item_tiles(const ScoreParams& p, const ItemInfo& it) {
-  if (it.nrows <= 0) return 0;
-  if constexpr (MODE == kModeLogits) return p.total_tiles;  // every output column of the rows
-  return (it.k_len + kTileKeys - 1) / kTileKeys;
-}
 
 // Visible key count of row t (rule of the public header).
 __device__ __forceinline__ int32_t row_visible(const ScoreParams& p, const ItemInfo& it, int32_t t) {
@@ -152,12 +131,53 @@ __device__ __forceinline__ int32_t row_visible(const ScoreParams& p, const ItemI
   return static_cast<int32_t>(vis);
 }
 
+__device__ __forceinline__ ItemInfo item_info(const ScoreParams& p, int32_t i, int rows_per_cta) {
+  ItemInfo it;
+  it.b = i / p.row_groups;
+  const int g = i - it.b * p.row_groups;
+  const int q0 = __ldg(p.cu_seqlens_q + it.b), q1 = __ldg(p.cu_seqlens_q + it.b + 1);
+  it.row0 = q0 + g * rows_per_cta;
+  const int n = q1 - it.row0;
+  it.nrows = n < 0 ? 0 : (n > rows_per_cta ? rows_per_cta : n);
+  it.k_len = __ldg(p.cu_seqlens_k + it.b + 1) - __ldg(p.cu_seqlens_k + it.b);
+  if (it.k_len < 0) it.k_len = 0;
+  it.table_base = p.page_offsets ? static_cast<int64_t>(__ldg(p.page_offsets + it.b))
+                                 : static_cast<int64_t>(it.b) * p.table_stride;
+  // the causal rule grows with the row: its last row sees the most
+  it.maxvis = 0;
+  if (it.nrows > 0) {
+    if (p.visible_len) {
+      for (int r = 0; r < it.nrows; ++r) it.maxvis = max(it.maxvis, row_visible(p, it, it.row0 + r));
+    } else {
+      it.maxvis = row_visible(p, it, it.row0 + it.nrows - 1);
+    }
+  }
+  return it;
+}
+
+// Tiles an item contributes to the concatenated work space: every output
+// column for logits, the tiles holding some visible key for top-k.
+template <int MODE>
+__device__ __forceinline__ int32_t item_tiles(const ScoreParams& p, const ItemInfo& it) {
+  if (it.nrows <= 0) return 0;
+  if constexpr (MODE == kModeLogits) return p.total_tiles;
+  return (it.maxvis + kTileKeys - 1) / kTileKeys;
+}
+
+// Whether tile j of the item holds a key some row of it can see; logits
+// tiles past that are written as -inf without loading or computing.
+__device__ __forceinline__ bool tile_has_visible(const ItemInfo& it, int j) {
+  return static_cast<int64_t>(j) * kTileKeys < it.maxvis;
+}
+
 // Cooperative over kNT threads (tid in [0, kNT)): prefix of item tiles.
 // Writes the total and, for the global tile x (if < total), the item
-// holding it and that item's start.  `scan` holds kNT ints.
+// holding it and that item's start.  `scan` holds kNT ints.  With
+// `starts` != nullptr the start of every item (and the total, at index
+// items) is also written there, for the merge.
 template <int MODE, int kNT>
 __device__ void plan_items(const ScoreParams& p, int rows_per_cta, int tid, int64_t x, int32_t* scan,
-                           int32_t* total_out, int32_t* item_out, int32_t* start_out) {
+                           int32_t* total_out, int32_t* item_out, int32_t* start_out, int32_t* starts) {
   const int items = p.num_seqs * p.row_groups;
   const int per = (items + kNT - 1) / kNT;
   const int i0 = tid * per;
@@ -176,9 +196,17 @@ __device__ void plan_items(const ScoreParams& p, int rows_per_cta, int tid, int6
     *total_out = acc;
     *item_out = -1;
     *start_out = 0;
+    if (starts) starts[items] = acc;
   }
   __syncthreads();
   const int32_t pre = scan[tid];
+  if (starts) {
+    int32_t acc = pre;
+    for (int i = i0; i < i1; ++i) {
+      starts[i] = acc;
+      acc += item_tiles<MODE>(p, item_info(p, i, rows_per_cta));
+    }
+  }
   if (x < *total_out && pre <= x && x < pre + s) {
     int32_t acc = pre;
     for (int i = i0; i < i1; ++i) {
@@ -401,13 +429,15 @@ __global__ void __launch_bounds__(96 + kEpiThreads * R, 1) score_kernel(const __
     int32_t total = 0, item = -1, start = 0;
     if (threadIdx.x == 0) st->abort = 0;
     // first pass only for the total; the chunk start depends on it
+    // CTA 0 also publishes every item's tile start for the merge
     plan_items<MODE, kThreads>(p, R, threadIdx.x, INT64_MAX, scan, &st->total_tiles, &st->item0,
-                               &st->item0_start);
+                               &st->item0_start, blockIdx.x == 0 ? p.item_start : nullptr);
     total = st->total_tiles;
     const int32_t chunk = (total + gridDim.x - 1) / gridDim.x;
     const int64_t x = static_cast<int64_t>(blockIdx.x) * chunk;
     if (chunk == 0 || x >= total) return;  // uniform: no work for this CTA
-    plan_items<MODE, kThreads>(p, R, threadIdx.x, x, scan, &st->total_tiles, &st->item0, &st->item0_start);
+    plan_items<MODE, kThreads>(p, R, threadIdx.x, x, scan, &st->total_tiles, &st->item0, &st->item0_start,
+                               nullptr);
     if (threadIdx.x == 0) st->chunk = chunk;
     (void)item;
     (void)start;
@@ -475,7 +505,7 @@ __global__ void __launch_bounds__(96 + kEpiThreads * R, 1) score_kernel(const __
       int32_t base = (lo * slots) & ~31;
       int32_t cur_ids = fetch(base), next_ids = fetch(base + 32);
       for (int j = lo; j < hi; ++j) {
-        if (MODE == kModeLogits && (j << 7) >= it.k_len) continue;
+        if (MODE == kModeLogits && !tile_has_visible(it, j)) continue;
         if ((tile_iter & 1u) != pidx) {  // the other producer's tile
           ++tile_iter;
           continue;
@@ -563,7 +593,7 @@ __global__ void __launch_bounds__(96 + kEpiThreads * R, 1) score_kernel(const __
       // The tiles: one thread issues everything (no per-tile warp traffic).
       if (lane == 0) {
         for (int j = lo; j < hi && ok; ++j) {
-          if (MODE == kModeLogits && static_cast<int64_t>(j) * kTileKeys >= it.k_len) continue;
+          if (MODE == kModeLogits && !tile_has_visible(it, j)) continue;
           const int s = tile_iter % kStages;
           const uint32_t ph = (tile_iter / kStages) & 1u;
           const int a = tile_iter % kAccBufs;
@@ -660,7 +690,7 @@ __global__ void __launch_bounds__(96 + kEpiThreads * R, 1) score_kernel(const __
       for (int j = lo; j < hi; ++j) {
         const int32_t pg_next = j + 1 < hi ? page_of(j + 1) : -1;
         const int32_t pos = (j << 7) + key_local;
-        const bool real = !(MODE == kModeLogits && (j << 7) >= it.k_len);
+        const bool real = !(MODE == kModeLogits && !tile_has_visible(it, j));
         float val = -INFINITY;
         if (real) {
           const int a = tile_iter % kAccBufs;

@@ -15,55 +15,29 @@ namespace {
 
 constexpr int kMergeThreads = 512;
 constexpr int kMergeWarps = kMergeThreads / 32;
-constexpr int kMergeLocal = 20480;  // candidate keys held in shared memory
-constexpr int kMaxSlots = 1024;     // partial lists of one row (<= score CTAs + 1)
 
+// kLocal: candidate keys held in shared memory.  Rows whose union is larger
+// run the same selection from global memory (L2).  The large variant serves
+// few rows with many partial lists (long decode); the small one lets three
+// CTAs share an SM when there are many rows (prefill).
+template <int kLocal>
 struct MergeSmem {
   uint32_t hist[kHistBins];
-  int32_t scan[kMergeThreads];
-  int32_t slot_cnt[kMaxSlots];
-  int32_t slot_off[kMaxSlots + 1];
-  int64_t slot_part[kMaxSlots];
+  int32_t slot_cnt[kMaxMergeSlots];
+  int32_t slot_off[kMaxMergeSlots + 1];
+  int64_t slot_part[kMaxMergeSlots];
   SelectScratch sc;
   int32_t info[8];
   uint64_t out[2048];
-  uint64_t buf[kMergeLocal];
+  uint64_t buf[kLocal];
 };
 
-// Tiles of all items before `item` and of all items (cooperative).
-__device__ void item_prefix(const ScoreParams& p, int rows_per_cta, int tid, int item, int32_t* scan,
-                            int32_t* before_out, int32_t* total_out) {
-  const int items = p.num_seqs * p.row_groups;
-  const int per = (items + kMergeThreads - 1) / kMergeThreads;
-  const int i0 = tid * per, i1 = min(items, i0 + per);
-  int32_t s_all = 0, s_before = 0;
-  for (int i = i0; i < i1; ++i) {
-    const int32_t ti = item_tiles<kModeTopk>(p, item_info(p, i, rows_per_cta));
-    s_all += ti;
-    if (i < item) s_before += ti;
-  }
-  scan[tid] = s_all;
-  __syncthreads();
-  if (tid == 0) {
-    int32_t acc = 0;
-    for (int j = 0; j < kMergeThreads; ++j) acc += scan[j];
-    *total_out = acc;
-  }
-  __syncthreads();
-  scan[tid] = s_before;
-  __syncthreads();
-  if (tid == 0) {
-    int32_t acc = 0;
-    for (int j = 0; j < kMergeThreads; ++j) acc += scan[j];
-    *before_out = acc;
-  }
-  __syncthreads();
-}
-
+template <int kMergeLocal>
 __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const __grid_constant__ MergeParams mp) {
   const ScoreParams& p = mp.sp;
   extern __shared__ uint8_t smem_raw[];
-  MergeSmem* sm = reinterpret_cast<MergeSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
+  using Smem = MergeSmem<kMergeLocal>;
+  Smem* sm = reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -84,14 +58,14 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const __grid_
   const int r = q_local % R;
 
   for (int i = tid; i < kHistBins; i += kMergeThreads) sm->hist[i] = 0;
-  item_prefix(p, R, tid, item, sm->scan, &sm->info[0], &sm->info[1]);
-  const int32_t P = sm->info[0], total = sm->info[1];
-  const ItemInfo it = item_info(p, item, R);
-  const int32_t tiles = item_tiles<kModeTopk>(p, it);
+  // tile range of the row's item in the scorer's concatenated tile space
+  const int items = p.num_seqs * p.row_groups;
+  const int32_t P = __ldg(p.item_start + item), total = __ldg(p.item_start + items);
+  const int32_t tiles = __ldg(p.item_start + item + 1) - P;
   const int C = p.score_ctas;
   const int32_t chunk = total > 0 ? (total + C - 1) / C : 1;
   const int c_lo = tiles > 0 ? P / chunk : 0;
-  const int nslots = tiles > 0 ? min((P + tiles - 1) / chunk - c_lo + 1, kMaxSlots) : 0;
+  const int nslots = tiles > 0 ? min((P + tiles - 1) / chunk - c_lo + 1, kMaxMergeSlots) : 0;
 
   // partial lists of this row: count and global offset of each
   for (int i = tid; i < nslots; i += kMergeThreads) {
@@ -210,15 +184,20 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const __grid_
   if (tid == 0 && mp.valid_count) mp.valid_count[t] = n_out;
 }
 
+template <int kLocal>
+cudaError_t launch_merge_t(const MergeParams& p, int rows, cudaStream_t stream) {
+  const int bytes = static_cast<int>(sizeof(MergeSmem<kLocal>) + 16);
+  cudaError_t e = cudaFuncSetAttribute(topk_merge_kernel<kLocal>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  topk_merge_kernel<kLocal><<<rows, kMergeThreads, bytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
-cudaError_t launch_topk_merge(const MergeParams& p, int rows, cudaStream_t stream) {
+cudaError_t launch_topk_merge(const MergeParams& p, int rows, bool many_rows, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
-  const int bytes = static_cast<int>(sizeof(MergeSmem) + 16);
-  cudaError_t e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e != cudaSuccess) return e;
-  topk_merge_kernel<<<rows, kMergeThreads, bytes, stream>>>(p);
-  return cudaGetLastError();
+  return many_rows ? launch_merge_t<4096>(p, rows, stream) : launch_merge_t<20480>(p, rows, stream);
 }
 
 }  // namespace fp4idx

@@ -74,3 +74,33 @@ def test_long_batched_decode_sampled_rows():
     idx, val, cnt = _run(p, 2048)
     rows = [0, 21, 63]
     compare_topk(p, rows, 2048, idx[rows], val[rows], cnt[rows])
+
+
+def test_causal_prefill_all_rows():
+    # two causal requests (one with an explicit offset), 64 heads: rows see 1.. keys
+    p = wl.make_problem(name="prefill_small", seed=14, fmt=wl.MXFP4, q_lens=[300, 77], k_lens=[300, 500],
+                        num_heads=64, e8m0_range=(120, 134), weights="normal", visibility="causal",
+                        qo_offset=[0, 400])
+    for k in (64, 2048):
+        _check(p, k, sorted_=(k == 64))
+
+
+def test_prefill_32k_causal_sampled_rows():
+    # 32,768 causal rows over 32,768 keys, 64 heads, top-2048
+    p = wl.prefill_32k()
+    idx, val, cnt = _run(p, 2048)
+    rows = [0, 1, 2046, 2047, 2048, 2049, 16383, 16384, 32766, 32767]
+    rows += [int(x) for x in np.random.default_rng(21).integers(0, 32768, size=4)]
+    compare_topk(p, rows, 2048, idx[rows], val[rows], cnt[rows])
+
+
+def test_many_rows_with_one_long_request():
+    # > 4 x SMs rows select the small-buffer merge; the long request's rows
+    # gather partial lists from most scorer CTAs (more than fit in its buffer)
+    q_lens = [4] * 160
+    k_lens = [200_000] + [100] * 159
+    p = wl.make_problem(name="many_rows", seed=15, fmt=wl.MXFP4, q_lens=q_lens, k_lens=k_lens, num_heads=32,
+                        e8m0_range=(120, 134), weights="normal")
+    idx, val, cnt = _run(p, 2048, sorted_=True)
+    rows = [0, 1, 2, 3, 4, 300, 639]
+    compare_topk(p, rows, 2048, idx[rows], val[rows], cnt[rows], sorted_order=True)
