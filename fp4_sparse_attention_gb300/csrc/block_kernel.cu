@@ -13,18 +13,22 @@
 // the last visible key of every row of the item are not computed; their
 // scores are written as -inf.
 //
-// Warp roles (64 + 128 * kGroups threads):
+// Warp roles (96 + 128 * kGroups threads):
 //   warp 0      producer: Q codes of each item by TMA and Q scales by cp.async
 //               (double buffered, one item ahead); per tile the K codes by TMA
-//               (64-byte swizzle) and the K scales by cp.async straight into the
-//               32x4x4 scale atom, into a kStages-deep ring.
-//   warp 1      MMA: TMEM owner.  Q scales -> TMEM once per item, K scales ->
-//               TMEM per tile, two K = 64 block-scaled MMAs per tile into a
-//               triple-buffered accumulator.
-//   warps 2..   epilogue, kGroups groups of four warps (one per TMEM lane
-//               quadrant) taking alternate tiles: tcgen05.ld of the 128
-//               columns, masked max (NaN-propagating), one fp32 store per
-//               (head, row).
+//               (64-byte swizzle) and the page's raw K scales by one bulk copy,
+//               into a kStages-deep ring: a handful of instructions per tile.
+//   warp 1      MMA: TMEM owner; one thread waits for the tile's scales and
+//               a free accumulator and issues two K = 64 block-scaled MMAs
+//               into a triple-buffered accumulator, nothing else.
+//   warp 2      scales: Q scales -> TMEM once per item; per tile the raw K
+//               scales are transposed into the 128-row scale layout (each
+//               row: the 32x4x4 atom line of its lane) and one tcgen05.cp
+//               128x128b/256b moves them to TMEM.
+//   warps 3..   epilogue, one group of four warps (one per TMEM lane
+//               quadrant) per accumulator buffer, so three tiles drain at
+//               once: tcgen05.ld of the 128 columns, masked max
+//               (NaN-propagating), one fp32 store per (head, row).
 //
 // Work split: the tiles of all items are concatenated and cut into one equal
 // contiguous chunk per CTA; every output element is produced by exactly one
@@ -37,11 +41,11 @@
 namespace fp4idx {
 namespace {
 
-constexpr int kStages = 12;
+constexpr int kStages = 16;
 constexpr int kAccBufs = 3;
 constexpr int kKsfSlots = 4;  // K-scale TMEM slots; > kAccBufs (see the MMA loop)
-constexpr int kGroups = 2;
-constexpr int kThreads = 64 + 128 * kGroups;
+constexpr int kGroups = kAccBufs;  // epilogue group e drains accumulator e
+constexpr int kThreads = 96 + 128 * kGroups;  // producer, MMA, scale warp, epilogue groups
 constexpr uint32_t kTmemCols = 512;
 static_assert(kAccBufs < kKsfSlots, "K-scale slot reuse");
 
@@ -60,10 +64,11 @@ struct BlockLayout {
   using F = FmtTraits<FMT>;
   static constexpr uint32_t kCodes = 0;                                // kStages x 8 KB K codes
   static constexpr uint32_t kQ = kCodes + kStages * 8192;              // 2 x 8 KB Q codes
-  static constexpr uint32_t kKsf = kQ + 2 * 8192;                      // kStages x kAtoms x 512
-  static constexpr uint32_t kQsf = kKsf + kStages * F::kAtoms * 512;   // 2 x kAtoms x 512
+  static constexpr uint32_t kKraw = kQ + 2 * 8192;                     // kStages x 128 keys x G raw K scales
+  static constexpr uint32_t kKsf = kKraw + kStages * 128 * F::G;       // kKsfSlots x kAtoms x 2048 (128 rows)
+  static constexpr uint32_t kQsf = kKsf + kKsfSlots * F::kAtoms * 2048;  // 2 x kAtoms x 512
   static constexpr uint32_t kBars = kQsf + 2 * F::kAtoms * 512;
-  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 4;
+  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 4 + kKsfSlots;
   static constexpr uint32_t kState = kBars + kNumBars * 8;
   static constexpr uint32_t kScan = (kState + sizeof(BlockCta) + 15) / 16 * 16;
   static constexpr uint32_t kEnd = kScan + kThreads * 4;
@@ -205,33 +210,30 @@ __device__ __forceinline__ float max3n(float a, float b, float c) {
   return d;
 }
 
-// Max of the 128 columns (four independent chains of three-input max).
-__device__ __forceinline__ float block_max_all(const uint32_t (&v)[128]) {
-  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+// Fold 64 columns into four running maxima (three-input max, four chains).
+__device__ __forceinline__ void block_max_accum(const uint32_t (&v)[64], float (&m)[4]) {
 #pragma unroll
-  for (int i = 0; i < 128; i += 8) {
+  for (int i = 0; i < 64; i += 8) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) m[c] = max3n(m[c], __uint_as_float(v[i + 2 * c]), __uint_as_float(v[i + 2 * c + 1]));
   }
-  return max2n(max2n(m[0], m[1]), max2n(m[2], m[3]));
 }
 
-// Max of the columns n in [lo, hi); -inf when empty.  Masked columns are
+// Same over the columns i of this half with (i - off) in [0, span): off is
+// the first visible column relative to the half.  Masked columns are
 // replaced by -inf by selection, so whatever they hold never reaches the max.
-__device__ __forceinline__ float block_max_range(const uint32_t (&v)[128], int lo, int hi) {
-  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-  const uint32_t span = hi > lo ? static_cast<uint32_t>(hi - lo) : 0u;
+__device__ __forceinline__ void block_max_accum_range(const uint32_t (&v)[64], int off, int span, float (&m)[4]) {
+  const uint32_t n = span > 0 ? static_cast<uint32_t>(span) : 0u;
 #pragma unroll
-  for (int i = 0; i < 128; i += 8) {
+  for (int i = 0; i < 64; i += 8) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const int n0 = i + 2 * c, n1 = n0 + 1;
-      const float a = static_cast<uint32_t>(n0 - lo) < span ? __uint_as_float(v[n0]) : -INFINITY;
-      const float b = static_cast<uint32_t>(n1 - lo) < span ? __uint_as_float(v[n1]) : -INFINITY;
+      const int i0 = i + 2 * c, i1 = i0 + 1;
+      const float a = static_cast<uint32_t>(i0 - off) < n ? __uint_as_float(v[i0]) : -INFINITY;
+      const float b = static_cast<uint32_t>(i1 - off) < n ? __uint_as_float(v[i1]) : -INFINITY;
       m[c] = max3n(m[c], a, b);
     }
   }
-  return max2n(max2n(m[0], m[1]), max2n(m[2], m[3]));
 }
 
 template <int FMT>
@@ -252,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
   auto acce_bar = [&](int a) { return bar0 + 8u * (2 * kStages + kAccBufs + a); };
   auto qfull_bar = [&](uint32_t qb) { return bar0 + 8u * (2 * kStages + 2 * kAccBufs + qb); };
   auto qempty_bar = [&](uint32_t qb) { return bar0 + 8u * (2 * kStages + 2 * kAccBufs + 2 + qb); };
+  auto sfready_bar = [&](int slot) { return bar0 + 8u * (2 * kStages + 2 * kAccBufs + 4 + slot); };
 
   BlockCta* st = reinterpret_cast<BlockCta*>(smem + L::kState);
   int32_t* scan = reinterpret_cast<int32_t*>(smem + L::kScan);
@@ -272,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
   // ---- one-time setup
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 1 + 32);  // expect-tx arrive + one cp.async arrive per producer lane
+      mbar_init(full_bar(s), 1);  // the producer's expect-tx arrive; TMA and bulk copies complete the bytes
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < kAccBufs; ++a) {
@@ -283,6 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
       mbar_init(qfull_bar(qb), 1 + 32);
       mbar_init(qempty_bar(qb), 1);
     }
+    for (int sl = 0; sl < kKsfSlots; ++sl) mbar_init(sfready_bar(sl), 1);
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc<kTmemCols>(smem_u32(&st->tmem_base));
@@ -293,7 +297,9 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
 
   const uint32_t codes_s = smem_u32(smem + L::kCodes);
   const uint32_t q_s = smem_u32(smem + L::kQ);
-  uint8_t* ksf_atoms = smem + L::kKsf;
+  const uint32_t kraw_s = smem_u32(smem + L::kKraw);
+  const uint8_t* kraw = smem + L::kKraw;
+  uint8_t* ksf_rows = smem + L::kKsf;
   uint8_t* qsf_atoms = smem + L::kQsf;
   const int pshift = p.page_shift;
   const int page = p.page_size;
@@ -363,29 +369,20 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
         // cache rows of the two slots (< 2^31 for resolved pages: checked on the host)
         const int32_t row0k = ok0 ? static_cast<int32_t>((static_cast<int64_t>(phys0) * p.num_kv_heads + it.hk) << pshift) : 0;
         const int32_t row1k = ok1 ? static_cast<int32_t>((static_cast<int64_t>(phys1) * p.num_kv_heads + it.hk) << pshift) : 0;
-        const uint32_t bytes = static_cast<uint32_t>((ok0 ? 1 : 0) + (ok1 ? 1 : 0)) * page * kCodeBytes;
+        const uint32_t bytes = static_cast<uint32_t>((ok0 ? 1 : 0) + (ok1 ? 1 : 0)) * page * (kCodeBytes + G);
         const int s = tile_iter % kStages;
         const uint32_t ph = (tile_iter / kStages) & 1u;
-        ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.err) : false, 0);
+        ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait_spin(empty_bar(s), ph ^ 1u, abort_flag, p.err) : false, 0);
         if (!ok) return;
         if (lane == 0) mbar_arrive_expect_tx(full_bar(s), bytes);
         __syncwarp();
-        if (lane < slots && (lane == 0 ? ok0 : ok1))
-          tma_load_2d(codes_s + s * 8192 + ((lane * kCodeBytes) << pshift), &p.tmap_k, 0,
-                      lane == 0 ? row0k : row1k, full_bar(s));
-        // key n = 32q + lane -> atom line `lane`, word q (second atom: scales 4..7)
-        uint8_t* atom = ksf_atoms + s * F::kAtoms * 512 + lane * 16;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int n = 32 * q + lane;
-          const int sl = n >> pshift;
-          if (sl == 0 ? ok0 : ok1) {
-            const uint8_t* src = p.k_scale + static_cast<int64_t>((sl == 0 ? row0k : row1k) + (n & (page - 1))) * G;
-            cp_async_4(smem_u32(atom + 4 * q), src);
-            if constexpr (G == 8) cp_async_4(smem_u32(atom + 512 + 4 * q), src + 4);
-          }
+        if (lane < slots && (lane == 0 ? ok0 : ok1)) {
+          const int32_t rowk = lane == 0 ? row0k : row1k;
+          tma_load_2d(codes_s + s * 8192 + ((lane * kCodeBytes) << pshift), &p.tmap_k, 0, rowk, full_bar(s));
+          // the page's scales are contiguous: [page keys][G]
+          bulk_load(kraw_s + s * (128 * G) + ((lane * G) << pshift), p.k_scale + static_cast<int64_t>(rowk) * G,
+                    static_cast<uint32_t>(page * G), full_bar(s));
         }
-        cp_async_arrive(full_bar(s));
         ++tile_iter;
       }
     });
@@ -400,88 +397,171 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
     __syncwarp();
   } else if (warp == 1) {
     // ================================================================ MMA issuer
-    const uint64_t q_desc0 = desc_kmajor_sw64(q_s);
-    const uint64_t k_desc0 = desc_kmajor_sw64(codes_s);
-    const uint64_t ksf_desc0 = desc_sf_atom(smem_u32(ksf_atoms));
+    // One thread does nothing but wait and issue: an MMA issue holds the
+    // issuing thread for most of the MMA's duration, so any other per-tile
+    // work here would leave the tensor pipe idle.
+    if (lane == 0) {
+      const uint64_t q_desc0 = desc_kmajor_sw64(q_s);
+      const uint64_t k_desc0 = desc_kmajor_sw64(codes_s);
+      uint32_t tile_iter = 0, item_iter = 0;
+      int acc_sel = 0;           // tile_iter % kAccBufs
+      uint32_t acc_phase = 0;    // bit a: phase of accumulator a's next use
+      uint32_t sf_phase = 0;     // bit slot: phase of the scale slot's next use
+      bool ok = true;
+      int last_acc = -1;
+      uint32_t last_acc_phase = 0;
+      block_segments(p, st, [&](int, const BlockItem& it, int lo, int hi) {
+        if (!ok) return;
+        const uint32_t qb = item_iter & 1u;
+        const uint32_t qsf_t = tmem + L::kQsfCol + qb * 8u;
+        const uint64_t adesc = q_desc0 + static_cast<uint64_t>((qb * 8192u) >> 4);
+        // the scale warp copies the item's Q scales before its first tile's
+        // K scales, so that tile's scale barrier covers both
+        for (int j = lo; j < hi && ok; ++j) {
+          if (!tile_computed(it, j)) continue;
+          const int s = tile_iter % kStages;
+          const int slot = tile_iter % kKsfSlots;
+          const int a = acc_sel;
+          const uint32_t aph = (acc_phase >> a) & 1u;
+          // scale slot ready implies the stage's codes landed (the scale warp waited for them)
+          if (!(ok = mbar_wait_spin(sfready_bar(slot), (sf_phase >> slot) & 1u, abort_flag, p.err))) break;
+          sf_phase ^= 1u << slot;
+          if (!(ok = mbar_wait_spin(acce_bar(a), aph ^ 1u, abort_flag, p.err))) break;
+          tc_fence_after();
+          const uint32_t ksf_t = tmem + L::kKsfCol + slot * 8u;
+          const uint32_t d = tmem + L::kAccCol + a * 128u;
+          const uint64_t bdesc = k_desc0 + static_cast<uint64_t>((s * 8192) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            constexpr uint32_t sf1 = F::kScaleVec == 2 ? 2u : 0u;
+            const uint32_t idesc =
+                kk == 0 ? idesc_fp4(128, 128, F::kUe8m0, 0, 0) : idesc_fp4(128, 128, F::kUe8m0, sf1, sf1);
+            const uint32_t col = F::kScaleVec == 2 ? 0u : 4u * kk;
+            tc_mma_fp4<F::kScaleVec>(d, adesc + 2u * kk, bdesc + 2u * kk, idesc, qsf_t + col, ksf_t + col,
+                                     static_cast<uint32_t>(kk));
+          }
+          tc_commit(empty_bar(s));
+          tc_commit(accf_bar(a));
+          last_acc = a;
+          last_acc_phase = aph;
+          acc_phase ^= 1u << a;
+          acc_sel = a == kAccBufs - 1 ? 0 : a + 1;
+          ++tile_iter;
+        }
+        if (!ok) return;
+        // Q buffer and Q-scale slot free once this item's MMAs complete.
+        tc_commit(qempty_bar(qb));
+        ++item_iter;
+      });
+      if (!ok && last_acc >= 0) {
+        // Outstanding MMAs must finish before TMEM is released.
+        volatile int never = 0;
+        mbar_wait(accf_bar(last_acc), last_acc_phase, &never, p.err);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ================================================================ scale warp
+    // Per item: Q scales (atoms written by the producer's cp.async) -> TMEM.
+    // Per tile: raw K scales [128 keys][G] -> 128 rows of the scale layout
+    // (row r holds the 32x4x4 atom line r % 32: the words of keys l, 32+l,
+    // 64+l, 96+l, l = r % 32; NVFP4's K half 1 in the second 16 bytes), one
+    // tcgen05.cp into TMEM slot tile % kKsfSlots, committed to that slot's
+    // barrier.  The slot (TMEM and shared staging) is reused by tile
+    // i + kKsfSlots only after the MMA of tile i completed (its stage's
+    // empty barrier), which also completes the copy that read the staging.
+    const uint64_t ksf_desc0 = desc_sf_rows(smem_u32(ksf_rows));
     const uint64_t qsf_desc0 = desc_sf_atom(smem_u32(qsf_atoms));
     uint32_t tile_iter = 0, item_iter = 0;
     bool ok = true;
-    int last_acc = -1;
-    uint32_t last_acc_phase = 0;
     block_segments(p, st, [&](int, const BlockItem& it, int lo, int hi) {
       if (!ok) return;
       const uint32_t qb = item_iter & 1u, qph = (item_iter >> 1) & 1u;
+      ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(qfull_bar(qb), qph, abort_flag, p.err) : false, 0);
+      if (!ok) return;
       if (lane == 0) {
-        ok = mbar_wait(qfull_bar(qb), qph, abort_flag, p.err);
-        if (ok) {
-          // Q scales were written by cp.async (generic proxy): make them
-          // visible to the tensor core's copy.
-          fence_proxy_async_smem();
-          tc_fence_after();
-          const uint32_t qsf_t = tmem + L::kQsfCol + qb * 8u;
+        // Q scales were written by cp.async (generic proxy): make them
+        // visible to the tensor core's copy.  The previous user of this Q
+        // slot (item - 2) finished: the producer waited for it (qempty)
+        // before loading this item's Q.
+        fence_proxy_async_smem();
+        tc_fence_after();
+        const uint32_t qsf_t = tmem + L::kQsfCol + qb * 8u;
 #pragma unroll
-          for (int at = 0; at < F::kAtoms; ++at)
-            tc_cp_32x128b_warpx4(qsf_t + 4u * at,
-                                 qsf_desc0 + static_cast<uint64_t>(((qb * F::kAtoms + at) * 512) >> 4));
-          const uint64_t adesc = q_desc0 + static_cast<uint64_t>((qb * 8192u) >> 4);
-          for (int j = lo; j < hi && ok; ++j) {
-            if (!tile_computed(it, j)) continue;
-            const int s = tile_iter % kStages;
-            const uint32_t ph = (tile_iter / kStages) & 1u;
-            const int a = tile_iter % kAccBufs;
-            const uint32_t aph = (tile_iter / kAccBufs) & 1u;
-            if (!(ok = mbar_wait(full_bar(s), ph, abort_flag, p.err))) break;
-            // K-scale slot of tile i is i % kKsfSlots: its previous reader, the
-            // MMA of tile i - kKsfSlots, completed before the accumulator of
-            // tile i - 1 could be free (kAccBufs < kKsfSlots).
-            const uint32_t ksf_t = tmem + L::kKsfCol + (tile_iter % kKsfSlots) * 8u;
-            fence_proxy_async_smem();
-#pragma unroll
-            for (int at = 0; at < F::kAtoms; ++at)
-              tc_cp_32x128b_warpx4(ksf_t + 4u * at, ksf_desc0 + static_cast<uint64_t>(((s * F::kAtoms + at) * 512) >> 4));
-            if (!(ok = mbar_wait(acce_bar(a), aph ^ 1u, abort_flag, p.err))) break;
-            tc_fence_after();
-            const uint32_t d = tmem + L::kAccCol + a * 128u;
-            const uint64_t bdesc = k_desc0 + static_cast<uint64_t>((s * 8192) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-              constexpr uint32_t sf1 = F::kScaleVec == 2 ? 2u : 0u;
-              const uint32_t idesc =
-                  kk == 0 ? idesc_fp4(128, 128, F::kUe8m0, 0, 0) : idesc_fp4(128, 128, F::kUe8m0, sf1, sf1);
-              const uint32_t col = F::kScaleVec == 2 ? 0u : 4u * kk;
-              tc_mma_fp4<F::kScaleVec>(d, adesc + 2u * kk, bdesc + 2u * kk, idesc, qsf_t + col, ksf_t + col,
-                                       static_cast<uint32_t>(kk));
-            }
-            tc_commit(empty_bar(s));
-            tc_commit(accf_bar(a));
-            last_acc = a;
-            last_acc_phase = aph;
-            ++tile_iter;
-          }
-          // Q buffer and Q-scale slot free once this item's MMAs complete.
-          tc_commit(qempty_bar(qb));
-        }
+        for (int at = 0; at < F::kAtoms; ++at)
+          tc_cp_32x128b_warpx4(qsf_t + 4u * at, qsf_desc0 + static_cast<uint64_t>(((qb * F::kAtoms + at) * 512) >> 4));
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+      __syncwarp();
+      for (int j = lo; j < hi; ++j) {
+        if (!tile_computed(it, j)) continue;
+        const int s = tile_iter % kStages;
+        const uint32_t ph = (tile_iter / kStages) & 1u;
+        const int slot = tile_iter % kKsfSlots;
+        bool got = false;
+        if (lane == 0) {
+          got = mbar_wait_spin(full_bar(s), ph, abort_flag, p.err);
+          if (got && tile_iter >= static_cast<uint32_t>(kKsfSlots)) {
+            const uint32_t u = tile_iter - kKsfSlots;  // previous user of the slot
+            got = mbar_wait(empty_bar(u % kStages), (u / kStages) & 1u, abort_flag, p.err);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, got, 0);
+        if (!ok) break;
+        {
+          const uint8_t* raw = kraw + s * (128 * G);
+          uint8_t* rows = ksf_rows + slot * (F::kAtoms * 2048);
+          if constexpr (G == 4) {
+            const uint32_t* r32 = reinterpret_cast<const uint32_t*>(raw);
+            const uint4 v = make_uint4(r32[lane], r32[32 + lane], r32[64 + lane], r32[96 + lane]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(rows + (32 * q + lane) * 16) = v;
+          } else {
+            const uint2* r64 = reinterpret_cast<const uint2*>(raw);
+            const uint2 a0 = r64[lane], a1 = r64[32 + lane], a2 = r64[64 + lane], a3 = r64[96 + lane];
+            const uint4 lo4 = make_uint4(a0.x, a1.x, a2.x, a3.x), hi4 = make_uint4(a0.y, a1.y, a2.y, a3.y);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              *reinterpret_cast<uint4*>(rows + (32 * q + lane) * 16) = lo4;
+              *reinterpret_cast<uint4*>(rows + 2048 + (32 * q + lane) * 16) = hi4;
+            }
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t ksf_t = tmem + L::kKsfCol + slot * 8u;
+          const uint64_t sdesc = ksf_desc0 + static_cast<uint64_t>((slot * F::kAtoms * 2048) >> 4);
+          if constexpr (G == 4) tc_cp_128x128b(ksf_t, sdesc);
+          else tc_cp_128x256b(ksf_t, sdesc);
+          tc_commit(sfready_bar(slot));
+        }
+        __syncwarp();
+        ++tile_iter;
+      }
       ++item_iter;
     });
-    if (!ok && last_acc >= 0 && lane == 0) {
-      // Outstanding MMAs must finish before TMEM is released.
+    if (lane == 0) {
+      // copies still in flight must land before TMEM is released
       volatile int never = 0;
-      mbar_wait(accf_bar(last_acc), last_acc_phase, &never, p.err);
+      const uint32_t first = tile_iter > static_cast<uint32_t>(kKsfSlots) ? tile_iter - kKsfSlots : 0;
+      for (uint32_t u = first; u < tile_iter; ++u)
+        mbar_wait(sfready_bar(u % kKsfSlots), (u / kKsfSlots) & 1u, &never, p.err);
     }
     __syncwarp();
   } else {
     // ================================================================ epilogue
-    const int e = (warp - 2) >> 2;  // group: takes the tiles with tile_iter % kGroups == e
-    Group<128, -1> g{static_cast<int>(threadIdx.x) - 64 - e * 128, 1 + e};
+    const int e = (warp - 3) >> 2;  // group e owns accumulator e: tiles with tile_iter % kAccBufs == e
+    Group<128, -1> g{static_cast<int>(threadIdx.x) - 96 - e * 128, 1 + e};
     const int quad = warp & 3;
     const int m = quad * 32 + lane;  // TMEM lane = MMA row
     const int h_local = m >> rt_shift;
     const int t_local = m & ((1 << rt_shift) - 1);
-    uint32_t tile_iter = 0;
+    int sel = 0;              // tile_iter % kAccBufs, kept incrementally
+    uint32_t own_phase = 0;   // phase of accumulator e for this group's next tile
     bool ok = true;
     const int64_t T = p.num_rows;
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + L::kAccCol + e * 128u;
     block_segments(p, st, [&](int, const BlockItem& it, int lo, int hi) {
       const int32_t t = it.row0 + t_local;
       const bool row_valid = t_local < it.nrows && t < p.num_rows;
@@ -492,49 +572,55 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
       for (int j = lo; j < hi; ++j) {
         bool owner;
         if (tile_computed(it, j)) {
-          owner = static_cast<int>(tile_iter % kGroups) == e;
+          owner = sel == e;
           if (owner) {
-            const int a = tile_iter % kAccBufs;
-            const uint32_t aph = (tile_iter / kAccBufs) & 1u;
-            if (g.tid == 0 && ok && !mbar_wait(accf_bar(a), aph, abort_flag, p.err)) st->abort = 1;
+            // page ids of the tile, loaded while the accumulator is awaited
+            const int32_t lp0 = j * slots;
+            int32_t ph_id[2] = {0, 0};
+            for (int sl = 0; sl < slots; ++sl)
+              if (((lp0 + sl) << pshift) < it.k_len) ph_id[sl] = __ldg(p.block_table + it.table_base + lp0 + sl);
+            if (g.tid == 0 && ok && !mbar_wait_spin(accf_bar(e), own_phase, abort_flag, p.err)) st->abort = 1;
+            own_phase ^= 1u;
             g.sync();
             // warp-uniform: tcgen05.ld below is a whole-warp instruction
             ok = __all_sync(0xffffffffu, ok && !*abort_flag);
             if (ok) {
-              tc_fence_after();
-              uint32_t v[128];
-              const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + L::kAccCol + a * 128u;
-#pragma unroll
-              for (int c = 0; c < 128; c += 32) {
-                uint32_t part[32];
-                tmem_ld_x32(taddr + c, part);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[c + i] = part[i];
-              }
-              tmem_wait_ld();
-              reg_fence(v);
-              tc_fence_before();
-              mbar_arrive(acce_bar(a));
               // columns [lo_c, hi_c) are visible keys of this row in pages that resolved
               int lo_c = 0;
               int hi_c = vis - j * kTileKeys;
               hi_c = hi_c < 0 ? 0 : (hi_c > kTileKeys ? kTileKeys : hi_c);
-              const int32_t lp0 = j * slots;
               for (int sl = 0; sl < slots; ++sl) {
                 if (((lp0 + sl) << pshift) >= it.k_len) break;
-                const int32_t ph_id = __ldg(p.block_table + it.table_base + lp0 + sl);
-                if (ph_id < 0 || ph_id >= p.num_pages) {
+                if (ph_id[sl] < 0 || ph_id[sl] >= p.num_pages) {
                   if (sl == 0) lo_c = page;  // 64-key pages: the second half may still count
                   else hi_c = min(hi_c, page);
                   if (slots == 1) hi_c = 0;
                 }
               }
-              const bool full = lo_c == 0 && hi_c == kTileKeys;
-              const float r = __all_sync(0xffffffffu, full) ? block_max_all(v) : block_max_range(v, lo_c, hi_c);
+              const bool full = __all_sync(0xffffffffu, lo_c == 0 && hi_c == kTileKeys);
+              tc_fence_after();
+              // two halves of 64 columns keep the live registers low; the
+              // accumulator is released after the second half is loaded
+              float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                uint32_t v[64];
+                tmem_ld_x32(taddr + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                tmem_ld_x32(taddr + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                tmem_wait_ld();
+                reg_fence(v);
+                if (half == 1) {
+                  tc_fence_before();
+                  mbar_arrive(acce_bar(e));
+                }
+                if (full) block_max_accum(v, mx);
+                else block_max_accum_range(v, lo_c - 64 * half, hi_c - lo_c, mx);
+              }
+              const float r = max2n(max2n(mx[0], mx[1]), max2n(mx[2], mx[3]));
               if (row_valid && j < p.ktiles) out[static_cast<int64_t>(j) * T] = r;
             }
           }
-          ++tile_iter;
+          sel = sel == kAccBufs - 1 ? 0 : sel + 1;
         } else {
           owner = e == 0;  // a tile nothing is computed for: group 0 writes its -inf
         }

@@ -62,6 +62,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same test without a suspend-time hint: returns at once (used for polls on
+// the critical path, where a suspended thread's wake-up would add latency).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded spin on mbar_test_wait; same contract as mbar_wait below.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile int* abort,
+                                               uint32_t* err) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      atomicOr(err, kErrTimeout);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
 // Wait for the phase of `parity` to complete.  Gives up after kWaitLimitNs or
 // when another thread has raised *abort; on a time-out it records
 // kErrTimeout and raises *abort so the rest of the CTA stops waiting too.
@@ -149,6 +180,15 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 // to all four lane quadrants.
 __device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+// 128 rows of 16 B (128x128b) or 32 B (128x256b) from shared memory into
+// TMEM lanes 0..127, four or eight columns.  The source is the canonical
+// unswizzled layout of desc_sf_rows().
+__device__ __forceinline__ void tc_cp_128x128b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 // D[tmem] (+)= A[smem] * B[smem]^T with per-block scales from TMEM.
 // kScaleVec 2: MXFP4 (ue8m0 per 32 values); 4: NVFP4 (ue4m3 per 16 values).
@@ -248,6 +288,16 @@ __device__ __forceinline__ uint64_t desc_sf_atom(uint32_t saddr) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
   d |= static_cast<uint64_t>(128 >> 4) << 16;   // leading byte offset
+  d |= static_cast<uint64_t>(128 >> 4) << 32;   // stride byte offset: 8 rows * 16 B
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+// 128 rows x 32 B for tcgen05.cp 128x128b / 128x256b, unswizzled: row r's
+// first 16 B at r*16, its second 16 B at 2048 + r*16.
+__device__ __forceinline__ uint64_t desc_sf_rows(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(2048 >> 4) << 16;  // leading byte offset: the second 16-byte column
   d |= static_cast<uint64_t>(128 >> 4) << 32;   // stride byte offset: 8 rows * 16 B
   d |= static_cast<uint64_t>(1) << 46;
   return d;
