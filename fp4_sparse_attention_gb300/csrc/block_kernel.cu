@@ -284,7 +284,10 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
     }
     for (uint32_t qb = 0; qb < 2; ++qb) {
       mbar_init(qfull_bar(qb), 1 + 32);
-      mbar_init(qempty_bar(qb), 1);
+      // freed by the MMA thread's commit (its MMAs read Q) and the scale
+      // warp's arrive (it has seen this load), so a buffer is never reloaded
+      // before both consumers observed the previous load's phase
+      mbar_init(qempty_bar(qb), 2);
     }
     for (int sl = 0; sl < kKsfSlots; ++sl) mbar_init(sfready_bar(sl), 1);
     fence_barrier_init();
@@ -372,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
         const uint32_t bytes = static_cast<uint32_t>((ok0 ? 1 : 0) + (ok1 ? 1 : 0)) * page * (kCodeBytes + G);
         const int s = tile_iter % kStages;
         const uint32_t ph = (tile_iter / kStages) & 1u;
-        ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait_spin(empty_bar(s), ph ^ 1u, abort_flag, p.err) : false, 0);
+        ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.err) : false, 0);
         if (!ok) return;
         if (lane == 0) mbar_arrive_expect_tx(full_bar(s), bytes);
         __syncwarp();
@@ -424,9 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
           const int a = acc_sel;
           const uint32_t aph = (acc_phase >> a) & 1u;
           // scale slot ready implies the stage's codes landed (the scale warp waited for them)
-          if (!(ok = mbar_wait_spin(sfready_bar(slot), (sf_phase >> slot) & 1u, abort_flag, p.err))) break;
+          if (!(ok = mbar_wait(sfready_bar(slot), (sf_phase >> slot) & 1u, abort_flag, p.err))) break;
           sf_phase ^= 1u << slot;
-          if (!(ok = mbar_wait_spin(acce_bar(a), aph ^ 1u, abort_flag, p.err))) break;
+          if (!(ok = mbar_wait(acce_bar(a), aph ^ 1u, abort_flag, p.err))) break;
           tc_fence_after();
           const uint32_t ksf_t = tmem + L::kKsfCol + slot * 8u;
           const uint32_t d = tmem + L::kAccCol + a * 128u;
@@ -483,13 +486,18 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
         // Q scales were written by cp.async (generic proxy): make them
         // visible to the tensor core's copy.  The previous user of this Q
         // slot (item - 2) finished: the producer waited for it (qempty)
-        // before loading this item's Q.
-        fence_proxy_async_smem();
-        tc_fence_after();
-        const uint32_t qsf_t = tmem + L::kQsfCol + qb * 8u;
+        // before loading this item's Q.  Copied only when some tile of the
+        // segment is computed (otherwise no MMA reads them, and no barrier
+        // would track the copy).
+        if (tile_computed(it, lo)) {
+          fence_proxy_async_smem();
+          tc_fence_after();
+          const uint32_t qsf_t = tmem + L::kQsfCol + qb * 8u;
 #pragma unroll
-        for (int at = 0; at < F::kAtoms; ++at)
-          tc_cp_32x128b_warpx4(qsf_t + 4u * at, qsf_desc0 + static_cast<uint64_t>(((qb * F::kAtoms + at) * 512) >> 4));
+          for (int at = 0; at < F::kAtoms; ++at)
+            tc_cp_32x128b_warpx4(qsf_t + 4u * at, qsf_desc0 + static_cast<uint64_t>(((qb * F::kAtoms + at) * 512) >> 4));
+        }
+        mbar_arrive(qempty_bar(qb));
       }
       __syncwarp();
       for (int j = lo; j < hi; ++j) {
@@ -499,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
         const int slot = tile_iter % kKsfSlots;
         bool got = false;
         if (lane == 0) {
-          got = mbar_wait_spin(full_bar(s), ph, abort_flag, p.err);
+          got = mbar_wait(full_bar(s), ph, abort_flag, p.err);
           if (got && tile_iter >= static_cast<uint32_t>(kKsfSlots)) {
             const uint32_t u = tile_iter - kKsfSlots;  // previous user of the slot
             got = mbar_wait(empty_bar(u % kStages), (u / kStages) & 1u, abort_flag, p.err);
@@ -579,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
             int32_t ph_id[2] = {0, 0};
             for (int sl = 0; sl < slots; ++sl)
               if (((lp0 + sl) << pshift) < it.k_len) ph_id[sl] = __ldg(p.block_table + it.table_base + lp0 + sl);
-            if (g.tid == 0 && ok && !mbar_wait_spin(accf_bar(e), own_phase, abort_flag, p.err)) st->abort = 1;
+            if (g.tid == 0 && ok && !mbar_wait(accf_bar(e), own_phase, abort_flag, p.err)) st->abort = 1;
             own_phase ^= 1u;
             g.sync();
             // warp-uniform: tcgen05.ld below is a whole-warp instruction

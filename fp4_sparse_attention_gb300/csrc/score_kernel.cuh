@@ -9,15 +9,19 @@
 // R rows x H heads of one request on N (TMEM columns).  The head sum then is
 // a serial loop inside one thread: thread = key, no shuffles.
 //
-// Warp roles (96 + 128*R threads):
+// Warp roles (128 + 128*R threads):
 //   warp 0 and the last warp: producers, each owning alternate tiles:
 //             resolve pages through the block table, issue the TMA gather of
-//             K codes (64-byte swizzle) and the bulk copy of K scales into a
-//             kStages-deep shared-memory ring; warp 0 also loads Q per item.
-//   warp 1    MMA: owns the TMEM allocation, rewrites K / Q scales into the
-//             32x4x4 scale-factor atom, copies them to TMEM (tcgen05.cp) and
-//             issues two K=64 MMAs per tile into a double-buffered accumulator.
-//   warps 2.. epilogue, one group of four warps (one warp per TMEM lane
+//             K codes (64-byte swizzle) and one bulk copy of each page's raw
+//             scales into a kStages-deep shared-memory ring; warp 0 also
+//             loads Q per item (double buffered).
+//   warp 1    MMA: owns the TMEM allocation; one thread waits for a tile's
+//             scales and a free accumulator and issues two K=64 MMAs into a
+//             triple-buffered fp32 accumulator, nothing else (an MMA issue
+//             holds its thread, so other work there idles the tensor pipe).
+//   warp 2    scales: Q scales -> 32x4x4 atoms -> TMEM per item; per tile
+//             the raw K scales -> 128-row scale layout -> one tcgen05.cp.
+//   warps 3.. epilogue, one group of four warps (one per TMEM lane
 //             quadrant) per query row of the item: tcgen05.ld of the row's
 //             H accumulator columns, ReLU * w summed over heads (packed fp32x2
 //             FMAs, four independent chains), visibility mask, then either the
@@ -65,29 +69,33 @@ struct RowState {  // epilogue view of the current item's rows
 
 template <int H, int R, int FMT, int MODE>
 struct ScoreLayout {
+  static constexpr int G = FmtTraits<FMT>::G;
+  static constexpr int kAtoms = FmtTraits<FMT>::kAtoms;
   // K-tile ring depth.  A loaded HBM round trip for a random page is ~2 us,
   // so ~100+ KB must be in flight per SM; the ring takes most of shared memory.
-  static constexpr int kStages = 20;
+  static constexpr int kStages = FMT == 0 ? 20 : 18;
   static constexpr int kGroups = R;  // epilogue groups, one query row each
-  // warp 0 and the last warp: producers (alternate tiles); warp 1: MMA
-  static constexpr int kProducer2Warp = 2 + 4 * kGroups;
-  static constexpr int kThreads = 96 + kEpiThreads * kGroups;
+  // warp 0 and the last warp: producers (alternate tiles); warp 1: MMA;
+  // warp 2: scales; warps 3 .. 3 + 4R - 1: epilogue
+  static constexpr int kEpiWarp0 = 3;
+  static constexpr int kProducer2Warp = kEpiWarp0 + 4 * kGroups;
+  static constexpr int kThreads = 128 + kEpiThreads * kGroups;
   static_assert(kStages % 2 == 0, "the two producers own alternate stages");
   static constexpr int N = H * R;
   static_assert(N % 16 == 0 && N >= 16 && N <= 128, "MMA N");
-  static constexpr int G = FmtTraits<FMT>::G;
-  static constexpr int kAtoms = FmtTraits<FMT>::kAtoms;
+  // K-scale slots (TMEM and shared staging): tile i uses slot i % kSfaSlots
+  static constexpr int kSfaSlots = 4;
   static constexpr uint32_t kCodes = 0;                                  // kStages x 8 KB
-  static constexpr uint32_t kQ = kCodes + kStages * 8192;                // N x 64 B
   static constexpr uint32_t kQBytes = ((N * 64 + 1023) / 1024) * 1024;
-  static constexpr uint32_t kSfa = kQ + kQBytes;                         // kStages x kAtoms x 512
-  static constexpr uint32_t kSfb = kSfa + kStages * kAtoms * 512;        // kAtoms x 512
-  static constexpr uint32_t kBars = kSfb + kAtoms * 512;                 // mbarriers
-  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 2;
+  static constexpr uint32_t kQ = kCodes + kStages * 8192;                // 2 x N x 64 B (double buffered)
+  static constexpr uint32_t kKraw = kQ + 2 * kQBytes;                    // kStages x 128 keys x G raw K scales
+  static constexpr uint32_t kSfaRows = kKraw + kStages * 128 * G;        // kSfaSlots x kAtoms x 2048 (128 rows)
+  static constexpr uint32_t kSfb = kSfaRows + kSfaSlots * kAtoms * 2048; // 2 x kAtoms x 512 Q-scale atoms
+  static constexpr uint32_t kBars = kSfb + 2 * kAtoms * 512;             // mbarriers
+  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 4 + kSfaSlots;
   static constexpr uint32_t kState = kBars + kNumBars * 8;
   static constexpr uint32_t kRows = (kState + sizeof(CtaState) + 15) / 16 * 16;
-  static constexpr uint32_t kW = (kRows + sizeof(RowState<R>) + 15) / 16 * 16;  // N floats
-  static constexpr uint32_t kScan = kW + N * 4;                                  // kThreads ints
+  static constexpr uint32_t kScan = (kRows + sizeof(RowState<R>) + 15) / 16 * 16;  // kThreads ints
   static constexpr uint32_t kScratch = kScan + kThreads * 4;                      // per group
   static constexpr uint32_t kHist = (kScratch + kGroups * sizeof(SelectScratch) + 15) / 16 * 16;
   static constexpr uint32_t kEnd = kHist + (MODE == kModeTopk ? R * kHistBins * 2 : 0);
@@ -96,11 +104,6 @@ struct ScoreLayout {
   static constexpr uint32_t kAccCol = 0;                  // kAccBufs accumulators of 128 columns
   static constexpr uint32_t kSfbCol = 128 * kAccBufs;     // two Q-scale slots of 8 columns
   static constexpr uint32_t kSfaCol = kSfbCol + 16;       // kSfaSlots K-scale slots of 8 columns
-  // K-scale TMEM slot of tile i is i % kSfaSlots; its previous reader, the MMA
-  // of tile i - kSfaSlots, has completed once the accumulator of tile i-1 was
-  // free (kAccBufs < kSfaSlots), which precedes the copy into the slot.
-  static constexpr int kSfaSlots = 4;
-  static_assert(kAccBufs < kSfaSlots, "scale slot reuse");
   static_assert(kSfaCol + 8 * kSfaSlots <= kTmemCols, "TMEM columns");
 };
 
@@ -255,20 +258,6 @@ __device__ __forceinline__ void for_each_segment(const ScoreParams& p, const Cta
 // 512-byte atom whose 16-byte line l holds, for row groups j = 0..3, the
 // four scale bytes of row 32j + l.
 // ---------------------------------------------------------------------------
-template <int FMT>
-__device__ __forceinline__ void k_scale_atoms(const uint8_t* raw, uint8_t* atoms, int lane) {
-  if constexpr (FMT == 0) {  // raw: [128 keys][4]
-    const uint32_t* r32 = reinterpret_cast<const uint32_t*>(raw);
-    uint4 v = make_uint4(r32[lane], r32[32 + lane], r32[64 + lane], r32[96 + lane]);
-    *reinterpret_cast<uint4*>(atoms + lane * 16) = v;
-  } else {  // raw: [128 keys][8]; atom 0 = scales 0..3, atom 1 = scales 4..7
-    const uint2* r64 = reinterpret_cast<const uint2*>(raw);
-    const uint2 a = r64[lane], b = r64[32 + lane], c = r64[64 + lane], d = r64[96 + lane];
-    *reinterpret_cast<uint4*>(atoms + lane * 16) = make_uint4(a.x, b.x, c.x, d.x);
-    *reinterpret_cast<uint4*>(atoms + 512 + lane * 16) = make_uint4(a.y, b.y, c.y, d.y);
-  }
-}
-
 // Q scales of the item's rows (B row n = r*H + h) into the atom layout.
 template <int H, int R, int FMT>
 __device__ __forceinline__ void q_scale_atoms(const ScoreParams& p, const ItemInfo& it, uint8_t* atoms,
@@ -298,22 +287,19 @@ __device__ __forceinline__ void q_scale_atoms(const ScoreParams& p, const ItemIn
     *reinterpret_cast<uint4*>(atoms + 512 + lane * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
 }
 
-// sum_h w[h] * max(v[h], 0) with packed fp32x2 FMAs in four independent
-// chains, given hw2[i] = (w[2i]/2, w[2i+1]/2).  The ReLU is taken as
-// x + |x| = 2*max(x, 0) (one add with an absolute-value operand, on the FMA
-// pipe): (w/2)*(x+|x|) is exactly w*max(x,0), so every FMA rounds the same
-// value as w*max(x,0) would; NaN stays NaN.
+// sum_h w[h] * max(v[h], 0): the ReLU as a NaN-propagating max per value,
+// then packed fp32x2 FMAs with w2[i] = (w[2i], w[2i+1]) in four independent
+// chains.
 template <int H>
-__device__ __forceinline__ float weighted_relu_reg(const uint32_t (&v)[H], const float2 (&hw2)[H / 2]) {
+__device__ __forceinline__ float weighted_relu_reg(const uint32_t (&v)[H], const float2 (&w2)[H / 2]) {
   constexpr int kChains = H >= 16 ? 4 : 2;
   float2 acc[kChains];
 #pragma unroll
   for (int c = 0; c < kChains; ++c) acc[c] = make_float2(0.0f, 0.0f);
 #pragma unroll
   for (int i = 0; i < H / 2; ++i) {
-    const float a = __uint_as_float(v[2 * i]), b = __uint_as_float(v[2 * i + 1]);
-    const float2 x = __fadd2_rn(make_float2(a, b), make_float2(fabsf(a), fabsf(b)));
-    acc[i % kChains] = __ffma2_rn(hw2[i], x, acc[i % kChains]);
+    const float2 x = make_float2(relu_nan(__uint_as_float(v[2 * i])), relu_nan(__uint_as_float(v[2 * i + 1])));
+    acc[i % kChains] = __ffma2_rn(w2[i], x, acc[i % kChains]);
   }
 #pragma unroll
   for (int c = 1; c < kChains; ++c) acc[0] = __fadd2_rn(acc[0], acc[c]);
@@ -325,27 +311,6 @@ __device__ __forceinline__ float weighted_relu_reg(const uint32_t (&v)[H], const
 __device__ __forceinline__ uint32_t ordered_bits(float v) {
   const uint32_t u = __float_as_uint(v + 0.0f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-template <int H>
-__device__ __forceinline__ float weighted_relu(const uint32_t* v, const float* w) {
-  constexpr int kChains = H >= 16 ? 4 : 2;
-  float2 acc[kChains];
-#pragma unroll
-  for (int c = 0; c < kChains; ++c) acc[c] = make_float2(0.0f, 0.0f);
-#pragma unroll
-  for (int h = 0; h < H; h += 4) {
-    const float4 ww = *reinterpret_cast<const float4*>(w + h);
-    const float2 x0 = make_float2(relu_nan(__uint_as_float(v[h])), relu_nan(__uint_as_float(v[h + 1])));
-    const float2 x1 =
-        make_float2(relu_nan(__uint_as_float(v[h + 2])), relu_nan(__uint_as_float(v[h + 3])));
-    const int c = (h / 2) % kChains;
-    acc[c] = __ffma2_rn(make_float2(ww.x, ww.y), x0, acc[c]);
-    acc[c + 1] = __ffma2_rn(make_float2(ww.z, ww.w), x1, acc[c + 1]);
-  }
-#pragma unroll
-  for (int c = 1; c < kChains; ++c) acc[0] = __fadd2_rn(acc[0], acc[c]);
-  return acc[0].x + acc[0].y;
 }
 
 // Keep the keys >= T of cand[0, n) in place (order not kept); returns the
@@ -393,7 +358,7 @@ __device__ int compact_keep_ge(const G& g, uint64_t* cand, int n, uint64_t T, Se
 // The kernel.
 // ---------------------------------------------------------------------------
 template <int H, int R, int FMT, int MODE>
-__global__ void __launch_bounds__(96 + kEpiThreads * R, 1) score_kernel(const __grid_constant__ ScoreParams p) {
+__global__ void __launch_bounds__(128 + kEpiThreads * R, 1) score_kernel(const __grid_constant__ ScoreParams p) {
   using L = ScoreLayout<H, R, FMT, MODE>;
   constexpr int kThreads = L::kThreads;
   using F = FmtTraits<FMT>;
@@ -412,12 +377,12 @@ __global__ void __launch_bounds__(96 + kEpiThreads * R, 1) score_kernel(const __
   auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
   auto accf_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
   auto acce_bar = [&](int a) { return bar0 + 8u * (2 * kStages + kAccBufs + a); };
-  const uint32_t qfull_bar = bar0 + 8u * (2 * kStages + 2 * kAccBufs);
-  const uint32_t qempty_bar = bar0 + 8u * (2 * kStages + 2 * kAccBufs + 1);
+  auto qfull_bar = [&](uint32_t qb) { return bar0 + 8u * (2 * kStages + 2 * kAccBufs + qb); };
+  auto qempty_bar = [&](uint32_t qb) { return bar0 + 8u * (2 * kStages + 2 * kAccBufs + 2 + qb); };
+  auto sfready_bar = [&](int slot) { return bar0 + 8u * (2 * kStages + 2 * kAccBufs + 4 + slot); };
 
   CtaState* st = reinterpret_cast<CtaState*>(smem + L::kState);
   RowState<R>* rs = reinterpret_cast<RowState<R>*>(smem + L::kRows);
-  float* w_s = reinterpret_cast<float*>(smem + L::kW);
   int32_t* scan = reinterpret_cast<int32_t*>(smem + L::kScan);
   SelectScratch* sc = reinterpret_cast<SelectScratch*>(smem + L::kScratch);
   uint32_t* hist_words = reinterpret_cast<uint32_t*>(smem + L::kHist);
@@ -446,15 +411,21 @@ __global__ void __launch_bounds__(96 + kEpiThreads * R, 1) score_kernel(const __
   // ---- one-time setup
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 1 + 32);  // producer's expect-tx arrive + one cp.async arrive per lane
+      mbar_init(full_bar(s), 1);  // the producer's expect-tx arrive; TMA and bulk copies complete the bytes
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < kAccBufs; ++a) {
       mbar_init(accf_bar(a), 1);
       mbar_init(acce_bar(a), L::kGroups * kEpiThreads);
     }
-    mbar_init(qfull_bar, 1);
-    mbar_init(qempty_bar, 1);
+    for (uint32_t qb = 0; qb < 2; ++qb) {
+      mbar_init(qfull_bar(qb), 1);
+      // freed by the MMA thread's commit (its MMAs read Q) and the scale
+      // warp's arrive (it has seen this load), so a buffer is never reloaded
+      // before both consumers observed the previous load's phase
+      mbar_init(qempty_bar(qb), 2);
+    }
+    for (int sl = 0; sl < L::kSfaSlots; ++sl) mbar_init(sfready_bar(sl), 1);
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc<kTmemCols>(smem_u32(&st->tmem_base));
@@ -465,7 +436,9 @@ __global__ void __launch_bounds__(96 + kEpiThreads * R, 1) score_kernel(const __
 
   const uint32_t codes_s = smem_u32(smem + L::kCodes);
   const uint32_t q_s = smem_u32(smem + L::kQ);
-  uint8_t* sfa_atoms = smem + L::kSfa;
+  const uint32_t kraw_s = smem_u32(smem + L::kKraw);
+  const uint8_t* kraw = smem + L::kKraw;
+  uint8_t* sfa_rows = smem + L::kSfaRows;
   uint8_t* sfb_atoms = smem + L::kSfb;
 
   if (warp == 0 || warp == L::kProducer2Warp) {
@@ -473,8 +446,8 @@ __global__ void __launch_bounds__(96 + kEpiThreads * R, 1) score_kernel(const __
     // Each producer warp walks every tile and issues the even (warp 0) or odd
     // (last warp) ones.  Lane l caches the physical id of logical page base+l
     // (and of the next 32, prefetched); for each tile the lanes sl < slots
-    // pick up the id of page sl and issue that page's code and scale copies
-    // together, one warp instruction per copy type.
+    // pick up the id of page sl and issue that page's code copy (TMA) and its
+    // raw scale copy (one bulk copy of the page's contiguous scales).
     const uint32_t pidx = warp == 0 ? 0u : 1u;
     uint32_t tile_iter = 0, item_iter = 0;
     bool ok = true;
@@ -488,11 +461,12 @@ __global__ void __launch_bounds__(96 + kEpiThreads * R, 1) score_kernel(const __
     for_each_segment<MODE, R>(p, st, [&](int, const ItemInfo& it, int lo, int hi, int) {
       if (!ok) return;
       if (pidx == 0) {
-        ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(qempty_bar, (item_iter & 1u) ^ 1u, abort_flag, p.err) : false, 0);
+        const uint32_t qb = item_iter & 1u, qph = (item_iter >> 1) & 1u;
+        ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(qempty_bar(qb), qph ^ 1u, abort_flag, p.err) : false, 0);
         if (!ok) return;
         if (lane == 0) {
-          mbar_arrive_expect_tx(qfull_bar, N * kCodeBytes);
-          tma_load_3d(q_s, &p.tmap_q, 0, 0, it.row0, qfull_bar);
+          mbar_arrive_expect_tx(qfull_bar(qb), N * kCodeBytes);
+          tma_load_3d(q_s + qb * L::kQBytes, &p.tmap_q, 0, 0, it.row0, qfull_bar(qb));
         }
       }
       ++item_iter;
@@ -526,89 +500,67 @@ __global__ void __launch_bounds__(96 + kEpiThreads * R, 1) score_kernel(const __
         const bool ok1 = slots == 2 && page_ok(1, phys1);
         if (lane < slots && ((lp0 + lane) << pshift) < it.k_len && !(lane == 0 ? ok0 : ok1))
           atomicOr(p.err, kErrPageRange);
-        const uint32_t bytes = static_cast<uint32_t>((ok0 ? 1 : 0) + (ok1 ? 1 : 0)) * page * kCodeBytes;
+        const uint32_t bytes = static_cast<uint32_t>((ok0 ? 1 : 0) + (ok1 ? 1 : 0)) * page * (kCodeBytes + G);
         const int s = tile_iter % kStages;
         const uint32_t ph = (tile_iter / kStages) & 1u;
         ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.err) : false, 0);
         if (!ok) return;
         if (lane == 0) mbar_arrive_expect_tx(full_bar(s), bytes);
         __syncwarp();
-        if (lane < slots && (lane == 0 ? ok0 : ok1))
-          tma_load_2d(codes_s + s * 8192 + ((lane * kCodeBytes) << pshift), &p.tmap_k, 0,
-                      (lane == 0 ? phys0 : phys1) << pshift, full_bar(s));
-        // K scales straight into the scale-factor atom: key m = 32q + lane goes
-        // to atom line `lane`, word q (and the second atom for scales 4..7).
-        uint8_t* atom = sfa_atoms + s * F::kAtoms * 512 + lane * 16;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int m = 32 * q + lane;
-          const int sl = m >> pshift;
-          if (sl == 0 ? ok0 : ok1) {
-            const uint8_t* src = p.k_scale + ((static_cast<int64_t>(sl == 0 ? phys0 : phys1) << pshift) + (m & (page - 1))) * G;
-            cp_async_4(smem_u32(atom + 4 * q), src);
-            if constexpr (G == 8) cp_async_4(smem_u32(atom + 512 + 4 * q), src + 4);
-          }
+        if (lane < slots && (lane == 0 ? ok0 : ok1)) {
+          const int32_t row = (lane == 0 ? phys0 : phys1) << pshift;  // cache row (one K head)
+          tma_load_2d(codes_s + s * 8192 + ((lane * kCodeBytes) << pshift), &p.tmap_k, 0, row, full_bar(s));
+          // the page's scales are contiguous: [page keys][G]
+          bulk_load(kraw_s + s * (128 * G) + ((lane * G) << pshift), p.k_scale + static_cast<int64_t>(row) * G,
+                    static_cast<uint32_t>(page * G), full_bar(s));
         }
-        cp_async_arrive(full_bar(s));
         ++tile_iter;
       }
     });
     if (!ok && lane == 0) {
       // Let copies already in flight land before the CTA can exit.
+      volatile int never = 0;
       const uint32_t first = tile_iter > static_cast<uint32_t>(kStages) ? tile_iter - kStages : 0;
       for (uint32_t u = first; u < tile_iter; ++u) {
         if ((u & 1u) != pidx) continue;
-        volatile int never = 0;
         mbar_wait(full_bar(u % kStages), (u / kStages) & 1u, &never, p.err);
       }
+      if (pidx == 0)
+        for (uint32_t u = item_iter > 2u ? item_iter - 2u : 0u; u < item_iter; ++u)
+          mbar_wait(qfull_bar(u & 1u), (u >> 1) & 1u, &never, p.err);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ================================================================ MMA issuer
-    // Descriptors of stage 0 / K half 0; other stages and the second K half
-    // only move the 16-byte-unit start address (+32 B = +2).
-    const uint64_t a_desc0 = desc_kmajor_sw64(codes_s);
-    const uint64_t b_desc0 = desc_kmajor_sw64(q_s);
-    const uint64_t sfa_desc0 = desc_sf_atom(smem_u32(sfa_atoms));
-    uint32_t tile_iter = 0, item_iter = 0;
-    bool ok = true;
-    int last_acc = -1;
-    uint32_t last_acc_phase = 0;
-    for_each_segment<MODE, R>(p, st, [&](int, const ItemInfo& it, int lo, int hi, int) {
-      if (!ok) return;
-      ok = __shfl_sync(0xffffffffu,
-                       lane == 0 ? mbar_wait(qfull_bar, item_iter & 1u, abort_flag, p.err) : false, 0);
-      if (!ok) return;
-      q_scale_atoms<H, R, FMT>(p, it, sfb_atoms, lane);
-      fence_proxy_async_smem();
-      __syncwarp();
-      tc_fence_after();
-      const uint32_t sfb_t = tmem + L::kSfbCol + (item_iter & 1u) * 8u;
-      if (lane == 0) {
-#pragma unroll
-        for (int a = 0; a < F::kAtoms; ++a)
-          tc_cp_32x128b_warpx4(sfb_t + 4u * a, desc_sf_atom(smem_u32(sfb_atoms + 512 * a)));
-      }
-      __syncwarp();
-      // The tiles: one thread issues everything (no per-tile warp traffic).
-      if (lane == 0) {
+    // One thread only waits and issues: an MMA issue holds the issuing
+    // thread for most of the MMA's duration, so any other per-tile work here
+    // would leave the tensor pipe idle.
+    if (lane == 0) {
+      const uint64_t a_desc0 = desc_kmajor_sw64(codes_s);
+      const uint64_t b_desc0 = desc_kmajor_sw64(q_s);
+      uint32_t tile_iter = 0, item_iter = 0;
+      uint32_t sf_phase = 0;  // bit slot: phase of the K-scale slot's next use
+      bool ok = true;
+      int last_acc = -1;
+      uint32_t last_acc_phase = 0;
+      for_each_segment<MODE, R>(p, st, [&](int, const ItemInfo& it, int lo, int hi, int) {
+        if (!ok) return;
+        const uint32_t qb = item_iter & 1u;
+        const uint32_t sfb_t = tmem + L::kSfbCol + qb * 8u;
+        const uint64_t bdesc = b_desc0 + static_cast<uint64_t>((qb * L::kQBytes) >> 4);
         for (int j = lo; j < hi && ok; ++j) {
           if (MODE == kModeLogits && !tile_has_visible(it, j)) continue;
           const int s = tile_iter % kStages;
-          const uint32_t ph = (tile_iter / kStages) & 1u;
+          const int slot = tile_iter % L::kSfaSlots;
           const int a = tile_iter % kAccBufs;
           const uint32_t aph = (tile_iter / kAccBufs) & 1u;
-          if (!(ok = mbar_wait(full_bar(s), ph, abort_flag, p.err))) break;
-          // The scale atoms were written by cp.async (generic proxy): make
-          // them visible to the tensor core's copy, then move them to TMEM
-          // now (the copy needs no accumulator).
-          const uint32_t sfa_t = tmem + L::kSfaCol + (tile_iter % L::kSfaSlots) * 8u;
-          fence_proxy_async_smem();
-#pragma unroll
-          for (int at = 0; at < F::kAtoms; ++at)
-            tc_cp_32x128b_warpx4(sfa_t + 4u * at, sfa_desc0 + static_cast<uint64_t>(((s * F::kAtoms + at) * 512) >> 4));
+          // the scale warp copied this tile's K scales (and, for an item's
+          // first tile, the item's Q scales) after the stage's codes landed
+          if (!(ok = mbar_wait(sfready_bar(slot), (sf_phase >> slot) & 1u, abort_flag, p.err))) break;
+          sf_phase ^= 1u << slot;
           if (!(ok = mbar_wait(acce_bar(a), aph ^ 1u, abort_flag, p.err))) break;
           tc_fence_after();
+          const uint32_t sfa_t = tmem + L::kSfaCol + slot * 8u;
           const uint32_t d = tmem + L::kAccCol + a * 128u;
           const uint64_t adesc = a_desc0 + static_cast<uint64_t>((s * 8192) >> 4);
 #pragma unroll
@@ -616,7 +568,7 @@ __global__ void __launch_bounds__(96 + kEpiThreads * R, 1) score_kernel(const __
             constexpr uint32_t sf1 = F::kScaleVec == 2 ? 2u : 0u;
             const uint32_t idesc = kk == 0 ? idesc_fp4(128, N, F::kUe8m0, 0, 0) : idesc_fp4(128, N, F::kUe8m0, sf1, sf1);
             const uint32_t col = F::kScaleVec == 2 ? 0u : 4u * kk;
-            tc_mma_fp4<F::kScaleVec>(d, adesc + 2u * kk, b_desc0 + 2u * kk, idesc, sfa_t + col, sfb_t + col,
+            tc_mma_fp4<F::kScaleVec>(d, adesc + 2u * kk, bdesc + 2u * kk, idesc, sfa_t + col, sfb_t + col,
                                      static_cast<uint32_t>(kk));
           }
           tc_commit(empty_bar(s));
@@ -625,24 +577,115 @@ __global__ void __launch_bounds__(96 + kEpiThreads * R, 1) score_kernel(const __
           last_acc_phase = aph;
           ++tile_iter;
         }
+        if (!ok) return;
+        // Q buffer and Q-scale slot free once this item's MMAs complete.
+        tc_commit(qempty_bar(qb));
+        ++item_iter;
+      });
+      if (!ok && last_acc >= 0) {
+        // Outstanding MMAs must finish before TMEM is released.
+        volatile int never = 0;
+        mbar_wait(accf_bar(last_acc), last_acc_phase, &never, p.err);
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ================================================================ scales
+    // Per item: the Q scales of its rows -> 32x4x4 atoms -> TMEM slot
+    // item % 2 (free: the producer loaded this item's Q only after the MMAs
+    // of item - 2 completed).  Per tile: raw K scales [128 keys][G] -> 128
+    // rows of the scale layout (row r holds atom line r % 32: the words of
+    // keys l, 32+l, 64+l, 96+l, l = r % 32; NVFP4's second K half in the
+    // second 16 bytes), one tcgen05.cp 128x128b/256b into TMEM slot
+    // tile % kSfaSlots, committed to that slot's barrier.  A slot (TMEM and
+    // shared staging) is rewritten only after the MMA of the tile that last
+    // used it completed (its stage's empty barrier).
+    const uint64_t sfa_desc0 = desc_sf_rows(smem_u32(sfa_rows));
+    uint32_t tile_iter = 0, item_iter = 0;
+    bool ok = true;
+    for_each_segment<MODE, R>(p, st, [&](int, const ItemInfo& it, int lo, int hi, int) {
       if (!ok) return;
-      if (lane == 0) tc_commit(qempty_bar);
+      const uint32_t qb = item_iter & 1u, qph = (item_iter >> 1) & 1u;
+      ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(qfull_bar(qb), qph, abort_flag, p.err) : false, 0);
+      if (!ok) return;
+      // Q scales only when some tile of the segment is computed (otherwise no
+      // MMA reads them, and no barrier would track the copy)
+      if (MODE != kModeLogits || tile_has_visible(it, lo)) {
+        q_scale_atoms<H, R, FMT>(p, it, sfb_atoms + qb * (F::kAtoms * 512), lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t sfb_t = tmem + L::kSfbCol + qb * 8u;
+#pragma unroll
+          for (int at = 0; at < F::kAtoms; ++at)
+            tc_cp_32x128b_warpx4(sfb_t + 4u * at, desc_sf_atom(smem_u32(sfb_atoms + (qb * F::kAtoms + at) * 512)));
+        }
+      }
+      if (lane == 0) mbar_arrive(qempty_bar(qb));
       __syncwarp();
+      for (int j = lo; j < hi; ++j) {
+        if (MODE == kModeLogits && !tile_has_visible(it, j)) continue;
+        const int s = tile_iter % kStages;
+        const uint32_t ph = (tile_iter / kStages) & 1u;
+        const int slot = tile_iter % L::kSfaSlots;
+        bool got = false;
+        if (lane == 0) {
+          got = mbar_wait(full_bar(s), ph, abort_flag, p.err);
+          if (got && tile_iter >= static_cast<uint32_t>(L::kSfaSlots)) {
+            const uint32_t u = tile_iter - L::kSfaSlots;  // previous user of the slot
+            got = mbar_wait(empty_bar(u % kStages), (u / kStages) & 1u, abort_flag, p.err);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, got, 0);
+        if (!ok) break;
+        {
+          const uint8_t* raw = kraw + s * (128 * G);
+          uint8_t* rows = sfa_rows + slot * (F::kAtoms * 2048);
+          if constexpr (G == 4) {
+            const uint32_t* r32 = reinterpret_cast<const uint32_t*>(raw);
+            const uint4 v = make_uint4(r32[lane], r32[32 + lane], r32[64 + lane], r32[96 + lane]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(rows + (32 * q + lane) * 16) = v;
+          } else {
+            const uint2* r64 = reinterpret_cast<const uint2*>(raw);
+            const uint2 a0 = r64[lane], a1 = r64[32 + lane], a2 = r64[64 + lane], a3 = r64[96 + lane];
+            const uint4 lo4 = make_uint4(a0.x, a1.x, a2.x, a3.x), hi4 = make_uint4(a0.y, a1.y, a2.y, a3.y);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              *reinterpret_cast<uint4*>(rows + (32 * q + lane) * 16) = lo4;
+              *reinterpret_cast<uint4*>(rows + 2048 + (32 * q + lane) * 16) = hi4;
+            }
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t sfa_t = tmem + L::kSfaCol + slot * 8u;
+          const uint64_t sdesc = sfa_desc0 + static_cast<uint64_t>((slot * F::kAtoms * 2048) >> 4);
+          if constexpr (G == 4) tc_cp_128x128b(sfa_t, sdesc);
+          else tc_cp_128x256b(sfa_t, sdesc);
+          tc_commit(sfready_bar(slot));
+        }
+        __syncwarp();
+        ++tile_iter;
+      }
       ++item_iter;
     });
-    if (!ok && last_acc >= 0 && lane == 0) {
-      // Outstanding MMAs must finish before TMEM is released.
+    if (lane == 0) {
+      // copies still in flight must land before TMEM is released
       volatile int never = 0;
-      mbar_wait(accf_bar(last_acc), last_acc_phase, &never, p.err);
+      const uint32_t first = tile_iter > static_cast<uint32_t>(L::kSfaSlots) ? tile_iter - L::kSfaSlots : 0;
+      for (uint32_t u = first; u < tile_iter; ++u)
+        mbar_wait(sfready_bar(u % L::kSfaSlots), (u / L::kSfaSlots) & 1u, &never, p.err);
     }
     __syncwarp();
   } else {
     // ================================================================ epilogue
     static_assert(L::kGroups == R, "one epilogue group per query row");
-    const int r = (warp - 2) >> 2;  // this group's query row within the item
-    Group<kEpiThreads, -1> g{static_cast<int>(threadIdx.x) - 64 - r * kEpiThreads, 1 + r};
+    const int r = (warp - L::kEpiWarp0) >> 2;  // this group's query row within the item
+    Group<kEpiThreads, -1> g{static_cast<int>(threadIdx.x) - 32 * L::kEpiWarp0 - r * kEpiThreads, 1 + r};
     SelectScratch* gsc = sc + r;
     const int quad = warp & 3;
     const int key_local = quad * 32 + lane;
@@ -663,11 +706,11 @@ __global__ void __launch_bounds__(96 + kEpiThreads * R, 1) score_kernel(const __
       const bool row_valid = r < it.nrows;
       const int32_t t = it.row0 + r;
       const int32_t vis = row_valid ? row_visible(p, it, t) : 0;
-      float2 w2[H / 2];  // half weights, see weighted_relu_reg
+      float2 w2[H / 2];  // head weight pairs, see weighted_relu_reg
 #pragma unroll
       for (int i = 0; i < H / 2; ++i) {
         const float* wr = p.w + static_cast<int64_t>(t) * p.w_row_stride + 2 * i;
-        w2[i] = row_valid ? make_float2(0.5f * __ldg(wr), 0.5f * __ldg(wr + 1)) : make_float2(0.0f, 0.0f);
+        w2[i] = row_valid ? make_float2(__ldg(wr), __ldg(wr + 1)) : make_float2(0.0f, 0.0f);
       }
       float thr_v = -INFINITY;
       uint32_t thr_p = 0xFFFFFFFFu;
@@ -695,12 +738,12 @@ __global__ void __launch_bounds__(96 + kEpiThreads * R, 1) score_kernel(const __
         if (real) {
           const int a = tile_iter % kAccBufs;
           const uint32_t aph = (tile_iter / kAccBufs) & 1u;
-          // One thread of the group polls the accumulator barrier; the rest
-          // block on the group's named barrier instead of spinning.
-          if (g.tid == 0 && ok && !mbar_wait(accf_bar(a), aph, abort_flag, p.err)) st->abort = 1;
-          g.sync();
-          // warp-uniform: tcgen05.ld below is a whole-warp instruction
-          ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+          // One lane per warp polls the accumulator barrier (no group
+          // barrier per tile); ok stays warp-uniform, as tcgen05.ld below
+          // is a whole-warp instruction.
+          bool got = false;
+          if (lane == 0) got = ok && mbar_wait(accf_bar(a), aph, abort_flag, p.err);
+          ok = __shfl_sync(0xffffffffu, got, 0);
           if (ok) {
             tc_fence_after();
             uint32_t v[H];
