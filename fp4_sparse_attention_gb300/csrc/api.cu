@@ -227,7 +227,7 @@ TopkWorkspace topk_workspace(const fp4idx_problem_t* p, int32_t k, int sms) {
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   TopkWorkspace ws;
   ws.keys_off = 0;
-  ws.count_off = up(static_cast<size_t>(slots) * k * 8);
+  ws.count_off = up(static_cast<size_t>(slots) * topk_capacity(k) * 8);
   ws.cand_off = ws.count_off + up(static_cast<size_t>(slots) * 4);
   ws.start_off = ws.cand_off + up(static_cast<size_t>(ctas) * R * topk_capacity(k) * 8);
   ws.bytes = ws.start_off + up(static_cast<size_t>(items + 1) * 4);

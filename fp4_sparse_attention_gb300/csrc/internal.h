@@ -46,9 +46,9 @@ struct ScoreParams {
   int64_t ld;
   // top-k partials: slot s (s < score_ctas: first segment of CTA s; else
   // score_ctas + item: an item that starts inside a CTA's chunk) x R rows,
-  // up to k keys each.
+  // up to topk_capacity(k) keys each (a superset of that slot's top-k).
   int32_t k;
-  uint64_t* part_keys;      // [slots * R][k]
+  uint64_t* part_keys;      // [slots * R][topk_capacity(k)]
   int32_t* part_count;      // [slots * R]
   uint64_t* cand;           // [score_ctas * R][candidate capacity] streaming candidate buffers
   int32_t* item_start;      // [items + 1] first global tile of each item, total last (top-k only)

@@ -74,7 +74,15 @@ struct ScoreLayout {
   // K-tile ring depth.  A loaded HBM round trip for a random page is ~2 us,
   // so ~100+ KB must be in flight per SM; the ring takes most of shared memory.
   static constexpr int kStages = FMT == 0 ? 20 : 18;
-  static constexpr int kGroups = R;  // epilogue groups, one query row each
+  // Rows of the item per epilogue group of four warps.  Logits: 64
+  // accumulator columns per thread and tile, so the per-tile fixed work
+  // (barrier poll, TMEM load, fences) is shared by several rows.  Top-k: one
+  // row per group, as each row's insert and compaction chain is serial
+  // within its group and more groups overlap more of them.
+  static constexpr int kRowsPerGroup =
+      MODE == kModeTopk ? 1 : (R < 64 / H ? R : (64 / H < 1 ? 1 : 64 / H));
+  static_assert(R % kRowsPerGroup == 0, "rows split evenly over the groups");
+  static constexpr int kGroups = R / kRowsPerGroup;
   // warp 0 and the last warp: producers (alternate tiles); warp 1: MMA;
   // warp 2: scales; warps 3 .. 3 + 4R - 1: epilogue
   static constexpr int kEpiWarp0 = 3;
@@ -358,7 +366,7 @@ __device__ int compact_keep_ge(const G& g, uint64_t* cand, int n, uint64_t T, Se
 // The kernel.
 // ---------------------------------------------------------------------------
 template <int H, int R, int FMT, int MODE>
-__global__ void __launch_bounds__(128 + kEpiThreads * R, 1) score_kernel(const __grid_constant__ ScoreParams p) {
+__global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) score_kernel(const __grid_constant__ ScoreParams p) {
   using L = ScoreLayout<H, R, FMT, MODE>;
   constexpr int kThreads = L::kThreads;
   using F = FmtTraits<FMT>;
@@ -683,10 +691,11 @@ __global__ void __launch_bounds__(128 + kEpiThreads * R, 1) score_kernel(const _
     __syncwarp();
   } else {
     // ================================================================ epilogue
-    static_assert(L::kGroups == R, "one epilogue group per query row");
-    const int r = (warp - L::kEpiWarp0) >> 2;  // this group's query row within the item
-    Group<kEpiThreads, -1> g{static_cast<int>(threadIdx.x) - 32 * L::kEpiWarp0 - r * kEpiThreads, 1 + r};
-    SelectScratch* gsc = sc + r;
+    constexpr int RG = L::kRowsPerGroup;  // query rows of this group
+    const int gi = (warp - L::kEpiWarp0) >> 2;
+    const int r0 = gi * RG;  // first row of the item this group handles
+    Group<kEpiThreads, -1> g{static_cast<int>(threadIdx.x) - 32 * L::kEpiWarp0 - gi * kEpiThreads, 1 + gi};
+    SelectScratch* gsc = sc + gi;
     const int quad = warp & 3;
     const int key_local = quad * 32 + lane;
     // Compaction is checked every `check_every` tiles; the buffer keeps that
@@ -696,45 +705,65 @@ __global__ void __launch_bounds__(128 + kEpiThreads * R, 1) score_kernel(const _
     int since_check = 0;
     uint32_t tile_iter = 0;
     bool ok = true;
-    const Hist16 hr{hist_words + r * (kHistBins / 2)};
-    // this row's candidate buffer: global workspace, L2-resident
-    uint64_t* cr = p.cand + (static_cast<int64_t>(blockIdx.x) * R + r) * cap;
-    // Acceptance threshold T of the candidate buffer (key >= T), kept as the
-    // logit value of T and the largest position accepted at that value.
+    auto hist_of = [&](int rr) { return Hist16{hist_words + (r0 + rr) * (kHistBins / 2)}; };
+    // each row's candidate buffer: global workspace, L2-resident
+    auto cand_of = [&](int rr) { return p.cand + (static_cast<int64_t>(blockIdx.x) * R + r0 + rr) * cap; };
     for_each_segment<MODE, R>(p, st, [&](int item, const ItemInfo& it, int lo, int hi, int seg) {
-      // -- this group's row of the item: weights in registers, visibility
-      const bool row_valid = r < it.nrows;
-      const int32_t t = it.row0 + r;
-      const int32_t vis = row_valid ? row_visible(p, it, t) : 0;
-      float2 w2[H / 2];  // head weight pairs, see weighted_relu_reg
+      // -- this group's rows of the item: weights in registers, visibility
+      bool row_valid[RG];
+      int32_t t[RG], vis[RG];
+      float2 w2[RG][H / 2];  // head weight pairs, see weighted_relu_reg
+      // acceptance threshold of each row's buffer (key >= T), kept as the
+      // logit value of T and the largest position accepted at that value
+      float thr_v[RG];
+      uint32_t thr_p[RG];
 #pragma unroll
-      for (int i = 0; i < H / 2; ++i) {
-        const float* wr = p.w + static_cast<int64_t>(t) * p.w_row_stride + 2 * i;
-        w2[i] = row_valid ? make_float2(__ldg(wr), __ldg(wr + 1)) : make_float2(0.0f, 0.0f);
+      for (int rr = 0; rr < RG; ++rr) {
+        row_valid[rr] = r0 + rr < it.nrows;
+        t[rr] = it.row0 + r0 + rr;
+        vis[rr] = row_valid[rr] ? row_visible(p, it, t[rr]) : 0;
+#pragma unroll
+        for (int i = 0; i < H / 2; ++i) {
+          const float* wr = p.w + static_cast<int64_t>(t[rr]) * p.w_row_stride + 2 * i;
+          w2[rr][i] = row_valid[rr] ? make_float2(__ldg(wr), __ldg(wr + 1)) : make_float2(0.0f, 0.0f);
+        }
+        thr_v[rr] = -INFINITY;
+        thr_p[rr] = 0xFFFFFFFFu;
       }
-      float thr_v = -INFINITY;
-      uint32_t thr_p = 0xFFFFFFFFu;
       g.sync();
       if constexpr (MODE == kModeTopk) {
-        if (g.tid == 0) {
-          rs->cnt[r] = 0;
-          rs->thr[r] = 0;
+#pragma unroll
+        for (int rr = 0; rr < RG; ++rr) {
+          if (g.tid == 0) rs->cnt[r0 + rr] = 0;
+          const Hist16 hr = hist_of(rr);
+          for (int e = g.tid; e < kHistBins / 2; e += kEpiThreads) hr.w[e] = 0;
         }
-        for (int e = g.tid; e < kHistBins / 2; e += kEpiThreads) hr.w[e] = 0;
       }
       g.sync();
       since_check = 0;
-      // page id of this thread's key, one tile ahead (validity check off the critical path)
-      auto page_of = [&](int j) -> int32_t {
-        const int32_t pos = (j << 7) + key_local;
-        return pos < it.k_len ? __ldg(p.block_table + it.table_base + (pos >> p.page_shift)) : -1;
+      // Page ids for the validity check: lane l caches the id of logical
+      // page pbase + l and the next 32 are loaded 32 pages ahead, so no
+      // table load latency is exposed per tile (a warp's 32 keys share a page).
+      const int32_t npages = (it.k_len + p.page_size - 1) >> p.page_shift;
+      auto fetch_ids = [&](int32_t b) -> int32_t {
+        const int32_t lp = b + lane;
+        return lp < npages ? __ldg(p.block_table + it.table_base + lp) : -1;
       };
-      int32_t pg_cur = lo < hi ? page_of(lo) : -1;
+      int32_t pbase = ((lo << 7) + quad * 32) >> p.page_shift & ~31;
+      int32_t ids_cur = fetch_ids(pbase), ids_next = fetch_ids(pbase + 32);
       for (int j = lo; j < hi; ++j) {
-        const int32_t pg_next = j + 1 < hi ? page_of(j + 1) : -1;
         const int32_t pos = (j << 7) + key_local;
+        const int32_t lp = ((j << 7) + quad * 32) >> p.page_shift;  // warp-uniform
+        if (lp >= pbase + 32) {
+          pbase += 32;
+          ids_cur = ids_next;
+          ids_next = fetch_ids(pbase + 32);
+        }
+        const int32_t pg_cur = __shfl_sync(0xffffffffu, ids_cur, lp - pbase);
         const bool real = !(MODE == kModeLogits && !tile_has_visible(it, j));
-        float val = -INFINITY;
+        float val[RG];
+#pragma unroll
+        for (int rr = 0; rr < RG; ++rr) val[rr] = -INFINITY;
         if (real) {
           const int a = tile_iter % kAccBufs;
           const uint32_t aph = (tile_iter / kAccBufs) & 1u;
@@ -746,44 +775,55 @@ __global__ void __launch_bounds__(128 + kEpiThreads * R, 1) score_kernel(const _
           ok = __shfl_sync(0xffffffffu, got, 0);
           if (ok) {
             tc_fence_after();
-            uint32_t v[H];
-            tmem_ld<H>(tmem + (static_cast<uint32_t>(quad * 32) << 16) + L::kAccCol + a * 128u + r * H, v);
+            uint32_t v[RG * H];
+            tmem_ld<RG * H>(tmem + (static_cast<uint32_t>(quad * 32) << 16) + L::kAccCol + a * 128u + r0 * H, v);
             tmem_wait_ld();
             reg_fence(v);
             tc_fence_before();
             mbar_arrive(acce_bar(a));
-            val = weighted_relu_reg<H>(v, w2);
+#pragma unroll
+            for (int rr = 0; rr < RG; ++rr)
+              val[rr] = weighted_relu_reg<H>(*reinterpret_cast<const uint32_t(*)[H]>(&v[rr * H]), w2[rr]);
           }
           ++tile_iter;
         }
-        const bool visible = pos < vis && pg_cur >= 0 && pg_cur < p.num_pages;
-        pg_cur = pg_next;
+        const bool page_good = pos < it.k_len && pg_cur >= 0 && pg_cur < p.num_pages;
         if constexpr (MODE == kModeLogits) {
-          if (ok && row_valid && pos < p.ld)
-            p.logits[static_cast<int64_t>(t) * p.ld + pos] = visible ? val : -INFINITY;
+#pragma unroll
+          for (int rr = 0; rr < RG; ++rr)
+            if (ok && row_valid[rr] && pos < p.ld)
+              p.logits[static_cast<int64_t>(t[rr]) * p.ld + pos] = page_good && pos < vis[rr] ? val[rr] : -INFINITY;
         } else {
-          // NaN logits are never selected (every comparison is false).
-          const bool take = ok && visible && (val > thr_v || (val == thr_v && static_cast<uint32_t>(pos) <= thr_p));
-          const uint32_t m = __ballot_sync(0xffffffffu, take);
-          if (m) {
-            const int leader = __ffs(m) - 1;
-            int base = 0;
-            if (lane == leader) base = atomicAdd(&rs->cnt[r], __popc(m));
-            base = __shfl_sync(0xffffffffu, base, leader);
-            const int slot_i = base + __popc(m & ((1u << lane) - 1u));
-            if (take && slot_i < cap) {
-              const uint64_t key = (static_cast<uint64_t>(ordered_bits(val)) << 32) |
-                                   static_cast<uint64_t>(~static_cast<uint32_t>(pos));
-              cr[slot_i] = key;
-              hr.add(static_cast<int>(key >> kHistShift));
+#pragma unroll
+          for (int rr = 0; rr < RG; ++rr) {
+            // NaN logits are never selected (every comparison is false).
+            const bool take = ok && page_good && pos < vis[rr] &&
+                              (val[rr] > thr_v[rr] || (val[rr] == thr_v[rr] && static_cast<uint32_t>(pos) <= thr_p[rr]));
+            const uint32_t m = __ballot_sync(0xffffffffu, take);
+            if (m) {
+              const int leader = __ffs(m) - 1;
+              int base = 0;
+              if (lane == leader) base = atomicAdd(&rs->cnt[r0 + rr], __popc(m));
+              base = __shfl_sync(0xffffffffu, base, leader);
+              const int slot_i = base + __popc(m & ((1u << lane) - 1u));
+              if (take && slot_i < cap) {
+                const uint64_t key = (static_cast<uint64_t>(ordered_bits(val[rr])) << 32) |
+                                     static_cast<uint64_t>(~static_cast<uint32_t>(pos));
+                cand_of(rr)[slot_i] = key;
+                hist_of(rr).add(static_cast<int>(key >> kHistShift));
+              }
             }
           }
           if (++since_check < check_every) continue;
           since_check = 0;
           g.sync();
-          // -- compaction of a full candidate buffer
-          const int n = rs->cnt[r];
-          if (n > cap - margin) {  // uniform: read after the barrier
+          // -- compaction of full candidate buffers, one row at a time
+#pragma unroll 1
+          for (int rr = 0; rr < RG; ++rr) {
+            const int n = rs->cnt[r0 + rr];
+            if (n <= cap - margin) continue;  // uniform: read after the barrier
+            const Hist16 hr = hist_of(rr);
+            uint64_t* cr = cand_of(rr);
             uint32_t above = 0;
             const uint32_t bkt = find_kth_bucket(g, hr, static_cast<uint32_t>(p.k), gsc, &above);
             const uint32_t kept = above + hr(static_cast<int>(bkt));
@@ -801,49 +841,63 @@ __global__ void __launch_bounds__(128 + kEpiThreads * R, 1) score_kernel(const _
             if (g.tid == 0) {
               if (bkt & 1u) hr.set(static_cast<int>(bkt) - 1, 0);
               if (exact) hr.set(static_cast<int>(bkt), static_cast<uint32_t>(p.k) - above);
-              rs->cnt[r] = left;
+              rs->cnt[r0 + rr] = left;
             }
-            thr_v = key_value(T);
-            thr_p = ~static_cast<uint32_t>(T);
+            // rr is uniform across the group; the threshold lives in registers
+#pragma unroll
+            for (int q = 0; q < RG; ++q)
+              if (q == rr) {
+                thr_v[q] = key_value(T);
+                thr_p[q] = ~static_cast<uint32_t>(T);
+              }
             g.sync();
           }
         }
       }
       if constexpr (MODE == kModeTopk) {
-        // -- flush the exact top-k of this group's row
+        // -- flush each of this group's rows: every candidate in or above the
+        // bucket of the row's k-th key (a superset of its top-k; the merge
+        // selects exactly), so no radix passes run here
         const int slot = seg == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + item;
-        g.sync();
-        const int n = rs->cnt[r];
-        uint64_t T = 0;
-        if (n > p.k) {
-          uint32_t above = 0;
-          const uint32_t bkt = find_kth_bucket(g, hr, static_cast<uint32_t>(p.k), gsc, &above);
-          T = select_in_bucket(g, bkt, static_cast<uint32_t>(p.k) - above, gsc, [&](auto&& fn) {
-            for (int e = g.tid; e < n; e += kEpiThreads) fn(cr[e]);
-          });
-        }
-        const int64_t part = static_cast<int64_t>(slot) * R + r;
-        uint64_t* out = p.part_keys + part * p.k;
-        if (g.tid == 0) gsc->bcast[3] = 0;
-        g.sync();
-        for (int base = 0; base < n; base += kEpiThreads) {
-          const int e = base + g.tid;
-          const uint64_t key = e < n ? cr[e] : 0;
-          const bool keep = ok && e < n && key >= T;
-          const uint32_t m = __ballot_sync(0xffffffffu, keep);
-          if (m) {
-            const int leader = __ffs(m) - 1;
-            uint32_t dst = 0;
-            if (lane == leader) dst = atomicAdd(&gsc->bcast[3], static_cast<uint32_t>(__popc(m)));
-            dst = __shfl_sync(0xffffffffu, dst, leader);
-            const uint32_t o = dst + __popc(m & ((1u << lane) - 1u));
-            if (keep && o < static_cast<uint32_t>(p.k)) out[o] = key;
+#pragma unroll 1
+        for (int rr = 0; rr < RG; ++rr) {
+          const Hist16 hr = hist_of(rr);
+          const uint64_t* cr = cand_of(rr);
+          g.sync();
+          const int n = rs->cnt[r0 + rr];
+          uint64_t T = 0;
+          if (n > p.k) {
+            uint32_t above = 0;
+            const uint32_t bkt = find_kth_bucket(g, hr, static_cast<uint32_t>(p.k), gsc, &above);
+            T = static_cast<uint64_t>(bkt) << kHistShift;
           }
-        }
-        g.sync();
-        if (g.tid == 0) {
-          const int32_t wrote = static_cast<int32_t>(min(gsc->bcast[3], static_cast<uint32_t>(p.k)));
-          p.part_count[part] = row_valid ? wrote : 0;
+          const int64_t part = static_cast<int64_t>(slot) * R + r0 + rr;
+          uint64_t* out = p.part_keys + part * cap;
+          if (g.tid == 0) gsc->bcast[3] = 0;
+          g.sync();
+          for (int base = 0; base < n; base += kEpiThreads) {
+            const int e = base + g.tid;
+            const uint64_t key = e < n ? cr[e] : 0;
+            const bool keep = ok && e < n && key >= T;
+            const uint32_t m = __ballot_sync(0xffffffffu, keep);
+            if (m) {
+              const int leader = __ffs(m) - 1;
+              uint32_t dst = 0;
+              if (lane == leader) dst = atomicAdd(&gsc->bcast[3], static_cast<uint32_t>(__popc(m)));
+              dst = __shfl_sync(0xffffffffu, dst, leader);
+              const uint32_t o = dst + __popc(m & ((1u << lane) - 1u));
+              if (keep && o < static_cast<uint32_t>(cap)) out[o] = key;
+            }
+          }
+          g.sync();
+          bool valid_rr = false;
+#pragma unroll
+          for (int q = 0; q < RG; ++q)
+            if (q == rr) valid_rr = row_valid[q];
+          if (g.tid == 0) {
+            const int32_t wrote = static_cast<int32_t>(min(gsc->bcast[3], static_cast<uint32_t>(cap)));
+            p.part_count[part] = valid_rr ? wrote : 0;
+          }
         }
       }
     });

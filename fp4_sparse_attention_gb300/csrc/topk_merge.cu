@@ -1,9 +1,9 @@
 // topk_merge.cu -- exact top-k of each query row from the per-CTA partial
 // candidate lists written by the scorer in top-k mode.
 //
-// Every scorer CTA kept, for each row of each item it touched, the exact
-// top-k of the keys it scored.  The union of those lists therefore holds the
-// row's global top-k; this kernel selects it exactly (bucket histogram, then
+// Every scorer CTA kept, for each row of each item it touched, a superset of
+// the top-k of the keys it scored.  The union of those lists therefore holds
+// the row's global top-k; this kernel selects it exactly (bucket histogram, then
 // radix passes inside the bucket of the k-th key) and writes logical
 // positions, values and the valid count.  One CTA per query row.  The row's
 // partial lists are read with one warp per list and, when the union fits,
@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const __grid_
   const int warp = tid >> 5;
   const int t = blockIdx.x;
   const int k = p.k;
+  const int cap = topk_capacity(k);  // keys per partial list
   const int R = mp.rows_per_cta;
   Group<kMergeThreads, 0> g{tid};
 
@@ -73,7 +74,7 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const __grid_
     const int s = static_cast<int64_t>(c) * chunk >= P ? c : C + item;
     const int64_t part = static_cast<int64_t>(s) * R + r;
     sm->slot_part[i] = part;
-    sm->slot_cnt[i] = min(max(__ldg(p.part_count + part), 0), k);
+    sm->slot_cnt[i] = min(max(__ldg(p.part_count + part), 0), cap);
   }
   g.sync();
   if (tid == 0) {
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const __grid_
   // visit every candidate in global memory: one warp per list
   auto for_each_global = [&](auto&& fn) {
     for (int i = warp; i < nslots; i += kMergeWarps) {
-      const uint64_t* keys = p.part_keys + sm->slot_part[i] * k;
+      const uint64_t* keys = p.part_keys + sm->slot_part[i] * cap;
       const int n = sm->slot_cnt[i];
       const int off = sm->slot_off[i];
       for (int e = lane; e < n; e += 32) fn(__ldg(keys + e), off + e);
