@@ -140,7 +140,7 @@ class ClockSampler:
 # kind "topk": [logits +] top-k score + merge; kind "block": block maxima.
 # bound: the roofline of the workload's scorer kernel.
 WORKLOADS = {
-    "verify16k": dict(maker="verify_decode_16k", kind="topk", k=2048, logits=True, bound="hbm"),
+    "verify16k": dict(maker="verify_decode_16k", kind="topk", k=2048, logits=True, fused=True, bound="hbm"),
     "long_decode": dict(maker="long_batched_decode", kind="topk", k=2048, logits=False, bound="hbm"),
     "block_scores": dict(maker="nvfp4_gqa_block_scores", kind="block", k=0, logits=False, bound="tensor"),
     "prefill": dict(maker="prefill_32k", kind="topk", k=2048, logits=False, bound="tensor"),
@@ -242,8 +242,13 @@ class OursBench:
             self.val = torch.empty((T, self.k), dtype=torch.float32, device=device)
             self.cnt = torch.empty((T,), dtype=torch.int32, device=device)
             self.ws = torch.empty((B.fp4idx_topk_workspace_bytes(base, self.k),), dtype=torch.uint8, device=device)
-            self.kernels = (["scorer_logits"] if spec["logits"] else []) + ["scorer_topk", "topk_merge"]
-        self.launches_per_step = len(self.kernels)
+            if spec.get("fused"):
+                # one call: scorer logits + per-row selection from them (two kernels)
+                self.kernels = ["logits_topk"]
+            else:
+                self.kernels = (["scorer_logits"] if spec["logits"] else []) + ["scorer_topk", "topk_merge"]
+            self.launch_count = 2 if spec.get("fused") else len(self.kernels)
+        self.launches_per_step = getattr(self, "launch_count", len(self.kernels))
         self.graphs = []
         self.events = []
 
@@ -252,6 +257,9 @@ class OursBench:
         prob, w = self.problems[n], self.ws_list[n]
         if self.block:
             return [lambda: B.fp4idx_block_scores(prob, out=self.scores)]
+        if self.spec.get("fused"):
+            return [lambda: B.fp4idx_logits_topk(prob, w, self.k, logits=self.logits, indices=self.idx,
+                                                 values=self.val, valid_count=self.cnt)]
         calls = []
         if self.logits is not None:
             calls.append(lambda: B.fp4idx_logits(prob, w, out=self.logits))
@@ -351,6 +359,9 @@ class OursBench:
                 d.copy_(h, non_blocking=True)
             if self.block:
                 B.fp4idx_block_scores(prob, out=self.scores)
+            elif self.spec.get("fused"):
+                B.fp4idx_logits_topk(prob, self.w, self.k, logits=self.logits, indices=self.idx, values=self.val,
+                                     valid_count=self.cnt)
             else:
                 if self.logits is not None:
                     B.fp4idx_logits(prob, self.w, out=self.logits)
@@ -383,6 +394,8 @@ def kernel_algorithmic_bytes(host, name: str, k: int) -> int:
         return kv + qb
     if name == "topk_merge":
         return T * k * 8 + T * 4
+    if name == "logits_topk":  # both kernels of the fused call: keys in, logits out (and read back), top-k out
+        return kv + qb + 2 * T * ((host.max_seqlen_k + 3) // 4 * 4) * 4 + T * k * 8 + T * 4
     if name == "block_scores":
         return kv + qb + H * ((host.max_seqlen_k + 127) // 128) * T * 4
     raise KeyError(name)
@@ -583,6 +596,8 @@ def run_ours(args, world, rank, local):
     roof["traffic"] = rec["bytes"] if rec and rec["sha"] == sha else None
     if spec["kind"] == "block":
         step_desc = f"block maxima [{host.num_heads}, {host.ktiles}, {host.q.shape[0]}]"
+    elif spec.get("fused"):
+        step_desc = f"logits + top-{spec['k']} in one call (scorer logits, per-row selection from them)"
     else:
         step_desc = ("logits + " if spec["logits"] else "") + f"top-{spec['k']} (score + merge)"
     line = {

@@ -9,6 +9,8 @@ The functions keep the C names:
     fp4idx_logits(problem, w, ld=None, out=None, stream=None) -> logits [T, ld]
     fp4idx_block_scores(problem, out=None, stream=None) -> scores [Hq, Ktiles, T]
     fp4idx_topk(problem, w, k, sorted=False, ...) -> (indices, values, valid_count)
+    fp4idx_logits_topk(problem, w, k, sorted=False, ...) -> (logits, indices, values, valid_count)
+    fp4idx_topk_score / fp4idx_topk_merge(...)  -- the streaming plan's two phases
     fp4idx_topk_workspace_bytes(problem, k) -> int
     fp4idx_get_error(clear=True, stream=None) -> int
 """
@@ -26,6 +28,7 @@ LIB_PATH = os.path.join(_PKG, "libfp4idx.so")
 
 FP4IDX_OK = 0
 FP4IDX_TOPK_SORTED = 0x1
+FP4IDX_TOPK_STREAMING = 0x2
 ERR_PAGE_RANGE = 0x1
 ERR_TIMEOUT = 0x2
 
@@ -36,6 +39,7 @@ EXPORTED = (
     "fp4idx_topk",
     "fp4idx_topk_score",
     "fp4idx_topk_merge",
+    "fp4idx_logits_topk",
     "fp4idx_get_error",
     "fp4idx_status_string",
     "fp4idx_last_error_message",
@@ -101,6 +105,8 @@ def load_library(path: str = LIB_PATH):
         lib.fp4idx_topk_workspace_bytes.argtypes = [P, i32]
         lib.fp4idx_topk_workspace_bytes.restype = sz
         lib.fp4idx_topk.argtypes = [P, vp, i64, i32, u32, vp, vp, vp, vp, sz, vp]
+        lib.fp4idx_logits_topk.argtypes = [P, vp, i64, vp, i64, i32, u32, vp, vp, vp, vp]
+        lib.fp4idx_logits_topk.restype = i32
         lib.fp4idx_topk.restype = i32
         lib.fp4idx_topk_score.argtypes = [P, vp, i64, i32, vp, sz, vp]
         lib.fp4idx_topk_score.restype = i32
@@ -241,8 +247,9 @@ def fp4idx_topk_workspace_bytes(problem: DeviceProblem, k: int) -> int:
 def fp4idx_topk(problem: DeviceProblem, w: torch.Tensor, k: int, sorted: bool = False,
                 indices: Optional[torch.Tensor] = None, values: Optional[torch.Tensor] = None,
                 valid_count: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                want_values: bool = True, stream=None):
-    """Top-k positions per row: (indices [T,k] i32 -1 padded, values [T,k] f32, valid_count [T] i32)."""
+                want_values: bool = True, streaming: bool = False, stream=None):
+    """Top-k positions per row: (indices [T,k] i32 -1 padded, values [T,k] f32, valid_count [T] i32).
+    ``streaming`` forces the streaming plan (FP4IDX_TOPK_STREAMING)."""
     lib = load_library()
     dev = w.device
     T = problem.num_rows
@@ -255,15 +262,39 @@ def fp4idx_topk(problem: DeviceProblem, w: torch.Tensor, k: int, sorted: bool = 
     need = fp4idx_topk_workspace_bytes(problem, k)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
-    flags = FP4IDX_TOPK_SORTED if sorted else 0
+    flags = (FP4IDX_TOPK_SORTED if sorted else 0) | (FP4IDX_TOPK_STREAMING if streaming else 0)
     _check(lib.fp4idx_topk(ctypes.byref(problem.c), _ptr(w), w.stride(0), int(k), flags, _ptr(indices),
                            _ptr(values), _ptr(valid_count), _ptr(workspace), workspace.numel(), _stream(stream)),
            "fp4idx_topk")
     return indices, values, valid_count
 
 
+def fp4idx_logits_topk(problem: DeviceProblem, w: torch.Tensor, k: int, sorted: bool = False,
+                       logits: Optional[torch.Tensor] = None, ld: Optional[int] = None,
+                       indices: Optional[torch.Tensor] = None, values: Optional[torch.Tensor] = None,
+                       valid_count: Optional[torch.Tensor] = None, stream=None):
+    """Full logits and their top-k in one call: (logits [T,ld], indices, values, valid_count)."""
+    lib = load_library()
+    dev = w.device
+    T = problem.num_rows
+    if logits is None:
+        ld = ld or (problem.max_seqlen_k + 3) // 4 * 4
+        logits = torch.empty((T, ld), dtype=torch.float32, device=dev)
+    if indices is None:
+        indices = torch.empty((T, k), dtype=torch.int32, device=dev)
+    if values is None:
+        values = torch.empty((T, k), dtype=torch.float32, device=dev)
+    if valid_count is None:
+        valid_count = torch.empty((T,), dtype=torch.int32, device=dev)
+    flags = FP4IDX_TOPK_SORTED if sorted else 0
+    _check(lib.fp4idx_logits_topk(ctypes.byref(problem.c), _ptr(w), w.stride(0), _ptr(logits), logits.stride(0),
+                                  int(k), flags, _ptr(indices), _ptr(values), _ptr(valid_count), _stream(stream)),
+           "fp4idx_logits_topk")
+    return logits, indices, values, valid_count
+
+
 def fp4idx_topk_score(problem: DeviceProblem, w: torch.Tensor, k: int, workspace: torch.Tensor, stream=None):
-    """Phase 1 of fp4idx_topk: scorer + per-CTA exact top-k partials in `workspace`."""
+    """Phase 1 of fp4idx_topk's streaming plan: scorer + per-CTA top-k partials in `workspace`."""
     lib = load_library()
     _check(lib.fp4idx_topk_score(ctypes.byref(problem.c), _ptr(w), w.stride(0), int(k), _ptr(workspace),
                                  workspace.numel(), _stream(stream)), "fp4idx_topk_score")

@@ -217,6 +217,13 @@ struct TopkWorkspace {
   size_t keys_off, count_off, cand_off, start_off, bytes;
 };
 
+// Short-context plan of fp4idx_topk: logits into the workspace, then a
+// per-row selection.  Decided from host scalars only.
+int64_t logits_plan_ld(const fp4idx_problem_t* p) { return (static_cast<int64_t>(p->max_seqlen_k) + 3) / 4 * 4; }
+bool use_logits_plan(const fp4idx_problem_t* p) {
+  return p->max_seqlen_k <= 16384 && static_cast<int64_t>(p->num_rows) * logits_plan_ld(p) <= (int64_t(1) << 24);
+}
+
 // Workspace of the top-k path: per-CTA partial lists, their counts, and each
 // scorer CTA's per-row streaming candidate buffers.
 TopkWorkspace topk_workspace(const fp4idx_problem_t* p, int32_t k, int sms) {
@@ -231,6 +238,11 @@ TopkWorkspace topk_workspace(const fp4idx_problem_t* p, int32_t k, int sms) {
   ws.cand_off = ws.count_off + up(static_cast<size_t>(slots) * 4);
   ws.start_off = ws.cand_off + up(static_cast<size_t>(ctas) * R * topk_capacity(k) * 8);
   ws.bytes = ws.start_off + up(static_cast<size_t>(items + 1) * 4);
+  // the short-context plan keeps the logits [T][ld] at offset 0 instead
+  if (use_logits_plan(p)) {
+    const size_t lb = up(static_cast<size_t>(p->num_rows) * logits_plan_ld(p) * 4);
+    if (lb > ws.bytes) ws.bytes = lb;
+  }
   return ws;
 }
 
@@ -378,15 +390,78 @@ fp4idx_status_t fp4idx_topk_merge(const fp4idx_problem_t* problem, int32_t k, ui
   return FP4IDX_OK;
 }
 
+}  // extern "C"
+
+namespace fp4idx {
+namespace {
+
+// Logits of every row into `logits` [T][ld], then each row's top-k from them.
+fp4idx_status_t logits_then_select(const fp4idx_problem_t* problem, const float* w, int64_t w_row_stride,
+                                   float* logits, int64_t ld, int32_t k, uint32_t flags, int32_t* indices,
+                                   float* values, int32_t* valid_count, void* stream) {
+  fp4idx_status_t s = fp4idx_logits(problem, w, w_row_stride, logits, ld, stream);
+  if (s != FP4IDX_OK) return s;
+  if (problem->num_rows == 0) return FP4IDX_OK;
+  DeviceInfo* dev;
+  if ((s = device_info(&dev)) != FP4IDX_OK) return s;
+  MergeParams mp;
+  std::memset(&mp, 0, sizeof(mp));
+  const int R = score_rows_per_cta(problem->num_heads);
+  if ((s = fill_score_params(problem, w, w_row_stride, &mp.sp, R, dev->err)) != FP4IDX_OK) return s;
+  mp.sp.logits = logits;
+  mp.sp.ld = ld;
+  mp.sp.k = k;
+  mp.rows_per_cta = R;
+  mp.flags = flags & FP4IDX_TOPK_SORTED;
+  mp.indices = indices;
+  mp.values = values;
+  mp.valid_count = valid_count;
+  cudaError_t e = launch_topk_select(mp, problem->num_rows, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "select launch");
+  return FP4IDX_OK;
+}
+
+}  // namespace
+}  // namespace fp4idx
+
+extern "C" {
+
 fp4idx_status_t fp4idx_topk(const fp4idx_problem_t* problem, const float* w, int64_t w_row_stride, int32_t k,
                             uint32_t flags, int32_t* indices, float* values, int32_t* valid_count,
                             void* workspace, size_t workspace_bytes, void* stream) {
   g_msg[0] = 0;
-  if (flags & ~static_cast<uint32_t>(FP4IDX_TOPK_SORTED)) return fail(FP4IDX_EINVAL, "unknown flags 0x%x", flags);
+  if (flags & ~static_cast<uint32_t>(FP4IDX_TOPK_SORTED | FP4IDX_TOPK_STREAMING))
+    return fail(FP4IDX_EINVAL, "unknown flags 0x%x", flags);
   if (!indices) return fail(FP4IDX_EINVAL, "indices is NULL");
+  if (!(flags & FP4IDX_TOPK_STREAMING) && problem && check_problem(problem) == FP4IDX_OK &&
+      use_logits_plan(problem)) {
+    // same validation and workspace contract as the streaming plan
+    ScoreParams sp;
+    int ctas = 0;
+    fp4idx_status_t s = topk_prepare(problem, w, w_row_stride, k, workspace, workspace_bytes, true, &sp, &ctas);
+    if (s != FP4IDX_OK) return s;
+    if (!aligned(workspace, 16)) return fail(FP4IDX_EINVAL, "workspace must be 16-byte aligned");
+    return logits_then_select(problem, w, w_row_stride, static_cast<float*>(workspace), logits_plan_ld(problem), k,
+                              flags, indices, values, valid_count, stream);
+  }
   fp4idx_status_t s = fp4idx_topk_score(problem, w, w_row_stride, k, workspace, workspace_bytes, stream);
   if (s != FP4IDX_OK) return s;
-  return fp4idx_topk_merge(problem, k, flags, indices, values, valid_count, workspace, workspace_bytes, stream);
+  return fp4idx_topk_merge(problem, k, flags & FP4IDX_TOPK_SORTED, indices, values, valid_count, workspace,
+                           workspace_bytes, stream);
+}
+
+fp4idx_status_t fp4idx_logits_topk(const fp4idx_problem_t* problem, const float* w, int64_t w_row_stride,
+                                   float* logits, int64_t ld, int32_t k, uint32_t flags, int32_t* indices,
+                                   float* values, int32_t* valid_count, void* stream) {
+  g_msg[0] = 0;
+  if (flags & ~static_cast<uint32_t>(FP4IDX_TOPK_SORTED)) return fail(FP4IDX_EINVAL, "unknown flags 0x%x", flags);
+  if (!indices) return fail(FP4IDX_EINVAL, "indices is NULL");
+  fp4idx_status_t s = check_problem(problem);
+  if (s != FP4IDX_OK) return s;
+  if ((s = check_weighted(problem, w, w_row_stride)) != FP4IDX_OK) return s;
+  if (k < 1 || k > 2048) return fail(FP4IDX_EUNSUPPORTED, "k = %d: supported 1..2048", k);
+  if (ld < problem->max_seqlen_k) return fail(FP4IDX_EINVAL, "ld must be >= max_seqlen_k");
+  return logits_then_select(problem, w, w_row_stride, logits, ld, k, flags, indices, values, valid_count, stream);
 }
 
 fp4idx_status_t fp4idx_block_scores(const fp4idx_problem_t* problem, float* scores, void* stream) {

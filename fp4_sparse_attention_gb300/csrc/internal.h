@@ -111,6 +111,8 @@ inline cudaError_t launch_score(const ScoreParams& p, int format, int mode, int 
 constexpr int kMaxMergeSlots = 256;
 // many_rows: the small-shared-memory variant (several CTAs per SM).
 cudaError_t launch_topk_merge(const MergeParams& p, int rows, bool many_rows, cudaStream_t stream);
+// Exact top-k of each row from p.sp.logits [T][p.sp.ld] (visibility from the problem).
+cudaError_t launch_topk_select(const MergeParams& p, int rows, cudaStream_t stream);
 cudaError_t launch_block_scores(const BlockParams& p, int format, dim3 grid, cudaStream_t stream);
 
 // Sets the message fp4idx_last_error_message() returns on this thread.

@@ -1,5 +1,6 @@
-// topk_merge.cu -- exact top-k of each query row from the per-CTA partial
-// candidate lists written by the scorer in top-k mode.
+// topk_merge.cu -- exact top-k of each query row: from the per-CTA partial
+// candidate lists written by the scorer in top-k mode (the merge), or
+// straight from the row's logits (the short-context plan).
 //
 // Every scorer CTA kept, for each row of each item it touched, a superset of
 // the top-k of the keys it scored.  The union of those lists therefore holds
@@ -31,6 +32,62 @@ struct MergeSmem {
   uint64_t out[2048];
   uint64_t buf[kLocal];
 };
+
+// The n_out keys >= T of a row (from shared memory when `local`, else
+// through for_each_global), optionally sorted by (value desc, position asc),
+// written as logical positions / values / valid count of row t.
+template <int kLocal, class ForEachGlobal>
+__device__ void gather_sort_write(MergeSmem<kLocal>* sm, const Group<kMergeThreads, 0>& g, uint64_t T, int n_out,
+                                  bool local, int M, ForEachGlobal&& for_each_global, uint32_t flags, int t, int k,
+                                  int32_t* indices, float* values, int32_t* valid_count) {
+  const int tid = g.tid;
+  if (tid == 0) sm->info[3] = 0;
+  g.sync();
+  auto keep = [&](uint64_t key) {
+    if (key >= T) {
+      const uint32_t o = atomicAdd(reinterpret_cast<uint32_t*>(&sm->info[3]), 1u);
+      if (o < 2048u) sm->out[o] = key;
+    }
+  };
+  if (local) {
+    for (int e = tid; e < M; e += kMergeThreads) keep(sm->buf[e]);
+  } else {
+    for_each_global([&](uint64_t key, int) { keep(key); });
+  }
+  g.sync();
+
+  if (flags & 1u) {
+    int P2 = 1;
+    while (P2 < n_out) P2 <<= 1;
+    for (int i = n_out + tid; i < P2; i += kMergeThreads) sm->out[i] = 0;
+    g.sync();
+    for (int size = 2; size <= P2; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = tid; i < P2; i += kMergeThreads) {
+          const int j = i ^ stride;
+          if (j > i) {
+            const uint64_t a = sm->out[i], c = sm->out[j];
+            const bool desc = (i & size) == 0;
+            if (desc ? (a < c) : (a > c)) {
+              sm->out[i] = c;
+              sm->out[j] = a;
+            }
+          }
+        }
+        g.sync();
+      }
+    }
+  }
+
+  const int64_t row = static_cast<int64_t>(t) * k;
+  for (int j = tid; j < k; j += kMergeThreads) {
+    const bool have = j < n_out;
+    const uint64_t key = have ? sm->out[j] : 0;
+    indices[row + j] = have ? key_pos(key) : -1;
+    if (values) values[row + j] = have ? key_value(key) : -INFINITY;
+  }
+  if (tid == 0 && valid_count) valid_count[t] = n_out;
+}
 
 template <int kMergeLocal>
 __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const __grid_constant__ MergeParams mp) {
@@ -136,53 +193,84 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const __grid_
     }
   }
 
-  // gather the selected keys
-  if (tid == 0) sm->info[3] = 0;
-  g.sync();
-  auto keep = [&](uint64_t key) {
-    if (key >= T) {
-      const uint32_t o = atomicAdd(reinterpret_cast<uint32_t*>(&sm->info[3]), 1u);
-      if (o < 2048u) sm->out[o] = key;
-    }
+  gather_sort_write(sm, g, T, n_out, local, M, for_each_global, mp.flags, t, k, mp.indices, mp.values,
+                    mp.valid_count);
+}
+
+// Exact top-k of row t straight from its logits (the short-context plan):
+// every visible position's key (value, position) is built from logits[t][s],
+// a NaN logit becomes key 0 (never selected), and the same bucket + radix
+// selection as the merge runs over them -- in shared memory when the row
+// fits, else re-reading the logits.
+constexpr int kSelectLocal = 20480;
+
+__global__ void __launch_bounds__(kMergeThreads) topk_select_kernel(const __grid_constant__ MergeParams mp) {
+  const ScoreParams& p = mp.sp;
+  extern __shared__ uint8_t smem_raw[];
+  using Smem = MergeSmem<kSelectLocal>;
+  Smem* sm = reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int t = blockIdx.x;
+  const int k = p.k;
+  Group<kMergeThreads, 0> g{tid};
+
+  // request of row t and its visible key count
+  int lo = 0, hi = p.num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(p.cu_seqlens_q + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  ItemInfo it;
+  it.b = lo;
+  it.k_len = max(__ldg(p.cu_seqlens_k + lo + 1) - __ldg(p.cu_seqlens_k + lo), 0);
+  const int M = static_cast<int>(min(static_cast<int64_t>(row_visible(p, it, t)), p.ld));
+  const bool local = M <= kSelectLocal;
+  const float* row_logits = p.logits + static_cast<int64_t>(t) * p.ld;
+  auto key_at = [&](int s) -> uint64_t {
+    const float v = __ldg(row_logits + s);
+    return isnan(v) ? 0ull : topk_key(v, static_cast<uint32_t>(s));
   };
-  if (local) {
-    for (int e = tid; e < M; e += kMergeThreads) keep(sm->buf[e]);
-  } else {
-    for_each_global([&](uint64_t key, int) { keep(key); });
-  }
-  g.sync();
+  auto for_each_global = [&](auto&& fn) {
+    for (int e = tid; e < M; e += kMergeThreads) fn(key_at(e), e);
+  };
 
-  if (mp.flags & 1u) {
-    int P2 = 1;
-    while (P2 < n_out) P2 <<= 1;
-    for (int i = n_out + tid; i < P2; i += kMergeThreads) sm->out[i] = 0;
-    g.sync();
-    for (int size = 2; size <= P2; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int i = tid; i < P2; i += kMergeThreads) {
-          const int j = i ^ stride;
-          if (j > i) {
-            const uint64_t a = sm->out[i], c = sm->out[j];
-            const bool desc = (i & size) == 0;
-            if (desc ? (a < c) : (a > c)) {
-              sm->out[i] = c;
-              sm->out[j] = a;
-            }
-          }
-        }
-        g.sync();
-      }
+  for (int i = tid; i < kHistBins; i += kMergeThreads) sm->hist[i] = 0;
+  if (tid == 0) sm->info[4] = 0;
+  g.sync();
+  // pass 1: keys (into shared memory when the row fits), bucket histogram, non-NaN count
+  uint32_t mine = 0;
+  for_each_global([&](uint64_t key, int at) {
+    if (local) sm->buf[at] = key;
+    if (key != 0) {
+      atomicAdd(&sm->hist[key >> kHistShift], 1u);
+      ++mine;
+    }
+  });
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+  if (lane == 0) atomicAdd(reinterpret_cast<uint32_t*>(&sm->info[4]), mine);
+  g.sync();
+  const int n_valid = sm->info[4];
+  const int n_out = min(n_valid, k);
+
+  auto hist_get = [&](int bin) { return sm->hist[bin]; };
+  uint64_t T = 1;  // keeps every non-NaN key (key 0 marks NaN)
+  if (n_valid > k) {
+    uint32_t above = 0;
+    const uint32_t bkt = find_kth_bucket(g, hist_get, static_cast<uint32_t>(k), &sm->sc, &above);
+    const uint32_t rank = static_cast<uint32_t>(k) - above;
+    if (local) {
+      T = select_in_bucket(g, bkt, rank, &sm->sc, [&](auto&& fn) {
+        for (int e = tid; e < M; e += kMergeThreads) fn(sm->buf[e]);
+      });
+    } else {
+      T = select_in_bucket(g, bkt, rank, &sm->sc,
+                           [&](auto&& fn) { for_each_global([&](uint64_t key, int) { fn(key); }); });
     }
   }
-
-  const int64_t row = static_cast<int64_t>(t) * k;
-  for (int j = tid; j < k; j += kMergeThreads) {
-    const bool have = j < n_out;
-    const uint64_t key = have ? sm->out[j] : 0;
-    mp.indices[row + j] = have ? key_pos(key) : -1;
-    if (mp.values) mp.values[row + j] = have ? key_value(key) : -INFINITY;
-  }
-  if (tid == 0 && mp.valid_count) mp.valid_count[t] = n_out;
+  gather_sort_write(sm, g, T, n_out, local, M, for_each_global, mp.flags, t, k, mp.indices, mp.values,
+                    mp.valid_count);
 }
 
 template <int kLocal>
@@ -195,6 +283,15 @@ cudaError_t launch_merge_t(const MergeParams& p, int rows, cudaStream_t stream) 
 }
 
 }  // namespace
+
+cudaError_t launch_topk_select(const MergeParams& p, int rows, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  const int bytes = static_cast<int>(sizeof(MergeSmem<kSelectLocal>) + 16);
+  cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  topk_select_kernel<<<rows, kMergeThreads, bytes, stream>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_topk_merge(const MergeParams& p, int rows, bool many_rows, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;

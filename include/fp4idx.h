@@ -72,6 +72,7 @@ typedef enum fp4idx_status {
 
 /* Flags of fp4idx_topk. */
 #define FP4IDX_TOPK_SORTED 0x1u     /* order each row by (value desc, index asc)  */
+#define FP4IDX_TOPK_STREAMING 0x2u  /* fp4idx_topk: always the streaming plan     */
 
 /*
  * The problem: queries, the paged key cache and the visibility rule.
@@ -167,10 +168,16 @@ fp4idx_status_t fp4idx_block_scores(const fp4idx_problem_t* problem, float* scor
  *                logit is NaN -- only possible with NaN/inf scale codes,
  *                outside the formats' contract -- has no rank and is never
  *                selected; it does not count towards vis(t) here.)
+ *   flags        FP4IDX_TOPK_SORTED; FP4IDX_TOPK_STREAMING forces the
+ *                streaming plan below (the results are the same).
  *   workspace    device scratch of at least fp4idx_topk_workspace_bytes();
  *                may be NULL when that size is 0.  Contents need no
  *                initialisation and are meaningless after the call.
- * Full logits are never written to memory.
+ * Plans, chosen from host scalars only: short contexts (max_seqlen_k <=
+ * 16,384 and T * max_seqlen_k <= 2^24) write the rows' logits into the
+ * workspace and select from them; otherwise the scorer keeps a streaming
+ * top-k per CTA and a merge selects each row's top-k, so full logits never
+ * reach memory.
  * Supported: num_kv_heads == 1; num_heads in {8, 16, 32, 64}; 1 <= k <= 2048.
  */
 size_t fp4idx_topk_workspace_bytes(const fp4idx_problem_t* problem, int32_t k);
@@ -180,11 +187,13 @@ fp4idx_status_t fp4idx_topk(const fp4idx_problem_t* problem, const float* w,
                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * The two phases of fp4idx_topk, for callers that schedule them separately
- * (fp4idx_topk is exactly fp4idx_topk_score followed by fp4idx_topk_merge
- * on the same stream, problem, k and workspace).
- *   fp4idx_topk_score  runs the scorer and leaves, in the workspace, the exact
- *                      top-k of every row within each CTA's share of the keys.
+ * The two phases of fp4idx_topk's streaming plan, for callers that schedule
+ * them separately (fp4idx_topk with FP4IDX_TOPK_STREAMING is exactly
+ * fp4idx_topk_score followed by fp4idx_topk_merge on the same stream,
+ * problem, k and workspace).
+ *   fp4idx_topk_score  runs the scorer and leaves, in the workspace, a
+ *                      superset of the top-k of every row within each CTA's
+ *                      share of the keys.
  *   fp4idx_topk_merge  selects each row's exact top-k from those partials and
  *                      writes indices / values / valid_count as fp4idx_topk.
  * The workspace must not be modified between the two calls.
@@ -195,6 +204,20 @@ fp4idx_status_t fp4idx_topk_score(const fp4idx_problem_t* problem, const float* 
 fp4idx_status_t fp4idx_topk_merge(const fp4idx_problem_t* problem, int32_t k, uint32_t flags,
                                   int32_t* indices, float* values, int32_t* valid_count,
                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Full logits and their top-k in one call: fp4idx_logits into the caller's
+ * logits [T][ld] (ld >= max_seqlen_k), then each row's exact top-k selected
+ * from those logits (same outputs as fp4idx_topk; flags: FP4IDX_TOPK_SORTED).
+ * No workspace: the logits are the intermediate.  For a step that needs both
+ * outputs (e.g. the verify rows of a short context), one scorer pass
+ * instead of two.
+ * Supported: as fp4idx_logits and fp4idx_topk.
+ */
+fp4idx_status_t fp4idx_logits_topk(const fp4idx_problem_t* problem, const float* w,
+                                   int64_t w_row_stride, float* logits, int64_t ld, int32_t k,
+                                   uint32_t flags, int32_t* indices, float* values,
+                                   int32_t* valid_count, void* stream);
 
 /*
  * fp4idx_topk without a caller-supplied workspace, for callers that cannot

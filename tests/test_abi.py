@@ -115,3 +115,12 @@ def test_block_scores_rejects_unsupported_groups_on_host(lib, over, status):
 def test_block_scores_null_output(lib):
     c = _problem()
     assert lib.fp4idx_block_scores(ctypes.byref(c), None, None) == 1
+
+
+def test_logits_topk_rejects_bad_arguments_on_host(lib):
+    c = _problem()
+    vp = ctypes.c_void_p(1 << 20)
+    assert lib.fp4idx_logits_topk(ctypes.byref(c), vp, 32, vp, 1024, 64, 0x2, vp, None, None, None) == 1  # flags
+    assert lib.fp4idx_logits_topk(ctypes.byref(c), vp, 32, vp, 512, 64, 0, vp, None, None, None) == 1  # ld
+    assert lib.fp4idx_logits_topk(ctypes.byref(c), vp, 32, vp, 1024, 0, 0, vp, None, None, None) == 2  # k
+    assert lib.fp4idx_topk(ctypes.byref(c), vp, 32, 64, 0x4, vp, None, None, vp, 1 << 30, None) == 1  # flags

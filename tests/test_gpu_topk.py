@@ -11,16 +11,16 @@ from tests.parity import compare_topk
 pytestmark = pytest.mark.gpu
 
 
-def _run(p, k, sorted_=False, dp=None):
+def _run(p, k, sorted_=False, dp=None, streaming=False):
     dp = dp or B.DeviceProblem.from_host(p)
-    idx, val, cnt = B.fp4idx_topk(dp, torch.as_tensor(p.w).cuda(), k, sorted=sorted_)
+    idx, val, cnt = B.fp4idx_topk(dp, torch.as_tensor(p.w).cuda(), k, sorted=sorted_, streaming=streaming)
     torch.cuda.synchronize()
     assert B.fp4idx_get_error() == 0
     return idx.cpu().numpy(), val.cpu().numpy(), cnt.cpu().numpy()
 
 
-def _check(p, k, rows=None, sorted_=False):
-    idx, val, cnt = _run(p, k, sorted_)
+def _check(p, k, rows=None, sorted_=False, streaming=False):
+    idx, val, cnt = _run(p, k, sorted_, streaming=streaming)
     rows = np.arange(p.num_rows) if rows is None else np.asarray(rows)
     return compare_topk(p, rows, k, idx[rows], val[rows], cnt[rows], sorted_order=sorted_)
 
@@ -104,3 +104,46 @@ def test_many_rows_with_one_long_request():
     idx, val, cnt = _run(p, 2048, sorted_=True)
     rows = [0, 1, 2, 3, 4, 300, 639]
     compare_topk(p, rows, 2048, idx[rows], val[rows], cnt[rows], sorted_order=True)
+
+
+# Short contexts take the logits plan by default; the same cases through the
+# streaming plan (scorer top-k partials + merge).
+@pytest.mark.parametrize("maker,k,sorted_", [(wl.tiny_mx_decode, 64, True), (wl.verify_decode_16k, 2048, False)])
+def test_streaming_plan_on_short_contexts(maker, k, sorted_):
+    _check(maker(), k, sorted_=sorted_, streaming=True)
+
+
+@pytest.mark.parametrize("fmt", [wl.MXFP4, wl.NVFP4])
+def test_streaming_plan_ragged_and_causal(fmt):
+    p = wl.make_problem(name=f"ragged_stream_f{fmt}", seed=230 + fmt, fmt=fmt, q_lens=[4, 1, 3, 6],
+                        k_lens=[5000, 129, 1, 2500], num_heads=32, e8m0_range=(120, 134), weights="normal",
+                        cache_pages=200)
+    _check(p, 300, sorted_=True, streaming=True)
+    p = wl.make_problem(name=f"causal_stream_f{fmt}", seed=240 + fmt, fmt=fmt, q_lens=[300, 77], k_lens=[300, 500],
+                        num_heads=64, e8m0_range=(120, 134), weights="normal", visibility="causal",
+                        qo_offset=[0, 400])
+    _check(p, 64, streaming=True)
+
+
+def test_logits_plan_matches_streaming_plan_exactly():
+    # both plans are exact: identical outputs on a tie-free problem
+    p = wl.verify_decode_16k(strict=True)
+    a = _run(p, 2048, sorted_=True)
+    b = _run(p, 2048, sorted_=True, streaming=True)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+
+
+def test_logits_topk_fused_call():
+    from tests.parity import compare_scores
+    for p, k in ((wl.verify_decode_16k(), 2048), (wl.tiny_mx_decode(), 64)):
+        dp = B.DeviceProblem.from_host(p)
+        w = torch.as_tensor(p.w).cuda()
+        logits, idx, val, cnt = B.fp4idx_logits_topk(dp, w, k, sorted=True)
+        torch.cuda.synchronize()
+        assert B.fp4idx_get_error() == 0
+        logits = logits.cpu().numpy()
+        ref, bound, safe = oracle.logits_rows(p, logits.shape[1])
+        compare_scores(logits, ref, bound, safe, p.name + " logits")
+        rows = np.arange(p.num_rows)
+        compare_topk(p, rows, k, idx.cpu().numpy(), val.cpu().numpy(), cnt.cpu().numpy(), sorted_order=True)
