@@ -148,12 +148,26 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const __grid_
   const int n_out = M < k ? M : k;
 
   // visit every candidate in global memory: one warp per list
+  // eight loads in flight per lane, so a long list is not a chain of L2 round trips
   auto for_each_global = [&](auto&& fn) {
+    constexpr int U = 8;
     for (int i = warp; i < nslots; i += kMergeWarps) {
       const uint64_t* keys = p.part_keys + sm->slot_part[i] * cap;
       const int n = sm->slot_cnt[i];
       const int off = sm->slot_off[i];
-      for (int e = lane; e < n; e += 32) fn(__ldg(keys + e), off + e);
+      for (int e0 = lane; e0 < n; e0 += 32 * U) {
+        uint64_t v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int e = e0 + 32 * u;
+          v[u] = e < n ? __ldg(keys + e) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int e = e0 + 32 * u;
+          if (e < n) fn(v[u], off + e);
+        }
+      }
     }
   };
   // pass 1: bucket histogram (and the copy into shared memory when it fits)
@@ -227,12 +241,32 @@ __global__ void __launch_bounds__(kMergeThreads) topk_select_kernel(const __grid
   const int M = static_cast<int>(min(static_cast<int64_t>(row_visible(p, it, t)), p.ld));
   const bool local = M <= kSelectLocal;
   const float* row_logits = p.logits + static_cast<int64_t>(t) * p.ld;
-  auto key_at = [&](int s) -> uint64_t {
-    const float v = __ldg(row_logits + s);
-    return isnan(v) ? 0ull : topk_key(v, static_cast<uint32_t>(s));
-  };
+  auto key_of = [](float v, int s) -> uint64_t { return isnan(v) ? 0ull : topk_key(v, static_cast<uint32_t>(s)); };
+  // the row's keys, four float4 loads in flight per thread (rows are 16-byte
+  // aligned: ld % 4 == 0 and a 16-byte aligned base)
   auto for_each_global = [&](auto&& fn) {
-    for (int e = tid; e < M; e += kMergeThreads) fn(key_at(e), e);
+    constexpr int U = 4;
+    const float4* row4 = reinterpret_cast<const float4*>(row_logits);
+    const int M4 = M >> 2;
+    for (int e0 = tid; e0 < M4; e0 += kMergeThreads * U) {
+      float4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = e0 + kMergeThreads * u;
+        v[u] = e < M4 ? __ldg(row4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = e0 + kMergeThreads * u;
+        if (e < M4) {
+          fn(key_of(v[u].x, 4 * e), 4 * e);
+          fn(key_of(v[u].y, 4 * e + 1), 4 * e + 1);
+          fn(key_of(v[u].z, 4 * e + 2), 4 * e + 2);
+          fn(key_of(v[u].w, 4 * e + 3), 4 * e + 3);
+        }
+      }
+    }
+    for (int e = 4 * M4 + tid; e < M; e += kMergeThreads) fn(key_of(__ldg(row_logits + e), e), e);
   };
 
   for (int i = tid; i < kHistBins; i += kMergeThreads) sm->hist[i] = 0;
