@@ -198,6 +198,7 @@ fp4idx_status_t fill_score_params(const fp4idx_problem_t* pr, const float* w, in
   sp->num_heads = pr->num_heads;
   sp->num_seqs = pr->num_seqs;
   sp->row_groups = (pr->max_seqlen_q + rows_per_cta - 1) / rows_per_cta;
+  sp->max_seqlen_k = pr->max_seqlen_k;
   sp->w = w;
   sp->w_row_stride = w_row_stride;
   sp->err = err;

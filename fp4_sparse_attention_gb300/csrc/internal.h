@@ -37,6 +37,7 @@ struct ScoreParams {
   int32_t num_heads;
   int32_t num_seqs;
   int32_t row_groups;       // ceil(max_seqlen_q / R) row groups per request
+  int32_t max_seqlen_k;     // host bound of every request's key count
   const float* w;
   int64_t w_row_stride;
   int32_t total_tiles;      // logits: output tiles per row group, ceil(ld / 128)

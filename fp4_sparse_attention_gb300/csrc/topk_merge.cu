@@ -307,6 +307,214 @@ __global__ void __launch_bounds__(kMergeThreads) topk_select_kernel(const __grid
                     mp.valid_count);
 }
 
+// ---------------------------------------------------------------------------
+// Rows of at most 16,384 visible keys: one 1024-thread CTA per row holds 16
+// keys per thread in registers and finds the k-th largest 64-bit key by
+// radix levels (11-bit digits), each level counting only the keys that still
+// match the prefix; a level whose digit bucket holds exactly the remaining
+// rank ends the search.  Then one uniform pass appends the keys >= the
+// threshold.
+// ---------------------------------------------------------------------------
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallPer = 16;
+constexpr int kSmallMaxKeys = kSmallThreads * kSmallPer;
+constexpr int kSmallCopies = 8;  // histogram copies: warp w counts into copy w % 8
+
+struct SmallSelectSmem {
+  uint32_t hist[kSmallCopies][2048];
+  uint32_t warp_sum[32];
+  uint32_t bcast[4];
+  uint64_t out[2048];
+};
+
+// Block-wide (1024 threads) exclusive prefix and total of v; `ws` holds 32
+// words.  Ends with a barrier, so ws may be reused after it.
+__device__ __forceinline__ uint32_t block_excl_prefix(uint32_t v, uint32_t* ws, uint32_t* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) ws[wid] = incl;
+  __syncthreads();
+  uint32_t before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < 32; ++w) {
+    const uint32_t x = ws[w];
+    before += w < wid ? x : 0u;
+    all += x;
+  }
+  __syncthreads();
+  *total = all;
+  return before + incl - v;
+}
+
+__global__ void __launch_bounds__(kSmallThreads) topk_select_small_kernel(const __grid_constant__ MergeParams mp) {
+  const ScoreParams& p = mp.sp;
+  extern __shared__ uint8_t smem_raw[];
+  SmallSelectSmem& sm = *reinterpret_cast<SmallSelectSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
+  const int tid = threadIdx.x;
+  const int wid = tid >> 5;
+  const int t = blockIdx.x;
+  const int k = p.k;
+  uint32_t* my_hist = sm.hist[wid % kSmallCopies];
+
+  int lo = 0, hi = p.num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(p.cu_seqlens_q + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  ItemInfo it;
+  it.b = lo;
+  it.k_len = max(__ldg(p.cu_seqlens_k + lo + 1) - __ldg(p.cu_seqlens_k + lo), 0);
+  const int M = static_cast<int>(min(static_cast<int64_t>(row_visible(p, it, t)),
+                                     min(p.ld, static_cast<int64_t>(kSmallMaxKeys))));
+
+  // keys: thread tid holds positions 4 (tid + 1024 u) + c; 0 = absent or NaN
+  const float4* row4 = reinterpret_cast<const float4*>(p.logits + static_cast<int64_t>(t) * p.ld);
+  float4 v[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int e = tid + kSmallThreads * u;
+    v[u] = 4 * e < M ? __ldg(row4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int i = tid; i < kSmallCopies * 2048; i += kSmallThreads) (&sm.hist[0][0])[i] = 0;
+  uint64_t key[kSmallPer];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int pos = 4 * (tid + kSmallThreads * u);
+    const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const bool ok = pos + c < M && !isnan(f[c]);
+      key[4 * u + c] = ok ? topk_key(f[c], static_cast<uint32_t>(pos + c)) : 0ull;
+    }
+  }
+  __syncthreads();
+
+  // Radix levels over the 64-bit keys: the 32 value bits as 11 + 11 + 10,
+  // then the inverted position, whose bits 31..14 are all ones (positions
+  // < 2^14) and are fixed without a level, then 7 + 7 position bits.  Each
+  // level counts only the keys matching the prefix fixed so far; the first
+  // level's total is the number of present keys.
+  constexpr int kLevels = 5;
+  constexpr int kWidth[kLevels] = {11, 11, 10, 7, 7};
+  uint64_t prefix = 0;
+  int bits = 0;
+  uint32_t rank = static_cast<uint32_t>(k);
+  uint32_t n_valid = 0;
+  bool all_kept = false;
+#pragma unroll 1
+  for (int level = 0; level < kLevels; ++level) {
+    if (level == 3) {
+      prefix = (prefix << 18) | 0x3FFFFull;
+      bits += 18;
+    }
+    const int w = kWidth[level];
+    const int shift = 64 - bits - w;
+    const uint32_t nb = 1u << w;
+    if (level > 0) {
+      for (int i = tid; i < kSmallCopies * 2048; i += kSmallThreads) (&sm.hist[0][0])[i] = 0;
+      __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < kSmallPer; ++i) {
+      const uint64_t kk = key[i];
+      if (kk != 0 && (bits == 0 || (kk >> (64 - bits)) == prefix))
+        atomicAdd(&my_hist[static_cast<uint32_t>(kk >> shift) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    // this thread's digits: 2 (w = 11) or 1 (w <= 10), summed over the copies
+    const int per = nb >= kSmallThreads ? static_cast<int>(nb / kSmallThreads) : 1;
+    const int d0 = tid * per;
+    uint32_t cnt[2] = {0, 0};
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+      if (i < per && d0 + i < static_cast<int>(nb))
+#pragma unroll
+        for (int c = 0; c < kSmallCopies; ++c) cnt[i] += sm.hist[c][d0 + i];
+    const uint32_t sloc = cnt[0] + cnt[1];
+    // keys in digits above mine: exclusive suffix = total - inclusive prefix
+    uint32_t total;
+    const uint32_t pre = block_excl_prefix(sloc, sm.warp_sum, &total);
+    const uint32_t after = total - pre - sloc;
+    if (level == 0) {
+      n_valid = total;
+      if (n_valid <= static_cast<uint32_t>(k)) {
+        all_kept = true;
+        break;
+      }
+    }
+    if (after < rank && after + sloc >= rank) {
+      uint32_t acc = after;
+      for (int i = per - 1; i >= 0; --i) {
+        if (acc + cnt[i] >= rank) {
+          sm.bcast[0] = static_cast<uint32_t>(d0 + i);
+          sm.bcast[1] = acc;
+          sm.bcast[2] = cnt[i];
+          break;
+        }
+        acc += cnt[i];
+      }
+    }
+    __syncthreads();
+    const uint32_t d = sm.bcast[0];
+    rank -= sm.bcast[1];
+    const uint32_t eq = sm.bcast[2];
+    prefix = (prefix << w) | d;
+    bits += w;
+    if (eq == rank) break;  // every key with this prefix is in the top-k
+  }
+  const uint64_t T = all_kept ? 1ull : (bits == 64 ? prefix : prefix << (64 - bits));
+  const int n_out = static_cast<int>(min(n_valid, static_cast<uint32_t>(k)));
+
+  // the n_out keys >= T, at offsets from a block prefix of per-thread counts
+  uint32_t mask = 0;
+#pragma unroll
+  for (int i = 0; i < kSmallPer; ++i) mask |= (key[i] != 0 && key[i] >= T) ? (1u << i) : 0u;
+  uint32_t total_kept;
+  uint32_t o = block_excl_prefix(static_cast<uint32_t>(__popc(mask)), sm.warp_sum, &total_kept);
+#pragma unroll
+  for (int i = 0; i < kSmallPer; ++i)
+    if ((mask >> i) & 1u) {
+      if (o < 2048u) sm.out[o] = key[i];
+      ++o;
+    }
+  __syncthreads();
+  if (mp.flags & 1u) {
+    int P2 = 1;
+    while (P2 < n_out) P2 <<= 1;
+    for (int i = n_out + tid; i < P2; i += kSmallThreads) sm.out[i] = 0;
+    __syncthreads();
+    for (int size = 2; size <= P2; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = tid; i < P2; i += kSmallThreads) {
+          const int j = i ^ stride;
+          if (j > i) {
+            const uint64_t a = sm.out[i], c = sm.out[j];
+            const bool desc = (i & size) == 0;
+            if (desc ? (a < c) : (a > c)) {
+              sm.out[i] = c;
+              sm.out[j] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+  }
+  const int64_t row = static_cast<int64_t>(t) * k;
+  for (int j = tid; j < k; j += kSmallThreads) {
+    const bool have = j < n_out;
+    const uint64_t kk = have ? sm.out[j] : 0;
+    mp.indices[row + j] = have ? key_pos(kk) : -1;
+    if (mp.values) mp.values[row + j] = have ? key_value(kk) : -INFINITY;
+  }
+  if (tid == 0 && mp.valid_count) mp.valid_count[t] = n_out;
+}
+
 template <int kLocal>
 cudaError_t launch_merge_t(const MergeParams& p, int rows, cudaStream_t stream) {
   const int bytes = static_cast<int>(sizeof(MergeSmem<kLocal>) + 16);
@@ -320,6 +528,13 @@ cudaError_t launch_merge_t(const MergeParams& p, int rows, cudaStream_t stream) 
 
 cudaError_t launch_topk_select(const MergeParams& p, int rows, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
+  if (p.sp.max_seqlen_k <= kSmallMaxKeys) {
+    const int sbytes = static_cast<int>(sizeof(SmallSelectSmem) + 16);
+    cudaError_t e = cudaFuncSetAttribute(topk_select_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sbytes);
+    if (e != cudaSuccess) return e;
+    topk_select_small_kernel<<<rows, kSmallThreads, sbytes, stream>>>(p);
+    return cudaGetLastError();
+  }
   const int bytes = static_cast<int>(sizeof(MergeSmem<kSelectLocal>) + 16);
   cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
