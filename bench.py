@@ -46,9 +46,9 @@ L2_BYTES = 129 * 1024 * 1024
 # DRAM bytes per launch from ncu captures, valid only for the kernel sources
 # they were taken on (sha256 of the csrc/ files, first 16 hex digits).
 RECORDED_TRAFFIC: dict = {
-    # ncu --set full, one launch of the long-decode top-k scorer: read 282,581,248 B
-    # + write 22,283,776 B.
-    ("long_decode", "scorer_topk"): {"sha": "556025c8954f9223", "bytes": 304865024},
+    # ncu --set full, one launch of the GQA NVFP4 block-score kernel: read 51,621,120 B
+    # + write 84,700,160 B.
+    ("block_scores", "block_scores"): {"sha": "d5e68283838be2fe", "bytes": 136321280},
 }
 
 
