@@ -13,19 +13,21 @@
 // the last visible key of every row of the item are not computed; their
 // scores are written as -inf.
 //
-// Warp roles (96 + 128 * kGroups threads):
-//   warp 0      producer: Q codes of each item by TMA and Q scales by cp.async
-//               (double buffered, one item ahead); per tile the K codes by TMA
-//               (64-byte swizzle) and the page's raw K scales by one bulk copy,
-//               into a kStages-deep ring: a handful of instructions per tile.
-//   warp 1      MMA: TMEM owner; one thread waits for the tile's scales and
-//               a free accumulator and issues two K = 64 block-scaled MMAs
-//               into a triple-buffered accumulator, nothing else.
-//   warp 2      scales: Q scales -> TMEM once per item; per tile the raw K
-//               scales are transposed into the 128-row scale layout (each
-//               row: the 32x4x4 atom line of its lane) and one tcgen05.cp
-//               128x128b/256b moves them to TMEM.
-//   warps 3..   epilogue, one group of four warps (one per TMEM lane
+// Warp roles (160 + 128 * kGroups threads):
+//   warps 0, 4  producers, alternate tiles: per tile the K codes by TMA
+//               (64-byte swizzle) and the page's raw K scales by one bulk
+//               copy, into a kStages-deep ring; warp 0 also loads Q codes of
+//               each item by TMA and Q scales by cp.async (double buffered,
+//               one item ahead).
+//   warp 1      MMA: TMEM owner; one thread waits for the tiles' scales and
+//               free accumulators and issues, two tiles at a time with their
+//               K halves interleaved, K = 64 block-scaled MMAs into a
+//               triple-buffered accumulator, nothing else.
+//   warps 2, 3  scales, alternate tiles: Q scales -> TMEM once per item
+//               (warp 2); per tile the raw K scales are transposed into the
+//               128-row scale layout (each row: the 32x4x4 atom line of its
+//               lane) and one tcgen05.cp 128x128b/256b moves them to TMEM.
+//   warps 5..   epilogue, one group of four warps (one per TMEM lane
 //               quadrant) per accumulator buffer, so three tiles drain at
 //               once: tcgen05.ld of the 128 columns, masked max
 //               (NaN-propagating), one fp32 store per (head, row).
@@ -43,9 +45,10 @@ namespace {
 
 constexpr int kStages = 16;
 constexpr int kAccBufs = 3;
-constexpr int kKsfSlots = 4;  // K-scale TMEM slots; > kAccBufs (see the MMA loop)
+constexpr int kKsfSlots = 8;  // K-scale slots (TMEM and staging); > kAccBufs (see the scale warps)
 constexpr int kGroups = kAccBufs;  // epilogue group e drains accumulator e
-constexpr int kThreads = 96 + 128 * kGroups;  // producer, MMA, scale warp, epilogue groups
+constexpr int kEpiWarp0 = 5;
+constexpr int kThreads = 32 * kEpiWarp0 + 128 * kGroups;  // producers, MMA, scale warps, epilogue groups
 constexpr uint32_t kTmemCols = 512;
 static_assert(kAccBufs < kKsfSlots, "K-scale slot reuse");
 
@@ -68,10 +71,10 @@ struct BlockLayout {
   static constexpr uint32_t kKsf = kKraw + kStages * 128 * F::G;       // kKsfSlots x kAtoms x 2048 (128 rows)
   static constexpr uint32_t kQsf = kKsf + kKsfSlots * F::kAtoms * 2048;  // 2 x kAtoms x 512
   static constexpr uint32_t kBars = kQsf + 2 * F::kAtoms * 512;
-  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 4 + kKsfSlots;
+  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 6 + kKsfSlots;
   static constexpr uint32_t kState = kBars + kNumBars * 8;
   static constexpr uint32_t kScan = (kState + sizeof(BlockCta) + 15) / 16 * 16;
-  static constexpr uint32_t kEnd = kScan + kThreads * 4;
+  static constexpr uint32_t kEnd = kScan + kThreads / 32 * 4;
   static constexpr uint32_t bytes() { return kEnd + 1024; }  // + alignment slack
   // TMEM columns
   static constexpr uint32_t kAccCol = 0;                      // kAccBufs x 128
@@ -139,30 +142,26 @@ __device__ __forceinline__ bool tile_computed(const BlockItem& it, int j) {
   return j * kTileKeys < it.maxvis;
 }
 
-// Cooperative over kThreads threads: total tiles and, for the global tile x
-// (if < total), the item holding it and that item's start.
-__device__ void block_plan(const BlockParams& p, int tid, int64_t x, int32_t* scan, BlockCta* st) {
+// Cooperative over kThreads threads: total tiles, this CTA's equal chunk of
+// them and the item holding the chunk's first tile (item0 = -1 when the CTA
+// has no tiles).
+__device__ void block_plan(const BlockParams& p, int tid, uint32_t* ws, BlockCta* st) {
   const int items = p.num_seqs * p.num_kv_heads * p.row_tiles;
   const int per = (items + kThreads - 1) / kThreads;
   const int i0 = tid * per, i1 = min(items, i0 + per);
   int32_t s = 0;
   for (int i = i0; i < i1; ++i) s += block_item(p, i).tiles;
-  scan[tid] = s;
-  __syncthreads();
+  if (tid == 0) st->item0 = -1;  // ordered before the writes below by the scan's barriers
+  uint32_t total_u;
+  const int32_t pre = static_cast<int32_t>(cta_excl_prefix<kThreads>(static_cast<uint32_t>(s), ws, &total_u));
+  const int32_t total = static_cast<int32_t>(total_u);
+  const int32_t chunk = (total + static_cast<int32_t>(gridDim.x) - 1) / static_cast<int32_t>(gridDim.x);
+  const int64_t x = static_cast<int64_t>(blockIdx.x) * chunk;
   if (tid == 0) {
-    int32_t acc = 0;
-    for (int j = 0; j < kThreads; ++j) {
-      const int32_t v = scan[j];
-      scan[j] = acc;
-      acc += v;
-    }
-    st->total_tiles = acc;
-    st->item0 = -1;
-    st->item0_start = 0;
+    st->total_tiles = total;
+    st->chunk = chunk;
   }
-  __syncthreads();
-  const int32_t pre = scan[tid];
-  if (x < st->total_tiles && pre <= x && x < pre + s) {
+  if (x < total && pre <= x && x < pre + s) {
     int32_t acc = pre;
     for (int i = i0; i < i1; ++i) {
       const int32_t ti = block_item(p, i).tiles;
@@ -255,22 +254,17 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
   auto qfull_bar = [&](uint32_t qb) { return bar0 + 8u * (2 * kStages + 2 * kAccBufs + qb); };
   auto qempty_bar = [&](uint32_t qb) { return bar0 + 8u * (2 * kStages + 2 * kAccBufs + 2 + qb); };
   auto sfready_bar = [&](int slot) { return bar0 + 8u * (2 * kStages + 2 * kAccBufs + 4 + slot); };
+  // Q scales of item slot qb in TMEM (committed by scale warp 2)
+  auto qsf_bar = [&](uint32_t qb) { return bar0 + 8u * (2 * kStages + 2 * kAccBufs + 4 + kKsfSlots + qb); };
 
   BlockCta* st = reinterpret_cast<BlockCta*>(smem + L::kState);
-  int32_t* scan = reinterpret_cast<int32_t*>(smem + L::kScan);
+  uint32_t* scan = reinterpret_cast<uint32_t*>(smem + L::kScan);
   volatile int* abort_flag = &st->abort;
 
   // ---- this CTA's chunk of the concatenated tile space
   if (threadIdx.x == 0) st->abort = 0;
-  block_plan(p, threadIdx.x, INT64_MAX, scan, st);
-  {
-    const int32_t total = st->total_tiles;
-    const int32_t chunk = (total + gridDim.x - 1) / gridDim.x;
-    const int64_t x = static_cast<int64_t>(blockIdx.x) * chunk;
-    if (chunk == 0 || x >= total) return;  // uniform: no work for this CTA
-    block_plan(p, threadIdx.x, x, scan, st);
-    if (threadIdx.x == 0) st->chunk = chunk;
-  }
+  block_plan(p, threadIdx.x, scan, st);
+  if (st->item0 < 0) return;  // uniform: no work for this CTA
 
   // ---- one-time setup
   if (threadIdx.x == 0) {
@@ -290,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
       mbar_init(qempty_bar(qb), 2);
     }
     for (int sl = 0; sl < kKsfSlots; ++sl) mbar_init(sfready_bar(sl), 1);
+    for (uint32_t qb = 0; qb < 2; ++qb) mbar_init(qsf_bar(qb), 1);
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc<kTmemCols>(smem_u32(&st->tmem_base));
@@ -309,17 +304,22 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
   const int slots = kTileKeys >> pshift;  // pages per tile: 2 (64-key pages) or 1 (128)
   const int rt_shift = p.rt_shift;
 
-  if (warp == 0) {
-    // ================================================================ producer
+  if (warp == 0 || warp == 4) {
+    // ================================================================ producers
+    // Two warps take alternate tiles (each tile's barrier wait, expect_tx and
+    // copies are a serial chain of ~500 cycles in one warp); warp 0 also
+    // loads each item's Q.
+    const uint32_t pidx = warp == 0 ? 0u : 1u;
     uint32_t tile_iter = 0, item_iter = 0;
     bool ok = true;
-    if (lane == 0) {
+    if (lane == 0 && pidx == 0) {
       prefetch_tmap(&p.tmap_k);
       prefetch_tmap(&p.tmap_q);
     }
     block_segments(p, st, [&](int, const BlockItem& it, int lo, int hi) {
       if (!ok) return;
       // -- Q of the item: codes by TMA, scales by cp.async into the atom
+      if (pidx == 0) {
       const uint32_t qb = item_iter & 1u, qph = (item_iter >> 1) & 1u;
       ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(qempty_bar(qb), qph ^ 1u, abort_flag, p.err) : false, 0);
       if (!ok) return;
@@ -343,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
         cp_async_arrive(qfull_bar(qb));
       }
       ++item_iter;
+      }
       // -- K tiles: lane l caches the physical id of logical page base + l
       const int32_t npages = (it.k_len + page - 1) >> pshift;
       const int32_t* table = p.block_table + it.table_base;
@@ -359,6 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
           base += 32;
           cur_ids = next_ids;
           next_ids = fetch(base + 32);
+        }
+        if ((tile_iter & 1u) != pidx) {  // the other producer's tile
+          ++tile_iter;
+          continue;
         }
         const int32_t phys0 = __shfl_sync(0xffffffffu, cur_ids, lp0 - base);
         const int32_t phys1 = __shfl_sync(0xffffffffu, cur_ids, lp0 - base + (slots - 1));
@@ -393,7 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
       // Let copies already in flight land before the CTA can exit.
       volatile int never = 0;
       const uint32_t first = tile_iter > static_cast<uint32_t>(kStages) ? tile_iter - kStages : 0;
-      for (uint32_t u = first; u < tile_iter; ++u) mbar_wait(full_bar(u % kStages), (u / kStages) & 1u, &never, p.err);
+      for (uint32_t u = first; u < tile_iter; ++u)
+        if ((u & 1u) == pidx) mbar_wait(full_bar(u % kStages), (u / kStages) & 1u, &never, p.err);
       for (uint32_t u = item_iter > 2u ? item_iter - 2u : 0u; u < item_iter; ++u)
         mbar_wait(qfull_bar(u & 1u), (u >> 1) & 1u, &never, p.err);
     }
@@ -410,6 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
       int acc_sel = 0;           // tile_iter % kAccBufs
       uint32_t acc_phase = 0;    // bit a: phase of accumulator a's next use
       uint32_t sf_phase = 0;     // bit slot: phase of the scale slot's next use
+      uint32_t qsf_phase = 0;    // bit qb: phase of the Q-scale slot's next use
       bool ok = true;
       int last_acc = -1;
       uint32_t last_acc_phase = 0;
@@ -418,38 +425,70 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
         const uint32_t qb = item_iter & 1u;
         const uint32_t qsf_t = tmem + L::kQsfCol + qb * 8u;
         const uint64_t adesc = q_desc0 + static_cast<uint64_t>((qb * 8192u) >> 4);
-        // the scale warp copies the item's Q scales before its first tile's
-        // K scales, so that tile's scale barrier covers both
-        for (int j = lo; j < hi && ok; ++j) {
-          if (!tile_computed(it, j)) continue;
-          const int s = tile_iter % kStages;
-          const int slot = tile_iter % kKsfSlots;
-          const int a = acc_sel;
-          const uint32_t aph = (acc_phase >> a) & 1u;
+        // the item's Q scales (copied by scale warp 2 when the segment computes a tile)
+        if (tile_computed(it, lo)) {
+          if (!(ok = mbar_wait(qsf_bar(qb), (qsf_phase >> qb) & 1u, abort_flag, p.err))) return;
+          qsf_phase ^= 1u << qb;
+        }
+        // Tiles go to the tensor pipe in pairs with their K halves interleaved
+        // (A0 B0 A1 B1): back-to-back dependent MMAs on one accumulator stall
+        // the pipe, two independent chains keep it busy (measured: ~226
+        // instead of ~565 cycles per tile).  Computed tiles are a prefix of
+        // the segment.
+        const int jend = min(hi, (it.maxvis + kTileKeys - 1) / kTileKeys);
+        for (int j = lo; j < jend && ok; j += 2) {
+          const int n = min(2, jend - j);
+          int sg[2], slot[2], a[2];
+          uint32_t aph[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const uint32_t ti = tile_iter + u;
+            sg[u] = ti % kStages;
+            slot[u] = ti % kKsfSlots;
+            a[u] = u == 0 ? acc_sel : (acc_sel == kAccBufs - 1 ? 0 : acc_sel + 1);
+            aph[u] = (acc_phase >> a[u]) & 1u;
+          }
           // scale slot ready implies the stage's codes landed (the scale warp waited for them)
-          if (!(ok = mbar_wait(sfready_bar(slot), (sf_phase >> slot) & 1u, abort_flag, p.err))) break;
-          sf_phase ^= 1u << slot;
-          if (!(ok = mbar_wait(acce_bar(a), aph ^ 1u, abort_flag, p.err))) break;
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            if (u >= n || !ok) continue;
+            ok = mbar_wait(sfready_bar(slot[u]), (sf_phase >> slot[u]) & 1u, abort_flag, p.err);
+            sf_phase ^= 1u << slot[u];
+          }
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            if (u >= n || !ok) continue;
+            ok = mbar_wait(acce_bar(a[u]), aph[u] ^ 1u, abort_flag, p.err);
+          }
+          if (!ok) break;
           tc_fence_after();
-          const uint32_t ksf_t = tmem + L::kKsfCol + slot * 8u;
-          const uint32_t d = tmem + L::kAccCol + a * 128u;
-          const uint64_t bdesc = k_desc0 + static_cast<uint64_t>((s * 8192) >> 4);
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {
             constexpr uint32_t sf1 = F::kScaleVec == 2 ? 2u : 0u;
             const uint32_t idesc =
                 kk == 0 ? idesc_fp4(128, 128, F::kUe8m0, 0, 0) : idesc_fp4(128, 128, F::kUe8m0, sf1, sf1);
             const uint32_t col = F::kScaleVec == 2 ? 0u : 4u * kk;
-            tc_mma_fp4<F::kScaleVec>(d, adesc + 2u * kk, bdesc + 2u * kk, idesc, qsf_t + col, ksf_t + col,
-                                     static_cast<uint32_t>(kk));
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              if (u >= n) continue;
+              const uint32_t ksf_t = tmem + L::kKsfCol + slot[u] * 8u;
+              const uint32_t d = tmem + L::kAccCol + a[u] * 128u;
+              const uint64_t bdesc = k_desc0 + static_cast<uint64_t>((sg[u] * 8192) >> 4);
+              tc_mma_fp4<F::kScaleVec>(d, adesc + 2u * kk, bdesc + 2u * kk, idesc, qsf_t + col, ksf_t + col,
+                                       static_cast<uint32_t>(kk));
+            }
           }
-          tc_commit(empty_bar(s));
-          tc_commit(accf_bar(a));
-          last_acc = a;
-          last_acc_phase = aph;
-          acc_phase ^= 1u << a;
-          acc_sel = a == kAccBufs - 1 ? 0 : a + 1;
-          ++tile_iter;
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            if (u >= n) continue;
+            tc_commit(empty_bar(sg[u]));
+            tc_commit(accf_bar(a[u]));
+            last_acc = a[u];
+            last_acc_phase = aph[u];
+            acc_phase ^= 1u << a[u];
+            acc_sel = a[u] == kAccBufs - 1 ? 0 : a[u] + 1;
+          }
+          tile_iter += n;
         }
         if (!ok) return;
         // Q buffer and Q-scale slot free once this item's MMAs complete.
@@ -463,8 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
       }
     }
     __syncwarp();
-  } else if (warp == 2) {
-    // ================================================================ scale warp
+  } else if (warp == 2 || warp == 3) {
+    // ================================================================ scale warps
     // Per item: Q scales (atoms written by the producer's cp.async) -> TMEM.
     // Per tile: raw K scales [128 keys][G] -> 128 rows of the scale layout
     // (row r holds the 32x4x4 atom line r % 32: the words of keys l, 32+l,
@@ -473,6 +512,8 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
     // barrier.  The slot (TMEM and shared staging) is reused by tile
     // i + kKsfSlots only after the MMA of tile i completed (its stage's
     // empty barrier), which also completes the copy that read the staging.
+    // Two warps take alternate tiles; warp 2 also copies each item's Q scales.
+    const uint32_t sidx = warp == 2 ? 0u : 1u;
     const uint64_t ksf_desc0 = desc_sf_rows(smem_u32(ksf_rows));
     const uint64_t qsf_desc0 = desc_sf_atom(smem_u32(qsf_atoms));
     uint32_t tile_iter = 0, item_iter = 0;
@@ -480,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
     block_segments(p, st, [&](int, const BlockItem& it, int lo, int hi) {
       if (!ok) return;
       const uint32_t qb = item_iter & 1u, qph = (item_iter >> 1) & 1u;
+      if (sidx == 0) {
       ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(qfull_bar(qb), qph, abort_flag, p.err) : false, 0);
       if (!ok) return;
       if (lane == 0) {
@@ -496,12 +538,18 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
 #pragma unroll
           for (int at = 0; at < F::kAtoms; ++at)
             tc_cp_32x128b_warpx4(qsf_t + 4u * at, qsf_desc0 + static_cast<uint64_t>(((qb * F::kAtoms + at) * 512) >> 4));
+          tc_commit(qsf_bar(qb));
         }
         mbar_arrive(qempty_bar(qb));
       }
       __syncwarp();
+      }
       for (int j = lo; j < hi; ++j) {
         if (!tile_computed(it, j)) continue;
+        if ((tile_iter & 1u) != sidx) {  // the other scale warp's tile
+          ++tile_iter;
+          continue;
+        }
         const int s = tile_iter % kStages;
         const uint32_t ph = (tile_iter / kStages) & 1u;
         const int slot = tile_iter % kKsfSlots;
@@ -554,13 +602,13 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
       volatile int never = 0;
       const uint32_t first = tile_iter > static_cast<uint32_t>(kKsfSlots) ? tile_iter - kKsfSlots : 0;
       for (uint32_t u = first; u < tile_iter; ++u)
-        mbar_wait(sfready_bar(u % kKsfSlots), (u / kKsfSlots) & 1u, &never, p.err);
+        if ((u & 1u) == sidx) mbar_wait(sfready_bar(u % kKsfSlots), (u / kKsfSlots) & 1u, &never, p.err);
     }
     __syncwarp();
   } else {
     // ================================================================ epilogue
-    const int e = (warp - 3) >> 2;  // group e owns accumulator e: tiles with tile_iter % kAccBufs == e
-    Group<128, -1> g{static_cast<int>(threadIdx.x) - 96 - e * 128, 1 + e};
+    const int e = (warp - kEpiWarp0) >> 2;  // group e owns accumulator e: tiles with tile_iter % kAccBufs == e
+    Group<128, -1> g{static_cast<int>(threadIdx.x) - 32 * kEpiWarp0 - e * 128, 1 + e};
     const int quad = warp & 3;
     const int m = quad * 32 + lane;  // TMEM lane = MMA row
     const int h_local = m >> rt_shift;

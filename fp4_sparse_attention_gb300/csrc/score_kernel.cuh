@@ -181,36 +181,32 @@ __device__ __forceinline__ bool tile_has_visible(const ItemInfo& it, int j) {
   return static_cast<int64_t>(j) * kTileKeys < it.maxvis;
 }
 
-// Cooperative over kNT threads (tid in [0, kNT)): prefix of item tiles.
-// Writes the total and, for the global tile x (if < total), the item
-// holding it and that item's start.  `scan` holds kNT ints.  With
-// `starts` != nullptr the start of every item (and the total, at index
-// items) is also written there, for the merge.
+// Cooperative over kNT threads (tid in [0, kNT), all of the CTA): the total
+// of the item tiles, this CTA's equal chunk of them and the item holding the
+// chunk's first tile with that item's start (item0 = -1 when the CTA has no
+// tiles).  `ws` holds kNT / 32 words.  With `starts` != nullptr the start of
+// every item (and the total, at index items) is also written there, for the
+// merge.
 template <int MODE, int kNT>
-__device__ void plan_items(const ScoreParams& p, int rows_per_cta, int tid, int64_t x, int32_t* scan,
-                           int32_t* total_out, int32_t* item_out, int32_t* start_out, int32_t* starts) {
+__device__ void plan_items(const ScoreParams& p, int rows_per_cta, int tid, uint32_t* ws, CtaState* st,
+                           int32_t* starts) {
   const int items = p.num_seqs * p.row_groups;
   const int per = (items + kNT - 1) / kNT;
   const int i0 = tid * per;
   const int i1 = min(items, i0 + per);
   int32_t s = 0;
   for (int i = i0; i < i1; ++i) s += item_tiles<MODE>(p, item_info(p, i, rows_per_cta));
-  scan[tid] = s;
-  __syncthreads();
+  if (tid == 0) st->item0 = -1;  // ordered before the writes below by the scan's barriers
+  uint32_t total_u;
+  const int32_t pre = static_cast<int32_t>(cta_excl_prefix<kNT>(static_cast<uint32_t>(s), ws, &total_u));
+  const int32_t total = static_cast<int32_t>(total_u);
+  const int32_t chunk = (total + static_cast<int32_t>(gridDim.x) - 1) / static_cast<int32_t>(gridDim.x);
+  const int64_t x = static_cast<int64_t>(blockIdx.x) * chunk;
   if (tid == 0) {
-    int32_t acc = 0;
-    for (int j = 0; j < kNT; ++j) {
-      const int32_t v = scan[j];
-      scan[j] = acc;
-      acc += v;
-    }
-    *total_out = acc;
-    *item_out = -1;
-    *start_out = 0;
-    if (starts) starts[items] = acc;
+    st->total_tiles = total;
+    st->chunk = chunk;
+    if (starts) starts[items] = total;
   }
-  __syncthreads();
-  const int32_t pre = scan[tid];
   if (starts) {
     int32_t acc = pre;
     for (int i = i0; i < i1; ++i) {
@@ -218,13 +214,13 @@ __device__ void plan_items(const ScoreParams& p, int rows_per_cta, int tid, int6
       acc += item_tiles<MODE>(p, item_info(p, i, rows_per_cta));
     }
   }
-  if (x < *total_out && pre <= x && x < pre + s) {
+  if (x < total && pre <= x && x < pre + s) {
     int32_t acc = pre;
     for (int i = i0; i < i1; ++i) {
       const int32_t ti = item_tiles<MODE>(p, item_info(p, i, rows_per_cta));
       if (x < acc + ti) {
-        *item_out = i;
-        *start_out = acc;
+        st->item0 = i;
+        st->item0_start = acc;
         break;
       }
       acc += ti;
@@ -391,30 +387,17 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
 
   CtaState* st = reinterpret_cast<CtaState*>(smem + L::kState);
   RowState<R>* rs = reinterpret_cast<RowState<R>*>(smem + L::kRows);
-  int32_t* scan = reinterpret_cast<int32_t*>(smem + L::kScan);
+  uint32_t* scan = reinterpret_cast<uint32_t*>(smem + L::kScan);
   SelectScratch* sc = reinterpret_cast<SelectScratch*>(smem + L::kScratch);
   uint32_t* hist_words = reinterpret_cast<uint32_t*>(smem + L::kHist);
   const int cap = topk_capacity(p.k);
   volatile int* abort_flag = &st->abort;
 
   // ---- plan this CTA's chunk of the concatenated tile space
-  {
-    int32_t total = 0, item = -1, start = 0;
-    if (threadIdx.x == 0) st->abort = 0;
-    // first pass only for the total; the chunk start depends on it
-    // CTA 0 also publishes every item's tile start for the merge
-    plan_items<MODE, kThreads>(p, R, threadIdx.x, INT64_MAX, scan, &st->total_tiles, &st->item0,
-                               &st->item0_start, blockIdx.x == 0 ? p.item_start : nullptr);
-    total = st->total_tiles;
-    const int32_t chunk = (total + gridDim.x - 1) / gridDim.x;
-    const int64_t x = static_cast<int64_t>(blockIdx.x) * chunk;
-    if (chunk == 0 || x >= total) return;  // uniform: no work for this CTA
-    plan_items<MODE, kThreads>(p, R, threadIdx.x, x, scan, &st->total_tiles, &st->item0, &st->item0_start,
-                               nullptr);
-    if (threadIdx.x == 0) st->chunk = chunk;
-    (void)item;
-    (void)start;
-  }
+  // (CTA 0 also publishes every item's tile start for the merge)
+  if (threadIdx.x == 0) st->abort = 0;
+  plan_items<MODE, kThreads>(p, R, threadIdx.x, scan, st, blockIdx.x == 0 ? p.item_start : nullptr);
+  if (st->item0 < 0) return;  // uniform: no work for this CTA
 
   // ---- one-time setup
   if (threadIdx.x == 0) {

@@ -70,6 +70,32 @@ __device__ __forceinline__ uint32_t group_excl_suffix(const Group<kThreads, kBar
   return after + incl - v;
 }
 
+// Exclusive prefix sum over all kThreads threads of the CTA (__syncthreads):
+// returns the sum of v over threads with a smaller threadIdx.x and the CTA
+// total in *total.  ws holds kThreads / 32 words.
+template <int kThreads>
+__device__ __forceinline__ uint32_t cta_excl_prefix(uint32_t v, uint32_t* ws, uint32_t* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) ws[wid] = incl;
+  __syncthreads();
+  uint32_t before = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const uint32_t x = ws[w];
+    before += w < wid ? x : 0u;
+    all += x;
+  }
+  __syncthreads();
+  *total = all;
+  return before + incl - v;
+}
+
 // Bucket histogram with 16-bit counters, two per 32-bit word (a row's
 // candidate buffer never holds 65,536 keys).
 struct Hist16 {
