@@ -397,6 +397,9 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
   // (CTA 0 also publishes every item's tile start for the merge)
   if (threadIdx.x == 0) st->abort = 0;
   plan_items<MODE, kThreads>(p, R, threadIdx.x, scan, st, blockIdx.x == 0 ? p.item_start : nullptr);
+  // the selection or merge kernel that follows may start its prologue now;
+  // it waits for this grid's completion before reading what it wrote
+  pdl_launch_dependents();
   if (st->item0 < 0) return;  // uniform: no work for this CTA
 
   // ---- one-time setup

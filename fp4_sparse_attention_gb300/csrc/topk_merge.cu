@@ -9,6 +9,8 @@
 // positions, values and the valid count.  One CTA per query row.  The row's
 // partial lists are read with one warp per list and, when the union fits,
 // copied into shared memory so that every later pass runs from there.
+#include <cstring>
+
 #include "score_kernel.cuh"
 
 namespace fp4idx {
@@ -116,6 +118,7 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const __grid_
   const int r = q_local % R;
 
   for (int i = tid; i < kHistBins; i += kMergeThreads) sm->hist[i] = 0;
+  pdl_wait();  // item starts and partial lists come from the scorer before this kernel
   // tile range of the row's item in the scorer's concatenated tile space
   const int items = p.num_seqs * p.row_groups;
   const int32_t P = __ldg(p.item_start + item), total = __ldg(p.item_start + items);
@@ -241,6 +244,7 @@ __global__ void __launch_bounds__(kMergeThreads) topk_select_kernel(const __grid
   const int M = static_cast<int>(min(static_cast<int64_t>(row_visible(p, it, t)), p.ld));
   const bool local = M <= kSelectLocal;
   const float* row_logits = p.logits + static_cast<int64_t>(t) * p.ld;
+  pdl_wait();  // the logits come from the kernel before this one
   auto key_of = [](float v, int s) -> uint64_t { return isnan(v) ? 0ull : topk_key(v, static_cast<uint32_t>(s)); };
   // the row's keys, four float4 loads in flight per thread (rows are 16-byte
   // aligned: ld % 4 == 0 and a 16-byte aligned base)
@@ -312,22 +316,27 @@ __global__ void __launch_bounds__(kMergeThreads) topk_select_kernel(const __grid
 // keys per thread in registers and finds the k-th largest 64-bit key by
 // radix levels (11-bit digits), each level counting only the keys that still
 // match the prefix; a level whose digit bucket holds exactly the remaining
-// rank ends the search.  Then one uniform pass appends the keys >= the
-// threshold.
+// rank ends the search.  Then one uniform pass writes the keys >= the
+// threshold.  Logits of one row often share a few exponent buckets, so the
+// digit counters (16-bit, two per word) come in 8 copies, lane l of every
+// warp counting into copy l % 8: at most 4 lanes of a warp update one word,
+// and the padded copy stride puts lanes that hold the same digit in
+// different copies on different banks.
 // ---------------------------------------------------------------------------
 constexpr int kSmallThreads = 1024;
 constexpr int kSmallPer = 16;
 constexpr int kSmallMaxKeys = kSmallThreads * kSmallPer;
-constexpr int kSmallCopies = 8;  // histogram copies: warp w counts into copy w % 8
+constexpr int kSmallCopies = 8;
+constexpr int kSmallRow = 1025;  // words per copy (1,024 + 1 of padding)
 
 struct SmallSelectSmem {
-  uint32_t hist[kSmallCopies][2048];
-  uint32_t warp_sum[32];
+  uint32_t hist[kSmallCopies][kSmallRow];  // [lane % 8][digit / 2], digit & 1 selects the half-word
+  uint32_t warp_sum[33];
   uint32_t bcast[4];
   uint64_t out[2048];
 };
 
-// Block-wide (1024 threads) exclusive prefix and total of v; `ws` holds 32
+// Block-wide (1024 threads) exclusive prefix and total of v; `ws` holds 33
 // words.  Ends with a barrier, so ws may be reused after it.
 __device__ __forceinline__ uint32_t block_excl_prefix(uint32_t v, uint32_t* ws, uint32_t* total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -339,16 +348,63 @@ __device__ __forceinline__ uint32_t block_excl_prefix(uint32_t v, uint32_t* ws, 
   }
   if (lane == 31) ws[wid] = incl;
   __syncthreads();
-  uint32_t before = 0, all = 0;
+  if (wid == 0) {  // warp 0 turns the 32 warp totals into exclusive offsets
+    const uint32_t x = ws[lane];
+    uint32_t y = x;
 #pragma unroll
-  for (int w = 0; w < 32; ++w) {
-    const uint32_t x = ws[w];
-    before += w < wid ? x : 0u;
-    all += x;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t z = __shfl_up_sync(0xffffffffu, y, o);
+      if (lane >= o) y += z;
+    }
+    ws[lane] = y - x;
+    if (lane == 31) ws[32] = y;
   }
   __syncthreads();
-  *total = all;
+  const uint32_t before = ws[wid];
+  *total = ws[32];
+  __syncthreads();
   return before + incl - v;
+}
+
+// One radix level: the keys flagged in `in` are counted by digit (dig[i] <
+// 2^W); the digit holding the rank-th largest counted key is returned in d,
+// the counted keys in higher digits are taken off rank, eq = keys in digit d,
+// total = all counted keys.
+template <int W>
+__device__ __forceinline__ void small_level(SmallSelectSmem& sm, uint32_t* my_hist, const uint32_t (&dig)[kSmallPer],
+                                            uint32_t in, uint32_t& rank, uint32_t& total, uint32_t& d, uint32_t& eq) {
+#pragma unroll
+  for (int i = 0; i < kSmallPer; ++i)
+    if ((in >> i) & 1u) atomicAdd(&my_hist[dig[i] >> 1], 1u << ((dig[i] & 1u) * 16));
+  __syncthreads();
+  // this thread's digits 2 tid and 2 tid + 1, summed over the copies (which
+  // it clears for the next level)
+  constexpr uint32_t nb = 1u << W;
+  const uint32_t tid = threadIdx.x;
+  const uint32_t d0 = 2u * tid;
+  uint32_t c0 = 0, c1 = 0;
+  if (d0 < nb) {
+#pragma unroll
+    for (int c = 0; c < kSmallCopies; ++c) {
+      const uint32_t x = sm.hist[c][tid];
+      c0 += x & 0xFFFFu;
+      c1 += x >> 16;
+      sm.hist[c][tid] = 0;
+    }
+  }
+  const uint32_t sloc = c0 + c1;
+  const uint32_t pre = block_excl_prefix(sloc, sm.warp_sum, &total);
+  const uint32_t after = total - pre - sloc;  // counted keys in higher digits
+  if (after < rank && after + sloc >= rank) {
+    const bool upper = after + c1 >= rank;
+    sm.bcast[0] = upper ? d0 + 1 : d0;
+    sm.bcast[1] = upper ? after : after + c1;
+    sm.bcast[2] = upper ? c1 : c0;
+  }
+  __syncthreads();
+  d = sm.bcast[0];
+  rank -= sm.bcast[1];
+  eq = sm.bcast[2];
 }
 
 __global__ void __launch_bounds__(kSmallThreads) topk_select_small_kernel(const __grid_constant__ MergeParams mp) {
@@ -356,11 +412,22 @@ __global__ void __launch_bounds__(kSmallThreads) topk_select_small_kernel(const 
   extern __shared__ uint8_t smem_raw[];
   SmallSelectSmem& sm = *reinterpret_cast<SmallSelectSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
   const int tid = threadIdx.x;
-  const int wid = tid >> 5;
+  const int lane = tid & 31;
   const int t = blockIdx.x;
   const int k = p.k;
-  uint32_t* my_hist = sm.hist[wid % kSmallCopies];
+  uint32_t* my_hist = sm.hist[lane % kSmallCopies];
 
+  // The row's stored logits are loaded at once (they lie inside the row's ld
+  // entries whatever its visible length), while the length is looked up.
+  const int cap = static_cast<int>(min(p.ld, static_cast<int64_t>(kSmallMaxKeys)));
+  const float4* row4 = reinterpret_cast<const float4*>(p.logits + static_cast<int64_t>(t) * p.ld);
+  pdl_wait();  // the logits come from the kernel before this one
+  float4 v[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int e = tid + kSmallThreads * u;
+    v[u] = 4 * e < cap ? __ldg(row4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   int lo = 0, hi = p.num_seqs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -369,19 +436,15 @@ __global__ void __launch_bounds__(kSmallThreads) topk_select_small_kernel(const 
   ItemInfo it;
   it.b = lo;
   it.k_len = max(__ldg(p.cu_seqlens_k + lo + 1) - __ldg(p.cu_seqlens_k + lo), 0);
-  const int M = static_cast<int>(min(static_cast<int64_t>(row_visible(p, it, t)),
-                                     min(p.ld, static_cast<int64_t>(kSmallMaxKeys))));
+  const int M = min(row_visible(p, it, t), cap);
+  for (int i = tid; i < kSmallCopies * kSmallRow; i += kSmallThreads) (&sm.hist[0][0])[i] = 0;
 
-  // keys: thread tid holds positions 4 (tid + 1024 u) + c; 0 = absent or NaN
-  const float4* row4 = reinterpret_cast<const float4*>(p.logits + static_cast<int64_t>(t) * p.ld);
-  float4 v[4];
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int e = tid + kSmallThreads * u;
-    v[u] = 4 * e < M ? __ldg(row4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  for (int i = tid; i < kSmallCopies * 2048; i += kSmallThreads) (&sm.hist[0][0])[i] = 0;
-  uint64_t key[kSmallPer];
+  // Key i of this thread (position 4 (tid + 1024 (i / 4)) + i % 4) as the
+  // two halves of its 64-bit top-k key: kh = order-preserving bits of the
+  // logit, kl = ~position (bits 31..14 all ones, positions < 2^14).  Bit i
+  // of `present`: the position is visible and the logit not NaN.
+  uint32_t kh[kSmallPer], kl[kSmallPer];
+  uint32_t present = 0;
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
     const int pos = 4 * (tid + kSmallThreads * u);
@@ -389,103 +452,97 @@ __global__ void __launch_bounds__(kSmallThreads) topk_select_small_kernel(const 
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const bool ok = pos + c < M && !isnan(f[c]);
-      key[4 * u + c] = ok ? topk_key(f[c], static_cast<uint32_t>(pos + c)) : 0ull;
+      const uint64_t key = topk_key(f[c], static_cast<uint32_t>(pos + c));
+      kh[4 * u + c] = static_cast<uint32_t>(key >> 32);
+      kl[4 * u + c] = static_cast<uint32_t>(key);
+      present |= ok ? 1u << (4 * u + c) : 0u;
     }
   }
   __syncthreads();
 
-  // Radix levels over the 64-bit keys: the 32 value bits as 11 + 11 + 10,
-  // then the inverted position, whose bits 31..14 are all ones (positions
-  // < 2^14) and are fixed without a level, then 7 + 7 position bits.  Each
-  // level counts only the keys matching the prefix fixed so far; the first
-  // level's total is the number of present keys.
-  constexpr int kLevels = 5;
-  constexpr int kWidth[kLevels] = {11, 11, 10, 7, 7};
-  uint64_t prefix = 0;
-  int bits = 0;
-  uint32_t rank = static_cast<uint32_t>(k);
-  uint32_t n_valid = 0;
-  bool all_kept = false;
-#pragma unroll 1
-  for (int level = 0; level < kLevels; ++level) {
-    if (level == 3) {
-      prefix = (prefix << 18) | 0x3FFFFull;
-      bits += 18;
-    }
-    const int w = kWidth[level];
-    const int shift = 64 - bits - w;
-    const uint32_t nb = 1u << w;
-    if (level > 0) {
-      for (int i = tid; i < kSmallCopies * 2048; i += kSmallThreads) (&sm.hist[0][0])[i] = 0;
-      __syncthreads();
-    }
+  // Radix levels over the key: the 32 value bits as 11 + 11 + 10, then the
+  // low 14 bits of ~position as 7 + 7.  Each level counts only the keys
+  // matching the prefix fixed so far; the first level's total is the number
+  // of present keys; a level whose digit holds exactly the remaining rank
+  // ends the search (every key with that prefix is in the top-k).
+  uint32_t dig[kSmallPer];
+  uint32_t rank = static_cast<uint32_t>(k), total = 0, d = 0, eq = 0;
 #pragma unroll
-    for (int i = 0; i < kSmallPer; ++i) {
-      const uint64_t kk = key[i];
-      if (kk != 0 && (bits == 0 || (kk >> (64 - bits)) == prefix))
-        atomicAdd(&my_hist[static_cast<uint32_t>(kk >> shift) & (nb - 1)], 1u);
-    }
-    __syncthreads();
-    // this thread's digits: 2 (w = 11) or 1 (w <= 10), summed over the copies
-    const int per = nb >= kSmallThreads ? static_cast<int>(nb / kSmallThreads) : 1;
-    const int d0 = tid * per;
-    uint32_t cnt[2] = {0, 0};
+  for (int i = 0; i < kSmallPer; ++i) dig[i] = kh[i] >> 21;
+  small_level<11>(sm, my_hist, dig, present, rank, total, d, eq);
+  const uint32_t n_valid = total;
+  const bool all_kept = n_valid <= static_cast<uint32_t>(k);
+  uint32_t Th = 0, Tl = 0;  // threshold key: exactly k present keys are >= (Th, Tl)
+  if (!all_kept) {
+    uint32_t P = d;  // 11-bit prefix
+    Th = P << 21;
+    if (eq != rank) {
+      uint32_t in = 0;
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
-      if (i < per && d0 + i < static_cast<int>(nb))
-#pragma unroll
-        for (int c = 0; c < kSmallCopies; ++c) cnt[i] += sm.hist[c][d0 + i];
-    const uint32_t sloc = cnt[0] + cnt[1];
-    // keys in digits above mine: exclusive suffix = total - inclusive prefix
-    uint32_t total;
-    const uint32_t pre = block_excl_prefix(sloc, sm.warp_sum, &total);
-    const uint32_t after = total - pre - sloc;
-    if (level == 0) {
-      n_valid = total;
-      if (n_valid <= static_cast<uint32_t>(k)) {
-        all_kept = true;
-        break;
+      for (int i = 0; i < kSmallPer; ++i) {
+        in |= (kh[i] >> 21) == P ? 1u << i : 0u;
+        dig[i] = (kh[i] >> 10) & 0x7FFu;
       }
-    }
-    if (after < rank && after + sloc >= rank) {
-      uint32_t acc = after;
-      for (int i = per - 1; i >= 0; --i) {
-        if (acc + cnt[i] >= rank) {
-          sm.bcast[0] = static_cast<uint32_t>(d0 + i);
-          sm.bcast[1] = acc;
-          sm.bcast[2] = cnt[i];
-          break;
+      small_level<11>(sm, my_hist, dig, in & present, rank, total, d, eq);
+      P = (P << 11) | d;  // 22 bits
+      Th = P << 10;
+      if (eq != rank) {
+        in = 0;
+#pragma unroll
+        for (int i = 0; i < kSmallPer; ++i) {
+          in |= (kh[i] >> 10) == P ? 1u << i : 0u;
+          dig[i] = kh[i] & 0x3FFu;
         }
-        acc += cnt[i];
+        small_level<10>(sm, my_hist, dig, in & present, rank, total, d, eq);
+        Th = (P << 10) | d;  // all 32 value bits
+        Tl = 0xFFFFC000u;
+        if (eq != rank) {
+          in = 0;
+#pragma unroll
+          for (int i = 0; i < kSmallPer; ++i) {
+            in |= kh[i] == Th ? 1u << i : 0u;
+            dig[i] = (kl[i] >> 7) & 0x7Fu;
+          }
+          small_level<7>(sm, my_hist, dig, in & present, rank, total, d, eq);
+          const uint32_t P2 = d;
+          Tl = 0xFFFFC000u | (P2 << 7);
+          if (eq != rank) {
+            in = 0;
+#pragma unroll
+            for (int i = 0; i < kSmallPer; ++i) {
+              in |= (kh[i] == Th && ((kl[i] >> 7) & 0x7Fu) == P2) ? 1u << i : 0u;
+              dig[i] = kl[i] & 0x7Fu;
+            }
+            small_level<7>(sm, my_hist, dig, in & present, rank, total, d, eq);
+            Tl |= d;
+          }
+        }
       }
     }
-    __syncthreads();
-    const uint32_t d = sm.bcast[0];
-    rank -= sm.bcast[1];
-    const uint32_t eq = sm.bcast[2];
-    prefix = (prefix << w) | d;
-    bits += w;
-    if (eq == rank) break;  // every key with this prefix is in the top-k
   }
-  const uint64_t T = all_kept ? 1ull : (bits == 64 ? prefix : prefix << (64 - bits));
   const int n_out = static_cast<int>(min(n_valid, static_cast<uint32_t>(k)));
 
-  // the n_out keys >= T, at offsets from a block prefix of per-thread counts
-  uint32_t mask = 0;
+  // the n_out keys >= the threshold, at offsets from a block prefix of
+  // per-thread counts
+  uint32_t mask = present;
+  if (!all_kept) {
 #pragma unroll
-  for (int i = 0; i < kSmallPer; ++i) mask |= (key[i] != 0 && key[i] >= T) ? (1u << i) : 0u;
+    for (int i = 0; i < kSmallPer; ++i)
+      if (!(kh[i] > Th || (kh[i] == Th && kl[i] >= Tl))) mask &= ~(1u << i);
+  }
   uint32_t total_kept;
   uint32_t o = block_excl_prefix(static_cast<uint32_t>(__popc(mask)), sm.warp_sum, &total_kept);
-#pragma unroll
-  for (int i = 0; i < kSmallPer; ++i)
-    if ((mask >> i) & 1u) {
-      if (o < 2048u) sm.out[o] = key[i];
-      ++o;
-    }
-  __syncthreads();
+  const int64_t row = static_cast<int64_t>(t) * k;
   if (mp.flags & 1u) {
+#pragma unroll
+    for (int i = 0; i < kSmallPer; ++i)
+      if ((mask >> i) & 1u) {
+        if (o < 2048u) sm.out[o] = (static_cast<uint64_t>(kh[i]) << 32) | kl[i];
+        ++o;
+      }
     int P2 = 1;
     while (P2 < n_out) P2 <<= 1;
+    __syncthreads();
     for (int i = n_out + tid; i < P2; i += kSmallThreads) sm.out[i] = 0;
     __syncthreads();
     for (int size = 2; size <= P2; size <<= 1) {
@@ -504,15 +561,50 @@ __global__ void __launch_bounds__(kSmallThreads) topk_select_small_kernel(const 
         __syncthreads();
       }
     }
-  }
-  const int64_t row = static_cast<int64_t>(t) * k;
-  for (int j = tid; j < k; j += kSmallThreads) {
-    const bool have = j < n_out;
-    const uint64_t kk = have ? sm.out[j] : 0;
-    mp.indices[row + j] = have ? key_pos(kk) : -1;
-    if (mp.values) mp.values[row + j] = have ? key_value(kk) : -INFINITY;
+    for (int j = tid; j < k; j += kSmallThreads) {
+      const bool have = j < n_out;
+      const uint64_t kk = have ? sm.out[j] : 0;
+      mp.indices[row + j] = have ? key_pos(kk) : -1;
+      if (mp.values) mp.values[row + j] = have ? key_value(kk) : -INFINITY;
+    }
+  } else {
+    // unsorted: each thread writes its kept keys straight to their slots
+#pragma unroll
+    for (int i = 0; i < kSmallPer; ++i)
+      if ((mask >> i) & 1u) {
+        if (o < static_cast<uint32_t>(n_out)) {
+          const uint64_t kk = (static_cast<uint64_t>(kh[i]) << 32) | kl[i];
+          mp.indices[row + o] = key_pos(kk);
+          if (mp.values) mp.values[row + o] = key_value(kk);
+        }
+        ++o;
+      }
+    for (int j = n_out + tid; j < k; j += kSmallThreads) {
+      mp.indices[row + j] = -1;
+      if (mp.values) mp.values[row + j] = -INFINITY;
+    }
   }
   if (tid == 0 && mp.valid_count) mp.valid_count[t] = n_out;
+}
+
+// Launch with programmatic stream serialization: the kernel's CTAs may be
+// scheduled once the previous kernel of the stream (the scorer, which
+// signals early) allows it; the kernel itself waits (pdl_wait) for that
+// kernel's completion before it reads the scorer's output.
+cudaError_t launch_dependent(void (*kern)(MergeParams), int grid, int threads, int smem_bytes, cudaStream_t stream,
+                             const MergeParams& p) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 template <int kLocal>
@@ -520,8 +612,7 @@ cudaError_t launch_merge_t(const MergeParams& p, int rows, cudaStream_t stream) 
   const int bytes = static_cast<int>(sizeof(MergeSmem<kLocal>) + 16);
   cudaError_t e = cudaFuncSetAttribute(topk_merge_kernel<kLocal>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  topk_merge_kernel<kLocal><<<rows, kMergeThreads, bytes, stream>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(topk_merge_kernel<kLocal>, rows, kMergeThreads, bytes, stream, p);
 }
 
 }  // namespace
@@ -532,14 +623,12 @@ cudaError_t launch_topk_select(const MergeParams& p, int rows, cudaStream_t stre
     const int sbytes = static_cast<int>(sizeof(SmallSelectSmem) + 16);
     cudaError_t e = cudaFuncSetAttribute(topk_select_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sbytes);
     if (e != cudaSuccess) return e;
-    topk_select_small_kernel<<<rows, kSmallThreads, sbytes, stream>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(topk_select_small_kernel, rows, kSmallThreads, sbytes, stream, p);
   }
   const int bytes = static_cast<int>(sizeof(MergeSmem<kSelectLocal>) + 16);
   cudaError_t e = cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
-  topk_select_kernel<<<rows, kMergeThreads, bytes, stream>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(topk_select_kernel, rows, kMergeThreads, bytes, stream, p);
 }
 
 cudaError_t launch_topk_merge(const MergeParams& p, int rows, bool many_rows, cudaStream_t stream) {
