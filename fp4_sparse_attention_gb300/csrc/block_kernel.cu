@@ -262,7 +262,12 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
   volatile int* abort_flag = &st->abort;
 
   // ---- this CTA's chunk of the concatenated tile space
-  if (threadIdx.x == 0) st->abort = 0;
+  if (threadIdx.x == 0) {
+    st->abort = 0;
+    // the first TMA waits for its descriptor: fetch both while the CTA plans
+    prefetch_tmap(&p.tmap_k);
+    prefetch_tmap(&p.tmap_q);
+  }
   block_plan(p, threadIdx.x, scan, st);
   if (st->item0 < 0) return;  // uniform: no work for this CTA
 
@@ -312,10 +317,6 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
     const uint32_t pidx = warp == 0 ? 0u : 1u;
     uint32_t tile_iter = 0, item_iter = 0;
     bool ok = true;
-    if (lane == 0 && pidx == 0) {
-      prefetch_tmap(&p.tmap_k);
-      prefetch_tmap(&p.tmap_q);
-    }
     block_segments(p, st, [&](int, const BlockItem& it, int lo, int hi) {
       if (!ok) return;
       // -- Q of the item: codes by TMA, scales by cp.async into the atom

@@ -358,6 +358,44 @@ __device__ int compact_keep_ge(const G& g, uint64_t* cand, int n, uint64_t T, Se
   return kept;
 }
 
+// Group-cooperative copy of the keys >= T of cand[0, n) to out[0, cap) in any
+// order; returns how many keys were >= T (possibly more than cap, of which
+// only cap are written).  Loads go out kPer at a time per thread.
+template <class G>
+__device__ uint32_t copy_keep_ge(const G& g, const uint64_t* cand, int n, uint64_t T, uint64_t* out, int cap,
+                                 SelectScratch* sc) {
+  const int lane = g.tid & 31;
+  if (g.tid == 0) sc->bcast[3] = 0;
+  g.sync();
+  constexpr int kPer = 8;
+  constexpr int kChunk = kEpiThreads * kPer;
+  for (int base = 0; base < n; base += kChunk) {
+    uint64_t v[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int idx = base + j * kEpiThreads + g.tid;
+      v[j] = idx < n ? cand[idx] : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const bool keep = base + j * kEpiThreads + g.tid < n && v[j] >= T;
+      const uint32_t m = __ballot_sync(0xffffffffu, keep);
+      if (m) {
+        const int leader = __ffs(m) - 1;
+        uint32_t dst = 0;
+        if (lane == leader) dst = atomicAdd(&sc->bcast[3], static_cast<uint32_t>(__popc(m)));
+        dst = __shfl_sync(0xffffffffu, dst, leader);
+        const uint32_t o = dst + __popc(m & ((1u << lane) - 1u));
+        if (keep && o < static_cast<uint32_t>(cap)) out[o] = v[j];
+      }
+    }
+  }
+  g.sync();
+  const uint32_t kept = sc->bcast[3];
+  g.sync();
+  return kept;
+}
+
 // ---------------------------------------------------------------------------
 // The kernel.
 // ---------------------------------------------------------------------------
@@ -395,7 +433,12 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
 
   // ---- plan this CTA's chunk of the concatenated tile space
   // (CTA 0 also publishes every item's tile start for the merge)
-  if (threadIdx.x == 0) st->abort = 0;
+  if (threadIdx.x == 0) {
+    st->abort = 0;
+    // the first TMA waits for its descriptor: fetch both while the CTA plans
+    prefetch_tmap(&p.tmap_k);
+    prefetch_tmap(&p.tmap_q);
+  }
   plan_items<MODE, kThreads>(p, R, threadIdx.x, scan, st, blockIdx.x == 0 ? p.item_start : nullptr);
   // the selection or merge kernel that follows may start its prologue now;
   // it waits for this grid's completion before reading what it wrote
@@ -448,10 +491,6 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
     const int page = p.page_size;
     const int pshift = p.page_shift;
     const int slots = kTileKeys >> pshift;  // 2 for 64-key pages, 1 for 128
-    if (lane == 0) {
-      prefetch_tmap(&p.tmap_k);
-      if (pidx == 0) prefetch_tmap(&p.tmap_q);
-    }
     for_each_segment<MODE, R>(p, st, [&](int, const ItemInfo& it, int lo, int hi, int) {
       if (!ok) return;
       if (pidx == 0) {
@@ -817,7 +856,18 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
             const bool exact = kept > static_cast<uint32_t>(cap - 2 * margin);
             if (exact) {
               T = select_in_bucket(g, bkt, static_cast<uint32_t>(p.k) - above, gsc, [&](auto&& fn) {
-                for (int e = g.tid; e < n; e += kEpiThreads) fn(cr[e]);
+                // eight loads in flight per thread
+                for (int base = 0; base < n; base += 8 * kEpiThreads) {
+                  uint64_t kv[8];
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) {
+                    const int e = base + j * kEpiThreads + g.tid;
+                    kv[j] = e < n ? cr[e] : 0;
+                  }
+#pragma unroll
+                  for (int j = 0; j < 8; ++j)
+                    if (base + j * kEpiThreads + g.tid < n) fn(kv[j]);
+                }
               });
             }
             const int left = compact_keep_ge(g, cr, n, T, gsc);
@@ -859,29 +909,15 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
           }
           const int64_t part = static_cast<int64_t>(slot) * R + r0 + rr;
           uint64_t* out = p.part_keys + part * cap;
-          if (g.tid == 0) gsc->bcast[3] = 0;
-          g.sync();
-          for (int base = 0; base < n; base += kEpiThreads) {
-            const int e = base + g.tid;
-            const uint64_t key = e < n ? cr[e] : 0;
-            const bool keep = ok && e < n && key >= T;
-            const uint32_t m = __ballot_sync(0xffffffffu, keep);
-            if (m) {
-              const int leader = __ffs(m) - 1;
-              uint32_t dst = 0;
-              if (lane == leader) dst = atomicAdd(&gsc->bcast[3], static_cast<uint32_t>(__popc(m)));
-              dst = __shfl_sync(0xffffffffu, dst, leader);
-              const uint32_t o = dst + __popc(m & ((1u << lane) - 1u));
-              if (keep && o < static_cast<uint32_t>(cap)) out[o] = key;
-            }
-          }
-          g.sync();
+          // (every thread of the group reaches the barriers inside; a warp
+          // that saw the abort copies nothing)
+          const uint32_t kept = copy_keep_ge(g, cr, ok ? n : 0, T, out, cap, gsc);
           bool valid_rr = false;
 #pragma unroll
           for (int q = 0; q < RG; ++q)
             if (q == rr) valid_rr = row_valid[q];
           if (g.tid == 0) {
-            const int32_t wrote = static_cast<int32_t>(min(gsc->bcast[3], static_cast<uint32_t>(cap)));
+            const int32_t wrote = static_cast<int32_t>(min(kept, static_cast<uint32_t>(cap)));
             p.part_count[part] = valid_rr ? wrote : 0;
           }
         }
