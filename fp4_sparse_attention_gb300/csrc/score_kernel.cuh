@@ -35,6 +35,8 @@
 // boundary reloads Q and, for top-k, flushes its per-row candidates.
 #pragma once
 
+#include <cstring>
+
 #include "formats.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -431,22 +433,13 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
   const int cap = topk_capacity(p.k);
   volatile int* abort_flag = &st->abort;
 
-  // ---- plan this CTA's chunk of the concatenated tile space
-  // (CTA 0 also publishes every item's tile start for the merge)
+  // ---- one-time setup: on-chip only, so it may overlap the previous kernel
+  // of the stream (launched with programmatic stream serialization)
   if (threadIdx.x == 0) {
     st->abort = 0;
-    // the first TMA waits for its descriptor: fetch both while the CTA plans
+    // the first TMA waits for its descriptor: fetch both early
     prefetch_tmap(&p.tmap_k);
     prefetch_tmap(&p.tmap_q);
-  }
-  plan_items<MODE, kThreads>(p, R, threadIdx.x, scan, st, blockIdx.x == 0 ? p.item_start : nullptr);
-  // the selection or merge kernel that follows may start its prologue now;
-  // it waits for this grid's completion before reading what it wrote
-  pdl_launch_dependents();
-  if (st->item0 < 0) return;  // uniform: no work for this CTA
-
-  // ---- one-time setup
-  if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), 1);  // the producer's expect-tx arrive; TMA and bulk copies complete the bytes
       mbar_init(empty_bar(s), 1);
@@ -470,6 +463,19 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = st->tmem_base;
+  // every input may come from the previous kernel of the stream
+  pdl_wait();
+
+  // ---- plan this CTA's chunk of the concatenated tile space
+  // (CTA 0 also publishes every item's tile start for the merge)
+  plan_items<MODE, kThreads>(p, R, threadIdx.x, scan, st, blockIdx.x == 0 ? p.item_start : nullptr);
+  // the selection or merge kernel that follows may start its prologue now;
+  // it waits for this grid's completion before reading what it wrote
+  pdl_launch_dependents();
+  if (st->item0 < 0) {  // uniform: no work for this CTA
+    if (warp == 1) tmem_dealloc<kTmemCols>(tmem);
+    return;
+  }
 
   const uint32_t codes_s = smem_u32(smem + L::kCodes);
   const uint32_t q_s = smem_u32(smem + L::kQ);
@@ -944,8 +950,21 @@ cudaError_t launch_score_t(const ScoreParams& p, dim3 grid, cudaStream_t stream)
   auto kern = score_kernel<H, R, FMT, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
-  kern<<<grid, L::kThreads, bytes, stream>>>(p);
-  return cudaGetLastError();
+  // programmatic stream serialization: the CTAs may start their on-chip
+  // setup while the previous kernel of the stream finishes (pdl_wait orders
+  // every global access after it)
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(L::kThreads);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 template <int FMT>

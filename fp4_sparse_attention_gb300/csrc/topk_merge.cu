@@ -422,6 +422,7 @@ __global__ void __launch_bounds__(kSmallThreads) topk_select_small_kernel(const 
   const int cap = static_cast<int>(min(p.ld, static_cast<int64_t>(kSmallMaxKeys)));
   const float4* row4 = reinterpret_cast<const float4*>(p.logits + static_cast<int64_t>(t) * p.ld);
   pdl_wait();  // the logits come from the kernel before this one
+  pdl_launch_dependents();  // the next kernel's on-chip setup may overlap this one
   float4 v[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
