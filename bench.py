@@ -137,7 +137,8 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # workloads
 # ---------------------------------------------------------------------------
-# kind "topk": [logits +] top-k score + merge; kind "block": block maxima.
+# kind "topk": [logits +] top-k score + merge; kind "block": block maxima;
+# kind "logits": the full logits alone (the pages' own per-call measurement).
 # bound: the roofline of the workload's scorer kernel.
 WORKLOADS = {
     "verify16k": dict(maker="verify_decode_16k", kind="topk", k=2048, logits=True, fused=True, bound="hbm"),
@@ -145,6 +146,9 @@ WORKLOADS = {
     "block_scores": dict(maker="nvfp4_gqa_block_scores", kind="block", k=0, logits=False, bound="tensor"),
     "prefill": dict(maker="prefill_32k", kind="topk", k=2048, logits=False, bound="tensor"),
     "tiny": dict(maker="tiny_mx_decode", kind="topk", k=64, logits=True, bound="hbm"),
+    "logits16k": dict(maker="verify_decode_16k", kind="logits", k=0, logits=True, bound="hbm"),
+    "logits100k": dict(maker="verify_decode_100k", kind="logits", k=0, logits=True, bound="hbm"),
+    "logits400k": dict(maker="verify_decode_400k", kind="logits", k=0, logits=True, bound="hbm"),
 }
 
 
@@ -241,8 +245,11 @@ class OursBench:
             self.idx = torch.empty((T, self.k), dtype=torch.int32, device=device)
             self.val = torch.empty((T, self.k), dtype=torch.float32, device=device)
             self.cnt = torch.empty((T,), dtype=torch.int32, device=device)
-            self.ws = torch.empty((B.fp4idx_topk_workspace_bytes(base, self.k),), dtype=torch.uint8, device=device)
-            if spec.get("fused"):
+            self.ws = torch.empty((B.fp4idx_topk_workspace_bytes(base, self.k) if self.k > 0 else 0,),
+                                  dtype=torch.uint8, device=device)
+            if spec["kind"] == "logits":
+                self.kernels = ["scorer_logits"]
+            elif spec.get("fused"):
                 # one call: scorer logits + per-row selection from them (two kernels)
                 self.kernels = ["logits_topk"]
             else:
@@ -257,6 +264,8 @@ class OursBench:
         prob, w = self.problems[n], self.ws_list[n]
         if self.block:
             return [lambda: B.fp4idx_block_scores(prob, out=self.scores)]
+        if self.spec["kind"] == "logits":
+            return [lambda: B.fp4idx_logits(prob, w, out=self.logits)]
         if self.spec.get("fused"):
             return [lambda: B.fp4idx_logits_topk(prob, w, self.k, logits=self.logits, indices=self.idx,
                                                  values=self.val, valid_count=self.cnt)]
@@ -345,6 +354,8 @@ class OursBench:
         h_in = [t.cpu().pin_memory() for t in d_in]
         if self.block:
             d_out = [self.scores]
+        elif self.spec["kind"] == "logits":
+            d_out = [self.logits]
         else:
             d_out = [self.idx, self.val, self.cnt] + ([self.logits] if self.logits is not None else [])
         h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in d_out]
@@ -359,6 +370,8 @@ class OursBench:
                 d.copy_(h, non_blocking=True)
             if self.block:
                 B.fp4idx_block_scores(prob, out=self.scores)
+            elif self.spec["kind"] == "logits":
+                B.fp4idx_logits(prob, self.w, out=self.logits)
             elif self.spec.get("fused"):
                 B.fp4idx_logits_topk(prob, self.w, self.k, logits=self.logits, indices=self.idx, values=self.val,
                                      valid_count=self.cnt)
@@ -444,6 +457,10 @@ def oracle_sample(host, spec):
         def step():
             oracle.block_scores(op, host.ktiles, rows=[row])
         what = f"row {row} ({vis} visible keys): its block maxima for all {host.num_heads} heads"
+    elif spec["kind"] == "logits":
+        def step():
+            oracle.logits_rows(op, vis, rows=[row])
+        what = f"row {row} ({vis} visible keys): its full logits"
     else:
         def step():
             if spec["logits"]:
@@ -596,6 +613,8 @@ def run_ours(args, world, rank, local):
     roof["traffic"] = rec["bytes"] if rec and rec["sha"] == sha else None
     if spec["kind"] == "block":
         step_desc = f"block maxima [{host.num_heads}, {host.ktiles}, {host.q.shape[0]}]"
+    elif spec["kind"] == "logits":
+        step_desc = f"full logits [{host.q.shape[0]}, {(host.max_seqlen_k + 3) // 4 * 4}] (no top-k)"
     elif spec.get("fused"):
         step_desc = f"logits + top-{spec['k']} in one call (scorer logits, per-row selection from them)"
     else:
@@ -615,6 +634,7 @@ def run_ours(args, world, rank, local):
         "dtype": "fp4-e2m1 x fp4-e2m1 -> fp32",
         "data": "synthetic",
         "config": {**host.summary(),
+                   "topk": spec["k"],
                    "step": step_desc,
                    "scores_per_step": pairs,
                    "l2": (f"inputs (q, k, scales, w) rotated over {bench.copies} copies "

@@ -248,6 +248,23 @@ def verify_decode_16k(strict: bool = False) -> Problem:
     return p
 
 
+def verify_decode_context(context: int) -> Problem:
+    """The same verify shape (4 rows x 32 heads, MXFP4, dyadic inputs,
+    shuffled 64-key pages) at another context length; the pages time the
+    logits of this shape at 16,384, 100,000 and 400,000 keys."""
+    return make_problem(name=f"verify_mxfp4_decode_{context // 1000}k", seed=1001 + context, fmt=MXFP4,
+                        q_lens=[4], k_lens=[context], num_heads=32, e8m0_range=(124, 130),
+                        weights="sixteenths", topk=2048)
+
+
+def verify_decode_100k() -> Problem:
+    return verify_decode_context(100_000)
+
+
+def verify_decode_400k() -> Problem:
+    return verify_decode_context(400_000)
+
+
 def long_batched_decode(num_requests: int = 16, cache_keys: int = 14_000_000) -> Problem:
     """16 requests x 4 rows, 32 heads, MXFP4, each context drawn from
     {100,000, 400,000}; 64-key pages dealt from one random permutation of a
