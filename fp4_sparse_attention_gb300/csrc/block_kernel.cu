@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
     }
     for (int a = 0; a < kAccBufs; ++a) {
       mbar_init(accf_bar(a), 1);
-      mbar_init(acce_bar(a), 128);  // the four warps of the group that owns the tile
+      mbar_init(acce_bar(a), 4);  // one arrive per warp of the group that owns the tile
     }
     for (uint32_t qb = 0; qb < 2; ++qb) {
       mbar_init(qfull_bar(qb), 1 + 32);
@@ -667,8 +667,10 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
                 tmem_wait_ld();
                 reg_fence(v);
                 if (half == 1) {
+                  // every lane's loads completed (wait::ld); one arrive per warp
                   tc_fence_before();
-                  mbar_arrive(acce_bar(e));
+                  __syncwarp();
+                  if (lane == 0) mbar_arrive(acce_bar(e));
                 }
                 if (full) block_max_accum(v, mx);
                 else block_max_accum_range(v, lo_c - 64 * half, hi_c - lo_c, mx);

@@ -73,9 +73,24 @@ template <int H, int R, int FMT, int MODE>
 struct ScoreLayout {
   static constexpr int G = FmtTraits<FMT>::G;
   static constexpr int kAtoms = FmtTraits<FMT>::kAtoms;
-  // K-tile ring depth.  A loaded HBM round trip for a random page is ~2 us,
-  // so ~100+ KB must be in flight per SM; the ring takes most of shared memory.
-  static constexpr int kStages = FMT == 0 ? 20 : 18;
+  // Top-k with two rows per CTA (64 heads): each row's candidate buffer
+  // lives in shared memory (a compaction then reads and writes it at
+  // shared-memory latency), kCandCap keys per row.  With four rows the
+  // buffers would leave too shallow a K ring (measured: long decode 286 ->
+  // 400 us with 3,072-key buffers and 8 stages), so they stay in the
+  // workspace (L2) there.
+  static constexpr bool kSmemCand = MODE == kModeTopk && R < 4;
+  static constexpr int kCandCap = kSmemCand ? 4096 : 0;
+  static constexpr uint32_t kCandBytes = static_cast<uint32_t>(R) * kCandCap * 8;
+  // Everything but the K ring, and the ring: as deep as shared memory allows
+  // (a loaded HBM round trip for a random page is ~2 us, so ~70+ KB in
+  // flight per SM), at most 20 stages.
+  static constexpr uint32_t kFixedBytes = 2 * (((H * R * 64 + 1023) / 1024) * 1024) + 4 * kAtoms * 2048 +
+                                          2 * kAtoms * 512 + 4096 + (128 + kEpiThreads * 4) * 4 + 4 * 1280 +
+                                          (MODE == kModeTopk ? R * kHistBins * 2 : 0) + kCandBytes + 2048;
+  static constexpr int kStagesFit = static_cast<int>((232448u - 1024u - kFixedBytes) / (8192u + 128u * G)) & ~1;
+  static constexpr int kStages = kStagesFit < 20 ? kStagesFit : 20;
+  static_assert(kStages >= 4, "K ring depth");
   // Rows of the item per epilogue group of four warps.  Logits: 64
   // accumulator columns per thread and tile, so the per-tile fixed work
   // (barrier poll, TMEM load, fences) is shared by several rows.  Top-k: one
@@ -108,8 +123,10 @@ struct ScoreLayout {
   static constexpr uint32_t kScan = (kRows + sizeof(RowState<R>) + 15) / 16 * 16;  // kThreads ints
   static constexpr uint32_t kScratch = kScan + kThreads * 4;                      // per group
   static constexpr uint32_t kHist = (kScratch + kGroups * sizeof(SelectScratch) + 15) / 16 * 16;
-  static constexpr uint32_t kEnd = kHist + (MODE == kModeTopk ? R * kHistBins * 2 : 0);
+  static constexpr uint32_t kCand = (kHist + (MODE == kModeTopk ? R * kHistBins * 2 : 0) + 15) / 16 * 16;
+  static constexpr uint32_t kEnd = kCand + kCandBytes;
   static constexpr uint32_t bytes() { return kEnd + 1024; }
+  static_assert(kEnd + 1024 <= 232448u, "shared memory");
   // TMEM columns
   static constexpr uint32_t kAccCol = 0;                  // kAccBufs accumulators of 128 columns
   static constexpr uint32_t kSfbCol = 128 * kAccBufs;     // two Q-scale slots of 8 columns
@@ -729,16 +746,21 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
     SelectScratch* gsc = sc + gi;
     const int quad = warp & 3;
     const int key_local = quad * 32 + lane;
-    // Compaction is checked every `check_every` tiles; the buffer keeps that
-    // many tiles of room above the trigger so appends never overflow it.
-    const int check_every = max(1, min(4, (cap - p.k) / (2 * kTileKeys)));
+    // Candidate buffer capacity (shared memory) of each row.  Compaction is
+    // checked every `check_every` tiles; the buffer keeps that many tiles of
+    // room above the trigger so appends never overflow it.
+    const int ccap = L::kSmemCand ? min(cap, L::kCandCap) : cap;
+    const int check_every = max(1, min(4, (ccap - p.k) / (2 * kTileKeys)));
     const int margin = check_every * kTileKeys;
     int since_check = 0;
     uint32_t tile_iter = 0;
     bool ok = true;
     auto hist_of = [&](int rr) { return Hist16{hist_words + (r0 + rr) * (kHistBins / 2)}; };
-    // each row's candidate buffer: global workspace, L2-resident
-    auto cand_of = [&](int rr) { return p.cand + (static_cast<int64_t>(blockIdx.x) * R + r0 + rr) * cap; };
+    // each row's candidate buffer: shared memory, or the workspace (L2-resident)
+    auto cand_of = [&](int rr) {
+      return L::kSmemCand ? reinterpret_cast<uint64_t*>(smem + L::kCand) + (r0 + rr) * L::kCandCap
+                          : p.cand + (static_cast<int64_t>(blockIdx.x) * R + r0 + rr) * cap;
+    };
     for_each_segment<MODE, R>(p, st, [&](int item, const ItemInfo& it, int lo, int hi, int seg) {
       // -- this group's rows of the item: weights in registers, visibility
       bool row_valid[RG];
@@ -837,7 +859,7 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
               if (lane == leader) base = atomicAdd(&rs->cnt[r0 + rr], __popc(m));
               base = __shfl_sync(0xffffffffu, base, leader);
               const int slot_i = base + __popc(m & ((1u << lane) - 1u));
-              if (take && slot_i < cap) {
+              if (take && slot_i < ccap) {
                 const uint64_t key = (static_cast<uint64_t>(ordered_bits(val[rr])) << 32) |
                                      static_cast<uint64_t>(~static_cast<uint32_t>(pos));
                 cand_of(rr)[slot_i] = key;
@@ -852,14 +874,14 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
 #pragma unroll 1
           for (int rr = 0; rr < RG; ++rr) {
             const int n = rs->cnt[r0 + rr];
-            if (n <= cap - margin) continue;  // uniform: read after the barrier
+            if (n <= ccap - margin) continue;  // uniform: read after the barrier
             const Hist16 hr = hist_of(rr);
             uint64_t* cr = cand_of(rr);
             uint32_t above = 0;
             const uint32_t bkt = find_kth_bucket(g, hr, static_cast<uint32_t>(p.k), gsc, &above);
             const uint32_t kept = above + hr(static_cast<int>(bkt));
             uint64_t T = static_cast<uint64_t>(bkt) << kHistShift;
-            const bool exact = kept > static_cast<uint32_t>(cap - 2 * margin);
+            const bool exact = kept > static_cast<uint32_t>(ccap - 2 * margin);
             if (exact) {
               T = select_in_bucket(g, bkt, static_cast<uint32_t>(p.k) - above, gsc, [&](auto&& fn) {
                 // eight loads in flight per thread
