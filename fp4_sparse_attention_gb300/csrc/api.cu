@@ -199,6 +199,7 @@ fp4idx_status_t fill_score_params(const fp4idx_problem_t* pr, const float* w, in
   sp->num_seqs = pr->num_seqs;
   sp->row_groups = (pr->max_seqlen_q + rows_per_cta - 1) / rows_per_cta;
   sp->max_seqlen_k = pr->max_seqlen_k;
+  sp->uniform_items = 0;
   sp->w = w;
   sp->w_row_stride = w_row_stride;
   sp->err = err;
@@ -292,6 +293,9 @@ fp4idx_status_t fp4idx_logits(const fp4idx_problem_t* problem, const float* w, i
   ScoreParams sp;
   if ((s = fill_score_params(problem, w, w_row_stride, &sp, R, dev->err)) != FP4IDX_OK) return s;
   sp.total_tiles = static_cast<int32_t>((ld + kTileKeys - 1) / kTileKeys);
+  // one request whose row count fills every row group: each item holds
+  // total_tiles tiles, so the CTAs need not read the metadata to plan
+  sp.uniform_items = problem->num_seqs == 1 && sp.row_groups == (problem->num_rows + R - 1) / R ? 1 : 0;
   sp.logits = logits;
   sp.ld = ld;
   sp.k = 1;

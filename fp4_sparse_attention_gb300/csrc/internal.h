@@ -41,6 +41,8 @@ struct ScoreParams {
   const float* w;
   int64_t w_row_stride;
   int32_t total_tiles;      // logits: output tiles per row group, ceil(ld / 128)
+  int32_t uniform_items;    // logits: 1 when every item is known (on the host) to hold
+                            // total_tiles tiles, so a CTA plans its chunk without device reads
   int32_t score_ctas;       // grid size of the scorer launch
   // logits output
   float* logits;

@@ -485,7 +485,20 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
 
   // ---- plan this CTA's chunk of the concatenated tile space
   // (CTA 0 also publishes every item's tile start for the merge)
-  plan_items<MODE, kThreads>(p, R, threadIdx.x, scan, st, blockIdx.x == 0 ? p.item_start : nullptr);
+  if (MODE == kModeLogits && p.uniform_items) {
+    if (threadIdx.x == 0) {
+      const int32_t total = p.num_seqs * p.row_groups * p.total_tiles;
+      const int32_t chunk = (total + static_cast<int32_t>(gridDim.x) - 1) / static_cast<int32_t>(gridDim.x);
+      const int64_t x = static_cast<int64_t>(blockIdx.x) * chunk;
+      st->total_tiles = total;
+      st->chunk = chunk;
+      st->item0 = x < total ? static_cast<int32_t>(x / p.total_tiles) : -1;
+      st->item0_start = st->item0 >= 0 ? st->item0 * p.total_tiles : 0;
+    }
+    __syncthreads();
+  } else {
+    plan_items<MODE, kThreads>(p, R, threadIdx.x, scan, st, blockIdx.x == 0 ? p.item_start : nullptr);
+  }
   // the selection or merge kernel that follows may start its prologue now;
   // it waits for this grid's completion before reading what it wrote
   pdl_launch_dependents();

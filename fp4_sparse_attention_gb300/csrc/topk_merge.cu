@@ -417,18 +417,12 @@ __global__ void __launch_bounds__(kSmallThreads) topk_select_small_kernel(const 
   const int k = p.k;
   uint32_t* my_hist = sm.hist[lane % kSmallCopies];
 
-  // The row's stored logits are loaded at once (they lie inside the row's ld
-  // entries whatever its visible length), while the length is looked up.
+  // The row's visible length and the cleared counters come first: they need
+  // nothing from the scorer, so they overlap its tail (this kernel may start
+  // before the scorer completes).  The row's stored logits are then loaded at
+  // once (they lie inside the row's ld entries whatever its visible length).
   const int cap = static_cast<int>(min(p.ld, static_cast<int64_t>(kSmallMaxKeys)));
   const float4* row4 = reinterpret_cast<const float4*>(p.logits + static_cast<int64_t>(t) * p.ld);
-  pdl_wait();  // the logits come from the kernel before this one
-  pdl_launch_dependents();  // the next kernel's on-chip setup may overlap this one
-  float4 v[4];
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int e = tid + kSmallThreads * u;
-    v[u] = 4 * e < cap ? __ldg(row4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
   int lo = 0, hi = p.num_seqs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -439,6 +433,14 @@ __global__ void __launch_bounds__(kSmallThreads) topk_select_small_kernel(const 
   it.k_len = max(__ldg(p.cu_seqlens_k + lo + 1) - __ldg(p.cu_seqlens_k + lo), 0);
   const int M = min(row_visible(p, it, t), cap);
   for (int i = tid; i < kSmallCopies * kSmallRow; i += kSmallThreads) (&sm.hist[0][0])[i] = 0;
+  pdl_wait();  // the logits come from the kernel before this one
+  pdl_launch_dependents();  // the next kernel's on-chip setup may overlap this one
+  float4 v[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int e = tid + kSmallThreads * u;
+    v[u] = 4 * e < cap ? __ldg(row4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 
   // Key i of this thread (position 4 (tid + 1024 (i / 4)) + i % 4) as the
   // two halves of its 64-bit top-k key: kh = order-preserving bits of the
