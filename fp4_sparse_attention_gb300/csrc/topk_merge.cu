@@ -333,6 +333,7 @@ struct SmallSelectSmem {
   uint32_t hist[kSmallCopies][kSmallRow];  // [lane % 8][digit / 2], digit & 1 selects the half-word
   uint32_t warp_sum[33];
   uint32_t bcast[4];
+  uint32_t win_count[4];
   uint64_t out[2048];
 };
 
@@ -433,6 +434,10 @@ __global__ void __launch_bounds__(kSmallThreads) topk_select_small_kernel(const 
   it.k_len = max(__ldg(p.cu_seqlens_k + lo + 1) - __ldg(p.cu_seqlens_k + lo), 0);
   const int M = min(row_visible(p, it, t), cap);
   for (int i = tid; i < kSmallCopies * kSmallRow; i += kSmallThreads) (&sm.hist[0][0])[i] = 0;
+  if (tid == 0) {
+    sm.bcast[3] = 0;
+    sm.win_count[0] = 0;
+  }
   pdl_wait();  // the logits come from the kernel before this one
   pdl_launch_dependents();  // the next kernel's on-chip setup may overlap this one
   float4 v[4];
@@ -470,11 +475,37 @@ __global__ void __launch_bounds__(kSmallThreads) topk_select_small_kernel(const 
   // ends the search (every key with that prefix is in the top-k).
   uint32_t dig[kSmallPer];
   uint32_t rank = static_cast<uint32_t>(k), total = 0, d = 0, eq = 0;
+  // The first level first counts only the keys within kWindow digits (six
+  // binades) below the largest key's digit: when they are at least k, the
+  // k-th key is among them and the other keys never touch the counters.
+  // Otherwise (or with fewer than k keys) the level is redone over all keys.
+  constexpr uint32_t kWindow = 24;
+  uint32_t top = 0, n_present = static_cast<uint32_t>(__popc(present));
 #pragma unroll
-  for (int i = 0; i < kSmallPer; ++i) dig[i] = kh[i] >> 21;
-  small_level<11>(sm, my_hist, dig, present, rank, total, d, eq);
-  const uint32_t n_valid = total;
+  for (int i = 0; i < kSmallPer; ++i) {
+    dig[i] = kh[i] >> 21;
+    if ((present >> i) & 1u) top = max(top, dig[i]);
+  }
+  top = __reduce_max_sync(0xffffffffu, top);
+  n_present = __reduce_add_sync(0xffffffffu, n_present);
+  if (lane == 0) {
+    atomicMax(&sm.bcast[3], top);
+    atomicAdd(&sm.win_count[0], n_present);
+  }
+  __syncthreads();
+  const uint32_t n_valid = sm.win_count[0];
   const bool all_kept = n_valid <= static_cast<uint32_t>(k);
+  if (!all_kept) {
+    const uint32_t lo_digit = sm.bcast[3] > kWindow ? sm.bcast[3] - kWindow : 0u;
+    uint32_t in = 0;
+#pragma unroll
+    for (int i = 0; i < kSmallPer; ++i) in |= dig[i] >= lo_digit ? 1u << i : 0u;
+    small_level<11>(sm, my_hist, dig, in & present, rank, total, d, eq);
+    if (total < static_cast<uint32_t>(k)) {
+      rank = static_cast<uint32_t>(k);
+      small_level<11>(sm, my_hist, dig, present, rank, total, d, eq);
+    }
+  }
   uint32_t Th = 0, Tl = 0;  // threshold key: exactly k present keys are >= (Th, Tl)
   if (!all_kept) {
     uint32_t P = d;  // 11-bit prefix
@@ -571,20 +602,20 @@ __global__ void __launch_bounds__(kSmallThreads) topk_select_small_kernel(const 
       if (mp.values) mp.values[row + j] = have ? key_value(kk) : -INFINITY;
     }
   } else {
-    // unsorted: each thread writes its kept keys straight to their slots
+    // unsorted: kept keys are placed in shared memory at their output slots,
+    // then written out in order (coalesced stores)
 #pragma unroll
     for (int i = 0; i < kSmallPer; ++i)
       if ((mask >> i) & 1u) {
-        if (o < static_cast<uint32_t>(n_out)) {
-          const uint64_t kk = (static_cast<uint64_t>(kh[i]) << 32) | kl[i];
-          mp.indices[row + o] = key_pos(kk);
-          if (mp.values) mp.values[row + o] = key_value(kk);
-        }
+        if (o < 2048u) sm.out[o] = (static_cast<uint64_t>(kh[i]) << 32) | kl[i];
         ++o;
       }
-    for (int j = n_out + tid; j < k; j += kSmallThreads) {
-      mp.indices[row + j] = -1;
-      if (mp.values) mp.values[row + j] = -INFINITY;
+    __syncthreads();
+    for (int j = tid; j < k; j += kSmallThreads) {
+      const bool have = j < n_out;
+      const uint64_t kk = have ? sm.out[j] : 0;
+      mp.indices[row + j] = have ? key_pos(kk) : -1;
+      if (mp.values) mp.values[row + j] = have ? key_value(kk) : -INFINITY;
     }
   }
   if (tid == 0 && mp.valid_count) mp.valid_count[t] = n_out;

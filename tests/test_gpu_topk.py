@@ -147,3 +147,37 @@ def test_logits_topk_fused_call():
         compare_scores(logits, ref, bound, safe, p.name + " logits")
         rows = np.arange(p.num_rows)
         compare_topk(p, rows, k, idx.cpu().numpy(), val.cpu().numpy(), cnt.cpu().numpy(), sorted_order=True)
+
+
+def _digits(x):
+    # top 11 bits of the order-preserving image of each fp32 logit
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    ordered = np.where(u >> 31, (~u) & 0xFFFFFFFF, u | 0x80000000)
+    return ordered >> 21
+
+
+@pytest.mark.parametrize("sorted_", [False, True])
+def test_short_select_with_outlier_keys(sorted_):
+    # a few keys with 2^30-times larger scales: in some row fewer than k keys
+    # lie within six binades of the largest logit, so the short-row select
+    # must count every key, not only those near the top
+    p = wl.tiny_mx_decode()
+    k = 64
+    rng = np.random.default_rng(77)
+    pages, page = p.block_table[0, :16], p.page_size
+    for key in rng.choice(1020, size=8, replace=False):
+        p.k_scale[pages[key // page], 0, key % page, :] = 157
+    ref, _, _ = oracle.logits_rows(p, 1024)
+    narrow = []
+    for t in range(p.num_rows):
+        v = np.asarray(ref[t])[: oracle.visible(p, t)]
+        d = _digits(v)
+        narrow.append(int((d >= d.max() - 24).sum()) < k)
+    assert any(narrow), "no row exercises the wide first level"
+    dp = B.DeviceProblem.from_host(p)
+    w = torch.as_tensor(p.w).cuda()
+    logits, idx, val, cnt = B.fp4idx_logits_topk(dp, w, k, sorted=sorted_)
+    torch.cuda.synchronize()
+    assert B.fp4idx_get_error() == 0
+    rows = np.arange(p.num_rows)
+    compare_topk(p, rows, k, idx.cpu().numpy(), val.cpu().numpy(), cnt.cpu().numpy(), sorted_order=sorted_)
