@@ -144,6 +144,8 @@ WORKLOADS = {
     "verify16k": dict(maker="verify_decode_16k", kind="topk", k=2048, logits=True, fused=True, bound="hbm"),
     "long_decode": dict(maker="long_batched_decode", kind="topk", k=2048, logits=False, bound="hbm"),
     "block_scores": dict(maker="nvfp4_gqa_block_scores", kind="block", k=0, logits=False, bound="tensor"),
+    "block_topk": dict(maker="nvfp4_gqa_block_scores", kind="block", k=0, block_k=16, logits=False,
+                       bound="tensor"),
     "prefill": dict(maker="prefill_32k", kind="topk", k=2048, logits=False, bound="tensor"),
     "tiny": dict(maker="tiny_mx_decode", kind="topk", k=64, logits=True, bound="hbm"),
     "logits16k": dict(maker="verify_decode_16k", kind="logits", k=0, logits=True, bound="hbm"),
@@ -239,6 +241,12 @@ class OursBench:
         if self.block:
             self.scores = torch.empty((base.num_heads, base.ktiles, T), dtype=torch.float32, device=device)
             self.kernels = ["block_scores"]
+            self.block_k = spec.get("block_k", 0)
+            if self.block_k:
+                self.bidx = torch.empty((base.num_heads, T, self.block_k), dtype=torch.int32, device=device)
+                self.bval = torch.empty((base.num_heads, T, self.block_k), dtype=torch.float32, device=device)
+                self.bcnt = torch.empty((base.num_heads, T), dtype=torch.int32, device=device)
+                self.kernels.append("block_topk")
         else:
             self.ld = (host.max_seqlen_k + 3) // 4 * 4
             self.logits = torch.empty((T, self.ld), dtype=torch.float32, device=device) if spec["logits"] else None
@@ -263,7 +271,10 @@ class OursBench:
         B = self.B
         prob, w = self.problems[n], self.ws_list[n]
         if self.block:
-            return [lambda: B.fp4idx_block_scores(prob, out=self.scores)]
+            calls = [lambda: B.fp4idx_block_scores(prob, out=self.scores)]
+            if self.block_k:
+                calls.append(lambda: B.fp4idx_block_topk(self.scores, self.block_k, self.bidx, self.bval, self.bcnt))
+            return calls
         if self.spec["kind"] == "logits":
             return [lambda: B.fp4idx_logits(prob, w, out=self.logits)]
         if self.spec.get("fused"):
@@ -353,7 +364,7 @@ class OursBench:
             [prob.visible_len] if prob.visible_len is not None else [])
         h_in = [t.cpu().pin_memory() for t in d_in]
         if self.block:
-            d_out = [self.scores]
+            d_out = [self.scores] + ([self.bidx, self.bval, self.bcnt] if self.block_k else [])
         elif self.spec["kind"] == "logits":
             d_out = [self.logits]
         else:
@@ -370,6 +381,8 @@ class OursBench:
                 d.copy_(h, non_blocking=True)
             if self.block:
                 B.fp4idx_block_scores(prob, out=self.scores)
+                if self.block_k:
+                    B.fp4idx_block_topk(self.scores, self.block_k, self.bidx, self.bval, self.bcnt)
             elif self.spec["kind"] == "logits":
                 B.fp4idx_logits(prob, self.w, out=self.logits)
             elif self.spec.get("fused"):
@@ -411,6 +424,9 @@ def kernel_algorithmic_bytes(host, name: str, k: int) -> int:
         return kv + qb + 2 * T * ((host.max_seqlen_k + 3) // 4 * 4) * 4 + T * k * 8 + T * 4
     if name == "block_scores":
         return kv + qb + H * ((host.max_seqlen_k + 127) // 128) * T * 4
+    if name == "block_topk":  # scores read once; indices, values, counts written
+        bk = k or 16
+        return H * ((host.max_seqlen_k + 127) // 128) * T * 4 + H * T * (bk * 8 + 4)
     raise KeyError(name)
 
 
@@ -438,7 +454,7 @@ def roofline(host, spec, name: str, launch_ms: float, step_ms: float, peaks: dic
                 "launch_us": launch_ms * 1e3,
                 "peak_source": f"{peaks['source']} bf16 {'sustained' if sustained else 'burst'} "
                                f"{bf16:.1f} TFLOP/s x {FP4_PER_BF16:g} (nominal FP4/bf16 ratio)"}
-    alg = kernel_algorithmic_bytes(host, name, spec["k"])
+    alg = kernel_algorithmic_bytes(host, name, spec.get("block_k", 0) if name == "block_topk" else spec["k"])
     achieved = alg / (launch_ms * 1e-3) / 1e9
     return {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes": alg,
@@ -454,9 +470,14 @@ def oracle_sample(host, spec):
     vis = oracle.visible(host, row)
     op = oracle.OracleProblem(host)
     if spec["kind"] == "block":
+        bk = spec.get("block_k", 0)
+
         def step():
-            oracle.block_scores(op, host.ktiles, rows=[row])
-        what = f"row {row} ({vis} visible keys): its block maxima for all {host.num_heads} heads"
+            sc, _, _ = oracle.block_scores(op, host.ktiles, rows=[row])
+            if bk:
+                oracle.block_topk(sc, bk)
+        what = f"row {row} ({vis} visible keys): its block maxima for all {host.num_heads} heads" + \
+            (f" and their top-{bk} blocks" if bk else "")
     elif spec["kind"] == "logits":
         def step():
             oracle.logits_rows(op, vis, rows=[row])
@@ -612,7 +633,8 @@ def run_ours(args, world, rank, local):
     rec = RECORDED_TRAFFIC.get((args.workload, dominant))
     roof["traffic"] = rec["bytes"] if rec and rec["sha"] == sha else None
     if spec["kind"] == "block":
-        step_desc = f"block maxima [{host.num_heads}, {host.ktiles}, {host.q.shape[0]}]"
+        step_desc = f"block maxima [{host.num_heads}, {host.ktiles}, {host.q.shape[0]}]" + \
+            (f" + top-{spec['block_k']} blocks per (head, row)" if spec.get("block_k") else "")
     elif spec["kind"] == "logits":
         step_desc = f"full logits [{host.q.shape[0]}, {(host.max_seqlen_k + 3) // 4 * 4}] (no top-k)"
     elif spec.get("fused"):
@@ -635,6 +657,7 @@ def run_ours(args, world, rank, local):
         "data": "synthetic",
         "config": {**host.summary(),
                    "topk": spec["k"],
+                   **({"block_topk": spec["block_k"]} if spec.get("block_k") else {}),
                    "step": step_desc,
                    "scores_per_step": pairs,
                    "l2": (f"inputs (q, k, scales, w) rotated over {bench.copies} copies "

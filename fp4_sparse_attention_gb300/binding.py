@@ -35,6 +35,7 @@ ERR_TIMEOUT = 0x2
 EXPORTED = (
     "fp4idx_logits",
     "fp4idx_block_scores",
+    "fp4idx_block_topk",
     "fp4idx_topk_workspace_bytes",
     "fp4idx_topk",
     "fp4idx_topk_score",
@@ -102,6 +103,8 @@ def load_library(path: str = LIB_PATH):
         lib.fp4idx_logits.restype = i32
         lib.fp4idx_block_scores.argtypes = [P, vp, vp]
         lib.fp4idx_block_scores.restype = i32
+        lib.fp4idx_block_topk.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp]
+        lib.fp4idx_block_topk.restype = i32
         lib.fp4idx_topk_workspace_bytes.argtypes = [P, i32]
         lib.fp4idx_topk_workspace_bytes.restype = sz
         lib.fp4idx_topk.argtypes = [P, vp, i64, i32, u32, vp, vp, vp, vp, sz, vp]
@@ -238,6 +241,27 @@ def fp4idx_block_scores(problem: DeviceProblem, out: Optional[torch.Tensor] = No
                           device=problem.q.device)
     _check(lib.fp4idx_block_scores(ctypes.byref(problem.c), _ptr(out), _stream(stream)), "fp4idx_block_scores")
     return out
+
+
+def fp4idx_block_topk(scores: torch.Tensor, k: int, indices: Optional[torch.Tensor] = None,
+                      values: Optional[torch.Tensor] = None, valid_count: Optional[torch.Tensor] = None,
+                      stream=None):
+    """Top-k blocks of each (head, row) column of block scores [Hq, Ktiles, T]:
+    (indices [Hq, T, k] int32, values [Hq, T, k] fp32, valid_count [Hq, T] int32)."""
+    lib = load_library()
+    if scores.dim() != 3 or scores.dtype != torch.float32 or not scores.is_contiguous():
+        raise ValueError("scores must be a contiguous [Hq, Ktiles, T] float32 tensor")
+    H, Kt, T = scores.shape
+    dev = scores.device
+    if indices is None:
+        indices = torch.empty((H, T, k), dtype=torch.int32, device=dev)
+    if values is None:
+        values = torch.empty((H, T, k), dtype=torch.float32, device=dev)
+    if valid_count is None:
+        valid_count = torch.empty((H, T), dtype=torch.int32, device=dev)
+    _check(lib.fp4idx_block_topk(_ptr(scores), H, Kt, T, k, _ptr(indices), _ptr(values), _ptr(valid_count),
+                                 _stream(stream)), "fp4idx_block_topk")
+    return indices, values, valid_count
 
 
 def fp4idx_topk_workspace_bytes(problem: DeviceProblem, k: int) -> int:

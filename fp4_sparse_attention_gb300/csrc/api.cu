@@ -469,6 +469,25 @@ fp4idx_status_t fp4idx_logits_topk(const fp4idx_problem_t* problem, const float*
   return logits_then_select(problem, w, w_row_stride, logits, ld, k, flags, indices, values, valid_count, stream);
 }
 
+fp4idx_status_t fp4idx_block_topk(const float* scores, int32_t num_heads, int32_t ktiles, int32_t num_rows,
+                                  int32_t k, int32_t* indices, float* values, int32_t* valid_count, void* stream) {
+  g_msg[0] = 0;
+  if (!scores) return fail(FP4IDX_EINVAL, "scores is NULL");
+  if (!indices) return fail(FP4IDX_EINVAL, "indices is NULL");
+  if (num_heads < 1 || ktiles < 1 || num_rows < 1 || k < 1)
+    return fail(FP4IDX_EINVAL, "num_heads, ktiles, num_rows and k must be positive");
+  if (k > 32) return fail(FP4IDX_EUNSUPPORTED, "k = %d: supported 1..32", k);
+  if (!aligned(scores, 4) || !aligned(indices, 4) || (values && !aligned(values, 4)) ||
+      (valid_count && !aligned(valid_count, 4)))
+    return fail(FP4IDX_EINVAL, "scores, indices, values and valid_count must be 4-byte aligned");
+  if (static_cast<int64_t>(num_heads) * num_rows > (int64_t(1) << 40))
+    return fail(FP4IDX_EUNSUPPORTED, "too many columns");
+  cudaError_t e = launch_block_topk(scores, num_heads, ktiles, num_rows, k, indices, values, valid_count,
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "block top-k launch");
+  return FP4IDX_OK;
+}
+
 fp4idx_status_t fp4idx_block_scores(const fp4idx_problem_t* problem, float* scores, void* stream) {
   g_msg[0] = 0;
   fp4idx_status_t s = check_problem(problem);

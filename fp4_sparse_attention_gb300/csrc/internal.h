@@ -117,6 +117,9 @@ cudaError_t launch_topk_merge(const MergeParams& p, int rows, bool many_rows, cu
 // Exact top-k of each row from p.sp.logits [T][p.sp.ld] (visibility from the problem).
 cudaError_t launch_topk_select(const MergeParams& p, int rows, cudaStream_t stream);
 cudaError_t launch_block_scores(const BlockParams& p, int format, dim3 grid, cudaStream_t stream);
+// Top-k blocks of each (head, row) column of [H][Kt][T] block scores, k <= 32.
+cudaError_t launch_block_topk(const float* scores, int32_t H, int32_t Kt, int32_t T, int32_t k, int32_t* indices,
+                              float* values, int32_t* valid_count, cudaStream_t stream);
 
 // Sets the message fp4idx_last_error_message() returns on this thread.
 void set_last_error(const char* fmt, ...);

@@ -155,6 +155,25 @@ fp4idx_status_t fp4idx_block_scores(const fp4idx_problem_t* problem, float* scor
                                     void* stream);
 
 /*
+ * Top-k blocks of every (head, row) column of a block-score tensor (M3-indexer
+ * README, "输出 shape 和类型": the block-score call returns the scores only,
+ * and a caller that needs a top-k takes it along Ktiles, dim 1).
+ *   scores       [Hq][ktiles][T] fp32, device, as written by fp4idx_block_scores.
+ *   indices      [Hq][T][k] int32, device: for each (h, t) the block numbers of
+ *                the min(k, n) largest scores, n = the blocks of the column
+ *                whose score is neither -inf (no visible key) nor NaN; order
+ *                (score desc, block asc); -1 after them.
+ *   values       [Hq][T][k] fp32 scores of those blocks (-inf padding), or NULL.
+ *   valid_count  [Hq][T] int32 = min(k, n), or NULL.
+ * Every pointer is caller-owned device memory (4-byte aligned); no workspace,
+ * no synchronisation (graph-capturable).  EINVAL for NULL scores / indices or
+ * a non-positive size, EUNSUPPORTED for k > 32.
+ */
+fp4idx_status_t fp4idx_block_topk(const float* scores, int32_t num_heads, int32_t ktiles,
+                                  int32_t num_rows, int32_t k, int32_t* indices, float* values,
+                                  int32_t* valid_count, void* stream);
+
+/*
  * Top-k positions of each row's logits (CURRENT_ISSUE..., "Fix (production
  * target)": ReLU + per-head weight epilogue followed by a top-k; the output
  * convention is that of a sparse-attention consumer: logical positions, -1

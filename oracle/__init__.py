@@ -92,6 +92,8 @@ def _load():
             lib.orc_block_scores.argtypes = [P, i32, vp, i32, vp, vp, vp]
             lib.orc_topk.restype = None
             lib.orc_topk.argtypes = [P, vp, i64, i32, vp, i32, vp, vp, vp]
+            lib.orc_block_topk.restype = None
+            lib.orc_block_topk.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp]
             lib.orc_num_threads.restype = i32
             lib.orc_num_threads.argtypes = []
             _lib = lib
@@ -264,4 +266,16 @@ def topk(prob, k: int, rows=None, w=None):
     cnt = np.empty((len(rows),), np.int32)
     _load().orc_topk(op.ref, _ptr(w), w.shape[1], k, _ptr(rows), len(rows), _ptr(idx), _ptr(val),
                      _ptr(cnt))
+    return idx, val, cnt
+
+
+def block_topk(scores, k: int):
+    """Top-k blocks of each (head, row) column of block scores [H, Kt, T]:
+    (indices [H, T, k] -1 padded, values [H, T, k] -inf padded, counts [H, T])."""
+    sc = np.ascontiguousarray(np.asarray(scores, dtype=np.float32))
+    H, Kt, T = sc.shape
+    idx = np.empty((H, T, k), np.int32)
+    val = np.empty((H, T, k), np.float32)
+    cnt = np.empty((H, T), np.int32)
+    _load().orc_block_topk(_ptr(sc), H, Kt, T, k, _ptr(idx), _ptr(val), _ptr(cnt))
     return idx, val, cnt

@@ -292,6 +292,43 @@ void orc_topk(const orc_problem* p, const float* w, int64_t w_row_stride, int32_
   }
 }
 
+void orc_block_topk(const float* scores, int32_t num_heads, int32_t ktiles, int32_t num_rows, int32_t k,
+                    int32_t* idx, float* val, int32_t* count) {
+  const int64_t cols = (int64_t)num_heads * num_rows;
+#pragma omp parallel
+  {
+    unsigned char* taken = (unsigned char*)malloc((size_t)ktiles);
+#pragma omp for schedule(dynamic, 64)
+    for (int64_t c = 0; c < cols; ++c) {
+      const int64_t h = c / num_rows, t = c % num_rows;
+      memset(taken, 0, (size_t)ktiles);
+      int32_t n = 0;
+      /* k rounds of "the best remaining candidate": the largest score, the
+       * lowest block among equal scores; -inf and NaN are not candidates */
+      for (int32_t r = 0; r < k; ++r) {
+        int32_t best = -1;
+        float bv = 0.0f;
+        for (int32_t b = 0; b < ktiles; ++b) {
+          const float v = scores[(h * ktiles + b) * num_rows + t];
+          if (taken[b] || isnan(v) || v == -INFINITY) continue;
+          if (best < 0 || v > bv) {
+            best = b;
+            bv = v;
+          }
+        }
+        idx[c * k + r] = best;
+        if (val) val[c * k + r] = best >= 0 ? bv : -INFINITY;
+        if (best >= 0) {
+          taken[best] = 1;
+          ++n;
+        }
+      }
+      if (count) count[c] = n;
+    }
+    free(taken);
+  }
+}
+
 int32_t orc_num_threads(void) {
 #ifdef _OPENMP
   return (int32_t)omp_get_max_threads();

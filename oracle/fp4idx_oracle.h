@@ -99,6 +99,15 @@ void orc_block_scores(const orc_problem* p, int32_t ktiles, const int32_t* rows,
 void orc_topk(const orc_problem* p, const float* w, int64_t w_row_stride, int32_t k,
               const int32_t* rows, int32_t nrows, int32_t* idx, float* val, int32_t* count);
 
+/* Top-k blocks of every (head, row) column of block scores [H][Kt][T]
+ * (M3-indexer README, "输出 shape 和类型": a caller that needs a top-k takes it
+ * along Ktiles).  A block is a candidate when its score is neither -inf (no
+ * visible key) nor NaN; order (score desc, block asc).  idx / val [H][T][k]
+ * (-1 / -inf padded; val nullable), count [H][T] = min(k, candidates)
+ * (nullable). */
+void orc_block_topk(const float* scores, int32_t num_heads, int32_t ktiles, int32_t num_rows, int32_t k,
+                    int32_t* idx, float* val, int32_t* count);
+
 /* Number of threads the parallel loops use (1 without OpenMP). */
 int32_t orc_num_threads(void);
 

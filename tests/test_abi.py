@@ -124,3 +124,15 @@ def test_logits_topk_rejects_bad_arguments_on_host(lib):
     assert lib.fp4idx_logits_topk(ctypes.byref(c), vp, 32, vp, 512, 64, 0, vp, None, None, None) == 1  # ld
     assert lib.fp4idx_logits_topk(ctypes.byref(c), vp, 32, vp, 1024, 0, 0, vp, None, None, None) == 2  # k
     assert lib.fp4idx_topk(ctypes.byref(c), vp, 32, 64, 0x4, vp, None, None, vp, 1 << 30, None) == 1  # flags
+
+
+def test_block_topk_rejects_bad_arguments_on_host(lib):
+    vp = ctypes.c_void_p(1 << 20)
+    bad = ctypes.c_void_p((1 << 20) + 2)  # not 4-byte aligned
+    assert lib.fp4idx_block_topk(None, 32, 64, 16, 16, vp, None, None, None) == 1       # scores
+    assert lib.fp4idx_block_topk(vp, 32, 64, 16, 16, None, None, None, None) == 1       # indices
+    assert lib.fp4idx_block_topk(vp, 0, 64, 16, 16, vp, None, None, None) == 1          # heads
+    assert lib.fp4idx_block_topk(vp, 32, 0, 16, 16, vp, None, None, None) == 1          # ktiles
+    assert lib.fp4idx_block_topk(vp, 32, 64, 16, 0, vp, None, None, None) == 1          # k
+    assert lib.fp4idx_block_topk(vp, 32, 64, 16, 33, vp, None, None, None) == 2         # k > 32
+    assert lib.fp4idx_block_topk(bad, 32, 64, 16, 16, vp, None, None, None) == 1        # alignment

@@ -336,3 +336,34 @@ def test_nan_query_scale_leaves_invisible_positions_neg_inf():
     assert np.isnan(out[0, :100]).all()
     assert np.isneginf(out[0, 100:]).all()
     assert np.isneginf(out[1]).all()
+
+
+def test_block_topk_hand_worked_column():
+    # one column: blocks 1 and 2 tie at 3 (lower block first), block 3 has no
+    # visible key (-inf) and block 4 a NaN score: neither is a candidate
+    s = np.array([1, 3, 3, -np.inf, np.nan, 2], np.float32).reshape(1, 6, 1)
+    idx, val, cnt = oracle.block_topk(s, 3)
+    assert idx[0, 0].tolist() == [1, 2, 5] and val[0, 0].tolist() == [3, 3, 2] and cnt[0, 0] == 3
+    idx, val, cnt = oracle.block_topk(s, 6)
+    assert idx[0, 0].tolist() == [1, 2, 5, 0, -1, -1] and cnt[0, 0] == 4
+    assert np.isneginf(val[0, 0, 4:]).all()
+
+
+def test_block_topk_matches_bruteforce_sort():
+    rng = np.random.default_rng(5)
+    H, Kt, T = 3, 37, 11
+    s = rng.integers(-4, 5, size=(H, Kt, T)).astype(np.float32)  # small integers: many ties
+    s[rng.random((H, Kt, T)) < 0.2] = -np.inf
+    s[rng.random((H, Kt, T)) < 0.05] = np.nan
+    s[0, :, 0] = -np.inf  # a column without candidates
+    for k in (1, 5, 16, 40):
+        idx, val, cnt = oracle.block_topk(s, k)
+        for h in range(H):
+            for t in range(T):
+                cands = [b for b in range(Kt) if not np.isnan(s[h, b, t]) and s[h, b, t] != -np.inf]
+                order = sorted(cands, key=lambda b: (-float(s[h, b, t]), b))[:k]
+                n = len(order)
+                assert cnt[h, t] == n
+                assert idx[h, t, :n].tolist() == order
+                assert (idx[h, t, n:] == -1).all() and np.isneginf(val[h, t, n:]).all()
+                np.testing.assert_array_equal(val[h, t, :n], s[h, order, t])
