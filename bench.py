@@ -143,6 +143,8 @@ class ClockSampler:
 WORKLOADS = {
     "verify16k": dict(maker="verify_decode_16k", kind="topk", k=2048, logits=True, fused=True, bound="hbm"),
     "long_decode": dict(maker="long_batched_decode", kind="topk", k=2048, logits=False, bound="hbm"),
+    "long_decode_slots": dict(maker="long_batched_decode", kind="topk", k=2048, logits=False, bound="hbm",
+                              slots=True),
     "block_scores": dict(maker="nvfp4_gqa_block_scores", kind="block", k=0, logits=False, bound="tensor"),
     "block_topk": dict(maker="nvfp4_gqa_block_scores", kind="block", k=0, block_k=16, logits=False,
                        bound="tensor"),
@@ -262,6 +264,9 @@ class OursBench:
                 self.kernels = ["logits_topk"]
             else:
                 self.kernels = (["scorer_logits"] if spec["logits"] else []) + ["scorer_topk", "topk_merge"]
+            if spec.get("slots"):
+                self.slots = torch.empty((T, self.k), dtype=torch.int32, device=device)
+                self.kernels.append("topk_slots")
             self.launch_count = 2 if spec.get("fused") else len(self.kernels)
         self.launches_per_step = getattr(self, "launch_count", len(self.kernels))
         self.graphs = []
@@ -285,6 +290,8 @@ class OursBench:
             calls.append(lambda: B.fp4idx_logits(prob, w, out=self.logits))
         calls.append(lambda: B.fp4idx_topk_score(prob, w, self.k, self.ws))
         calls.append(lambda: B.fp4idx_topk_merge(prob, self.k, self.idx, self.val, self.cnt, self.ws))
+        if self.spec.get("slots"):
+            calls.append(lambda: B.fp4idx_topk_slots(prob, self.idx, slots=self.slots))
         return calls
 
     def _step(self, n, evs=None):
@@ -368,7 +375,8 @@ class OursBench:
         elif self.spec["kind"] == "logits":
             d_out = [self.logits]
         else:
-            d_out = [self.idx, self.val, self.cnt] + ([self.logits] if self.logits is not None else [])
+            d_out = [self.idx, self.val, self.cnt] + ([self.logits] if self.logits is not None else []) + (
+                [self.slots] if self.spec.get("slots") else [])
         h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in d_out]
         bi = sum(t.numel() * t.element_size() for t in h_in)
         bo = sum(t.numel() * t.element_size() for t in h_out)
@@ -393,6 +401,8 @@ class OursBench:
                     B.fp4idx_logits(prob, self.w, out=self.logits)
                 B.fp4idx_topk(prob, self.w, self.k, indices=self.idx, values=self.val, valid_count=self.cnt,
                               workspace=self.ws)
+                if self.spec.get("slots"):
+                    B.fp4idx_topk_slots(prob, self.idx, slots=self.slots)
             for h, d in zip(h_out, d_out):
                 h.copy_(d, non_blocking=True)
         end.record()
@@ -424,6 +434,8 @@ def kernel_algorithmic_bytes(host, name: str, k: int) -> int:
         return kv + qb + 2 * T * ((host.max_seqlen_k + 3) // 4 * 4) * 4 + T * k * 8 + T * 4
     if name == "block_scores":
         return kv + qb + H * ((host.max_seqlen_k + 127) // 128) * T * 4
+    if name == "topk_slots":  # positions read, one table entry gathered per position, slots written
+        return T * k * 12
     if name == "block_topk":  # scores read once; indices, values, counts written
         bk = k or 16
         return H * ((host.max_seqlen_k + 127) // 128) * T * 4 + H * T * (bk * 8 + 4)
@@ -640,7 +652,8 @@ def run_ours(args, world, rank, local):
     elif spec.get("fused"):
         step_desc = f"logits + top-{spec['k']} in one call (scorer logits, per-row selection from them)"
     else:
-        step_desc = ("logits + " if spec["logits"] else "") + f"top-{spec['k']} (score + merge)"
+        step_desc = ("logits + " if spec["logits"] else "") + f"top-{spec['k']} (score + merge)" + (
+            " + physical slots" if spec.get("slots") else "")
     line = {
         "metric": METRIC,
         "value": value,

@@ -36,6 +36,7 @@ EXPORTED = (
     "fp4idx_logits",
     "fp4idx_block_scores",
     "fp4idx_block_topk",
+    "fp4idx_topk_slots",
     "fp4idx_topk_workspace_bytes",
     "fp4idx_topk",
     "fp4idx_topk_score",
@@ -105,6 +106,8 @@ def load_library(path: str = LIB_PATH):
         lib.fp4idx_block_scores.restype = i32
         lib.fp4idx_block_topk.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp]
         lib.fp4idx_block_topk.restype = i32
+        lib.fp4idx_topk_slots.argtypes = [P, vp, i32, vp, i32, vp, vp]
+        lib.fp4idx_topk_slots.restype = i32
         lib.fp4idx_topk_workspace_bytes.argtypes = [P, i32]
         lib.fp4idx_topk_workspace_bytes.restype = sz
         lib.fp4idx_topk.argtypes = [P, vp, i64, i32, u32, vp, vp, vp, vp, sz, vp]
@@ -262,6 +265,24 @@ def fp4idx_block_topk(scores: torch.Tensor, k: int, indices: Optional[torch.Tens
     _check(lib.fp4idx_block_topk(_ptr(scores), H, Kt, T, k, _ptr(indices), _ptr(values), _ptr(valid_count),
                                  _stream(stream)), "fp4idx_block_topk")
     return indices, values, valid_count
+
+
+def fp4idx_topk_slots(problem: DeviceProblem, indices: torch.Tensor, ncols: Optional[int] = None,
+                      slots: Optional[torch.Tensor] = None, stream=None):
+    """Physical cache slots [T, ncols] of the logical positions [T, k]
+    (page << offset_bits | page offset, -1 when masked or past k); returns
+    (slots, offset_bits)."""
+    lib = load_library()
+    if indices.dim() != 2 or indices.dtype != torch.int32 or not indices.is_contiguous():
+        raise ValueError("indices must be a contiguous [T, k] int32 tensor")
+    T, k = indices.shape
+    ncols = k if ncols is None else ncols
+    if slots is None:
+        slots = torch.empty((T, ncols), dtype=torch.int32, device=indices.device)
+    bits = ctypes.c_int32(0)
+    _check(lib.fp4idx_topk_slots(ctypes.byref(problem.c), _ptr(indices), k, _ptr(slots), ncols,
+                                 ctypes.byref(bits), _stream(stream)), "fp4idx_topk_slots")
+    return slots, bits.value
 
 
 def fp4idx_topk_workspace_bytes(problem: DeviceProblem, k: int) -> int:

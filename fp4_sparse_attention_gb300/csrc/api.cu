@@ -469,6 +469,41 @@ fp4idx_status_t fp4idx_logits_topk(const fp4idx_problem_t* problem, const float*
   return logits_then_select(problem, w, w_row_stride, logits, ld, k, flags, indices, values, valid_count, stream);
 }
 
+fp4idx_status_t fp4idx_topk_slots(const fp4idx_problem_t* problem, const int32_t* indices, int32_t k,
+                                  int32_t* slots, int32_t ncols, int32_t* offset_bits, void* stream) {
+  g_msg[0] = 0;
+  fp4idx_status_t s = check_problem(problem);
+  if (s != FP4IDX_OK) return s;
+  if (!indices || !slots) return fail(FP4IDX_EINVAL, "indices or slots is NULL");
+  if (k < 1 || ncols < k) return fail(FP4IDX_EINVAL, "need ncols >= k >= 1 (k = %d, ncols = %d)", k, ncols);
+  if (!aligned(indices, 4) || !aligned(slots, 4)) return fail(FP4IDX_EINVAL, "indices and slots must be 4-byte aligned");
+  int bits = 1;
+  while ((1 << bits) < problem->page_size) ++bits;  // bit length of page_size - 1, at least 1
+  if (static_cast<int64_t>(problem->num_pages) << bits >= (int64_t(1) << 31))
+    return fail(FP4IDX_EUNSUPPORTED, "num_pages << %d does not fit in 31 bits", bits);
+  if (offset_bits) *offset_bits = bits;
+  if (problem->num_rows == 0) return FP4IDX_OK;
+  SlotParams sp;
+  std::memset(&sp, 0, sizeof(sp));
+  sp.indices = indices;
+  sp.slots = slots;
+  sp.cu_seqlens_q = problem->cu_seqlens_q;
+  sp.cu_seqlens_k = problem->cu_seqlens_k;
+  sp.block_table = problem->block_table;
+  sp.page_offsets = problem->page_offsets;
+  sp.table_stride = problem->table_stride;
+  sp.num_seqs = problem->num_seqs;
+  sp.num_pages = static_cast<int32_t>(problem->num_pages);
+  sp.page_size = problem->page_size;
+  sp.page_shift = problem->page_size == 128 ? 7 : 6;
+  sp.offset_bits = bits;
+  sp.k = k;
+  sp.ncols = ncols;
+  cudaError_t e = launch_topk_slots(sp, problem->num_rows, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "slot launch");
+  return FP4IDX_OK;
+}
+
 fp4idx_status_t fp4idx_block_topk(const float* scores, int32_t num_heads, int32_t ktiles, int32_t num_rows,
                                   int32_t k, int32_t* indices, float* values, int32_t* valid_count, void* stream) {
   g_msg[0] = 0;

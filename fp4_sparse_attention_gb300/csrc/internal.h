@@ -117,6 +117,25 @@ cudaError_t launch_topk_merge(const MergeParams& p, int rows, bool many_rows, cu
 // Exact top-k of each row from p.sp.logits [T][p.sp.ld] (visibility from the problem).
 cudaError_t launch_topk_select(const MergeParams& p, int rows, cudaStream_t stream);
 cudaError_t launch_block_scores(const BlockParams& p, int format, dim3 grid, cudaStream_t stream);
+// Physical slots of selected positions (fp4idx_topk_slots).
+struct SlotParams {
+  const int32_t* indices;   // [T][k]
+  int32_t* slots;           // [T][ncols]
+  const int32_t* cu_seqlens_q;
+  const int32_t* cu_seqlens_k;
+  const int32_t* block_table;
+  const int32_t* page_offsets;
+  int64_t table_stride;
+  int32_t num_seqs;
+  int32_t num_pages;
+  int32_t page_size;
+  int32_t page_shift;
+  int32_t offset_bits;
+  int32_t k;
+  int32_t ncols;
+};
+cudaError_t launch_topk_slots(const SlotParams& p, int32_t rows, cudaStream_t stream);
+
 // Top-k blocks of each (head, row) column of [H][Kt][T] block scores, k <= 32.
 cudaError_t launch_block_topk(const float* scores, int32_t H, int32_t Kt, int32_t T, int32_t k, int32_t* indices,
                               float* values, int32_t* valid_count, cudaStream_t stream);

@@ -263,6 +263,28 @@ fp4idx_status_t fp4idx_topk_noalloc(const fp4idx_problem_t* problem, const float
                                     void* stream);
 
 /*
+ * Physical cache slots of selected positions, for a sparse-attention consumer
+ * that gathers K/V rows by slot (vLLM QSA page, _qsa_physical_slots_kernel:
+ * each logical token of a row goes through its request's page table once,
+ * becoming page << offset_bits | page offset; masked entries and the padding
+ * past the selection become -1).
+ *   indices   [T][k] int32, device: logical positions of each row (e.g. the
+ *             output of fp4idx_topk), -1 for none.
+ *   slots     [T][ncols] int32, device: for c < k and s = indices[t][c] with
+ *             0 <= s < the key count of t's request and a physical page
+ *             p = table(request, s / page_size) in [0, num_pages):
+ *                 (p << offset_bits) | (s % page_size);
+ *             -1 otherwise, and for every k <= c < ncols.
+ *   offset_bits = max(1, bit length of page_size - 1) (6 for 64-key pages, 7
+ *             for 128), returned through *offset_bits when not NULL.
+ * Requires ncols >= k >= 1 and num_pages << offset_bits < 2^31 (EUNSUPPORTED
+ * otherwise).  Device metadata is read on the device only; graph-capturable.
+ */
+fp4idx_status_t fp4idx_topk_slots(const fp4idx_problem_t* problem, const int32_t* indices,
+                                  int32_t k, int32_t* slots, int32_t ncols,
+                                  int32_t* offset_bits, void* stream);
+
+/*
  * Device error word of the current device (FP4IDX_ERR_* bits).  Synchronises
  * `stream` first; when clear != 0 the word is reset to 0 afterwards.
  */

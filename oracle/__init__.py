@@ -92,6 +92,8 @@ def _load():
             lib.orc_block_scores.argtypes = [P, i32, vp, i32, vp, vp, vp]
             lib.orc_topk.restype = None
             lib.orc_topk.argtypes = [P, vp, i64, i32, vp, i32, vp, vp, vp]
+            lib.orc_topk_slots.restype = None
+            lib.orc_topk_slots.argtypes = [P, vp, i32, i32, vp]
             lib.orc_block_topk.restype = None
             lib.orc_block_topk.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp]
             lib.orc_num_threads.restype = i32
@@ -279,3 +281,14 @@ def block_topk(scores, k: int):
     cnt = np.empty((H, T), np.int32)
     _load().orc_block_topk(_ptr(sc), H, Kt, T, k, _ptr(idx), _ptr(val), _ptr(cnt))
     return idx, val, cnt
+
+
+def topk_slots(prob, indices, ncols=None):
+    """Physical cache slots [T, ncols] of the logical positions indices [T, k]."""
+    op = _as_oracle(prob)
+    ind = np.ascontiguousarray(np.asarray(indices, dtype=np.int32))
+    T, k = ind.shape
+    ncols = k if ncols is None else ncols
+    out = np.empty((T, ncols), np.int32)
+    _load().orc_topk_slots(op.ref, _ptr(ind), k, ncols, _ptr(out))
+    return out

@@ -329,6 +329,27 @@ void orc_block_topk(const float* scores, int32_t num_heads, int32_t ktiles, int3
   }
 }
 
+void orc_topk_slots(const orc_problem* p, const int32_t* indices, int32_t k, int32_t ncols, int32_t* slots) {
+  int32_t bits = 1;
+  while ((1 << bits) < p->page_size) ++bits;
+  for (int32_t t = 0; t < p->num_rows; ++t) {
+    const int32_t b = orc_request_of_row(p, t);
+    const int64_t k_len = (int64_t)p->cu_seqlens_k[b + 1] - p->cu_seqlens_k[b];
+    for (int32_t c = 0; c < ncols; ++c) {
+      int32_t slot = -1;
+      if (c < k) {
+        const int64_t s = indices[(int64_t)t * k + c];
+        if (s >= 0 && s < k_len) {
+          const int64_t base = p->page_offsets ? (int64_t)p->page_offsets[b] : (int64_t)b * p->table_stride;
+          const int64_t page = p->block_table[base + s / p->page_size];
+          if (page >= 0 && page < p->num_pages) slot = (int32_t)((page << bits) | (s % p->page_size));
+        }
+      }
+      slots[(int64_t)t * ncols + c] = slot;
+    }
+  }
+}
+
 int32_t orc_num_threads(void) {
 #ifdef _OPENMP
   return (int32_t)omp_get_max_threads();

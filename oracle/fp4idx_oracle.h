@@ -108,6 +108,13 @@ void orc_topk(const orc_problem* p, const float* w, int64_t w_row_stride, int32_
 void orc_block_topk(const float* scores, int32_t num_heads, int32_t ktiles, int32_t num_rows, int32_t k,
                     int32_t* idx, float* val, int32_t* count);
 
+/* Physical cache slots of logical positions (vLLM QSA page,
+ * _qsa_physical_slots_kernel): for c < k and s = indices[t][c] with
+ * 0 <= s < the key count of t's request and page = table(request, s / page)
+ * in [0, num_pages): (page << bits) | (s % page_size), bits = max(1, bit
+ * length of page_size - 1); -1 otherwise and for k <= c < ncols. */
+void orc_topk_slots(const orc_problem* p, const int32_t* indices, int32_t k, int32_t ncols, int32_t* slots);
+
 /* Number of threads the parallel loops use (1 without OpenMP). */
 int32_t orc_num_threads(void);
 

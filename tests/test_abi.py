@@ -136,3 +136,19 @@ def test_block_topk_rejects_bad_arguments_on_host(lib):
     assert lib.fp4idx_block_topk(vp, 32, 64, 16, 0, vp, None, None, None) == 1          # k
     assert lib.fp4idx_block_topk(vp, 32, 64, 16, 33, vp, None, None, None) == 2         # k > 32
     assert lib.fp4idx_block_topk(bad, 32, 64, 16, 16, vp, None, None, None) == 1        # alignment
+
+
+def test_topk_slots_rejects_bad_arguments_on_host(lib):
+    vp = ctypes.c_void_p(1 << 20)
+    bits = ctypes.c_int32(0)
+    c = _problem()
+    assert lib.fp4idx_topk_slots(ctypes.byref(c), None, 16, vp, 16, None, None) == 1          # indices
+    assert lib.fp4idx_topk_slots(ctypes.byref(c), vp, 16, None, 16, None, None) == 1          # slots
+    assert lib.fp4idx_topk_slots(ctypes.byref(c), vp, 0, vp, 16, None, None) == 1             # k
+    assert lib.fp4idx_topk_slots(ctypes.byref(c), vp, 16, vp, 8, None, None) == 1             # ncols < k
+    big = _problem(page_size=128, num_pages=1 << 24)
+    assert lib.fp4idx_topk_slots(ctypes.byref(big), vp, 16, vp, 16, ctypes.byref(bits), None) == 2
+    # an empty problem writes nothing but reports the layout
+    empty = _problem(num_rows=0, page_size=128)
+    assert lib.fp4idx_topk_slots(ctypes.byref(empty), vp, 16, vp, 16, ctypes.byref(bits), None) == 0
+    assert bits.value == 7

@@ -367,3 +367,25 @@ def test_block_topk_matches_bruteforce_sort():
                 assert idx[h, t, :n].tolist() == order
                 assert (idx[h, t, n:] == -1).all() and np.isneginf(val[h, t, n:]).all()
                 np.testing.assert_array_equal(val[h, t, :n], s[h, order, t])
+
+
+def test_topk_slots_hand_worked():
+    # 64-key pages: offset_bits 6; position 130 is logical page 2, offset 2
+    p = _small(q_lens=[2], k_lens=[300], visibility="full", cache_pages=12)
+    p.block_table[0, :5] = [7, 3, 11, 0, 5]
+    ind = np.array([[130, 0, -1, 299], [300, 63, 64, 192]], np.int32)
+    got = oracle.topk_slots(p, ind, ncols=6)
+    assert got[0].tolist() == [(11 << 6) | 2, (7 << 6) | 0, -1, (5 << 6) | 43, -1, -1]
+    # 300 is past the request's 300 keys; 63 and 64 straddle pages 0 and 1
+    assert got[1].tolist() == [-1, (7 << 6) | 63, (3 << 6) | 0, (0 << 6) | 0, -1, -1]
+
+
+def test_topk_slots_128_key_pages_and_bad_pages():
+    p = _small(q_lens=[1, 1], k_lens=[256, 200], page_size=128, visibility="full", table_form="offsets")
+    table = p.block_table.reshape(-1)
+    b0, b1 = int(p.page_offsets[0]), int(p.page_offsets[1])
+    table[b0:b0 + 2] = [2, p.num_pages]  # second page out of range
+    table[b1:b1 + 2] = [1, -3]
+    ind = np.array([[5, 130], [127, 199]], np.int32)
+    got = oracle.topk_slots(p, ind)
+    assert got.tolist() == [[(2 << 7) | 5, -1], [(1 << 7) | 127, -1]]
