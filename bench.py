@@ -41,6 +41,11 @@ sys.path.insert(0, ROOT)
 
 METRIC = ("query×key scores/sec and µs/call; % of HBM BW (decode) / FP4 TC peak (prefill)")
 UNIT = "scores/s"
+
+
+def unit_of(spec) -> str:
+    """The K-cache writer counts keys written; every other workload scores."""
+    return "keys/s" if spec["kind"] == "store" else UNIT
 L2_BYTES = 129 * 1024 * 1024
 
 # DRAM bytes per launch from ncu captures, valid only for the kernel sources
@@ -150,6 +155,7 @@ WORKLOADS = {
                        bound="tensor"),
     "prefill": dict(maker="prefill_32k", kind="topk", k=2048, logits=False, bound="tensor"),
     "tiny": dict(maker="tiny_mx_decode", kind="topk", k=64, logits=True, bound="hbm"),
+    "store_k": dict(maker="kcache_write_1m", kind="store", k=0, logits=False, bound="hbm", tokens=1 << 20),
     "logits16k": dict(maker="verify_decode_16k", kind="logits", k=0, logits=True, bound="hbm"),
     "logits100k": dict(maker="verify_decode_100k", kind="logits", k=0, logits=True, bound="hbm"),
     "logits400k": dict(maker="verify_decode_400k", kind="logits", k=0, logits=True, bound="hbm"),
@@ -221,6 +227,7 @@ class OursBench:
         self.host, self.spec, self.device = host, spec, device
         self.k = spec["k"]
         self.block = spec["kind"] == "block"
+        self.store = spec["kind"] == "store"
         base = B.DeviceProblem.from_host(host, device=device)
         T = base.num_rows
         self.w = None if host.w is None else torch.as_tensor(host.w).to(device)
@@ -240,7 +247,15 @@ class OursBench:
                 causal=base.causal, qo_offset=base.qo_offset, max_seqlen_q=base.max_seqlen_q,
                 max_seqlen_k=base.max_seqlen_k))
             self.ws_list.append(None if self.w is None else self.w.clone())
-        if self.block:
+        if self.store:
+            # 2^20 tokens of bf16 keys (256 MB, larger than 2x L2) to distinct random slots
+            g = torch.Generator(device="cpu").manual_seed(7)
+            self.tokens = spec["tokens"]
+            self.keys = (torch.randn((self.tokens, base.num_kv_heads, 128), generator=g) * 4).to(torch.bfloat16).to(device)
+            cap = base.k.shape[0] * base.page_size
+            self.slots = torch.randperm(cap, generator=g)[: self.tokens].to(torch.int32).to(device)
+            self.kernels = ["store_k"]
+        elif self.block:
             self.scores = torch.empty((base.num_heads, base.ktiles, T), dtype=torch.float32, device=device)
             self.kernels = ["block_scores"]
             self.block_k = spec.get("block_k", 0)
@@ -275,6 +290,8 @@ class OursBench:
     def _calls(self, n):
         B = self.B
         prob, w = self.problems[n], self.ws_list[n]
+        if self.store:
+            return [lambda: B.fp4idx_store_k(self.keys, self.slots, prob.page_size, prob.k, prob.k_scale)]
         if self.block:
             calls = [lambda: B.fp4idx_block_scores(prob, out=self.scores)]
             if self.block_k:
@@ -369,8 +386,12 @@ class OursBench:
         prob = self.problems[0]
         d_in = [prob.q, prob.q_scale, prob.block_table] + ([self.w] if self.w is not None else []) + (
             [prob.visible_len] if prob.visible_len is not None else [])
+        if self.store:
+            d_in = [self.keys, self.slots]
         h_in = [t.cpu().pin_memory() for t in d_in]
-        if self.block:
+        if self.store:
+            d_out = [self.slots[:1]]  # completion marker (the cache is resident state)
+        elif self.block:
             d_out = [self.scores] + ([self.bidx, self.bval, self.bcnt] if self.block_k else [])
         elif self.spec["kind"] == "logits":
             d_out = [self.logits]
@@ -387,7 +408,9 @@ class OursBench:
         for _ in range(steps):
             for h, d in zip(h_in, d_in):
                 d.copy_(h, non_blocking=True)
-            if self.block:
+            if self.store:
+                B.fp4idx_store_k(self.keys, self.slots, prob.page_size, prob.k, prob.k_scale)
+            elif self.block:
                 B.fp4idx_block_scores(prob, out=self.scores)
                 if self.block_k:
                     B.fp4idx_block_topk(self.scores, self.block_k, self.bidx, self.bval, self.bcnt)
@@ -434,6 +457,8 @@ def kernel_algorithmic_bytes(host, name: str, k: int) -> int:
         return kv + qb + 2 * T * ((host.max_seqlen_k + 3) // 4 * 4) * 4 + T * k * 8 + T * 4
     if name == "block_scores":
         return kv + qb + H * ((host.max_seqlen_k + 127) // 128) * T * 4
+    if name == "store_k":  # bf16 keys read, codes + scales written, per token and K head
+        return k * host.num_kv_heads * (256 + 68) + k * 4
     if name == "topk_slots":  # positions read, one table entry gathered per position, slots written
         return T * k * 12
     if name == "block_topk":  # scores read once; indices, values, counts written
@@ -466,7 +491,8 @@ def roofline(host, spec, name: str, launch_ms: float, step_ms: float, peaks: dic
                 "launch_us": launch_ms * 1e3,
                 "peak_source": f"{peaks['source']} bf16 {'sustained' if sustained else 'burst'} "
                                f"{bf16:.1f} TFLOP/s x {FP4_PER_BF16:g} (nominal FP4/bf16 ratio)"}
-    alg = kernel_algorithmic_bytes(host, name, spec.get("block_k", 0) if name == "block_topk" else spec["k"])
+    kk = spec.get("block_k", 0) if name == "block_topk" else (spec.get("tokens", 0) if name == "store_k" else spec["k"])
+    alg = kernel_algorithmic_bytes(host, name, kk)
     achieved = alg / (launch_ms * 1e-3) / 1e9
     return {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes": alg,
@@ -481,6 +507,16 @@ def oracle_sample(host, spec):
     row = int(host.cu_seqlens_q[1]) - 1
     vis = oracle.visible(host, row)
     op = oracle.OracleProblem(host)
+    if spec["kind"] == "store":
+        n = 8192
+        rng = np.random.default_rng(0)
+        keys = (rng.standard_normal((n, host.num_kv_heads, 128)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        slots = rng.permutation(host.k.shape[0] * host.page_size)[:n].astype(np.int32)
+        k, ks = host.k.copy(), host.k_scale.copy()
+
+        def step():
+            oracle.store_k(keys, slots, host.page_size, k, ks)
+        return step, n, f"{n} keys quantized and written"
     if spec["kind"] == "block":
         bk = spec.get("block_k", 0)
 
@@ -517,7 +553,7 @@ def cpu_baseline(host, spec, budget_s: float = 10.0) -> dict:
         if time.perf_counter() - t0 >= budget_s:
             break
     el = time.perf_counter() - t0
-    return {"value": reps * vis / el, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+    return {"value": reps * vis / el, "unit": unit_of(spec), "cores": oracle.num_threads(), "kind": "oracle",
             "sample": what, "seconds": round(el, 2), "reps": reps}
 
 
@@ -573,13 +609,13 @@ def run_reference(args, world, rank):
     value = args.steps * vis / el
     sample = what + " per step"
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit_of(spec), "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {**host.summary(), "sample": sample},
-        "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": oracle.num_threads(),
+        "cpu_baseline": {"value": value, "unit": unit_of(spec), "kind": "oracle", "cores": oracle.num_threads(),
                          "sample": sample},
-        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": value, "unit": unit_of(spec), "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
@@ -597,7 +633,7 @@ def run_ours(args, world, rank, local):
     host = make_host_problem(args.workload)
     bench = OursBench(host, spec, device)
     bench.capture()
-    pairs = visible_pairs(host)
+    pairs = spec["tokens"] if spec["kind"] == "store" else visible_pairs(host)
     for j in range(args.warmup):
         bench.run(j)
     torch.cuda.synchronize(device)
@@ -644,7 +680,9 @@ def run_ours(args, world, rank, local):
     sha = source_sha()
     rec = RECORDED_TRAFFIC.get((args.workload, dominant))
     roof["traffic"] = rec["bytes"] if rec and rec["sha"] == sha else None
-    if spec["kind"] == "block":
+    if spec["kind"] == "store":
+        step_desc = f"MXFP4 K-cache write of {spec['tokens']} bf16 keys to random slots"
+    elif spec["kind"] == "block":
         step_desc = f"block maxima [{host.num_heads}, {host.ktiles}, {host.q.shape[0]}]" + \
             (f" + top-{spec['block_k']} blocks per (head, row)" if spec.get("block_k") else "")
     elif spec["kind"] == "logits":
@@ -657,7 +695,7 @@ def run_ours(args, world, rank, local):
     line = {
         "metric": METRIC,
         "value": value,
-        "unit": UNIT,
+        "unit": unit_of(spec),
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -684,7 +722,7 @@ def run_ours(args, world, rank, local):
                              for n in kt for r in [roofline(host, spec, n, kt[n], step_ms, peaks)]},
         "kernels_us": {n: round(v * 1e3, 3) for n, v in kt.items()},
         "kernels_timing": kt_method,
-        "e2e": {"value": world * e2e_steps * pairs / (e2e_ms * 1e-3), "unit": UNIT,
+        "e2e": {"value": world * e2e_steps * pairs / (e2e_ms * 1e-3), "unit": unit_of(spec),
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": e2e_ms / e2e_steps},
         "gpu_launches": args.steps * bench.launches_per_step,

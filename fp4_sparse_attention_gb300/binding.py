@@ -37,6 +37,7 @@ EXPORTED = (
     "fp4idx_block_scores",
     "fp4idx_block_topk",
     "fp4idx_topk_slots",
+    "fp4idx_store_k",
     "fp4idx_topk_workspace_bytes",
     "fp4idx_topk",
     "fp4idx_topk_score",
@@ -108,6 +109,8 @@ def load_library(path: str = LIB_PATH):
         lib.fp4idx_block_topk.restype = i32
         lib.fp4idx_topk_slots.argtypes = [P, vp, i32, vp, i32, vp, vp]
         lib.fp4idx_topk_slots.restype = i32
+        lib.fp4idx_store_k.argtypes = [vp, i64, i32, i32, vp, i32, i64, vp, vp, vp]
+        lib.fp4idx_store_k.restype = i32
         lib.fp4idx_topk_workspace_bytes.argtypes = [P, i32]
         lib.fp4idx_topk_workspace_bytes.restype = sz
         lib.fp4idx_topk.argtypes = [P, vp, i64, i32, u32, vp, vp, vp, vp, sz, vp]
@@ -283,6 +286,19 @@ def fp4idx_topk_slots(problem: DeviceProblem, indices: torch.Tensor, ncols: Opti
     _check(lib.fp4idx_topk_slots(ctypes.byref(problem.c), _ptr(indices), k, _ptr(slots), ncols,
                                  ctypes.byref(bits), _stream(stream)), "fp4idx_topk_slots")
     return slots, bits.value
+
+
+def fp4idx_store_k(keys: torch.Tensor, slots: torch.Tensor, page_size: int, k: torch.Tensor,
+                   k_scale: torch.Tensor, stream=None) -> None:
+    """Quantize bf16 keys [N, Hkv, 128] into the MXFP4 cache k [P, Hkv, page, 64] /
+    k_scale [P, Hkv, page, 4] (uint8, written in place) at token slots [N]."""
+    lib = load_library()
+    if keys.dim() != 3 or keys.dtype != torch.bfloat16 or keys.shape[2] != 128 or keys.stride(2) != 1 \
+            or keys.stride(1) != 128:
+        raise ValueError("keys must be [N, Hkv, 128] bfloat16 with contiguous rows")
+    N, Hkv, _ = keys.shape
+    _check(lib.fp4idx_store_k(_ptr(keys), keys.stride(0), N, Hkv, _ptr(slots), page_size, k.shape[0], _ptr(k),
+                              _ptr(k_scale), _stream(stream)), "fp4idx_store_k")
 
 
 def fp4idx_topk_workspace_bytes(problem: DeviceProblem, k: int) -> int:

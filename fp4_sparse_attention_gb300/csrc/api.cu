@@ -469,6 +469,39 @@ fp4idx_status_t fp4idx_logits_topk(const fp4idx_problem_t* problem, const float*
   return logits_then_select(problem, w, w_row_stride, logits, ld, k, flags, indices, values, valid_count, stream);
 }
 
+fp4idx_status_t fp4idx_store_k(const uint16_t* keys, int64_t key_row_stride, int32_t num_tokens,
+                               int32_t num_kv_heads, const int32_t* slots, int32_t page_size, int64_t num_pages,
+                               uint8_t* k, uint8_t* k_scale, void* stream) {
+  g_msg[0] = 0;
+  if (!keys || !slots || !k || !k_scale) return fail(FP4IDX_EINVAL, "keys, slots, k or k_scale is NULL");
+  if (num_tokens < 0 || num_kv_heads < 1 || num_pages < 1)
+    return fail(FP4IDX_EINVAL, "num_tokens >= 0, num_kv_heads >= 1 and num_pages >= 1 required");
+  if (page_size != 64 && page_size != 128) return fail(FP4IDX_EUNSUPPORTED, "page_size %d: 64 or 128", page_size);
+  if (key_row_stride < static_cast<int64_t>(num_kv_heads) * 128 || key_row_stride % 8 != 0)
+    return fail(FP4IDX_EINVAL, "key_row_stride must be >= num_kv_heads * 128 and a multiple of 8");
+  if (!aligned(keys, 16) || !aligned(k, 16) || !aligned(slots, 4))
+    return fail(FP4IDX_EINVAL, "keys and k must be 16-byte aligned, slots 4-byte aligned");
+  if (num_tokens == 0) return FP4IDX_OK;
+  DeviceInfo* dev;
+  fp4idx_status_t s;
+  if ((s = device_info(&dev)) != FP4IDX_OK) return s;
+  StoreParams sp;
+  std::memset(&sp, 0, sizeof(sp));
+  sp.keys = keys;
+  sp.key_row_stride = key_row_stride;
+  sp.slots = slots;
+  sp.k = k;
+  sp.k_scale = k_scale;
+  sp.num_pages = num_pages;
+  sp.num_tokens = num_tokens;
+  sp.num_kv_heads = num_kv_heads;
+  sp.page_size = page_size;
+  sp.err = dev->err;
+  cudaError_t e = launch_store_k(sp, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "store launch");
+  return FP4IDX_OK;
+}
+
 fp4idx_status_t fp4idx_topk_slots(const fp4idx_problem_t* problem, const int32_t* indices, int32_t k,
                                   int32_t* slots, int32_t ncols, int32_t* offset_bits, void* stream) {
   g_msg[0] = 0;

@@ -117,6 +117,21 @@ cudaError_t launch_topk_merge(const MergeParams& p, int rows, bool many_rows, cu
 // Exact top-k of each row from p.sp.logits [T][p.sp.ld] (visibility from the problem).
 cudaError_t launch_topk_select(const MergeParams& p, int rows, cudaStream_t stream);
 cudaError_t launch_block_scores(const BlockParams& p, int format, dim3 grid, cudaStream_t stream);
+// MXFP4 K-cache writer (fp4idx_store_k).
+struct StoreParams {
+  const uint16_t* keys;     // [N][Hkv][128] bf16 words, token stride key_row_stride
+  int64_t key_row_stride;
+  const int32_t* slots;     // [N]
+  uint8_t* k;               // [P][Hkv][page][64]
+  uint8_t* k_scale;         // [P][Hkv][page][4]
+  int64_t num_pages;
+  int32_t num_tokens;
+  int32_t num_kv_heads;
+  int32_t page_size;
+  uint32_t* err;
+};
+cudaError_t launch_store_k(const StoreParams& p, cudaStream_t stream);
+
 // Physical slots of selected positions (fp4idx_topk_slots).
 struct SlotParams {
   const int32_t* indices;   // [T][k]

@@ -265,6 +265,13 @@ def verify_decode_400k() -> Problem:
     return verify_decode_context(400_000)
 
 
+def kcache_write_1m() -> Problem:
+    """Cache geometry for the K-cache writer: 32,768 pages of 64 keys, one K
+    head (the keys written are generated by the caller)."""
+    return make_problem(name="mxfp4_kcache_write_1m", seed=1005, fmt=MXFP4, q_lens=[1], k_lens=[64], num_heads=8,
+                        weights="sixteenths", visibility="full", cache_pages=32768, topk=0)
+
+
 def long_batched_decode(num_requests: int = 16, cache_keys: int = 14_000_000) -> Problem:
     """16 requests x 4 rows, 32 heads, MXFP4, each context drawn from
     {100,000, 400,000}; 64-key pages dealt from one random permutation of a

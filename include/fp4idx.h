@@ -263,6 +263,34 @@ fp4idx_status_t fp4idx_topk_noalloc(const fp4idx_problem_t* problem, const float
                                     void* stream);
 
 /*
+ * Write keys into the MXFP4 cache (SGLang PR 42861: the benchmark fills the
+ * cache with store_fp4_index_k_cache(keys, table, slots, page_size, rne=True);
+ * "Modifications": the quantizer clamps E8M0 exponents to 1..254 and the
+ * E2M1 level set is [0, 0.5, 1, 1.5, 2, 3, 4, 6]).  The pages do not print
+ * the scale rule; this call uses the OCP microscaling one:
+ *   per group of 32 values of one (token, K head) row:
+ *     code  = clamp(floor(log2(max |x|)) - 2 + 127, 1, 254)   (1 for all zeros)
+ *     scale = 2^(code - 127)
+ *     each value: x / scale rounded to the nearest E2M1 level, ties to the
+ *     even level (round-to-nearest-even on the E2M1 grid), saturating at 6;
+ *     sign bit set only for a non-zero level.
+ *   keys      [N][Hkv][128] bfloat16 (raw 16-bit words), device; key_row_stride
+ *             = elements between consecutive tokens (>= Hkv * 128).  Finite.
+ *   slots     [N] int32, device: token i is written at page slots[i] / page_size,
+ *             offset slots[i] % page_size of every K head; a negative slot is
+ *             skipped; a slot >= num_pages * page_size is skipped and sets
+ *             FP4IDX_ERR_PAGE_RANGE.
+ *   k, k_scale  the cache of fp4idx_problem_t with format FP4IDX_MXFP4:
+ *             [num_pages][Hkv][page_size][64] and [num_pages][Hkv][page_size][4].
+ * Graph-capturable, no workspace.  EINVAL on NULL pointers, sizes or
+ * misalignment (keys 16-byte aligned with key_row_stride a multiple of 8;
+ * k 16-byte aligned), EUNSUPPORTED for page_size other than 64 or 128.
+ */
+fp4idx_status_t fp4idx_store_k(const uint16_t* keys, int64_t key_row_stride, int32_t num_tokens,
+                               int32_t num_kv_heads, const int32_t* slots, int32_t page_size,
+                               int64_t num_pages, uint8_t* k, uint8_t* k_scale, void* stream);
+
+/*
  * Physical cache slots of selected positions, for a sparse-attention consumer
  * that gathers K/V rows by slot (vLLM QSA page, _qsa_physical_slots_kernel:
  * each logical token of a row goes through its request's page table once,

@@ -92,6 +92,8 @@ def _load():
             lib.orc_block_scores.argtypes = [P, i32, vp, i32, vp, vp, vp]
             lib.orc_topk.restype = None
             lib.orc_topk.argtypes = [P, vp, i64, i32, vp, i32, vp, vp, vp]
+            lib.orc_store_k.restype = None
+            lib.orc_store_k.argtypes = [vp, i64, i32, i32, vp, i32, i64, vp, vp]
             lib.orc_topk_slots.restype = None
             lib.orc_topk_slots.argtypes = [P, vp, i32, i32, vp]
             lib.orc_block_topk.restype = None
@@ -292,3 +294,15 @@ def topk_slots(prob, indices, ncols=None):
     out = np.empty((T, ncols), np.int32)
     _load().orc_topk_slots(op.ref, _ptr(ind), k, ncols, _ptr(out))
     return out
+
+
+def store_k(keys_bf16, slots, page_size: int, k, k_scale):
+    """Write keys (bf16 words [N, Hkv, 128], uint16) into the MXFP4 cache
+    arrays k [P, Hkv, page, 64] / k_scale [P, Hkv, page, 4] (uint8, modified in
+    place) at the given slots."""
+    keys = np.ascontiguousarray(np.asarray(keys_bf16, dtype=np.uint16))
+    N, Hkv, D = keys.shape
+    assert D == 128 and k.dtype == np.uint8 and k_scale.dtype == np.uint8
+    assert k.flags.c_contiguous and k_scale.flags.c_contiguous
+    sl = np.ascontiguousarray(np.asarray(slots, dtype=np.int32))
+    _load().orc_store_k(_ptr(keys), Hkv * 128, N, Hkv, _ptr(sl), page_size, k.shape[0], _ptr(k), _ptr(k_scale))

@@ -350,6 +350,61 @@ void orc_topk_slots(const orc_problem* p, const int32_t* indices, int32_t k, int
   }
 }
 
+/* value of a bfloat16 word from its fields: (-1)^s 2^(e-127) (1 + m/128), or
+ * (-1)^s 2^-126 m/128 for e = 0 */
+static double bf16_value(uint16_t w) {
+  const int s = w >> 15, e = (w >> 7) & 0xFF, m = w & 0x7F;
+  double v;
+  if (e == 0) v = ldexp((double)m / 128.0, -126);
+  else if (e == 255) v = m ? NAN : INFINITY;
+  else v = ldexp(1.0 + (double)m / 128.0, e - 127);
+  return s ? -v : v;
+}
+
+void orc_store_k(const uint16_t* keys, int64_t key_row_stride, int32_t num_tokens, int32_t num_kv_heads,
+                 const int32_t* slots, int32_t page_size, int64_t num_pages, uint8_t* k, uint8_t* k_scale) {
+  for (int32_t i = 0; i < num_tokens; ++i) {
+    const int64_t slot = slots[i];
+    if (slot < 0 || slot >= num_pages * page_size) continue;
+    for (int32_t h = 0; h < num_kv_heads; ++h) {
+      const int64_t crow = ((slot / page_size) * num_kv_heads + h) * page_size + slot % page_size;
+      for (int g = 0; g < 4; ++g) {
+        double x[32], amax = 0.0;
+        for (int j = 0; j < 32; ++j) {
+          x[j] = bf16_value(keys[i * key_row_stride + h * 128 + g * 32 + j]);
+          if (fabs(x[j]) > amax) amax = fabs(x[j]);
+        }
+        /* shared exponent: floor(log2(amax)) minus E2M1's largest exponent (2) */
+        int code = 1;
+        if (amax > 0.0) {
+          int ex;
+          frexp(amax, &ex); /* amax = f 2^ex, f in [0.5, 1): floor(log2 amax) = ex - 1 */
+          code = ex - 1 - 2 + 127;
+          if (code < 1) code = 1;
+          if (code > 254) code = 254;
+        }
+        const double scale = ldexp(1.0, code - 127);
+        k_scale[crow * 4 + g] = (uint8_t)code;
+        for (int j = 0; j < 32; j += 2) {
+          uint8_t byte = 0;
+          for (int u = 0; u < 2; ++u) {
+            const double y = fabs(x[j + u]) / scale;
+            /* nearest E2M1 level; on a tie the level with the even index */
+            int best = 0;
+            for (int l = 1; l < 8; ++l) {
+              const double d = fabs(y - kE2M1Levels[l]), db = fabs(y - kE2M1Levels[best]);
+              if (d < db || (d == db && (l & 1) == 0)) best = l;
+            }
+            const int nib = best | ((x[j + u] < 0.0 && best != 0) ? 8 : 0);
+            byte |= (uint8_t)(nib << (4 * u));
+          }
+          k[crow * 64 + g * 16 + j / 2] = byte;
+        }
+      }
+    }
+  }
+}
+
 int32_t orc_num_threads(void) {
 #ifdef _OPENMP
   return (int32_t)omp_get_max_threads();

@@ -115,6 +115,18 @@ void orc_block_topk(const float* scores, int32_t num_heads, int32_t ktiles, int3
  * length of page_size - 1); -1 otherwise and for k <= c < ncols. */
 void orc_topk_slots(const orc_problem* p, const int32_t* indices, int32_t k, int32_t ncols, int32_t* slots);
 
+/* MXFP4 K-cache writer (SGLang PR 42861: store_fp4_index_k_cache with
+ * round-to-nearest-even; E8M0 codes clamped to 1..254; the scale rule is the
+ * OCP microscaling one, a reading): per 32-value group of a (token, head)
+ * row, code = clamp(floor(log2 max|x|) - 2 + 127, 1, 254) (1 for zeros), each
+ * value the nearest E2M1 level of |x| / 2^(code-127), ties to the even
+ * level, saturating at 6, sign only on a non-zero level.  keys [N][Hkv][128]
+ * bf16 words with token stride key_row_stride; token i goes to slot
+ * slots[i] (page slot / page_size, offset slot % page_size); negative or
+ * out-of-range slots are skipped. */
+void orc_store_k(const uint16_t* keys, int64_t key_row_stride, int32_t num_tokens, int32_t num_kv_heads,
+                 const int32_t* slots, int32_t page_size, int64_t num_pages, uint8_t* k, uint8_t* k_scale);
+
 /* Number of threads the parallel loops use (1 without OpenMP). */
 int32_t orc_num_threads(void);
 

@@ -152,3 +152,14 @@ def test_topk_slots_rejects_bad_arguments_on_host(lib):
     empty = _problem(num_rows=0, page_size=128)
     assert lib.fp4idx_topk_slots(ctypes.byref(empty), vp, 16, vp, 16, ctypes.byref(bits), None) == 0
     assert bits.value == 7
+
+
+def test_store_k_rejects_bad_arguments_on_host(lib):
+    vp = ctypes.c_void_p(1 << 20)
+    assert lib.fp4idx_store_k(None, 128, 4, 1, vp, 64, 16, vp, vp, None) == 1      # keys
+    assert lib.fp4idx_store_k(vp, 128, 4, 1, None, 64, 16, vp, vp, None) == 1      # slots
+    assert lib.fp4idx_store_k(vp, 128, 4, 0, vp, 64, 16, vp, vp, None) == 1        # heads
+    assert lib.fp4idx_store_k(vp, 100, 4, 1, vp, 64, 16, vp, vp, None) == 1        # row stride
+    assert lib.fp4idx_store_k(vp, 128, 4, 1, vp, 32, 16, vp, vp, None) == 2        # page size
+    assert lib.fp4idx_store_k(ctypes.c_void_p((1 << 20) + 8), 128, 4, 1, vp, 64, 16, vp, vp, None) == 1
+    assert lib.fp4idx_store_k(vp, 128, 0, 1, vp, 64, 16, vp, vp, None) == 0        # nothing to write

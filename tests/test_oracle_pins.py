@@ -389,3 +389,88 @@ def test_topk_slots_128_key_pages_and_bad_pages():
     ind = np.array([[5, 130], [127, 199]], np.int32)
     got = oracle.topk_slots(p, ind)
     assert got.tolist() == [[(2 << 7) | 5, -1], [(1 << 7) | 127, -1]]
+
+
+# ---------------------------------------------------------------------------
+# MXFP4 K-cache writer
+# ---------------------------------------------------------------------------
+
+def _bf16(x):
+    a = np.asarray(x, np.float32)
+    w = (a.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal((w.astype(np.uint32) << 16).view(np.float32), a), "value not exact in bfloat16"
+    return w
+
+
+def _store_one(values, page_size=64, pages=2):
+    """One token, one head: 128 values -> (codes [128] nibbles, scale codes [4])."""
+    keys = _bf16(np.asarray(values, np.float32).reshape(1, 1, 128))
+    k = np.zeros((pages, 1, page_size, 64), np.uint8)
+    ks = np.zeros((pages, 1, page_size, 4), np.uint8)
+    oracle.store_k(keys, np.array([page_size + 3], np.int32), page_size, k, ks)
+    row = k[1, 0, 3]
+    nib = np.stack([row & 0xF, row >> 4], axis=1).reshape(-1)
+    return nib, ks[1, 0, 3]
+
+
+def test_store_k_grid_values_round_trip():
+    # a group whose largest magnitude is 6 * 2^3: scale 2^3 (code 130), every
+    # value an E2M1 level times 8, so the codes are those levels exactly
+    levels = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float32)
+    g = np.concatenate([levels, -levels, levels[::-1], -levels[::-1]]) * 8
+    nib, sc = _store_one(np.tile(g, 4))
+    assert (sc == 130).all()
+    idx = np.concatenate([np.arange(8), np.arange(8), np.arange(8)[::-1], np.arange(8)[::-1]])
+    sign = np.concatenate([np.zeros(8), np.ones(8), np.zeros(8), np.ones(8)]).astype(int)
+    want = idx | (8 * (sign * (idx != 0)))
+    assert nib[:32].tolist() == want.tolist()
+
+
+def test_store_k_ties_round_to_even_level_and_saturate():
+    # scale 1 (max 6 -> floor(log2 6) - 2 = 0, code 127)
+    g = np.zeros(32, np.float32)
+    g[:9] = [6, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.75]
+    nib, sc = _store_one(np.tile(g, 4))
+    assert sc[0] == 127
+    assert nib[:9].tolist() == [7, 0, 2, 2, 4, 4, 6, 6, 8 | 2]
+    # max 7: still scale 1 (floor(log2 7) = 2), 7 saturates to 6
+    g2 = np.zeros(32, np.float32)
+    g2[0], g2[1] = 7, -7
+    nib, sc = _store_one(np.tile(g2, 4))
+    assert sc[0] == 127 and nib[:2].tolist() == [7, 8 | 7]
+
+
+def test_store_k_zero_and_tiny_groups_take_code_one():
+    g = np.zeros(128, np.float32)
+    g[40] = 2.0 ** -130  # a subnormal bfloat16 in group 1
+    nib, sc = _store_one(g)
+    assert sc.tolist() == [1, 1, 1, 1] and (nib == 0).all()
+
+
+def test_store_k_error_bound_on_random_groups():
+    # |x - decoded| <= half the E2M1 spacing at |x| / scale, times scale,
+    # unless |x| / scale is past 6 (saturation); decodes through the oracle's
+    # pinned E2M1 / E8M0 tables
+    rng = np.random.default_rng(3)
+    vals = (rng.standard_normal(128) * 2.0 ** rng.integers(-20, 20, size=128)).astype(np.float32)
+    vals = ((vals.view(np.uint32) >> 16) << 16).view(np.float32)  # round toward zero to bfloat16
+    nib, sc = _store_one(vals)
+    for i in range(128):
+        scale = oracle.e8m0(int(sc[i // 32]))
+        dq = oracle.e2m1(int(nib[i])) * scale
+        y = abs(float(vals[i])) / scale
+        step = 0.5 if y < 2 else (1.0 if y < 4 else 2.0)
+        assert abs(float(vals[i]) - dq) <= (step / 2) * scale or y > 6
+
+
+def test_store_k_places_tokens_by_slot_and_skips_negative_slots():
+    rng = np.random.default_rng(4)
+    keys = _bf16(rng.integers(-6, 7, size=(3, 2, 128)).astype(np.float32))
+    k = np.full((4, 2, 64, 64), 0xAB, np.uint8)
+    ks = np.full((4, 2, 64, 4), 0xCD, np.uint8)
+    oracle.store_k(keys, np.array([130, -1, 5], np.int32), 64, k, ks)
+    written = {(2, 2), (0, 5)}  # (page, offset) of tokens 0 and 2
+    for pg in range(4):
+        for off in range(64):
+            untouched = (pg, off) not in written
+            assert ((k[pg, :, off] == 0xAB).all() and (ks[pg, :, off] == 0xCD).all()) == untouched
