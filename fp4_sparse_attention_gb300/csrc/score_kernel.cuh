@@ -9,7 +9,7 @@
 // R rows x H heads of one request on N (TMEM columns).  The head sum then is
 // a serial loop inside one thread: thread = key, no shuffles.
 //
-// Warp roles (128 + 128*R threads):
+// Warp roles (128 + 128 * groups threads):
 //   warp 0 and the last warp: producers, each owning alternate tiles:
 //             resolve pages through the block table, issue the TMA gather of
 //             K codes (64-byte swizzle) and one bulk copy of each page's raw
@@ -21,13 +21,19 @@
 //             holds its thread, so other work there idles the tensor pipe).
 //   warp 2    scales: Q scales -> 32x4x4 atoms -> TMEM per item; per tile
 //             the raw K scales -> 128-row scale layout -> one tcgen05.cp.
-//   warps 3.. epilogue, one group of four warps (one per TMEM lane
-//             quadrant) per query row of the item: tcgen05.ld of the row's
-//             H accumulator columns, ReLU * w summed over heads (packed fp32x2
-//             FMAs, four independent chains), visibility mask, then either the
-//             fp32 logits store or the streaming top-k append.  Each group
-//             synchronises on its own named barrier, only every few tiles, so
-//             one row's candidate compaction never stalls another row.
+//   warps 3.. epilogue, groups of four warps (one per TMEM lane quadrant):
+//             one query row per group for top-k, several rows per group for
+//             logits; tcgen05.ld of the rows' H accumulator columns, ReLU * w
+//             summed over heads (packed fp32x2 FMAs, four independent
+//             chains), visibility mask, then either the fp32 logits store or
+//             the streaming top-k append (candidate buffers in shared memory
+//             for two-row CTAs, in the workspace for four-row ones).  Each
+//             group synchronises on its own named barrier, only every few
+//             tiles, so one row's candidate compaction never stalls another.
+//
+// The barrier initialisation and TMEM allocation come before any global
+// access, so under programmatic stream serialisation they overlap the
+// previous kernel; griddepcontrol.wait then orders the rest after it.
 //
 // Work split: the tiles of all (request, row-group) items are concatenated
 // and cut into gridDim.x equal contiguous chunks, one per CTA, so long and
