@@ -12,7 +12,10 @@
  * ReLU(q.K); M3-indexer README, "数学语义": Q_real/K_real are E2M1 values times
  * their block scale, hk = h / (Hq/Hkv)).  Three outputs are offered: the full
  * logits, the per-128-key block max of dot (M3-indexer README, "输出 shape 和
- * 类型"), and the top-k positions of each row.
+ * 类型"), and the top-k positions of each row.  Around them: the top-k blocks
+ * of a block-score tensor, the physical cache slots of selected positions
+ * (the sparse-attention consumer's input) and the MXFP4 K-cache writer (the
+ * producer of the cache).
  *
  * Formats (M3-indexer README, "FP4 和 scale layout"; SGLang PR 42861,
  * "Modifications"):
@@ -27,8 +30,8 @@
  * outputs and the workspace are DEVICE pointers owned by the caller; the
  * library never allocates, frees or retains them.  The library reads no
  * device memory on the host and performs no host<->device synchronisation
- * in fp4idx_logits / fp4idx_block_scores / fp4idx_topk, so those calls can be
- * captured in a CUDA graph; the device metadata (sequence bounds, block
+ * in any call but fp4idx_get_error, so the calls can be captured in a CUDA
+ * graph; the device metadata (sequence bounds, block
  * table, visible lengths) is read on the device at run time, so replays see
  * updated contents.
  *
