@@ -26,14 +26,6 @@ __device__ __forceinline__ uint64_t globaltimer() {
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred = 0;
-  asm volatile(
-      "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(pred));
-  return pred != 0;
-}
-
 // ---------------------------------------------------------------- dependent launch
 // A kernel launched with programmatic stream serialization may start while
 // the previous kernel of the stream still runs; pdl_wait() blocks until that
@@ -68,37 +60,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
       : "memory");
   return ok != 0;
-}
-
-// Same test without a suspend-time hint: returns at once (used for polls on
-// the critical path, where a suspended thread's wake-up would add latency).
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded spin on mbar_test_wait; same contract as mbar_wait below.
-__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile int* abort,
-                                               uint32_t* err) {
-  if (mbar_test_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (;;) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_test_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
-      atomicOr(err, kErrTimeout);
-      *abort = 1;
-      return false;
-    }
-  }
 }
 
 // Wait for the phase of `parity` to complete.  Gives up after kWaitLimitNs or
