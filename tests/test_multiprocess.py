@@ -27,13 +27,15 @@ def _env():
 
 
 def test_reduce_max_and_barrier_over_two_gloo_ranks(tmp_path):
+    out = tmp_path / "out"
+    out.mkdir()
     script = (
-        "import os, bench\n"
+        "import os, sys, bench\n"
         "world, rank, local = bench.dist_setup()\n"
         "assert world == 2\n"
         "bench.barrier(world)\n"
         "m = bench.reduce_max(float(rank) + 0.5, world)\n"
-        "print('RANK', rank, 'MAX', m, flush=True)\n"
+        f"open(os.path.join({str(out)!r}, 'rank%d' % rank), 'w').write('RANK %d MAX %s' % (rank, m))\n"
         "import torch.distributed as dist\n"
         "dist.destroy_process_group()\n"
     )
@@ -43,8 +45,8 @@ def test_reduce_max_and_barrier_over_two_gloo_ranks(tmp_path):
            "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), str(path)]
     r = subprocess.run(cmd, cwd=ROOT, env=_env(), capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
-    lines = [l for l in r.stdout.splitlines() if l.startswith("RANK")]
-    assert sorted(lines) == ["RANK 0 MAX 1.5", "RANK 1 MAX 1.5"]
+    lines = sorted((out / f).read_text() for f in ("rank0", "rank1"))
+    assert lines == ["RANK 0 MAX 1.5", "RANK 1 MAX 1.5"]
 
 
 def test_reference_arm_prints_once_under_torchrun():
