@@ -516,6 +516,7 @@ fp4idx_status_t fp4idx_topk_slots(const fp4idx_problem_t* problem, const int32_t
     return fail(FP4IDX_EUNSUPPORTED, "num_pages << %d does not fit in 31 bits", bits);
   if (offset_bits) *offset_bits = bits;
   if (problem->num_rows == 0) return FP4IDX_OK;
+  if (problem->num_rows > 65535) return fail(FP4IDX_EUNSUPPORTED, "more than 65,535 rows");  // grid.y
   SlotParams sp;
   std::memset(&sp, 0, sizeof(sp));
   sp.indices = indices;
@@ -548,7 +549,7 @@ fp4idx_status_t fp4idx_block_topk(const float* scores, int32_t num_heads, int32_
   if (!aligned(scores, 4) || !aligned(indices, 4) || (values && !aligned(values, 4)) ||
       (valid_count && !aligned(valid_count, 4)))
     return fail(FP4IDX_EINVAL, "scores, indices, values and valid_count must be 4-byte aligned");
-  if (static_cast<int64_t>(num_heads) * num_rows > (int64_t(1) << 40))
+  if (static_cast<int64_t>(num_heads) * num_rows >= (int64_t(1) << 38))  // grid.x < 2^31 blocks of 256
     return fail(FP4IDX_EUNSUPPORTED, "too many columns");
   cudaError_t e = launch_block_topk(scores, num_heads, ktiles, num_rows, k, indices, values, valid_count,
                                     static_cast<cudaStream_t>(stream));

@@ -308,8 +308,8 @@ fp4idx_status_t fp4idx_store_k(const uint16_t* keys, int64_t key_row_stride, int
  *             -1 otherwise, and for every k <= c < ncols.
  *   offset_bits = max(1, bit length of page_size - 1) (6 for 64-key pages, 7
  *             for 128), returned through *offset_bits when not NULL.
- * Requires ncols >= k >= 1 and num_pages << offset_bits < 2^31 (EUNSUPPORTED
- * otherwise).  Device metadata is read on the device only; graph-capturable.
+ * Requires ncols >= k >= 1, num_pages << offset_bits < 2^31 and at most 65,535
+ * rows (EUNSUPPORTED otherwise).  Device metadata is read on the device only; graph-capturable.
  */
 fp4idx_status_t fp4idx_topk_slots(const fp4idx_problem_t* problem, const int32_t* indices,
                                   int32_t k, int32_t* slots, int32_t ncols,

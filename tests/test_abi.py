@@ -146,6 +146,8 @@ def test_topk_slots_rejects_bad_arguments_on_host(lib):
     assert lib.fp4idx_topk_slots(ctypes.byref(c), vp, 16, None, 16, None, None) == 1          # slots
     assert lib.fp4idx_topk_slots(ctypes.byref(c), vp, 0, vp, 16, None, None) == 1             # k
     assert lib.fp4idx_topk_slots(ctypes.byref(c), vp, 16, vp, 8, None, None) == 1             # ncols < k
+    many = _problem(num_rows=70000, max_seqlen_q=70000)
+    assert lib.fp4idx_topk_slots(ctypes.byref(many), vp, 16, vp, 16, None, None) == 2        # rows
     big = _problem(page_size=128, num_pages=1 << 24)
     assert lib.fp4idx_topk_slots(ctypes.byref(big), vp, 16, vp, 16, ctypes.byref(bits), None) == 2
     # an empty problem writes nothing but reports the layout
