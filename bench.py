@@ -4,14 +4,15 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 One step is one pass of the scorer over one batch of synthetic input, through
-the C ABI.  The default workload is the 4-row x 32-head verify decode over
-16,384 MXFP4 keys on shuffled 64-key pages (SGLang PR 42861's benchmark
-shape): per step the full logits [4, 16384] and the top-2048 of every row.
-Other workloads: ``long_decode`` (16 requests x 4 rows over 100k/400k keys,
-fused top-2048), ``block_scores`` (4 x 4,096 causal rows over 8,192 keys,
-Hq=32 / Hkv=4, NVFP4: the [Hq, 64, T] block maxima), ``prefill`` (32,768
-causal rows over 32,768 keys, 64 heads, fused top-2048), ``tiny`` (4 rows x
-8 heads over 1,024 keys).
+the C ABI.  The default workload is the causal prefill: 32,768 query rows
+over 32,768 MXFP4 keys, 64 heads, the top-2048 of every row with full logits
+never materialised (the largest single-GPU shape; its roofline is the FP4
+tensor pipe).  Other workloads: ``verify16k`` (SGLang PR 42861's benchmark
+shape: 4 rows x 32 heads over 16,384 keys, full logits + top-2048),
+``long_decode`` (16 requests x 4 rows over 100k/400k keys, fused top-2048),
+``block_scores`` (4 x 4,096 causal rows over 8,192 keys, Hq=32 / Hkv=4,
+NVFP4: the [Hq, 64, T] block maxima), ``tiny`` (4 rows x 8 heads over 1,024
+keys) and the ones listed in WORKLOADS.
 
 Prints one JSON line.  ``value`` is query x key scores per second over all
 ranks (a score is one (row, visible key) pair of the step, over all heads),
@@ -435,8 +436,10 @@ class OursBench:
 
 
 def kernel_algorithmic_bytes(host, name: str, k: int) -> int:
-    """Algorithmic HBM bytes of one launch: K codes + scales of every key a
-    request can see (each read once), Q codes + scales, w, and the outputs."""
+    """Algorithmic HBM bytes of one launch.  Scorer kernels: the K codes +
+    scales of every key a request can see (each read once per request), Q
+    codes + scales and w -- the inputs only; what they write is reported
+    apart (kernel_output_bytes).  Other kernels: what they read and write."""
     import oracle
 
     vis = oracle.visible_all(host)
@@ -447,16 +450,10 @@ def kernel_algorithmic_bytes(host, name: str, k: int) -> int:
     kv = keys * kv_bytes_per_key(host.format) * host.num_kv_heads
     T, H = host.q.shape[0], host.num_heads
     qb = host.q.nbytes + host.q_scale.nbytes + (T * H * 4 if host.w is not None else 0)
-    if name == "scorer_logits":
-        return kv + qb + T * ((host.max_seqlen_k + 3) // 4 * 4) * 4
-    if name == "scorer_topk":
+    if name in ("scorer_logits", "scorer_topk", "logits_topk", "block_scores"):
         return kv + qb
     if name == "topk_merge":
         return T * k * 8 + T * 4
-    if name == "logits_topk":  # both kernels of the fused call: keys in, logits out (and read back), top-k out
-        return kv + qb + 2 * T * ((host.max_seqlen_k + 3) // 4 * 4) * 4 + T * k * 8 + T * 4
-    if name == "block_scores":
-        return kv + qb + H * ((host.max_seqlen_k + 127) // 128) * T * 4
     if name == "store_k":  # bf16 keys read, codes + scales written, per token and K head
         return k * host.num_kv_heads * (256 + 68) + k * 4
     if name == "topk_slots":  # positions read, one table entry gathered per position, slots written
@@ -465,6 +462,20 @@ def kernel_algorithmic_bytes(host, name: str, k: int) -> int:
         bk = k or 16
         return H * ((host.max_seqlen_k + 127) // 128) * T * 4 + H * T * (bk * 8 + 4)
     raise KeyError(name)
+
+
+def kernel_output_bytes(host, name: str, k: int) -> int:
+    """Bytes a scorer launch writes (not part of its roofline bytes): full
+    logits, the top-k (indices + values + counts) or the block maxima."""
+    T, H = host.q.shape[0], host.num_heads
+    ld = (host.max_seqlen_k + 3) // 4 * 4
+    if name == "scorer_logits":
+        return T * ld * 4
+    if name == "logits_topk":
+        return T * ld * 4 + T * k * 8 + T * 4
+    if name == "block_scores":
+        return H * ((host.max_seqlen_k + 127) // 128) * T * 4
+    return 0
 
 
 def kernel_algorithmic_flops(host) -> int:
@@ -494,9 +505,13 @@ def roofline(host, spec, name: str, launch_ms: float, step_ms: float, peaks: dic
     kk = spec.get("block_k", 0) if name == "block_topk" else (spec.get("tokens", 0) if name == "store_k" else spec["k"])
     alg = kernel_algorithmic_bytes(host, name, kk)
     achieved = alg / (launch_ms * 1e-3) / 1e9
-    return {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes": alg,
-            "launch_us": launch_ms * 1e3, "peak_source": peaks["source"]}
+    out = {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+           "frac": achieved / peaks["hbm_gbs"], "traffic": None, "algorithmic_bytes": alg,
+           "launch_us": launch_ms * 1e3, "peak_source": peaks["source"]}
+    ob = kernel_output_bytes(host, name, kk)
+    if ob:
+        out["output_bytes"] = ob  # written by the launch, outside algorithmic_bytes and frac
+    return out
 
 
 def oracle_sample(host, spec):
@@ -744,7 +759,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="verify16k")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="prefill")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

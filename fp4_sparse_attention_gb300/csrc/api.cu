@@ -310,7 +310,7 @@ fp4idx_status_t fp4idx_logits(const fp4idx_problem_t* problem, const float* w, i
 }
 
 size_t fp4idx_topk_workspace_bytes(const fp4idx_problem_t* problem, int32_t k) {
-  if (check_problem(problem) != FP4IDX_OK || k < 1) return 0;
+  if (check_problem(problem) != FP4IDX_OK || k < 1 || k > 2048) return 0;
   DeviceInfo* dev;
   if (device_info(&dev) != FP4IDX_OK) return 0;
   return topk_workspace(problem, k, dev->sms).bytes;

@@ -106,6 +106,11 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const __grid_
   const int R = mp.rows_per_cta;
   Group<kMergeThreads, 0> g{tid};
 
+  // Only the shared-memory clear overlaps the previous kernel: every global
+  // input (the problem metadata too) may be written by it.
+  for (int i = tid; i < kHistBins; i += kMergeThreads) sm->hist[i] = 0;
+  pdl_wait();  // item starts and partial lists come from the scorer before this kernel
+
   // request of row t: largest b with cu_seqlens_q[b] <= t
   int lo = 0, hi = p.num_seqs - 1;
   while (lo < hi) {
@@ -116,9 +121,6 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const __grid_
   const int q_local = t - __ldg(p.cu_seqlens_q + b);
   const int item = b * p.row_groups + q_local / R;
   const int r = q_local % R;
-
-  for (int i = tid; i < kHistBins; i += kMergeThreads) sm->hist[i] = 0;
-  pdl_wait();  // item starts and partial lists come from the scorer before this kernel
   // tile range of the row's item in the scorer's concatenated tile space
   const int items = p.num_seqs * p.row_groups;
   const int32_t P = __ldg(p.item_start + item), total = __ldg(p.item_start + items);
@@ -232,6 +234,7 @@ __global__ void __launch_bounds__(kMergeThreads) topk_select_kernel(const __grid
   const int k = p.k;
   Group<kMergeThreads, 0> g{tid};
 
+  pdl_wait();  // the logits (and any metadata) may come from the kernel before this one
   // request of row t and its visible key count
   int lo = 0, hi = p.num_seqs - 1;
   while (lo < hi) {
@@ -244,7 +247,6 @@ __global__ void __launch_bounds__(kMergeThreads) topk_select_kernel(const __grid
   const int M = static_cast<int>(min(static_cast<int64_t>(row_visible(p, it, t)), p.ld));
   const bool local = M <= kSelectLocal;
   const float* row_logits = p.logits + static_cast<int64_t>(t) * p.ld;
-  pdl_wait();  // the logits come from the kernel before this one
   auto key_of = [](float v, int s) -> uint64_t { return isnan(v) ? 0ull : topk_key(v, static_cast<uint32_t>(s)); };
   // the row's keys, four float4 loads in flight per thread (rows are 16-byte
   // aligned: ld % 4 == 0 and a 16-byte aligned base)
@@ -418,12 +420,21 @@ __global__ void __launch_bounds__(kSmallThreads) topk_select_small_kernel(const 
   const int k = p.k;
   uint32_t* my_hist = sm.hist[lane % kSmallCopies];
 
-  // The row's visible length and the cleared counters come first: they need
-  // nothing from the scorer, so they overlap its tail (this kernel may start
-  // before the scorer completes).  The row's stored logits are then loaded at
-  // once (they lie inside the row's ld entries whatever its visible length).
+  // The cleared counters come first: they touch shared memory only, so they
+  // overlap the scorer's tail (this kernel may start before the scorer
+  // completes).  Every global read -- the problem metadata too, which the
+  // previous kernel may have written -- waits for it.  The row's stored
+  // logits are then loaded at once (they lie inside the row's ld entries
+  // whatever its visible length).
   const int cap = static_cast<int>(min(p.ld, static_cast<int64_t>(kSmallMaxKeys)));
   const float4* row4 = reinterpret_cast<const float4*>(p.logits + static_cast<int64_t>(t) * p.ld);
+  for (int i = tid; i < kSmallCopies * kSmallRow; i += kSmallThreads) (&sm.hist[0][0])[i] = 0;
+  if (tid == 0) {
+    sm.bcast[3] = 0;
+    sm.win_count[0] = 0;
+  }
+  pdl_wait();  // the logits come from the kernel before this one
+  pdl_launch_dependents();  // the next kernel's on-chip setup may overlap this one
   int lo = 0, hi = p.num_seqs - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -433,13 +444,6 @@ __global__ void __launch_bounds__(kSmallThreads) topk_select_small_kernel(const 
   it.b = lo;
   it.k_len = max(__ldg(p.cu_seqlens_k + lo + 1) - __ldg(p.cu_seqlens_k + lo), 0);
   const int M = min(row_visible(p, it, t), cap);
-  for (int i = tid; i < kSmallCopies * kSmallRow; i += kSmallThreads) (&sm.hist[0][0])[i] = 0;
-  if (tid == 0) {
-    sm.bcast[3] = 0;
-    sm.win_count[0] = 0;
-  }
-  pdl_wait();  // the logits come from the kernel before this one
-  pdl_launch_dependents();  // the next kernel's on-chip setup may overlap this one
   float4 v[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) {

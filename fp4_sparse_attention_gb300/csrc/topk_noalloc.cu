@@ -67,6 +67,8 @@ extern "C" {
 fp4idx_status_t fp4idx_topk_noalloc(const fp4idx_problem_t* problem, const float* w, int64_t w_row_stride,
                                     int32_t k, uint32_t flags, int32_t* indices, float* values,
                                     int32_t* valid_count, void* stream) {
+  // A size of 0 means an invalid or unsupported problem or k: fp4idx_topk
+  // below then reports the same status it would give any caller.
   const size_t need = fp4idx_topk_workspace_bytes(problem, k);
   if (need > fp4idx::kScratchBytes) {
     fp4idx::set_last_error("top-k needs %zu bytes of scratch; the static scratch holds %zu (use fp4idx_topk)",

@@ -302,6 +302,32 @@ def prefill_32k() -> Problem:
                         visibility="causal", topk=2048)
 
 
+# E4M3 codes of the hand-built NaN case (bias 7): 0x28 = 0.25, 0x30 = 0.5,
+# 0x38 = 1, 0x40 = 2, 0x48 = 4; 0x7F is NaN.
+NAN_CASE_KEY_SCALES = (0x38, 0x40, 0x7F, 0x30, 0x40, 0x7F, 0x48, 0x28)
+
+
+def nan_scale_keys_case(num_heads: int = 8) -> Problem:
+    """Hand-built NVFP4 case with NaN scales.  1 request, 2 rows, 8 keys on
+    one 64-key page, every visible.  Every q and k value is E2M1 code 2 (1.0)
+    and every q scale E4M3 1.0, so the dot of key s is 128 * kscale(s) for
+    each head; key s carries the E4M3 scale NAN_CASE_KEY_SCALES[s] in all
+    eight groups (keys 2 and 5: NaN).  w = (1, 0, ..., 0).  Row 1 has NaN q
+    scales on head 0, so every one of its logits is NaN."""
+    p = make_problem(name="nan_scale_keys", seed=17, fmt=NVFP4, q_lens=[2], k_lens=[8], num_heads=num_heads,
+                     weights="sixteenths", visibility="full")
+    p.q[...] = 0x22
+    p.k[...] = 0x22
+    p.q_scale[...] = 0x38
+    p.k_scale[...] = 0x38
+    for s, code in enumerate(NAN_CASE_KEY_SCALES):
+        p.k_scale[int(p.block_table[0, 0]), 0, s, :] = code
+    p.q_scale[1, 0, :] = 0x7F
+    p.w[...] = 0.0
+    p.w[:, 0] = 1.0
+    return p
+
+
 WORKLOADS = {
     "tiny": tiny_mx_decode,
     "verify16k": verify_decode_16k,

@@ -201,6 +201,8 @@ fp4idx_status_t fp4idx_block_topk(const float* scores, int32_t num_heads, int32_
  * top-k per CTA and a merge selects each row's top-k, so full logits never
  * reach memory.
  * Supported: num_kv_heads == 1; num_heads in {8, 16, 32, 64}; 1 <= k <= 2048.
+ * fp4idx_topk_workspace_bytes returns 0 for an invalid problem or a k
+ * outside 1..2048 (fp4idx_topk then returns the matching status).
  */
 size_t fp4idx_topk_workspace_bytes(const fp4idx_problem_t* problem, int32_t k);
 fp4idx_status_t fp4idx_topk(const fp4idx_problem_t* problem, const float* w,

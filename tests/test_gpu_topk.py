@@ -181,3 +181,35 @@ def test_short_select_with_outlier_keys(sorted_):
     assert B.fp4idx_get_error() == 0
     rows = np.arange(p.num_rows)
     compare_topk(p, rows, k, idx.cpu().numpy(), val.cpu().numpy(), cnt.cpu().numpy(), sorted_order=sorted_)
+
+
+@pytest.mark.parametrize("streaming", [False, True])
+def test_nan_logits_are_never_selected(streaming):
+    # hand-built: keys 2 and 5 have NaN scales, row 1 NaN q scales everywhere
+    p = wl.nan_scale_keys_case()
+    o_idx, o_val, o_cnt = oracle.topk(p, 8)
+    idx, val, cnt = _run(p, 8, sorted_=True, streaming=streaming)
+    np.testing.assert_array_equal(cnt, o_cnt)
+    np.testing.assert_array_equal(idx, o_idx)
+    np.testing.assert_array_equal(val, o_val)
+    # random NaN group scales on ~3% of the keys of a ragged NVFP4 problem
+    p = wl.make_problem(name="nan_keys", seed=41, fmt=wl.NVFP4, q_lens=[4, 3], k_lens=[5000, 20000],
+                        num_heads=32, weights="normal", cache_pages=400)
+    rng = np.random.default_rng(42)
+    flat = p.k_scale.reshape(-1, p.k_scale.shape[-1])
+    flat[rng.random(flat.shape[0]) < 0.03, 5] = 0x7F
+    _check(p, 300, sorted_=True, streaming=streaming)
+
+
+def test_nan_logits_are_never_selected_fused_call():
+    p = wl.nan_scale_keys_case()
+    dp = B.DeviceProblem.from_host(p)
+    logits, idx, val, cnt = B.fp4idx_logits_topk(dp, torch.as_tensor(p.w).cuda(), 8, sorted=True)
+    torch.cuda.synchronize()
+    assert B.fp4idx_get_error() == 0
+    o_idx, o_val, o_cnt = oracle.topk(p, 8)
+    np.testing.assert_array_equal(cnt.cpu().numpy(), o_cnt)
+    np.testing.assert_array_equal(idx.cpu().numpy(), o_idx)
+    np.testing.assert_array_equal(val.cpu().numpy(), o_val)
+    lg = logits.cpu().numpy()[:, :8]
+    assert np.isnan(lg[0, [2, 5]]).all() and np.isnan(lg[1]).all()

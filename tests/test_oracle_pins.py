@@ -338,6 +338,46 @@ def test_nan_query_scale_leaves_invisible_positions_neg_inf():
     assert np.isneginf(out[1]).all()
 
 
+def test_topk_skips_nan_logits_hand_worked():
+    # Keys' dots are 128 * kscale: 128, 256, NaN, 64, 256, NaN, 512, 32 (w
+    # picks head 0).  A NaN logit has no rank: never selected, not counted;
+    # the rest keep (value desc, position asc) order.  Row 1's head-0 q scale
+    # is NaN, so all its logits are NaN and nothing is selected.
+    p = wl.nan_scale_keys_case()
+    full, _, _ = oracle.logits_rows(p, 8)
+    np.testing.assert_array_equal(full[0, [0, 1, 3, 4, 6, 7]], [128, 256, 64, 256, 512, 32])
+    assert np.isnan(full[0, [2, 5]]).all() and np.isnan(full[1]).all()
+    idx, val, cnt = oracle.topk(p, 8)
+    assert list(cnt) == [6, 0]
+    assert list(idx[0]) == [6, 1, 4, 0, 3, 7, -1, -1]
+    np.testing.assert_array_equal(val[0, :6], [512, 256, 256, 128, 64, 32])
+    assert np.isneginf(val[0, 6:]).all() and np.isneginf(val[1]).all()
+    assert np.all(idx[1] == -1)
+    idx, val, cnt = oracle.topk(p, 3)
+    assert list(cnt) == [3, 0] and list(idx[0]) == [6, 1, 4]
+
+
+def test_topk_with_random_nan_keys_is_sort_of_the_rest():
+    p = _small(fmt=wl.NVFP4, q_lens=[3, 2], k_lens=[300, 129])
+    rng = np.random.default_rng(5)
+    flat = p.k_scale.reshape(-1, p.k_scale.shape[-1])
+    flat[rng.random(flat.shape[0]) < 0.05, 1] = 0x7F  # some keys get one NaN group scale
+    full, _, _ = oracle.logits_rows(p, 300)
+    vis = oracle.visible_all(p)
+    k = 150
+    idx, val, cnt = oracle.topk(p, k)
+    nan_seen = 0
+    for t in range(p.num_rows):
+        row = full[t, : vis[t]]
+        ok = [s for s in range(vis[t]) if not np.isnan(row[s])]
+        nan_seen += vis[t] - len(ok)
+        order = sorted(ok, key=lambda s: (-(float(row[s]) + 0.0), s))[:k]
+        assert cnt[t] == len(order)
+        assert list(idx[t, : len(order)]) == order
+        assert np.all(idx[t, len(order):] == -1)
+    assert nan_seen > 0
+
+
 def test_block_topk_hand_worked_column():
     # one column: blocks 1 and 2 tie at 3 (lower block first), block 3 has no
     # visible key (-inf) and block 4 a NaN score: neither is a candidate

@@ -65,6 +65,47 @@ def test_noalloc_matches_workspace_topk_on_consecutive_calls(noalloc, maker, k):
     assert B.fp4idx_get_error() == 0
 
 
+def _reference(dp, w, k, streaming):
+    r = B.fp4idx_topk(dp, w, k, sorted=True, streaming=streaming)
+    torch.cuda.synchronize()
+    return [x.cpu().numpy() for x in r]
+
+
+def test_noalloc_streaming_plan_after_a_call_of_another_shape(noalloc):
+    # The streaming plan keeps per-CTA partial lists, their counts, candidate
+    # buffers and item starts in the scratch.  Calls of different shapes (and
+    # plans) in a row must not see each other's leftovers.
+    lib, f = noalloc
+    tiny = wl.tiny_mx_decode()
+    long_ = wl.make_problem(name="noalloc_long", seed=31, fmt=wl.MXFP4, q_lens=[4, 3], k_lens=[40000, 20000],
+                            num_heads=32, e8m0_range=(120, 134), weights="normal", cache_pages=1000)
+    verify = wl.verify_decode_16k()
+    cases = [(tiny, 64, 0), (long_, 2048, 0), (verify, 2048, B.FP4IDX_TOPK_STREAMING), (long_, 300, 0),
+             (tiny, 64, B.FP4IDX_TOPK_STREAMING), (long_, 2048, 0)]
+    for i, (p, k, extra) in enumerate(cases):
+        dp = B.DeviceProblem.from_host(p)
+        w = torch.as_tensor(p.w).cuda()
+        assert B.fp4idx_topk_workspace_bytes(dp, k) <= 64 << 20
+        ref = _reference(dp, w, k, streaming=bool(extra) or p.max_seqlen_k > 16384)
+        st, idx, val, cnt = _call(f, dp, w, k, B.FP4IDX_TOPK_SORTED | extra)
+        assert st == 0, lib.fp4idx_last_error_message()
+        for got, want, what in zip((idx, val, cnt), ref, ("indices", "values", "counts")):
+            np.testing.assert_array_equal(got, want, err_msg=f"call {i} ({p.name}, k={k}): {what}")
+    assert B.fp4idx_get_error() == 0
+
+
+def test_noalloc_reports_unsupported_k_like_topk(noalloc):
+    lib, f = noalloc
+    p = wl.tiny_mx_decode()
+    dp = B.DeviceProblem.from_host(p)
+    w = torch.as_tensor(p.w).cuda()
+    assert B.fp4idx_topk_workspace_bytes(dp, 2049) == 0
+    st, idx, _, _ = _call(f, dp, w, 2049, 0)
+    assert st == 2, lib.fp4idx_last_error_message()  # FP4IDX_EUNSUPPORTED, as fp4idx_topk gives
+    assert b"2048" in lib.fp4idx_last_error_message()
+    assert np.all(idx == -7)  # nothing ran
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch(noalloc):
     lib, f = noalloc
     p = wl.make_problem(name="many_rows", seed=3, fmt=wl.MXFP4, q_lens=[4096], k_lens=[256], num_heads=32,
