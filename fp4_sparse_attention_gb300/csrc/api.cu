@@ -236,9 +236,9 @@ TopkWorkspace topk_workspace(const fp4idx_problem_t* p, int32_t k, int sms) {
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   TopkWorkspace ws;
   ws.keys_off = 0;
-  ws.count_off = up(static_cast<size_t>(slots) * topk_capacity(k) * 8);
+  ws.count_off = up(static_cast<size_t>(slots) * topk_part_capacity(k) * 8);
   ws.cand_off = ws.count_off + up(static_cast<size_t>(slots) * 4);
-  ws.start_off = ws.cand_off + up(static_cast<size_t>(ctas) * R * topk_capacity(k) * 8);
+  ws.start_off = ws.cand_off + up(static_cast<size_t>(ctas) * R * topk_cand_capacity(k) * 8);
   ws.bytes = ws.start_off + up(static_cast<size_t>(items + 1) * 4);
   // the short-context plan keeps the logits [T][ld] at offset 0 instead
   if (use_logits_plan(p)) {
@@ -344,6 +344,7 @@ fp4idx_status_t topk_prepare(const fp4idx_problem_t* problem, const float* w, in
   sp->part_count = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + ws.count_off);
   sp->cand = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(workspace) + ws.cand_off);
   sp->item_start = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + ws.start_off);
+  sp->item_overhead = kTopkItemOverhead;
   *ctas = topk_ctas(problem, dev->sms);
   if (*ctas >= kMaxMergeSlots) return fail(FP4IDX_EUNSUPPORTED, "more than %d SMs", kMaxMergeSlots - 1);
   sp->score_ctas = *ctas;

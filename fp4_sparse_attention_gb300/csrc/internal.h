@@ -49,12 +49,17 @@ struct ScoreParams {
   int64_t ld;
   // top-k partials: slot s (s < score_ctas: first segment of CTA s; else
   // score_ctas + item: an item that starts inside a CTA's chunk) x R rows,
-  // up to topk_capacity(k) keys each (a superset of that slot's top-k).
+  // up to topk_part_capacity(k) keys each (a superset of that slot's top-k).
   int32_t k;
-  uint64_t* part_keys;      // [slots * R][topk_capacity(k)]
+  uint64_t* part_keys;      // [slots * R][topk_part_capacity(k)]
   int32_t* part_count;      // [slots * R]
   uint64_t* cand;           // [score_ctas * R][candidate capacity] streaming candidate buffers
-  int32_t* item_start;      // [items + 1] first global tile of each item, total last (top-k only)
+  int32_t* item_start;      // [items + 1] first unit of each item, total last (top-k only)
+  // Work units of an item with tiles: its tiles plus this many units that
+  // stand for the per-item cost (Q load, weights, flush), so that the equal
+  // split of the concatenated units balances CTAs with many short items
+  // against CTAs with a few long ones (0: tiles only).
+  int32_t item_overhead;
   uint32_t* err;
 };
 
@@ -158,11 +163,23 @@ cudaError_t launch_block_topk(const float* scores, int32_t H, int32_t Kt, int32_
 // Sets the message fp4idx_last_error_message() returns on this thread.
 void set_last_error(const char* fmt, ...);
 
-// Keys a streaming top-k candidate buffer holds per row: at least twice k
-// (rounded to whole tiles), at least 1,024.
+// Twice k rounded to whole tiles, at least 1,024.
 __host__ __device__ constexpr int topk_capacity(int k) {
   return 2 * ((k + 127) / 128) * 128 < 1024 ? 1024 : 2 * ((k + 127) / 128) * 128;
 }
+// Keys a scorer CTA's streaming candidate buffer holds per row when it lives
+// in the workspace: four times k (rounded), so a buffer is compacted only
+// after about three times k insertions.
+__host__ __device__ constexpr int topk_cand_capacity(int k) { return 2 * topk_capacity(k); }
+// Keys of one partial list: a scorer CTA writes a row's whole candidate
+// buffer there (no selection in the scorer), so a list holds as many keys
+// as the largest candidate buffer (shared memory 8,192, or the workspace
+// buffer).
+__host__ __device__ constexpr int topk_part_capacity(int k) {
+  return topk_cand_capacity(k) > 8192 ? topk_cand_capacity(k) : 8192;
+}
+// Work units standing for one item's fixed cost in the top-k scorer's split.
+constexpr int kTopkItemOverhead = 2;
 
 // Query rows per scorer CTA for a head count (the MMA N is rows * heads).
 inline int score_rows_per_cta(int heads) { return heads >= 64 ? 2 : 4; }

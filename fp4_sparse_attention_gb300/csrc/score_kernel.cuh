@@ -51,6 +51,38 @@
 namespace fp4idx {
 
 constexpr int kEpiThreads = 128;  // one epilogue group: four warps, one per TMEM lane quadrant
+
+// Time attribution for profiling builds (-DFP4IDX_STAMPS only; product
+// builds compile none of it): every warp of a role attributes the clock64
+// cycles since its previous stamp to one category of its role; the sums are
+// added to fp4idx_stamps[role][category] at the end of the kernel (category
+// 7 counts tiles).  Roles: 0 producers, 1 MMA thread, 2 scale warp,
+// 3 epilogue warps.
+#ifdef FP4IDX_STAMPS
+constexpr int kStampCats = 8;
+static __device__ unsigned long long fp4idx_stamps[4 * kStampCats];
+#define FP4IDX_STAMP_INIT() \
+  unsigned long long stamp_acc_[kStampCats] = {}; \
+  long long stamp_t_ = clock64()
+#define FP4IDX_STAMP(c)                 \
+  do {                                  \
+    const long long n_ = clock64();     \
+    stamp_acc_[c] += n_ - stamp_t_;     \
+    stamp_t_ = n_;                      \
+  } while (0)
+#define FP4IDX_STAMP_COUNT() (stamp_acc_[7] += 1)
+#define FP4IDX_STAMP_DONE(role)                                                      \
+  do {                                                                               \
+    if ((threadIdx.x & 31) == 0)                                                     \
+      for (int c_ = 0; c_ < kStampCats; ++c_)                                        \
+        atomicAdd(&fp4idx_stamps[(role) * kStampCats + c_], stamp_acc_[c_]);         \
+  } while (0)
+#else
+#define FP4IDX_STAMP_INIT() do { } while (0)
+#define FP4IDX_STAMP(c) do { } while (0)
+#define FP4IDX_STAMP_COUNT() do { } while (0)
+#define FP4IDX_STAMP_DONE(role) do { } while (0)
+#endif
 constexpr uint32_t kTmemCols = 512;
 constexpr int kAccBufs = 3;  // accumulator buffers: the MMA may run two tiles ahead of the epilogue
 
@@ -60,18 +92,14 @@ struct CtaState {
   int32_t abort;
   int32_t item0;        // item holding the first tile of this CTA's chunk
   int32_t item0_start;  // global tile index where item0 starts
-  int32_t total_tiles;  // over all items
+  int32_t total_tiles;  // work units over all items (tiles, plus per-item units in top-k mode)
   int32_t chunk;        // tiles per CTA
   int32_t pad[2];
 };
 
 template <int R>
-struct RowState {  // epilogue view of the current item's rows
-  int32_t vis[R];
-  int32_t valid[R];
-  int32_t cnt[R];
-  int32_t pad[R];
-  uint64_t thr[R];  // inclusive acceptance threshold of each candidate buffer
+struct RowState {  // top-k: candidates each epilogue warp appended to its region of each row
+  int32_t wc[2][R][4];  // double buffered: publication p writes wc[p & 1]
 };
 
 
@@ -81,18 +109,19 @@ struct ScoreLayout {
   static constexpr int kAtoms = FmtTraits<FMT>::kAtoms;
   // Top-k with two rows per CTA (64 heads): each row's candidate buffer
   // lives in shared memory (a compaction then reads and writes it at
-  // shared-memory latency), kCandCap keys per row.  With four rows the
-  // buffers would leave too shallow a K ring (measured: long decode 286 ->
-  // 400 us with 3,072-key buffers and 8 stages), so they stay in the
-  // workspace (L2) there.
+  // shared-memory latency), kCandCap keys per row -- large, so that a row
+  // rarely needs a compaction at all (about 3k insertions before the first).
+  // With four rows the buffers would leave too shallow a K ring (measured:
+  // long decode 286 -> 400 us with 3,072-key buffers and 8 stages), so they
+  // stay in the workspace (L2) there.
   static constexpr bool kSmemCand = MODE == kModeTopk && R < 4;
-  static constexpr int kCandCap = kSmemCand ? 4096 : 0;
+  static constexpr int kCandCap = kSmemCand ? (FMT == 0 ? 8192 : 6144) : 0;
   static constexpr uint32_t kCandBytes = static_cast<uint32_t>(R) * kCandCap * 8;
   // Everything but the K ring, and the ring: as deep as shared memory allows
   // (a loaded HBM round trip for a random page is ~2 us, so ~70+ KB in
   // flight per SM), at most 20 stages.
   static constexpr uint32_t kFixedBytes = 2 * (((H * R * 64 + 1023) / 1024) * 1024) + 4 * kAtoms * 2048 +
-                                          2 * kAtoms * 512 + 4096 + (128 + kEpiThreads * 4) * 4 + 4 * 1280 +
+                                          2 * kAtoms * 512 + 4096 + (160 + kEpiThreads * 4) * 4 + 4 * 1280 +
                                           (MODE == kModeTopk ? R * kHistBins * 2 : 0) + kCandBytes + 2048;
   static constexpr int kStagesFit = static_cast<int>((232448u - 1024u - kFixedBytes) / (8192u + 128u * G)) & ~1;
   static constexpr int kStages = kStagesFit < 20 ? kStagesFit : 20;
@@ -106,11 +135,20 @@ struct ScoreLayout {
       MODE == kModeTopk ? 1 : (R < 64 / H ? R : (64 / H < 1 ? 1 : 64 / H));
   static_assert(R % kRowsPerGroup == 0, "rows split evenly over the groups");
   static constexpr int kGroups = R / kRowsPerGroup;
-  // warp 0 and the last warp: producers (alternate tiles); warp 1: MMA;
-  // warp 2: scales; warps 3 .. 3 + 4R - 1: epilogue
+  // warp 0 and kProducer2Warp: producers (alternate tiles); warp 1: MMA;
+  // warp 2 (and kScale2Warp, when there are two): scales (alternate
+  // tiles); warps 3 .. 3 + 4 * kGroups - 1: epilogue.  Registers are
+  // reserved for whole groups of four warps, so the CTA is rounded up to a
+  // multiple of four warps (the extra ones idle); a second scale warp is
+  // used where that leaves the epilogue enough registers.
   static constexpr int kEpiWarp0 = 3;
   static constexpr int kProducer2Warp = kEpiWarp0 + 4 * kGroups;
-  static constexpr int kThreads = 128 + kEpiThreads * kGroups;
+  static constexpr int kScaleWarps = (kProducer2Warp + 1) % 4 == 0 ? 1 : 2;
+  static constexpr int kScale2Warp = kProducer2Warp + 1;
+  static constexpr int kWarpsUsed = kProducer2Warp + kScaleWarps;
+  static constexpr int kThreads = ((kWarpsUsed + 3) / 4) * 4 * 32;
+  // registers per thread with one CTA of kThreads on an SM (a multiple of 8)
+  static constexpr int kMaxRegs = (65536 / kThreads) / 8 * 8 > 255 ? 255 : (65536 / kThreads) / 8 * 8;
   static_assert(kStages % 2 == 0, "the two producers own alternate stages");
   static constexpr int N = H * R;
   static_assert(N % 16 == 0 && N >= 16 && N <= 128, "MMA N");
@@ -123,7 +161,7 @@ struct ScoreLayout {
   static constexpr uint32_t kSfaRows = kKraw + kStages * 128 * G;        // kSfaSlots x kAtoms x 2048 (128 rows)
   static constexpr uint32_t kSfb = kSfaRows + kSfaSlots * kAtoms * 2048; // 2 x kAtoms x 512 Q-scale atoms
   static constexpr uint32_t kBars = kSfb + 2 * kAtoms * 512;             // mbarriers
-  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 4 + kSfaSlots;
+  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 4 + kSfaSlots + 2;
   static constexpr uint32_t kState = kBars + kNumBars * 8;
   static constexpr uint32_t kRows = (kState + sizeof(CtaState) + 15) / 16 * 16;
   static constexpr uint32_t kScan = (kRows + sizeof(RowState<R>) + 15) / 16 * 16;  // kThreads ints
@@ -200,6 +238,14 @@ __device__ __forceinline__ int32_t item_tiles(const ScoreParams& p, const ItemIn
   return (it.maxvis + kTileKeys - 1) / kTileKeys;
 }
 
+// Units an item occupies in the concatenated work space: its tiles plus,
+// when it has any, p.item_overhead units without a tile (its fixed cost).
+template <int MODE>
+__device__ __forceinline__ int32_t item_units(const ScoreParams& p, const ItemInfo& it) {
+  const int32_t t = item_tiles<MODE>(p, it);
+  return t > 0 ? t + p.item_overhead : 0;
+}
+
 // Whether tile j of the item holds a key some row of it can see; logits
 // tiles past that are written as -inf without loading or computing.
 __device__ __forceinline__ bool tile_has_visible(const ItemInfo& it, int j) {
@@ -207,9 +253,9 @@ __device__ __forceinline__ bool tile_has_visible(const ItemInfo& it, int j) {
 }
 
 // Cooperative over kNT threads (tid in [0, kNT), all of the CTA): the total
-// of the item tiles, this CTA's equal chunk of them and the item holding the
-// chunk's first tile with that item's start (item0 = -1 when the CTA has no
-// tiles).  `ws` holds kNT / 32 words.  With `starts` != nullptr the start of
+// of the item units, this CTA's equal chunk of them and the item holding the
+// chunk's first unit with that item's start (item0 = -1 when the CTA has no
+// units).  `ws` holds kNT / 32 words.  With `starts` != nullptr the start of
 // every item (and the total, at index items) is also written there, for the
 // merge.
 template <int MODE, int kNT>
@@ -220,7 +266,7 @@ __device__ void plan_items(const ScoreParams& p, int rows_per_cta, int tid, uint
   const int i0 = tid * per;
   const int i1 = min(items, i0 + per);
   int32_t s = 0;
-  for (int i = i0; i < i1; ++i) s += item_tiles<MODE>(p, item_info(p, i, rows_per_cta));
+  for (int i = i0; i < i1; ++i) s += item_units<MODE>(p, item_info(p, i, rows_per_cta));
   if (tid == 0) st->item0 = -1;  // ordered before the writes below by the scan's barriers
   uint32_t total_u;
   const int32_t pre = static_cast<int32_t>(cta_excl_prefix<kNT>(static_cast<uint32_t>(s), ws, &total_u));
@@ -236,13 +282,13 @@ __device__ void plan_items(const ScoreParams& p, int rows_per_cta, int tid, uint
     int32_t acc = pre;
     for (int i = i0; i < i1; ++i) {
       starts[i] = acc;
-      acc += item_tiles<MODE>(p, item_info(p, i, rows_per_cta));
+      acc += item_units<MODE>(p, item_info(p, i, rows_per_cta));
     }
   }
   if (x < total && pre <= x && x < pre + s) {
     int32_t acc = pre;
     for (int i = i0; i < i1; ++i) {
-      const int32_t ti = item_tiles<MODE>(p, item_info(p, i, rows_per_cta));
+      const int32_t ti = item_units<MODE>(p, item_info(p, i, rows_per_cta));
       if (x < acc + ti) {
         st->item0 = i;
         st->item0_start = acc;
@@ -255,28 +301,26 @@ __device__ void plan_items(const ScoreParams& p, int rows_per_cta, int tid, uint
 }
 
 // Visit the (item, tile range) segments of this CTA's chunk in order:
-// f(item, info, lo, hi, seg) with tiles [lo, hi) of the item, seg = index of
-// the segment within the chunk.
+// f(item, info, lo, hi, own) with tiles [lo, hi) of the item; own is true
+// when the chunk starts at or after the item's first unit (the item is the
+// chunk's first), false when the item starts inside the chunk.  The merge
+// finds a CTA's partial list of an item by the same rule.
 template <int MODE, int R, class F>
 __device__ __forceinline__ void for_each_segment(const ScoreParams& p, const CtaState* st, F&& f) {
   const int items = p.num_seqs * p.row_groups;
-  int64_t x = static_cast<int64_t>(blockIdx.x) * st->chunk;
+  const int64_t x = static_cast<int64_t>(blockIdx.x) * st->chunk;
   const int64_t end = min(static_cast<int64_t>(st->total_tiles), x + st->chunk);
   if (x >= end || st->item0 < 0) return;
   int32_t i = st->item0;
   int64_t start = st->item0_start;
-  int seg = 0;
-  while (x < end && i < items) {
+  while (start < end && i < items) {
     const ItemInfo it = item_info(p, i, R);
-    const int32_t ti = item_tiles<MODE>(p, it);
-    const int64_t lo = x - start;
-    const int64_t hi = min(end, start + ti) - start;
-    if (hi > lo) {
-      f(i, it, static_cast<int>(lo), static_cast<int>(hi), seg);
-      ++seg;
-      x = start + hi;
-    }
-    start += ti;
+    const int32_t units = item_units<MODE>(p, it);
+    const int64_t tiles = units > 0 ? units - p.item_overhead : 0;
+    const int64_t lo = max(x - start, int64_t(0));
+    const int64_t hi = min(end - start, tiles);
+    if (hi > lo) f(i, it, static_cast<int>(lo), static_cast<int>(hi), x >= start);
+    start += units;
     ++i;
   }
 }
@@ -316,22 +360,24 @@ __device__ __forceinline__ void q_scale_atoms(const ScoreParams& p, const ItemIn
     *reinterpret_cast<uint4*>(atoms + 512 + lane * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
 }
 
-// sum_h w[h] * max(v[h], 0): the ReLU as a NaN-propagating max per value,
-// then packed fp32x2 FMAs with w2[i] = (w[2i], w[2i+1]) in four independent
-// chains.
-template <int H>
-__device__ __forceinline__ float weighted_relu_reg(const uint32_t (&v)[H], const float2 (&w2)[H / 2]) {
-  constexpr int kChains = H >= 16 ? 4 : 2;
-  float2 acc[kChains];
+// acc[(i0 + i) % 4] += w2[i0 + i] * (max(v[2i], 0), max(v[2i+1], 0)) for the
+// C columns of one TMEM load (head pairs i0 .. i0 + C/2 - 1): the ReLU as a
+// NaN-propagating max per value, then packed fp32x2 FMAs in four chains
+// fixed by the head pair, so a row's sum does not depend on how its
+// columns were loaded.  wrelu_total adds the chains.
+template <int C, int HP>
+__device__ __forceinline__ void wrelu_chunk(const uint32_t (&v)[C], const float2 (&w2)[HP], int i0,
+                                            float2 (&acc)[4]) {
 #pragma unroll
-  for (int c = 0; c < kChains; ++c) acc[c] = make_float2(0.0f, 0.0f);
-#pragma unroll
-  for (int i = 0; i < H / 2; ++i) {
+  for (int i = 0; i < C / 2; ++i) {
     const float2 x = make_float2(relu_nan(__uint_as_float(v[2 * i])), relu_nan(__uint_as_float(v[2 * i + 1])));
-    acc[i % kChains] = __ffma2_rn(w2[i], x, acc[i % kChains]);
+    acc[(i0 + i) % 4] = __ffma2_rn(w2[i0 + i], x, acc[(i0 + i) % 4]);
   }
-#pragma unroll
-  for (int c = 1; c < kChains; ++c) acc[0] = __fadd2_rn(acc[0], acc[c]);
+}
+__device__ __forceinline__ float wrelu_total(float2 (&acc)[4]) {
+  acc[0] = __fadd2_rn(acc[0], acc[1]);
+  acc[2] = __fadd2_rn(acc[2], acc[3]);
+  acc[0] = __fadd2_rn(acc[0], acc[2]);
   return acc[0].x + acc[0].y;
 }
 
@@ -350,13 +396,13 @@ __device__ int compact_keep_ge(const G& g, uint64_t* cand, int n, uint64_t T, Se
   if (g.tid == 0) sc->bcast[3] = 0;
   g.sync();
   constexpr int kPer = 8;
-  constexpr int kChunk = kEpiThreads * kPer;
+  constexpr int kChunk = G::kSize * kPer;
   for (int base = 0; base < n; base += kChunk) {
     uint64_t v[kPer];
     bool keep[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-      const int idx = base + j * kEpiThreads + g.tid;
+      const int idx = base + j * G::kSize + g.tid;
       keep[j] = false;
       v[j] = 0;
       if (idx < n) {
@@ -393,17 +439,17 @@ __device__ uint32_t copy_keep_ge(const G& g, const uint64_t* cand, int n, uint64
   if (g.tid == 0) sc->bcast[3] = 0;
   g.sync();
   constexpr int kPer = 8;
-  constexpr int kChunk = kEpiThreads * kPer;
+  constexpr int kChunk = G::kSize * kPer;
   for (int base = 0; base < n; base += kChunk) {
     uint64_t v[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-      const int idx = base + j * kEpiThreads + g.tid;
+      const int idx = base + j * G::kSize + g.tid;
       v[j] = idx < n ? cand[idx] : 0;
     }
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
-      const bool keep = base + j * kEpiThreads + g.tid < n && v[j] >= T;
+      const bool keep = base + j * G::kSize + g.tid < n && v[j] >= T;
       const uint32_t m = __ballot_sync(0xffffffffu, keep);
       if (m) {
         const int leader = __ffs(m) - 1;
@@ -425,7 +471,7 @@ __device__ uint32_t copy_keep_ge(const G& g, const uint64_t* cand, int n, uint64
 // The kernel.
 // ---------------------------------------------------------------------------
 template <int H, int R, int FMT, int MODE>
-__global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) score_kernel(const __grid_constant__ ScoreParams p) {
+__global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kernel(const __grid_constant__ ScoreParams p) {
   using L = ScoreLayout<H, R, FMT, MODE>;
   constexpr int kThreads = L::kThreads;
   using F = FmtTraits<FMT>;
@@ -447,6 +493,7 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
   auto qfull_bar = [&](uint32_t qb) { return bar0 + 8u * (2 * kStages + 2 * kAccBufs + qb); };
   auto qempty_bar = [&](uint32_t qb) { return bar0 + 8u * (2 * kStages + 2 * kAccBufs + 2 + qb); };
   auto sfready_bar = [&](int slot) { return bar0 + 8u * (2 * kStages + 2 * kAccBufs + 4 + slot); };
+  auto qsready_bar = [&](uint32_t qb) { return bar0 + 8u * (2 * kStages + 2 * kAccBufs + 4 + L::kSfaSlots + qb); };
 
   CtaState* st = reinterpret_cast<CtaState*>(smem + L::kState);
   RowState<R>* rs = reinterpret_cast<RowState<R>*>(smem + L::kRows);
@@ -454,6 +501,7 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
   SelectScratch* sc = reinterpret_cast<SelectScratch*>(smem + L::kScratch);
   uint32_t* hist_words = reinterpret_cast<uint32_t*>(smem + L::kHist);
   const int cap = topk_capacity(p.k);
+  const int pcap = topk_part_capacity(p.k);  // keys of one partial list
   volatile int* abort_flag = &st->abort;
 
   // ---- one-time setup: on-chip only, so it may overlap the previous kernel
@@ -469,7 +517,7 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
     }
     for (int a = 0; a < kAccBufs; ++a) {
       mbar_init(accf_bar(a), 1);
-      mbar_init(acce_bar(a), L::kGroups * kEpiThreads);
+      mbar_init(acce_bar(a), L::kGroups * 4);  // one arrive per epilogue warp
     }
     for (uint32_t qb = 0; qb < 2; ++qb) {
       mbar_init(qfull_bar(qb), 1);
@@ -479,6 +527,7 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
       mbar_init(qempty_bar(qb), 2);
     }
     for (int sl = 0; sl < L::kSfaSlots; ++sl) mbar_init(sfready_bar(sl), 1);
+    for (uint32_t qb = 0; qb < 2; ++qb) mbar_init(qsready_bar(qb), 1);  // the item's Q scales are in TMEM
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc<kTmemCols>(smem_u32(&st->tmem_base));
@@ -533,11 +582,14 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
     const int page = p.page_size;
     const int pshift = p.page_shift;
     const int slots = kTileKeys >> pshift;  // 2 for 64-key pages, 1 for 128
+    FP4IDX_STAMP_INIT();
     for_each_segment<MODE, R>(p, st, [&](int, const ItemInfo& it, int lo, int hi, int) {
       if (!ok) return;
       if (pidx == 0) {
         const uint32_t qb = item_iter & 1u, qph = (item_iter >> 1) & 1u;
+        FP4IDX_STAMP(3);
         ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(qempty_bar(qb), qph ^ 1u, abort_flag, p.err) : false, 0);
+        FP4IDX_STAMP(0);
         if (!ok) return;
         if (lane == 0) {
           mbar_arrive_expect_tx(qfull_bar(qb), N * kCodeBytes);
@@ -578,7 +630,9 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
         const uint32_t bytes = static_cast<uint32_t>((ok0 ? 1 : 0) + (ok1 ? 1 : 0)) * page * (kCodeBytes + G);
         const int s = tile_iter % kStages;
         const uint32_t ph = (tile_iter / kStages) & 1u;
+        FP4IDX_STAMP(3);
         ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.err) : false, 0);
+        FP4IDX_STAMP(1);
         if (!ok) return;
         if (lane == 0) mbar_arrive_expect_tx(full_bar(s), bytes);
         __syncwarp();
@@ -589,9 +643,13 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
           bulk_load(kraw_s + s * (128 * G) + ((lane * G) << pshift), p.k_scale + static_cast<int64_t>(row) * G,
                     static_cast<uint32_t>(page * G), full_bar(s));
         }
+        FP4IDX_STAMP(2);
+        FP4IDX_STAMP_COUNT();
         ++tile_iter;
       }
     });
+    FP4IDX_STAMP(3);
+    FP4IDX_STAMP_DONE(0);
     if (!ok && lane == 0) {
       // Let copies already in flight land before the CTA can exit.
       volatile int never = 0;
@@ -618,9 +676,13 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
       bool ok = true;
       int last_acc = -1;
       uint32_t last_acc_phase = 0;
+      FP4IDX_STAMP_INIT();
       for_each_segment<MODE, R>(p, st, [&](int, const ItemInfo& it, int lo, int hi, int) {
         if (!ok) return;
         const uint32_t qb = item_iter & 1u;
+        // the first scale warp copied (or, with no tile to compute, skipped)
+        // this item's Q scales
+        if (!(ok = mbar_wait(qsready_bar(qb), (item_iter >> 1) & 1u, abort_flag, p.err))) return;
         const uint32_t sfb_t = tmem + L::kSfbCol + qb * 8u;
         const uint64_t bdesc = b_desc0 + static_cast<uint64_t>((qb * L::kQBytes) >> 4);
         for (int j = lo; j < hi && ok; ++j) {
@@ -629,11 +691,14 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
           const int slot = tile_iter % L::kSfaSlots;
           const int a = tile_iter % kAccBufs;
           const uint32_t aph = (tile_iter / kAccBufs) & 1u;
-          // the scale warp copied this tile's K scales (and, for an item's
-          // first tile, the item's Q scales) after the stage's codes landed
+          // a scale warp copied this tile's K scales after the stage's codes
+          // landed
+          FP4IDX_STAMP(3);
           if (!(ok = mbar_wait(sfready_bar(slot), (sf_phase >> slot) & 1u, abort_flag, p.err))) break;
+          FP4IDX_STAMP(0);
           sf_phase ^= 1u << slot;
           if (!(ok = mbar_wait(acce_bar(a), aph ^ 1u, abort_flag, p.err))) break;
+          FP4IDX_STAMP(1);
           tc_fence_after();
           const uint32_t sfa_t = tmem + L::kSfaCol + slot * 8u;
           const uint32_t d = tmem + L::kAccCol + a * 128u;
@@ -648,6 +713,8 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
           }
           tc_commit(empty_bar(s));
           tc_commit(accf_bar(a));
+          FP4IDX_STAMP(2);
+          FP4IDX_STAMP_COUNT();
           last_acc = a;
           last_acc_phase = aph;
           ++tile_iter;
@@ -657,6 +724,8 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
         tc_commit(qempty_bar(qb));
         ++item_iter;
       });
+      FP4IDX_STAMP(3);
+      FP4IDX_STAMP_DONE(1);
       if (!ok && last_acc >= 0) {
         // Outstanding MMAs must finish before TMEM is released.
         volatile int never = 0;
@@ -664,53 +733,72 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
       }
     }
     __syncwarp();
-  } else if (warp == 2) {
+  } else if (warp == 2 || (L::kScaleWarps == 2 && warp == L::kScale2Warp)) {
     // ================================================================ scales
-    // Per item: the Q scales of its rows -> 32x4x4 atoms -> TMEM slot
-    // item % 2 (free: the producer loaded this item's Q only after the MMAs
-    // of item - 2 completed).  Per tile: raw K scales [128 keys][G] -> 128
+    // Two warps, alternate tiles (warp 2 the even ones).  Per item (warp 2
+    // only): the Q scales of its rows -> 32x4x4 atoms -> TMEM slot item % 2
+    // (free: the producer loaded this item's Q only after the MMAs of
+    // item - 2 completed), committed to the item's Q-scale barrier.  Per
+    // tile: raw K scales [128 keys][G] -> 128
     // rows of the scale layout (row r holds atom line r % 32: the words of
     // keys l, 32+l, 64+l, 96+l, l = r % 32; NVFP4's second K half in the
     // second 16 bytes), one tcgen05.cp 128x128b/256b into TMEM slot
     // tile % kSfaSlots, committed to that slot's barrier.  A slot (TMEM and
     // shared staging) is rewritten only after the MMA of the tile that last
     // used it completed (its stage's empty barrier).
+    const uint32_t sidx = warp == 2 ? 0u : 1u;
+    const uint32_t smask = L::kScaleWarps == 2 ? 1u : 0u;  // tiles of this warp: (tile & smask) == sidx
     const uint64_t sfa_desc0 = desc_sf_rows(smem_u32(sfa_rows));
     uint32_t tile_iter = 0, item_iter = 0;
     bool ok = true;
+    FP4IDX_STAMP_INIT();
     for_each_segment<MODE, R>(p, st, [&](int, const ItemInfo& it, int lo, int hi, int) {
       if (!ok) return;
+      FP4IDX_STAMP(4);
       const uint32_t qb = item_iter & 1u, qph = (item_iter >> 1) & 1u;
-      ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(qfull_bar(qb), qph, abort_flag, p.err) : false, 0);
-      if (!ok) return;
-      // Q scales only when some tile of the segment is computed (otherwise no
-      // MMA reads them, and no barrier would track the copy)
-      if (MODE != kModeLogits || tile_has_visible(it, lo)) {
-        q_scale_atoms<H, R, FMT>(p, it, sfb_atoms + qb * (F::kAtoms * 512), lane);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tc_fence_after();
-          const uint32_t sfb_t = tmem + L::kSfbCol + qb * 8u;
+      if (sidx == 0) {
+        ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(qfull_bar(qb), qph, abort_flag, p.err) : false, 0);
+        if (!ok) return;
+        // Q scales only when some tile of the segment is computed (otherwise
+        // no MMA reads them); the barrier is committed either way
+        if (MODE != kModeLogits || tile_has_visible(it, lo)) {
+          q_scale_atoms<H, R, FMT>(p, it, sfb_atoms + qb * (F::kAtoms * 512), lane);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t sfb_t = tmem + L::kSfbCol + qb * 8u;
 #pragma unroll
-          for (int at = 0; at < F::kAtoms; ++at)
-            tc_cp_32x128b_warpx4(sfb_t + 4u * at, desc_sf_atom(smem_u32(sfb_atoms + (qb * F::kAtoms + at) * 512)));
+            for (int at = 0; at < F::kAtoms; ++at)
+              tc_cp_32x128b_warpx4(sfb_t + 4u * at, desc_sf_atom(smem_u32(sfb_atoms + (qb * F::kAtoms + at) * 512)));
+          }
         }
+        if (lane == 0) {
+          tc_commit(qsready_bar(qb));
+          mbar_arrive(qempty_bar(qb));
+        }
+        __syncwarp();
       }
-      if (lane == 0) mbar_arrive(qempty_bar(qb));
-      __syncwarp();
+      FP4IDX_STAMP(0);
       for (int j = lo; j < hi; ++j) {
         if (MODE == kModeLogits && !tile_has_visible(it, j)) continue;
+        if ((tile_iter & smask) != sidx) {  // the other scale warp's tile
+          ++tile_iter;
+          continue;
+        }
         const int s = tile_iter % kStages;
         const uint32_t ph = (tile_iter / kStages) & 1u;
         const int slot = tile_iter % L::kSfaSlots;
         bool got = false;
+        FP4IDX_STAMP(4);
         if (lane == 0) {
           got = mbar_wait(full_bar(s), ph, abort_flag, p.err);
+          FP4IDX_STAMP(1);
           if (got && tile_iter >= static_cast<uint32_t>(L::kSfaSlots)) {
             const uint32_t u = tile_iter - L::kSfaSlots;  // previous user of the slot
             got = mbar_wait(empty_bar(u % kStages), (u / kStages) & 1u, abort_flag, p.err);
           }
+          FP4IDX_STAMP(2);
         }
         ok = __shfl_sync(0xffffffffu, got, 0);
         if (!ok) break;
@@ -744,18 +832,28 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
           tc_commit(sfready_bar(slot));
         }
         __syncwarp();
+        FP4IDX_STAMP(3);
+        FP4IDX_STAMP_COUNT();
         ++tile_iter;
       }
       ++item_iter;
     });
+    FP4IDX_STAMP(4);
+    FP4IDX_STAMP_DONE(2);
     if (lane == 0) {
       // copies still in flight must land before TMEM is released
       volatile int never = 0;
       const uint32_t first = tile_iter > static_cast<uint32_t>(L::kSfaSlots) ? tile_iter - L::kSfaSlots : 0;
       for (uint32_t u = first; u < tile_iter; ++u)
-        mbar_wait(sfready_bar(u % L::kSfaSlots), (u / L::kSfaSlots) & 1u, &never, p.err);
+        if ((u & smask) == sidx) mbar_wait(sfready_bar(u % L::kSfaSlots), (u / L::kSfaSlots) & 1u, &never, p.err);
+      if (sidx == 0 && item_iter > 0) {
+        const uint32_t u = item_iter - 1;
+        mbar_wait(qsready_bar(u & 1u), (u >> 1) & 1u, &never, p.err);
+      }
     }
     __syncwarp();
+  } else if (warp >= L::kWarpsUsed) {
+    // spare warp (the CTA is a whole number of four-warp groups)
   } else {
     // ================================================================ epilogue
     constexpr int RG = L::kRowsPerGroup;  // query rows of this group
@@ -765,30 +863,123 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
     SelectScratch* gsc = sc + gi;
     const int quad = warp & 3;
     const int key_local = quad * 32 + lane;
-    // Candidate buffer capacity (shared memory) of each row.  Compaction is
-    // checked every `check_every` tiles; the buffer keeps that many tiles of
-    // room above the trigger so appends never overflow it.
-    const int ccap = L::kSmemCand ? min(cap, L::kCandCap) : cap;
-    const int check_every = max(1, min(4, (ccap - p.k) / (2 * kTileKeys)));
-    const int margin = check_every * kTileKeys;
+    // Candidate buffer of each row (shared memory for two-row CTAs, else the
+    // workspace), ccap keys laid out as
+    //   [0, seg0)                       keys kept by the last compaction
+    //   [seg0 + q * rsz, + wc[q])       keys warp q of the group appended since
+    // with rsz = (ccap - seg0) / 4, so an append needs no atomic: each warp
+    // owns its region and keeps its count in a register.  The counts are
+    // published and checked every `check_every` tiles; a region then keeps
+    // that many tiles of room (32 keys per tile and warp) above the trigger.
+    const int ccap = L::kSmemCand ? L::kCandCap : topk_cand_capacity(p.k);
+    const int check_every = ccap >= 4096 ? 8 : 4;  // a region is at least ccap / 8 keys
+    const int margin = check_every * 32;
+    const uint32_t kk = static_cast<uint32_t>(p.k);
     int since_check = 0;
     uint32_t tile_iter = 0;
     bool ok = true;
-    auto hist_of = [&](int rr) { return Hist16{hist_words + (r0 + rr) * (kHistBins / 2)}; };
-    // each row's candidate buffer: shared memory, or the workspace (L2-resident)
     auto cand_of = [&](int rr) {
       return L::kSmemCand ? reinterpret_cast<uint64_t*>(smem + L::kCand) + (r0 + rr) * L::kCandCap
-                          : p.cand + (static_cast<int64_t>(blockIdx.x) * R + r0 + rr) * cap;
+                          : p.cand + (static_cast<int64_t>(blockIdx.x) * R + r0 + rr) * ccap;
     };
-    for_each_segment<MODE, R>(p, st, [&](int item, const ItemInfo& it, int lo, int hi, int seg) {
+    // Segmented view of one row's buffer: virtual index i < seg0 + sum(c)
+    // -> position in the buffer.
+    struct SegView {
+      int seg0, rsz, c0, c1, c2, c3;
+      __device__ __forceinline__ int n() const { return seg0 + c0 + c1 + c2 + c3; }
+      __device__ __forceinline__ int pos(int i) const {
+        if (i < seg0) return i;
+        int j = i - seg0;
+        if (j < c0) return seg0 + j;
+        j -= c0;
+        if (j < c1) return seg0 + rsz + j;
+        j -= c1;
+        if (j < c2) return seg0 + 2 * rsz + j;
+        return seg0 + 3 * rsz + (j - c2);
+      }
+    };
+    // Group-cooperative visit of every key of a row's buffer, eight loads in
+    // flight per thread.  fn runs only on the lanes that hold a key, so it
+    // must not contain warp-synchronous operations.
+    auto visit = [&](const uint64_t* cr, const SegView& sv, auto&& fn) {
+      const int n = sv.n();
+      for (int base = 0; base < n; base += 8 * kEpiThreads) {
+        uint64_t kv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int e = base + j * kEpiThreads + g.tid;
+          kv[j] = e < n ? cr[sv.pos(e)] : 0;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (base + j * kEpiThreads + g.tid < n) fn(kv[j]);
+      }
+    };
+    // Each row keeps a bucket histogram (top kHistShift.. key bits) of the
+    // keys appended to its buffer.  The lower edge of the bucket holding the
+    // k-th largest of them is a valid threshold for the row (the k-th
+    // largest of any subset of a row's keys is at most its k-th largest), so
+    // the threshold rises at every check without touching the buffer.
+    auto hist_of = [&](int rr) { return Hist16{hist_words + (r0 + rr) * (kHistBins / 2)}; };
+    // Keys >= T of the buffer moved, in place, to [0, kept); returns kept.
+    // A round reads 8 * kEpiThreads keys into registers before writing any:
+    // every write lands below the number of keys read so far, and an unread
+    // key sits at a position at least its virtual index, so none is
+    // overwritten before it is read.
+    auto compact = [&](uint64_t* cr, const SegView& sv, uint64_t T) -> int {
+      if (g.tid == 0) gsc->bcast[3] = 0;
+      g.sync();
+      const int n = sv.n();
+      for (int base = 0; base < n; base += 8 * kEpiThreads) {
+        uint64_t kv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int e = base + j * kEpiThreads + g.tid;
+          kv[j] = e < n ? cr[sv.pos(e)] : 0;
+        }
+        g.sync();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const bool keep = base + j * kEpiThreads + g.tid < n && kv[j] >= T;
+          const uint32_t m = __ballot_sync(0xffffffffu, keep);
+          if (m) {
+            const int leader = __ffs(m) - 1;
+            uint32_t dst = 0;
+            if (lane == leader) dst = atomicAdd(&gsc->bcast[3], static_cast<uint32_t>(__popc(m)));
+            dst = __shfl_sync(0xffffffffu, dst, leader);
+            if (keep) cr[dst + __popc(m & ((1u << lane) - 1u))] = kv[j];
+          }
+        }
+        g.sync();
+      }
+      const int kept = static_cast<int>(gsc->bcast[3]);
+      g.sync();
+      return kept;
+    };
+    // Region counts are published (each warp's lane 0 writes its counts,
+    // then the group barrier) into alternate copies, so a publication never
+    // overwrites the copy a slower warp may still be reading: it read it
+    // before reaching the barrier of the next publication.
+    int pub = 0;
+    auto publish = [&](const int (&wcnt)[L::kRowsPerGroup], bool valid) {
+      ++pub;
+#pragma unroll
+      for (int rr = 0; rr < L::kRowsPerGroup; ++rr)
+        if (lane == 0) rs->wc[pub & 1][r0 + rr][quad] = valid ? wcnt[rr] : 0;
+    };
+    auto view_of = [&](int rr, int seg0) {
+      const int32_t* c = rs->wc[pub & 1][r0 + rr];
+      return SegView{seg0, (ccap - seg0) >> 2, c[0], c[1], c[2], c[3]};
+    };
+    FP4IDX_STAMP_INIT();
+    for_each_segment<MODE, R>(p, st, [&](int item, const ItemInfo& it, int lo, int hi, bool own) {
       // -- this group's rows of the item: weights in registers, visibility
       bool row_valid[RG];
       int32_t t[RG], vis[RG];
-      float2 w2[RG][H / 2];  // head weight pairs, see weighted_relu_reg
-      // acceptance threshold of each row's buffer (key >= T), kept as the
-      // logit value of T and the largest position accepted at that value
-      float thr_v[RG];
-      uint32_t thr_p[RG];
+      float2 w2[RG][H / 2];  // head weight pairs, see wrelu_chunk
+      uint64_t thr[RG];      // each row's buffer accepts keys >= thr
+      int seg0[RG];          // keys kept by the row's last compaction (front of its buffer)
+      int wcnt[RG];          // keys this warp appended to its region of the row's buffer
 #pragma unroll
       for (int rr = 0; rr < RG; ++rr) {
         row_valid[rr] = r0 + rr < it.nrows;
@@ -799,19 +990,18 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
           const float* wr = p.w + static_cast<int64_t>(t[rr]) * p.w_row_stride + 2 * i;
           w2[rr][i] = row_valid[rr] ? make_float2(__ldg(wr), __ldg(wr + 1)) : make_float2(0.0f, 0.0f);
         }
-        thr_v[rr] = -INFINITY;
-        thr_p[rr] = 0xFFFFFFFFu;
+        thr[rr] = 0;
+        seg0[rr] = 0;
+        wcnt[rr] = 0;
       }
-      g.sync();
       if constexpr (MODE == kModeTopk) {
 #pragma unroll
         for (int rr = 0; rr < RG; ++rr) {
-          if (g.tid == 0) rs->cnt[r0 + rr] = 0;
           const Hist16 hr = hist_of(rr);
           for (int e = g.tid; e < kHistBins / 2; e += kEpiThreads) hr.w[e] = 0;
         }
+        g.sync();  // cleared before any warp of the group appends
       }
-      g.sync();
       since_check = 0;
       // Page ids for the validity check: lane l caches the id of logical
       // page pbase + l and the next 32 are loaded 32 pages ahead, so no
@@ -823,6 +1013,7 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
       };
       int32_t pbase = ((lo << 7) + quad * 32) >> p.page_shift & ~31;
       int32_t ids_cur = fetch_ids(pbase), ids_next = fetch_ids(pbase + 32);
+      FP4IDX_STAMP(0);
       for (int j = lo; j < hi; ++j) {
         const int32_t pos = (j << 7) + key_local;
         const int32_t lp = ((j << 7) + quad * 32) >> p.page_shift;  // warp-uniform
@@ -843,20 +1034,39 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
           // barrier per tile); ok stays warp-uniform, as tcgen05.ld below
           // is a whole-warp instruction.
           bool got = false;
+          FP4IDX_STAMP(4);
           if (lane == 0) got = ok && mbar_wait(accf_bar(a), aph, abort_flag, p.err);
           ok = __shfl_sync(0xffffffffu, got, 0);
+          FP4IDX_STAMP(1);
           if (ok) {
             tc_fence_after();
-            uint32_t v[RG * H];
-            tmem_ld<RG * H>(tmem + (static_cast<uint32_t>(quad * 32) << 16) + L::kAccCol + a * 128u + r0 * H, v);
-            tmem_wait_ld();
-            reg_fence(v);
-            tc_fence_before();
-            mbar_arrive(acce_bar(a));
+            // each row's H columns in chunks of at most 32 (registers); the
+            // accumulator is released once its last chunk is loaded
+            const uint32_t tcol = tmem + (static_cast<uint32_t>(quad * 32) << 16) + L::kAccCol + a * 128u + r0 * H;
+            constexpr int kChunk = L::kMaxRegs >= 160 || H < 32 ? H : 32;
 #pragma unroll
-            for (int rr = 0; rr < RG; ++rr)
-              val[rr] = weighted_relu_reg<H>(*reinterpret_cast<const uint32_t(*)[H]>(&v[rr * H]), w2[rr]);
+            for (int rr = 0; rr < RG; ++rr) {
+              float2 acc[4];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) acc[c] = make_float2(0.0f, 0.0f);
+#pragma unroll
+              for (int c0 = 0; c0 < H; c0 += kChunk) {
+                uint32_t v[kChunk];
+                tmem_ld<kChunk>(tcol + rr * H + c0, v);
+                tmem_wait_ld();
+                reg_fence(v);
+                if (rr == RG - 1 && c0 + kChunk == H) {
+                  tc_fence_before();
+                  __syncwarp();
+                  if (lane == 0) mbar_arrive(acce_bar(a));
+                }
+                wrelu_chunk<kChunk>(v, w2[rr], c0 / 2, acc);
+              }
+              val[rr] = wrelu_total(acc);
+            }
+            FP4IDX_STAMP(3);
           }
+          FP4IDX_STAMP_COUNT();
           ++tile_iter;
         }
         const bool page_good = pos < it.k_len && pg_cur >= 0 && pg_cur < p.num_pages;
@@ -868,108 +1078,164 @@ __global__ void __launch_bounds__(ScoreLayout<H, R, FMT, MODE>::kThreads, 1) sco
         } else {
 #pragma unroll
           for (int rr = 0; rr < RG; ++rr) {
-            // NaN logits are never selected (every comparison is false).
-            const bool take = ok && page_good && pos < vis[rr] &&
-                              (val[rr] > thr_v[rr] || (val[rr] == thr_v[rr] && static_cast<uint32_t>(pos) <= thr_p[rr]));
+            // NaN logits are never selected
+            const uint64_t key = (static_cast<uint64_t>(ordered_bits(val[rr])) << 32) |
+                                 static_cast<uint64_t>(~static_cast<uint32_t>(pos));
+            const bool take = ok && page_good && pos < vis[rr] && !isnan(val[rr]) && key >= thr[rr];
             const uint32_t m = __ballot_sync(0xffffffffu, take);
             if (m) {
-              const int leader = __ffs(m) - 1;
-              int base = 0;
-              if (lane == leader) base = atomicAdd(&rs->cnt[r0 + rr], __popc(m));
-              base = __shfl_sync(0xffffffffu, base, leader);
-              const int slot_i = base + __popc(m & ((1u << lane) - 1u));
-              if (take && slot_i < ccap) {
-                const uint64_t key = (static_cast<uint64_t>(ordered_bits(val[rr])) << 32) |
-                                     static_cast<uint64_t>(~static_cast<uint32_t>(pos));
-                cand_of(rr)[slot_i] = key;
+              // this warp's region: no other warp writes there
+              const int slot_i = wcnt[rr] + __popc(m & ((1u << lane) - 1u));
+              if (take) {
+                cand_of(rr)[seg0[rr] + quad * ((ccap - seg0[rr]) >> 2) + slot_i] = key;
                 hist_of(rr).add(static_cast<int>(key >> kHistShift));
               }
+              wcnt[rr] += __popc(m);
             }
           }
+          FP4IDX_STAMP(4);
           if (++since_check < check_every) continue;
           since_check = 0;
+          publish(wcnt, true);
           g.sync();
-          // -- compaction of full candidate buffers, one row at a time
+          // -- threshold raise from each row's histogram; compaction of a row
+          // whose fullest region is near its end, one row at a time
 #pragma unroll 1
           for (int rr = 0; rr < RG; ++rr) {
-            const int n = rs->cnt[r0 + rr];
-            if (n <= ccap - margin) continue;  // uniform: read after the barrier
-            const Hist16 hr = hist_of(rr);
-            uint64_t* cr = cand_of(rr);
-            uint32_t above = 0;
-            const uint32_t bkt = find_kth_bucket(g, hr, static_cast<uint32_t>(p.k), gsc, &above);
-            const uint32_t kept = above + hr(static_cast<int>(bkt));
-            uint64_t T = static_cast<uint64_t>(bkt) << kHistShift;
-            const bool exact = kept > static_cast<uint32_t>(ccap - 2 * margin);
-            if (exact) {
-              T = select_in_bucket(g, bkt, static_cast<uint32_t>(p.k) - above, gsc, [&](auto&& fn) {
-                // eight loads in flight per thread
-                for (int base = 0; base < n; base += 8 * kEpiThreads) {
-                  uint64_t kv[8];
-#pragma unroll
-                  for (int j = 0; j < 8; ++j) {
-                    const int e = base + j * kEpiThreads + g.tid;
-                    kv[j] = e < n ? cr[e] : 0;
-                  }
-#pragma unroll
-                  for (int j = 0; j < 8; ++j)
-                    if (base + j * kEpiThreads + g.tid < n) fn(kv[j]);
-                }
-              });
-            }
-            const int left = compact_keep_ge(g, cr, n, T, gsc);
-            // buckets below bkt are empty now
-            for (int wd = g.tid; wd < static_cast<int>(bkt >> 1); wd += kEpiThreads) hr.w[wd] = 0;
-            g.sync();
-            if (g.tid == 0) {
-              if (bkt & 1u) hr.set(static_cast<int>(bkt) - 1, 0);
-              if (exact) hr.set(static_cast<int>(bkt), static_cast<uint32_t>(p.k) - above);
-              rs->cnt[r0 + rr] = left;
-            }
-            // rr is uniform across the group; the threshold lives in registers
+            int sg = 0;  // rr is uniform across the group: registers of row rr
+            uint64_t T = 0;
 #pragma unroll
             for (int q = 0; q < RG; ++q)
               if (q == rr) {
-                thr_v[q] = key_value(T);
-                thr_p[q] = ~static_cast<uint32_t>(T);
+                sg = seg0[q];
+                T = thr[q];
               }
-            g.sync();
+            const SegView sv = view_of(rr, sg);
+            if (sv.n() <= p.k) continue;  // uniform: read after the barrier
+            const Hist16 hr = hist_of(rr);
+            uint32_t above = 0;
+            const uint32_t bkt = find_kth_bucket(g, hr, kk, gsc, &above);
+            const uint64_t Tb = static_cast<uint64_t>(bkt) << kHistShift;
+            T = Tb > T ? Tb : T;
+            const int fullest = max(max(sv.c0, sv.c1), max(sv.c2, sv.c3));
+            if (fullest > sv.rsz - margin) {
+              // keep the bucket of the k-th key and above, or exactly the k
+              // largest when that would keep more than half the buffer
+              uint64_t* cr = cand_of(rr);
+              const bool exact = above + hr(static_cast<int>(bkt)) > static_cast<uint32_t>(ccap / 2);
+              if (exact) T = select_in_bucket(g, bkt, kk - above, gsc, [&](auto&& fn) { visit(cr, sv, fn); });
+              const int left = compact(cr, sv, T);
+              // the histogram follows the buffer: buckets below bkt are empty now
+              for (int wd = g.tid; wd < static_cast<int>(bkt >> 1); wd += kEpiThreads) hr.w[wd] = 0;
+              g.sync();
+              if (g.tid == 0) {
+                if (bkt & 1u) hr.set(static_cast<int>(bkt) - 1, 0);
+                if (exact) hr.set(static_cast<int>(bkt), kk - above);
+              }
+              g.sync();
+#pragma unroll
+              for (int q = 0; q < RG; ++q)
+                if (q == rr) {
+                  seg0[q] = left;
+                  wcnt[q] = 0;
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < RG; ++q)
+              if (q == rr) thr[q] = T;
           }
+          FP4IDX_STAMP(5);
         }
       }
       if constexpr (MODE == kModeTopk) {
-        // -- flush each of this group's rows: every candidate in or above the
-        // bucket of the row's k-th key (a superset of its top-k; the merge
-        // selects exactly), so no radix passes run here
-        const int slot = seg == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + item;
+        // -- flush each of this group's rows: its candidates go to the row's
+        // partial list, a superset of the top k of the keys this CTA scored
+        // (the merge selects exactly).  Two-row CTAs (long items, one or two
+        // lists per row) copy every candidate: a threshold here costs the
+        // scorer more than it saves the merge (measured).  Four-row CTAs
+        // (decode: a row's keys spread over many CTAs, so many lists per
+        // row) keep only the keys in or above the bucket of the k-th largest,
+        // which the row's histogram gives without a pass over the buffer.
+        const int slot = own ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + item;
+        publish(wcnt, ok);
 #pragma unroll 1
         for (int rr = 0; rr < RG; ++rr) {
-          const Hist16 hr = hist_of(rr);
           const uint64_t* cr = cand_of(rr);
           g.sync();
-          const int n = rs->cnt[r0 + rr];
-          uint64_t T = 0;
-          if (n > p.k) {
-            uint32_t above = 0;
-            const uint32_t bkt = find_kth_bucket(g, hr, static_cast<uint32_t>(p.k), gsc, &above);
-            T = static_cast<uint64_t>(bkt) << kHistShift;
-          }
+          int sg = 0;
+#pragma unroll
+          for (int q = 0; q < RG; ++q)
+            if (q == rr) sg = ok ? seg0[q] : 0;
+          const SegView sv = view_of(rr, sg);
+          const int n = sv.n();
           const int64_t part = static_cast<int64_t>(slot) * R + r0 + rr;
-          uint64_t* out = p.part_keys + part * cap;
-          // (every thread of the group reaches the barriers inside; a warp
-          // that saw the abort copies nothing)
-          const uint32_t kept = copy_keep_ge(g, cr, ok ? n : 0, T, out, cap, gsc);
+          uint64_t* out = p.part_keys + part * pcap;
+          int wrote = n;
+          if constexpr (L::kSmemCand) {
+            // n <= ccap <= pcap: the buffer's keys, in order, eight in
+            // flight per thread
+            for (int base = 0; base < n; base += 8 * kEpiThreads) {
+              uint64_t kv[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int e = base + j * kEpiThreads + g.tid;
+                kv[j] = e < n ? cr[sv.pos(e)] : 0;
+              }
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int e = base + j * kEpiThreads + g.tid;
+                if (e < n) out[e] = kv[j];
+              }
+            }
+          } else {
+            uint64_t T = 0;
+#pragma unroll
+            for (int q = 0; q < RG; ++q)
+              if (q == rr) T = thr[q];
+            if (n > p.k) {  // uniform
+              uint32_t above = 0;
+              const uint64_t Tb = static_cast<uint64_t>(find_kth_bucket(g, hist_of(rr), kk, gsc, &above))
+                                  << kHistShift;
+              T = Tb > T ? Tb : T;
+            }
+            // keys >= T, every lane taking part in each ballot
+            if (g.tid == 0) gsc->bcast[3] = 0;
+            g.sync();
+            for (int base = 0; base < n; base += 8 * kEpiThreads) {
+              uint64_t kv[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int e = base + j * kEpiThreads + g.tid;
+                kv[j] = e < n ? cr[sv.pos(e)] : 0;
+              }
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const bool keep = base + j * kEpiThreads + g.tid < n && kv[j] >= T;
+                const uint32_t m = __ballot_sync(0xffffffffu, keep);
+                if (m) {
+                  const int leader = __ffs(m) - 1;
+                  uint32_t dst = 0;
+                  if (lane == leader) dst = atomicAdd(&gsc->bcast[3], static_cast<uint32_t>(__popc(m)));
+                  dst = __shfl_sync(0xffffffffu, dst, leader);
+                  if (keep) out[dst + __popc(m & ((1u << lane) - 1u))] = kv[j];
+                }
+              }
+            }
+            g.sync();
+            wrote = static_cast<int>(gsc->bcast[3]);
+            g.sync();
+          }
           bool valid_rr = false;
 #pragma unroll
           for (int q = 0; q < RG; ++q)
             if (q == rr) valid_rr = row_valid[q];
-          if (g.tid == 0) {
-            const int32_t wrote = static_cast<int32_t>(min(kept, static_cast<uint32_t>(cap)));
-            p.part_count[part] = valid_rr ? wrote : 0;
-          }
+          if (g.tid == 0) p.part_count[part] = valid_rr ? wrote : 0;
         }
+        FP4IDX_STAMP(6);
       }
     });
+    FP4IDX_STAMP(0);
+    FP4IDX_STAMP_DONE(3);
   }
 
   // ---- teardown

@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const __grid_
   const int warp = tid >> 5;
   const int t = blockIdx.x;
   const int k = p.k;
-  const int cap = topk_capacity(k);  // keys per partial list
+  const int cap = topk_part_capacity(k);  // keys per partial list
   const int R = mp.rows_per_cta;
   Group<kMergeThreads, 0> g{tid};
 
@@ -121,10 +121,11 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const __grid_
   const int q_local = t - __ldg(p.cu_seqlens_q + b);
   const int item = b * p.row_groups + q_local / R;
   const int r = q_local % R;
-  // tile range of the row's item in the scorer's concatenated tile space
+  // tile range of the row's item in the scorer's concatenated unit space
+  // (an item with tiles holds its tiles, then p.item_overhead units of no tile)
   const int items = p.num_seqs * p.row_groups;
   const int32_t P = __ldg(p.item_start + item), total = __ldg(p.item_start + items);
-  const int32_t tiles = __ldg(p.item_start + item + 1) - P;
+  const int32_t tiles = max(__ldg(p.item_start + item + 1) - P - p.item_overhead, 0);
   const int C = p.score_ctas;
   const int32_t chunk = total > 0 ? (total + C - 1) / C : 1;
   const int c_lo = tiles > 0 ? P / chunk : 0;
@@ -671,7 +672,7 @@ cudaError_t launch_topk_select(const MergeParams& p, int rows, cudaStream_t stre
 
 cudaError_t launch_topk_merge(const MergeParams& p, int rows, bool many_rows, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
-  return many_rows ? launch_merge_t<4096>(p, rows, stream) : launch_merge_t<20480>(p, rows, stream);
+  return many_rows ? launch_merge_t<8192>(p, rows, stream) : launch_merge_t<20480>(p, rows, stream);
 }
 
 }  // namespace fp4idx

@@ -25,7 +25,7 @@
 namespace fp4idx {
 namespace {
 
-constexpr size_t kScratchBytes = 64u << 20;  // 64 MiB
+constexpr size_t kScratchBytes = 128u << 20;  // 128 MiB
 
 static __device__ __align__(256) unsigned char g_topk_scratch[kScratchBytes];
 

@@ -20,14 +20,17 @@ constexpr int kHistShift = 53;  // bucket = key >> 53 (sign, exponent, 2 mantiss
 
 // Group of kThreads threads (a multiple of 32, <= 1024) that synchronise
 // with a named barrier: barrier 0 is __syncthreads, kBarrierId < 0 takes the
-// barrier id from `bar` at run time.
+// barrier id from `bar` at run time; a group of one warp uses __syncwarp.
 template <int kThreads, int kBarrierId>
 struct Group {
   static_assert(kThreads % 32 == 0, "whole warps");
+  static constexpr int kSize = kThreads;
   int tid;  // 0 .. kThreads-1
   int bar = kBarrierId;
   __device__ __forceinline__ void sync() const {
-    if constexpr (kBarrierId == 0)
+    if constexpr (kThreads == 32)
+      __syncwarp();  // a one-warp group
+    else if constexpr (kBarrierId == 0)
       __syncthreads();
     else if constexpr (kBarrierId > 0)
       asm volatile("bar.sync %0, %1;" ::"n"(kBarrierId), "n"(kThreads) : "memory");

@@ -252,9 +252,9 @@ fp4idx_status_t fp4idx_logits_topk(const fp4idx_problem_t* problem, const float*
  * for these callers.
  *
  * Results are those of fp4idx_topk (same arguments, minus the workspace).
- * The scratch is a fixed 64 MiB array inside the library's device memory,
+ * The scratch is a fixed 128 MiB array inside the library's device memory,
  * held by every GPU that loads the library until the process exits.  A
- * problem whose fp4idx_topk_workspace_bytes() exceeds 64 MiB is rejected
+ * problem whose fp4idx_topk_workspace_bytes() exceeds 128 MiB is rejected
  * with FP4IDX_EWORKSPACE before anything runs.  The first call on a device
  * looks up the array's device address (with that device current); make that
  * first call before capturing any stream.  All calls on a device share the

@@ -85,7 +85,7 @@ def test_noalloc_streaming_plan_after_a_call_of_another_shape(noalloc):
     for i, (p, k, extra) in enumerate(cases):
         dp = B.DeviceProblem.from_host(p)
         w = torch.as_tensor(p.w).cuda()
-        assert B.fp4idx_topk_workspace_bytes(dp, k) <= 64 << 20
+        assert B.fp4idx_topk_workspace_bytes(dp, k) <= 128 << 20
         ref = _reference(dp, w, k, streaming=bool(extra) or p.max_seqlen_k > 16384)
         st, idx, val, cnt = _call(f, dp, w, k, B.FP4IDX_TOPK_SORTED | extra)
         assert st == 0, lib.fp4idx_last_error_message()
@@ -112,7 +112,7 @@ def test_noalloc_rejects_problems_beyond_its_scratch(noalloc):
                         visibility="full")
     dp = B.DeviceProblem.from_host(p)
     w = torch.as_tensor(p.w).cuda()
-    assert B.fp4idx_topk_workspace_bytes(dp, 2048) > 64 << 20
+    assert B.fp4idx_topk_workspace_bytes(dp, 2048) > 128 << 20
     st, idx, _, _ = _call(f, dp, w, 2048, 0)
     assert st == 3  # FP4IDX_EWORKSPACE
     assert b"static scratch" in lib.fp4idx_last_error_message()
