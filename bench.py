@@ -155,6 +155,7 @@ WORKLOADS = {
     "block_topk": dict(maker="nvfp4_gqa_block_scores", kind="block", k=0, block_k=16, logits=False,
                        bound="tensor"),
     "prefill": dict(maker="prefill_32k", kind="topk", k=2048, logits=False, bound="tensor"),
+    "prefill_8k": dict(maker="prefill_8k", kind="topk", k=2048, logits=False, bound="tensor"),
     "tiny": dict(maker="tiny_mx_decode", kind="topk", k=64, logits=True, bound="hbm"),
     "store_k": dict(maker="kcache_write_1m", kind="store", k=0, logits=False, bound="hbm", tokens=1 << 20),
     "logits16k": dict(maker="verify_decode_16k", kind="logits", k=0, logits=True, bound="hbm"),

@@ -63,6 +63,12 @@ class Problem:
     topk: int = 0
     q_lens: Sequence[int] = ()
     k_lens: Sequence[int] = ()
+    # SGLang PR 42861's input variants (see the constructors below)
+    kv_layout: int = 0                     # 1: k is the fused table [P, Hkv, page*(64+G)]
+    cand_mask: Optional[np.ndarray] = None  # [T, ld] uint8, 0 = not a candidate
+    req: Optional[np.ndarray] = None        # [T] int32 request of each row
+    req_table: Optional[np.ndarray] = None  # [B, cap] int32 cache slot of each position, -1 none
+    q_dtype: int = 0                       # 1: q is bf16 words [T, Hq, 128] uint16
 
     @property
     def num_rows(self) -> int:
@@ -300,6 +306,90 @@ def prefill_32k() -> Problem:
     return make_problem(name="prefill_mxfp4_32k_h64_top2048", seed=1004, fmt=MXFP4, q_lens=[32768],
                         k_lens=[32768], num_heads=64, e8m0_range=(120, 134), weights="normal",
                         visibility="causal", topk=2048)
+
+
+def prefill_8k() -> Problem:
+    """The prefill shape at a quarter of the rows and keys: 8,192 causal rows
+    over 8,192 keys, 64 heads, MXFP4 (E8M0 120..134), w ~ N(0,1), 64-key
+    pages, top-2048 (a case small enough for many-pass profiler captures)."""
+    return make_problem(name="prefill_mxfp4_8k_h64_top2048", seed=1004, fmt=MXFP4, q_lens=[8192],
+                        k_lens=[8192], num_heads=64, e8m0_range=(120, 134), weights="normal",
+                        visibility="causal", topk=2048)
+
+
+# ---------------------------------------------------------------------------
+# SGLang PR 42861's input variants ("bench_fp4_index_scorer.py"): the same
+# problem re-expressed; no scorer arithmetic happens here.
+# ---------------------------------------------------------------------------
+
+def fused_pages(p: Problem) -> Problem:
+    """The K cache as one table of page*(64+G) bytes per (page, K head): the
+    page's 64-byte code rows, then its G-byte scale rows (the order inside a
+    page is not printed; this is the reading)."""
+    P, Hkv, page = p.k.shape[:3]
+    G = groups(p.format)
+    fused = np.empty((P, Hkv, page * (64 + G)), np.uint8)
+    fused[:, :, : page * 64] = p.k.reshape(P, Hkv, page * 64)
+    fused[:, :, page * 64:] = p.k_scale.reshape(P, Hkv, page * G)
+    return dataclasses.replace(p, name=p.name + "_fused", k=fused, kv_layout=1)
+
+
+def token_table(p: Problem, extra: int = 64) -> Problem:
+    """The request of every row and a per-request table of cache slots, one
+    per logical position (slot = page * page_size + offset, -1 past the
+    request's keys), cap = max keys + extra columns, the rows' visible
+    lengths as lens -- the metadata form of the PR's benchmark.  Needs
+    explicit visible lengths."""
+    assert p.visible_len is not None and p.page_offsets is None
+    B = p.num_seqs
+    cap = p.max_seqlen_k + extra
+    req = np.zeros(p.num_rows, np.int32)
+    table = np.full((B, cap), -1, np.int32)
+    for b in range(B):
+        q0, q1 = int(p.cu_seqlens_q[b]), int(p.cu_seqlens_q[b + 1])
+        req[q0:q1] = b
+        kl = int(p.cu_seqlens_k[b + 1] - p.cu_seqlens_k[b])
+        s = np.arange(kl)
+        table[b, :kl] = p.block_table[b, s // p.page_size] * p.page_size + s % p.page_size
+    return dataclasses.replace(p, name=p.name + "_tokens", req=req, req_table=table)
+
+
+def shuffle_tokens(p: Problem, seed: int) -> Problem:
+    """The tokens of every physical page stored in a random order (codes and
+    scales moved together) and the per-token table pointing at their new
+    offsets: the same keys, a table that is no longer page-ordered."""
+    assert p.req_table is not None and p.kv_layout == 0
+    rng = np.random.default_rng(seed)
+    P, Hkv, page = p.k.shape[:3]
+    perm = np.stack([rng.permutation(page) for _ in range(P)])   # new offset of each token
+    k = np.empty_like(p.k)
+    ks = np.empty_like(p.k_scale)
+    for pg in range(P):
+        k[pg][:, perm[pg]] = p.k[pg]
+        ks[pg][:, perm[pg]] = p.k_scale[pg]
+    table = p.req_table.copy()
+    ok = table >= 0
+    pg, off = table[ok] // page, table[ok] % page
+    table[ok] = pg * page + perm[pg, off]
+    return dataclasses.replace(p, name=p.name + "_shuffled", k=k, k_scale=ks, req_table=table)
+
+
+def with_cand_mask(p: Problem, density: float, seed: int) -> Problem:
+    """A candidate mask [T, ld] (ld = max keys rounded to 16) with about
+    `density` of its entries set."""
+    rng = np.random.default_rng(seed)
+    ld = (p.max_seqlen_k + 15) // 16 * 16
+    mask = (rng.random((p.num_rows, ld)) < density).astype(np.uint8)
+    return dataclasses.replace(p, name=p.name + "_masked", cand_mask=mask)
+
+
+def with_bf16_queries(p: Problem, seed: int) -> Problem:
+    """bf16 queries as in the PR's benchmark: integers in [-8, 8] / 8 (exact
+    dyadic values), stored as raw bf16 words [T, Hq, 128]."""
+    rng = np.random.default_rng(seed)
+    vals = rng.integers(-8, 9, size=(p.num_rows, p.num_heads, 128)).astype(np.float32) / 8
+    words = (vals.view(np.uint32) >> 16).astype(np.uint16)  # exact: these values need 4 mantissa bits
+    return dataclasses.replace(p, name=p.name + "_bf16q", q=words, q_dtype=1)
 
 
 # E4M3 codes of the hand-built NaN case (bias 7): 0x28 = 0.25, 0x30 = 0.5,

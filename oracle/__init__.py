@@ -65,6 +65,13 @@ class _Problem(ctypes.Structure):
         ("visible_len", ctypes.c_void_p),
         ("causal", ctypes.c_int32),
         ("qo_offset", ctypes.c_void_p),
+        ("kv_layout", ctypes.c_int32),
+        ("cand_mask", ctypes.c_void_p),
+        ("mask_ld", ctypes.c_int64),
+        ("req", ctypes.c_void_p),
+        ("req_table", ctypes.c_void_p),
+        ("req_stride", ctypes.c_int64),
+        ("q_dtype", ctypes.c_int32),
     ]
 
 
@@ -125,14 +132,24 @@ class OracleProblem:
     ``q_scale`` [T,Hq,G] u8, ``k`` [P,Hkv,page,64] u8, ``k_scale`` [P,Hkv,page,G]
     u8, ``cu_seqlens_q``/``cu_seqlens_k`` [B+1] i32, ``block_table`` [B,stride]
     i32, optional ``page_offsets`` [B], ``visible_len`` [T], ``causal``,
-    optional ``qo_offset`` [B] and ``w`` [T,Hq] f32.
+    optional ``qo_offset`` [B] and ``w`` [T,Hq] f32.  SGLang PR 42861's input
+    variants, all optional: ``kv_layout`` 1 with ``k`` the fused table
+    [P,Hkv,page*(64+G)] u8 (``k_scale`` unused); ``cand_mask`` [T,ld] u8;
+    ``req`` [T] i32 with ``req_table`` [B,stride] i32 slots (then
+    ``visible_len`` gives the lens); ``q_dtype`` 1 with ``q`` the bf16 words
+    [T,Hq,128] u16 (``q_scale`` unused).
     """
 
     def __init__(self, prob):
-        self.q = _np(prob.q, np.uint8)
-        self.q_scale = _np(prob.q_scale, np.uint8)
+        self.q_dtype = int(getattr(prob, "q_dtype", 0))
+        self.kv_layout = int(getattr(prob, "kv_layout", 0))
+        self.q = _np(prob.q, np.uint16 if self.q_dtype == 1 else np.uint8)
+        self.q_scale = None if self.q_dtype == 1 else _np(prob.q_scale, np.uint8)
         self.k = _np(prob.k, np.uint8)
-        self.k_scale = _np(prob.k_scale, np.uint8)
+        self.k_scale = None if self.kv_layout == 1 else _np(prob.k_scale, np.uint8)
+        self.cand_mask = _np(getattr(prob, "cand_mask", None), np.uint8)
+        self.req = _np(getattr(prob, "req", None), np.int32)
+        self.req_table = _np(getattr(prob, "req_table", None), np.int32)
         self.cu_q = _np(prob.cu_seqlens_q, np.int32)
         self.cu_k = _np(prob.cu_seqlens_k, np.int32)
         self.table = _np(prob.block_table, np.int32)
@@ -146,8 +163,13 @@ class OracleProblem:
         self.num_seqs = self.cu_q.shape[0] - 1
         fmt = int(prob.format)
         G = 4 if fmt == 0 else 8
-        assert self.q.shape[2] == 64 and self.q_scale.shape[2] == G
+        if self.q_dtype == 1:
+            assert self.q.shape[2] == 128
+        else:
+            assert self.q.shape[2] == 64 and self.q_scale.shape[2] == G
         table_stride = self.table.shape[1] if self.table.ndim == 2 else 0
+        if self.req_table is not None:
+            self.num_seqs = self.req_table.shape[0]
         self.c = _Problem(
             format=fmt,
             num_seqs=self.num_seqs,
@@ -159,7 +181,7 @@ class OracleProblem:
             table_stride=table_stride,
             q=_ptr(self.q),
             q_scale=_ptr(self.q_scale),
-            q_row_stride=Hq * 64,
+            q_row_stride=Hq * (256 if self.q_dtype == 1 else 64),
             q_scale_row_stride=Hq * G,
             k=_ptr(self.k),
             k_scale=_ptr(self.k_scale),
@@ -170,6 +192,13 @@ class OracleProblem:
             visible_len=_ptr(self.visible_len),
             causal=int(bool(getattr(prob, "causal", False))),
             qo_offset=_ptr(self.qo_offset),
+            kv_layout=self.kv_layout,
+            cand_mask=_ptr(self.cand_mask),
+            mask_ld=0 if self.cand_mask is None else self.cand_mask.shape[1],
+            req=_ptr(self.req),
+            req_table=_ptr(self.req_table),
+            req_stride=0 if self.req_table is None else self.req_table.shape[1],
+            q_dtype=self.q_dtype,
         )
         self.ref = ctypes.byref(self.c)
 

@@ -56,6 +56,10 @@ static double scale_value(const orc_problem* p, uint8_t code) {
 }
 
 int32_t orc_request_of_row(const orc_problem* p, int32_t t) {
+  if (p->req) {  /* per-token table: the row's request is given */
+    int32_t b = p->req[t];
+    return (b >= 0 && b < p->num_seqs) ? b : -1;
+  }
   for (int32_t b = 0; b < p->num_seqs; ++b)
     if (t >= p->cu_seqlens_q[b] && t < p->cu_seqlens_q[b + 1]) return b;
   return -1;
@@ -67,6 +71,12 @@ int32_t orc_request_of_row(const orc_problem* p, int32_t t) {
 int64_t orc_visible(const orc_problem* p, int32_t t) {
   int32_t b = orc_request_of_row(p, t);
   if (b < 0) return 0;
+  if (p->req_table) {  /* per-token table: lens, clipped to the table width */
+    int64_t v = p->visible_len ? p->visible_len[t] : p->req_stride;
+    if (v < 0) v = 0;
+    if (v > p->req_stride) v = p->req_stride;
+    return v;
+  }
   int64_t q_len = p->cu_seqlens_q[b + 1] - p->cu_seqlens_q[b];
   int64_t k_len = p->cu_seqlens_k[b + 1] - p->cu_seqlens_k[b];
   int64_t q_local = t - p->cu_seqlens_q[b];
@@ -123,30 +133,84 @@ static int tracker_safe(const exact_tracker* tr) {
   return tr->abs_sum < ldexp(tr->min_lsb, 24);
 }
 
-/* Byte address of key s (request b, kv head hk) inside the paged cache. */
-static int64_t key_row(const orc_problem* p, int32_t b, int32_t hk, int64_t s) {
-  int64_t base = p->page_offsets ? (int64_t)p->page_offsets[b] : (int64_t)b * p->table_stride;
-  int64_t page = p->block_table[base + s / p->page_size];
-  int64_t token = s % p->page_size;
-  return (page * p->num_kv_heads + hk) * p->page_size + token;
+/* value of a bfloat16 word from its fields: (-1)^s 2^(e-127) (1 + m/128), or
+ * (-1)^s 2^-126 m/128 for e = 0 */
+static double bf16_value(uint16_t w) {
+  const int s = w >> 15, e = (w >> 7) & 0xFF, m = w & 0x7F;
+  double v;
+  if (e == 0) v = ldexp((double)m / 128.0, -126);
+  else if (e == 255) v = m ? NAN : INFINITY;
+  else v = ldexp(1.0 + (double)m / 128.0, e - 127);
+  return s ? -v : v;
 }
+
+/* Codes and scales of key s (request b, kv head hk) inside the paged cache;
+ * 0 when position s has no key (a per-token table entry < 0 or a page
+ * outside the cache). */
+static int key_addr(const orc_problem* p, int32_t b, int32_t hk, int64_t s, const uint8_t** codes,
+                    const uint8_t** scales) {
+  const int G = num_groups(p);
+  int64_t page, token;
+  if (p->req_table) {
+    int64_t slot = p->req_table[(int64_t)b * p->req_stride + s];
+    if (slot < 0) return 0;
+    page = slot / p->page_size;
+    token = slot % p->page_size;
+  } else {
+    int64_t base = p->page_offsets ? (int64_t)p->page_offsets[b] : (int64_t)b * p->table_stride;
+    page = p->block_table[base + s / p->page_size];
+    token = s % p->page_size;
+  }
+  if (page < 0 || page >= p->num_pages) return 0;
+  int64_t block = page * p->num_kv_heads + hk;  /* one (page, K head) */
+  if (p->kv_layout == 1) {
+    const uint8_t* pg = p->k + block * (int64_t)p->page_size * (64 + G);
+    *codes = pg + token * 64;
+    *scales = pg + (int64_t)p->page_size * 64 + token * G;
+  } else {
+    int64_t row = block * p->page_size + token;
+    *codes = p->k + row * 64;
+    *scales = p->k_scale + row * G;
+  }
+  return 1;
+}
+
+/* Whether position s of row t holds a key the row may select: visible, in
+ * the cache, and not cleared by the candidate mask. */
+static int is_candidate(const orc_problem* p, int32_t t, int64_t s, int64_t vis) {
+  if (s >= vis) return 0;
+  if (p->cand_mask && p->cand_mask[(int64_t)t * p->mask_ld + s] == 0) return 0;
+  const uint8_t *c, *sc;
+  return key_addr(p, orc_request_of_row(p, t), 0, s, &c, &sc);
+}
+
 
 double orc_dot(const orc_problem* p, int32_t t, int32_t hq, int64_t s, double* abs_sum, int32_t* safe) {
   const int G = num_groups(p), S = group_size(p);
   int32_t b = orc_request_of_row(p, t);
   int32_t hk = hq / (p->num_heads / p->num_kv_heads);
-  int64_t krow = key_row(p, b, hk, s);
-  const uint8_t* qc = p->q + (int64_t)t * p->q_row_stride + (int64_t)hq * 64;
-  const uint8_t* qs = p->q_scale + (int64_t)t * p->q_scale_row_stride + (int64_t)hq * G;
-  const uint8_t* kc = p->k + krow * 64;
-  const uint8_t* ks = p->k_scale + krow * G;
+  const uint8_t *kc = NULL, *ks = NULL;
+  if (b < 0 || !key_addr(p, b, hk, s, &kc, &ks)) {  /* no key at s */
+    if (abs_sum) *abs_sum = 0.0;
+    if (safe) *safe = 1;
+    return NAN;
+  }
+  const uint8_t* qc = p->q + (int64_t)t * p->q_row_stride + (int64_t)hq * (p->q_dtype == 1 ? 256 : 64);
+  const uint8_t* qs = p->q_dtype == 1 ? NULL : p->q_scale + (int64_t)t * p->q_scale_row_stride + (int64_t)hq * G;
   exact_tracker tr;
   tracker_init(&tr);
   double sum = 0.0, asum = 0.0;
   for (int d = 0; d < HEAD_DIM; ++d) {
     uint32_t qn = (d & 1) ? (qc[d >> 1] >> 4) : (qc[d >> 1] & 15u);
     uint32_t kn = (d & 1) ? (kc[d >> 1] >> 4) : (kc[d >> 1] & 15u);
-    double qr = orc_e2m1(qn) * scale_value(p, qs[d / S]);
+    double qr;
+    if (p->q_dtype == 1) {
+      uint16_t wq;
+      memcpy(&wq, qc + 2 * d, sizeof(wq));
+      qr = bf16_value(wq);
+    } else {
+      qr = orc_e2m1(qn) * scale_value(p, qs[d / S]);
+    }
     double kr = orc_e2m1(kn) * scale_value(p, ks[d / S]);
     double prod = qr * kr;
     sum += prod;
@@ -161,7 +225,7 @@ double orc_dot(const orc_problem* p, int32_t t, int32_t hq, int64_t s, double* a
 /* One weighted-ReLU logit in fp64 with its bound and exactness flag. */
 static float logit_one(const orc_problem* p, const float* w, int64_t w_row_stride, int32_t t,
                        int64_t s, int64_t vis, double* bound, uint8_t* safe) {
-  if (s >= vis) {
+  if (!is_candidate(p, t, s, vis)) {
     if (bound) *bound = 0.0;
     if (safe) *safe = 1;
     return -INFINITY;
@@ -231,6 +295,8 @@ void orc_block_scores(const orc_problem* p, int32_t ktiles, const int32_t* rows,
         double best = -INFINITY, bnd = 0.0;
         int found = 0, all_safe = 1;
         for (int64_t s = (int64_t)kb * BLOCK_KEYS; s < (int64_t)(kb + 1) * BLOCK_KEYS && s < vis; ++s) {
+          const uint8_t *kc, *ks;
+          if (!key_addr(p, orc_request_of_row(p, t), h / (H / p->num_kv_heads), s, &kc, &ks)) continue;
           double asum;
           int32_t dsafe;
           double dot = orc_dot(p, t, h, s, &asum, &dsafe);
@@ -277,10 +343,12 @@ void orc_topk(const orc_problem* p, const float* w, int64_t w_row_stride, int32_
       all[s].value = logit_one(p, w, w_row_stride, t, s, vis, NULL, NULL);
       all[s].index = s;
     }
-    /* A NaN logit has no place in the order: such positions are not selected. */
+    /* A NaN logit has no place in the order: such positions are not selected;
+     * neither are positions that are not candidates (no key, or cleared by
+     * the candidate mask: their logit is -inf by definition, not a value). */
     int64_t m = 0;
     for (int64_t s = 0; s < vis; ++s)
-      if (!isnan(all[s].value)) all[m++] = all[s];
+      if (!isnan(all[s].value) && is_candidate(p, t, s, vis)) all[m++] = all[s];
     qsort(all, (size_t)m, sizeof(scored_pos), cmp_scored);
     int64_t n = m < k ? m : k;
     for (int64_t j = 0; j < k; ++j) {
@@ -350,16 +418,6 @@ void orc_topk_slots(const orc_problem* p, const int32_t* indices, int32_t k, int
   }
 }
 
-/* value of a bfloat16 word from its fields: (-1)^s 2^(e-127) (1 + m/128), or
- * (-1)^s 2^-126 m/128 for e = 0 */
-static double bf16_value(uint16_t w) {
-  const int s = w >> 15, e = (w >> 7) & 0xFF, m = w & 0x7F;
-  double v;
-  if (e == 0) v = ldexp((double)m / 128.0, -126);
-  else if (e == 255) v = m ? NAN : INFINITY;
-  else v = ldexp(1.0 + (double)m / 128.0, e - 127);
-  return s ? -v : v;
-}
 
 void orc_store_k(const uint16_t* keys, int64_t key_row_stride, int32_t num_tokens, int32_t num_kv_heads,
                  const int32_t* slots, int32_t page_size, int64_t num_pages, uint8_t* k, uint8_t* k_scale) {

@@ -25,6 +25,12 @@
  *   - top-k = full sort of the visible positions by (value desc, index asc),
  *     first k kept, -1 padded; a position whose logit is NaN has no rank and
  *     is not selected.
+ *   - SGLang PR 42861's input variants (its benchmark script): the fused K
+ *     table of PAGE_SIZE * (64 + G) bytes per page (order inside a page not
+ *     printed; read as the page's codes, then its scales), the per-token
+ *     slot table req_table[req[t]][s], the optional candidate mask (a
+ *     position it clears is not a candidate: -inf, never selected), and
+ *     bf16 queries (Q_real = the bf16 value, no block scale).
  *
  * Parity pins: see tests/test_oracle_pins.py (exhaustive decodes, closed forms,
  * library-routine cross-checks, brute-force top-k, invariants).
@@ -59,6 +65,22 @@ typedef struct orc_problem {
   const int32_t* visible_len;   /* [T] or NULL */
   int32_t causal;
   const int32_t* qo_offset;     /* [B] or NULL */
+  /* SGLang PR 42861's variants of the inputs ("bench_fp4_index_scorer.py":
+   * the K table of PAGE_SIZE * 68 bytes per page, req / req_table / lens,
+   * the candidate-mask argument, bf16 q). */
+  int32_t kv_layout;            /* 0: k and k_scale arrays; 1: fused pages, k only:
+                                   [P][Hkv][page*64 code bytes, then page*G scale bytes] */
+  const uint8_t* cand_mask;     /* [T][mask_ld] or NULL: position s of row t is a
+                                   candidate only when cand_mask[t][s] != 0 */
+  int64_t mask_ld;
+  const int32_t* req;           /* [T] request of each row, or NULL (cu_seqlens_q rule) */
+  const int32_t* req_table;     /* [B][req_stride] cache slot of each logical position
+                                   (slot = page*page_size + offset; < 0: no key); with it,
+                                   block_table / page_offsets / cu_seqlens_k are unused and
+                                   vis(t) = clamp(visible_len[t], 0, req_stride) */
+  int64_t req_stride;
+  int32_t q_dtype;              /* 0: FP4 codes + scales; 1: bf16 words [T][Hq][128]
+                                   (row stride q_row_stride bytes; q_scale unused) */
 } orc_problem;
 
 /* element decodes */

@@ -514,3 +514,111 @@ def test_store_k_places_tokens_by_slot_and_skips_negative_slots():
         for off in range(64):
             untouched = (pg, off) not in written
             assert ((k[pg, :, off] == 0xAB).all() and (ks[pg, :, off] == 0xCD).all()) == untouched
+
+
+# ---------------------------------------------------------------------------
+# SGLang PR 42861's input variants: fused pages, per-token slot table,
+# candidate mask, bf16 queries
+# ---------------------------------------------------------------------------
+
+def test_fused_pages_give_the_split_arrays_results():
+    # the fused table holds the same bytes: every output must be identical,
+    # and moving one scale byte inside the fused page must change exactly the
+    # key it belongs to
+    for fmt in (wl.MXFP4, wl.NVFP4):
+        p = _small(fmt=fmt, q_lens=[3, 2], k_lens=[300, 129])
+        f = wl.fused_pages(p)
+        a, _, _ = oracle.logits_rows(p, 300)
+        b, _, _ = oracle.logits_rows(f, 300)
+        np.testing.assert_array_equal(a, b)
+        np.testing.assert_array_equal(oracle.topk(p, 50)[0], oracle.topk(f, 50)[0])
+        np.testing.assert_array_equal(oracle.block_scores(p, 3)[0], oracle.block_scores(f, 3)[0])
+    p = _small(q_lens=[1], k_lens=[128], num_heads=4, visibility="full")
+    f = wl.fused_pages(p)
+    pg, tok = int(p.block_table[0, 1]), 5  # logical key 64 + 5 = 69
+    f.k[pg, 0, 64 * tok: 64 * tok + 64] = 0x22  # that key's codes: every value 1.0
+    f.k[pg, 0, 64 * 64 + 4 * tok: 64 * 64 + 4 * tok + 4] = 127  # its four E8M0 scales: 1
+    before = [oracle.dot(f, 0, 1, s)[0] for s in (68, 69, 70)]
+    f.k[pg, 0, 64 * 64 + 4 * tok + 1] = 128  # second scale of that key: 2
+    after = [oracle.dot(f, 0, 1, s)[0] for s in (68, 69, 70)]
+    assert before[0] == after[0] and before[2] == after[2]  # neighbours untouched
+    q = np.array([oracle.e2m1(int(c) >> (4 * (d & 1)) & 15) for d, c in
+                  ((d, p.q[0, 1, d // 2]) for d in range(32, 64))]) * oracle.e8m0(int(p.q_scale[0, 1, 1]))
+    assert after[1] - before[1] == q.sum()  # the values of group 1 now weigh twice
+
+
+def test_token_table_matches_block_table():
+    p = _small(q_lens=[3, 2], k_lens=[300, 129])
+    t = wl.token_table(p)
+    a, _, _ = oracle.logits_rows(p, 300)
+    b, _, _ = oracle.logits_rows(t, 300)
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(oracle.topk(p, 40)[0], oracle.topk(t, 40)[0])
+
+
+def test_token_table_follows_every_slot():
+    # tokens stored in a different order inside each page, table pointing at
+    # them: the same keys, so the same logits
+    p = _small(q_lens=[3, 2], k_lens=[300, 129])
+    t = wl.token_table(p)
+    sh = wl.shuffle_tokens(t, seed=4)
+    assert not np.array_equal(sh.k, t.k)
+    a, _, _ = oracle.logits_rows(t, 300)
+    b, _, _ = oracle.logits_rows(sh, 300)
+    np.testing.assert_array_equal(a, b)
+    # a slot of -1 inside the visible range is not a candidate
+    sh.req_table[0, 7] = -1
+    c, _, _ = oracle.logits_rows(sh, 300)
+    assert np.isneginf(c[:3, 7]).all()
+    np.testing.assert_array_equal(np.delete(c, 7, axis=1), np.delete(b, 7, axis=1))
+    idx, _, cnt = oracle.topk(sh, 400)
+    assert 7 not in idx[:3].tolist() and list(cnt[:3]) == [int(v) - 1 for v in oracle.visible_all(sh)[:3]]
+
+
+def test_candidate_mask_closed_form_and_topk():
+    p = _small(q_lens=[3, 2], k_lens=[300, 129])
+    m = wl.with_cand_mask(p, density=0.3, seed=8)
+    full, _, _ = oracle.logits_rows(p, 300)
+    got, _, _ = oracle.logits_rows(m, 300)
+    keep = m.cand_mask[:, :300] != 0
+    np.testing.assert_array_equal(got[keep], full[keep])
+    assert np.isneginf(got[~keep]).all()
+    vis = oracle.visible_all(m)
+    k = 25
+    idx, val, cnt = oracle.topk(m, k)
+    for t in range(m.num_rows):
+        cands = [s for s in range(vis[t]) if m.cand_mask[t, s]]
+        order = sorted(cands, key=lambda s: (-(float(full[t, s]) + 0.0), s))[:k]
+        assert cnt[t] == len(order)
+        assert list(idx[t, : len(order)]) == order
+
+
+def test_bf16_queries_closed_form():
+    # every q value 1.0 (bf16 0x3F80), every k value 1.0 at scale 1: dot = 128
+    p = _small(q_lens=[2], k_lens=[64], num_heads=4, visibility="full")
+    b = wl.with_bf16_queries(p, seed=1)
+    b.q[...] = 0x3F80
+    b.k[...] = 0x22
+    b.k_scale[...] = 127
+    for h in range(4):
+        d, asum, safe = oracle.dot(b, 0, h, 10)
+        assert d == 128.0 and asum == 128.0 and safe
+    b.q[:, :, ::2] = 0xBF80  # -1.0 on even dims: the dot cancels to 0
+    assert oracle.dot(b, 1, 2, 33)[0] == 0.0
+
+
+def test_bf16_queries_match_library_matmul():
+    # torch's own bf16 -> float64 conversion of the query words, times the
+    # independently dequantised keys
+    p = _small(q_lens=[3, 2], k_lens=[300, 129])
+    b = wl.with_bf16_queries(p, seed=6)
+    qv = torch.from_numpy(b.q.astype(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    kd = _dequant(b.k, b.k_scale, b.format)  # [P, Hkv, page, 128]
+    got, _, _ = oracle.logits_rows(b, 300)
+    vis = oracle.visible_all(b)
+    for t in range(b.num_rows):
+        req = 0 if t < 3 else 1
+        keys = np.stack([kd[b.block_table[req, s // 64], 0, s % 64] for s in range(vis[t])])
+        d = qv[t] @ keys.T  # [H, vis]
+        lg = (b.w[t].astype(np.float64)[:, None] * np.maximum(d, 0.0)).sum(axis=0)
+        np.testing.assert_array_equal(got[t, : vis[t]], lg.astype(np.float32))
