@@ -31,6 +31,9 @@ FP4IDX_TOPK_SORTED = 0x1
 FP4IDX_TOPK_STREAMING = 0x2
 ERR_PAGE_RANGE = 0x1
 ERR_TIMEOUT = 0x2
+ERR_TOKEN_TABLE = 0x4
+KV_SPLIT = 0
+KV_FUSED = 1
 
 EXPORTED = (
     "fp4idx_logits",
@@ -38,6 +41,8 @@ EXPORTED = (
     "fp4idx_block_topk",
     "fp4idx_topk_slots",
     "fp4idx_store_k",
+    "fp4idx_store_k_fused",
+    "fp4idx_pages_from_token_table",
     "fp4idx_topk_workspace_bytes",
     "fp4idx_topk",
     "fp4idx_topk_score",
@@ -76,6 +81,9 @@ class CProblem(ctypes.Structure):
         ("visible_len", ctypes.c_void_p),
         ("causal", ctypes.c_int32),
         ("qo_offset", ctypes.c_void_p),
+        ("kv_layout", ctypes.c_int32),
+        ("cand_mask", ctypes.c_void_p),
+        ("mask_ld", ctypes.c_int64),
     ]
 
 
@@ -111,6 +119,10 @@ def load_library(path: str = LIB_PATH):
         lib.fp4idx_topk_slots.restype = i32
         lib.fp4idx_store_k.argtypes = [vp, i64, i32, i32, vp, i32, i64, vp, vp, vp]
         lib.fp4idx_store_k.restype = i32
+        lib.fp4idx_store_k_fused.argtypes = [vp, i64, i32, i32, vp, i32, i64, vp, vp]
+        lib.fp4idx_store_k_fused.restype = i32
+        lib.fp4idx_pages_from_token_table.argtypes = [vp, i32, vp, i32, i64, i32, i64, vp, vp, vp, vp]
+        lib.fp4idx_pages_from_token_table.restype = i32
         lib.fp4idx_topk_workspace_bytes.argtypes = [P, i32]
         lib.fp4idx_topk_workspace_bytes.restype = sz
         lib.fp4idx_topk.argtypes = [P, vp, i64, i32, u32, vp, vp, vp, vp, sz, vp]
@@ -155,13 +167,15 @@ class DeviceProblem:
     Fields follow include/fp4idx.h: q [T,Hq,64] u8, q_scale [T,Hq,G] u8,
     k [P,Hkv,page,64] u8, k_scale [P,Hkv,page,G] u8, cu_seqlens_q/k [B+1] i32,
     block_table [B,stride] (or flat with page_offsets [B]), visible_len [T],
-    causal, qo_offset [B]; host scalars max_seqlen_q/k.
+    causal, qo_offset [B]; host scalars max_seqlen_q/k.  kv_layout KV_FUSED:
+    k is the fused table [P,Hkv,page*(64+G)] and k_scale is None; cand_mask
+    [T,ld] u8 or None.
     """
 
     def __init__(self, *, format: int, num_heads: int, num_kv_heads: int, page_size: int,
                  q, q_scale, k, k_scale, cu_seqlens_q, cu_seqlens_k, block_table,
                  max_seqlen_q: int, max_seqlen_k: int, page_offsets=None, visible_len=None,
-                 causal: bool = False, qo_offset=None):
+                 causal: bool = False, qo_offset=None, kv_layout: int = KV_SPLIT, cand_mask=None):
         self.format = int(format)
         self.num_heads = int(num_heads)
         self.num_kv_heads = int(num_kv_heads)
@@ -171,6 +185,7 @@ class DeviceProblem:
         self.block_table, self.page_offsets = block_table, page_offsets
         self.visible_len, self.qo_offset = visible_len, qo_offset
         self.causal = bool(causal)
+        self.kv_layout, self.cand_mask = int(kv_layout), cand_mask
         self.max_seqlen_q, self.max_seqlen_k = int(max_seqlen_q), int(max_seqlen_k)
         self.num_rows = int(q.shape[0])
         self.num_seqs = int(cu_seqlens_q.shape[0]) - 1
@@ -190,7 +205,7 @@ class DeviceProblem:
             q_row_stride=int(q.stride(0)),
             q_scale_row_stride=int(q_scale.stride(0)),
             k=k.data_ptr(),
-            k_scale=k_scale.data_ptr(),
+            k_scale=None if k_scale is None else k_scale.data_ptr(),
             cu_seqlens_q=cu_seqlens_q.data_ptr(),
             cu_seqlens_k=cu_seqlens_k.data_ptr(),
             block_table=block_table.data_ptr(),
@@ -198,6 +213,9 @@ class DeviceProblem:
             visible_len=None if visible_len is None else visible_len.data_ptr(),
             causal=int(self.causal),
             qo_offset=None if qo_offset is None else qo_offset.data_ptr(),
+            kv_layout=self.kv_layout,
+            cand_mask=None if cand_mask is None else cand_mask.data_ptr(),
+            mask_ld=0 if cand_mask is None else int(cand_mask.stride(0)),
         )
 
     @property
@@ -214,9 +232,14 @@ class DeviceProblem:
             if t.dtype != dtype:
                 t = t.to(dtype)
             return t.to(device, non_blocking=non_blocking).contiguous()
+        if getattr(prob, "q_dtype", 0) != 0:
+            raise NotImplementedError("bf16 queries have no device path")
+        fused = getattr(prob, "kv_layout", 0) == KV_FUSED
         return cls(format=prob.format, num_heads=prob.num_heads, num_kv_heads=prob.num_kv_heads,
                    page_size=prob.page_size, q=dev(prob.q, torch.uint8), q_scale=dev(prob.q_scale, torch.uint8),
-                   k=dev(prob.k, torch.uint8), k_scale=dev(prob.k_scale, torch.uint8),
+                   k=dev(prob.k, torch.uint8), k_scale=None if fused else dev(prob.k_scale, torch.uint8),
+                   kv_layout=KV_FUSED if fused else KV_SPLIT,
+                   cand_mask=dev(getattr(prob, "cand_mask", None), torch.uint8),
                    cu_seqlens_q=dev(prob.cu_seqlens_q, torch.int32),
                    cu_seqlens_k=dev(prob.cu_seqlens_k, torch.int32),
                    block_table=dev(prob.block_table, torch.int32),
@@ -299,6 +322,31 @@ def fp4idx_store_k(keys: torch.Tensor, slots: torch.Tensor, page_size: int, k: t
     N, Hkv, _ = keys.shape
     _check(lib.fp4idx_store_k(_ptr(keys), keys.stride(0), N, Hkv, _ptr(slots), page_size, k.shape[0], _ptr(k),
                               _ptr(k_scale), _stream(stream)), "fp4idx_store_k")
+
+
+def fp4idx_store_k_fused(keys: torch.Tensor, slots: torch.Tensor, page_size: int, table: torch.Tensor,
+                         stream=None):
+    """fp4idx_store_k into the fused table [P, Hkv, page*68] uint8."""
+    lib = load_library()
+    N, Hkv = keys.shape[0], keys.shape[1]
+    _check(lib.fp4idx_store_k_fused(_ptr(keys), keys.stride(0), N, Hkv, _ptr(slots), page_size, table.shape[0],
+                                    _ptr(table), _stream(stream)), "fp4idx_store_k_fused")
+
+
+def fp4idx_pages_from_token_table(req: torch.Tensor, req_table: torch.Tensor, page_size: int, num_pages: int,
+                                  stream=None):
+    """(cu_seqlens_q [B+1], cu_seqlens_k [B+1], block_table [B, ceil(cap/page)]) of a per-token
+    slot table req_table [B, cap] and the rows' requests req [T] (int32, device)."""
+    lib = load_library()
+    B, cap = req_table.shape
+    dev = req_table.device
+    cu_q = torch.empty((B + 1,), dtype=torch.int32, device=dev)
+    cu_k = torch.empty((B + 1,), dtype=torch.int32, device=dev)
+    bt = torch.empty((B, (cap + page_size - 1) // page_size), dtype=torch.int32, device=dev)
+    _check(lib.fp4idx_pages_from_token_table(_ptr(req), req.shape[0], _ptr(req_table), B, req_table.stride(0),
+                                             page_size, num_pages, _ptr(cu_q), _ptr(cu_k), _ptr(bt),
+                                             _stream(stream)), "fp4idx_pages_from_token_table")
+    return cu_q, cu_k, bt
 
 
 def fp4idx_topk_workspace_bytes(problem: DeviceProblem, k: int) -> int:

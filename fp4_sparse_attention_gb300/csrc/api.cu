@@ -117,12 +117,20 @@ fp4idx_status_t check_problem(const fp4idx_problem_t* p) {
     return fail(FP4IDX_EUNSUPPORTED, "cache rows exceed 2^31");
   if (p->max_seqlen_q < 1) return fail(FP4IDX_EINVAL, "max_seqlen_q must be >= 1");
   if (p->max_seqlen_k < 0) return fail(FP4IDX_EINVAL, "max_seqlen_k must be >= 0");
-  if (!p->q || !p->q_scale || !p->k || !p->k_scale || !p->cu_seqlens_q || !p->cu_seqlens_k || !p->block_table)
-    return fail(FP4IDX_EINVAL, "q, q_scale, k, k_scale, cu_seqlens_q, cu_seqlens_k and block_table are required");
+  if (p->kv_layout != FP4IDX_KV_SPLIT && p->kv_layout != FP4IDX_KV_FUSED)
+    return fail(FP4IDX_EINVAL, "kv_layout %d is neither split (0) nor fused (1)", p->kv_layout);
+  const bool fused = p->kv_layout == FP4IDX_KV_FUSED;
+  if (!p->q || !p->q_scale || !p->k || (!fused && !p->k_scale) || !p->cu_seqlens_q || !p->cu_seqlens_k ||
+      !p->block_table)
+    return fail(FP4IDX_EINVAL, "q, q_scale, k, k_scale (split layout), cu_seqlens_q, cu_seqlens_k and block_table "
+                               "are required");
   if (!aligned(p->q, 128) || !aligned(p->k, 128))
     return fail(FP4IDX_EINVAL, "q and k must be 128-byte aligned");
-  if (!aligned(p->q_scale, 16) || !aligned(p->k_scale, 16))
+  if (!aligned(p->q_scale, 16) || (!fused && !aligned(p->k_scale, 16)))
     return fail(FP4IDX_EINVAL, "q_scale and k_scale must be 16-byte aligned");
+  if (p->cand_mask && p->mask_ld < p->max_seqlen_k)
+    return fail(FP4IDX_EINVAL, "mask_ld %lld < max_seqlen_k %d", static_cast<long long>(p->mask_ld),
+                p->max_seqlen_k);
   const int G = groups_of(p->format);
   if (p->q_row_stride < static_cast<int64_t>(p->num_heads) * 64 || p->q_row_stride % 16 != 0)
     return fail(FP4IDX_EINVAL, "q_row_stride %lld must be a multiple of 16 and >= num_heads*64",
@@ -160,16 +168,32 @@ fp4idx_status_t check_weighted(const fp4idx_problem_t* p, const float* w, int64_
   return FP4IDX_OK;
 }
 
+// TMA map of the K codes -- 3D {64 B, page, num_pages*Hkv blocks}, one box
+// per (page, K head) block -- and where each block's scales start, for
+// either cache layout.
+fp4idx_status_t k_access(const fp4idx_problem_t* pr, CUtensorMap* tmap, const uint8_t** kscale_base,
+                         int64_t* kscale_block_stride) {
+  const int G = groups_of(pr->format);
+  const int64_t page = pr->page_size;
+  const bool fused = pr->kv_layout == FP4IDX_KV_FUSED;
+  const int64_t block_bytes = fused ? page * (64 + G) : page * 64;
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(page), static_cast<cuuint64_t>(pr->num_pages) * pr->num_kv_heads};
+  cuuint64_t strides[2] = {64, static_cast<cuuint64_t>(block_bytes)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(page), 1};
+  fp4idx_status_t s = make_tmap(tmap, pr->k, 3, dims, strides, box);
+  if (s != FP4IDX_OK) return s;
+  *kscale_base = fused ? pr->k + page * 64 : pr->k_scale;
+  *kscale_block_stride = fused ? block_bytes : page * G;
+  return FP4IDX_OK;
+}
+
 // Common part of the scorer parameters.
 fp4idx_status_t fill_score_params(const fp4idx_problem_t* pr, const float* w, int64_t w_row_stride,
                                   ScoreParams* sp, int rows_per_cta, uint32_t* err) {
   std::memset(sp, 0, sizeof(*sp));
   const int G = groups_of(pr->format);
   {
-    cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(pr->num_pages) * pr->num_kv_heads * pr->page_size};
-    cuuint64_t strides[1] = {64};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(pr->page_size)};
-    fp4idx_status_t s = make_tmap(&sp->tmap_k, pr->k, 2, dims, strides, box);
+    fp4idx_status_t s = k_access(pr, &sp->tmap_k, &sp->kscale_base, &sp->kscale_block_stride);
     if (s != FP4IDX_OK) return s;
   }
   {
@@ -180,7 +204,8 @@ fp4idx_status_t fill_score_params(const fp4idx_problem_t* pr, const float* w, in
     if (s != FP4IDX_OK) return s;
   }
   (void)G;
-  sp->k_scale = pr->k_scale;
+  sp->cand_mask = pr->cand_mask;
+  sp->mask_ld = pr->mask_ld;
   sp->q_scale = pr->q_scale;
   sp->q_scale_row_stride = pr->q_scale_row_stride;
   sp->cu_seqlens_q = pr->cu_seqlens_q;
@@ -470,11 +495,17 @@ fp4idx_status_t fp4idx_logits_topk(const fp4idx_problem_t* problem, const float*
   return logits_then_select(problem, w, w_row_stride, logits, ld, k, flags, indices, values, valid_count, stream);
 }
 
-fp4idx_status_t fp4idx_store_k(const uint16_t* keys, int64_t key_row_stride, int32_t num_tokens,
-                               int32_t num_kv_heads, const int32_t* slots, int32_t page_size, int64_t num_pages,
-                               uint8_t* k, uint8_t* k_scale, void* stream) {
+}  // extern "C"
+
+namespace fp4idx {
+namespace {
+
+// Both layouts of the K-cache writer (k_scale == nullptr: the fused table).
+fp4idx_status_t store_k_any(const uint16_t* keys, int64_t key_row_stride, int32_t num_tokens,
+                            int32_t num_kv_heads, const int32_t* slots, int32_t page_size, int64_t num_pages,
+                            uint8_t* k, uint8_t* k_scale, void* stream) {
   g_msg[0] = 0;
-  if (!keys || !slots || !k || !k_scale) return fail(FP4IDX_EINVAL, "keys, slots, k or k_scale is NULL");
+  if (!keys || !slots || !k) return fail(FP4IDX_EINVAL, "keys, slots or the cache is NULL");
   if (num_tokens < 0 || num_kv_heads < 1 || num_pages < 1)
     return fail(FP4IDX_EINVAL, "num_tokens >= 0, num_kv_heads >= 1 and num_pages >= 1 required");
   if (page_size != 64 && page_size != 128) return fail(FP4IDX_EUNSUPPORTED, "page_size %d: 64 or 128", page_size);
@@ -493,6 +524,7 @@ fp4idx_status_t fp4idx_store_k(const uint16_t* keys, int64_t key_row_stride, int
   sp.slots = slots;
   sp.k = k;
   sp.k_scale = k_scale;
+  sp.fused = k_scale ? 0 : 1;
   sp.num_pages = num_pages;
   sp.num_tokens = num_tokens;
   sp.num_kv_heads = num_kv_heads;
@@ -500,6 +532,64 @@ fp4idx_status_t fp4idx_store_k(const uint16_t* keys, int64_t key_row_stride, int
   sp.err = dev->err;
   cudaError_t e = launch_store_k(sp, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "store launch");
+  return FP4IDX_OK;
+}
+
+}  // namespace
+}  // namespace fp4idx
+
+extern "C" {
+
+fp4idx_status_t fp4idx_store_k(const uint16_t* keys, int64_t key_row_stride, int32_t num_tokens,
+                               int32_t num_kv_heads, const int32_t* slots, int32_t page_size, int64_t num_pages,
+                               uint8_t* k, uint8_t* k_scale, void* stream) {
+  if (!k_scale) {
+    g_msg[0] = 0;
+    return fail(FP4IDX_EINVAL, "k_scale is NULL");
+  }
+  return store_k_any(keys, key_row_stride, num_tokens, num_kv_heads, slots, page_size, num_pages, k, k_scale,
+                     stream);
+}
+
+fp4idx_status_t fp4idx_store_k_fused(const uint16_t* keys, int64_t key_row_stride, int32_t num_tokens,
+                                     int32_t num_kv_heads, const int32_t* slots, int32_t page_size,
+                                     int64_t num_pages, uint8_t* table, void* stream) {
+  return store_k_any(keys, key_row_stride, num_tokens, num_kv_heads, slots, page_size, num_pages, table, nullptr,
+                     stream);
+}
+
+fp4idx_status_t fp4idx_pages_from_token_table(const int32_t* req, int32_t num_rows, const int32_t* req_table,
+                                              int32_t num_reqs, int64_t req_stride, int32_t page_size,
+                                              int64_t num_pages, int32_t* cu_seqlens_q, int32_t* cu_seqlens_k,
+                                              int32_t* block_table, void* stream) {
+  g_msg[0] = 0;
+  if (!req || !req_table || !cu_seqlens_q || !cu_seqlens_k || !block_table)
+    return fail(FP4IDX_EINVAL, "req, req_table, cu_seqlens_q, cu_seqlens_k and block_table are required");
+  if (num_rows < 0 || num_reqs < 1 || req_stride < 1 || num_pages < 1)
+    return fail(FP4IDX_EINVAL, "num_rows >= 0, num_reqs >= 1, req_stride >= 1 and num_pages >= 1 required");
+  if (page_size != 64 && page_size != 128) return fail(FP4IDX_EUNSUPPORTED, "page_size %d: 64 or 128", page_size);
+  if (req_stride > INT32_MAX || static_cast<int64_t>(num_reqs) * req_stride > INT32_MAX)
+    return fail(FP4IDX_EUNSUPPORTED, "more than 2^31 table entries");
+  if (num_reqs > 65535 * 64) return fail(FP4IDX_EUNSUPPORTED, "too many requests");
+  DeviceInfo* dev;
+  fp4idx_status_t s;
+  if ((s = device_info(&dev)) != FP4IDX_OK) return s;
+  TokenTableParams tp;
+  std::memset(&tp, 0, sizeof(tp));
+  tp.req = req;
+  tp.req_table = req_table;
+  tp.req_stride = req_stride;
+  tp.num_rows = num_rows;
+  tp.num_reqs = num_reqs;
+  tp.page_size = page_size;
+  tp.num_pages = num_pages;
+  tp.cu_seqlens_q = cu_seqlens_q;
+  tp.cu_seqlens_k = cu_seqlens_k;
+  tp.block_table = block_table;
+  tp.table_pages = static_cast<int32_t>((req_stride + page_size - 1) / page_size);
+  tp.err = dev->err;
+  cudaError_t e = launch_token_table(tp, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "token-table launch");
   return FP4IDX_OK;
 }
 
@@ -579,12 +669,7 @@ fp4idx_status_t fp4idx_block_scores(const fp4idx_problem_t* problem, float* scor
   if ((s = device_info(&dev)) != FP4IDX_OK) return s;
   BlockParams bp;
   std::memset(&bp, 0, sizeof(bp));
-  {
-    cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(problem->num_pages) * problem->num_kv_heads * problem->page_size};
-    cuuint64_t strides[1] = {64};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(problem->page_size)};
-    if ((s = make_tmap(&bp.tmap_k, problem->k, 2, dims, strides, box)) != FP4IDX_OK) return s;
-  }
+  if ((s = k_access(problem, &bp.tmap_k, &bp.kscale_base, &bp.kscale_block_stride)) != FP4IDX_OK) return s;
   {
     // rows (t) before heads (h) in the box: MMA row m = h_local * RT + t_local
     cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(problem->num_rows), static_cast<cuuint64_t>(problem->num_heads)};
@@ -592,7 +677,7 @@ fp4idx_status_t fp4idx_block_scores(const fp4idx_problem_t* problem, float* scor
     cuuint32_t box[3] = {64, static_cast<cuuint32_t>(1 << rt_shift), static_cast<cuuint32_t>(g)};
     if ((s = make_tmap(&bp.tmap_q, problem->q, 3, dims, strides, box)) != FP4IDX_OK) return s;
   }
-  bp.k_scale = problem->k_scale;
+
   bp.q_scale = problem->q_scale;
   bp.q_scale_row_stride = problem->q_scale_row_stride;
   bp.cu_seqlens_q = problem->cu_seqlens_q;

@@ -375,9 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
         const bool ok1 = slots == 2 && page_ok(1, phys1);
         if (lane < slots && ((lp0 + lane) << pshift) < it.k_len && !(lane == 0 ? ok0 : ok1))
           atomicOr(p.err, kErrPageRange);
-        // cache rows of the two slots (< 2^31 for resolved pages: checked on the host)
-        const int32_t row0k = ok0 ? static_cast<int32_t>((static_cast<int64_t>(phys0) * p.num_kv_heads + it.hk) << pshift) : 0;
-        const int32_t row1k = ok1 ? static_cast<int32_t>((static_cast<int64_t>(phys1) * p.num_kv_heads + it.hk) << pshift) : 0;
+        // (page, K head) blocks of the two slots (< 2^31 for resolved pages: checked on the host)
+        const int32_t row0k = ok0 ? static_cast<int32_t>(static_cast<int64_t>(phys0) * p.num_kv_heads + it.hk) : 0;
+        const int32_t row1k = ok1 ? static_cast<int32_t>(static_cast<int64_t>(phys1) * p.num_kv_heads + it.hk) : 0;
         const uint32_t bytes = static_cast<uint32_t>((ok0 ? 1 : 0) + (ok1 ? 1 : 0)) * page * (kCodeBytes + G);
         const int s = tile_iter % kStages;
         const uint32_t ph = (tile_iter / kStages) & 1u;
@@ -386,11 +386,12 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
         if (lane == 0) mbar_arrive_expect_tx(full_bar(s), bytes);
         __syncwarp();
         if (lane < slots && (lane == 0 ? ok0 : ok1)) {
-          const int32_t rowk = lane == 0 ? row0k : row1k;
-          tma_load_2d(codes_s + s * 8192 + ((lane * kCodeBytes) << pshift), &p.tmap_k, 0, rowk, full_bar(s));
+          const int32_t blk = lane == 0 ? row0k : row1k;
+          tma_load_3d(codes_s + s * 8192 + ((lane * kCodeBytes) << pshift), &p.tmap_k, 0, 0, blk, full_bar(s));
           // the page's scales are contiguous: [page keys][G]
-          bulk_load(kraw_s + s * (128 * G) + ((lane * G) << pshift), p.k_scale + static_cast<int64_t>(rowk) * G,
-                    static_cast<uint32_t>(page * G), full_bar(s));
+          bulk_load(kraw_s + s * (128 * G) + ((lane * G) << pshift),
+                    p.kscale_base + static_cast<int64_t>(blk) * p.kscale_block_stride, static_cast<uint32_t>(page * G),
+                    full_bar(s));
         }
         ++tile_iter;
       }

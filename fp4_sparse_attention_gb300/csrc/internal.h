@@ -17,9 +17,14 @@ enum Mode : int { kModeLogits = 0, kModeTopk = 1 };
 // Keys-on-M scorer: one CTA owns up to R query rows of one request (the MMA
 // N dimension is R*H) and a contiguous chunk of 128-key tiles.
 struct ScoreParams {
-  CUtensorMap tmap_k;   // 2D {64 B, num_pages*Hkv*page}, box {64, page}, 64B swizzle
+  CUtensorMap tmap_k;   // 3D {64 B, page, num_pages*Hkv blocks}, box {64, page, 1}, 64B swizzle
   CUtensorMap tmap_q;   // 3D {64 B, Hq, T}, box {64, H, R}, 64B swizzle
-  const uint8_t* k_scale;
+  // scales of (page, K head) block z: page*G bytes at kscale_base + z * kscale_block_stride
+  // (separate scale array, or the scale rows of a fused page)
+  const uint8_t* kscale_base;
+  int64_t kscale_block_stride;
+  const uint8_t* cand_mask;  // [T][mask_ld] or nullptr: 0 = not a candidate
+  int64_t mask_ld;
   const uint8_t* q_scale;
   int64_t q_scale_row_stride;
   const int32_t* cu_seqlens_q;
@@ -78,9 +83,10 @@ struct MergeParams {
 // (row m = h_local * RT + t_local, RT = 128 / g).  Tiles are the item's
 // 128-key blocks; the tiles of all items are split evenly across CTAs.
 struct BlockParams {
-  CUtensorMap tmap_k;   // 2D {64 B, num_pages*Hkv*page}, box {64, page}, 64B swizzle
+  CUtensorMap tmap_k;   // 3D {64 B, page, num_pages*Hkv blocks}, box {64, page, 1}, 64B swizzle
   CUtensorMap tmap_q;   // 3D {64 B, T (q_row_stride), Hq (64 B)}, box {64, RT, g}, 64B swizzle
-  const uint8_t* k_scale;
+  const uint8_t* kscale_base;  // as ScoreParams
+  int64_t kscale_block_stride;
   const uint8_t* q_scale;
   int64_t q_scale_row_stride;
   const int32_t* cu_seqlens_q;
@@ -122,13 +128,14 @@ cudaError_t launch_topk_merge(const MergeParams& p, int rows, bool many_rows, cu
 // Exact top-k of each row from p.sp.logits [T][p.sp.ld] (visibility from the problem).
 cudaError_t launch_topk_select(const MergeParams& p, int rows, cudaStream_t stream);
 cudaError_t launch_block_scores(const BlockParams& p, int format, dim3 grid, cudaStream_t stream);
-// MXFP4 K-cache writer (fp4idx_store_k).
+// MXFP4 K-cache writer (fp4idx_store_k, fp4idx_store_k_fused).
 struct StoreParams {
   const uint16_t* keys;     // [N][Hkv][128] bf16 words, token stride key_row_stride
   int64_t key_row_stride;
   const int32_t* slots;     // [N]
-  uint8_t* k;               // [P][Hkv][page][64]
-  uint8_t* k_scale;         // [P][Hkv][page][4]
+  uint8_t* k;               // [P][Hkv][page][64], or the fused table [P][Hkv][page*68]
+  uint8_t* k_scale;         // [P][Hkv][page][4] (nullptr with the fused table)
+  int32_t fused;
   int64_t num_pages;
   int32_t num_tokens;
   int32_t num_kv_heads;
@@ -159,6 +166,23 @@ cudaError_t launch_topk_slots(const SlotParams& p, int32_t rows, cudaStream_t st
 // Top-k blocks of each (head, row) column of [H][Kt][T] block scores, k <= 32.
 cudaError_t launch_block_topk(const float* scores, int32_t H, int32_t Kt, int32_t T, int32_t k, int32_t* indices,
                               float* values, int32_t* valid_count, cudaStream_t stream);
+
+// Cache metadata of a per-token slot table (fp4idx_pages_from_token_table).
+struct TokenTableParams {
+  const int32_t* req;        // [T]
+  const int32_t* req_table;  // [B][req_stride]
+  int64_t req_stride;
+  int32_t num_rows;
+  int32_t num_reqs;
+  int32_t page_size;
+  int64_t num_pages;
+  int32_t* cu_seqlens_q;     // [B+1]
+  int32_t* cu_seqlens_k;     // [B+1]
+  int32_t* block_table;      // [B][pages per request]
+  int32_t table_pages;       // ceil(req_stride / page_size)
+  uint32_t* err;
+};
+cudaError_t launch_token_table(const TokenTableParams& p, cudaStream_t stream);
 
 // Sets the message fp4idx_last_error_message() returns on this thread.
 void set_last_error(const char* fmt, ...);

@@ -11,6 +11,7 @@ namespace fp4idx {
 
 constexpr uint32_t kErrPageRange = 0x1u;
 constexpr uint32_t kErrTimeout = 0x2u;
+constexpr uint32_t kErrTokenTable = 0x4u;  // a per-token slot table page that is not one page in order
 // Upper bound of any single pipeline wait (ns of %globaltimer).
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
 

@@ -637,11 +637,12 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
         if (lane == 0) mbar_arrive_expect_tx(full_bar(s), bytes);
         __syncwarp();
         if (lane < slots && (lane == 0 ? ok0 : ok1)) {
-          const int32_t row = (lane == 0 ? phys0 : phys1) << pshift;  // cache row (one K head)
-          tma_load_2d(codes_s + s * 8192 + ((lane * kCodeBytes) << pshift), &p.tmap_k, 0, row, full_bar(s));
+          const int32_t blk = lane == 0 ? phys0 : phys1;  // (page, K head) block: one K head
+          tma_load_3d(codes_s + s * 8192 + ((lane * kCodeBytes) << pshift), &p.tmap_k, 0, 0, blk, full_bar(s));
           // the page's scales are contiguous: [page keys][G]
-          bulk_load(kraw_s + s * (128 * G) + ((lane * G) << pshift), p.k_scale + static_cast<int64_t>(row) * G,
-                    static_cast<uint32_t>(page * G), full_bar(s));
+          bulk_load(kraw_s + s * (128 * G) + ((lane * G) << pshift),
+                    p.kscale_base + static_cast<int64_t>(blk) * p.kscale_block_stride, static_cast<uint32_t>(page * G),
+                    full_bar(s));
         }
         FP4IDX_STAMP(2);
         FP4IDX_STAMP_COUNT();
@@ -1070,18 +1071,24 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
           ++tile_iter;
         }
         const bool page_good = pos < it.k_len && pg_cur >= 0 && pg_cur < p.num_pages;
+        // candidate mask: a cleared position is not a candidate (-inf, never selected)
+        bool cand[RG];
+#pragma unroll
+        for (int rr = 0; rr < RG; ++rr)
+          cand[rr] = !p.cand_mask || (pos < vis[rr] && __ldg(p.cand_mask + static_cast<int64_t>(t[rr]) * p.mask_ld + pos) != 0);
         if constexpr (MODE == kModeLogits) {
 #pragma unroll
           for (int rr = 0; rr < RG; ++rr)
             if (ok && row_valid[rr] && pos < p.ld)
-              p.logits[static_cast<int64_t>(t[rr]) * p.ld + pos] = page_good && pos < vis[rr] ? val[rr] : -INFINITY;
+              p.logits[static_cast<int64_t>(t[rr]) * p.ld + pos] =
+                  page_good && pos < vis[rr] && cand[rr] ? val[rr] : -INFINITY;
         } else {
 #pragma unroll
           for (int rr = 0; rr < RG; ++rr) {
             // NaN logits are never selected
             const uint64_t key = (static_cast<uint64_t>(ordered_bits(val[rr])) << 32) |
                                  static_cast<uint64_t>(~static_cast<uint32_t>(pos));
-            const bool take = ok && page_good && pos < vis[rr] && !isnan(val[rr]) && key >= thr[rr];
+            const bool take = ok && page_good && pos < vis[rr] && cand[rr] && !isnan(val[rr]) && key >= thr[rr];
             const uint32_t m = __ballot_sync(0xffffffffu, take);
             if (m) {
               // this warp's region: no other warp writes there

@@ -80,10 +80,19 @@ __global__ void __launch_bounds__(kStoreThreads) store_k_kernel(const StoreParam
     const uint32_t nib = idx | ((idx != 0 && (__float_as_uint(x[i]) >> 31)) ? 8u : 0u);
     packed[i >> 3] |= nib << (4 * (i & 7));
   }
-  const int64_t crow = (static_cast<int64_t>(slot / p.page_size) * p.num_kv_heads + hk) * p.page_size +
-                       slot % p.page_size;
-  *reinterpret_cast<uint4*>(p.k + crow * 64 + g * 16) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-  p.k_scale[crow * 4 + g] = static_cast<uint8_t>(code);
+  const int64_t blk = static_cast<int64_t>(slot / p.page_size) * p.num_kv_heads + hk;  // (page, K head)
+  const int64_t off = slot % p.page_size;
+  uint8_t* codes;
+  uint8_t* scales;
+  if (p.fused) {  // [page*64 code bytes][page*4 scale bytes] per block
+    codes = p.k + blk * p.page_size * 68 + off * 64;
+    scales = p.k + blk * p.page_size * 68 + static_cast<int64_t>(p.page_size) * 64 + off * 4;
+  } else {
+    codes = p.k + (blk * p.page_size + off) * 64;
+    scales = p.k_scale + (blk * p.page_size + off) * 4;
+  }
+  *reinterpret_cast<uint4*>(codes + g * 16) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  scales[g] = static_cast<uint8_t>(code);
 }
 
 }  // namespace

@@ -248,7 +248,11 @@ __global__ void __launch_bounds__(kMergeThreads) topk_select_kernel(const __grid
   const int M = static_cast<int>(min(static_cast<int64_t>(row_visible(p, it, t)), p.ld));
   const bool local = M <= kSelectLocal;
   const float* row_logits = p.logits + static_cast<int64_t>(t) * p.ld;
-  auto key_of = [](float v, int s) -> uint64_t { return isnan(v) ? 0ull : topk_key(v, static_cast<uint32_t>(s)); };
+  // a NaN logit or a position the candidate mask clears has no rank: key 0
+  const uint8_t* row_mask = p.cand_mask ? p.cand_mask + static_cast<int64_t>(t) * p.mask_ld : nullptr;
+  auto key_of = [&](float v, int s) -> uint64_t {
+    return isnan(v) || (row_mask && __ldg(row_mask + s) == 0) ? 0ull : topk_key(v, static_cast<uint32_t>(s));
+  };
   // the row's keys, four float4 loads in flight per thread (rows are 16-byte
   // aligned: ld % 4 == 0 and a 16-byte aligned base)
   auto for_each_global = [&](auto&& fn) {
@@ -455,7 +459,8 @@ __global__ void __launch_bounds__(kSmallThreads) topk_select_small_kernel(const 
   // Key i of this thread (position 4 (tid + 1024 (i / 4)) + i % 4) as the
   // two halves of its 64-bit top-k key: kh = order-preserving bits of the
   // logit, kl = ~position (bits 31..14 all ones, positions < 2^14).  Bit i
-  // of `present`: the position is visible and the logit not NaN.
+  // of `present`: the position is visible, not cleared by the candidate
+  // mask, and the logit not NaN.
   uint32_t kh[kSmallPer], kl[kSmallPer];
   uint32_t present = 0;
 #pragma unroll
@@ -464,7 +469,8 @@ __global__ void __launch_bounds__(kSmallThreads) topk_select_small_kernel(const 
     const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const bool ok = pos + c < M && !isnan(f[c]);
+      const bool ok = pos + c < M && !isnan(f[c]) &&
+                      (!p.cand_mask || __ldg(p.cand_mask + static_cast<int64_t>(t) * p.mask_ld + pos + c) != 0);
       const uint64_t key = topk_key(f[c], static_cast<uint32_t>(pos + c));
       kh[4 * u + c] = static_cast<uint32_t>(key >> 32);
       kl[4 * u + c] = static_cast<uint32_t>(key);

@@ -72,6 +72,14 @@ typedef enum fp4idx_status {
 /* Bits of the device error word. */
 #define FP4IDX_ERR_PAGE_RANGE 0x1u  /* block-table entry outside [0, num_pages)   */
 #define FP4IDX_ERR_TIMEOUT    0x2u  /* a pipeline wait exceeded its time limit    */
+#define FP4IDX_ERR_TOKEN_TABLE 0x4u /* fp4idx_pages_from_token_table: a page of a
+                                       request's slots is not one cache page in
+                                       order, or the rows' requests are not
+                                       non-decreasing                            */
+
+/* Key-cache layouts (fp4idx_problem_t.kv_layout). */
+#define FP4IDX_KV_SPLIT 0  /* k [P][Hkv][page][64] and k_scale [P][Hkv][page][G]     */
+#define FP4IDX_KV_FUSED 1  /* one table [P][Hkv][page*(64+G)]: codes, then scales   */
 
 /* Flags of fp4idx_topk. */
 #define FP4IDX_TOPK_SORTED 0x1u     /* order each row by (value desc, index asc)  */
@@ -98,6 +106,20 @@ typedef enum fp4idx_status {
  *            form), else b * table_stride (a [B][table_stride] table).
  *   max_seqlen_q, max_seqlen_k  host upper bounds of q_len[b], k_len[b];
  *            they size grids and outputs and must hold for the device data.
+ *
+ *   kv_layout  FP4IDX_KV_SPLIT (0): k and k_scale as above.  FP4IDX_KV_FUSED (1):
+ *            k is one table of page*(64+G) bytes per (page, K head) --
+ *            [num_pages][Hkv][page_size*(64+G)], 128-byte aligned: the page's
+ *            64-byte code rows, then its G-byte scale rows -- and k_scale is
+ *            unused (SGLang PR 42861, bench_fp4_index_scorer.py: a K table of
+ *            PAGE_SIZE * 68 bytes per page; the order inside a page is not
+ *            printed there, this is the order read).
+ *   cand_mask  NULL, or [T][mask_ld] bytes (mask_ld >= max_seqlen_k): position
+ *            s of row t is a candidate only when cand_mask[t*mask_ld + s] != 0;
+ *            other positions are -inf in the logits and never selected (the
+ *            candidate-mask argument of SGLang PR 42861's fp4_index_logits_paged,
+ *            None in its benchmark).  Used by the weighted-ReLU calls
+ *            (logits, top-k); fp4idx_block_scores ignores it.
  *
  * Visible keys of row t in request b (q_local = t - cu_seqlens_q[b]):
  *   visible_len != NULL:  vis = clamp(visible_len[t], 0, k_len[b])
@@ -132,6 +154,9 @@ typedef struct fp4idx_problem {
   const int32_t* visible_len;
   int32_t causal;
   const int32_t* qo_offset;
+  int32_t kv_layout;          /* FP4IDX_KV_SPLIT or FP4IDX_KV_FUSED (0 = split) */
+  const uint8_t* cand_mask;   /* [T][mask_ld] or NULL */
+  int64_t mask_ld;
 } fp4idx_problem_t;
 
 /*
@@ -294,6 +319,47 @@ fp4idx_status_t fp4idx_topk_noalloc(const fp4idx_problem_t* problem, const float
 fp4idx_status_t fp4idx_store_k(const uint16_t* keys, int64_t key_row_stride, int32_t num_tokens,
                                int32_t num_kv_heads, const int32_t* slots, int32_t page_size,
                                int64_t num_pages, uint8_t* k, uint8_t* k_scale, void* stream);
+
+/*
+ * The MXFP4 K-cache writer of fp4idx_store_k into the fused layout
+ * (FP4IDX_KV_FUSED): table is [num_pages][num_kv_heads][page_size * 68] bytes,
+ * 16-byte aligned; token i of K head h lands at page slots[i] / page_size,
+ * offset o = slots[i] % page_size: its 64 code bytes at o*64 and its 4 scale
+ * bytes at page_size*64 + o*4 of the (page, h) block (SGLang PR 42861: its
+ * benchmark's writer fills such a table).  Codes, scales, slot rules and errors
+ * are those of fp4idx_store_k.
+ */
+fp4idx_status_t fp4idx_store_k_fused(const uint16_t* keys, int64_t key_row_stride, int32_t num_tokens,
+                                     int32_t num_kv_heads, const int32_t* slots, int32_t page_size,
+                                     int64_t num_pages, uint8_t* table, void* stream);
+
+/*
+ * This ABI's request metadata from a per-token slot table (SGLang PR 42861,
+ * fp4_index_logits_paged's req / req_table arguments):
+ *   req        [num_rows] int32, device: the request of each query row; the
+ *              rows of a request must be contiguous, requests non-decreasing.
+ *   req_table  [num_reqs][req_stride] int32, device: the cache slot (page *
+ *              page_size + offset) of every logical position, < 0 for none.
+ * Writes, on the device:
+ *   cu_seqlens_q  [num_reqs + 1]: rows per request, from req.
+ *   cu_seqlens_k  [num_reqs + 1]: keys per request = 1 + the last position
+ *              with a slot >= 0.
+ *   block_table   [num_reqs][ceil(req_stride / page_size)]: logical page j of
+ *              request b is cache page req_table[b][j*page_size] / page_size
+ *              when the slots of its positions below the request's key count
+ *              are that page's offsets in order (the layout the benchmark's
+ *              writer produces); otherwise -1, and FP4IDX_ERR_TOKEN_TABLE is
+ *              set (the scorer then treats that page's keys as absent and sets
+ *              FP4IDX_ERR_PAGE_RANGE).  Also -1 for a page with no slot.
+ * A problem with these arrays, table_stride = ceil(req_stride / page_size),
+ * max_seqlen_k = req_stride, and the rows' lens as visible_len scores what
+ * fp4_index_logits_paged scores.  Graph-capturable; no workspace.  EINVAL for
+ * NULL pointers or non-positive sizes, EUNSUPPORTED for page_size not 64/128.
+ */
+fp4idx_status_t fp4idx_pages_from_token_table(const int32_t* req, int32_t num_rows, const int32_t* req_table,
+                                              int32_t num_reqs, int64_t req_stride, int32_t page_size,
+                                              int64_t num_pages, int32_t* cu_seqlens_q, int32_t* cu_seqlens_k,
+                                              int32_t* block_table, void* stream);
 
 /*
  * Physical cache slots of selected positions, for a sparse-attention consumer
