@@ -335,3 +335,23 @@ def store_k(keys_bf16, slots, page_size: int, k, k_scale):
     assert k.flags.c_contiguous and k_scale.flags.c_contiguous
     sl = np.ascontiguousarray(np.asarray(slots, dtype=np.int32))
     _load().orc_store_k(_ptr(keys), Hkv * 128, N, Hkv, _ptr(sl), page_size, k.shape[0], _ptr(k), _ptr(k_scale))
+
+
+def quantize_q(q_bf16):
+    """Quantise bf16 queries (raw words [T, Hq, 128], uint16) to MXFP4 codes
+    [T, Hq, 64] and E8M0 scales [T, Hq, 4] (uint8) by the K writer's rule
+    (SGLang PR 42861, "Modifications": E2M1 levels [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    with round-to-nearest-even, E8M0 exponents clamped to 1..254; the scale
+    exponent floor(log2 max|x|) - 2 of a 32-value group is the OCP
+    microscaling rule).  Each query row is written as if it were a cache
+    token on a one-token page of its own: the cache arrays of orc_store_k
+    with page_size 1 and slot t for row t are exactly [T, Hq, 64] / [T, Hq, 4].
+    The PR scores bf16 queries without quantising them; this step is the
+    framework's reading for running them on the FP4 tensor cores."""
+    q = np.ascontiguousarray(np.asarray(q_bf16, dtype=np.uint16))
+    T, H, D = q.shape
+    assert D == 128
+    codes = np.zeros((T, H, 1, 64), np.uint8)
+    scales = np.zeros((T, H, 1, 4), np.uint8)
+    store_k(q, np.arange(T, dtype=np.int32), 1, codes, scales)
+    return codes.reshape(T, H, 64), scales.reshape(T, H, 4)

@@ -5,6 +5,7 @@ Each test checks the oracle against one of: values the pages print
 on independently dequantised operands), a closed form, a brute-force
 computation on tiny inputs, or an invariant of the definition.
 """
+import dataclasses
 import math
 
 import numpy as np
@@ -622,3 +623,66 @@ def test_bf16_queries_match_library_matmul():
         d = qv[t] @ keys.T  # [H, vis]
         lg = (b.w[t].astype(np.float64)[:, None] * np.maximum(d, 0.0)).sum(axis=0)
         np.testing.assert_array_equal(got[t, : vis[t]], lg.astype(np.float32))
+
+
+# ---------------------------------------------------------------------------
+# bf16 queries quantised to MXFP4 (the K writer's rule applied per query row)
+# ---------------------------------------------------------------------------
+
+def test_quantize_q_hand_worked_group():
+    # group max 1.0: floor(log2 1) - 2 = -2, code 125, scale 1/4; the scaled
+    # values 4, -2.5, 1.5, 0.5, 0.25, -3.5, 3 go to levels 4 (index 6),
+    # 2 (tie 2|3 -> even index 4, sign), 1.5 (3), 0.5 (1), 0 (tie 0|0.5 ->
+    # index 0), 4 (tie 3|4 -> even index 6, sign) and 3 (5)
+    x = np.zeros((1, 2, 128), np.float32)
+    x[0, 1, 32:39] = [1.0, -0.625, 0.375, 0.125, 0.0625, -0.875, 0.75]
+    codes, scales = oracle.quantize_q(_bf16(x))
+    assert codes.shape == (1, 2, 64) and scales.shape == (1, 2, 4)
+    assert scales[0, 1].tolist() == [1, 125, 1, 1] and scales[0, 0].tolist() == [1, 1, 1, 1]
+    assert codes[0, 1, 16:20].tolist() == [0xC6, 0x13, 0xE0, 0x05]
+    assert not codes[0, 0].any() and not codes[0, 1, :16].any() and not codes[0, 1, 20:].any()
+
+
+def test_quantize_q_rows_and_heads_land_in_query_layout():
+    # row t, head h of the output is what the cache writer stores for a token
+    # holding those 128 values
+    rng = np.random.default_rng(21)
+    x = (rng.integers(-8, 9, size=(3, 4, 128)) / 8.0 * 2.0 ** rng.integers(-3, 4, size=(3, 4, 1))).astype(np.float32)
+    codes, scales = oracle.quantize_q(_bf16(x))
+    for t in range(3):
+        for h in range(4):
+            nib, sc = _store_one(x[t, h])
+            assert sc.tolist() == scales[t, h].tolist()
+            assert np.stack([codes[t, h] & 0xF, codes[t, h] >> 4], axis=1).reshape(-1).tolist() == nib.tolist()
+
+
+def _dequant_q(codes, scales):
+    lv = np.array([oracle.e2m1(c) for c in range(16)])
+    nib = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(*codes.shape[:-1], 128)
+    sc = np.array([oracle.e8m0(int(c)) for c in range(256)])[scales]  # [..., 4]
+    return lv[nib] * np.repeat(sc, 32, axis=-1)
+
+
+def test_quantized_query_scores_stay_within_the_quantisation_bound():
+    # relu is 1-Lipschitz, so |logit(q) - logit(Q(q))| <= sum_h |w_h| *
+    # sum_d |q_d - Q(q)_d| |k_d|, with both logits from the oracle (the
+    # exact bf16 one and the one on the quantised codes)
+    p = _small(q_lens=[3], k_lens=[200])
+    b = wl.with_bf16_queries(p, seed=8)
+    qv = torch.from_numpy(b.q.astype(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    codes, scales = oracle.quantize_q(b.q)
+    dq = _dequant_q(codes, scales)
+    err = np.abs(qv - dq)
+    assert err.max() > 0  # the pages' dyadic queries are not all on the E2M1 grid
+    qz = dataclasses.replace(b, q=codes, q_scale=scales, q_dtype=0)
+    exact, _, _ = oracle.logits_rows(b, 200)
+    quant, _, _ = oracle.logits_rows(qz, 200)
+    kd = _dequant(b.k, b.k_scale, b.format)
+    vis = oracle.visible_all(b)
+    for t in range(b.num_rows):
+        keys = np.stack([kd[b.block_table[0, s // 64], 0, s % 64] for s in range(vis[t])])
+        bound = (np.abs(b.w[t].astype(np.float64))[:, None] * (err[t] @ np.abs(keys).T)).sum(axis=0)
+        e, z = exact[t, : vis[t]].astype(np.float64), quant[t, : vis[t]].astype(np.float64)
+        # plus one float32 rounding of each stored logit
+        assert np.all(np.abs(e - z) <= bound + 2.0 ** -23 * (np.abs(e) + np.abs(z)))
+        assert np.all(np.isneginf(quant[t, vis[t]:]))
