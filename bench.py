@@ -161,6 +161,11 @@ WORKLOADS = {
     "logits16k": dict(maker="verify_decode_16k", kind="logits", k=0, logits=True, bound="hbm"),
     "logits100k": dict(maker="verify_decode_100k", kind="logits", k=0, logits=True, bound="hbm"),
     "logits400k": dict(maker="verify_decode_400k", kind="logits", k=0, logits=True, bound="hbm"),
+    # SGLang PR 42861's full call: bf16 queries quantised, the per-token slot
+    # table turned into request metadata, fused-table logits
+    "p1_paged16k": dict(maker="p1_paged_16k", kind="paged", k=0, logits=True, bound="hbm"),
+    "p1_paged100k": dict(maker="p1_paged_100k", kind="paged", k=0, logits=True, bound="hbm"),
+    "p1_paged400k": dict(maker="p1_paged_400k", kind="paged", k=0, logits=True, bound="hbm"),
 }
 
 
@@ -230,6 +235,9 @@ class OursBench:
         self.k = spec["k"]
         self.block = spec["kind"] == "block"
         self.store = spec["kind"] == "store"
+        if spec["kind"] == "paged":
+            self._init_paged()
+            return
         base = B.DeviceProblem.from_host(host, device=device)
         T = base.num_rows
         self.w = None if host.w is None else torch.as_tensor(host.w).to(device)
@@ -289,8 +297,51 @@ class OursBench:
         self.graphs = []
         self.events = []
 
+    def _init_paged(self):
+        """Per copy: bf16 queries, the fused table, req / req_table / lens and
+        w as inputs; the quantised queries and the request metadata as the
+        step's own intermediate buffers."""
+        torch, B, host, device = self.torch, self.B, self.host, self.device
+        T, H = host.num_rows, host.num_heads
+        nb, cap = host.req_table.shape
+        npg = (cap + host.page_size - 1) // host.page_size
+        dev = lambda a: torch.as_tensor(a).to(device).contiguous()
+        src = dict(qb=dev(host.q.view(np.int16)).view(torch.bfloat16), table=dev(host.k), req=dev(host.req),
+                   rt=dev(host.req_table), lens=dev(host.visible_len), w=dev(host.w))
+        self.input_bytes = sum(t.numel() * t.element_size() for t in src.values())
+        self.copies = 1 if self.input_bytes >= 2 * L2_BYTES else int(min(512, -(-2 * L2_BYTES // self.input_bytes)))
+        self.sets, self.problems = [], []
+        for c in range(self.copies):
+            st = dict(src) if c == 0 else {n: t.clone() for n, t in src.items()}
+            st["codes"] = torch.empty((T, H, 64), dtype=torch.uint8, device=device)
+            st["scales"] = torch.empty((T, H, 4), dtype=torch.uint8, device=device)
+            st["cu_q"] = torch.empty((nb + 1,), dtype=torch.int32, device=device)
+            st["cu_k"] = torch.empty((nb + 1,), dtype=torch.int32, device=device)
+            st["bt"] = torch.empty((nb, npg), dtype=torch.int32, device=device)
+            st["prob"] = B.DeviceProblem(
+                format=host.format, num_heads=H, num_kv_heads=host.num_kv_heads, page_size=host.page_size,
+                q=st["codes"], q_scale=st["scales"], k=st["table"], k_scale=None, kv_layout=B.KV_FUSED,
+                cu_seqlens_q=st["cu_q"], cu_seqlens_k=st["cu_k"], block_table=st["bt"], visible_len=st["lens"],
+                max_seqlen_q=T, max_seqlen_k=cap)
+            self.sets.append(st)
+            self.problems.append(st["prob"])
+        self.ld = cap
+        self.logits = torch.empty((T, cap), dtype=torch.float32, device=device)
+        self.kernels = ["quantize_q", "token_table", "scorer_logits"]
+        self.launches_per_step = 5  # the token table takes three kernels
+        self.graphs, self.events = [], []
+
+    def _paged_calls(self, st):
+        B, host = self.B, self.host
+        return [lambda: B.fp4idx_quantize_q(st["qb"], st["codes"], st["scales"]),
+                lambda: B.fp4idx_pages_from_token_table(st["req"], st["rt"], host.page_size, host.k.shape[0],
+                                                        out=(st["cu_q"], st["cu_k"], st["bt"])),
+                lambda: B.fp4idx_logits(st["prob"], st["w"], out=self.logits)]
+
     def _calls(self, n):
         B = self.B
+        if self.spec["kind"] == "paged":
+            return self._paged_calls(self.sets[n])
         prob, w = self.problems[n], self.ws_list[n]
         if self.store:
             return [lambda: B.fp4idx_store_k(self.keys, self.slots, prob.page_size, prob.k, prob.k_scale)]
@@ -333,20 +384,39 @@ class OursBench:
                 self._step(n)
         torch.cuda.current_stream(self.device).wait_stream(s)
         torch.cuda.synchronize(self.device)
+        # the timed graphs hold the step's kernels alone (event-record nodes
+        # between them would break the programmatic-launch overlap of
+        # consecutive kernels); a second set, with an event-record node after
+        # every call, gives the per-kernel times
         self.timed_nodes = True
         for n in range(len(self.problems)):
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(self.launches_per_step + 1)]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self._step(n)
+            self.graphs.append(g)
+        self.probe_graphs = []
+        for n in range(min(len(self.problems), 64)):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(self.kernels) + 1)]
             for e in evs:  # torch creates the CUDA event lazily, on its first record
                 e.record(s)
             torch.cuda.synchronize(self.device)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
                 self.timed_nodes &= self._step(n, evs)
-            self.graphs.append(g)
+            self.probe_graphs.append(g)
             self.events.append(evs)
 
     def run(self, j: int):
         self.graphs[j % len(self.graphs)].replay()
+
+    def run_probes(self, steps: int) -> int:
+        """Replay the instrumented graphs (inputs rotated as in the timed
+        region); returns how many replays the event times cover."""
+        used = min(steps, len(self.probe_graphs))
+        for j in range(used):
+            self.probe_graphs[j].replay()
+        self.torch.cuda.synchronize(self.device)
+        return used
 
     def kernel_times_ms(self, used: int) -> dict:
         """Mean device time of each kernel of the step over the timed replays,
@@ -385,6 +455,8 @@ class OursBench:
     def e2e(self, steps: int) -> dict:
         torch = self.torch
         B = self.B
+        if self.spec["kind"] == "paged":
+            return self._e2e_paged(steps)
         prob = self.problems[0]
         d_in = [prob.q, prob.q_scale, prob.block_table] + ([self.w] if self.w is not None else []) + (
             [prob.visible_len] if prob.visible_len is not None else [])
@@ -436,6 +508,33 @@ class OursBench:
         return {"ms": start.elapsed_time(end), "wall_s": wall, "h2d": bi, "d2h": bo}
 
 
+    def _e2e_paged(self, steps: int) -> dict:
+        """The PR's call from pinned host buffers: bf16 queries, req,
+        req_table, lens and w copied in every step (the fused table is
+        resident cache state), the logits read back."""
+        torch = self.torch
+        st = self.sets[0]
+        d_in = [st["qb"], st["req"], st["rt"], st["lens"], st["w"]]
+        h_in = [t.cpu().pin_memory() for t in d_in]
+        h_out = torch.empty(self.logits.shape, dtype=self.logits.dtype, pin_memory=True)
+        bi = sum(t.numel() * t.element_size() for t in h_in)
+        bo = h_out.numel() * h_out.element_size()
+        calls = self._paged_calls(st)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(self.device)
+        t0 = time.perf_counter()
+        start.record()
+        for _ in range(steps):
+            for h, d in zip(h_in, d_in):
+                d.copy_(h, non_blocking=True)
+            for call in calls:
+                call()
+            h_out.copy_(self.logits, non_blocking=True)
+        end.record()
+        torch.cuda.synchronize(self.device)
+        return {"ms": start.elapsed_time(end), "wall_s": time.perf_counter() - t0, "h2d": bi, "d2h": bo}
+
+
 def kernel_algorithmic_bytes(host, name: str, k: int) -> int:
     """Algorithmic HBM bytes of one launch.  Scorer kernels: the K codes +
     scales of every key a request can see (each read once per request), Q
@@ -450,9 +549,16 @@ def kernel_algorithmic_bytes(host, name: str, k: int) -> int:
         keys += int(vis[r0:r1].max()) if r1 > r0 else 0
     kv = keys * kv_bytes_per_key(host.format) * host.num_kv_heads
     T, H = host.q.shape[0], host.num_heads
-    qb = host.q.nbytes + host.q_scale.nbytes + (T * H * 4 if host.w is not None else 0)
+    # the scorer reads FP4 query codes and scales (bf16 queries: after quantisation)
+    qcodes = T * H * (64 + (4 if host.format == 0 else 8))
+    qb = qcodes + (T * H * 4 if host.w is not None else 0)
     if name in ("scorer_logits", "scorer_topk", "logits_topk", "block_scores"):
         return kv + qb
+    if name == "quantize_q":  # bf16 queries read, codes + scales written
+        return T * H * (256 + 68)
+    if name == "token_table":  # req and the slot table read, metadata written
+        nb, cap = host.req_table.shape
+        return T * 4 + nb * cap * 4 + 2 * (nb + 1) * 4 + nb * ((cap + host.page_size - 1) // host.page_size) * 4
     if name == "topk_merge":
         return T * k * 8 + T * 4
     if name == "store_k":  # bf16 keys read, codes + scales written, per token and K head
@@ -542,10 +648,11 @@ def oracle_sample(host, spec):
                 oracle.block_topk(sc, bk)
         what = f"row {row} ({vis} visible keys): its block maxima for all {host.num_heads} heads" + \
             (f" and their top-{bk} blocks" if bk else "")
-    elif spec["kind"] == "logits":
+    elif spec["kind"] in ("logits", "paged"):
         def step():
             oracle.logits_rows(op, vis, rows=[row])
-        what = f"row {row} ({vis} visible keys): its full logits"
+        what = f"row {row} ({vis} visible keys): its full logits" + (
+            " (bf16 queries, per-token slot table, fused table)" if spec["kind"] == "paged" else "")
     else:
         def step():
             if spec["logits"]:
@@ -674,11 +781,11 @@ def run_ours(args, world, rank, local):
         barrier(world)
     ms = start.elapsed_time(end)
     ms_max = reduce_max(ms, world)
-    kt_method = "event-record nodes inside the timed step graphs"
+    kt_method = "event-record nodes after every call, in copies of the step graphs replayed after the timed region"
     try:
         if not bench.timed_nodes:
             raise RuntimeError("event-record nodes unavailable")
-        kt = bench.kernel_times_ms(min(args.steps, len(bench.graphs)))
+        kt = bench.kernel_times_ms(bench.run_probes(max(args.steps, 16)))
     except RuntimeError:
         kt = bench.kernel_times_isolated_ms()
         kt_method = "each kernel back to back in single-kernel graphs"
@@ -703,6 +810,9 @@ def run_ours(args, world, rank, local):
             (f" + top-{spec['block_k']} blocks per (head, row)" if spec.get("block_k") else "")
     elif spec["kind"] == "logits":
         step_desc = f"full logits [{host.q.shape[0]}, {(host.max_seqlen_k + 3) // 4 * 4}] (no top-k)"
+    elif spec["kind"] == "paged":
+        step_desc = (f"bf16 queries quantised + per-token slot table to request metadata + full logits "
+                     f"[{host.q.shape[0]}, {host.req_table.shape[1]}] from the fused table")
     elif spec.get("fused"):
         step_desc = f"logits + top-{spec['k']} in one call (scorer logits, per-row selection from them)"
     else:

@@ -42,6 +42,7 @@ EXPORTED = (
     "fp4idx_topk_slots",
     "fp4idx_store_k",
     "fp4idx_store_k_fused",
+    "fp4idx_quantize_q",
     "fp4idx_pages_from_token_table",
     "fp4idx_topk_workspace_bytes",
     "fp4idx_topk",
@@ -121,6 +122,8 @@ def load_library(path: str = LIB_PATH):
         lib.fp4idx_store_k.restype = i32
         lib.fp4idx_store_k_fused.argtypes = [vp, i64, i32, i32, vp, i32, i64, vp, vp]
         lib.fp4idx_store_k_fused.restype = i32
+        lib.fp4idx_quantize_q.argtypes = [vp, i64, i32, i32, vp, vp, vp]
+        lib.fp4idx_quantize_q.restype = i32
         lib.fp4idx_pages_from_token_table.argtypes = [vp, i32, vp, i32, i64, i32, i64, vp, vp, vp, vp]
         lib.fp4idx_pages_from_token_table.restype = i32
         lib.fp4idx_topk_workspace_bytes.argtypes = [P, i32]
@@ -233,10 +236,16 @@ class DeviceProblem:
                 t = t.to(dtype)
             return t.to(device, non_blocking=non_blocking).contiguous()
         if getattr(prob, "q_dtype", 0) != 0:
-            raise NotImplementedError("bf16 queries have no device path")
+            # bf16 queries: quantised on the device (MXFP4 problems only)
+            if prob.format != 0:
+                raise ValueError("bf16 queries need the MXFP4 format")
+            qb = torch.as_tensor(prob.q.view("int16")).to(device).view(torch.bfloat16).contiguous()
+            q, q_scale = fp4idx_quantize_q(qb)
+        else:
+            q, q_scale = dev(prob.q, torch.uint8), dev(prob.q_scale, torch.uint8)
         fused = getattr(prob, "kv_layout", 0) == KV_FUSED
         return cls(format=prob.format, num_heads=prob.num_heads, num_kv_heads=prob.num_kv_heads,
-                   page_size=prob.page_size, q=dev(prob.q, torch.uint8), q_scale=dev(prob.q_scale, torch.uint8),
+                   page_size=prob.page_size, q=q, q_scale=q_scale,
                    k=dev(prob.k, torch.uint8), k_scale=None if fused else dev(prob.k_scale, torch.uint8),
                    kv_layout=KV_FUSED if fused else KV_SPLIT,
                    cand_mask=dev(getattr(prob, "cand_mask", None), torch.uint8),
@@ -333,16 +342,42 @@ def fp4idx_store_k_fused(keys: torch.Tensor, slots: torch.Tensor, page_size: int
                                     _ptr(table), _stream(stream)), "fp4idx_store_k_fused")
 
 
+def fp4idx_quantize_q(q: torch.Tensor, codes: Optional[torch.Tensor] = None,
+                      scales: Optional[torch.Tensor] = None, stream=None):
+    """MXFP4 codes [T, H, 64] and E8M0 scales [T, H, 4] (uint8) of bf16 queries q [T, H, 128]."""
+    lib = load_library()
+    T, H, D = q.shape
+    if q.dtype != torch.bfloat16 or D != 128 or q.stride(2) != 1 or q.stride(1) != 128:
+        raise ValueError("q must be bfloat16 [T, H, 128] with dense heads")
+    if codes is None:
+        codes = torch.empty((T, H, 64), dtype=torch.uint8, device=q.device)
+    if scales is None:
+        scales = torch.empty((T, H, 4), dtype=torch.uint8, device=q.device)
+    if tuple(codes.shape) != (T, H, 64) or tuple(scales.shape) != (T, H, 4) or not (
+            codes.is_contiguous() and scales.is_contiguous()):
+        raise ValueError("codes [T, H, 64] and scales [T, H, 4], contiguous")
+    _check(lib.fp4idx_quantize_q(_ptr(q), q.stride(0), T, H, _ptr(codes), _ptr(scales), _stream(stream)),
+           "fp4idx_quantize_q")
+    return codes, scales
+
+
 def fp4idx_pages_from_token_table(req: torch.Tensor, req_table: torch.Tensor, page_size: int, num_pages: int,
-                                  stream=None):
+                                  out=None, stream=None):
     """(cu_seqlens_q [B+1], cu_seqlens_k [B+1], block_table [B, ceil(cap/page)]) of a per-token
-    slot table req_table [B, cap] and the rows' requests req [T] (int32, device)."""
+    slot table req_table [B, cap] and the rows' requests req [T] (int32, device); `out` may
+    give the three tensors to write."""
     lib = load_library()
     B, cap = req_table.shape
     dev = req_table.device
-    cu_q = torch.empty((B + 1,), dtype=torch.int32, device=dev)
-    cu_k = torch.empty((B + 1,), dtype=torch.int32, device=dev)
-    bt = torch.empty((B, (cap + page_size - 1) // page_size), dtype=torch.int32, device=dev)
+    if out is None:
+        cu_q = torch.empty((B + 1,), dtype=torch.int32, device=dev)
+        cu_k = torch.empty((B + 1,), dtype=torch.int32, device=dev)
+        bt = torch.empty((B, (cap + page_size - 1) // page_size), dtype=torch.int32, device=dev)
+    else:
+        cu_q, cu_k, bt = out
+        if tuple(bt.shape) != (B, (cap + page_size - 1) // page_size) or cu_q.numel() != B + 1 or \
+                cu_k.numel() != B + 1:
+            raise ValueError("out: cu_seqlens_q [B+1], cu_seqlens_k [B+1], block_table [B, ceil(cap/page)]")
     _check(lib.fp4idx_pages_from_token_table(_ptr(req), req.shape[0], _ptr(req_table), B, req_table.stride(0),
                                              page_size, num_pages, _ptr(cu_q), _ptr(cu_k), _ptr(bt),
                                              _stream(stream)), "fp4idx_pages_from_token_table")

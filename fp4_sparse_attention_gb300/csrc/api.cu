@@ -558,6 +558,38 @@ fp4idx_status_t fp4idx_store_k_fused(const uint16_t* keys, int64_t key_row_strid
                      stream);
 }
 
+fp4idx_status_t fp4idx_quantize_q(const uint16_t* q, int64_t q_row_stride, int32_t num_rows, int32_t num_heads,
+                                  uint8_t* q_codes, uint8_t* q_scale, void* stream) {
+  g_msg[0] = 0;
+  if (!q || !q_codes || !q_scale) return fail(FP4IDX_EINVAL, "q, q_codes or q_scale is NULL");
+  if (num_rows < 0 || num_heads < 1) return fail(FP4IDX_EINVAL, "num_rows >= 0 and num_heads >= 1 required");
+  if (q_row_stride < static_cast<int64_t>(num_heads) * 128 || q_row_stride % 8 != 0)
+    return fail(FP4IDX_EINVAL, "q_row_stride must be >= num_heads * 128 and a multiple of 8");
+  if (!aligned(q, 16) || !aligned(q_codes, 16)) return fail(FP4IDX_EINVAL, "q and q_codes must be 16-byte aligned");
+  if (num_rows == 0) return FP4IDX_OK;
+  DeviceInfo* dev;
+  fp4idx_status_t s;
+  if ((s = device_info(&dev)) != FP4IDX_OK) return s;
+  // each query row is a token on a one-token page of its own: the cache
+  // arrays [rows][heads][1][64] / [rows][heads][1][4] are the query layout
+  StoreParams sp;
+  std::memset(&sp, 0, sizeof(sp));
+  sp.keys = q;
+  sp.key_row_stride = q_row_stride;
+  sp.slots = nullptr;
+  sp.k = q_codes;
+  sp.k_scale = q_scale;
+  sp.fused = 0;
+  sp.num_pages = num_rows;
+  sp.num_tokens = num_rows;
+  sp.num_kv_heads = num_heads;
+  sp.page_size = 1;
+  sp.err = dev->err;
+  cudaError_t e = launch_store_k(sp, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return FP4IDX_OK;
+}
+
 fp4idx_status_t fp4idx_pages_from_token_table(const int32_t* req, int32_t num_rows, const int32_t* req_table,
                                               int32_t num_reqs, int64_t req_stride, int32_t page_size,
                                               int64_t num_pages, int32_t* cu_seqlens_q, int32_t* cu_seqlens_k,
@@ -570,7 +602,8 @@ fp4idx_status_t fp4idx_pages_from_token_table(const int32_t* req, int32_t num_ro
   if (page_size != 64 && page_size != 128) return fail(FP4IDX_EUNSUPPORTED, "page_size %d: 64 or 128", page_size);
   if (req_stride > INT32_MAX || static_cast<int64_t>(num_reqs) * req_stride > INT32_MAX)
     return fail(FP4IDX_EUNSUPPORTED, "more than 2^31 table entries");
-  if (num_reqs > 65535 * 64) return fail(FP4IDX_EUNSUPPORTED, "too many requests");
+  if ((req_stride + page_size - 1) / page_size > 65535 * 8)
+    return fail(FP4IDX_EUNSUPPORTED, "more than 524,280 pages per request");  // grid.y of the page pass
   DeviceInfo* dev;
   fp4idx_status_t s;
   if ((s = device_info(&dev)) != FP4IDX_OK) return s;

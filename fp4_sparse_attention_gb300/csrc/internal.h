@@ -128,11 +128,12 @@ cudaError_t launch_topk_merge(const MergeParams& p, int rows, bool many_rows, cu
 // Exact top-k of each row from p.sp.logits [T][p.sp.ld] (visibility from the problem).
 cudaError_t launch_topk_select(const MergeParams& p, int rows, cudaStream_t stream);
 cudaError_t launch_block_scores(const BlockParams& p, int format, dim3 grid, cudaStream_t stream);
-// MXFP4 K-cache writer (fp4idx_store_k, fp4idx_store_k_fused).
+// MXFP4 K-cache writer (fp4idx_store_k, fp4idx_store_k_fused) and query
+// quantiser (fp4idx_quantize_q: no slots, one-token pages).
 struct StoreParams {
   const uint16_t* keys;     // [N][Hkv][128] bf16 words, token stride key_row_stride
   int64_t key_row_stride;
-  const int32_t* slots;     // [N]
+  const int32_t* slots;     // [N], or nullptr: token i at slot i
   uint8_t* k;               // [P][Hkv][page][64], or the fused table [P][Hkv][page*68]
   uint8_t* k_scale;         // [P][Hkv][page][4] (nullptr with the fused table)
   int32_t fused;

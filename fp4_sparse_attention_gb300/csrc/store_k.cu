@@ -1,6 +1,9 @@
 // store_k.cu -- MXFP4 K-cache writer: bf16 keys -> E2M1 codes + E8M0 scales
 // in the paged cache layout (SGLang PR 42861: store_fp4_index_k_cache with
-// round-to-nearest-even; E8M0 exponents clamped to 1..254).
+// round-to-nearest-even; E8M0 exponents clamped to 1..254).  With no slot
+// table (slots == nullptr) token i goes to slot i; on one-token pages that
+// is the dense query layout [T][H][64] / [T][H][4], which is how bf16
+// queries are quantised (fp4idx_quantize_q).
 //
 // One thread per 32-value group of one (token, K head) row: four 16-byte
 // loads of bf16, the group's max magnitude, the shared exponent from its
@@ -8,6 +11,8 @@
 // comparisons against the midpoints between levels (a tie goes to the level
 // with the even index, i.e. the even mantissa), 16 bytes of codes and one
 // scale byte stored.  Memory-bound: 64 bytes read, 17 written per group.
+#include <cstring>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -31,6 +36,8 @@ __device__ __forceinline__ uint32_t e2m1_rne_index(float a) {
 }
 
 __global__ void __launch_bounds__(kStoreThreads) store_k_kernel(const StoreParams p) {
+  pdl_wait();  // the keys may come from the kernel before this one
+  pdl_launch_dependents();
   const int64_t gidx = static_cast<int64_t>(blockIdx.x) * kStoreThreads + threadIdx.x;
   const int64_t groups = static_cast<int64_t>(p.num_tokens) * p.num_kv_heads * 4;
   if (gidx >= groups) return;
@@ -38,9 +45,9 @@ __global__ void __launch_bounds__(kStoreThreads) store_k_kernel(const StoreParam
   const int64_t row = gidx >> 2;  // token * Hkv + head
   const int64_t tok = row / p.num_kv_heads;
   const int hk = static_cast<int>(row - tok * p.num_kv_heads);
-  const int32_t slot = __ldg(p.slots + tok);
+  const int64_t slot = p.slots ? static_cast<int64_t>(__ldg(p.slots + tok)) : tok;
   if (slot < 0) return;
-  if (static_cast<int64_t>(slot) >= p.num_pages * p.page_size) {
+  if (slot >= p.num_pages * p.page_size) {
     if (g == 0 && hk == 0) atomicOr(p.err, kErrPageRange);
     return;
   }
@@ -101,8 +108,19 @@ cudaError_t launch_store_k(const StoreParams& p, cudaStream_t stream) {
   const int64_t groups = static_cast<int64_t>(p.num_tokens) * p.num_kv_heads * 4;
   if (groups == 0) return cudaSuccess;
   const unsigned grid = static_cast<unsigned>((groups + kStoreThreads - 1) / kStoreThreads);
-  store_k_kernel<<<grid, kStoreThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the next kernel may be scheduled while
+  // this one runs (it waits for this one's writes with griddepcontrol.wait)
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kStoreThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, store_k_kernel, p);
 }
 
 }  // namespace fp4idx

@@ -4,14 +4,18 @@
 // request of query row t and req_table[b][s] the cache slot (page * page_size
 // + offset) of logical position s of request b.
 //
-// Three launches, no workspace (cu_seqlens_k carries the per-request key
-// counts between the first two):
-//   1. per request: its key count = 1 + the last position with a slot >= 0;
+// Two launches, no workspace, chained by programmatic dependent launch:
+//   1. one warp per (request, logical page): the page's slots must be one
+//      cache page's offsets in order, followed only by empty entries (< 0);
+//      its block-table entry is that page, -1 for a page with no slot, and
+//      -1 with FP4IDX_ERR_TOKEN_TABLE otherwise.  An empty entry followed by
+//      a filled one is reported too.  The page holding the request's last
+//      filled position (found locally: the next page starts empty) writes
+//      the request's key count, 1 + that position, to cu_seqlens_k[b + 1].
 //   2. one CTA: the prefix sums of the key counts, and each request's first
-//      row (binary search in req, which must be non-decreasing);
-//   3. per (request, logical page): the page's slots below the key count
-//      must be one cache page's offsets in order; then the block-table entry
-//      is that page, else -1 (FP4IDX_ERR_TOKEN_TABLE).
+//      row (binary search in req, which must be non-decreasing).
+#include <cstring>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -19,27 +23,57 @@ namespace fp4idx {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kPagesPerCta = kThreads / 32;
 
-// cu_seqlens_k[b + 1] = key count of request b (the prefix sum comes next).
-__global__ void __launch_bounds__(kThreads) token_counts_kernel(const TokenTableParams p) {
+__global__ void __launch_bounds__(kThreads) token_pages_kernel(const TokenTableParams p) {
+  pdl_wait();  // the table may come from the kernel before this one
+  pdl_launch_dependents();
   const int b = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int j = blockIdx.y * kPagesPerCta + static_cast<int>(threadIdx.x >> 5);
+  if (j >= p.table_pages) return;
   const int32_t* row = p.req_table + static_cast<int64_t>(b) * p.req_stride;
-  int32_t last = -1;
-  for (int64_t s = threadIdx.x; s < p.req_stride; s += kThreads)
-    if (__ldg(row + s) >= 0) last = static_cast<int32_t>(s);
-  last = __reduce_max_sync(0xffffffffu, last);
-  __shared__ int32_t wmax[kThreads / 32];
-  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = last;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int32_t m = -1;
-    for (int w = 0; w < kThreads / 32; ++w) m = max(m, wmax[w]);
-    p.cu_seqlens_k[b + 1] = m + 1;
+  const int64_t s0 = static_cast<int64_t>(j) * p.page_size;
+  const int per = p.page_size / 32;  // 2 or 4 entries per lane
+  int32_t v[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int64_t s = s0 + u * 32 + lane;  // coalesced: one 128-byte line per u
+    v[u] = (u < per && s < p.req_stride) ? __ldg(row + s) : -1;  // past the table: empty
   }
+  const int32_t first = __shfl_sync(0xffffffffu, v[0], 0);
+  int last_filled = -1, first_empty = p.page_size;
+  bool ordered = true;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    if (u >= per) break;
+    const int i = u * 32 + lane;
+    if (v[u] >= 0) {
+      last_filled = max(last_filled, i);
+      ordered &= v[u] == first + i;
+    } else {
+      first_empty = min(first_empty, i);
+    }
+  }
+  last_filled = __reduce_max_sync(0xffffffffu, last_filled);
+  first_empty = __reduce_min_sync(0xffffffffu, first_empty);
+  ordered = __all_sync(0xffffffffu, ordered);
+  if (lane != 0) return;
+  const int64_t next_s = s0 + p.page_size;
+  const int32_t next_first = next_s < p.req_stride ? __ldg(row + next_s) : -1;
+  const bool any = last_filled >= 0;
+  const bool good = any && ordered && last_filled < first_empty && first % p.page_size == 0 &&
+                    first / p.page_size < p.num_pages;
+  p.block_table[static_cast<int64_t>(b) * p.table_pages + j] = good ? first / p.page_size : -1;
+  const bool hole = first_empty < p.page_size && next_first >= 0;  // an empty entry before a filled one
+  if ((any && !good) || hole) atomicOr(p.err, kErrTokenTable);
+  if ((any || j == 0) && next_first < 0) p.cu_seqlens_k[b + 1] = static_cast<int32_t>(s0 + last_filled + 1);
 }
 
 // One CTA: prefix sums of the key counts; the first row of every request.
 __global__ void __launch_bounds__(kThreads) token_offsets_kernel(const TokenTableParams p) {
+  pdl_wait();  // the key counts come from token_pages_kernel
+  pdl_launch_dependents();
   __shared__ int32_t carry;
   if (threadIdx.x == 0) {
     carry = 0;
@@ -86,36 +120,28 @@ __global__ void __launch_bounds__(kThreads) token_offsets_kernel(const TokenTabl
   }
 }
 
-// Block-table entry of logical page blockIdx.x of request blockIdx.y.
-__global__ void __launch_bounds__(128) token_pages_kernel(const TokenTableParams p) {
-  const int j = blockIdx.x, b = blockIdx.y;
-  const int32_t klen = p.cu_seqlens_k[b + 1] - p.cu_seqlens_k[b];
-  const int64_t s0 = static_cast<int64_t>(j) * p.page_size;
-  const int32_t* row = p.req_table + static_cast<int64_t>(b) * p.req_stride;
-  const int32_t first = s0 < klen ? __ldg(row + s0) : -1;
-  bool good = first >= 0 && first % p.page_size == 0 && first / p.page_size < p.num_pages;
-  for (int i = threadIdx.x; i < p.page_size; i += 128) {
-    const int64_t s = s0 + i;
-    if (s < klen && __ldg(row + s) != first + i) good = false;
-  }
-  good = __syncthreads_and(good);
-  if (threadIdx.x == 0) {
-    const bool any = s0 < klen;
-    p.block_table[static_cast<int64_t>(b) * p.table_pages + j] = any && good ? first / p.page_size : -1;
-    if (any && !good) atomicOr(p.err, kErrTokenTable);
-  }
+template <class K>
+cudaError_t launch_pdl(K kern, dim3 grid, cudaStream_t stream, const TokenTableParams& p) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace
 
 cudaError_t launch_token_table(const TokenTableParams& p, cudaStream_t stream) {
-  token_counts_kernel<<<p.num_reqs, kThreads, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  const dim3 grid(static_cast<unsigned>(p.num_reqs), static_cast<unsigned>((p.table_pages + kPagesPerCta - 1) / kPagesPerCta));
+  cudaError_t e = launch_pdl(token_pages_kernel, grid, stream, p);
   if (e != cudaSuccess) return e;
-  token_offsets_kernel<<<1, kThreads, 0, stream>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  token_pages_kernel<<<dim3(p.table_pages, p.num_reqs), 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(token_offsets_kernel, dim3(1), stream, p);
 }
 
 }  // namespace fp4idx

@@ -99,6 +99,10 @@ class Problem:
             "max_seqlen_k": self.max_seqlen_k,
             "cache_pages": self.num_pages,
             "topk": self.topk,
+            **({"kv_layout": "fused (page * (64 + G) bytes per page and K head)"} if self.kv_layout == 1 else {}),
+            **({"metadata": "per-token slot table (req, req_table, lens)"} if self.req_table is not None else {}),
+            **({"queries": "bf16, quantised to MXFP4 on the device"} if self.q_dtype == 1 else {}),
+            **({"candidate_mask": "yes"} if self.cand_mask is not None else {}),
         }
 
 
@@ -390,6 +394,25 @@ def with_bf16_queries(p: Problem, seed: int) -> Problem:
     vals = rng.integers(-8, 9, size=(p.num_rows, p.num_heads, 128)).astype(np.float32) / 8
     words = (vals.view(np.uint32) >> 16).astype(np.uint16)  # exact: these values need 4 mantissa bits
     return dataclasses.replace(p, name=p.name + "_bf16q", q=words, q_dtype=1)
+
+
+def _p1_paged(p: Problem) -> Problem:
+    """SGLang PR 42861's full call on one of its benchmark contexts: bf16
+    queries, the fused 68-byte-per-token table, a per-token slot table with
+    cap = context + 64 columns and the rows' lens."""
+    return with_bf16_queries(token_table(fused_pages(p)), seed=719)
+
+
+def p1_paged_16k() -> Problem:
+    return _p1_paged(verify_decode_16k())
+
+
+def p1_paged_100k() -> Problem:
+    return _p1_paged(verify_decode_100k())
+
+
+def p1_paged_400k() -> Problem:
+    return _p1_paged(verify_decode_400k())
 
 
 # E4M3 codes of the hand-built NaN case (bias 7): 0x28 = 0.25, 0x30 = 0.5,

@@ -334,6 +334,28 @@ fp4idx_status_t fp4idx_store_k_fused(const uint16_t* keys, int64_t key_row_strid
                                      int64_t num_pages, uint8_t* table, void* stream);
 
 /*
+ * Quantise bf16 queries to the MXFP4 query operand of fp4idx_problem_t
+ * (format FP4IDX_MXFP4).  SGLang PR 42861's fp4_index_logits_paged takes
+ * bf16 queries and multiplies them with the dequantised keys; this library
+ * runs every contraction on the FP4 tensor cores, so bf16 queries are first
+ * quantised here, group by group, by the rule of fp4idx_store_k (E8M0 code
+ * clamp(floor(log2 max|x|) - 2 + 127, 1, 254) per 32 values, each value
+ * rounded to the nearest E2M1 level, ties to even, saturating at 6).  The
+ * scores then differ from the bf16-query ones by at most
+ * sum_h |w[t,h]| * sum_d |q - Q(q)|_d * |k_d| (ReLU is 1-Lipschitz).
+ *   q        [num_rows][num_heads][128] bfloat16 words, device; q_row_stride =
+ *            elements between rows (>= num_heads * 128, a multiple of 8);
+ *            16-byte aligned.  Finite.
+ *   q_codes  [num_rows][num_heads][64] uint8, device, 16-byte aligned: the
+ *            problem's q (two E2M1 codes per byte, low nibble first).
+ *   q_scale  [num_rows][num_heads][4] uint8, device: the problem's q_scale.
+ * Graph-capturable, no workspace; one launch (none for num_rows == 0).
+ * EINVAL on NULL pointers, sizes, strides or misalignment.
+ */
+fp4idx_status_t fp4idx_quantize_q(const uint16_t* q, int64_t q_row_stride, int32_t num_rows, int32_t num_heads,
+                                  uint8_t* q_codes, uint8_t* q_scale, void* stream);
+
+/*
  * This ABI's request metadata from a per-token slot table (SGLang PR 42861,
  * fp4_index_logits_paged's req / req_table arguments):
  *   req        [num_rows] int32, device: the request of each query row; the
@@ -343,7 +365,7 @@ fp4idx_status_t fp4idx_store_k_fused(const uint16_t* keys, int64_t key_row_strid
  * Writes, on the device:
  *   cu_seqlens_q  [num_reqs + 1]: rows per request, from req.
  *   cu_seqlens_k  [num_reqs + 1]: keys per request = 1 + the last position
- *              with a slot >= 0.
+ *              with a slot >= 0 (in a table that passes the checks below).
  *   block_table   [num_reqs][ceil(req_stride / page_size)]: logical page j of
  *              request b is cache page req_table[b][j*page_size] / page_size
  *              when the slots of its positions below the request's key count
@@ -351,10 +373,15 @@ fp4idx_status_t fp4idx_store_k_fused(const uint16_t* keys, int64_t key_row_strid
  *              writer produces); otherwise -1, and FP4IDX_ERR_TOKEN_TABLE is
  *              set (the scorer then treats that page's keys as absent and sets
  *              FP4IDX_ERR_PAGE_RANGE).  Also -1 for a page with no slot.
+ *              A position without a slot (< 0) followed, in the same request,
+ *              by one with a slot sets FP4IDX_ERR_TOKEN_TABLE as well; with a
+ *              reported table the key count is that of one of its pages.
  * A problem with these arrays, table_stride = ceil(req_stride / page_size),
  * max_seqlen_k = req_stride, and the rows' lens as visible_len scores what
- * fp4_index_logits_paged scores.  Graph-capturable; no workspace.  EINVAL for
- * NULL pointers or non-positive sizes, EUNSUPPORTED for page_size not 64/128.
+ * fp4_index_logits_paged scores.  Graph-capturable; no workspace; two
+ * launches.  EINVAL for NULL pointers or non-positive sizes, EUNSUPPORTED for
+ * page_size not 64/128, more than 2^31 table entries or more than 524,280
+ * pages per request.
  */
 fp4idx_status_t fp4idx_pages_from_token_table(const int32_t* req, int32_t num_rows, const int32_t* req_table,
                                               int32_t num_reqs, int64_t req_stride, int32_t page_size,

@@ -204,3 +204,22 @@ def test_fused_writer_matches_oracle(page, Hkv):
     torch.cuda.synchronize()
     assert B.fp4idx_get_error(clear=True) == 0
     np.testing.assert_array_equal(table.cpu().numpy(), want)
+
+
+def test_token_table_holes_and_empty_requests():
+    # request 1 has no slot at all (key count 0, every page -1, no report);
+    # a table with an empty entry before a filled one is reported
+    p = _ragged(wl.MXFP4, 8)
+    t = wl.token_table(p)
+    t.req_table[1, :] = -1
+    B.fp4idx_get_error(clear=True)
+    _, cu_q, cu_k, bt = _table_problem(t)
+    assert B.fp4idx_get_error(clear=True) == 0
+    assert cu_k[2] - cu_k[1] == 0 and (bt[1] == -1).all()
+    assert cu_k[1] == p.k_lens[0] and cu_k[3] - cu_k[2] == p.k_lens[2]
+    h = wl.token_table(p)
+    h.req_table[2, 700] = -1  # a hole inside request 2's keys
+    B.fp4idx_get_error(clear=True)
+    _, _, cu_k, bt = _table_problem(h)
+    assert B.fp4idx_get_error(clear=True) & B.ERR_TOKEN_TABLE
+    assert bt[2, 700 // 64] == -1
