@@ -88,7 +88,7 @@ fp4idx_status_t make_tmap(CUtensorMap* m, const void* base, int rank, const cuui
   EncodeTiledFn fn;
   fp4idx_status_t s = encode_fn(&fn);
   if (s != FP4IDX_OK) return s;
-  cuuint32_t elem[3] = {1, 1, 1};
+  cuuint32_t elem[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), dims, strides, box, elem,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -168,19 +168,32 @@ fp4idx_status_t check_weighted(const fp4idx_problem_t* p, const float* w, int64_
   return FP4IDX_OK;
 }
 
-// TMA map of the K codes -- 3D {64 B, page, num_pages*Hkv blocks}, one box
-// per (page, K head) block -- and where each block's scales start, for
-// either cache layout.
+// TMA map of the K codes and where each (page, K head) block's scales
+// start, for either cache layout.  Plain: 3D {64 B, page, num_pages*Hkv
+// blocks}, one box per block.  Strided (the MXFP4 scorer): 4D {64 B, 4,
+// page / 4, blocks} with strides {64 B, 256 B, block}, one box per (block,
+// c) holding keys c, c + 4, c + 8, ... of the page -- the key order in
+// which the page's raw scale bytes form the scale-factor layout the MMA
+// reads (see score_kernel.cuh).
 fp4idx_status_t k_access(const fp4idx_problem_t* pr, CUtensorMap* tmap, const uint8_t** kscale_base,
-                         int64_t* kscale_block_stride) {
+                         int64_t* kscale_block_stride, bool strided = false) {
   const int G = groups_of(pr->format);
   const int64_t page = pr->page_size;
   const bool fused = pr->kv_layout == FP4IDX_KV_FUSED;
   const int64_t block_bytes = fused ? page * (64 + G) : page * 64;
-  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(page), static_cast<cuuint64_t>(pr->num_pages) * pr->num_kv_heads};
-  cuuint64_t strides[2] = {64, static_cast<cuuint64_t>(block_bytes)};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(page), 1};
-  fp4idx_status_t s = make_tmap(tmap, pr->k, 3, dims, strides, box);
+  const cuuint64_t blocks = static_cast<cuuint64_t>(pr->num_pages) * pr->num_kv_heads;
+  fp4idx_status_t s;
+  if (strided) {
+    cuuint64_t dims[4] = {64, 4, static_cast<cuuint64_t>(page / 4), blocks};
+    cuuint64_t strides[3] = {64, 256, static_cast<cuuint64_t>(block_bytes)};
+    cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(page / 4), 1};
+    s = make_tmap(tmap, pr->k, 4, dims, strides, box);
+  } else {
+    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(page), blocks};
+    cuuint64_t strides[2] = {64, static_cast<cuuint64_t>(block_bytes)};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(page), 1};
+    s = make_tmap(tmap, pr->k, 3, dims, strides, box);
+  }
   if (s != FP4IDX_OK) return s;
   *kscale_base = fused ? pr->k + page * 64 : pr->k_scale;
   *kscale_block_stride = fused ? block_bytes : page * G;
@@ -193,7 +206,8 @@ fp4idx_status_t fill_score_params(const fp4idx_problem_t* pr, const float* w, in
   std::memset(sp, 0, sizeof(*sp));
   const int G = groups_of(pr->format);
   {
-    fp4idx_status_t s = k_access(pr, &sp->tmap_k, &sp->kscale_base, &sp->kscale_block_stride);
+    fp4idx_status_t s = k_access(pr, &sp->tmap_k, &sp->kscale_base, &sp->kscale_block_stride,
+                                 pr->format == FP4IDX_MXFP4);
     if (s != FP4IDX_OK) return s;
   }
   {

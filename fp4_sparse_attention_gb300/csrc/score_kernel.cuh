@@ -107,6 +107,14 @@ template <int H, int R, int FMT, int MODE>
 struct ScoreLayout {
   static constexpr int G = FmtTraits<FMT>::G;
   static constexpr int kAtoms = FmtTraits<FMT>::kAtoms;
+  // MXFP4: the K tile's codes arrive in the strided key order (MMA row
+  // m = 32c + l holds key 4l + c), so the tile's raw scale bytes -- 128
+  // keys x 4 B, as the pages hold them -- already are the 32-line atom the
+  // MMA reads (line l, word c = key 4l + c = row 32c + l).  The MMA thread
+  // copies them into TMEM itself: no scale warp work per tile, no shared-
+  // memory staging.  NVFP4's 8 scale bytes per key do not line up that way
+  // and keep the scale warps' per-tile transposition.
+  static constexpr bool kDirectSf = FMT == 0;
   // Top-k with two rows per CTA (64 heads): each row's candidate buffer
   // lives in shared memory (a compaction then reads and writes it at
   // shared-memory latency), kCandCap keys per row -- large, so that a row
@@ -120,7 +128,7 @@ struct ScoreLayout {
   // Everything but the K ring, and the ring: as deep as shared memory allows
   // (a loaded HBM round trip for a random page is ~2 us, so ~70+ KB in
   // flight per SM), at most 20 stages.
-  static constexpr uint32_t kFixedBytes = 2 * (((H * R * 64 + 1023) / 1024) * 1024) + 4 * kAtoms * 2048 +
+  static constexpr uint32_t kFixedBytes = 2 * (((H * R * 64 + 1023) / 1024) * 1024) + (kDirectSf ? 0 : 4 * kAtoms * 2048) +
                                           2 * kAtoms * 512 + 4096 + (160 + kEpiThreads * 4) * 4 + 4 * 1280 +
                                           (MODE == kModeTopk ? R * kHistBins * 2 : 0) + kCandBytes + 2048;
   static constexpr int kStagesFit = static_cast<int>((232448u - 1024u - kFixedBytes) / (8192u + 128u * G)) & ~1;
@@ -143,7 +151,7 @@ struct ScoreLayout {
   // used where that leaves the epilogue enough registers.
   static constexpr int kEpiWarp0 = 3;
   static constexpr int kProducer2Warp = kEpiWarp0 + 4 * kGroups;
-  static constexpr int kScaleWarps = (kProducer2Warp + 1) % 4 == 0 ? 1 : 2;
+  static constexpr int kScaleWarps = kDirectSf || (kProducer2Warp + 1) % 4 == 0 ? 1 : 2;
   static constexpr int kScale2Warp = kProducer2Warp + 1;
   static constexpr int kWarpsUsed = kProducer2Warp + kScaleWarps;
   static constexpr int kThreads = ((kWarpsUsed + 3) / 4) * 4 * 32;
@@ -152,14 +160,16 @@ struct ScoreLayout {
   static_assert(kStages % 2 == 0, "the two producers own alternate stages");
   static constexpr int N = H * R;
   static_assert(N % 16 == 0 && N >= 16 && N <= 128, "MMA N");
-  // K-scale slots (TMEM and shared staging): tile i uses slot i % kSfaSlots
-  static constexpr int kSfaSlots = 4;
+  // K-scale slots (TMEM and shared staging): tile i uses slot i % kSfaSlots;
+  // direct scales use the accumulator's index (the accumulator's release
+  // then also frees the slot)
+  static constexpr int kSfaSlots = kDirectSf ? kAccBufs : 4;
   static constexpr uint32_t kCodes = 0;                                  // kStages x 8 KB
   static constexpr uint32_t kQBytes = ((N * 64 + 1023) / 1024) * 1024;
   static constexpr uint32_t kQ = kCodes + kStages * 8192;                // 2 x N x 64 B (double buffered)
   static constexpr uint32_t kKraw = kQ + 2 * kQBytes;                    // kStages x 128 keys x G raw K scales
   static constexpr uint32_t kSfaRows = kKraw + kStages * 128 * G;        // kSfaSlots x kAtoms x 2048 (128 rows)
-  static constexpr uint32_t kSfb = kSfaRows + kSfaSlots * kAtoms * 2048; // 2 x kAtoms x 512 Q-scale atoms
+  static constexpr uint32_t kSfb = kSfaRows + (kDirectSf ? 0 : kSfaSlots * kAtoms * 2048); // 2 x kAtoms x 512 Q-scale atoms
   static constexpr uint32_t kBars = kSfb + 2 * kAtoms * 512;             // mbarriers
   static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 4 + kSfaSlots + 2;
   static constexpr uint32_t kState = kBars + kNumBars * 8;
@@ -636,7 +646,20 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
         if (!ok) return;
         if (lane == 0) mbar_arrive_expect_tx(full_bar(s), bytes);
         __syncwarp();
-        if (lane < slots && (lane == 0 ? ok0 : ok1)) {
+        if constexpr (L::kDirectSf) {
+          // codes in the strided key order: lane 4 sl + c copies keys c, c+4,
+          // ... of page slot sl (page / 4 of them) to rows 32c + (page / 4) sl
+          if (lane < 4 * slots) {
+            const int sl = lane >> 2, c = lane & 3;
+            if (sl == 0 ? ok0 : ok1)
+              tma_load_4d(codes_s + s * 8192 + ((32 * c + (page >> 2) * sl) * kCodeBytes), &p.tmap_k, 0, c, 0,
+                          sl == 0 ? phys0 : phys1, full_bar(s));
+          }
+          if (lane < slots && (lane == 0 ? ok0 : ok1))
+            bulk_load(kraw_s + s * (128 * G) + ((lane * G) << pshift),
+                      p.kscale_base + static_cast<int64_t>(lane == 0 ? phys0 : phys1) * p.kscale_block_stride,
+                      static_cast<uint32_t>(page * G), full_bar(s));
+        } else if (lane < slots && (lane == 0 ? ok0 : ok1)) {
           const int32_t blk = lane == 0 ? phys0 : phys1;  // (page, K head) block: one K head
           tma_load_3d(codes_s + s * 8192 + ((lane * kCodeBytes) << pshift), &p.tmap_k, 0, 0, blk, full_bar(s));
           // the page's scales are contiguous: [page keys][G]
@@ -692,16 +715,28 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
           const int slot = tile_iter % L::kSfaSlots;
           const int a = tile_iter % kAccBufs;
           const uint32_t aph = (tile_iter / kAccBufs) & 1u;
-          // a scale warp copied this tile's K scales after the stage's codes
-          // landed
           FP4IDX_STAMP(3);
-          if (!(ok = mbar_wait(sfready_bar(slot), (sf_phase >> slot) & 1u, abort_flag, p.err))) break;
+          if constexpr (L::kDirectSf) {
+            // the stage's codes and raw scales landed
+            if (!(ok = mbar_wait(full_bar(s), (tile_iter / kStages) & 1u, abort_flag, p.err))) break;
+          } else {
+            // a scale warp copied this tile's K scales after the stage's
+            // codes landed
+            if (!(ok = mbar_wait(sfready_bar(slot), (sf_phase >> slot) & 1u, abort_flag, p.err))) break;
+            sf_phase ^= 1u << slot;
+          }
           FP4IDX_STAMP(0);
-          sf_phase ^= 1u << slot;
           if (!(ok = mbar_wait(acce_bar(a), aph ^ 1u, abort_flag, p.err))) break;
           FP4IDX_STAMP(1);
           tc_fence_after();
           const uint32_t sfa_t = tmem + L::kSfaCol + slot * 8u;
+          if constexpr (L::kDirectSf) {
+            // slot == a: the MMA that last read it finished before the
+            // epilogue released accumulator a; the copy completes before
+            // the MMAs below read it (tcgen05 operations of one thread run
+            // in issue order)
+            tc_cp_32x128b_warpx4(sfa_t, desc_sf_atom(kraw_s + s * (128 * G)));
+          }
           const uint32_t d = tmem + L::kAccCol + a * 128u;
           const uint64_t adesc = a_desc0 + static_cast<uint64_t>((s * 8192) >> 4);
 #pragma unroll
@@ -740,7 +775,8 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
     // only): the Q scales of its rows -> 32x4x4 atoms -> TMEM slot item % 2
     // (free: the producer loaded this item's Q only after the MMAs of
     // item - 2 completed), committed to the item's Q-scale barrier.  Per
-    // tile: raw K scales [128 keys][G] -> 128
+    // tile (NVFP4 only: MXFP4 scales go from the stage to TMEM by the MMA
+    // thread): raw K scales [128 keys][G] -> 128
     // rows of the scale layout (row r holds atom line r % 32: the words of
     // keys l, 32+l, 64+l, 96+l, l = r % 32; NVFP4's second K half in the
     // second 16 bytes), one tcgen05.cp 128x128b/256b into TMEM slot
@@ -781,6 +817,10 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
         __syncwarp();
       }
       FP4IDX_STAMP(0);
+      if constexpr (L::kDirectSf) {  // the MMA thread copies the K scales
+        ++item_iter;
+        return;
+      }
       for (int j = lo; j < hi; ++j) {
         if (MODE == kModeLogits && !tile_has_visible(it, j)) continue;
         if ((tile_iter & smask) != sidx) {  // the other scale warp's tile
@@ -845,7 +885,7 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
       // copies still in flight must land before TMEM is released
       volatile int never = 0;
       const uint32_t first = tile_iter > static_cast<uint32_t>(L::kSfaSlots) ? tile_iter - L::kSfaSlots : 0;
-      for (uint32_t u = first; u < tile_iter; ++u)
+      for (uint32_t u = first; u < tile_iter && !L::kDirectSf; ++u)
         if ((u & smask) == sidx) mbar_wait(sfready_bar(u % L::kSfaSlots), (u / L::kSfaSlots) & 1u, &never, p.err);
       if (sidx == 0 && item_iter > 0) {
         const uint32_t u = item_iter - 1;
@@ -863,7 +903,9 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
     Group<kEpiThreads, -1> g{static_cast<int>(threadIdx.x) - 32 * L::kEpiWarp0 - gi * kEpiThreads, 1 + gi};
     SelectScratch* gsc = sc + gi;
     const int quad = warp & 3;
-    const int key_local = quad * 32 + lane;
+    // key of this thread's accumulator lane 32 quad + lane within the tile
+    // (MXFP4: the strided order of the producer's code boxes)
+    const int key_local = L::kDirectSf ? 4 * lane + quad : quad * 32 + lane;
     // Candidate buffer of each row (shared memory for two-row CTAs, else the
     // workspace), ccap keys laid out as
     //   [0, seg0)                       keys kept by the last compaction
@@ -1012,18 +1054,23 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
         const int32_t lp = b + lane;
         return lp < npages ? __ldg(p.block_table + it.table_base + lp) : -1;
       };
-      int32_t pbase = ((lo << 7) + quad * 32) >> p.page_shift & ~31;
+      int32_t pbase = ((lo << 7) >> p.page_shift) & ~31;
       int32_t ids_cur = fetch_ids(pbase), ids_next = fetch_ids(pbase + 32);
       FP4IDX_STAMP(0);
       for (int j = lo; j < hi; ++j) {
         const int32_t pos = (j << 7) + key_local;
-        const int32_t lp = ((j << 7) + quad * 32) >> p.page_shift;  // warp-uniform
-        if (lp >= pbase + 32) {
+        const int32_t lp0 = (j << 7) >> p.page_shift;  // the tile's first page (warp-uniform)
+        if (lp0 >= pbase + 32) {
           pbase += 32;
           ids_cur = ids_next;
           ids_next = fetch_ids(pbase + 32);
         }
-        const int32_t pg_cur = __shfl_sync(0xffffffffu, ids_cur, lp - pbase);
+        // this lane's page: lp0 or, with 64-key pages, lp0 + 1 (then
+        // possibly the first of the next 32)
+        const int32_t d = (pos >> p.page_shift) - pbase;
+        const int32_t id_a = __shfl_sync(0xffffffffu, ids_cur, d & 31);
+        const int32_t id_b = __shfl_sync(0xffffffffu, ids_next, d & 31);
+        const int32_t pg_cur = d < 32 ? id_a : id_b;
         const bool real = !(MODE == kModeLogits && !tile_has_visible(it, j));
         float val[RG];
 #pragma unroll
