@@ -168,32 +168,19 @@ fp4idx_status_t check_weighted(const fp4idx_problem_t* p, const float* w, int64_
   return FP4IDX_OK;
 }
 
-// TMA map of the K codes and where each (page, K head) block's scales
-// start, for either cache layout.  Plain: 3D {64 B, page, num_pages*Hkv
-// blocks}, one box per block.  Strided (the MXFP4 scorer): 4D {64 B, 4,
-// page / 4, blocks} with strides {64 B, 256 B, block}, one box per (block,
-// c) holding keys c, c + 4, c + 8, ... of the page -- the key order in
-// which the page's raw scale bytes form the scale-factor layout the MMA
-// reads (see score_kernel.cuh).
+// TMA map of the K codes -- 3D {64 B, page, num_pages*Hkv blocks}, one box
+// per (page, K head) block -- and where each block's scales start, for
+// either cache layout.
 fp4idx_status_t k_access(const fp4idx_problem_t* pr, CUtensorMap* tmap, const uint8_t** kscale_base,
-                         int64_t* kscale_block_stride, bool strided = false) {
+                         int64_t* kscale_block_stride) {
   const int G = groups_of(pr->format);
   const int64_t page = pr->page_size;
   const bool fused = pr->kv_layout == FP4IDX_KV_FUSED;
   const int64_t block_bytes = fused ? page * (64 + G) : page * 64;
-  const cuuint64_t blocks = static_cast<cuuint64_t>(pr->num_pages) * pr->num_kv_heads;
-  fp4idx_status_t s;
-  if (strided) {
-    cuuint64_t dims[4] = {64, 4, static_cast<cuuint64_t>(page / 4), blocks};
-    cuuint64_t strides[3] = {64, 256, static_cast<cuuint64_t>(block_bytes)};
-    cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(page / 4), 1};
-    s = make_tmap(tmap, pr->k, 4, dims, strides, box);
-  } else {
-    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(page), blocks};
-    cuuint64_t strides[2] = {64, static_cast<cuuint64_t>(block_bytes)};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(page), 1};
-    s = make_tmap(tmap, pr->k, 3, dims, strides, box);
-  }
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(page), static_cast<cuuint64_t>(pr->num_pages) * pr->num_kv_heads};
+  cuuint64_t strides[2] = {64, static_cast<cuuint64_t>(block_bytes)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(page), 1};
+  fp4idx_status_t s = make_tmap(tmap, pr->k, 3, dims, strides, box);
   if (s != FP4IDX_OK) return s;
   *kscale_base = fused ? pr->k + page * 64 : pr->k_scale;
   *kscale_block_stride = fused ? block_bytes : page * G;
@@ -206,9 +193,13 @@ fp4idx_status_t fill_score_params(const fp4idx_problem_t* pr, const float* w, in
   std::memset(sp, 0, sizeof(*sp));
   const int G = groups_of(pr->format);
   {
-    fp4idx_status_t s = k_access(pr, &sp->tmap_k, &sp->kscale_base, &sp->kscale_block_stride,
-                                 pr->format == FP4IDX_MXFP4);
-    if (s != FP4IDX_OK) return s;
+    // codes and scales of each (page, K head) block, either cache layout
+    const int64_t page = pr->page_size;
+    const bool fused = pr->kv_layout == FP4IDX_KV_FUSED;
+    sp->kcode_base = pr->k;
+    sp->kcode_block_stride = fused ? page * (64 + G) : page * 64;
+    sp->kscale_base = fused ? pr->k + page * 64 : pr->k_scale;
+    sp->kscale_block_stride = fused ? page * (64 + G) : page * G;
   }
   {
     cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(pr->num_heads), static_cast<cuuint64_t>(pr->num_rows)};
@@ -217,7 +208,6 @@ fp4idx_status_t fill_score_params(const fp4idx_problem_t* pr, const float* w, in
     fp4idx_status_t s = make_tmap(&sp->tmap_q, pr->q, 3, dims, strides, box);
     if (s != FP4IDX_OK) return s;
   }
-  (void)G;
   sp->cand_mask = pr->cand_mask;
   sp->mask_ld = pr->mask_ld;
   sp->q_scale = pr->q_scale;
@@ -255,8 +245,15 @@ int topk_ctas(const fp4idx_problem_t* p, int sms) {
 }
 
 struct TopkWorkspace {
-  size_t keys_off, count_off, cand_off, start_off, bytes;
+  size_t keys_off, count_off, cand_off, start_off, pool_off, pool_bytes, bytes;
 };
+
+// Whether the streaming top-k pools its bucket counts across CTAs: rows
+// scored by four-row CTAs (their keys spread over many CTAs), few enough
+// rows that the counts (8 KB a row) are cheap to clear.
+bool use_pool(const fp4idx_problem_t* p) {
+  return score_rows_per_cta(p->num_heads) == 4 && p->num_rows <= kPoolMaxRows;
+}
 
 // Short-context plan of fp4idx_topk: logits into the workspace, then a
 // per-row selection.  Decided from host scalars only.
@@ -278,7 +275,9 @@ TopkWorkspace topk_workspace(const fp4idx_problem_t* p, int32_t k, int sms) {
   ws.count_off = up(static_cast<size_t>(slots) * topk_part_capacity(k) * 8);
   ws.cand_off = ws.count_off + up(static_cast<size_t>(slots) * 4);
   ws.start_off = ws.cand_off + up(static_cast<size_t>(ctas) * R * topk_cand_capacity(k) * 8);
-  ws.bytes = ws.start_off + up(static_cast<size_t>(items + 1) * 4);
+  ws.pool_off = ws.start_off + up(static_cast<size_t>(items + 1) * 4);
+  ws.pool_bytes = use_pool(p) ? up(static_cast<size_t>(p->num_rows) * (kPoolBins + 1) * 4) : 0;
+  ws.bytes = ws.pool_off + ws.pool_bytes;
   // the short-context plan keeps the logits [T][ld] at offset 0 instead
   if (use_logits_plan(p)) {
     const size_t lb = up(static_cast<size_t>(p->num_rows) * logits_plan_ld(p) * 4);
@@ -384,6 +383,10 @@ fp4idx_status_t topk_prepare(const fp4idx_problem_t* problem, const float* w, in
   sp->cand = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(workspace) + ws.cand_off);
   sp->item_start = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + ws.start_off);
   sp->item_overhead = kTopkItemOverhead;
+  if (ws.pool_bytes) {
+    sp->pool_hist = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + ws.pool_off);
+    sp->pool_top = sp->pool_hist + static_cast<size_t>(problem->num_rows) * kPoolBins;
+  }
   *ctas = topk_ctas(problem, dev->sms);
   if (*ctas >= kMaxMergeSlots) return fail(FP4IDX_EUNSUPPORTED, "more than %d SMs", kMaxMergeSlots - 1);
   sp->score_ctas = *ctas;
@@ -403,6 +406,11 @@ fp4idx_status_t fp4idx_topk_score(const fp4idx_problem_t* problem, const float* 
   int ctas = 0;
   fp4idx_status_t s = topk_prepare(problem, w, w_row_stride, k, workspace, workspace_bytes, true, &sp, &ctas);
   if (s != FP4IDX_OK) return s;
+  if (sp.pool_hist) {
+    const size_t bytes = static_cast<size_t>(problem->num_rows) * (kPoolBins + 1) * 4;
+    cudaError_t e = cudaMemsetAsync(sp.pool_hist, 0, bytes, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pooled-count clear");
+  }
   cudaError_t e = launch_score(sp, problem->format, kModeTopk, problem->num_heads, dim3(ctas),
                                static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "scorer launch");

@@ -17,8 +17,10 @@ enum Mode : int { kModeLogits = 0, kModeTopk = 1 };
 // Keys-on-M scorer: one CTA owns up to R query rows of one request (the MMA
 // N dimension is R*H) and a contiguous chunk of 128-key tiles.
 struct ScoreParams {
-  CUtensorMap tmap_k;   // 3D {64 B, page, num_pages*Hkv blocks}, box {64, page, 1}, 64B swizzle
   CUtensorMap tmap_q;   // 3D {64 B, Hq, T}, box {64, H, R}, 64B swizzle
+  // codes of (page, K head) block z: page*64 bytes at kcode_base + z * kcode_block_stride
+  const uint8_t* kcode_base;
+  int64_t kcode_block_stride;
   // scales of (page, K head) block z: page*G bytes at kscale_base + z * kscale_block_stride
   // (separate scale array, or the scale rows of a fused page)
   const uint8_t* kscale_base;
@@ -65,6 +67,12 @@ struct ScoreParams {
   // split of the concatenated units balances CTAs with many short items
   // against CTAs with a few long ones (0: tiles only).
   int32_t item_overhead;
+  // Pooled bucket counts of every row (top-k with four-row CTAs and at most
+  // kPoolMaxRows rows; nullptr otherwise), zeroed before the launch:
+  // pool_hist[t][b] = keys of row t that some CTA appended in bucket b,
+  // pool_top[t] = the highest such bucket.
+  uint32_t* pool_hist;
+  uint32_t* pool_top;
   uint32_t* err;
 };
 
@@ -187,6 +195,9 @@ cudaError_t launch_token_table(const TokenTableParams& p, cudaStream_t stream);
 
 // Sets the message fp4idx_last_error_message() returns on this thread.
 void set_last_error(const char* fmt, ...);
+
+constexpr int kPoolMaxRows = 2048;
+constexpr int kPoolBins = 2048;  // the streaming top-k's bucket count (kHistBins)
 
 // Twice k rounded to whole tiles, at least 1,024.
 __host__ __device__ constexpr int topk_capacity(int k) {

@@ -130,7 +130,7 @@ struct ScoreLayout {
   // flight per SM), at most 20 stages.
   static constexpr uint32_t kFixedBytes = 2 * (((H * R * 64 + 1023) / 1024) * 1024) + (kDirectSf ? 0 : 4 * kAtoms * 2048) +
                                           2 * kAtoms * 512 + 4096 + (160 + kEpiThreads * 4) * 4 + 4 * 1280 +
-                                          (MODE == kModeTopk ? R * kHistBins * 2 : 0) + kCandBytes + 2048;
+                                          (MODE == kModeTopk ? R * kHistBins * 2 + R * H * 4 : 0) + kCandBytes + 2048;
   static constexpr int kStagesFit = static_cast<int>((232448u - 1024u - kFixedBytes) / (8192u + 128u * G)) & ~1;
   static constexpr int kStages = kStagesFit < 20 ? kStagesFit : 20;
   static_assert(kStages >= 4, "K ring depth");
@@ -178,7 +178,10 @@ struct ScoreLayout {
   static constexpr uint32_t kScratch = kScan + kThreads * 4;                      // per group
   static constexpr uint32_t kHist = (kScratch + kGroups * sizeof(SelectScratch) + 15) / 16 * 16;
   static constexpr uint32_t kCand = (kHist + (MODE == kModeTopk ? R * kHistBins * 2 : 0) + 15) / 16 * 16;
-  static constexpr uint32_t kEnd = kCand + kCandBytes;
+  // top-k: the item rows' head weights (the epilogue reads them from here,
+  // not from registers, which the top-k state needs)
+  static constexpr uint32_t kW = kCand + kCandBytes;
+  static constexpr uint32_t kEnd = kW + (MODE == kModeTopk ? R * H * 4 : 0);
   static constexpr uint32_t bytes() { return kEnd + 1024; }
   static_assert(kEnd + 1024 <= 232448u, "shared memory");
   // TMEM columns
@@ -375,9 +378,8 @@ __device__ __forceinline__ void q_scale_atoms(const ScoreParams& p, const ItemIn
 // NaN-propagating max per value, then packed fp32x2 FMAs in four chains
 // fixed by the head pair, so a row's sum does not depend on how its
 // columns were loaded.  wrelu_total adds the chains.
-template <int C, int HP>
-__device__ __forceinline__ void wrelu_chunk(const uint32_t (&v)[C], const float2 (&w2)[HP], int i0,
-                                            float2 (&acc)[4]) {
+template <int C, class W>
+__device__ __forceinline__ void wrelu_chunk(const uint32_t (&v)[C], const W& w2, int i0, float2 (&acc)[4]) {
 #pragma unroll
   for (int i = 0; i < C / 2; ++i) {
     const float2 x = make_float2(relu_nan(__uint_as_float(v[2 * i])), relu_nan(__uint_as_float(v[2 * i + 1])));
@@ -519,10 +521,9 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
   if (threadIdx.x == 0) {
     st->abort = 0;
     // the first TMA waits for its descriptor: fetch both early
-    prefetch_tmap(&p.tmap_k);
     prefetch_tmap(&p.tmap_q);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 1);  // the producer's expect-tx arrive; TMA and bulk copies complete the bytes
+      mbar_init(full_bar(s), 64);  // one arrive per producer lane, once its copies have landed
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < kAccBufs; ++a) {
@@ -581,17 +582,21 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
 
   if (warp == 0 || warp == L::kProducer2Warp) {
     // ================================================================ producers
-    // Each producer warp walks every tile and issues the even (warp 0) or odd
-    // (last warp) ones.  Lane l caches the physical id of logical page base+l
-    // (and of the next 32, prefetched); for each tile the lanes sl < slots
-    // pick up the id of page sl and issue that page's code copy (TMA) and its
-    // raw scale copy (one bulk copy of the page's contiguous scales).
+    // Both producer warps work on every tile: warp 0 copies keys 0..63 of
+    // the tile, the last warp keys 64..127 -- one 64-key page each, or one
+    // half of a 128-key page -- with 16-byte cp.async copies (a page is far
+    // too small for a tensor copy to pay its issue cost): its 4 KB of codes
+    // in eight coalesced 512-byte warp copies, each 16-byte chunk placed at
+    // its key's MMA row (the strided order for MXFP4) under the operand's
+    // 64-byte swizzle, and its 64 G scale bytes unchanged.  Every lane then
+    // arrives on the stage's full barrier once its copies have landed
+    // (64 arrivals a phase).  Lane l caches the physical id of logical page
+    // base + l (and of the next 32, prefetched).  Warp 0 also loads each
+    // item's Q codes by TMA.
     const uint32_t pidx = warp == 0 ? 0u : 1u;
     uint32_t tile_iter = 0, item_iter = 0;
     bool ok = true;
-    const int page = p.page_size;
     const int pshift = p.page_shift;
-    const int slots = kTileKeys >> pshift;  // 2 for 64-key pages, 1 for 128
     FP4IDX_STAMP_INIT();
     for_each_segment<MODE, R>(p, st, [&](int, const ItemInfo& it, int lo, int hi, int) {
       if (!ok) return;
@@ -607,66 +612,52 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
         }
       }
       ++item_iter;
-      const int32_t npages = (it.k_len + page - 1) >> pshift;
+      const int32_t npages = (it.k_len + p.page_size - 1) >> pshift;
       const int32_t* table = p.block_table + it.table_base;
       auto fetch = [&](int32_t b) -> int32_t {
         const int32_t lp = b + lane;
         return lp < npages ? __ldg(table + lp) : -1;
       };
-      int32_t base = (lo * slots) & ~31;
+      const int32_t half = 64 * static_cast<int32_t>(pidx);  // this warp's first key in a tile
+      int32_t base = (((lo << 7) + half) >> pshift) & ~31;
       int32_t cur_ids = fetch(base), next_ids = fetch(base + 32);
       for (int j = lo; j < hi; ++j) {
         if (MODE == kModeLogits && !tile_has_visible(it, j)) continue;
-        if ((tile_iter & 1u) != pidx) {  // the other producer's tile
-          ++tile_iter;
-          continue;
-        }
-        const int32_t lp0 = j * slots;
-        if (lp0 >= base + 32) {  // warp-uniform
+        const int32_t key0 = (j << 7) + half;  // first logical position of this warp's 64 keys
+        const int32_t lp = key0 >> pshift;     // their page (warp-uniform)
+        if (lp >= base + 32) {
           base += 32;
           cur_ids = next_ids;
           next_ids = fetch(base + 32);
         }
-        // physical page of slot 0 and 1 of this tile (slot 1 only for 64-key pages)
-        const int32_t phys0 = __shfl_sync(0xffffffffu, cur_ids, lp0 - base);
-        const int32_t phys1 = __shfl_sync(0xffffffffu, cur_ids, lp0 - base + (slots - 1));
-        auto page_ok = [&](int sl, int32_t ph_id) {
-          return ((lp0 + sl) << pshift) < it.k_len && ph_id >= 0 && ph_id < p.num_pages;
-        };
-        const bool ok0 = page_ok(0, phys0);
-        const bool ok1 = slots == 2 && page_ok(1, phys1);
-        if (lane < slots && ((lp0 + lane) << pshift) < it.k_len && !(lane == 0 ? ok0 : ok1))
-          atomicOr(p.err, kErrPageRange);
-        const uint32_t bytes = static_cast<uint32_t>((ok0 ? 1 : 0) + (ok1 ? 1 : 0)) * page * (kCodeBytes + G);
+        const int32_t phys = __shfl_sync(0xffffffffu, cur_ids, lp - base);
+        const bool in_len = key0 < it.k_len;
+        const bool good = in_len && phys >= 0 && phys < p.num_pages;
+        // one report per page: a 128-key page's first half reports it
+        if (lane == 0 && in_len && !good && (key0 & (p.page_size - 1)) == 0) atomicOr(p.err, kErrPageRange);
         const int s = tile_iter % kStages;
         const uint32_t ph = (tile_iter / kStages) & 1u;
         FP4IDX_STAMP(3);
         ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.err) : false, 0);
         FP4IDX_STAMP(1);
         if (!ok) return;
-        if (lane == 0) mbar_arrive_expect_tx(full_bar(s), bytes);
-        __syncwarp();
-        if constexpr (L::kDirectSf) {
-          // codes in the strided key order: lane 4 sl + c copies keys c, c+4,
-          // ... of page slot sl (page / 4 of them) to rows 32c + (page / 4) sl
-          if (lane < 4 * slots) {
-            const int sl = lane >> 2, c = lane & 3;
-            if (sl == 0 ? ok0 : ok1)
-              tma_load_4d(codes_s + s * 8192 + ((32 * c + (page >> 2) * sl) * kCodeBytes), &p.tmap_k, 0, c, 0,
-                          sl == 0 ? phys0 : phys1, full_bar(s));
+        if (good) {
+          const int32_t in_page = key0 & (p.page_size - 1);
+          const uint8_t* codes = p.kcode_base + static_cast<int64_t>(phys) * p.kcode_block_stride + in_page * kCodeBytes;
+          const uint32_t dst0 = codes_s + s * 8192;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int c = 32 * u + lane;       // 16-byte chunk of the warp's 4 KB
+            const int kq = half + (c >> 2);    // key within the tile
+            const int m = L::kDirectSf ? 32 * (kq & 3) + (kq >> 2) : kq;  // its MMA row
+            const int jj = (c & 3) ^ ((m >> 1) & 3);                       // 64-byte swizzle
+            cp_async_16(dst0 + m * kCodeBytes + jj * 16, codes + c * 16);
           }
-          if (lane < slots && (lane == 0 ? ok0 : ok1))
-            bulk_load(kraw_s + s * (128 * G) + ((lane * G) << pshift),
-                      p.kscale_base + static_cast<int64_t>(lane == 0 ? phys0 : phys1) * p.kscale_block_stride,
-                      static_cast<uint32_t>(page * G), full_bar(s));
-        } else if (lane < slots && (lane == 0 ? ok0 : ok1)) {
-          const int32_t blk = lane == 0 ? phys0 : phys1;  // (page, K head) block: one K head
-          tma_load_3d(codes_s + s * 8192 + ((lane * kCodeBytes) << pshift), &p.tmap_k, 0, 0, blk, full_bar(s));
-          // the page's scales are contiguous: [page keys][G]
-          bulk_load(kraw_s + s * (128 * G) + ((lane * G) << pshift),
-                    p.kscale_base + static_cast<int64_t>(blk) * p.kscale_block_stride, static_cast<uint32_t>(page * G),
-                    full_bar(s));
+          if (lane < 4 * G)  // 64 keys x G scale bytes
+            cp_async_16(kraw_s + s * (128 * G) + half * G + lane * 16,
+                        p.kscale_base + static_cast<int64_t>(phys) * p.kscale_block_stride + in_page * G + lane * 16);
         }
+        cp_async_arrive(full_bar(s));
         FP4IDX_STAMP(2);
         FP4IDX_STAMP_COUNT();
         ++tile_iter;
@@ -674,18 +665,14 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
     });
     FP4IDX_STAMP(3);
     FP4IDX_STAMP_DONE(0);
-    if (!ok && lane == 0) {
-      // Let copies already in flight land before the CTA can exit.
+    if (lane == 0 && pidx == 0 && !ok) {
+      // Let the Q copies in flight land before the CTA can exit.
       volatile int never = 0;
-      const uint32_t first = tile_iter > static_cast<uint32_t>(kStages) ? tile_iter - kStages : 0;
-      for (uint32_t u = first; u < tile_iter; ++u) {
-        if ((u & 1u) != pidx) continue;
-        mbar_wait(full_bar(u % kStages), (u / kStages) & 1u, &never, p.err);
-      }
-      if (pidx == 0)
-        for (uint32_t u = item_iter > 2u ? item_iter - 2u : 0u; u < item_iter; ++u)
-          mbar_wait(qfull_bar(u & 1u), (u >> 1) & 1u, &never, p.err);
+      for (uint32_t u = item_iter > 2u ? item_iter - 2u : 0u; u < item_iter; ++u)
+        mbar_wait(qfull_bar(u & 1u), (u >> 1) & 1u, &never, p.err);
     }
+    // this thread's own cp.async copies land before it exits
+    cp_async_wait_all();
     __syncwarp();
   } else if (warp == 1) {
     // ================================================================ MMA issuer
@@ -729,6 +716,9 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
           if (!(ok = mbar_wait(acce_bar(a), aph ^ 1u, abort_flag, p.err))) break;
           FP4IDX_STAMP(1);
           tc_fence_after();
+          // the stage was written by cp.async (generic proxy); the MMA and
+          // the scale copy read it through the async proxy
+          fence_proxy_async_smem();
           const uint32_t sfa_t = tmem + L::kSfaCol + slot * 8u;
           if constexpr (L::kDirectSf) {
             // slot == a: the MMA that last read it finished before the
@@ -964,6 +954,7 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
     // largest of any subset of a row's keys is at most its k-th largest), so
     // the threshold rises at every check without touching the buffer.
     auto hist_of = [&](int rr) { return Hist16{hist_words + (r0 + rr) * (kHistBins / 2)}; };
+    static_assert(kHistBins == kPoolBins, "pooled and per-CTA buckets agree");
     // Keys >= T of the buffer moved, in place, to [0, kept); returns kept.
     // A round reads 8 * kEpiThreads keys into registers before writing any:
     // every write lands below the number of keys read so far, and an unread
@@ -1023,19 +1014,31 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
       uint64_t thr[RG];      // each row's buffer accepts keys >= thr
       int seg0[RG];          // keys kept by the row's last compaction (front of its buffer)
       int wcnt[RG];          // keys this warp appended to its region of the row's buffer
+      // pooled counts (see pool_raise): this lane's highest appended bucket,
+      // the window top and bucket count loaded at the last check, the row's
+      // pooled top loaded then
+      uint32_t pl_top[RG], pl_win[RG], pl_cnt[RG], pl_next[RG];
 #pragma unroll
       for (int rr = 0; rr < RG; ++rr) {
         row_valid[rr] = r0 + rr < it.nrows;
         t[rr] = it.row0 + r0 + rr;
         vis[rr] = row_valid[rr] ? row_visible(p, it, t[rr]) : 0;
+        if constexpr (MODE == kModeTopk) {
+          // ordered before any read by the group barrier after the histogram clear
+          float* ws = reinterpret_cast<float*>(smem + L::kW) + (r0 + rr) * H;
+          for (int h = g.tid; h < H; h += kEpiThreads)
+            ws[h] = row_valid[rr] ? __ldg(p.w + static_cast<int64_t>(t[rr]) * p.w_row_stride + h) : 0.0f;
+        } else {
 #pragma unroll
-        for (int i = 0; i < H / 2; ++i) {
-          const float* wr = p.w + static_cast<int64_t>(t[rr]) * p.w_row_stride + 2 * i;
-          w2[rr][i] = row_valid[rr] ? make_float2(__ldg(wr), __ldg(wr + 1)) : make_float2(0.0f, 0.0f);
+          for (int i = 0; i < H / 2; ++i) {
+            const float* wr = p.w + static_cast<int64_t>(t[rr]) * p.w_row_stride + 2 * i;
+            w2[rr][i] = row_valid[rr] ? make_float2(__ldg(wr), __ldg(wr + 1)) : make_float2(0.0f, 0.0f);
+          }
         }
         thr[rr] = 0;
         seg0[rr] = 0;
         wcnt[rr] = 0;
+        pl_top[rr] = pl_win[rr] = pl_cnt[rr] = pl_next[rr] = 0;
       }
       if constexpr (MODE == kModeTopk) {
 #pragma unroll
@@ -1108,7 +1111,11 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
                   __syncwarp();
                   if (lane == 0) mbar_arrive(acce_bar(a));
                 }
-                wrelu_chunk<kChunk>(v, w2[rr], c0 / 2, acc);
+                if constexpr (MODE == kModeTopk)
+                  wrelu_chunk<kChunk>(v, reinterpret_cast<const float2*>(smem + L::kW) + (r0 + rr) * (H / 2),
+                                      c0 / 2, acc);
+                else
+                  wrelu_chunk<kChunk>(v, w2[rr], c0 / 2, acc);
               }
               val[rr] = wrelu_total(acc);
             }
@@ -1140,9 +1147,14 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
             if (m) {
               // this warp's region: no other warp writes there
               const int slot_i = wcnt[rr] + __popc(m & ((1u << lane) - 1u));
+              const uint32_t bkt = static_cast<uint32_t>(key >> kHistShift);
               if (take) {
                 cand_of(rr)[seg0[rr] + quad * ((ccap - seg0[rr]) >> 2) + slot_i] = key;
-                hist_of(rr).add(static_cast<int>(key >> kHistShift));
+                hist_of(rr).add(static_cast<int>(bkt));
+                if (!L::kSmemCand && p.pool_hist) {
+                  red_add_u32(p.pool_hist + static_cast<int64_t>(t[rr]) * kHistBins + bkt, 1u);
+                  pl_top[rr] = max(pl_top[rr], bkt);
+                }
               }
               wcnt[rr] += __popc(m);
             }
@@ -1150,6 +1162,40 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
           FP4IDX_STAMP(4);
           if (++since_check < check_every) continue;
           since_check = 0;
+          if (!L::kSmemCand && p.pool_hist) {
+            // Pooled threshold, per warp and without waiting on memory: the
+            // 32 buckets below the top read at the last check hold counts
+            // that every CTA scoring a row adds to as it appends keys; each
+            // count read is at most the row's count at that moment and every
+            // counted key exists, so k keys in buckets >= b make b's lower
+            // edge a valid threshold (the k-th largest key of the row is at
+            // least that large).  Then this warp's highest bucket is pooled
+            // and the next window's counts and top are requested.
+#pragma unroll
+            for (int rr = 0; rr < RG; ++rr) {
+              if (!row_valid[rr]) continue;  // warp-uniform
+              const uint32_t wm = __reduce_max_sync(0xffffffffu, pl_top[rr]);
+              if (lane == 0 && wm > 0) red_max_u32(p.pool_top + t[rr], wm);
+              const int b = static_cast<int>(pl_win[rr]) - 31 + lane;
+              const uint32_t c = b >= 0 ? pl_cnt[rr] : 0u;
+              uint32_t incl = c;  // keys in this lane's bucket and above
+#pragma unroll
+              for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_down_sync(0xffffffffu, incl, o);
+                if (lane + o < 32) incl += y;
+              }
+              const uint32_t hit = __ballot_sync(0xffffffffu, incl >= kk && incl - c < kk);
+              if (hit) {
+                const uint64_t Tp = static_cast<uint64_t>(static_cast<int>(pl_win[rr]) - 31 + (__ffs(hit) - 1))
+                                    << kHistShift;
+                if (Tp > thr[rr]) thr[rr] = Tp;
+              }
+              pl_win[rr] = pl_next[rr];
+              const int nb = static_cast<int>(pl_win[rr]) - 31 + lane;
+              pl_cnt[rr] = nb >= 0 ? ld_relaxed_u32(p.pool_hist + static_cast<int64_t>(t[rr]) * kHistBins + nb) : 0u;
+              pl_next[rr] = ld_relaxed_u32(p.pool_top + t[rr]);
+            }
+          }
           publish(wcnt, true);
           g.sync();
           // -- threshold raise from each row's histogram; compaction of a row
@@ -1177,7 +1223,10 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
               // largest when that would keep more than half the buffer
               uint64_t* cr = cand_of(rr);
               const bool exact = above + hr(static_cast<int>(bkt)) > static_cast<uint32_t>(ccap / 2);
-              if (exact) T = select_in_bucket(g, bkt, kk - above, gsc, [&](auto&& fn) { visit(cr, sv, fn); });
+              if (exact) {
+                const uint64_t Te = select_in_bucket(g, bkt, kk - above, gsc, [&](auto&& fn) { visit(cr, sv, fn); });
+                T = Te > T ? Te : T;  // T may be a warp's higher pooled threshold
+              }
               const int left = compact(cr, sv, T);
               // the histogram follows the buffer: buckets below bkt are empty now
               for (int wd = g.tid; wd < static_cast<int>(bkt >> 1); wd += kEpiThreads) hr.w[wd] = 0;
