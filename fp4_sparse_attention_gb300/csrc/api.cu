@@ -691,13 +691,17 @@ fp4idx_status_t fp4idx_block_topk(const float* scores, int32_t num_heads, int32_
   if (!indices) return fail(FP4IDX_EINVAL, "indices is NULL");
   if (num_heads < 1 || ktiles < 1 || num_rows < 1 || k < 1)
     return fail(FP4IDX_EINVAL, "num_heads, ktiles, num_rows and k must be positive");
-  if (k > 32) return fail(FP4IDX_EUNSUPPORTED, "k = %d: supported 1..32", k);
+  if (k > 128) return fail(FP4IDX_EUNSUPPORTED, "k = %d: supported 1..128", k);
+  if (k > 32 && ktiles > 1024) return fail(FP4IDX_EUNSUPPORTED, "k = %d > 32 needs ktiles <= 1024 (got %d)", k, ktiles);
   if (!aligned(scores, 4) || !aligned(indices, 4) || (values && !aligned(values, 4)) ||
       (valid_count && !aligned(valid_count, 4)))
     return fail(FP4IDX_EINVAL, "scores, indices, values and valid_count must be 4-byte aligned");
   if (static_cast<int64_t>(num_heads) * num_rows >= (int64_t(1) << 38))  // grid.x < 2^31 blocks of 256
     return fail(FP4IDX_EUNSUPPORTED, "too many columns");
-  cudaError_t e = launch_block_topk(scores, num_heads, ktiles, num_rows, k, indices, values, valid_count,
+  DeviceInfo* dev;
+  fp4idx_status_t s;
+  if ((s = device_info(&dev)) != FP4IDX_OK) return s;
+  cudaError_t e = launch_block_topk(scores, num_heads, ktiles, num_rows, k, indices, values, valid_count, dev->sms,
                                     static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "block top-k launch");
   return FP4IDX_OK;

@@ -174,7 +174,7 @@ cudaError_t launch_topk_slots(const SlotParams& p, int32_t rows, cudaStream_t st
 
 // Top-k blocks of each (head, row) column of [H][Kt][T] block scores, k <= 32.
 cudaError_t launch_block_topk(const float* scores, int32_t H, int32_t Kt, int32_t T, int32_t k, int32_t* indices,
-                              float* values, int32_t* valid_count, cudaStream_t stream);
+                              float* values, int32_t* valid_count, int sms, cudaStream_t stream);
 
 // Cache metadata of a per-token slot table (fp4idx_pages_from_token_table).
 struct TokenTableParams {

@@ -195,7 +195,9 @@ fp4idx_status_t fp4idx_block_scores(const fp4idx_problem_t* problem, float* scor
  *   valid_count  [Hq][T] int32 = min(k, n), or NULL.
  * Every pointer is caller-owned device memory (4-byte aligned); no workspace,
  * no synchronisation (graph-capturable).  EINVAL for NULL scores / indices or
- * a non-positive size, EUNSUPPORTED for k > 32.
+ * a non-positive size, EUNSUPPORTED for k > 128, or k > 32 with ktiles > 1024.
+ * For k <= 32 the scores are read 16 bytes at a time when num_rows is a
+ * multiple of 4 and scores is 16-byte aligned, else 4 bytes at a time.
  */
 fp4idx_status_t fp4idx_block_topk(const float* scores, int32_t num_heads, int32_t ktiles,
                                   int32_t num_rows, int32_t k, int32_t* indices, float* values,

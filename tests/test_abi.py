@@ -134,7 +134,8 @@ def test_block_topk_rejects_bad_arguments_on_host(lib):
     assert lib.fp4idx_block_topk(vp, 0, 64, 16, 16, vp, None, None, None) == 1          # heads
     assert lib.fp4idx_block_topk(vp, 32, 0, 16, 16, vp, None, None, None) == 1          # ktiles
     assert lib.fp4idx_block_topk(vp, 32, 64, 16, 0, vp, None, None, None) == 1          # k
-    assert lib.fp4idx_block_topk(vp, 32, 64, 16, 33, vp, None, None, None) == 2         # k > 32
+    assert lib.fp4idx_block_topk(vp, 32, 64, 16, 129, vp, None, None, None) == 2        # k > 128
+    assert lib.fp4idx_block_topk(vp, 32, 1025, 16, 33, vp, None, None, None) == 2       # k > 32, ktiles > 1024
     assert lib.fp4idx_block_topk(bad, 32, 64, 16, 16, vp, None, None, None) == 1        # alignment
 
 

@@ -50,6 +50,27 @@ def test_shapes(H, Kt, T, k):
     _check(_scores(H, Kt, T, seed=H * 1000 + Kt, ties=Kt < 100), k)
 
 
+@pytest.mark.parametrize("k", [33, 64, 100, 128])
+def test_large_k(k):
+    # one warp per column: fewer blocks than k (every candidate, in order),
+    # more blocks than k, and T not a multiple of 4
+    _check(_scores(3, 37, 300, seed=k), k)
+    _check(_scores(2, 200, 65, seed=k + 1, ties=False), k)
+    _check(_scores(1, 64, 129, seed=k + 2), k)
+
+
+def test_large_k_long_columns():
+    _check(_scores(1, 1000, 40, seed=5, ties=False), 128)
+    _check(_scores(2, 700, 33, seed=6), 64)
+
+
+def test_many_chunks_and_unaligned_rows():
+    # the k <= 32 path streams 64-block chunks: several chunks, and rows
+    # that are and are not a multiple of 4
+    _check(_scores(2, 300, 256, seed=7, ties=False), 32)
+    _check(_scores(3, 130, 31, seed=8), 16)
+
+
 def test_on_gqa_block_scores():
     # the block-score tensor of the GQA NVFP4 workload, top-16 blocks per (head, row)
     p = wl.nvfp4_gqa_block_scores()
