@@ -97,6 +97,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Whole-warp wait (every lane calls it with the same arguments): every lane
+// tests the phase -- the same barrier word, so the same answer -- and only
+// when it is not yet complete does lane 0 wait and broadcast the outcome.
+// Returns the same value on every lane.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint32_t* err) {
+  if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
+  const int lane = threadIdx.x & 31;
+  return __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(bar, parity, abort, err) : false, 0);
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");

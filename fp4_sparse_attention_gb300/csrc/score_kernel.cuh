@@ -603,7 +603,7 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
       if (pidx == 0) {
         const uint32_t qb = item_iter & 1u, qph = (item_iter >> 1) & 1u;
         FP4IDX_STAMP(3);
-        ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(qempty_bar(qb), qph ^ 1u, abort_flag, p.err) : false, 0);
+        ok = warp_wait(qempty_bar(qb), qph ^ 1u, abort_flag, p.err);
         FP4IDX_STAMP(0);
         if (!ok) return;
         if (lane == 0) {
@@ -638,7 +638,7 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
         const int s = tile_iter % kStages;
         const uint32_t ph = (tile_iter / kStages) & 1u;
         FP4IDX_STAMP(3);
-        ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.err) : false, 0);
+        ok = warp_wait(empty_bar(s), ph ^ 1u, abort_flag, p.err);
         FP4IDX_STAMP(1);
         if (!ok) return;
         if (good) {
@@ -784,7 +784,7 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
       FP4IDX_STAMP(4);
       const uint32_t qb = item_iter & 1u, qph = (item_iter >> 1) & 1u;
       if (sidx == 0) {
-        ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(qfull_bar(qb), qph, abort_flag, p.err) : false, 0);
+        ok = warp_wait(qfull_bar(qb), qph, abort_flag, p.err);
         if (!ok) return;
         // Q scales only when some tile of the segment is computed (otherwise
         // no MMA reads them); the barrier is committed either way
@@ -1081,13 +1081,11 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
         if (real) {
           const int a = tile_iter % kAccBufs;
           const uint32_t aph = (tile_iter / kAccBufs) & 1u;
-          // One lane per warp polls the accumulator barrier (no group
-          // barrier per tile); ok stays warp-uniform, as tcgen05.ld below
-          // is a whole-warp instruction.
-          bool got = false;
+          // Each warp waits for the accumulator itself (no group barrier per
+          // tile); ok stays warp-uniform, as tcgen05.ld below is a
+          // whole-warp instruction.
           FP4IDX_STAMP(4);
-          if (lane == 0) got = ok && mbar_wait(accf_bar(a), aph, abort_flag, p.err);
-          ok = __shfl_sync(0xffffffffu, got, 0);
+          ok = ok && warp_wait(accf_bar(a), aph, abort_flag, p.err);
           FP4IDX_STAMP(1);
           if (ok) {
             tc_fence_after();
