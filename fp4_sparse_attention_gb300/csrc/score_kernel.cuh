@@ -97,9 +97,9 @@ struct CtaState {
   int32_t pad[2];
 };
 
-template <int R>
+template <int R, int NREG>
 struct RowState {  // top-k: candidates each epilogue warp appended to its region of each row
-  int32_t wc[2][R][4];  // double buffered: publication p writes wc[p & 1]
+  int32_t wc[2][R][NREG];  // double buffered: publication p writes wc[p & 1]
 };
 
 
@@ -143,14 +143,21 @@ struct ScoreLayout {
       MODE == kModeTopk ? 1 : (R < 64 / H ? R : (64 / H < 1 ? 1 : 64 / H));
   static_assert(R % kRowsPerGroup == 0, "rows split evenly over the groups");
   static constexpr int kGroups = R / kRowsPerGroup;
-  // warp 0 and kProducer2Warp: producers (alternate tiles); warp 1: MMA;
-  // warp 2 (and kScale2Warp, when there are two): scales (alternate
-  // tiles); warps 3 .. 3 + 4 * kGroups - 1: epilogue.  Registers are
-  // reserved for whole groups of four warps, so the CTA is rounded up to a
-  // multiple of four warps (the extra ones idle); a second scale warp is
-  // used where that leaves the epilogue enough registers.
+  // Two-row top-k CTAs (64 heads) give each row two sets of four warps that
+  // take alternate tiles (tile parity), so the per-tile epilogue chain of a
+  // row runs on twice the warps; a row's checks, compactions and flush stay
+  // cooperative over both sets (eight warps, eight append regions).
+  static constexpr int kSets = MODE == kModeTopk && R == 2 ? 2 : 1;
+  static constexpr int kEpiGroups = kGroups * kSets;
+  static constexpr int kRegions = 4 * kSets;
+  // warp 0 and kProducer2Warp: producers; warp 1: MMA; warp 2 (and
+  // kScale2Warp, when there are two): scales (alternate tiles); warps 3 ..
+  // 3 + 4 * kEpiGroups - 1: epilogue.  Registers are reserved for whole
+  // groups of four warps, so the CTA is rounded up to a multiple of four
+  // warps (the extra ones idle); a second scale warp is used where that
+  // leaves the epilogue enough registers.
   static constexpr int kEpiWarp0 = 3;
-  static constexpr int kProducer2Warp = kEpiWarp0 + 4 * kGroups;
+  static constexpr int kProducer2Warp = kEpiWarp0 + 4 * kEpiGroups;
   static constexpr int kScaleWarps = kDirectSf || (kProducer2Warp + 1) % 4 == 0 ? 1 : 2;
   static constexpr int kScale2Warp = kProducer2Warp + 1;
   static constexpr int kWarpsUsed = kProducer2Warp + kScaleWarps;
@@ -174,7 +181,7 @@ struct ScoreLayout {
   static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 4 + kSfaSlots + 2;
   static constexpr uint32_t kState = kBars + kNumBars * 8;
   static constexpr uint32_t kRows = (kState + sizeof(CtaState) + 15) / 16 * 16;
-  static constexpr uint32_t kScan = (kRows + sizeof(RowState<R>) + 15) / 16 * 16;  // kThreads ints
+  static constexpr uint32_t kScan = (kRows + sizeof(RowState<R, kRegions>) + 15) / 16 * 16;  // kThreads ints
   static constexpr uint32_t kScratch = kScan + kThreads * 4;                      // per group
   static constexpr uint32_t kHist = (kScratch + kGroups * sizeof(SelectScratch) + 15) / 16 * 16;
   static constexpr uint32_t kCand = (kHist + (MODE == kModeTopk ? R * kHistBins * 2 : 0) + 15) / 16 * 16;
@@ -508,7 +515,7 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
   auto qsready_bar = [&](uint32_t qb) { return bar0 + 8u * (2 * kStages + 2 * kAccBufs + 4 + L::kSfaSlots + qb); };
 
   CtaState* st = reinterpret_cast<CtaState*>(smem + L::kState);
-  RowState<R>* rs = reinterpret_cast<RowState<R>*>(smem + L::kRows);
+  RowState<R, L::kRegions>* rs = reinterpret_cast<RowState<R, L::kRegions>*>(smem + L::kRows);
   uint32_t* scan = reinterpret_cast<uint32_t*>(smem + L::kScan);
   SelectScratch* sc = reinterpret_cast<SelectScratch*>(smem + L::kScratch);
   uint32_t* hist_words = reinterpret_cast<uint32_t*>(smem + L::kHist);
@@ -528,7 +535,7 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
     }
     for (int a = 0; a < kAccBufs; ++a) {
       mbar_init(accf_bar(a), 1);
-      mbar_init(acce_bar(a), L::kGroups * 4);  // one arrive per epilogue warp
+      mbar_init(acce_bar(a), L::kGroups * 4);  // one arrive per epilogue warp of the tile's set
     }
     for (uint32_t qb = 0; qb < 2; ++qb) {
       mbar_init(qfull_bar(qb), 1);
@@ -888,25 +895,31 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
   } else {
     // ================================================================ epilogue
     constexpr int RG = L::kRowsPerGroup;  // query rows of this group
-    const int gi = (warp - L::kEpiWarp0) >> 2;
+    constexpr int kG = kEpiThreads * L::kSets;  // threads of a row group (all its sets)
+    constexpr int kRegions = L::kRegions;
+    const int gi4 = (warp - L::kEpiWarp0) >> 2;  // four-warp group
+    const int set = gi4 / L::kGroups;            // the tile parity it takes (two sets)
+    const int gi = gi4 - set * L::kGroups;       // its row group
     const int r0 = gi * RG;  // first row of the item this group handles
-    Group<kEpiThreads, -1> g{static_cast<int>(threadIdx.x) - 32 * L::kEpiWarp0 - gi * kEpiThreads, 1 + gi};
+    Group<kG, -1> g{set * kEpiThreads + static_cast<int>(threadIdx.x) - 32 * L::kEpiWarp0 - gi4 * kEpiThreads, 1 + gi};
     SelectScratch* gsc = sc + gi;
     const int quad = warp & 3;
+    const int region = set * 4 + quad;  // this warp's append region of each row
     // key of this thread's accumulator lane 32 quad + lane within the tile
     // (MXFP4: the strided order of the producer's code boxes)
     const int key_local = L::kDirectSf ? 4 * lane + quad : quad * 32 + lane;
     // Candidate buffer of each row (shared memory for two-row CTAs, else the
     // workspace), ccap keys laid out as
     //   [0, seg0)                       keys kept by the last compaction
-    //   [seg0 + q * rsz, + wc[q])       keys warp q of the group appended since
-    // with rsz = (ccap - seg0) / 4, so an append needs no atomic: each warp
-    // owns its region and keeps its count in a register.  The counts are
-    // published and checked every `check_every` tiles; a region then keeps
-    // that many tiles of room (32 keys per tile and warp) above the trigger.
+    //   [seg0 + q * rsz, + wc[q])       keys warp q of the row group appended since
+    // with rsz = (ccap - seg0) / kRegions, so an append needs no atomic: each
+    // warp owns its region and keeps its count in a register.  The counts
+    // are published and checked every `check_every` tiles (a set takes
+    // check_every / kSets of them); a region then keeps that many tiles of
+    // room (32 keys per tile and warp) above the trigger.
     const int ccap = L::kSmemCand ? L::kCandCap : topk_cand_capacity(p.k);
-    const int check_every = ccap >= 4096 ? 8 : 4;  // a region is at least ccap / 8 keys
-    const int margin = check_every * 32;
+    const int check_every = ccap >= 4096 ? 8 : 4;  // a region is at least ccap / 16 keys
+    const int margin = check_every / L::kSets * 32;
     const uint32_t kk = static_cast<uint32_t>(p.k);
     int since_check = 0;
     uint32_t tile_iter = 0;
@@ -918,17 +931,28 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
     // Segmented view of one row's buffer: virtual index i < seg0 + sum(c)
     // -> position in the buffer.
     struct SegView {
-      int seg0, rsz, c0, c1, c2, c3;
-      __device__ __forceinline__ int n() const { return seg0 + c0 + c1 + c2 + c3; }
+      int seg0, rsz, c[kRegions];
+      __device__ __forceinline__ int n() const {
+        int s = seg0;
+#pragma unroll
+        for (int q = 0; q < kRegions; ++q) s += c[q];
+        return s;
+      }
       __device__ __forceinline__ int pos(int i) const {
         if (i < seg0) return i;
         int j = i - seg0;
-        if (j < c0) return seg0 + j;
-        j -= c0;
-        if (j < c1) return seg0 + rsz + j;
-        j -= c1;
-        if (j < c2) return seg0 + 2 * rsz + j;
-        return seg0 + 3 * rsz + (j - c2);
+#pragma unroll
+        for (int q = 0; q < kRegions - 1; ++q) {
+          if (j < c[q]) return seg0 + q * rsz + j;
+          j -= c[q];
+        }
+        return seg0 + (kRegions - 1) * rsz + j;
+      }
+      __device__ __forceinline__ int fullest() const {
+        int m = 0;
+#pragma unroll
+        for (int q = 0; q < kRegions; ++q) m = max(m, c[q]);
+        return m;
       }
     };
     // Group-cooperative visit of every key of a row's buffer, eight loads in
@@ -936,16 +960,16 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
     // must not contain warp-synchronous operations.
     auto visit = [&](const uint64_t* cr, const SegView& sv, auto&& fn) {
       const int n = sv.n();
-      for (int base = 0; base < n; base += 8 * kEpiThreads) {
+      for (int base = 0; base < n; base += 8 * kG) {
         uint64_t kv[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const int e = base + j * kEpiThreads + g.tid;
+          const int e = base + j * kG + g.tid;
           kv[j] = e < n ? cr[sv.pos(e)] : 0;
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          if (base + j * kEpiThreads + g.tid < n) fn(kv[j]);
+          if (base + j * kG + g.tid < n) fn(kv[j]);
       }
     };
     // Each row keeps a bucket histogram (top kHistShift.. key bits) of the
@@ -956,7 +980,7 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
     auto hist_of = [&](int rr) { return Hist16{hist_words + (r0 + rr) * (kHistBins / 2)}; };
     static_assert(kHistBins == kPoolBins, "pooled and per-CTA buckets agree");
     // Keys >= T of the buffer moved, in place, to [0, kept); returns kept.
-    // A round reads 8 * kEpiThreads keys into registers before writing any:
+    // A round reads 8 * kG keys into registers before writing any:
     // every write lands below the number of keys read so far, and an unread
     // key sits at a position at least its virtual index, so none is
     // overwritten before it is read.
@@ -964,17 +988,17 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
       if (g.tid == 0) gsc->bcast[3] = 0;
       g.sync();
       const int n = sv.n();
-      for (int base = 0; base < n; base += 8 * kEpiThreads) {
+      for (int base = 0; base < n; base += 8 * kG) {
         uint64_t kv[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const int e = base + j * kEpiThreads + g.tid;
+          const int e = base + j * kG + g.tid;
           kv[j] = e < n ? cr[sv.pos(e)] : 0;
         }
         g.sync();
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const bool keep = base + j * kEpiThreads + g.tid < n && kv[j] >= T;
+          const bool keep = base + j * kG + g.tid < n && kv[j] >= T;
           const uint32_t m = __ballot_sync(0xffffffffu, keep);
           if (m) {
             const int leader = __ffs(m) - 1;
@@ -999,11 +1023,16 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
       ++pub;
 #pragma unroll
       for (int rr = 0; rr < L::kRowsPerGroup; ++rr)
-        if (lane == 0) rs->wc[pub & 1][r0 + rr][quad] = valid ? wcnt[rr] : 0;
+        if (lane == 0) rs->wc[pub & 1][r0 + rr][region] = valid ? wcnt[rr] : 0;
     };
     auto view_of = [&](int rr, int seg0) {
       const int32_t* c = rs->wc[pub & 1][r0 + rr];
-      return SegView{seg0, (ccap - seg0) >> 2, c[0], c[1], c[2], c[3]};
+      SegView v;
+      v.seg0 = seg0;
+      v.rsz = (ccap - seg0) / kRegions;
+#pragma unroll
+      for (int q = 0; q < kRegions; ++q) v.c[q] = c[q];
+      return v;
     };
     FP4IDX_STAMP_INIT();
     for_each_segment<MODE, R>(p, st, [&](int item, const ItemInfo& it, int lo, int hi, bool own) {
@@ -1026,7 +1055,7 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
         if constexpr (MODE == kModeTopk) {
           // ordered before any read by the group barrier after the histogram clear
           float* ws = reinterpret_cast<float*>(smem + L::kW) + (r0 + rr) * H;
-          for (int h = g.tid; h < H; h += kEpiThreads)
+          for (int h = g.tid; h < H; h += kG)
             ws[h] = row_valid[rr] ? __ldg(p.w + static_cast<int64_t>(t[rr]) * p.w_row_stride + h) : 0.0f;
         } else {
 #pragma unroll
@@ -1044,7 +1073,7 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
 #pragma unroll
         for (int rr = 0; rr < RG; ++rr) {
           const Hist16 hr = hist_of(rr);
-          for (int e = g.tid; e < kHistBins / 2; e += kEpiThreads) hr.w[e] = 0;
+          for (int e = g.tid; e < kHistBins / 2; e += kG) hr.w[e] = 0;
         }
         g.sync();  // cleared before any warp of the group appends
       }
@@ -1075,10 +1104,13 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
         const int32_t id_b = __shfl_sync(0xffffffffu, ids_next, d & 31);
         const int32_t pg_cur = d < 32 ? id_a : id_b;
         const bool real = !(MODE == kModeLogits && !tile_has_visible(it, j));
+        // with two sets, this group's tiles are those of its parity
+        const bool mine = L::kSets == 1 || (tile_iter & 1u) == static_cast<uint32_t>(set);
         float val[RG];
 #pragma unroll
         for (int rr = 0; rr < RG; ++rr) val[rr] = -INFINITY;
-        if (real) {
+        if (real && !mine) ++tile_iter;
+        if (real && mine) {
           const int a = tile_iter % kAccBufs;
           const uint32_t aph = (tile_iter / kAccBufs) & 1u;
           // Each warp waits for the accumulator itself (no group barrier per
@@ -1140,14 +1172,14 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
             // NaN logits are never selected
             const uint64_t key = (static_cast<uint64_t>(ordered_bits(val[rr])) << 32) |
                                  static_cast<uint64_t>(~static_cast<uint32_t>(pos));
-            const bool take = ok && page_good && pos < vis[rr] && cand[rr] && !isnan(val[rr]) && key >= thr[rr];
+            const bool take = mine && ok && page_good && pos < vis[rr] && cand[rr] && !isnan(val[rr]) && key >= thr[rr];
             const uint32_t m = __ballot_sync(0xffffffffu, take);
             if (m) {
               // this warp's region: no other warp writes there
               const int slot_i = wcnt[rr] + __popc(m & ((1u << lane) - 1u));
               const uint32_t bkt = static_cast<uint32_t>(key >> kHistShift);
               if (take) {
-                cand_of(rr)[seg0[rr] + quad * ((ccap - seg0[rr]) >> 2) + slot_i] = key;
+                cand_of(rr)[seg0[rr] + region * ((ccap - seg0[rr]) / kRegions) + slot_i] = key;
                 hist_of(rr).add(static_cast<int>(bkt));
                 if (!L::kSmemCand && p.pool_hist) {
                   red_add_u32(p.pool_hist + static_cast<int64_t>(t[rr]) * kHistBins + bkt, 1u);
@@ -1215,8 +1247,7 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
             const uint32_t bkt = find_kth_bucket(g, hr, kk, gsc, &above);
             const uint64_t Tb = static_cast<uint64_t>(bkt) << kHistShift;
             T = Tb > T ? Tb : T;
-            const int fullest = max(max(sv.c0, sv.c1), max(sv.c2, sv.c3));
-            if (fullest > sv.rsz - margin) {
+            if (sv.fullest() > sv.rsz - margin) {
               // keep the bucket of the k-th key and above, or exactly the k
               // largest when that would keep more than half the buffer
               uint64_t* cr = cand_of(rr);
@@ -1227,7 +1258,7 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
               }
               const int left = compact(cr, sv, T);
               // the histogram follows the buffer: buckets below bkt are empty now
-              for (int wd = g.tid; wd < static_cast<int>(bkt >> 1); wd += kEpiThreads) hr.w[wd] = 0;
+              for (int wd = g.tid; wd < static_cast<int>(bkt >> 1); wd += kG) hr.w[wd] = 0;
               g.sync();
               if (g.tid == 0) {
                 if (bkt & 1u) hr.set(static_cast<int>(bkt) - 1, 0);
@@ -1275,16 +1306,16 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
           if constexpr (L::kSmemCand) {
             // n <= ccap <= pcap: the buffer's keys, in order, eight in
             // flight per thread
-            for (int base = 0; base < n; base += 8 * kEpiThreads) {
+            for (int base = 0; base < n; base += 8 * kG) {
               uint64_t kv[8];
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
-                const int e = base + j * kEpiThreads + g.tid;
+                const int e = base + j * kG + g.tid;
                 kv[j] = e < n ? cr[sv.pos(e)] : 0;
               }
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
-                const int e = base + j * kEpiThreads + g.tid;
+                const int e = base + j * kG + g.tid;
                 if (e < n) out[e] = kv[j];
               }
             }
@@ -1302,16 +1333,16 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
             // keys >= T, every lane taking part in each ballot
             if (g.tid == 0) gsc->bcast[3] = 0;
             g.sync();
-            for (int base = 0; base < n; base += 8 * kEpiThreads) {
+            for (int base = 0; base < n; base += 8 * kG) {
               uint64_t kv[8];
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
-                const int e = base + j * kEpiThreads + g.tid;
+                const int e = base + j * kG + g.tid;
                 kv[j] = e < n ? cr[sv.pos(e)] : 0;
               }
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
-                const bool keep = base + j * kEpiThreads + g.tid < n && kv[j] >= T;
+                const bool keep = base + j * kG + g.tid < n && kv[j] >= T;
                 const uint32_t m = __ballot_sync(0xffffffffu, keep);
                 if (m) {
                   const int leader = __ffs(m) - 1;
