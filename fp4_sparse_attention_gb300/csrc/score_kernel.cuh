@@ -1282,12 +1282,11 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
       if constexpr (MODE == kModeTopk) {
         // -- flush each of this group's rows: its candidates go to the row's
         // partial list, a superset of the top k of the keys this CTA scored
-        // (the merge selects exactly).  Two-row CTAs (long items, one or two
-        // lists per row) copy every candidate: a threshold here costs the
-        // scorer more than it saves the merge (measured).  Four-row CTAs
-        // (decode: a row's keys spread over many CTAs, so many lists per
-        // row) keep only the keys in or above the bucket of the k-th largest,
-        // which the row's histogram gives without a pass over the buffer.
+        // (the merge selects exactly): only the keys in or above the bucket
+        // of the k-th largest, which the row's histogram gives without a
+        // pass over the buffer.  (Two-row CTAs with one set of epilogue warps
+        // copy every candidate: there the threshold cost the scorer more than
+        // it saved the merge; with two sets it saves more, measured.)
         const int slot = own ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + item;
         publish(wcnt, ok);
 #pragma unroll 1
@@ -1303,7 +1302,7 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
           const int64_t part = static_cast<int64_t>(slot) * R + r0 + rr;
           uint64_t* out = p.part_keys + part * pcap;
           int wrote = n;
-          if constexpr (L::kSmemCand) {
+          if constexpr (L::kSmemCand && L::kSets == 1) {
             // n <= ccap <= pcap: the buffer's keys, in order, eight in
             // flight per thread
             for (int base = 0; base < n; base += 8 * kG) {
