@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
       // -- Q of the item: codes by TMA, scales by cp.async into the atom
       if (pidx == 0) {
       const uint32_t qb = item_iter & 1u, qph = (item_iter >> 1) & 1u;
-      ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(qempty_bar(qb), qph ^ 1u, abort_flag, p.err) : false, 0);
+      ok = warp_wait(qempty_bar(qb), qph ^ 1u, abort_flag, p.err);
       if (!ok) return;
       if (lane == 0) {
         mbar_arrive_expect_tx(qfull_bar(qb), 128 * kCodeBytes);
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
         const uint32_t bytes = static_cast<uint32_t>((ok0 ? 1 : 0) + (ok1 ? 1 : 0)) * page * (kCodeBytes + G);
         const int s = tile_iter % kStages;
         const uint32_t ph = (tile_iter / kStages) & 1u;
-        ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.err) : false, 0);
+        ok = warp_wait(empty_bar(s), ph ^ 1u, abort_flag, p.err);
         if (!ok) return;
         if (lane == 0) mbar_arrive_expect_tx(full_bar(s), bytes);
         __syncwarp();
@@ -524,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1) block_score_kernel(const __grid_c
       if (!ok) return;
       const uint32_t qb = item_iter & 1u, qph = (item_iter >> 1) & 1u;
       if (sidx == 0) {
-      ok = __shfl_sync(0xffffffffu, lane == 0 ? mbar_wait(qfull_bar(qb), qph, abort_flag, p.err) : false, 0);
+      ok = warp_wait(qfull_bar(qb), qph, abort_flag, p.err);
       if (!ok) return;
       if (lane == 0) {
         // Q scales were written by cp.async (generic proxy): make them
