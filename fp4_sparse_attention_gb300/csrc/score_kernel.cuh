@@ -1121,10 +1121,11 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
           FP4IDX_STAMP(1);
           if (ok) {
             tc_fence_after();
-            // each row's H columns in chunks of at most 32 (registers); the
+            // each row's H columns in chunks (registers: 32 columns, 16 for
+            // the 64-head top-k, whose warps run at 96 registers); the
             // accumulator is released once its last chunk is loaded
             const uint32_t tcol = tmem + (static_cast<uint32_t>(quad * 32) << 16) + L::kAccCol + a * 128u + r0 * H;
-            constexpr int kChunk = L::kMaxRegs >= 160 || H < 32 ? H : 32;
+            constexpr int kChunk = L::kMaxRegs >= 160 || H < 32 ? H : (MODE == kModeTopk && H == 64 ? 16 : 32);
 #pragma unroll
             for (int rr = 0; rr < RG; ++rr) {
               float2 acc[4];
