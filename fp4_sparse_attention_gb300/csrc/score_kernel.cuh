@@ -1242,7 +1242,11 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
                 T = thr[q];
               }
             const SegView sv = view_of(rr, sg);
-            if (sv.n() <= p.k) continue;  // uniform: read after the barrier
+            // uniform: read after the barrier.  With pooled counts the warps
+            // raise their thresholds from the pool; the row's own bucket is
+            // then only needed for a compaction.
+            if (sv.n() <= p.k) continue;
+            if (!L::kSmemCand && p.pool_hist && sv.fullest() <= sv.rsz - margin) continue;
             const Hist16 hr = hist_of(rr);
             uint32_t above = 0;
             const uint32_t bkt = find_kth_bucket(g, hr, kk, gsc, &above);
