@@ -1090,106 +1090,111 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
       int32_t ids_cur = fetch_ids(pbase), ids_next = fetch_ids(pbase + 32);
       FP4IDX_STAMP(0);
       for (int j = lo; j < hi; ++j) {
-        const int32_t pos = (j << 7) + key_local;
-        const int32_t lp0 = (j << 7) >> p.page_shift;  // the tile's first page (warp-uniform)
-        if (lp0 >= pbase + 32) {
-          pbase += 32;
-          ids_cur = ids_next;
-          ids_next = fetch_ids(pbase + 32);
-        }
-        // this lane's page: lp0 or, with 64-key pages, lp0 + 1 (then
-        // possibly the first of the next 32)
-        const int32_t d = (pos >> p.page_shift) - pbase;
-        const int32_t id_a = __shfl_sync(0xffffffffu, ids_cur, d & 31);
-        const int32_t id_b = __shfl_sync(0xffffffffu, ids_next, d & 31);
-        const int32_t pg_cur = d < 32 ? id_a : id_b;
         const bool real = !(MODE == kModeLogits && !tile_has_visible(it, j));
-        // with two sets, this group's tiles are those of its parity
+        // with two sets, this group's tiles are those of its parity; the
+        // other set's tiles only count toward the checks
         const bool mine = L::kSets == 1 || (tile_iter & 1u) == static_cast<uint32_t>(set);
-        float val[RG];
-#pragma unroll
-        for (int rr = 0; rr < RG; ++rr) val[rr] = -INFINITY;
         if (real && !mine) ++tile_iter;
-        if (real && mine) {
-          const int a = tile_iter % kAccBufs;
-          const uint32_t aph = (tile_iter / kAccBufs) & 1u;
-          // Each warp waits for the accumulator itself (no group barrier per
-          // tile); ok stays warp-uniform, as tcgen05.ld below is a
-          // whole-warp instruction.
-          FP4IDX_STAMP(4);
-          ok = ok && warp_wait(accf_bar(a), aph, abort_flag, p.err);
-          FP4IDX_STAMP(1);
-          if (ok) {
-            tc_fence_after();
-            // each row's H columns in chunks (registers: 32 columns, 16 for
-            // the 64-head top-k, whose warps run at 96 registers); the
-            // accumulator is released once its last chunk is loaded
-            const uint32_t tcol = tmem + (static_cast<uint32_t>(quad * 32) << 16) + L::kAccCol + a * 128u + r0 * H;
-            constexpr int kChunk = L::kMaxRegs >= 160 || H < 32 ? H : (MODE == kModeTopk && H == 64 ? 16 : 32);
-#pragma unroll
-            for (int rr = 0; rr < RG; ++rr) {
-              float2 acc[4];
-#pragma unroll
-              for (int c = 0; c < 4; ++c) acc[c] = make_float2(0.0f, 0.0f);
-#pragma unroll
-              for (int c0 = 0; c0 < H; c0 += kChunk) {
-                uint32_t v[kChunk];
-                tmem_ld<kChunk>(tcol + rr * H + c0, v);
-                tmem_wait_ld();
-                reg_fence(v);
-                if (rr == RG - 1 && c0 + kChunk == H) {
-                  tc_fence_before();
-                  __syncwarp();
-                  if (lane == 0) mbar_arrive(acce_bar(a));
-                }
-                if constexpr (MODE == kModeTopk)
-                  wrelu_chunk<kChunk>(v, reinterpret_cast<const float2*>(smem + L::kW) + (r0 + rr) * (H / 2),
-                                      c0 / 2, acc);
-                else
-                  wrelu_chunk<kChunk>(v, w2[rr], c0 / 2, acc);
-              }
-              val[rr] = wrelu_total(acc);
-            }
-            FP4IDX_STAMP(3);
+        if (mine) {
+          const int32_t pos = (j << 7) + key_local;
+          const int32_t lp0 = (j << 7) >> p.page_shift;  // the tile's first page (warp-uniform)
+          if (lp0 >= pbase + 32) {
+            pbase += 32;
+            ids_cur = ids_next;
+            ids_next = fetch_ids(pbase + 32);
           }
-          FP4IDX_STAMP_COUNT();
-          ++tile_iter;
-        }
-        const bool page_good = pos < it.k_len && pg_cur >= 0 && pg_cur < p.num_pages;
-        // candidate mask: a cleared position is not a candidate (-inf, never selected)
-        bool cand[RG];
+          // this lane's page: lp0 or, with 64-key pages, lp0 + 1 (then
+          // possibly the first of the next 32)
+          const int32_t d = (pos >> p.page_shift) - pbase;
+          const int32_t id_a = __shfl_sync(0xffffffffu, ids_cur, d & 31);
+          const int32_t id_b = __shfl_sync(0xffffffffu, ids_next, d & 31);
+          const int32_t pg_cur = d < 32 ? id_a : id_b;
+          float val[RG];
 #pragma unroll
-        for (int rr = 0; rr < RG; ++rr)
-          cand[rr] = !p.cand_mask || (pos < vis[rr] && __ldg(p.cand_mask + static_cast<int64_t>(t[rr]) * p.mask_ld + pos) != 0);
-        if constexpr (MODE == kModeLogits) {
+          for (int rr = 0; rr < RG; ++rr) val[rr] = -INFINITY;
+          if (real) {
+            const int a = tile_iter % kAccBufs;
+            const uint32_t aph = (tile_iter / kAccBufs) & 1u;
+            // Each warp waits for the accumulator itself (no group barrier per
+            // tile); ok stays warp-uniform, as tcgen05.ld below is a
+            // whole-warp instruction.
+            FP4IDX_STAMP(4);
+            ok = ok && warp_wait(accf_bar(a), aph, abort_flag, p.err);
+            FP4IDX_STAMP(1);
+            if (ok) {
+              tc_fence_after();
+              // each row's H columns in chunks (registers: 32 columns, 16 for
+              // the 64-head top-k, whose warps run at 96 registers); the
+              // accumulator is released once its last chunk is loaded
+              const uint32_t tcol = tmem + (static_cast<uint32_t>(quad * 32) << 16) + L::kAccCol + a * 128u + r0 * H;
+              constexpr int kChunk = L::kMaxRegs >= 160 || H < 32 ? H : (MODE == kModeTopk && H == 64 ? 16 : 32);
+#pragma unroll
+              for (int rr = 0; rr < RG; ++rr) {
+                float2 acc[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[c] = make_float2(0.0f, 0.0f);
+#pragma unroll
+                for (int c0 = 0; c0 < H; c0 += kChunk) {
+                  uint32_t v[kChunk];
+                  tmem_ld<kChunk>(tcol + rr * H + c0, v);
+                  tmem_wait_ld();
+                  reg_fence(v);
+                  if (rr == RG - 1 && c0 + kChunk == H) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acce_bar(a));
+                  }
+                  if constexpr (MODE == kModeTopk)
+                    wrelu_chunk<kChunk>(v, reinterpret_cast<const float2*>(smem + L::kW) + (r0 + rr) * (H / 2),
+                                        c0 / 2, acc);
+                  else
+                    wrelu_chunk<kChunk>(v, w2[rr], c0 / 2, acc);
+                }
+                val[rr] = wrelu_total(acc);
+              }
+              FP4IDX_STAMP(3);
+            }
+            FP4IDX_STAMP_COUNT();
+            ++tile_iter;
+          }
+          const bool page_good = pos < it.k_len && pg_cur >= 0 && pg_cur < p.num_pages;
+          // candidate mask: a cleared position is not a candidate (-inf, never selected)
+          bool cand[RG];
 #pragma unroll
           for (int rr = 0; rr < RG; ++rr)
-            if (ok && row_valid[rr] && pos < p.ld)
-              p.logits[static_cast<int64_t>(t[rr]) * p.ld + pos] =
-                  page_good && pos < vis[rr] && cand[rr] ? val[rr] : -INFINITY;
-        } else {
+            cand[rr] = !p.cand_mask || (pos < vis[rr] && __ldg(p.cand_mask + static_cast<int64_t>(t[rr]) * p.mask_ld + pos) != 0);
+          if constexpr (MODE == kModeLogits) {
 #pragma unroll
-          for (int rr = 0; rr < RG; ++rr) {
-            // NaN logits are never selected
-            const uint64_t key = (static_cast<uint64_t>(ordered_bits(val[rr])) << 32) |
-                                 static_cast<uint64_t>(~static_cast<uint32_t>(pos));
-            const bool take = mine && ok && page_good && pos < vis[rr] && cand[rr] && !isnan(val[rr]) && key >= thr[rr];
-            const uint32_t m = __ballot_sync(0xffffffffu, take);
-            if (m) {
-              // this warp's region: no other warp writes there
-              const int slot_i = wcnt[rr] + __popc(m & ((1u << lane) - 1u));
-              const uint32_t bkt = static_cast<uint32_t>(key >> kHistShift);
-              if (take) {
-                cand_of(rr)[seg0[rr] + region * ((ccap - seg0[rr]) / kRegions) + slot_i] = key;
-                hist_of(rr).add(static_cast<int>(bkt));
-                if (!L::kSmemCand && p.pool_hist) {
-                  red_add_u32(p.pool_hist + static_cast<int64_t>(t[rr]) * kHistBins + bkt, 1u);
-                  pl_top[rr] = max(pl_top[rr], bkt);
+            for (int rr = 0; rr < RG; ++rr)
+              if (ok && row_valid[rr] && pos < p.ld)
+                p.logits[static_cast<int64_t>(t[rr]) * p.ld + pos] =
+                    page_good && pos < vis[rr] && cand[rr] ? val[rr] : -INFINITY;
+          } else {
+#pragma unroll
+            for (int rr = 0; rr < RG; ++rr) {
+              // NaN logits are never selected
+              const uint64_t key = (static_cast<uint64_t>(ordered_bits(val[rr])) << 32) |
+                                   static_cast<uint64_t>(~static_cast<uint32_t>(pos));
+              const bool take = ok && page_good && pos < vis[rr] && cand[rr] && !isnan(val[rr]) && key >= thr[rr];
+              const uint32_t m = __ballot_sync(0xffffffffu, take);
+              if (m) {
+                // this warp's region: no other warp writes there
+                const int slot_i = wcnt[rr] + __popc(m & ((1u << lane) - 1u));
+                const uint32_t bkt = static_cast<uint32_t>(key >> kHistShift);
+                if (take) {
+                  cand_of(rr)[seg0[rr] + region * ((ccap - seg0[rr]) / kRegions) + slot_i] = key;
+                  hist_of(rr).add(static_cast<int>(bkt));
+                  if (!L::kSmemCand && p.pool_hist) {
+                    red_add_u32(p.pool_hist + static_cast<int64_t>(t[rr]) * kHistBins + bkt, 1u);
+                    pl_top[rr] = max(pl_top[rr], bkt);
+                  }
                 }
+                wcnt[rr] += __popc(m);
               }
-              wcnt[rr] += __popc(m);
             }
           }
+        }
+        if constexpr (MODE == kModeTopk) {
           FP4IDX_STAMP(4);
           if (++since_check < check_every) continue;
           since_check = 0;
