@@ -918,7 +918,9 @@ __global__ void __maxnreg__((ScoreLayout<H, R, FMT, MODE>::kMaxRegs)) score_kern
     // check_every / kSets of them); a region then keeps that many tiles of
     // room (32 keys per tile and warp) above the trigger.
     const int ccap = L::kSmemCand ? L::kCandCap : topk_cand_capacity(p.k);
-    const int check_every = ccap >= 4096 ? 8 : 4;  // a region is at least ccap / 16 keys
+    // a region is at least ccap / 16 keys; two-row CTAs (two sets, each
+    // taking half of the tiles between checks) check every 16 tiles
+    const int check_every = ccap >= 4096 ? (L::kSmemCand ? 16 : 8) : 4;
     const int margin = check_every / L::kSets * 32;
     const uint32_t kk = static_cast<uint32_t>(p.k);
     int since_check = 0;
