@@ -214,8 +214,11 @@ __host__ __device__ constexpr int topk_cand_capacity(int k) { return 2 * topk_ca
 __host__ __device__ constexpr int topk_part_capacity(int k) {
   return topk_cand_capacity(k) > 8192 ? topk_cand_capacity(k) : 8192;
 }
-// Work units standing for one item's fixed cost in the top-k scorer's split.
-constexpr int kTopkItemOverhead = 2;
+// Work units (128-key tiles) standing for one item's fixed cost -- its
+// setup and the flush of its candidates -- in the top-k scorer's split
+// (measured: 12 balances the causal prefill, whose items range from one
+// tile to 256; long decode items are indifferent to it).
+constexpr int kTopkItemOverhead = 12;
 
 // Query rows per scorer CTA for a head count (the MMA N is rows * heads).
 inline int score_rows_per_cta(int heads) { return heads >= 64 ? 2 : 4; }
