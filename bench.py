@@ -56,14 +56,14 @@ RECORDED_TRAFFIC: dict = {
     # + write 84,700,160 B.
     ("block_scores", "block_scores"): {"sha": "d5e68283838be2fe", "bytes": 136321280},
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (one pass), one launch on
-    # the full workload: read 156,160,000 B (inputs: q 142.6 MB, w 8.4 MB, K 2.2 MB) +
-    # write 504,516,096 B (every CTA's candidates at or above its k-th bucket, for the merge).
-    ("prefill", "scorer_topk"): {"sha": "578a4c1dd256fad9", "bytes": 660676096},
-    # the same for the long batched decode: read 290,544,128 B (272.1 MB of K) + write
-    # 22,832,896 B (partial lists).
-    ("long_decode", "scorer_topk"): {"sha": "578a4c1dd256fad9", "bytes": 313377024},
-    # the same, prefill 8k: read 40,071,936 B + write 64,958,976 B.
-    ("prefill_8k", "scorer_topk"): {"sha": "578a4c1dd256fad9", "bytes": 105030912},
+    # the full workload: read 156,827,392 B (inputs: q 142.6 MB, w 8.4 MB, K 2.2 MB) +
+    # write 503,829,504 B (every CTA's candidates at or above its k-th bucket, for the merge).
+    ("prefill", "scorer_topk"): {"sha": "1877393667011ce8", "bytes": 660656896},
+    # the same for the long batched decode: read 290,736,896 B (272.1 MB of K) + write
+    # 22,938,880 B (partial lists).
+    ("long_decode", "scorer_topk"): {"sha": "1877393667011ce8", "bytes": 313675776},
+    # the same, prefill 8k: read 39,294,208 B + write 64,458,240 B.
+    ("prefill_8k", "scorer_topk"): {"sha": "1877393667011ce8", "bytes": 103752448},
 }
 
 
