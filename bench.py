@@ -52,9 +52,11 @@ L2_BYTES = 129 * 1024 * 1024
 # DRAM bytes per launch from ncu captures, valid only for the kernel sources
 # they were taken on (sha256 of the csrc/ files, first 16 hex digits).
 RECORDED_TRAFFIC: dict = {
-    # ncu --set full, one launch of the GQA NVFP4 block-score kernel: read 51,621,120 B
-    # + write 84,700,160 B.
-    ("block_scores", "block_scores"): {"sha": "d5e68283838be2fe", "bytes": 136321280},
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (one pass), one launch of
+    # the GQA NVFP4 block-score kernel: read 51,905,024 B + write 84,663,040 B (the
+    # [32, 64, 16,384] fp32 scores).
+    ("block_scores", "block_scores"): {"sha": "1877393667011ce8", "bytes": 136568064},
+    ("block_topk", "block_scores"): {"sha": "1877393667011ce8", "bytes": 136568064},
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (one pass), one launch on
     # the full workload: read 156,827,392 B (inputs: q 142.6 MB, w 8.4 MB, K 2.2 MB) +
     # write 503,829,504 B (every CTA's candidates at or above its k-th bucket, for the merge).
