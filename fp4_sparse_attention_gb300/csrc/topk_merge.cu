@@ -9,6 +9,7 @@
 // positions, values and the valid count.  One CTA per query row.  The row's
 // partial lists are read with one warp per list and, when the union fits,
 // copied into shared memory so that every later pass runs from there.
+#include <cstdint>
 #include <cstring>
 
 #include "score_kernel.cuh"
@@ -632,6 +633,388 @@ __global__ void __launch_bounds__(kSmallThreads) topk_select_small_kernel(const 
   if (tid == 0 && mp.valid_count) mp.valid_count[t] = n_out;
 }
 
+// ---------------------------------------------------------------------------
+// The same rows, unsorted output: one cluster of 8 CTAs per row, so that a
+// row's keys are counted by eight SMs.  CTA r of the cluster holds positions
+// [2048 r, 2048 r + 2048), eight keys per thread in registers, as 46-bit
+// search keys: the 32 order-preserving value bits, then the low 14 bits of
+// ~position (positions are < 2^14 here, so the dropped bits of ~position are
+// all ones and the order is that of the full top-k key).
+//
+// A radix level counts the keys it is given into each CTA's own digit
+// counters.  After a cluster barrier, CTA r sums digits [r per, (r+1) per)
+// over the eight CTAs' counters (distributed shared memory), scans them, and
+// stores their total in every CTA; after a second barrier every CTA knows
+// which CTA's digits hold the rank-th key and finds the digit by reading
+// that CTA's scanned sums.  All CTAs take every decision from the same
+// exchanged data, so they pass the same barriers, and a cluster barrier
+// costs about as much as a pass over the keys, so there are few of them.
+//
+// The first level counts the top 16 bits of the keys within 1,024 digits
+// (eight binades) of the largest.  Each CTA counts within 1,024 digits of
+// its own largest key and stores that key's digit and its number of
+// selectable keys in every CTA before the first barrier; the row's window
+// (below the largest of them) lies inside every CTA's own at a known shift,
+// so the owners read the counts at shifted indices.  When fewer than k keys
+// lie in the window, an 11-bit level over every key takes its place.
+// Further levels narrow the digit until it holds exactly the remaining rank,
+// or at most kClCand keys: those are gathered into every CTA, with each
+// CTA's count of keys above the digit, and the rank-th of them is found by
+// direct comparison; every CTA then knows each CTA's count of kept keys, so
+// the output offsets need no further exchange.
+// ---------------------------------------------------------------------------
+constexpr int kClCtas = 8;
+constexpr int kClThreads = 256;
+constexpr int kClPer = 8;            // keys per thread
+constexpr int kClCand = kClThreads;  // gathered keys: one per thread when ranked
+constexpr int kClRows = 12;          // exchange rows: start (2), at most 8 levels, output, above-digit counts
+constexpr int kClAboveRow = kClRows - 1;
+static_assert(kClCtas * kClThreads * kClPer == kSmallMaxKeys, "the cluster covers every short row");
+
+struct ClusterSelectSmem {
+  uint32_t hist[2048];              // this CTA's digit counters
+  uint32_t bsum[kClThreads];        // owned digits: counts summed over the cluster
+  uint32_t babove[kClThreads];      // owned digits: counted keys in the higher owned digits
+  uint64_t cand[kClCand];           // gathered keys of the final digit
+  uint32_t xchg[kClRows][kClCtas];  // [exchange][source CTA]
+  uint32_t ws[kClThreads / 32];
+  uint32_t kc[kClCtas];             // gathered keys kept, by source CTA
+  uint32_t bc[3];
+  uint32_t cand_n, lmax, lcnt, labove;
+  uint64_t thr;
+};
+
+// Exclusive prefix of v over the CTA's threads and its total.  ws (one word
+// per warp) is read after the barrier inside; the caller separates two uses
+// by a barrier.
+__device__ __forceinline__ uint32_t cl_prefix(uint32_t v, uint32_t* ws, uint32_t* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) ws[wid] = incl;
+  __syncthreads();
+  uint32_t before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kClThreads / 32; ++w) {
+    const uint32_t x = ws[w];
+    before += w < wid ? x : 0u;
+    tot += x;
+  }
+  *total = tot;
+  return before + incl - v;
+}
+
+// Second half of a radix level over the cluster, after the barrier that
+// follows the counting: CTA c counted digit b of the level at index
+// b + shift[c] of its counters (counts past nbins are zero).  When the cluster
+// counted at least `rank` keys: d = the digit holding the rank-th largest
+// counted key, rank -= the counted keys in higher digits, eq = the keys
+// counted in d.  total = all counted keys (d, rank, eq unchanged when total <
+// rank).  The counters are zero on return.
+__device__ __forceinline__ void cluster_resolve(ClusterSelectSmem& sm, uint32_t r, int xrow, int nbins,
+                                                const uint32_t (&shift)[kClCtas], uint32_t& rank, uint32_t& d,
+                                                uint32_t& eq, uint32_t& total) {
+  const int tid = threadIdx.x;
+  const int per = (nbins + kClCtas - 1) / kClCtas;
+  const int b = static_cast<int>(r) * per + tid;
+  uint32_t s = 0;
+  if (tid < per && b < nbins) {
+    uint32_t a[kClCtas];
+#pragma unroll
+    for (int c = 0; c < kClCtas; ++c) {
+      const uint32_t bi = static_cast<uint32_t>(b) + shift[c];
+      a[c] = bi < static_cast<uint32_t>(nbins) ? dsmem_ld_u32(dsmem_addr(&sm.hist[bi], c)) : 0u;
+    }
+#pragma unroll
+    for (int c = 0; c < kClCtas; ++c) s += a[c];
+  }
+  uint32_t tot;
+  const uint32_t pre = cl_prefix(s, sm.ws, &tot);
+  if (tid < per) {
+    sm.bsum[tid] = s;
+    sm.babove[tid] = tot - pre - s;  // owned digits are ascending with tid
+  }
+  if (tid < kClCtas) dsmem_st_u32(dsmem_addr(&sm.xchg[xrow][r], tid), tot);
+  cluster_sync();  // every owner's total and scanned sums are in place
+  // the owner of the rank-th key's digit: CTAs own ascending digit ranges
+  uint32_t acc = 0, ro = 0, rk = 0;
+  bool found = false;
+#pragma unroll
+  for (int c = kClCtas - 1; c >= 0; --c) {
+    const uint32_t x = sm.xchg[xrow][c];
+    if (!found && acc + x >= rank) {
+      found = true;
+      ro = static_cast<uint32_t>(c);
+      rk = rank - acc;
+    }
+    acc += x;
+  }
+  total = acc;
+  // every CTA read this CTA's counters before the barrier
+  for (int i = tid; i < nbins; i += kClThreads) sm.hist[i] = 0;
+  if (found && tid < per) {
+    const uint32_t x = dsmem_ld_u32(dsmem_addr(&sm.bsum[tid], ro));
+    const uint32_t above = dsmem_ld_u32(dsmem_addr(&sm.babove[tid], ro));
+    if (above < rk && above + x >= rk) {
+      sm.bc[0] = ro * static_cast<uint32_t>(per) + static_cast<uint32_t>(tid);
+      sm.bc[1] = rk - above;
+      sm.bc[2] = x;
+    }
+  }
+  __syncthreads();
+  if (found) {
+    d = sm.bc[0];
+    rank = sm.bc[1];
+    eq = sm.bc[2];
+  }
+}
+
+// One whole radix level over the cluster: key i of this thread is counted
+// under digit dig(i) (< nbins) when bit i of `in` is set; then as
+// cluster_resolve with no shifts.  The counters are zero on entry.
+template <class Dig>
+__device__ __forceinline__ void cluster_level(ClusterSelectSmem& sm, uint32_t r, int xrow, uint32_t in, int nbins,
+                                              Dig dig, uint32_t& rank, uint32_t& d, uint32_t& eq,
+                                              uint32_t& total) {
+#pragma unroll
+  for (int i = 0; i < kClPer; ++i)
+    if ((in >> i) & 1u) atomicAdd(&sm.hist[dig(i)], 1u);
+  cluster_sync();  // every CTA's counters are complete
+  const uint32_t none[kClCtas] = {0, 0, 0, 0, 0, 0, 0, 0};
+  cluster_resolve(sm, r, xrow, nbins, none, rank, d, eq, total);
+}
+
+__global__ void __launch_bounds__(kClThreads) topk_select_cluster_kernel(const __grid_constant__ MergeParams mp) {
+  const ScoreParams& p = mp.sp;
+  __shared__ ClusterSelectSmem sm;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const uint32_t r = cluster_ctarank();
+  const int t = static_cast<int>(blockIdx.x / kClCtas);
+  const int k = p.k;
+
+  // This CTA's own state first (shared memory only, so it overlaps the
+  // scorer's tail); the arrive publishes it to the cluster, whose CTAs touch
+  // it only after the matching wait.
+  for (int i = tid; i < 2048; i += kClThreads) sm.hist[i] = 0;
+  if (tid < kClCtas) sm.kc[tid] = 0;
+  if (tid == 0) {
+    sm.cand_n = 0;
+    sm.lmax = 0;
+    sm.lcnt = 0;
+    sm.labove = 0;
+    sm.thr = 0;
+  }
+  cluster_arrive();
+  pdl_wait();  // the logits come from the kernel before this one
+  pdl_launch_dependents();
+  int lo = 0, hi = p.num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(p.cu_seqlens_q + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  ItemInfo it;
+  it.b = lo;
+  it.k_len = max(__ldg(p.cu_seqlens_k + lo + 1) - __ldg(p.cu_seqlens_k + lo), 0);
+  const int cap = static_cast<int>(min(p.ld, static_cast<int64_t>(kSmallMaxKeys)));
+  const int M = min(row_visible(p, it, t), cap);
+  const float4* row4 = reinterpret_cast<const float4*>(p.logits + static_cast<int64_t>(t) * p.ld);
+  float4 v[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int e = static_cast<int>(r) * (kClThreads * 2) + tid + kClThreads * u;
+    v[u] = 4 * e < cap ? __ldg(row4 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  // Key i of this thread: position 4 (512 r + tid + 256 (i / 4)) + i % 4.
+  // Bit i of `present`: visible, not cleared by the candidate mask, not NaN.
+  uint64_t K[kClPer];
+  uint32_t present = 0, top = 0;
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int pos = 4 * (static_cast<int>(r) * (kClThreads * 2) + tid + kClThreads * u);
+    const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const bool ok = pos + c < M && !isnan(f[c]) &&
+                      (!p.cand_mask || __ldg(p.cand_mask + static_cast<int64_t>(t) * p.mask_ld + pos + c) != 0);
+      const uint64_t key = topk_key(f[c], static_cast<uint32_t>(pos + c));
+      const uint64_t s46 = ((key >> 32) << 14) | (key & 0x3FFFu);
+      K[4 * u + c] = s46;
+      present |= ok ? 1u << (4 * u + c) : 0u;
+      if (ok) top = max(top, static_cast<uint32_t>(s46 >> 30));
+    }
+  }
+  top = __reduce_max_sync(0xffffffffu, top);
+  const uint32_t cnt = __reduce_add_sync(0xffffffffu, static_cast<uint32_t>(__popc(present)));
+  __syncthreads();  // the zeroed state above is visible to the whole CTA
+  if (lane == 0) {
+    atomicMax(&sm.lmax, top);
+    atomicAdd(&sm.lcnt, cnt);
+  }
+  __syncthreads();
+  // first level, counting half: the top 16 bits within 1,024 digits of this
+  // CTA's largest
+  const uint32_t lmax = sm.lmax;
+  const uint32_t lwlo = lmax >= 1023u ? lmax - 1023u : 0u;
+#pragma unroll
+  for (int i = 0; i < kClPer; ++i) {
+    const uint32_t dg = static_cast<uint32_t>(K[i] >> 30);
+    if (((present >> i) & 1u) && dg >= lwlo) atomicAdd(&sm.hist[dg - lwlo], 1u);
+  }
+  cluster_wait();  // every CTA of the cluster has set up its state
+  if (tid < kClCtas) {
+    dsmem_st_u32(dsmem_addr(&sm.xchg[0][r], static_cast<uint32_t>(tid)), lmax);
+    dsmem_st_u32(dsmem_addr(&sm.xchg[1][r], static_cast<uint32_t>(tid)), sm.lcnt);
+  }
+  cluster_sync();  // counters complete; every CTA's largest digit and count in place
+  uint32_t gmax = 0, n_valid = 0;
+#pragma unroll
+  for (int c = 0; c < kClCtas; ++c) {
+    gmax = max(gmax, sm.xchg[0][c]);
+    n_valid += sm.xchg[1][c];
+  }
+
+  int xrow = 2;
+  const bool all_kept = n_valid <= static_cast<uint32_t>(k);
+  bool counted = all_kept;  // every CTA's count of kept keys known without an exchange
+  uint32_t base = 0, n_all = n_valid;
+  if (all_kept) {
+#pragma unroll
+    for (int c = 0; c < kClCtas; ++c) base += c < static_cast<int>(r) ? sm.xchg[1][c] : 0u;
+  }
+  uint64_t T46 = 0;  // kept: present keys >= T46 (every present key when all_kept)
+  if (!all_kept) {
+    uint32_t rank = static_cast<uint32_t>(k), d = 0, eq = 0, total = 0;
+    // the row's window [wlo, gmax] lies inside CTA c's [lwlo_c, lmax_c]
+    // wherever CTA c has keys: digit wlo + b is at index b + wlo - lwlo_c
+    const uint32_t wlo = gmax >= 1023u ? gmax - 1023u : 0u;
+    uint32_t shift[kClCtas];
+#pragma unroll
+    for (int c = 0; c < kClCtas; ++c) {
+      const uint32_t m = sm.xchg[0][c];
+      shift[c] = wlo - (m >= 1023u ? m - 1023u : 0u);
+    }
+    cluster_resolve(sm, r, xrow++, 1024, shift, rank, d, eq, total);
+    uint64_t pre;
+    int sh;
+    if (total >= rank) {
+      pre = wlo + d;
+      sh = 30;
+    } else {
+      cluster_level(sm, r, xrow++, present, 2048, [&](int i) { return static_cast<uint32_t>(K[i] >> 35); }, rank,
+                    d, eq, total);
+      pre = d;
+      sh = 35;
+    }
+    bool ranked = false;
+    // sh > 0 while eq != rank (a full 46-bit prefix matches one key); the
+    // level count is bounded all the same (at most four levels follow)
+    for (int lv = 0; lv < 6 && eq != rank && sh > 0; ++lv) {
+      if (eq <= static_cast<uint32_t>(kClCand)) {
+        // gather the eq keys of the digit into every CTA, with this CTA's
+        // count of keys above the digit, then rank them
+        uint32_t n_above = 0;
+#pragma unroll
+        for (int i = 0; i < kClPer; ++i) {
+          if (!((present >> i) & 1u)) continue;
+          const uint64_t dg = K[i] >> sh;
+          if (dg > pre) {
+            ++n_above;
+          } else if (dg == pre) {
+            const uint32_t slot = dsmem_atom_add_u32(dsmem_addr(&sm.cand_n, 0), 1u);
+            if (slot < static_cast<uint32_t>(kClCand)) {
+#pragma unroll
+              for (int c = 0; c < kClCtas; ++c) dsmem_st_u64(dsmem_addr(&sm.cand[slot], c), K[i]);
+            }
+          }
+        }
+        n_above = __reduce_add_sync(0xffffffffu, n_above);
+        if (lane == 0) atomicAdd(&sm.labove, n_above);
+        __syncthreads();
+        if (tid < kClCtas) dsmem_st_u32(dsmem_addr(&sm.xchg[kClAboveRow][r], static_cast<uint32_t>(tid)), sm.labove);
+        cluster_sync();  // the last access to another CTA's shared memory on this path is before it
+        uint64_t x = 0;
+        if (tid < static_cast<int>(eq)) {
+          x = sm.cand[tid];
+          uint32_t above = 0;
+          for (uint32_t j = 0; j < eq; ++j) above += sm.cand[j] > x ? 1u : 0u;
+          if (above == rank - 1) sm.thr = x;
+        }
+        __syncthreads();
+        T46 = sm.thr;
+        // kept gathered keys by source CTA (position / 2048; ~position in the low bits)
+        if (tid < static_cast<int>(eq) && x >= T46)
+          atomicAdd(&sm.kc[((~static_cast<uint32_t>(x)) & 0x3FFFu) >> 11], 1u);
+        __syncthreads();
+        n_all = 0;
+#pragma unroll
+        for (int c = 0; c < kClCtas; ++c) {
+          const uint32_t n = sm.xchg[kClAboveRow][c] + sm.kc[c];
+          base += c < static_cast<int>(r) ? n : 0u;
+          n_all += n;
+        }
+        counted = true;
+        ranked = true;
+        break;
+      }
+      const int w = sh < 11 ? sh : 11;
+      const int shn = sh - w;
+      uint32_t in = 0;
+#pragma unroll
+      for (int i = 0; i < kClPer; ++i) in |= (K[i] >> sh) == pre ? 1u << i : 0u;
+      cluster_level(sm, r, xrow++, in & present, 1 << w,
+                    [&](int i) { return static_cast<uint32_t>(K[i] >> shn) & ((1u << w) - 1u); }, rank, d, eq,
+                    total);
+      pre = (pre << w) | d;
+      sh = shn;
+    }
+    if (!ranked) T46 = pre << sh;
+  }
+
+  uint32_t keep = present;
+  if (!all_kept) {
+#pragma unroll
+    for (int i = 0; i < kClPer; ++i)
+      if (K[i] < T46) keep &= ~(1u << i);
+  }
+  uint32_t ctot;
+  uint32_t o = cl_prefix(static_cast<uint32_t>(__popc(keep)), sm.ws, &ctot);
+  if (!counted) {
+    if (tid < kClCtas) dsmem_st_u32(dsmem_addr(&sm.xchg[xrow][r], static_cast<uint32_t>(tid)), ctot);
+    cluster_sync();  // the last access to another CTA's shared memory on this path is before it
+    base = 0;
+    n_all = 0;
+#pragma unroll
+    for (int c = 0; c < kClCtas; ++c) {
+      const uint32_t x = sm.xchg[xrow][c];
+      base += c < static_cast<int>(r) ? x : 0u;
+      n_all += x;
+    }
+  }
+  o += base;
+  const int n_out = static_cast<int>(min(n_all, static_cast<uint32_t>(k)));
+  const int64_t row = static_cast<int64_t>(t) * k;
+#pragma unroll
+  for (int i = 0; i < kClPer; ++i)
+    if ((keep >> i) & 1u) {
+      if (o < static_cast<uint32_t>(k)) {
+        const uint64_t key = ((K[i] >> 14) << 32) | 0xFFFFC000u | (K[i] & 0x3FFFu);
+        mp.indices[row + o] = key_pos(key);
+        if (mp.values) mp.values[row + o] = key_value(key);
+      }
+      ++o;
+    }
+  for (int j = n_out + static_cast<int>(r) * kClThreads + tid; j < k; j += kClCtas * kClThreads) {
+    mp.indices[row + j] = -1;
+    if (mp.values) mp.values[row + j] = -INFINITY;
+  }
+  if (r == 0 && tid == 0 && mp.valid_count) mp.valid_count[t] = n_out;
+}
+
 // Launch with programmatic stream serialization: the kernel's CTAs may be
 // scheduled once the previous kernel of the stream (the scorer, which
 // signals early) allows it; the kernel itself waits (pdl_wait) for that
@@ -664,6 +1047,24 @@ cudaError_t launch_merge_t(const MergeParams& p, int rows, cudaStream_t stream) 
 
 cudaError_t launch_topk_select(const MergeParams& p, int rows, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
+  if (p.sp.max_seqlen_k <= kSmallMaxKeys && !(p.flags & 1u) &&
+      static_cast<int64_t>(rows) * kClCtas <= static_cast<int64_t>(INT32_MAX)) {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(rows * kClCtas));
+    cfg.blockDim = dim3(kClThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kClCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, topk_select_cluster_kernel, p);
+  }
   if (p.sp.max_seqlen_k <= kSmallMaxKeys) {
     const int sbytes = static_cast<int>(sizeof(SmallSelectSmem) + 16);
     cudaError_t e = cudaFuncSetAttribute(topk_select_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sbytes);
