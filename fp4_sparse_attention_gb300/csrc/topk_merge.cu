@@ -651,36 +651,46 @@ __global__ void __launch_bounds__(kSmallThreads) topk_select_small_kernel(const 
 // costs about as much as a pass over the keys, so there are few of them.
 //
 // The first level counts the top 16 bits of the keys within 1,024 digits
-// (eight binades) of the largest.  Each CTA counts within 1,024 digits of
-// its own largest key and stores that key's digit and its number of
-// selectable keys in every CTA before the first barrier; the row's window
-// (below the largest of them) lies inside every CTA's own at a known shift,
-// so the owners read the counts at shifted indices.  When fewer than k keys
-// lie in the window, an 11-bit level over every key takes its place.
+// (eight binades) of the largest, with stores instead of remote reads.  Each
+// CTA counts within 1,024 digits of its own largest key and, before the
+// first barrier, stores each count at the digit's residue mod 1,024 in the
+// CTA owning that residue, and its largest digit and number of selectable
+// keys in every CTA.  The row's window (the 1,024 digits below the largest
+// of all) holds one digit of each residue and lies inside every CTA's own
+// window wherever that CTA has keys, so an owner sums, per residue, the
+// counts of the CTAs whose largest digit is at or above the window's digit
+// of that residue, and stores the sums in every CTA; after the second
+// barrier every CTA scans the whole window by itself.  When fewer than k
+// keys lie in the window, an 11-bit level over every key takes its place.
 // Further levels narrow the digit until it holds exactly the remaining rank,
-// or at most kClCand keys: those are gathered into every CTA, with each
-// CTA's count of keys above the digit, and the rank-th of them is found by
-// direct comparison; every CTA then knows each CTA's count of kept keys, so
-// the output offsets need no further exchange.
+// or at most kClCand keys: those are gathered into every CTA (a region per
+// source CTA), with each CTA's count of keys above the digit, and the
+// rank-th of them is found by direct comparison; every CTA then knows each
+// CTA's count of kept keys, so the output offsets need no further exchange.
 // ---------------------------------------------------------------------------
 constexpr int kClCtas = 8;
 constexpr int kClThreads = 256;
 constexpr int kClPer = 8;            // keys per thread
 constexpr int kClCand = kClThreads;  // gathered keys: one per thread when ranked
-constexpr int kClRows = 12;          // exchange rows: start (2), at most 8 levels, output, above-digit counts
+constexpr int kClWin = 1024;         // first-level window (digits)
+constexpr int kClRows = 12;          // exchange rows: start (2), at most 7 levels, output, gathered counts (2)
 constexpr int kClAboveRow = kClRows - 1;
+constexpr int kClCandRow = kClRows - 2;
 static_assert(kClCtas * kClThreads * kClPer == kSmallMaxKeys, "the cluster covers every short row");
 
 struct ClusterSelectSmem {
   uint32_t hist[2048];              // this CTA's digit counters
   uint32_t bsum[kClThreads];        // owned digits: counts summed over the cluster
   uint32_t babove[kClThreads];      // owned digits: counted keys in the higher owned digits
-  uint64_t cand[kClCand];           // gathered keys of the final digit
+  uint64_t cand[kClCtas][kClCand];  // gathered keys of the final digit, by source CTA
+  uint64_t flat[kClCand];           // the same keys, regions in order
+  uint32_t inc[kClCtas][kClWin / kClCtas];  // owner: first-level counts of its residues, by source CTA
+  uint32_t gh[kClWin];              // first-level counts of the window, by residue
   uint32_t xchg[kClRows][kClCtas];  // [exchange][source CTA]
   uint32_t ws[kClThreads / 32];
   uint32_t kc[kClCtas];             // gathered keys kept, by source CTA
   uint32_t bc[3];
-  uint32_t cand_n, lmax, lcnt, labove;
+  uint32_t cand_n, lmax, lcnt, labove;  // cand_n: this CTA's gathered keys
   uint64_t thr;
 };
 
@@ -708,27 +718,28 @@ __device__ __forceinline__ uint32_t cl_prefix(uint32_t v, uint32_t* ws, uint32_t
   return before + incl - v;
 }
 
-// Second half of a radix level over the cluster, after the barrier that
-// follows the counting: CTA c counted digit b of the level at index
-// b + shift[c] of its counters (counts past nbins are zero).  When the cluster
-// counted at least `rank` keys: d = the digit holding the rank-th largest
-// counted key, rank -= the counted keys in higher digits, eq = the keys
-// counted in d.  total = all counted keys (d, rank, eq unchanged when total <
-// rank).  The counters are zero on return.
-__device__ __forceinline__ void cluster_resolve(ClusterSelectSmem& sm, uint32_t r, int xrow, int nbins,
-                                                const uint32_t (&shift)[kClCtas], uint32_t& rank, uint32_t& d,
-                                                uint32_t& eq, uint32_t& total) {
+// One radix level over the cluster.  Key i of this thread is counted under
+// digit dig(i) (< nbins) when bit i of `in` is set.  When the cluster counted
+// at least `rank` keys: d = the digit holding the rank-th largest counted
+// key, rank -= the counted keys in higher digits, eq = the keys counted in d.
+// total = all counted keys (d, rank, eq unchanged when total < rank).  The
+// counters are zero on entry and on return.
+template <class Dig>
+__device__ __forceinline__ void cluster_level(ClusterSelectSmem& sm, uint32_t r, int xrow, uint32_t in, int nbins,
+                                              Dig dig, uint32_t& rank, uint32_t& d, uint32_t& eq,
+                                              uint32_t& total) {
   const int tid = threadIdx.x;
+#pragma unroll
+  for (int i = 0; i < kClPer; ++i)
+    if ((in >> i) & 1u) atomicAdd(&sm.hist[dig(i)], 1u);
+  cluster_sync();  // every CTA's counters are complete
   const int per = (nbins + kClCtas - 1) / kClCtas;
   const int b = static_cast<int>(r) * per + tid;
   uint32_t s = 0;
   if (tid < per && b < nbins) {
     uint32_t a[kClCtas];
 #pragma unroll
-    for (int c = 0; c < kClCtas; ++c) {
-      const uint32_t bi = static_cast<uint32_t>(b) + shift[c];
-      a[c] = bi < static_cast<uint32_t>(nbins) ? dsmem_ld_u32(dsmem_addr(&sm.hist[bi], c)) : 0u;
-    }
+    for (int c = 0; c < kClCtas; ++c) a[c] = dsmem_ld_u32(dsmem_addr(&sm.hist[b], c));
 #pragma unroll
     for (int c = 0; c < kClCtas; ++c) s += a[c];
   }
@@ -771,21 +782,6 @@ __device__ __forceinline__ void cluster_resolve(ClusterSelectSmem& sm, uint32_t 
     rank = sm.bc[1];
     eq = sm.bc[2];
   }
-}
-
-// One whole radix level over the cluster: key i of this thread is counted
-// under digit dig(i) (< nbins) when bit i of `in` is set; then as
-// cluster_resolve with no shifts.  The counters are zero on entry.
-template <class Dig>
-__device__ __forceinline__ void cluster_level(ClusterSelectSmem& sm, uint32_t r, int xrow, uint32_t in, int nbins,
-                                              Dig dig, uint32_t& rank, uint32_t& d, uint32_t& eq,
-                                              uint32_t& total) {
-#pragma unroll
-  for (int i = 0; i < kClPer; ++i)
-    if ((in >> i) & 1u) atomicAdd(&sm.hist[dig(i)], 1u);
-  cluster_sync();  // every CTA's counters are complete
-  const uint32_t none[kClCtas] = {0, 0, 0, 0, 0, 0, 0, 0};
-  cluster_resolve(sm, r, xrow, nbins, none, rank, d, eq, total);
 }
 
 __global__ void __launch_bounds__(kClThreads) topk_select_cluster_kernel(const __grid_constant__ MergeParams mp) {
@@ -865,7 +861,17 @@ __global__ void __launch_bounds__(kClThreads) topk_select_cluster_kernel(const _
     const uint32_t dg = static_cast<uint32_t>(K[i] >> 30);
     if (((present >> i) & 1u) && dg >= lwlo) atomicAdd(&sm.hist[dg - lwlo], 1u);
   }
+  __syncthreads();
   cluster_wait();  // every CTA of the cluster has set up its state
+  // each count to the owner of its digit's residue (and cleared)
+#pragma unroll
+  for (int j = 0; j < kClWin / kClThreads; ++j) {
+    const uint32_t idx = static_cast<uint32_t>(tid + kClThreads * j);
+    const uint32_t x = sm.hist[idx];
+    sm.hist[idx] = 0;
+    const uint32_t rho = (lwlo + idx) & (kClWin - 1);
+    dsmem_st_u32(dsmem_addr(&sm.inc[r][rho % (kClWin / kClCtas)], rho / (kClWin / kClCtas)), x);
+  }
   if (tid < kClCtas) {
     dsmem_st_u32(dsmem_addr(&sm.xchg[0][r], static_cast<uint32_t>(tid)), lmax);
     dsmem_st_u32(dsmem_addr(&sm.xchg[1][r], static_cast<uint32_t>(tid)), sm.lcnt);
@@ -889,16 +895,54 @@ __global__ void __launch_bounds__(kClThreads) topk_select_cluster_kernel(const _
   uint64_t T46 = 0;  // kept: present keys >= T46 (every present key when all_kept)
   if (!all_kept) {
     uint32_t rank = static_cast<uint32_t>(k), d = 0, eq = 0, total = 0;
-    // the row's window [wlo, gmax] lies inside CTA c's [lwlo_c, lmax_c]
-    // wherever CTA c has keys: digit wlo + b is at index b + wlo - lwlo_c
+    // the row's window [wlo, gmax]: this CTA owns residues
+    // [128 r, 128 r + 128); the window's digit of residue rho is
+    // wlo + ((rho - wlo) mod 1024), counted by CTA c when c's largest digit
+    // is at or above it (c's window [lwlo_c, lmax_c] then holds it, as
+    // lwlo_c <= wlo)
     const uint32_t wlo = gmax >= 1023u ? gmax - 1023u : 0u;
-    uint32_t shift[kClCtas];
+    constexpr int kOwn = kClWin / kClCtas;
+    if (tid < kOwn) {
+      const uint32_t rho = r * kOwn + static_cast<uint32_t>(tid);
+      const uint32_t g = wlo + ((rho - wlo) & (kClWin - 1));
+      uint32_t s = 0;
 #pragma unroll
-    for (int c = 0; c < kClCtas; ++c) {
-      const uint32_t m = sm.xchg[0][c];
-      shift[c] = wlo - (m >= 1023u ? m - 1023u : 0u);
+      for (int c = 0; c < kClCtas; ++c) s += g <= sm.xchg[0][c] ? sm.inc[c][tid] : 0u;
+#pragma unroll
+      for (int c = 0; c < kClCtas; ++c) dsmem_st_u32(dsmem_addr(&sm.gh[rho], static_cast<uint32_t>(c)), s);
     }
-    cluster_resolve(sm, r, xrow++, 1024, shift, rank, d, eq, total);
+    cluster_sync();  // the window's counts are in every CTA
+    {
+      // digits wlo + 4 tid .. + 3 of the window
+      constexpr int kQ = kClWin / kClThreads;
+      uint32_t c4[kQ], s4 = 0;
+#pragma unroll
+      for (int q = 0; q < kQ; ++q) {
+        c4[q] = sm.gh[(wlo + kQ * tid + q) & (kClWin - 1)];
+        s4 += c4[q];
+      }
+      uint32_t tot;
+      uint32_t a = cl_prefix(s4, sm.ws, &tot);
+      a = tot - a - s4;  // window keys in the digits of higher threads
+      total = tot;
+      if (total >= rank) {
+#pragma unroll
+        for (int q = kQ - 1; q >= 0; --q) {
+          if (a < rank && a + c4[q] >= rank) {
+            sm.bc[0] = static_cast<uint32_t>(kQ * tid + q);
+            sm.bc[1] = rank - a;
+            sm.bc[2] = c4[q];
+          }
+          a += c4[q];
+        }
+      }
+      __syncthreads();
+      if (total >= rank) {
+        d = sm.bc[0];
+        rank = sm.bc[1];
+        eq = sm.bc[2];
+      }
+    }
     uint64_t pre;
     int sh;
     if (total >= rank) {
@@ -920,35 +964,58 @@ __global__ void __launch_bounds__(kClThreads) topk_select_cluster_kernel(const _
         uint32_t n_above = 0;
 #pragma unroll
         for (int i = 0; i < kClPer; ++i) {
-          if (!((present >> i) & 1u)) continue;
+          const bool sel = (present >> i) & 1u;
           const uint64_t dg = K[i] >> sh;
-          if (dg > pre) {
-            ++n_above;
-          } else if (dg == pre) {
-            const uint32_t slot = dsmem_atom_add_u32(dsmem_addr(&sm.cand_n, 0), 1u);
-            if (slot < static_cast<uint32_t>(kClCand)) {
+          n_above += sel && dg > pre ? 1u : 0u;
+          const bool mine = sel && dg == pre;
+          const uint32_t m = __ballot_sync(0xffffffffu, mine);
+          if (m) {  // one slot reservation per warp
+            const int leader = __ffs(m) - 1;
+            uint32_t b0 = 0;
+            if (lane == leader) b0 = atomicAdd(&sm.cand_n, static_cast<uint32_t>(__popc(m)));
+            b0 = __shfl_sync(0xffffffffu, b0, leader);
+            const uint32_t slot = b0 + static_cast<uint32_t>(__popc(m & ((1u << lane) - 1u)));
+            if (mine && slot < static_cast<uint32_t>(kClCand)) {
 #pragma unroll
-              for (int c = 0; c < kClCtas; ++c) dsmem_st_u64(dsmem_addr(&sm.cand[slot], c), K[i]);
+              for (int c = 0; c < kClCtas; ++c) dsmem_st_u64(dsmem_addr(&sm.cand[r][slot], c), K[i]);
             }
           }
         }
         n_above = __reduce_add_sync(0xffffffffu, n_above);
         if (lane == 0) atomicAdd(&sm.labove, n_above);
         __syncthreads();
-        if (tid < kClCtas) dsmem_st_u32(dsmem_addr(&sm.xchg[kClAboveRow][r], static_cast<uint32_t>(tid)), sm.labove);
+        if (tid < kClCtas) {
+          dsmem_st_u32(dsmem_addr(&sm.xchg[kClAboveRow][r], static_cast<uint32_t>(tid)), sm.labove);
+          dsmem_st_u32(dsmem_addr(&sm.xchg[kClCandRow][r], static_cast<uint32_t>(tid)), sm.cand_n);
+        }
         cluster_sync();  // the last access to another CTA's shared memory on this path is before it
+        // candidate tid of the regions taken in order (eq of them, at most kClCand)
+        uint32_t ncs[kClCtas];
+#pragma unroll
+        for (int c = 0; c < kClCtas; ++c) ncs[c] = min(sm.xchg[kClCandRow][c], static_cast<uint32_t>(kClCand));
         uint64_t x = 0;
+        int src = 0;
         if (tid < static_cast<int>(eq)) {
-          x = sm.cand[tid];
+          int j = tid;
+#pragma unroll
+          for (int c = 0; c < kClCtas; ++c)
+            if (src == c && j >= static_cast<int>(ncs[c])) {
+              j -= static_cast<int>(ncs[c]);
+              src = c + 1;
+            }
+          if (src < kClCtas) x = sm.cand[src][j];
+          sm.flat[tid] = x;
+        }
+        __syncthreads();
+        if (tid < static_cast<int>(eq) && src < kClCtas) {
           uint32_t above = 0;
-          for (uint32_t j = 0; j < eq; ++j) above += sm.cand[j] > x ? 1u : 0u;
+          for (uint32_t jj = 0; jj < eq; ++jj) above += sm.flat[jj] > x ? 1u : 0u;
           if (above == rank - 1) sm.thr = x;
         }
         __syncthreads();
         T46 = sm.thr;
-        // kept gathered keys by source CTA (position / 2048; ~position in the low bits)
-        if (tid < static_cast<int>(eq) && x >= T46)
-          atomicAdd(&sm.kc[((~static_cast<uint32_t>(x)) & 0x3FFFu) >> 11], 1u);
+        // kept gathered keys by source CTA
+        if (tid < static_cast<int>(eq) && src < kClCtas && x >= T46) atomicAdd(&sm.kc[src], 1u);
         __syncthreads();
         n_all = 0;
 #pragma unroll

@@ -90,3 +90,20 @@ def test_nvfp4_many_rows():
     p = wl.make_problem(name="cluster_nv", seed=518, fmt=wl.NVFP4, q_lens=[40], k_lens=[12000], num_heads=64,
                         e8m0_range=(120, 134), weights="normal", visibility="minus_row")
     _check(p, 512)
+
+
+def test_key_ranges_with_distant_maxima():
+    # each 2048-key range of the row gets its own power-of-two key scale, so
+    # the ranges' largest logits lie up to ten binades apart: the first
+    # level's 1,024-digit window holds part of some ranges' keys and none of
+    # others', and counts of digits below the window share residues with
+    # digits inside it
+    p = wl.make_problem(name="cluster_shift", seed=519, fmt=wl.MXFP4, q_lens=[2], k_lens=[16384], num_heads=32,
+                        e8m0_range=(124, 130), weights="normal", visibility="full")
+    deltas = [0, 4, -3, 6, -8, 2, 5, -1]
+    for c, dlt in enumerate(deltas):
+        for lp in range(2048 * c // p.page_size, 2048 * (c + 1) // p.page_size):
+            pg = p.block_table[0, lp]
+            p.k_scale[pg] = (p.k_scale[pg].astype(np.int16) + dlt).astype(np.uint8)
+    for k in (300, 2048):
+        _check(p, k)
