@@ -7,10 +7,12 @@
 //
 // One thread per 32-value group of one (token, K head) row: four 16-byte
 // loads of bf16, the group's max magnitude, the shared exponent from its
-// float exponent field, then each value placed on the E2M1 grid by
-// comparisons against the midpoints between levels (a tie goes to the level
-// with the even index, i.e. the even mantissa), 16 bytes of codes and one
-// scale byte stored.  Memory-bound: 64 bytes read, 17 written per group.
+// float exponent field, then each scaled value converted to E2M1 by the
+// hardware conversion (round to nearest, ties to the even mantissa, i.e. the
+// level with the even index; saturating at 6), 16 bytes of codes and one
+// scale byte stored.  A value that rounds to zero is stored as +0, and a NaN
+// value as +0 (a group holding one takes a slower path that also leaves it
+// out of the max).  Memory-bound: 64 bytes read, 17 written per group.
 #include <cstring>
 
 #include "internal.h"
@@ -21,18 +23,28 @@ namespace {
 
 constexpr int kStoreThreads = 256;
 
-// E2M1 index (0..7) of |y| rounded to the nearest level of
-// [0, 0.5, 1, 1.5, 2, 3, 4, 6], ties to the even index, saturating at 6.
-__device__ __forceinline__ uint32_t e2m1_rne_index(float a) {
-  uint32_t i = 0;
-  i += a > 0.25f;
-  i += a >= 0.75f;  // tie 0.75 -> 1.0 (index 2)
-  i += a > 1.25f;
-  i += a >= 1.75f;  // tie 1.75 -> 2.0 (index 4)
-  i += a > 2.5f;
-  i += a >= 3.5f;   // tie 3.5 -> 4.0 (index 6)
-  i += a > 5.0f;
-  return i;
+// Eight values to eight E2M1 codes (value j in bits 4j..4j+3): round to
+// the nearest of [0, 0.5, 1, 1.5, 2, 3, 4, 6] with ties to the even
+// mantissa, saturating, sign in bit 3 -- then a zero magnitude loses its
+// sign, so every value that rounds to zero is stored as +0.
+__device__ __forceinline__ uint32_t e2m1x8(const float* y) {
+  uint32_t w;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(w)
+      : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]), "f"(y[4]), "f"(y[5]), "f"(y[6]), "f"(y[7]));
+  const uint32_t nz = (w | (w >> 1) | (w >> 2)) & 0x11111111u;  // bit 0 of a nibble: magnitude != 0
+  return w & (0x77777777u | (nz << 3));
+}
+
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
 }
 
 __global__ void __launch_bounds__(kStoreThreads) store_k_kernel(const StoreParams p) {
@@ -70,7 +82,15 @@ __global__ void __launch_bounds__(kStoreThreads) store_k_kernel(const StoreParam
   }
   float amax = 0.0f;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  for (int i = 0; i < 32; ++i) amax = max_nan(amax, fabsf(x[i]));
+  if (isnan(amax)) {  // NaN values: left out of the max, stored as +0
+    amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      x[i] = isnan(x[i]) ? 0.0f : x[i];
+      amax = fmaxf(amax, fabsf(x[i]));
+    }
+  }
   // floor(log2(amax)) of a normal float is its exponent field - 127; the
   // E2M1 largest exponent is 2, so code = field - 2, clamped (a zero or
   // subnormal max gives code 1)
@@ -79,14 +99,13 @@ __global__ void __launch_bounds__(kStoreThreads) store_k_kernel(const StoreParam
   // 1 / scale = 2^(127 - code), exact: exponent field 254 - code (code 254,
   // unreachable from a finite max, would be the subnormal 2^-127)
   const float inv = code <= 253 ? __uint_as_float(static_cast<uint32_t>(254 - code) << 23) : 0x1p-127f;
-  uint32_t packed[4] = {0, 0, 0, 0};
+  // x * inv is exact (a power-of-two scale of a bf16 value)
+  float y[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float y = x[i] * inv;
-    const uint32_t idx = e2m1_rne_index(fabsf(y));
-    const uint32_t nib = idx | ((idx != 0 && (__float_as_uint(x[i]) >> 31)) ? 8u : 0u);
-    packed[i >> 3] |= nib << (4 * (i & 7));
-  }
+  for (int i = 0; i < 32; ++i) y[i] = x[i] * inv;
+  uint32_t packed[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) packed[q] = e2m1x8(y + 8 * q);
   const int64_t blk = static_cast<int64_t>(slot / p.page_size) * p.num_kv_heads + hk;  // (page, K head)
   const int64_t off = slot % p.page_size;
   uint8_t* codes;
