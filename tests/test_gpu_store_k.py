@@ -45,6 +45,29 @@ def test_writer_matches_oracle(page, Hkv):
     np.testing.assert_array_equal(dk.cpu().numpy(), k)
 
 
+def test_nan_keys_match_oracle():
+    # NaN values are stored as +0 and stay out of their group's max: some
+    # groups hold a few NaNs (either sign), one group per token is all NaN
+    rng = np.random.default_rng(21)
+    N, P, page = 300, 8, 64
+    keys = _keys(rng, N, 1)
+    nan = rng.random(keys.shape) < 0.05
+    keys[nan] = np.where(rng.random(int(nan.sum())) < 0.5, 0x7FC0, 0xFFC0).astype(np.uint16)
+    keys[:, 0, 96:128] = 0x7FC0
+    slots = rng.permutation(P * page)[:N].astype(np.int32)
+    k = np.zeros((P, 1, page, 64), np.uint8)
+    ks = np.zeros((P, 1, page, 4), np.uint8)
+    oracle.store_k(keys, slots, page, k, ks)
+    dk, ds = torch.zeros_like(torch.as_tensor(k)).cuda(), torch.zeros_like(torch.as_tensor(ks)).cuda()
+    kt = torch.as_tensor(keys.view(np.int16)).cuda().view(torch.bfloat16)
+    B.fp4idx_get_error(clear=True)
+    B.fp4idx_store_k(kt, torch.as_tensor(slots).cuda(), page, dk, ds)
+    torch.cuda.synchronize()
+    assert B.fp4idx_get_error(clear=True) == 0
+    np.testing.assert_array_equal(ds.cpu().numpy(), ks)
+    np.testing.assert_array_equal(dk.cpu().numpy(), k)
+
+
 def test_out_of_range_slot_is_skipped_and_reported():
     rng = np.random.default_rng(8)
     keys = _keys(rng, 4, 1)

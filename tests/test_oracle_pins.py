@@ -488,6 +488,26 @@ def test_store_k_zero_and_tiny_groups_take_code_one():
     assert sc.tolist() == [1, 1, 1, 1] and (nib == 0).all()
 
 
+def test_store_k_nan_values_store_zero_and_stay_out_of_the_max():
+    # the pages fix no rule for NaN keys; reading: stored as +0, left out of
+    # the group's max.  Group 0: NaN, 1, -2, 0, ... -> max 2: floor(log2 2) - 2
+    # = -1, code 126, scale 1/2, so 1 -> 2 (index 4) and -2 -> 4 (index 6,
+    # sign); group 1 all NaN (negative NaN) -> like an all-zero group, code 1
+    vals = np.zeros(128, np.float32)
+    vals[1], vals[2] = 1.0, -2.0
+    keys = _bf16(vals.reshape(1, 1, 128))
+    keys[0, 0, 0] = 0x7FC0
+    keys[0, 0, 32:64] = 0xFFC0
+    k = np.zeros((2, 1, 64, 64), np.uint8)
+    ks = np.zeros((2, 1, 64, 4), np.uint8)
+    oracle.store_k(keys, np.array([67], np.int32), 64, k, ks)
+    row = k[1, 0, 3]
+    nib = np.stack([row & 0xF, row >> 4], axis=1).reshape(-1)
+    assert ks[1, 0, 3].tolist() == [126, 1, 1, 1]
+    assert nib[:4].tolist() == [0, 4, 8 | 6, 0]
+    assert (nib[4:] == 0).all()
+
+
 def test_store_k_error_bound_on_random_groups():
     # |x - decoded| <= half the E2M1 spacing at |x| / scale, times scale,
     # unless |x| / scale is past 6 (saturation); decodes through the oracle's
