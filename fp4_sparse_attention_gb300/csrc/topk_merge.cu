@@ -46,10 +46,18 @@ __device__ void gather_sort_write(MergeSmem<kLocal>* sm, const Group<kMergeThrea
   const int tid = g.tid;
   if (tid == 0) sm->info[3] = 0;
   g.sync();
+  // one slot reservation per group of converged lanes, not per kept key
   auto keep = [&](uint64_t key) {
-    if (key >= T) {
-      const uint32_t o = atomicAdd(reinterpret_cast<uint32_t*>(&sm->info[3]), 1u);
-      if (o < 2048u) sm->out[o] = key;
+    const unsigned act = __activemask();
+    const bool want = key >= T;
+    const unsigned m = __ballot_sync(act, want);
+    if (m) {
+      const int lane = tid & 31;
+      const int leader = __ffs(m) - 1;
+      uint32_t o = 0;
+      if (lane == leader) o = atomicAdd(reinterpret_cast<uint32_t*>(&sm->info[3]), static_cast<uint32_t>(__popc(m)));
+      o = __shfl_sync(act, o, leader) + static_cast<uint32_t>(__popc(m & ((1u << lane) - 1u)));
+      if (want && o < 2048u) sm->out[o] = key;
     }
   };
   if (local) {
@@ -154,10 +162,33 @@ __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const __grid_
   const bool local = M <= kMergeLocal;
   const int n_out = M < k ? M : k;
 
-  // visit every candidate in global memory: one warp per list
-  // eight loads in flight per lane, so a long list is not a chain of L2 round trips
+  // visit every candidate in global memory, eight loads in flight per lane
+  // so that a long list is not a chain of L2 round trips: with fewer lists
+  // than warps (a prefill row has one or two) every thread works on each
+  // list in turn, else one warp per list
   auto for_each_global = [&](auto&& fn) {
     constexpr int U = 8;
+    if (nslots < kMergeWarps) {
+      for (int i = 0; i < nslots; ++i) {
+        const uint64_t* keys = p.part_keys + sm->slot_part[i] * cap;
+        const int n = sm->slot_cnt[i];
+        const int off = sm->slot_off[i];
+        for (int e0 = tid; e0 < n; e0 += kMergeThreads * U) {
+          uint64_t v[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int e = e0 + kMergeThreads * u;
+            v[u] = e < n ? __ldg(keys + e) : 0;
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int e = e0 + kMergeThreads * u;
+            if (e < n) fn(v[u], off + e);
+          }
+        }
+      }
+      return;
+    }
     for (int i = warp; i < nslots; i += kMergeWarps) {
       const uint64_t* keys = p.part_keys + sm->slot_part[i] * cap;
       const int n = sm->slot_cnt[i];
@@ -320,7 +351,8 @@ __global__ void __launch_bounds__(kMergeThreads) topk_select_kernel(const __grid
 }
 
 // ---------------------------------------------------------------------------
-// Rows of at most 16,384 visible keys: one 1024-thread CTA per row holds 16
+// Rows of at most 16,384 visible keys, sorted output (unsorted output takes
+// the cluster kernel below): one 1024-thread CTA per row holds 16
 // keys per thread in registers and finds the k-th largest 64-bit key by
 // radix levels (11-bit digits), each level counting only the keys that still
 // match the prefix; a level whose digit bucket holds exactly the remaining
