@@ -53,19 +53,19 @@ L2_BYTES = 129 * 1024 * 1024
 # they were taken on (sha256 of the csrc/ files, first 16 hex digits).
 RECORDED_TRAFFIC: dict = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (one pass), one launch of
-    # the GQA NVFP4 block-score kernel: read 51,978,752 B + write 84,788,224 B (the
+    # the GQA NVFP4 block-score kernel: read 52,000,256 B + write 84,906,240 B (the
     # [32, 64, 16,384] fp32 scores).
-    ("block_scores", "block_scores"): {"sha": "02d0a01fc26a55ea", "bytes": 136766976},
-    ("block_topk", "block_scores"): {"sha": "02d0a01fc26a55ea", "bytes": 136766976},
+    ("block_scores", "block_scores"): {"sha": "27c1a344977f94ff", "bytes": 136906496},
+    ("block_topk", "block_scores"): {"sha": "27c1a344977f94ff", "bytes": 136906496},
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (one pass), one launch on
-    # the full workload: read 157,020,672 B (inputs: q 142.6 MB, w 8.4 MB, K 2.2 MB) +
-    # write 504,148,224 B (every CTA's candidates at or above its k-th bucket, for the merge).
-    ("prefill", "scorer_topk"): {"sha": "02d0a01fc26a55ea", "bytes": 661168896},
-    # the same for the long batched decode: read 290,650,112 B (272.1 MB of K) + write
-    # 23,033,600 B (partial lists).
-    ("long_decode", "scorer_topk"): {"sha": "02d0a01fc26a55ea", "bytes": 313683712},
-    # the same, prefill 8k: read 39,293,440 B + write 64,520,448 B.
-    ("prefill_8k", "scorer_topk"): {"sha": "02d0a01fc26a55ea", "bytes": 103813888},
+    # the full workload: read 157,189,376 B (inputs: q 142.6 MB, w 8.4 MB, K 2.2 MB) +
+    # write 504,214,528 B (every CTA's candidates at or above its k-th bucket, for the merge).
+    ("prefill", "scorer_topk"): {"sha": "27c1a344977f94ff", "bytes": 661403904},
+    # the same for the long batched decode: read 290,656,256 B (272.1 MB of K) + write
+    # 23,139,584 B (partial lists).
+    ("long_decode", "scorer_topk"): {"sha": "27c1a344977f94ff", "bytes": 313795840},
+    # the same, prefill 8k: read 39,348,736 B + write 64,539,136 B.
+    ("prefill_8k", "scorer_topk"): {"sha": "27c1a344977f94ff", "bytes": 103887872},
 }
 
 
