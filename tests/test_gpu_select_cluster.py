@@ -107,3 +107,31 @@ def test_key_ranges_with_distant_maxima():
             p.k_scale[pg] = (p.k_scale[pg].astype(np.int16) + dlt).astype(np.uint8)
     for k in (300, 2048):
         _check(p, k)
+
+
+@pytest.mark.parametrize("sorted_", [False, True])
+def test_positions_alone_with_null_values_and_counts(sorted_):
+    # values and valid_count are optional in the C ABI: the positions written
+    # without them are those of the full call
+    import ctypes
+
+    p = wl.verify_decode_16k()
+    dp = B.DeviceProblem.from_host(p)
+    w = torch.as_tensor(p.w).cuda()
+    k = 2048
+    logits, idx, _, cnt = B.fp4idx_logits_topk(dp, w, k, sorted=sorted_)
+    lib = B.load_library()
+    logits2 = torch.empty_like(logits)
+    idx2 = torch.full_like(idx, 7)
+    flags = B.FP4IDX_TOPK_SORTED if sorted_ else 0
+    st = lib.fp4idx_logits_topk(ctypes.byref(dp.c), B._ptr(w), w.stride(0), B._ptr(logits2), logits2.stride(0), k,
+                                flags, B._ptr(idx2), None, None, B._stream(None))
+    torch.cuda.synchronize()
+    assert st == 0 and B.fp4idx_get_error() == 0
+    a, b, n = idx.cpu().numpy(), idx2.cpu().numpy(), cnt.cpu().numpy()
+    for t in range(p.num_rows):
+        if sorted_:
+            np.testing.assert_array_equal(b[t], a[t])
+        else:
+            np.testing.assert_array_equal(np.sort(b[t, : n[t]]), np.sort(a[t, : n[t]]))
+            assert np.all(b[t, n[t]:] == -1)
